@@ -1,0 +1,244 @@
+/*
+ * moe.h — C ABI of a B300-native (sm_103a) forward pass of one token-choice
+ * Mixture-of-Experts FFN layer.
+ *
+ * The layer, as the source pages state it:
+ *   - "Mixture of Experts for LLM Inference", section "Opening the router":
+ *     a small linear layer gives one raw score per expert, a softmax turns the
+ *     scores into shares, top-K keeps the K largest and renormalises them, and
+ *     those K weights blend the chosen experts' outputs. Some models (DeepSeek-V3)
+ *     use a sigmoid affinity plus normalisation over the chosen K instead.
+ *   - "Chapter 19: Mixture-of-Experts Models", §19.3.2 "A concrete router
+ *     computation": logits = hidden_state @ W_router; softmax over the top-K
+ *     logits equals full softmax + renormalisation over the chosen K.
+ *   - same chapter, §19.3.4: a per-expert bias shifts the scores used for
+ *     top-K selection only; the mixing weights come from the unbiased scores.
+ *   - "Mixture of Experts for LLM Inference", "Shared experts: stop relearning
+ *     the basics": a shared expert runs on every token, outside the router.
+ *   - "Chapter 19", §19.6.3 "How expert parallelism dispatches tokens" ("Route
+ *     and pack"): token copies are grouped by expert before the expert FFNs run
+ *     and returned to token order for the weighted aggregation.
+ *   - Each expert is an FFN with three matrices ("Mixture of Experts Explained:
+ *     Conditional Computation From Zero", "The slot it replaces, and what an
+ *     expert is"); this library reads it as SwiGLU:
+ *       E(x) = W_down (SiLU(W_gate x) * (W_up x)),  SiLU(z) = z * sigmoid(z).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     stated otherwise. The library allocates no device memory and keeps no
+ *     per-call global state; scratch lives in a caller-provided workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All work is enqueued asynchronously on it; no entry point synchronises
+ *     except moe_get_device_status.
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call returns an error status and enqueues nothing.
+ *   - Launch failures return MOE_ERR_CUDA. Faults the kernels detect on the
+ *     device (an expert index out of range, a pipeline wait that ran out of
+ *     time) are recorded in an error word inside the workspace and reported by
+ *     moe_get_device_status; kernels never trap.
+ *   - Row-major layouts throughout. bf16 is IEEE bfloat16 stored as uint16.
+ *   - Layer outputs exclude the residual stream (the residual path lies
+ *     outside the FFN slot the layer replaces).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* a null required pointer, a bad size or flag */
+  MOE_ERR_UNSUPPORTED = -2,   /* a valid problem this build does not handle */
+  MOE_ERR_WORKSPACE = -3,     /* ws is NULL, misaligned or smaller than needed */
+  MOE_ERR_CUDA = -4,          /* a CUDA runtime call or a launch failed */
+  MOE_ERR_TIMEOUT = -5,       /* device: a bounded pipeline wait gave up */
+  MOE_ERR_DEVICE_BOUNDS = -6  /* device: an input index was out of range */
+} moe_status_t;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn_t;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Which call a workspace is sized for (moe_workspace_bytes). */
+typedef enum {
+  MOE_CALL_PERMUTE = 0,
+  MOE_CALL_GROUPED_SWIGLU = 1,
+  MOE_CALL_LAYER_FORWARD = 2
+} moe_call_t;
+
+/*
+ * The problem statement, in the pages' terms: T tokens, d_model, N routed
+ * experts, K chosen per token, the FFN width of a routed expert, the number of
+ * always-on shared experts and their width, and the score function.
+ */
+typedef struct moe_problem {
+  int64_t T;             /* tokens in this call, >= 0 (T == 0 is a no-op)      */
+  int32_t d_model;       /* hidden size d, > 0, multiple of 8                  */
+  int32_t n_experts;     /* N routed experts, 1..256                           */
+  int32_t top_k;         /* K experts per token, 1..min(N, 32)                 */
+  int32_t ffn;           /* F, routed expert FFN width, > 0, multiple of 8     */
+  int32_t n_shared;      /* S always-on shared experts, >= 0                   */
+  int32_t shared_ffn;    /* Fs, shared expert width (multiple of 8 if S > 0)   */
+  int32_t score_fn;      /* moe_score_fn_t                                     */
+  int32_t renormalize;   /* 1: chosen weights renormalised to sum to 1;
+                            0: softmax -> the full-softmax probability of each
+                               chosen expert, sigmoid -> its raw sigmoid score */
+  int32_t hidden_dtype;  /* moe_dtype_t of `hidden`                           */
+} moe_problem_t;
+
+/*
+ * Weights of one layer. Routed experts are stacked: w_gate/w_up are
+ * bf16 [N][F][d] (row f of expert e holds the d inputs of unit f, i.e. the
+ * operand is K-major), w_down is bf16 [N][d][F]. Shared experts likewise:
+ * ws_gate/ws_up bf16 [S][Fs][d], ws_down bf16 [S][d][Fs]; NULL when S == 0.
+ * The router is fp32 (kept in higher precision than the experts, per
+ * "Chapter 19", §19.6.2 table, "Higher-precision router"):
+ *   w_router     fp32 [d][N]   logits = hidden @ w_router (+ router_bias)
+ *   router_bias  fp32 [N] or NULL: the bias term of the router's linear layer,
+ *                added to every logit
+ *   sel_bias     fp32 [N] or NULL: selection-only bias, added to the sigmoid
+ *                score before top-K, never to the mixing weights (sigmoid
+ *                scoring only)
+ */
+typedef struct moe_weights {
+  const float* w_router;
+  const float* router_bias;
+  const float* sel_bias;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const void* ws_gate;
+  const void* ws_up;
+  const void* ws_down;
+} moe_weights_t;
+
+/* Human-readable name of a moe_status_t. Never NULL. Host only. */
+const char* moe_status_string(int32_t status);
+
+/*
+ * Host-only validation of a problem statement (no CUDA call). Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG (p NULL, a size out of range, a bad enum) or
+ * MOE_ERR_UNSUPPORTED (a valid statement this build does not handle).
+ */
+moe_status_t moe_problem_check(const moe_problem_t* p);
+
+/*
+ * Bytes of workspace the given call needs for problem p (host only, no CUDA
+ * call). Returns 0 if p is invalid. The workspace must be 256-byte aligned.
+ */
+size_t moe_workspace_bytes(const moe_problem_t* p, int32_t call);
+
+/*
+ * Router, scoring, top-K and gate weights, per token ("Mixture of Experts for
+ * LLM Inference", "Opening the router"; "Chapter 19", §19.3.2 and §19.3.4;
+ * "AI Infrastructure series Part 12", "How does the router decide? A worked
+ * example").
+ *   hidden      [T][d], p->hidden_dtype
+ *   w_router    fp32 [d][N];  router_bias, sel_bias: fp32 [N] or NULL
+ *   topk_idx    out int32 [T][K]: chosen experts in descending key order;
+ *               equal keys are broken toward the lower expert index
+ *   topk_w      out fp32 [T][K]: gate weight of each chosen expert
+ *   logits_opt  out fp32 [T][N] or NULL: the router logits (debug)
+ * Key used for selection: softmax -> the logit (monotone in the softmax);
+ * sigmoid -> sigmoid(logit) + sel_bias. Weights: softmax -> softmax over the
+ * chosen logits; sigmoid -> chosen sigmoid scores / their sum.
+ * sel_bias with softmax scoring returns MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden,
+                             const float* w_router, const float* router_bias,
+                             const float* sel_bias, int32_t* topk_idx,
+                             float* topk_w, float* logits_opt, void* stream);
+
+/*
+ * Route and pack ("Chapter 19", §19.6.3): per-expert histogram, exclusive
+ * prefix sum and a stable expert-major permutation of the T*K token copies
+ * (expert ascending, then token ascending), plus the gather of the hidden rows
+ * into that order.
+ *   topk_idx   int32 [T][K], every entry in [0, N)
+ *   hidden     [T][d], p->hidden_dtype
+ *   counts     out int32 [N]:   counts[e] = #{(t,k) : topk_idx[t][k] == e}
+ *   offsets    out int32 [N+1]: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   perm_src   out int32 [T*K]: permuted row r holds token copy perm_src[r] = t*K + k
+ *   inv_row    out int32 [T*K]: inv_row[t*K + k] = r (the inverse of perm_src)
+ *   x_perm     out bf16 [T*K][d]: x_perm[r] = bf16(hidden[perm_src[r] / K])
+ *   ws         workspace of moe_workspace_bytes(p, MOE_CALL_PERMUTE) bytes
+ * The result is deterministic. An index outside [0, N) sets
+ * MOE_ERR_DEVICE_BOUNDS in the workspace error word; outputs are then undefined.
+ */
+moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx,
+                         const void* hidden, int32_t* counts, int32_t* offsets,
+                         int32_t* perm_src, int32_t* inv_row, void* x_perm,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The routed experts' SwiGLU FFNs over the packed rows, as grouped GEMMs on
+ * the tensor cores (bf16 operands, fp32 accumulation):
+ *   for every expert e and row r in [offsets[e], offsets[e+1]):
+ *     h_perm[r] = bf16( SiLU(W_gate[e] x_perm[r]) * (W_up[e] x_perm[r]) )
+ *     y_perm[r] = bf16( W_down[e] h_perm[r] )          (not yet weighted)
+ *   x_perm  bf16 [T*K][d];  offsets int32 [N+1] as written by moe_permute
+ *   w_gate, w_up bf16 [N][F][d];  w_down bf16 [N][d][F]
+ *   h_perm  out bf16 [T*K][F];  y_perm out bf16 [T*K][d]
+ *   ws      workspace of moe_workspace_bytes(p, MOE_CALL_GROUPED_SWIGLU) bytes
+ * p->n_shared is ignored here. A shared expert runs through this same call as
+ * one group over every token: n_experts = 1, top_k = 1, offsets = {0, T},
+ * x_perm = the hidden rows in bf16, weights = that shared expert's.
+ */
+moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm,
+                                const int32_t* offsets, const void* w_gate,
+                                const void* w_up, const void* w_down,
+                                void* h_perm, void* y_perm, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/*
+ * Gate-weighted combine back to token order ("Chapter 19", §19.2 flowchart,
+ * "Sum with gate weights"; "Mixture of Experts for LLM Inference", "The MoE
+ * change is surprisingly local"):
+ *   out[t] = bf16( sum_k topk_w[t][k] * y_perm[inv_row[t*K + k]]
+ *                  + shared_out[t] )
+ * with fp32 accumulation in slot order k = 0..K-1 (deterministic).
+ *   y_perm bf16 [T*K][d]; inv_row int32 [T*K]; topk_w fp32 [T][K]
+ *   shared_out bf16 [T][d] or NULL;  out bf16 [T][d]
+ */
+moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm,
+                         const int32_t* inv_row, const float* topk_w,
+                         const void* shared_out, void* out, void* stream);
+
+/*
+ * The whole layer: router + top-K, route and pack, grouped SwiGLU with the
+ * SiLU*up product fused into the up-projection epilogue and the gate-weighted
+ * scatter-add fused into the down-projection epilogue, the shared experts
+ * (weight 1) and the final fp32 -> bf16 rounding.
+ *   w            the layer's weights (device pointers inside)
+ *   hidden       [T][d], p->hidden_dtype
+ *   out          out bf16 [T][d]
+ *   topk_idx_opt, topk_w_opt  out int32/fp32 [T][K] or NULL
+ *   counts_opt   out int32 [N] or NULL (per-expert token counts)
+ *   ws           workspace of moe_workspace_bytes(p, MOE_CALL_LAYER_FORWARD)
+ * The fp32 scatter-add makes `out` reproducible only up to the order of
+ * floating-point additions (last-bit differences between runs are possible);
+ * the step-wise calls above are bit-reproducible.
+ */
+moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
+                               const void* hidden, void* out,
+                               int32_t* topk_idx_opt, float* topk_w_opt,
+                               int32_t* counts_opt, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word in `ws`
+ * (a workspace previously passed to moe_permute, moe_grouped_swiglu or
+ * moe_layer_forward). Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS,
+ * or MOE_ERR_CUDA if the stream itself reports an error.
+ */
+moe_status_t moe_get_device_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,147 @@
+"""Seeded synthetic inputs for the MoE layer workloads.
+
+This module only draws random tensors of the right shapes, distributions and
+dtypes. It holds none of the layer's arithmetic (no routing, scoring or FFN), so
+the CUDA path and the oracle can both take their inputs from it.
+
+Recipe (every tensor is drawn in this fixed order from its own seeded stream):
+  * hidden   ~ N(0, 1), [T, d]; fp32 for the tiny workload, else rounded to bf16
+  * w_router ~ N(0, 1/d) * router_scale, fp32 [d, N]
+  * router_bias (the router's bias term): a Zipf(s) popularity tilt
+    -s * ln(rank_e) with rank a seeded permutation of 1..N, else none
+  * sel_bias (selection-only): N(0, variance v), else none
+  * per routed expert e: W_gate[e], W_up[e] ~ N(0, 1/d) [F, d];
+    W_down[e] ~ N(0, 1/F) [d, F]; drawn in fp32, rounded once to bf16
+  * per shared expert s: the same with Fs in place of F
+Router-side tensors (hidden, w_router, biases) always come from a CPU
+generator, so routing is identical whatever device holds the experts. Expert
+weights come from a generator on `device` seeded per expert: large workloads
+draw them on the GPU (the CPU and CUDA generators give different, equally
+distributed values).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEConfig:
+    name: str
+    T: int
+    d: int
+    N: int
+    K: int
+    F: int
+    S: int = 0
+    Fs: int = 0
+    score: str = "softmax"          # "softmax" | "sigmoid"
+    renormalize: int = 1
+    hidden_dtype: str = "bf16"      # "f32" | "bf16"
+    router_scale: float = 1.0
+    sel_bias_var: Optional[float] = None
+    zipf: Optional[float] = None
+
+    def with_(self, **kw) -> "MoEConfig":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def score_fn(self) -> int:
+        return 0 if self.score == "softmax" else 1
+
+
+# Scale of w_router that makes the token-mean of the largest full-softmax
+# probability 0.40 on the Mixtral-shaped workload ("top-1 share about 0.4").
+# Found by bisection with the oracle router on this module's seed-0 inputs:
+# tests/golden/make_mixtral_router_scale.py writes it to
+# tests/golden/mixtral_router_scale.json, and a test checks the two agree.
+MIXTRAL_ROUTER_SCALE = 1.1661
+
+TINY = MoEConfig("tiny", T=64, d=128, N=8, K=2, F=256, score="softmax", hidden_dtype="f32")
+MIXTRAL = MoEConfig("mixtral", T=4096, d=4096, N=8, K=2, F=14336,
+                    router_scale=MIXTRAL_ROUTER_SCALE)
+DSV3 = MoEConfig("dsv3", T=8192, d=7168, N=256, K=8, F=2048, S=1, Fs=2048, score="sigmoid",
+                 sel_bias_var=0.1, zipf=1.1)
+GPTOSS = MoEConfig("gptoss", T=2048, d=2880, N=128, K=4, F=2880)
+QWEN_DECODE = MoEConfig("qwen_decode", T=1, d=4096, N=128, K=8, F=1536)
+DECODE_BATCHES = (1, 8, 32, 128, 512)
+
+CONFIGS = {c.name: c for c in (TINY, MIXTRAL, DSV3, GPTOSS, QWEN_DECODE)}
+
+
+def _seed(seed: int, *parts) -> int:
+    """Derive a stream seed from the base seed and a label (stable across runs)."""
+    h = 1469598103934665603
+    for p in (seed,) + parts:
+        for ch in str(p).encode():
+            h = ((h ^ ch) * 1099511628211) & ((1 << 63) - 1)
+        h = ((h ^ 0x2F) * 1099511628211) & ((1 << 63) - 1)
+    return h
+
+
+def make_router_inputs(cfg: MoEConfig, seed: int = 0) -> dict:
+    """hidden, w_router, router_bias, sel_bias on the CPU."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(_seed(seed, "hidden"))
+    hidden = torch.randn(cfg.T, cfg.d, generator=g, dtype=torch.float32)
+    if cfg.hidden_dtype == "bf16":
+        hidden = hidden.to(torch.bfloat16)
+    g.manual_seed(_seed(seed, "w_router"))
+    w_router = torch.randn(cfg.d, cfg.N, generator=g, dtype=torch.float32)
+    w_router.mul_(cfg.router_scale / math.sqrt(cfg.d))
+    router_bias = None
+    if cfg.zipf is not None:
+        g.manual_seed(_seed(seed, "zipf"))
+        rank = torch.randperm(cfg.N, generator=g).to(torch.float64) + 1.0
+        router_bias = (-cfg.zipf * torch.log(rank)).to(torch.float32)
+    sel_bias = None
+    if cfg.sel_bias_var is not None:
+        g.manual_seed(_seed(seed, "sel_bias"))
+        sel_bias = torch.randn(cfg.N, generator=g, dtype=torch.float32)
+        sel_bias.mul_(math.sqrt(cfg.sel_bias_var))
+    return dict(hidden=hidden, w_router=w_router, router_bias=router_bias, sel_bias=sel_bias)
+
+
+def _draw_bf16(out: torch.Tensor, gen: torch.Generator, std: float) -> None:
+    tmp = torch.randn(out.shape, generator=gen, dtype=torch.float32, device=out.device)
+    tmp.mul_(std)
+    out.copy_(tmp)
+
+
+def make_expert_weights(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
+    """Stacked bf16 expert weights on `device`:
+    w_gate, w_up [N, F, d]; w_down [N, d, F]; ws_gate, ws_up [S, Fs, d];
+    ws_down [S, d, Fs] (None when S == 0)."""
+    device = torch.device(device)
+    bf = torch.bfloat16
+    w_gate = torch.empty(cfg.N, cfg.F, cfg.d, dtype=bf, device=device)
+    w_up = torch.empty_like(w_gate)
+    w_down = torch.empty(cfg.N, cfg.d, cfg.F, dtype=bf, device=device)
+    g = torch.Generator(device=device)
+    for e in range(cfg.N):
+        g.manual_seed(_seed(seed, "routed", e))
+        _draw_bf16(w_gate[e], g, 1.0 / math.sqrt(cfg.d))
+        _draw_bf16(w_up[e], g, 1.0 / math.sqrt(cfg.d))
+        _draw_bf16(w_down[e], g, 1.0 / math.sqrt(cfg.F))
+    ws_gate = ws_up = ws_down = None
+    if cfg.S > 0:
+        ws_gate = torch.empty(cfg.S, cfg.Fs, cfg.d, dtype=bf, device=device)
+        ws_up = torch.empty_like(ws_gate)
+        ws_down = torch.empty(cfg.S, cfg.d, cfg.Fs, dtype=bf, device=device)
+        for s in range(cfg.S):
+            g.manual_seed(_seed(seed, "shared", s))
+            _draw_bf16(ws_gate[s], g, 1.0 / math.sqrt(cfg.d))
+            _draw_bf16(ws_up[s], g, 1.0 / math.sqrt(cfg.d))
+            _draw_bf16(ws_down[s], g, 1.0 / math.sqrt(cfg.Fs))
+    return dict(w_gate=w_gate, w_up=w_up, w_down=w_down, ws_gate=ws_gate, ws_up=ws_up,
+                ws_down=ws_down)
+
+
+def make_inputs(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
+    """Router-side inputs (CPU) plus expert weights on `device`."""
+    out = make_router_inputs(cfg, seed)
+    out.update(make_expert_weights(cfg, seed, device))
+    return out

@@ -1,0 +1,358 @@
+/*
+ * moe_oracle.c — the ORACLE for the token-choice MoE FFN layer forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct CPU
+ * statement of what the layer computes. Only the test suite, the smoke check
+ * and the benchmark's CPU-baseline leg may load it. It shares no code, header,
+ * table or helper with the CUDA library, and the CUDA library never calls it.
+ *
+ * Arithmetic: fp64 throughout, plain loops in the order the definition states,
+ * with one deliberate exception. The router is an fp32 layer ("Chapter 19:
+ * Mixture-of-Experts Models", §19.6.2 table, "Higher-precision router": the
+ * router is kept in higher precision than the bf16 experts). So each logit is
+ * the fp64 dot product rounded once to fp32, and the top-K decision compares
+ * fp32 keys: the same precision the device kernel decides in. Everything after
+ * the decision (weights, expert FFNs, combine) is fp64.
+ *
+ * Expert weights arrive as bf16 bit patterns (uint16) and are widened exactly
+ * to fp64 element by element; hidden rows arrive as fp32 (a bf16 hidden is
+ * widened exactly by the caller).
+ *
+ * Parity status of every function: pinned (see the tests of the oracle).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG -1
+#define ORACLE_ERR_MISSING_EXPERT -2
+
+static double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int moe_oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* SiLU(z) = z * sigmoid(z) = z / (1 + e^-z): the gate nonlinearity of the
+ * SwiGLU reading of "an ordinary MLP" with "3 matrices" ("AI Infrastructure
+ * series Part 12", "What is a Mixture of Experts model?"; "Mixture of Experts
+ * Explained", "The slot it replaces"). */
+double moe_oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* Logistic sigmoid, the DeepSeek-V3 affinity ("Mixture of Experts for LLM
+ * Inference", "Opening the router": sigmoid + normalisation instead of a
+ * softmax). */
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/*
+ * Router for one token ("Mixture of Experts for LLM Inference", "Opening the
+ * router"; "Chapter 19", §19.3.2 and §19.3.4; "AI Infrastructure series Part
+ * 12", "How does the router decide? A worked example").
+ *
+ * 1. logit_e = sum_j x_j * W_router[j][e]  (+ router_bias_e), fp64, j ascending;
+ *    then rounded once to fp32.
+ * 2. softmax scoring: key_e = logit_e; probs_e = full softmax over all N.
+ *    sigmoid scoring: s_e = sigmoid(logit_e); key_e = fp32(s_e + sel_bias_e);
+ *    probs_e = s_e.
+ * 3. top-K: repeatedly take the largest remaining key; equal keys go to the
+ *    lower expert index. Slot k holds the k-th pick.
+ * 4. margin = the smallest gap between consecutive keys among the first
+ *    min(K+1, N) picks: how far the token is from a different choice or a
+ *    different slot order.
+ * 5. weights: softmax + renormalise -> exp(l_j - l_max) / sum over the chosen;
+ *    softmax, no renormalise -> probs of the chosen;
+ *    sigmoid + renormalise -> s_j / sum of chosen s (unbiased: the selection
+ *    bias never reaches the weights); sigmoid, no renormalise -> s_j.
+ */
+static void router_one_token(int32_t d, int32_t N, int32_t K, int32_t score_fn,
+                             int32_t renormalize, const float* x,
+                             const float* w_router, const float* router_bias,
+                             const float* sel_bias, double* logits_out,
+                             double* probs_out, float* keys_out,
+                             int32_t* idx_out, double* w_out, double* margin_out,
+                             float* l32, double* prob, float* key,
+                             unsigned char* taken, int32_t* order) {
+  for (int32_t e = 0; e < N; ++e) {
+    double acc = 0.0;
+    for (int32_t j = 0; j < d; ++j) acc += (double)x[j] * (double)w_router[(int64_t)j * N + e];
+    if (router_bias) acc += (double)router_bias[e];
+    l32[e] = (float)acc;
+    if (logits_out) logits_out[e] = (double)l32[e];
+  }
+  if (score_fn == 0) {
+    double mx = -INFINITY;
+    for (int32_t e = 0; e < N; ++e) if ((double)l32[e] > mx) mx = (double)l32[e];
+    double z = 0.0;
+    for (int32_t e = 0; e < N; ++e) z += exp((double)l32[e] - mx);
+    for (int32_t e = 0; e < N; ++e) {
+      prob[e] = exp((double)l32[e] - mx) / z;
+      key[e] = l32[e];
+    }
+  } else {
+    for (int32_t e = 0; e < N; ++e) {
+      prob[e] = sigmoid((double)l32[e]);
+      double b = sel_bias ? (double)sel_bias[e] : 0.0;
+      key[e] = (float)(prob[e] + b);
+    }
+  }
+  if (probs_out) for (int32_t e = 0; e < N; ++e) probs_out[e] = prob[e];
+  if (keys_out) for (int32_t e = 0; e < N; ++e) keys_out[e] = key[e];
+
+  int32_t picks = (K + 1 < N) ? K + 1 : N;
+  for (int32_t e = 0; e < N; ++e) taken[e] = 0;
+  for (int32_t k = 0; k < picks; ++k) {
+    int32_t best = -1;
+    for (int32_t e = 0; e < N; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || key[e] > key[best]) best = e; /* strict: ties keep the lower index */
+    }
+    taken[best] = 1;
+    order[k] = best;
+  }
+  double margin = INFINITY;
+  for (int32_t k = 0; k + 1 < picks; ++k) {
+    double gap = (double)key[order[k]] - (double)key[order[k + 1]];
+    if (gap < margin) margin = gap;
+  }
+  *margin_out = margin;
+
+  for (int32_t k = 0; k < K; ++k) idx_out[k] = order[k];
+  if (score_fn == 0) {
+    if (renormalize) {
+      double lmax = (double)l32[order[0]];
+      double z = 0.0;
+      for (int32_t k = 0; k < K; ++k) z += exp((double)l32[order[k]] - lmax);
+      for (int32_t k = 0; k < K; ++k) w_out[k] = exp((double)l32[order[k]] - lmax) / z;
+    } else {
+      for (int32_t k = 0; k < K; ++k) w_out[k] = prob[order[k]];
+    }
+  } else {
+    if (renormalize) {
+      double z = 0.0;
+      for (int32_t k = 0; k < K; ++k) z += prob[order[k]];
+      for (int32_t k = 0; k < K; ++k) w_out[k] = prob[order[k]] / z;
+    } else {
+      for (int32_t k = 0; k < K; ++k) w_out[k] = prob[order[k]];
+    }
+  }
+}
+
+static int router_args_ok(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_fn,
+                          const float* hidden, const float* w_router) {
+  if (T < 0 || d <= 0 || N <= 0 || K <= 0 || K > N) return 0;
+  if (score_fn != 0 && score_fn != 1) return 0;
+  if ((T > 0 && !hidden) || !w_router) return 0;
+  return 1;
+}
+
+/*
+ * Router over T tokens (rows of `hidden`, fp32 [T][d]). Outputs per token:
+ * logits/probs (fp64 [T][N], nullable), keys (fp32 [T][N], nullable),
+ * topk_idx [T][K], topk_w (fp64 [T][K]), margin (fp64 [T]).
+ */
+int moe_oracle_router(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_fn,
+                      int32_t renormalize, const float* hidden, const float* w_router,
+                      const float* router_bias, const float* sel_bias,
+                      double* logits_out, double* probs_out, float* keys_out,
+                      int32_t* topk_idx, double* topk_w, double* margin) {
+  if (!router_args_ok(T, d, N, K, score_fn, hidden, w_router)) return ORACLE_ERR_ARG;
+  if (!topk_idx || !topk_w || !margin) return ORACLE_ERR_ARG;
+  int failed = 0;
+#pragma omp parallel
+  {
+    float* l32 = (float*)malloc(sizeof(float) * (size_t)N);
+    double* prob = (double*)malloc(sizeof(double) * (size_t)N);
+    float* key = (float*)malloc(sizeof(float) * (size_t)N);
+    unsigned char* taken = (unsigned char*)malloc((size_t)N);
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    if (!l32 || !prob || !key || !taken || !order) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t t = 0; t < T; ++t) {
+        router_one_token(d, N, K, score_fn, renormalize, hidden + t * d, w_router,
+                         router_bias, sel_bias, logits_out ? logits_out + t * N : NULL,
+                         probs_out ? probs_out + t * N : NULL,
+                         keys_out ? keys_out + t * N : NULL, topk_idx + t * K,
+                         topk_w + t * K, margin + t, l32, prob, key, taken, order);
+      }
+    }
+    free(l32); free(prob); free(key); free(taken); free(order);
+  }
+  return failed ? ORACLE_ERR_ARG : ORACLE_OK;
+}
+
+/*
+ * Route and pack ("Chapter 19", §19.6.3): a counting sort of the T*K token
+ * copies by expert.
+ *   counts[e]    = number of copies whose expert is e (histogram)
+ *   offsets[0]   = 0, offsets[e+1] = offsets[e] + counts[e] (exclusive scan)
+ *   perm_src[r]  = t*K + k for the copies in expert-major order; inside one
+ *                  expert the copies keep their (t, k) order, i.e. token
+ *                  ascending (a token picks an expert at most once)
+ *   inv_row[t*K+k] = r, the inverse permutation.
+ * Returns ORACLE_ERR_ARG if an index lies outside [0, N).
+ */
+int moe_oracle_permute(int64_t T, int32_t K, int32_t N, const int32_t* topk_idx,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                       int32_t* inv_row) {
+  if (T < 0 || K <= 0 || N <= 0 || !counts || !offsets) return ORACLE_ERR_ARG;
+  if (T > 0 && (!topk_idx || !perm_src || !inv_row)) return ORACLE_ERR_ARG;
+  const int64_t n = T * K;
+  for (int32_t e = 0; e < N; ++e) counts[e] = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t e = topk_idx[i];
+    if (e < 0 || e >= N) return ORACLE_ERR_ARG;
+    counts[e] += 1;
+  }
+  offsets[0] = 0;
+  for (int32_t e = 0; e < N; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  if (!cursor) return ORACLE_ERR_ARG;
+  for (int32_t e = 0; e < N; ++e) cursor[e] = offsets[e];
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t r = cursor[topk_idx[i]]++;
+    perm_src[r] = (int32_t)i;
+    inv_row[i] = r;
+  }
+  free(cursor);
+  return ORACLE_OK;
+}
+
+/*
+ * One expert FFN on one token, SwiGLU reading:
+ *   g = W_gate x,  u = W_up x         (W_gate, W_up: bf16 [F][d])
+ *   h_f = SiLU(g_f) * u_f
+ *   y = W_down h                      (W_down: bf16 [d][F])
+ * `h` is caller scratch of F doubles; y is fp64 [d].
+ */
+void moe_oracle_expert_ffn(int32_t d, int32_t F, const double* x, const uint16_t* w_gate,
+                           const uint16_t* w_up, const uint16_t* w_down, double* h,
+                           double* y) {
+  for (int32_t f = 0; f < F; ++f) {
+    double g = 0.0, u = 0.0;
+    const uint16_t* wg = w_gate + (int64_t)f * d;
+    const uint16_t* wu = w_up + (int64_t)f * d;
+    for (int32_t j = 0; j < d; ++j) {
+      g += bf16_bits_to_double(wg[j]) * x[j];
+      u += bf16_bits_to_double(wu[j]) * x[j];
+    }
+    h[f] = moe_oracle_silu(g) * u;
+  }
+  for (int32_t i = 0; i < d; ++i) {
+    double acc = 0.0;
+    const uint16_t* wd = w_down + (int64_t)i * F;
+    for (int32_t f = 0; f < F; ++f) acc += bf16_bits_to_double(wd[f]) * h[f];
+    y[i] = acc;
+  }
+}
+
+/*
+ * Gate-weighted combine for one token ("Chapter 19", §19.3.2 and the §19.2
+ * flowchart "Sum with gate weights"; "AI Infrastructure series Part 12",
+ * worked example): out = sum_k w_k * y_k  (+ shared, weight 1, if given).
+ *   w [K], y [K][d], shared [d] or NULL, out [d].
+ */
+void moe_oracle_combine(int32_t K, int32_t d, const double* w, const double* y,
+                        const double* shared, double* out) {
+  for (int32_t i = 0; i < d; ++i) {
+    double acc = 0.0;
+    for (int32_t k = 0; k < K; ++k) acc += w[k] * y[(int64_t)k * d + i];
+    if (shared) acc += shared[i];
+    out[i] = acc;
+  }
+}
+
+/*
+ * The whole layer for `n_rows` tokens whose hidden rows are given (fp32
+ * [n_rows][d]): router, top-K, every chosen expert's FFN, the always-on shared
+ * experts ("Mixture of Experts for LLM Inference", "Shared experts": they run
+ * for every token and never go through the router; added with weight 1), and
+ * the weighted combine.
+ *
+ * Expert weights are passed as one pointer per expert (each expert is its own
+ * allocation, as "Mixture of Experts Explained", "Three honest caveats" notes);
+ * a NULL pointer means "not provided" and is an error only if a token picks it.
+ *   w_gate[e], w_up[e]: bf16 [F][d];  w_down[e]: bf16 [d][F]
+ *   ws_gate[s], ws_up[s]: bf16 [Fs][d]; ws_down[s]: bf16 [d][Fs]
+ * Outputs: topk_idx [n][K], topk_w fp64 [n][K], margin fp64 [n], out fp64 [n][d].
+ */
+int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
+                     int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
+                     const float* hidden, const float* w_router, const float* router_bias,
+                     const float* sel_bias, const uint16_t* const* w_gate,
+                     const uint16_t* const* w_up, const uint16_t* const* w_down,
+                     const uint16_t* const* ws_gate, const uint16_t* const* ws_up,
+                     const uint16_t* const* ws_down, int32_t* topk_idx, double* topk_w,
+                     double* margin, double* out) {
+  if (!router_args_ok(n_rows, d, N, K, score_fn, hidden, w_router)) return ORACLE_ERR_ARG;
+  if (F <= 0 || S < 0 || (S > 0 && Fs <= 0)) return ORACLE_ERR_ARG;
+  if (!w_gate || !w_up || !w_down || !topk_idx || !topk_w || !margin || !out)
+    return ORACLE_ERR_ARG;
+  if (S > 0 && (!ws_gate || !ws_up || !ws_down)) return ORACLE_ERR_ARG;
+  int status = ORACLE_OK;
+  const int32_t Fmax = (S > 0 && Fs > F) ? Fs : F;
+#pragma omp parallel
+  {
+    float* l32 = (float*)malloc(sizeof(float) * (size_t)N);
+    double* prob = (double*)malloc(sizeof(double) * (size_t)N);
+    float* key = (float*)malloc(sizeof(float) * (size_t)N);
+    unsigned char* taken = (unsigned char*)malloc((size_t)N);
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    double* x = (double*)malloc(sizeof(double) * (size_t)d);
+    double* h = (double*)malloc(sizeof(double) * (size_t)Fmax);
+    double* y = (double*)malloc(sizeof(double) * (size_t)K * (size_t)d);
+    double* sh = (double*)malloc(sizeof(double) * (size_t)d);
+    double* ys = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!l32 || !prob || !key || !taken || !order || !x || !h || !y || !sh || !ys) {
+#pragma omp atomic write
+      status = ORACLE_ERR_ARG;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t t = 0; t < n_rows; ++t) {
+        const float* xr = hidden + t * d;
+        int32_t* idx = topk_idx + t * K;
+        double* w = topk_w + t * K;
+        router_one_token(d, N, K, score_fn, renormalize, xr, w_router, router_bias,
+                         sel_bias, NULL, NULL, NULL, idx, w, margin + t, l32, prob, key,
+                         taken, order);
+        for (int32_t j = 0; j < d; ++j) x[j] = (double)xr[j];
+        int missing = 0;
+        for (int32_t k = 0; k < K; ++k) {
+          int32_t e = idx[k];
+          if (!w_gate[e] || !w_up[e] || !w_down[e]) { missing = 1; break; }
+          moe_oracle_expert_ffn(d, F, x, w_gate[e], w_up[e], w_down[e], h, y + (int64_t)k * d);
+        }
+        if (missing) {
+#pragma omp atomic write
+          status = ORACLE_ERR_MISSING_EXPERT;
+          continue;
+        }
+        for (int32_t i = 0; i < d; ++i) sh[i] = 0.0;
+        for (int32_t s = 0; s < S; ++s) {
+          moe_oracle_expert_ffn(d, Fs, x, ws_gate[s], ws_up[s], ws_down[s], h, ys);
+          for (int32_t i = 0; i < d; ++i) sh[i] += ys[i];
+        }
+        moe_oracle_combine(K, d, w, y, S > 0 ? sh : NULL, out + t * d);
+      }
+    }
+    free(l32); free(prob); free(key); free(taken); free(order);
+    free(x); free(h); free(y); free(sh); free(ys);
+  }
+  return status;
+}

@@ -1,0 +1,218 @@
+"""Python view of the MoE layer ORACLE (oracle/moe_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
+benchmark's CPU-baseline leg, never by the CUDA library or its binding. The
+arithmetic lives in moe_oracle.c (plain C, fp64, fp32 router decision); this
+module only marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into oracle/liboracle.so with gcc + OpenMP."""
+    if force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    ):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        lib.moe_oracle_router.argtypes = [i64, i32, i32, i32, i32, i32] + [P] * 10
+        lib.moe_oracle_router.restype = ctypes.c_int
+        lib.moe_oracle_permute.argtypes = [i64, i32, i32, P, P, P, P, P]
+        lib.moe_oracle_permute.restype = ctypes.c_int
+        lib.moe_oracle_expert_ffn.argtypes = [i32, i32, P, P, P, P, P, P]
+        lib.moe_oracle_expert_ffn.restype = None
+        lib.moe_oracle_combine.argtypes = [i32, i32, P, P, P, P]
+        lib.moe_oracle_combine.restype = None
+        lib.moe_oracle_layer.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32] + [P] * 14
+        lib.moe_oracle_layer.restype = ctypes.c_int
+        lib.moe_oracle_silu.argtypes = [ctypes.c_double]
+        lib.moe_oracle_silu.restype = ctypes.c_double
+        lib.moe_oracle_num_threads.argtypes = []
+        lib.moe_oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _bf16_bits(a):
+    """Accept a uint16 array of bf16 bit patterns (or a torch bf16 tensor)."""
+    if a is None:
+        return None
+    if hasattr(a, "view") and hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+
+        return np.ascontiguousarray(a.contiguous().view(torch.int16).numpy().view(np.uint16))
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("expert weights must be bf16 bit patterns (uint16)")
+    return a
+
+
+SOFTMAX, SIGMOID = 0, 1
+
+
+def num_threads() -> int:
+    return int(_load().moe_oracle_num_threads())
+
+
+def silu(z: float) -> float:
+    return float(_load().moe_oracle_silu(float(z)))
+
+
+def router(hidden, w_router, K, score_fn=SOFTMAX, renormalize=1, router_bias=None,
+           sel_bias=None):
+    """Router over the rows of `hidden` (fp32 [T][d]). Returns a dict with
+    logits (fp64 [T][N]), probs (fp64 [T][N]: full softmax or sigmoid scores),
+    keys (fp32 [T][N]), idx (int32 [T][K]), w (fp64 [T][K]), margin (fp64 [T])."""
+    lib = _load()
+    x = _f32(hidden)
+    W = _f32(w_router)
+    T, d = x.shape
+    d2, N = W.shape
+    assert d == d2
+    rb, sb = _f32(router_bias), _f32(sel_bias)
+    logits = np.empty((T, N), np.float64)
+    probs = np.empty((T, N), np.float64)
+    keys = np.empty((T, N), np.float32)
+    idx = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float64)
+    margin = np.empty((T,), np.float64)
+    rc = lib.moe_oracle_router(T, d, N, K, score_fn, renormalize, _ptr(x), _ptr(W), _ptr(rb),
+                               _ptr(sb), _ptr(logits), _ptr(probs), _ptr(keys), _ptr(idx),
+                               _ptr(w), _ptr(margin))
+    if rc != 0:
+        raise ValueError(f"moe_oracle_router failed ({rc})")
+    return dict(logits=logits, probs=probs, keys=keys, idx=idx, w=w, margin=margin)
+
+
+def permute(topk_idx, N):
+    """Counting sort of the token copies by expert. Returns counts, offsets,
+    perm_src, inv_row (int32)."""
+    lib = _load()
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, K = idx.shape
+    counts = np.empty((N,), np.int32)
+    offsets = np.empty((N + 1,), np.int32)
+    perm_src = np.empty((T * K,), np.int32)
+    inv_row = np.empty((T * K,), np.int32)
+    rc = lib.moe_oracle_permute(T, K, N, _ptr(idx), _ptr(counts), _ptr(offsets), _ptr(perm_src),
+                                _ptr(inv_row))
+    if rc != 0:
+        raise ValueError(f"moe_oracle_permute failed ({rc})")
+    return dict(counts=counts, offsets=offsets, perm_src=perm_src, inv_row=inv_row)
+
+
+def expert_ffn(x, w_gate, w_up, w_down):
+    """One SwiGLU expert on one token: x fp64 [d], weights bf16 bit patterns."""
+    lib = _load()
+    x = _f64(x)
+    wg, wu, wd = _bf16_bits(w_gate), _bf16_bits(w_up), _bf16_bits(w_down)
+    F, d = wg.shape
+    assert x.shape == (d,) and wu.shape == (F, d) and wd.shape == (d, F)
+    h = np.empty((F,), np.float64)
+    y = np.empty((d,), np.float64)
+    lib.moe_oracle_expert_ffn(d, F, _ptr(x), _ptr(wg), _ptr(wu), _ptr(wd), _ptr(h), _ptr(y))
+    return y
+
+
+def combine(w, y, shared=None):
+    """out = sum_k w[k] * y[k] (+ shared)."""
+    lib = _load()
+    w = _f64(w)
+    y = _f64(y)
+    K, d = y.shape
+    sh = _f64(shared)
+    out = np.empty((d,), np.float64)
+    lib.moe_oracle_combine(K, d, _ptr(w), _ptr(y), _ptr(sh), _ptr(out))
+    return out
+
+
+def _ptr_array(mats, n):
+    arr = (ctypes.c_void_p * n)()
+    keep = []
+    for i in range(n):
+        m = mats[i] if mats is not None and i < len(mats) else None
+        if m is None:
+            arr[i] = None
+        else:
+            b = _bf16_bits(m)
+            keep.append(b)
+            arr[i] = b.ctypes.data
+    return arr, keep
+
+
+def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormalize=1,
+          router_bias=None, sel_bias=None, ws_gate=None, ws_up=None, ws_down=None):
+    """The whole layer for the rows of `hidden` (fp32 [n][d]).
+
+    w_gate / w_up / w_down: sequences of N per-expert bf16 matrices (uint16 bit
+    patterns or torch bf16), an entry may be None if no token picks it.
+    ws_*: sequences of S shared-expert matrices or None.
+    Returns dict(idx, w, margin, out) with out fp64 [n][d].
+    """
+    lib = _load()
+    x = _f32(hidden)
+    W = _f32(w_router)
+    n, d = x.shape
+    N = W.shape[1]
+    F = next(_bf16_bits(m).shape[0] for m in w_gate if m is not None)
+    S = 0 if ws_gate is None else len(ws_gate)
+    Fs = _bf16_bits(ws_gate[0]).shape[0] if S else 0
+    g_arr, k1 = _ptr_array(w_gate, N)
+    u_arr, k2 = _ptr_array(w_up, N)
+    d_arr, k3 = _ptr_array(w_down, N)
+    sg_arr, k4 = _ptr_array(ws_gate, max(S, 1))
+    su_arr, k5 = _ptr_array(ws_up, max(S, 1))
+    sd_arr, k6 = _ptr_array(ws_down, max(S, 1))
+    rb, sb = _f32(router_bias), _f32(sel_bias)
+    idx = np.empty((n, K), np.int32)
+    w = np.empty((n, K), np.float64)
+    margin = np.empty((n,), np.float64)
+    out = np.empty((n, d), np.float64)
+    rc = lib.moe_oracle_layer(n, d, N, K, F, S, Fs, score_fn, renormalize, _ptr(x), _ptr(W),
+                              _ptr(rb), _ptr(sb), ctypes.cast(g_arr, ctypes.c_void_p),
+                              ctypes.cast(u_arr, ctypes.c_void_p),
+                              ctypes.cast(d_arr, ctypes.c_void_p),
+                              ctypes.cast(sg_arr, ctypes.c_void_p) if S else None,
+                              ctypes.cast(su_arr, ctypes.c_void_p) if S else None,
+                              ctypes.cast(sd_arr, ctypes.c_void_p) if S else None,
+                              _ptr(idx), _ptr(w), _ptr(margin), _ptr(out))
+    del k1, k2, k3, k4, k5, k6
+    if rc != 0:
+        raise ValueError(f"moe_oracle_layer failed ({rc})")
+    return dict(idx=idx, w=w, margin=margin, out=out)

@@ -1,0 +1,390 @@
+"""Pins of the oracle (CPU only).
+
+Each test ties the oracle to something other than itself: a worked example
+printed on the pages, a library routine (numpy / scipy / torch), a closed form,
+an invariant the pages state, or brute force on tiny inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import oracle
+from mixture_experts_layer_94_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bf16_bits(a):
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _bf16_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _identity_router(logits):
+    """hidden = logits and W_router = I, so the router's logits are the given values."""
+    logits = np.asarray(logits, dtype=np.float32)[None, :]
+    return logits, np.eye(logits.shape[1], dtype=np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Worked examples printed on the pages
+# ---------------------------------------------------------------------------
+
+def test_p5_worked_example_top2_softmax_over_pair():
+    """"Mixture of Experts Explained", 'The router, with real numbers'."""
+    g = _golden("p5_router_example.json")
+    pr = g["printed"]
+    x, W = _identity_router(g["logits"])
+    r = oracle.router(x, W, K=2, score_fn=oracle.SOFTMAX, renormalize=1)
+    assert (r["idx"][0] + 1).tolist() == pr["top2_experts_1based"]
+    l1, l2 = r["logits"][0, r["idx"][0]]
+    assert round(math.exp(l1), 1) == pr["exp_winner1"]
+    assert round(math.exp(l2), 1) == pr["exp_winner2"]
+    assert abs(math.exp(l1) + math.exp(l2) - pr["exp_sum"]) < 0.05
+    assert round(r["w"][0, 0], 3) == pr["gate_winner1"]
+    assert round(r["w"][0, 1], 3) == pr["gate_winner2"]
+    # The page's "about" values for the full 8-way softmax of the winners.
+    p = r["probs"][0, r["idx"][0]]
+    assert abs(p[0] - pr["full_softmax_winner1_about"]) < 0.005
+    assert abs(p[1] - pr["full_softmax_winner2_about"]) < 0.005
+    assert abs(p.sum() - pr["full_softmax_pair_sum_about"]) < 0.005
+    # Without renormalisation the weights are those full-softmax values.
+    r0 = oracle.router(x, W, K=2, score_fn=oracle.SOFTMAX, renormalize=0)
+    np.testing.assert_allclose(r0["w"][0], p, rtol=0, atol=1e-15)
+
+
+def test_p2_worked_example_router_and_mix():
+    """"AI Infrastructure series Part 12", 'How does the router decide? A worked
+    example': full softmax, keep two, renormalise, mix the two expert vectors."""
+    g = _golden("p2_router_example.json")
+    pr = g["printed"]
+    x, W = _identity_router(g["reconstructed_logits"])
+    assert abs(np.exp(np.asarray(g["reconstructed_logits"])).sum() - pr["exp_sum"]) < 0.005
+    r = oracle.router(x, W, K=2, score_fn=oracle.SOFTMAX, renormalize=1)
+    assert (r["idx"][0] + 1).tolist() == pr["winners_1based"]
+    p = r["probs"][0, r["idx"][0]]
+    assert round(p[0], 3) == pr["prob_winner1"]
+    assert round(p[1], 3) == pr["prob_winner2"]
+    assert round(p.sum(), 3) == pr["prob_pair_sum"]
+    assert round(r["w"][0, 0], 2) == pr["weight_winner1"]
+    assert round(r["w"][0, 1], 2) == pr["weight_winner2"]
+    y = np.array([pr["expert_out_winner1_prefix"], pr["expert_out_winner2_prefix"]])
+    out = oracle.combine(r["w"][0], y)
+    np.testing.assert_allclose(out, g["output_prefix_from_printed_weights"], atol=0.006)
+    # And exactly the printed-weight arithmetic when fed the printed weights.
+    out_printed = oracle.combine([pr["weight_winner1"], pr["weight_winner2"]], y)
+    np.testing.assert_allclose(out_printed, g["output_prefix_from_printed_weights"], atol=5e-4)
+
+
+# ---------------------------------------------------------------------------
+# Router: library routines, equivalences the pages state, brute force
+# ---------------------------------------------------------------------------
+
+def _rand_router_case(rng, T, d, N, dup_cols=0):
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    W = (rng.standard_normal((d, N)) / math.sqrt(d)).astype(np.float32)
+    for _ in range(dup_cols):  # exact ties: two experts with identical router columns
+        a, b = rng.choice(N, size=2, replace=False)
+        W[:, b] = W[:, a]
+    return x, W
+
+
+def test_logits_match_library_matmul_with_router_bias():
+    rng = np.random.default_rng(1)
+    x, W = _rand_router_case(rng, 200, 96, 16)
+    b = rng.standard_normal(16).astype(np.float32)
+    r = oracle.router(x, W, K=3, router_bias=b)
+    ref = (x.astype(np.float64) @ W.astype(np.float64) + b).astype(np.float32)
+    ulp = np.spacing(np.abs(ref)).astype(np.float64)
+    assert np.all(np.abs(r["logits"] - ref) <= ulp)
+
+
+def test_softmax_over_topk_equals_full_softmax_renormalised():
+    """"Chapter 19", §19.3.2: softmax over the selected logits equals softmax
+    over all logits, then Top-K, then renormalisation ("AI Infrastructure
+    series Part 12": Mixtral's top-two softmax gives the same weights)."""
+    rng = np.random.default_rng(2)
+    x, W = _rand_router_case(rng, 10000, 32, 8)
+    r = oracle.router(x, W, K=2, score_fn=oracle.SOFTMAX, renormalize=1)
+    full = scipy.special.softmax(r["logits"], axis=1)           # library softmax
+    np.testing.assert_allclose(r["probs"], full, rtol=1e-12, atol=1e-15)
+    chosen = np.take_along_axis(full, r["idx"].astype(np.int64), axis=1)
+    ren = chosen / chosen.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(r["w"], ren, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("score_fn", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_weights_sum_to_one(score_fn):
+    """"Mixture of Experts for LLM Inference", 'Opening the router': the survivors
+    are renormalised so the budget adds back to 1."""
+    rng = np.random.default_rng(3)
+    x, W = _rand_router_case(rng, 3000, 40, 32)
+    sb = rng.standard_normal(32).astype(np.float32) * 0.3 if score_fn == oracle.SIGMOID else None
+    for K in (1, 2, 8, 32):
+        r = oracle.router(x, W, K=K, score_fn=score_fn, sel_bias=sb)
+        np.testing.assert_allclose(r["w"].sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        assert np.all(r["w"] >= 0)
+
+
+def test_sigmoid_selection_bias_hand_case():
+    """DeepSeek-V3 style ("Chapter 19", §19.3.4; "AI Infrastructure series Part
+    12", worked example): sigmoid scores, a bias that shifts selection only,
+    chosen scores normalised to sum to 1."""
+    logits = [2.0, 1.0, 0.5, -1.0]
+    sel = np.array([0.0, 0.0, 0.5, 0.0], np.float32)
+    x, W = _identity_router(logits)
+    s = scipy.special.expit(np.asarray(logits, np.float64))     # library sigmoid
+    r = oracle.router(x, W, K=2, score_fn=oracle.SIGMOID, sel_bias=sel)
+    # keys: s + b = [0.881, 0.731, 1.122, 0.269]: the bias moves expert 2 to the top
+    assert r["idx"][0].tolist() == [2, 0]
+    np.testing.assert_allclose(r["w"][0], [s[2] / (s[2] + s[0]), s[0] / (s[2] + s[0])],
+                               rtol=0, atol=1e-12)
+    # without the bias the selection is the two largest logits
+    r0 = oracle.router(x, W, K=2, score_fn=oracle.SIGMOID)
+    assert r0["idx"][0].tolist() == [0, 1]
+    np.testing.assert_allclose(r0["w"][0], [s[0] / (s[0] + s[1]), s[1] / (s[0] + s[1])],
+                               rtol=0, atol=1e-12)
+    # no renormalisation -> the raw sigmoid scores of the chosen experts
+    r1 = oracle.router(x, W, K=2, score_fn=oracle.SIGMOID, sel_bias=sel, renormalize=0)
+    np.testing.assert_allclose(r1["w"][0], [s[2], s[0]], rtol=0, atol=1e-12)
+
+
+def test_sigmoid_zero_bias_selects_top_logits():
+    rng = np.random.default_rng(4)
+    x, W = _rand_router_case(rng, 2000, 64, 64)
+    r = oracle.router(x, W, K=8, score_fn=oracle.SIGMOID)
+    ref = np.argsort(-r["logits"], axis=1, kind="stable")[:, :8]
+    ok = r["margin"] > 0
+    assert ok.mean() > 0.99
+    assert np.array_equal(r["idx"][ok], ref[ok])
+
+
+@pytest.mark.parametrize("score_fn", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_topk_equals_brute_force_sort_with_ties(score_fn):
+    """Top-K equals a full stable sort by (key descending, expert ascending),
+    including exact ties made by duplicated router columns."""
+    rng = np.random.default_rng(5)
+    for N in (1, 2, 3, 5, 8):
+        x, W = _rand_router_case(rng, 300, 12, N, dup_cols=1 if N >= 2 else 0)
+        sb = (rng.standard_normal(N) * 0.2).astype(np.float32) if score_fn else None
+        if sb is not None and N >= 2:
+            sb[1] = sb[0]  # keep some ties alive through the bias
+        lg = (x.astype(np.float64) @ W.astype(np.float64)).astype(np.float32)
+        if score_fn == oracle.SOFTMAX:
+            keys = lg
+        else:
+            keys = (scipy.special.expit(lg.astype(np.float64)) + sb.astype(np.float64)).astype(np.float32)
+        for K in range(1, N + 1):
+            r = oracle.router(x, W, K=K, score_fn=score_fn, sel_bias=sb)
+            assert np.all(np.abs(r["keys"].astype(np.float64) - keys) <=
+                          np.spacing(np.abs(keys)).astype(np.float64))
+            ks = r["keys"]
+            for t in range(x.shape[0]):
+                order = sorted(range(N), key=lambda e: (-float(ks[t, e]), e))
+                assert r["idx"][t].tolist() == order[:K]
+
+
+def test_margin_definition_hand_case():
+    x, W = _identity_router([3.0, 2.0, 2.5, 0.0])
+    r = oracle.router(x, W, K=2)
+    assert r["idx"][0].tolist() == [0, 2]
+    assert r["margin"][0] == pytest.approx(0.5)          # gaps 0.5 (3->2.5) and 0.5 (2.5->2)
+    x, W = _identity_router([3.0, 3.0, 1.0])
+    r = oracle.router(x, W, K=1)
+    assert r["idx"][0].tolist() == [0] and r["margin"][0] == 0.0
+    x, W = _identity_router([1.0, 4.0, 2.0])
+    r = oracle.router(x, W, K=3)                           # K == N: all consecutive gaps
+    assert r["idx"][0].tolist() == [1, 2, 0] and r["margin"][0] == pytest.approx(1.0)
+
+
+# ---------------------------------------------------------------------------
+# Route and pack: invariants and a library stable sort
+# ---------------------------------------------------------------------------
+
+def _random_topk(rng, T, N, K, skew=False):
+    idx = np.empty((T, K), np.int32)
+    p = None
+    if skew:
+        p = 1.0 / np.arange(1, N + 1) ** 1.5
+        p /= p.sum()
+    for t in range(T):
+        idx[t] = rng.choice(N, size=K, replace=False, p=p)
+    return idx
+
+
+@pytest.mark.parametrize("T,N,K,skew", [(0, 4, 2, False), (1, 8, 8, False), (37, 8, 2, False),
+                                        (500, 64, 6, True), (300, 256, 8, True)])
+def test_permute_invariants_and_stable_sort(T, N, K, skew):
+    rng = np.random.default_rng(6)
+    idx = _random_topk(rng, T, N, K, skew)
+    p = oracle.permute(idx, N)
+    flat = idx.reshape(-1)
+    assert np.array_equal(p["counts"], np.bincount(flat, minlength=N))
+    assert np.array_equal(p["offsets"], np.concatenate([[0], np.cumsum(p["counts"])]))
+    assert p["counts"].sum() == T * K
+    assert np.array_equal(p["perm_src"], np.argsort(flat, kind="stable").astype(np.int32))
+    assert np.array_equal(p["inv_row"][p["perm_src"]], np.arange(T * K))
+    for e in range(N):  # each expert's segment: that expert only, tokens ascending
+        seg = p["perm_src"][p["offsets"][e]:p["offsets"][e + 1]]
+        assert np.all(flat[seg] == e)
+        assert np.all(np.diff(seg // K) > 0)
+
+
+def test_permute_rejects_out_of_range_index():
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[0, 9]], np.int32), 8)
+
+
+# ---------------------------------------------------------------------------
+# Expert FFN, combine and the whole layer: closed forms and library routines
+# ---------------------------------------------------------------------------
+
+def test_silu_closed_form():
+    assert oracle.silu(0.0) == 0.0
+    for z in (-20.0, -3.0, -0.5, 0.7, 1.0, 4.0, 30.0):
+        assert oracle.silu(z) == pytest.approx(z * scipy.special.expit(z), rel=1e-14, abs=1e-300)
+    assert oracle.silu(1.0) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+
+
+def _torch_swiglu(x, wg, wu, wd):
+    """Dense SwiGLU FFN from torch library routines, fp64."""
+    x = torch.as_tensor(x, dtype=torch.float64)
+    g = torch.as_tensor(_bf16_to_f64(wg)) @ x
+    u = torch.as_tensor(_bf16_to_f64(wu)) @ x
+    return (torch.as_tensor(_bf16_to_f64(wd)) @ (torch.nn.functional.silu(g) * u)).numpy()
+
+
+def test_expert_ffn_matches_torch():
+    rng = np.random.default_rng(7)
+    d, F = 24, 40
+    x = rng.standard_normal(d)
+    wg = _bf16_bits(rng.standard_normal((F, d)) / math.sqrt(d))
+    wu = _bf16_bits(rng.standard_normal((F, d)) / math.sqrt(d))
+    wd = _bf16_bits(rng.standard_normal((d, F)) / math.sqrt(F))
+    y = oracle.expert_ffn(x, wg, wu, wd)
+    np.testing.assert_allclose(y, _torch_swiglu(x, wg, wu, wd), rtol=1e-12, atol=1e-14)
+
+
+def _rand_experts(rng, n, d, F):
+    return ([_bf16_bits(rng.standard_normal((F, d)) / math.sqrt(d)) for _ in range(n)],
+            [_bf16_bits(rng.standard_normal((F, d)) / math.sqrt(d)) for _ in range(n)],
+            [_bf16_bits(rng.standard_normal((d, F)) / math.sqrt(F)) for _ in range(n)])
+
+
+def test_K_equals_N_is_dense_softmax_mixture():
+    """K = N with renormalisation: every expert runs and the weights are the full
+    softmax, so the layer is the textbook dense mixture sum_e softmax(l)_e E_e(x)."""
+    rng = np.random.default_rng(8)
+    T, d, N, F = 6, 16, 4, 20
+    x, W = _rand_router_case(rng, T, d, N)
+    wg, wu, wd = _rand_experts(rng, N, d, F)
+    r = oracle.layer(x, W, wg, wu, wd, K=N)
+    lg = torch.as_tensor((x.astype(np.float64) @ W.astype(np.float64)).astype(np.float32),
+                         dtype=torch.float64)
+    p = torch.softmax(lg, dim=1).numpy()
+    ref = np.stack([sum(p[t, e] * _torch_swiglu(x[t].astype(np.float64), wg[e], wu[e], wd[e])
+                        for e in range(N)) for t in range(T)])
+    np.testing.assert_allclose(r["out"], ref, rtol=1e-9, atol=1e-12)
+
+
+@pytest.mark.parametrize("score_fn", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_single_expert_is_dense_ffn(score_fn):
+    """N = K = 1: the router always picks the one expert with weight 1 and the
+    layer is a dense SwiGLU FFN."""
+    rng = np.random.default_rng(9)
+    T, d, F = 5, 32, 48
+    x, W = _rand_router_case(rng, T, d, 1)
+    wg, wu, wd = _rand_experts(rng, 1, d, F)
+    r = oracle.layer(x, W, wg, wu, wd, K=1, score_fn=score_fn)
+    assert np.all(r["idx"] == 0) and np.all(r["w"] == 1.0)
+    ref = np.stack([_torch_swiglu(x[t].astype(np.float64), wg[0], wu[0], wd[0]) for t in range(T)])
+    np.testing.assert_allclose(r["out"], ref, rtol=1e-10, atol=1e-13)
+
+
+def test_shared_expert_alone_when_routed_outputs_vanish():
+    """"Mixture of Experts for LLM Inference", 'Shared experts': the shared expert
+    runs for every token outside the router; with the routed experts' W_down all
+    zero the layer output is exactly the shared FFN."""
+    rng = np.random.default_rng(10)
+    T, d, N, K, F, Fs = 7, 16, 6, 2, 24, 40
+    x, W = _rand_router_case(rng, T, d, N)
+    wg, wu, _ = _rand_experts(rng, N, d, F)
+    wd = [np.zeros((d, F), np.uint16) for _ in range(N)]
+    sg, su, sd = _rand_experts(rng, 1, d, Fs)
+    r = oracle.layer(x, W, wg, wu, wd, K=K, score_fn=oracle.SIGMOID, ws_gate=sg, ws_up=su,
+                     ws_down=sd)
+    ref = np.stack([_torch_swiglu(x[t].astype(np.float64), sg[0], su[0], sd[0]) for t in range(T)])
+    np.testing.assert_allclose(r["out"], ref, rtol=1e-10, atol=1e-13)
+    # two shared experts add up
+    sg2, su2, sd2 = _rand_experts(rng, 1, d, Fs)
+    r2 = oracle.layer(x, W, wg, wu, wd, K=K, ws_gate=sg + sg2, ws_up=su + su2, ws_down=sd + sd2)
+    ref2 = ref + np.stack([_torch_swiglu(x[t].astype(np.float64), sg2[0], su2[0], sd2[0])
+                           for t in range(T)])
+    np.testing.assert_allclose(r2["out"], ref2, rtol=1e-10, atol=1e-13)
+
+
+def test_layer_matches_independent_numpy_on_tiny_workload():
+    """Cross-check (not a pin): an independent numpy fp64 statement of the whole
+    layer on the tiny workload agrees with the C oracle."""
+    cfg = inputs.TINY
+    ins = inputs.make_inputs(cfg, seed=0)
+    x = ins["hidden"].numpy().astype(np.float32)
+    W = ins["w_router"].numpy()
+    bits = {k: ins[k].view(torch.int16).numpy().view(np.uint16) for k in ("w_gate", "w_up", "w_down")}
+    r = oracle.layer(x, W, list(bits["w_gate"]), list(bits["w_up"]), list(bits["w_down"]), K=cfg.K)
+    lg = (x.astype(np.float64) @ W.astype(np.float64)).astype(np.float32).astype(np.float64)
+    idx = np.argsort(-lg, axis=1, kind="stable")[:, :cfg.K]
+    assert np.array_equal(idx, r["idx"])
+    sel = np.take_along_axis(lg, idx, axis=1)
+    w = np.exp(sel - sel[:, :1])
+    w /= w.sum(axis=1, keepdims=True)
+    wg, wu, wd = (_bf16_to_f64(bits[k]) for k in ("w_gate", "w_up", "w_down"))
+    out = np.zeros((cfg.T, cfg.d))
+    for t in range(cfg.T):
+        for k in range(cfg.K):
+            e = idx[t, k]
+            g = wg[e] @ x[t].astype(np.float64)
+            u = wu[e] @ x[t].astype(np.float64)
+            out[t] += w[t, k] * (wd[e] @ (g / (1 + np.exp(-g)) * u))
+    np.testing.assert_allclose(r["out"], out, rtol=1e-9, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Generator sanity and stored constants
+# ---------------------------------------------------------------------------
+
+def test_union_of_touched_experts_follows_independent_routing_formula():
+    """"AI Infrastructure series Part 12", 'What happens when many users share the
+    GPU?' and "Mixture of Experts Explained", 'Why batching erodes the advantage':
+    with independent routing, B tokens picking k of N touch N(1-(1-k/N)^B)
+    distinct experts on average. A sanity check of the decode workload's
+    Gaussian router, not of the oracle."""
+    cfg = inputs.QWEN_DECODE
+    for T in (8, 32):
+        counts = []
+        for seed in range(6):
+            ri = inputs.make_router_inputs(cfg.with_(T=T), seed=seed)
+            r = oracle.router(ri["hidden"].float().numpy(), ri["w_router"].numpy(), K=cfg.K)
+            counts.append(len(np.unique(r["idx"])))
+        p = 1 - (1 - cfg.K / cfg.N) ** T
+        mean, sd = cfg.N * p, math.sqrt(cfg.N * p * (1 - p))
+        assert all(abs(c - mean) <= 4 * sd for c in counts), (T, counts, mean, sd)
+
+
+def test_mixtral_router_scale_constant_matches_fixture():
+    g = _golden("mixtral_router_scale.json")
+    assert g["router_scale"] == inputs.MIXTRAL_ROUTER_SCALE
+    assert abs(g["top1_share_at_scale"] - 0.40) < 0.002
