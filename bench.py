@@ -1,0 +1,393 @@
+#!/usr/bin/env python
+"""MoE layer benchmark: tokens/s of one token-choice MoE FFN layer forward on a
+B300, and the roofline fraction of its dominant kernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one moe_layer_forward over one batch of the workload (router + top-K,
+route and pack, grouped SwiGLU GEMMs, weighted combine) with inputs resident in
+HBM. With N > 1 (torchrun), every rank runs an independent replica on its own
+batch (weak scaling; the layer has no exchange step when tokens are split
+across replicas); only the timing uses a barrier and a max over ranks.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_94_b300 import inputs  # noqa: E402
+
+METRIC = "MoE layer tokens/s on 1 B300; % of roofline (bf16 TFLOP/s prefill, HBM GB/s decode)"
+WORKLOADS = {
+    "mixtral": (inputs.MIXTRAL, "Mixtral-8x7B-shaped prefill layer"),
+    "dsv3": (inputs.DSV3, "DeepSeek-V3-shaped prefill layer"),
+    "gptoss": (inputs.GPTOSS, "gpt-oss-120b-shaped layer"),
+    "tiny": (inputs.TINY, "tiny Mixtral-style layer"),
+}
+for _T in inputs.DECODE_BATCHES:
+    WORKLOADS[f"decode{_T}"] = (inputs.QWEN_DECODE.with_(T=_T), f"Qwen3-235B-like decode layer, T={_T}")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work of the oracle baseline sample (rank 0, N=1)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def work_model(cfg, counts=None):
+    """Algorithmic FLOPs and bytes of one layer forward (tile padding excluded).
+    Bytes: the weights of touched experts, the router, and hidden in + out."""
+    T, d, N, K, F, S, Fs = cfg.T, cfg.d, cfg.N, cfg.K, cfg.F, cfg.S, cfg.Fs
+    hid_b = 4 if cfg.hidden_dtype == "f32" else 2
+    flops_router = 2 * T * d * N
+    flops_gu = 4 * d * F * T * K + 4 * d * Fs * T * S
+    flops_dn = 2 * d * F * T * K + 2 * d * Fs * T * S
+    touched = N if counts is None else int((np.asarray(counts) > 0).sum())
+    w_expert = 3 * d * F * 2
+    bytes_w = touched * w_expert + S * 3 * d * Fs * 2 + 4 * d * N
+    bytes_act = T * d * (hid_b + 2)
+    return dict(flops=flops_router + flops_gu + flops_dn, flops_gateup=flops_gu, flops_down=flops_dn,
+                bytes=bytes_w + bytes_act, bytes_gateup=touched * 2 * d * F * 2 + S * 2 * d * Fs * 2,
+                bytes_down=touched * d * F * 2 + S * d * Fs * 2, touched=touched)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:  # no nvidia-smi: no clock record
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or [p for (_, p) in self.samples]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_from_profiles(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.md,
+    or None when absent or taken on other kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = os.path.join(ROOT, "mixture_experts_layer_94_b300", "csrc", "grouped_gemm.cu")
+    import hashlib
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
+    for line in text.splitlines():
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+            if cells[3] != digest:
+                return None
+            try:
+                return float(cells[2])
+            except ValueError:
+                return None
+    return None
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle legs
+def oracle_rows_timed(cfg, ins, rows):
+    """Run the oracle layer on the given token rows; returns (tokens, seconds, threads)."""
+    from oracle import oracle
+
+    x = ins["hidden"].float().cpu().numpy()[rows]
+    r = oracle.router(x, ins["w_router"].cpu().numpy(), K=cfg.K, score_fn=cfg.score_fn,
+                      renormalize=cfg.renormalize,
+                      router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
+                      sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy())
+    used = sorted(set(r["idx"].reshape(-1).tolist()))
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    wg, wu, wd = [None] * cfg.N, [None] * cfg.N, [None] * cfg.N
+    for e in used:
+        wg[e], wu[e], wd[e] = bits(ins["w_gate"][e]), bits(ins["w_up"][e]), bits(ins["w_down"][e])
+    sh = {}
+    if cfg.S:
+        sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in ("ws_gate", "ws_up", "ws_down")}
+    t0 = time.perf_counter()
+    oracle.layer(x, ins["w_router"].cpu().numpy(), wg, wu, wd, K=cfg.K, score_fn=cfg.score_fn,
+                 renormalize=cfg.renormalize,
+                 router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
+                 sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), **sh)
+    return len(rows), time.perf_counter() - t0, oracle.num_threads()
+
+
+def cpu_baseline(cfg, ins, budget_s):
+    from oracle import oracle
+
+    thr = oracle.num_threads()
+    done, spent, start = 0, 0.0, 0
+    while spent < budget_s and start < cfg.T:
+        rows = np.arange(start, min(cfg.T, start + thr))
+        n, s, _ = oracle_rows_timed(cfg, ins, rows)
+        done, spent, start = done + n, spent + s, start + n
+    return {"value": done / spent, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "sample": f"first {done} tokens of the same workload through the fp64 oracle layer "
+                      f"(router, top-K, SwiGLU experts, combine), {spent:.1f} s of CPU wall time"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, cfg, desc, world, rank):
+    """The oracle as it stands, on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    from oracle import oracle
+
+    ins = inputs.make_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    thr = oracle.num_threads()
+    rows = np.arange(min(cfg.T, thr))
+    for _ in range(args.warmup):
+        oracle_rows_timed(cfg, ins, rows)
+    tok, sec = 0, 0.0
+    for _ in range(args.steps):
+        n, s, _ = oracle_rows_timed(cfg, ins, rows)
+        tok, sec = tok + n, sec + s
+    value = tok / sec
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(cfg, desc, args), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{len(rows)} tokens of the workload per step through the fp64 "
+                                       f"oracle layer"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg, desc, args):
+    return {"workload": desc, "T": cfg.T, "d_model": cfg.d, "n_experts": cfg.N, "top_k": cfg.K,
+            "ffn": cfg.F, "n_shared": cfg.S, "shared_ffn": cfg.Fs, "score": cfg.score,
+            "hidden_dtype": cfg.hidden_dtype, "global_batch": cfg.T * args.gpus,
+            "parallelism": f"replicas x{args.gpus}",
+            "l2": "inputs larger than L2 (expert weights stream from HBM every step)"
+            if 3 * cfg.d * cfg.F * 2 * cfg.N > 126e6 else "L2 not flushed (working set fits in L2)"}
+
+
+def run_ours(args, cfg, desc, world, rank):
+    from mixture_experts_layer_94_b300 import binding as B
+
+    peaks, peak_src = load_peaks()
+    ins = inputs.make_inputs(cfg, seed=0, device="cuda")
+    if rank > 0:  # each replica its own batch
+        ins["hidden"] = inputs.make_router_inputs(cfg, seed=rank)["hidden"]
+    dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
+    layer = B.MoELayer(cfg, dev)
+    p = B.problem(cfg)
+    ws = layer.workspace(cfg.T)
+    hidden = dev["hidden"]
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    counts = torch.empty(cfg.N, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    nst = len(B.LAYER_STAGES)
+
+    layer.forward(hidden, out, counts=counts)
+    torch.cuda.synchronize()
+    st = B.get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after first step: {B.status_string(st)}")
+    counts_h = counts.cpu().numpy()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        B.layer_forward_profiled(p, layer.ws_struct, hidden, out, ws, ev[0], stream)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        B.layer_forward_profiled(p, layer.ws_struct, hidden, out, ws, ev[i], stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.monotonic()
+    sampler.stop()
+    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    st = B.get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {B.status_string(st)}")
+    stage_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j in range(nst)]
+
+    value = world * cfg.T * args.steps / elapsed_s
+    ms_step = 1e3 * elapsed_s / args.steps
+    wm = work_model(cfg, counts_h)
+    decode = cfg.T <= 512 and cfg.name == "qwen_decode"
+    gu, dn = B.LAYER_STAGES.index("gateup_swiglu_gemm"), B.LAYER_STAGES.index("down_scatter_gemm")
+    dom = gu if stage_ms[gu] >= stage_ms[dn] else dn
+    dom_name = B.LAYER_STAGES[dom]
+    long_region = elapsed_s >= 1.0
+    if decode:
+        bytes_ = wm["bytes_gateup"] if dom == gu else wm["bytes_down"]
+        achieved = bytes_ / (stage_ms[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "algorithmic_bytes_per_launch": bytes_}
+        t_roof = max(wm["flops"] / (peaks["bf16_tflops"] * 1e12), wm["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    else:
+        flops = wm["flops_gateup"] if dom == gu else wm["flops_down"]
+        achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
+        key = "bf16_tflops_sustained" if long_region and "bf16_tflops_sustained" in peaks else "bf16_tflops"
+        peak = peaks[key]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "algorithmic_flops_per_launch": flops}
+        t_roof = max(wm["flops"] / (peak * 1e12), wm["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    roof.update({"kernel": dom_name, "peak_source": f"{peak_src} ({'sustained' if (not decode and long_region) else 'burst'})",
+                 "traffic": traffic_from_profiles(dom_name, args.workload)})
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+            "config": config_block(cfg, desc, args), "roofline": roof,
+            "layer_roofline": {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],
+                               "t_roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step},
+            "stages_ms": dict(zip(B.LAYER_STAGES, stage_ms)),
+            "gpu_launches": B.layer_forward_kernel_count(p) * args.steps,
+            "clocks": sampler.summary(t_wall0, t_wall1)}
+
+    if not args.no_e2e:
+        hid_host = torch.empty(hidden.shape, dtype=hidden.dtype, pin_memory=True)
+        hid_host.copy_(hidden)
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        hid_dev = torch.empty_like(hidden)
+        for _ in range(max(3, args.warmup)):
+            hid_dev.copy_(hid_host, non_blocking=True)
+            layer.forward(hid_dev, out)
+            out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            hid_dev.copy_(hid_host, non_blocking=True)
+            layer.forward(hid_dev, out)
+            out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+        line["e2e"] = {"value": world * cfg.T * args.steps / e2e_s, "unit": "tokens/s",
+                       "h2d_bytes_per_step": hid_host.numel() * hid_host.element_size(),
+                       "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, ins, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    cfg, desc = WORKLOADS[args.workload]
+    world, rank, _ = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, cfg, desc, world, rank)
+    else:
+        run_ours(args, cfg, desc, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -32,6 +32,9 @@
  *     except moe_get_device_status.
  *   - Arguments are validated on the host before anything is enqueued; an
  *     invalid call returns an error status and enqueues nothing.
+ *   - A workspace's first 256 bytes hold the device error word: zero them
+ *     once before the workspace's first use (moe_get_device_status clears the
+ *     word after reading it).
  *   - Launch failures return MOE_ERR_CUDA. Faults the kernels detect on the
  *     device (an expert index out of range, a pipeline wait that ran out of
  *     time) are recorded in an error word inside the workspace and reported by
@@ -228,6 +231,28 @@ moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
                                int32_t* topk_idx_opt, float* topk_w_opt,
                                int32_t* counts_opt, void* ws, size_t ws_bytes,
                                void* stream);
+
+/*
+ * moe_layer_forward with stage timing: identical work and kernels, plus a
+ * cudaEventRecord on `stream` before the first kernel and after each stage.
+ *   stage_events  array of MOE_LAYER_STAGES cudaEvent_t (passed as void*),
+ *                 created by the caller; event i+1 minus event i is stage i:
+ *                 0 router+top-K, 1 route and pack, 2 GEMM schedule,
+ *                 3 gate/up GEMM + SwiGLU, 4 down GEMM + weighted scatter-add,
+ *                 5 fp32 -> bf16 finalise.
+ * Used by the benchmark to time each kernel inside the timed region.
+ */
+#define MOE_LAYER_STAGES 6
+moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weights_t* w,
+                                        const void* hidden, void* out, void* ws,
+                                        size_t ws_bytes, void* const* stage_events,
+                                        void* stream);
+
+/*
+ * Number of kernels one moe_layer_forward call launches for problem p (host
+ * only, no CUDA call); 0 if p is invalid.
+ */
+int32_t moe_layer_forward_kernel_count(const moe_problem_t* p);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word in `ws`

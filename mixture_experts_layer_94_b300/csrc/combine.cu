@@ -1,0 +1,89 @@
+// combine.cu — back to token order.
+//
+// finalize: out = bf16(out_acc), the last step of the fused layer whose
+//   down-projection epilogue already scatter-added w_{t,k} * y into out_acc.
+// combine:  the step-wise, deterministic gate-weighted sum ("Chapter 19:
+//   Mixture-of-Experts Models", §19.3.2 and the §19.2 flowchart "Sum with gate
+//   weights"): out[t] = bf16(sum_k w[t][k] * y_perm[inv_row[t*K+k]] + shared[t]),
+//   fp32 accumulation in slot order.
+// Both are HBM-bound streams: 16-byte vector loads and stores, one thread per
+// 8 output elements, grid-stride over the whole output.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc,
+                                                       __nv_bfloat16* __restrict__ out, int64_t nvec) {
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * v];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * v + 1];
+    reinterpret_cast<uint4*>(out)[v] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v, float w) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u[j]);
+    const float2 f = __bfloat1622float2(b);
+    acc[2 * j] = fmaf(w, f.x, acc[2 * j]);
+    acc[2 * j + 1] = fmaf(w, f.y, acc[2 * j + 1]);
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(int64_t T, int32_t K, int32_t d,
+                                                      const __nv_bfloat16* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ inv_row,
+                                                      const float* __restrict__ topk_w,
+                                                      const __nv_bfloat16* __restrict__ shared_out,
+                                                      __nv_bfloat16* __restrict__ out) {
+  const int64_t vpr = d / 8;  // 16-byte vectors per row
+  const int64_t total = T * vpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / vpr, v = i - t * vpr;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const int64_t r = __ldg(inv_row + t * K + k);
+      const float w = __ldg(topk_w + t * K + k);
+      add_bf16x8(acc, reinterpret_cast<const uint4*>(y_perm + r * d)[v], w);
+    }
+    if (shared_out) add_bf16x8(acc, reinterpret_cast<const uint4*>(shared_out + t * d)[v], 1.f);
+    reinterpret_cast<uint4*>(out + t * d)[v] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;
+  return (int)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, int64_t n, cudaStream_t s) {
+  const int64_t nvec = n / 8;
+  if (nvec == 0) return cudaSuccess;
+  finalize_kernel<<<grid_for(nvec, 256), 256, 0, s>>>(acc, out, nvec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int64_t T, int32_t K, int32_t d, const __nv_bfloat16* y_perm, const int32_t* inv_row,
+                           const float* topk_w, const __nv_bfloat16* shared_out, __nv_bfloat16* out,
+                           cudaStream_t s) {
+  const int64_t work = T * (d / 8);
+  if (work == 0) return cudaSuccess;
+  combine_kernel<<<grid_for(work, 256), 256, 0, s>>>(T, K, d, y_perm, inv_row, topk_w, shared_out, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,377 @@
+// grouped_gemm.cu — the expert FFNs as grouped GEMMs on the 5th-generation
+// tensor cores (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+//
+// What is computed (per group = one routed or shared expert, over its rows):
+//   gate/up phase:  g = X W_gate^T, u = X W_up^T, h = bf16(SiLU(g) * u)
+//   down phase:     y = h W_down^T, then either
+//                   out_acc[token] += w_{t,k} * y   (fused gate-weighted combine)
+//                   or y_perm = bf16(y)             (step-wise path)
+// The expert FFN is the SwiGLU reading of the three-matrix expert ("Mixture of
+// Experts Explained: Conditional Computation From Zero", "The slot it replaces,
+// and what an expert is"); the weighted sum back to token order is "Chapter 19:
+// Mixture-of-Experts Models", §19.3.2 and the §19.2 flowchart ("Sum with gate
+// weights"); the shared expert adds with weight 1 ("Mixture of Experts for LLM
+// Inference", "Shared experts").
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0     TMA producer: per K block, one 128x64 activation box and one
+//              256x64 weight box (gate rows | up rows, or 256 down rows), 128-byte
+//              swizzled, into a 4-stage shared-memory ring (48 KB per stage).
+//   warp 1     allocates 512 TMEM columns; one lane issues tcgen05.mma
+//              (M=128, N=256, K=16, bf16 -> fp32) into one of two 256-column
+//              accumulators and commits stage releases / tile completion to
+//              mbarriers.
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//              32*(w%4)..+31, one output row per thread), apply the fused
+//              SwiGLU or weighted scatter-add, release the accumulator.
+// The double-buffered accumulator lets the epilogue of tile i overlap the MMAs
+// of tile i+1. Tiles are (group, m block, n block), n-major inside a group so
+// CTAs running side by side share weight tiles in L2; a CTA walks tiles
+// blockIdx.x, +gridDim.x, ... and finds each tile's group by binary search over
+// the device-built prefix of tile counts (no host round trip).
+// Every mbarrier wait is bounded: on a stall the kernel records a timeout in
+// the workspace error word, drains its own copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
+constexpr uint32_t kStageB = 256 * kBK * 2;   // 32 KB
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 256);
+constexpr uint64_t kDrainTimeoutNs = 50000000ull;  // 50 ms per in-flight copy on abort
+
+constexpr size_t kBarrierBytes = 256;
+constexpr size_t kGemmSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + kBarrierBytes;
+
+struct TileInfo {
+  GroupDesc g;
+  int m_blk, n_blk;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int tile, const GemmArgs& a) {
+  int lo = 0, hi = a.G - 1;
+  while (lo < hi) {  // last group whose first tile is <= tile (skips empty groups)
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.tile_start + mid) <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.g = a.groups[lo];
+  const int local = tile - __ldg(a.tile_start + lo);
+  ti.n_blk = local / ti.g.m_tiles;
+  ti.m_blk = local - ti.n_blk * ti.g.m_tiles;
+  return ti;
+}
+
+__device__ __forceinline__ bool wait_raw(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+template <int PHASE, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmU1,
+                        const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_base);
+  const uint32_t sA = base;                              // kStages x 16 KB
+  const uint32_t sB = base + kStages * kStageA;          // kStages x 32 KB
+  const uint32_t sBar = base + kStages * kStageBytes;    // barriers
+  uint8_t* gBar = gbase + kStages * kStageBytes;
+  auto full_bar = [&](int s) { return sBar + 8u * s; };
+  auto empty_bar = [&](int s) { return sBar + 8u * (kStages + s); };
+  auto tfull_bar = [&](int i) { return sBar + 8u * (2 * kStages + i); };
+  auto tempty_bar = [&](int i) { return sBar + 8u * (2 * kStages + 2 + i); };
+  const uint32_t drain_bar = sBar + 8u * (2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 8 * (2 * kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * (2 * kStages + 5) + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = __ldg(a.tile_start + a.G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(tfull_bar(i), 1);
+      ptx::mbar_init(tempty_bar(i), 128);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+    ptx::fence_proxy_async_shared();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA0);
+    ptx::prefetch_tmap(&tmB0);
+    if (PHASE == kPhaseGateUp) ptx::prefetch_tmap(&tmU0);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, a);
+        const int kind = ti.g.kind;
+        const CUtensorMap* mA = kind ? &tmA1 : &tmA0;
+        const CUtensorMap* mB = kind ? &tmB1 : &tmB0;
+        const CUtensorMap* mU = kind ? &tmU1 : &tmU0;
+        const int a_row = (PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kBM;
+        const int b_row = ti.g.index * a.w_rows[kind] +
+                          ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
+        const int nkb = a.k_blocks[kind];
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) {
+            aborted = true;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+          ptx::tma_load_2d(sA + stage * kStageA, mA, full_bar(stage), kb * kBK, a_row);
+          if (PHASE == kPhaseGateUp) {
+            ptx::tma_load_2d(sB + stage * kStageB, mB, full_bar(stage), kb * kBK, b_row);
+            ptx::tma_load_2d(sB + stage * kStageB + kStageB / 2, mU, full_bar(stage), kb * kBK, b_row);
+          } else {
+            ptx::tma_load_2d(sB + stage * kStageB, mB, full_bar(stage), kb * kBK, b_row);
+          }
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        // Wait for this CTA's own copies still in flight (the last kStages issues).
+        const uint32_t n = issued < (uint32_t)kStages ? issued : (uint32_t)kStages;
+        for (uint32_t j = issued - n; j < issued; ++j)
+          wait_raw(full_bar(j % kStages), (j / kStages) & 1u, kDrainTimeoutNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, a);
+        const int nkb = a.k_blocks[ti.g.kind];
+        if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, a.err)) {
+            aborted = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t adesc = ptx::smem_desc_sw128(sA + stage * kStageA);
+          const uint64_t bdesc = ptx::smem_desc_sw128(sB + stage * kStageB);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        ptx::mma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      ptx::mma_commit(drain_bar);
+      wait_raw(drain_bar, 0, kWaitTimeoutNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, a);
+      const int kind = ti.g.kind;
+      if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
+      ptx::tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
+      const int r_local = ti.m_blk * kBM + row_in_tile;
+      const bool row_ok = r_local < ti.g.rows;
+      if (PHASE == kPhaseGateUp) {
+        const int n_ext = a.n_ext[kind];
+        const int col0 = ti.n_blk * kBNGateUp;
+        __nv_bfloat16* hrow = a.h[kind] + (int64_t)(ti.g.h_row0 + (row_ok ? r_local : 0)) * a.ldh[kind];
+#pragma unroll 1
+        for (int c = 0; c < kBNGateUp / 32; ++c) {
+          uint32_t gv[32], uv[32];
+          ptx::tmem_ld_32x32b_x32(tacc + c * 32, gv);
+          ptx::tmem_ld_32x32b_x32(tacc + kBNGateUp + c * 32, uv);
+          ptx::tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int f0 = col0 + c * 32 + v * 8;
+              if (f0 < n_ext) {
+                uint32_t p[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float g0 = __uint_as_float(gv[v * 8 + 2 * j]);
+                  const float g1 = __uint_as_float(gv[v * 8 + 2 * j + 1]);
+                  const float u0 = __uint_as_float(uv[v * 8 + 2 * j]);
+                  const float u1 = __uint_as_float(uv[v * 8 + 2 * j + 1]);
+                  p[j] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+                }
+                *reinterpret_cast<uint4*>(hrow + f0) = make_uint4(p[0], p[1], p[2], p[3]);
+              }
+            }
+          }
+        }
+      } else {
+        const int col0 = ti.n_blk * kBNDown;
+        int64_t t = 0;
+        float w = 1.f;
+        if (EPI == kEpiScatter && row_ok) {
+          if (kind == 0) {
+            const int32_t src = __ldg(a.perm_src + ti.g.h_row0 + r_local);
+            t = src / a.top_k;
+            w = __ldg(a.topk_w + src);
+          } else {
+            t = r_local;
+          }
+        }
+#pragma unroll 1
+        for (int c = 0; c < kBNDown / 32; ++c) {
+          uint32_t yv[32];
+          ptx::tmem_ld_32x32b_x32(tacc + c * 32, yv);
+          ptx::tmem_wait_ld();
+          if (row_ok) {
+            if (EPI == kEpiScatter) {
+              float* orow = a.out_acc + t * a.d;
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const int n0 = col0 + c * 32 + v * 4;
+                if (n0 < a.d) {
+                  float4 val = make_float4(w * __uint_as_float(yv[v * 4 + 0]), w * __uint_as_float(yv[v * 4 + 1]),
+                                           w * __uint_as_float(yv[v * 4 + 2]), w * __uint_as_float(yv[v * 4 + 3]));
+                  atomicAdd(reinterpret_cast<float4*>(orow + n0), val);
+                }
+              }
+            } else {
+              __nv_bfloat16* yrow = a.y + (int64_t)(ti.g.h_row0 + r_local) * a.d;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int n0 = col0 + c * 32 + v * 8;
+                if (n0 < a.d) {
+                  uint32_t p[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    p[j] = pack_bf16x2(__uint_as_float(yv[v * 8 + 2 * j]), __uint_as_float(yv[v * 8 + 2 * j + 1]));
+                  *reinterpret_cast<uint4*>(yrow + n0) = make_uint4(p[0], p[1], p[2], p[3]);
+                }
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int PHASE, int EPI>
+cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<PHASE, EPI>;
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  kern<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(m.a[0], m.a[1], m.b[0], m.b[1], m.bu[0], m.bu[1], a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T, int32_t F,
+                        int32_t Fs, int32_t d) {
+  // sum_e ceil(n_e / BM) <= routed_rows / BM + N
+  const int64_t m_routed = routed_rows / kBM + N;
+  const int64_t m_shared = (int64_t)S * ((T + kBM - 1) / kBM);
+  if (phase == kPhaseGateUp)
+    return m_routed * ((F + kBNGateUp - 1) / kBNGateUp) + m_shared * ((Fs + kBNGateUp - 1) / kBNGateUp);
+  return (m_routed + m_shared) * ((d + kBNDown - 1) / kBNDown);
+}
+
+cudaError_t launch_grouped_gemm(int phase, int epilogue, const GemmMaps& maps, const GemmArgs& a,
+                                int64_t tile_bound, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)(tile_bound < sms ? (tile_bound < 1 ? 1 : tile_bound) : sms);
+  if (phase == kPhaseGateUp) return launch_t<kPhaseGateUp, kEpiSwiGLU>(maps, a, grid, s);
+  if (epilogue == kEpiScatter) return launch_t<kPhaseDown, kEpiScatter>(maps, a, grid, s);
+  return launch_t<kPhaseDown, kEpiStoreY>(maps, a, grid, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,92 @@
+// kernels.h — host-side launch functions of libmoe's kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RouterArgs {
+  int64_t T;
+  int32_t d, N, K, score_fn, renormalize;
+  const void* hidden;  // [T][d] fp32 or bf16
+  const float* w_router;
+  const float* router_bias;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* logits;
+};
+cudaError_t launch_router(const RouterArgs& a, bool hidden_bf16, cudaStream_t s);
+
+struct PermuteArgs {
+  int64_t T;
+  int32_t d, N, K, C;  // C = number of 32-token chunks
+  const int32_t* topk_idx;
+  const void* hidden;
+  bool hidden_bf16;
+  int32_t* chunk_counts;  // [N][C] scratch; holds per-chunk bases after the scan
+  int32_t* counts;        // [N]
+  int32_t* offsets;       // [N+1]
+  int32_t* perm_src;      // [T*K]
+  int32_t* inv_row;       // [T*K]
+  __nv_bfloat16* x_perm;  // [T*K][d]
+  float* zero_rows;       // [T][d] fp32 to clear, or nullptr
+  __nv_bfloat16* x_bf16;  // [T][d] bf16 copy of hidden, or nullptr
+  uint32_t* err;
+};
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
+
+struct ScheduleArgs {
+  int32_t N, S, F, Fs, d;
+  int64_t T;
+  const int32_t* offsets;  // [N+1]
+  GroupDesc* groups;       // [N+S]
+  int32_t* tile_start_gu;  // [N+S+1]
+  int32_t* tile_start_dn;  // [N+S+1]
+};
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s);
+
+enum GemmPhase { kPhaseGateUp = 0, kPhaseDown = 1 };
+enum GemmEpilogue { kEpiSwiGLU = 0, kEpiScatter = 1, kEpiStoreY = 2 };
+
+struct GemmArgs {
+  const GroupDesc* groups;
+  const int32_t* tile_start;  // [G+1]
+  int32_t G;
+  int32_t n_ext[2];      // output columns of a group, per kind (gate/up: F, Fs; down: d)
+  int32_t n_tiles[2];    // output column tiles of a group, per kind
+  int32_t k_blocks[2];   // kBK-wide K blocks, per kind
+  int32_t w_rows[2];     // rows one group occupies in its stacked weight matrix, per kind
+  __nv_bfloat16* h[2];   // SwiGLU epilogue output, per kind
+  int64_t ldh[2];
+  float* out_acc;        // scatter epilogue: fp32 [T][d]
+  const int32_t* perm_src;
+  const float* topk_w;
+  int32_t top_k;
+  __nv_bfloat16* y;      // store epilogue: bf16 [rows][d]
+  int32_t d;
+  uint32_t* err;
+};
+
+struct GemmMaps {
+  CUtensorMap a[2];   // activations per kind
+  CUtensorMap b[2];   // weights per kind (gate for the gate/up phase)
+  CUtensorMap bu[2];  // up weights per kind (gate/up phase only)
+};
+
+// Upper bound on the tile count (host, from sizes only), used for the grid.
+int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T,
+                        int32_t F, int32_t Fs, int32_t d);
+cudaError_t launch_grouped_gemm(int phase, int epilogue, const GemmMaps& maps, const GemmArgs& a,
+                                int64_t tile_bound, cudaStream_t s);
+
+cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, int64_t n, cudaStream_t s);
+cudaError_t launch_combine(int64_t T, int32_t K, int32_t d, const __nv_bfloat16* y_perm,
+                           const int32_t* inv_row, const float* topk_w,
+                           const __nv_bfloat16* shared_out, __nv_bfloat16* out, cudaStream_t s);
+
+}  // namespace moe

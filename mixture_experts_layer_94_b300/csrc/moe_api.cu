@@ -1,0 +1,491 @@
+// moe_api.cu — the C ABI (include/moe.h): argument validation, workspace
+// layout, TMA tensor maps and the launch sequence of each entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int64_t kInt32Max = 2147483647;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t err, chunk, groups, ts_gu, ts_dn;
+  size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_bf16, h, h_sh, out_acc;
+  size_t total;
+};
+
+Layout make_layout(const moe_problem_t& p, int call) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const int64_t T = p.T, TK = p.T * p.top_k;
+  const int64_t C = (T + kTokensPerChunk - 1) / kTokensPerChunk;
+  const int G = p.n_experts + p.n_shared;
+  L.err = take(256);
+  L.chunk = take((size_t)p.n_experts * C * 4);
+  L.groups = take((size_t)G * sizeof(GroupDesc));
+  L.ts_gu = take((size_t)(G + 1) * 4);
+  L.ts_dn = take((size_t)(G + 1) * 4);
+  if (call == MOE_CALL_LAYER_FORWARD) {
+    L.topk_idx = take((size_t)TK * 4);
+    L.topk_w = take((size_t)TK * 4);
+    L.counts = take((size_t)p.n_experts * 4);
+    L.offsets = take((size_t)(p.n_experts + 1) * 4);
+    L.perm_src = take((size_t)TK * 4);
+    L.inv_row = take((size_t)TK * 4);
+    L.x_perm = take((size_t)TK * p.d_model * 2);
+    if (p.n_shared > 0 && p.hidden_dtype == MOE_F32) L.x_bf16 = take((size_t)T * p.d_model * 2);
+    L.h = take((size_t)TK * p.ffn * 2);
+    if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
+    L.out_acc = take((size_t)T * p.d_model * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool have_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 matrix [rows][inner] (row stride = inner elements), box [box_rows][64],
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                          \
+  do {                                         \
+    const moe_status_t _st = (expr);           \
+    if (_st != MOE_OK) return _st;             \
+  } while (0)
+#define MOE_TRY_CUDA(expr)                     \
+  do {                                         \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+moe_status_t check_ws(const moe_problem_t* p, int call, void* ws, size_t ws_bytes, Layout* L) {
+  *L = make_layout(*p, call);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// The two GEMM phases over groups already described in the workspace.
+struct GemmPlan {
+  int32_t N, S, F, Fs, d, K;
+  int64_t T, routed_rows;
+  const void* x_routed;   // [routed_rows][d] bf16
+  const void* x_shared;   // [T][d] bf16 (S > 0)
+  const void* wg;         // [N][F][d]
+  const void* wu;
+  const void* wd;         // [N][d][F]
+  const void* sg;         // [S][Fs][d]
+  const void* su;
+  const void* sd;         // [S][d][Fs]
+  __nv_bfloat16* h;       // [routed_rows][F]
+  __nv_bfloat16* h_sh;    // [S*T][Fs]
+  int epilogue;           // kEpiScatter or kEpiStoreY
+  float* out_acc;
+  const int32_t* perm_src;
+  const float* topk_w;
+  __nv_bfloat16* y;
+  const GroupDesc* groups;
+  const int32_t* ts_gu;
+  const int32_t* ts_dn;
+  uint32_t* err;
+};
+
+moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup = nullptr) {
+  if (!have_encode()) return MOE_ERR_CUDA;
+  const bool sh = g.S > 0;
+  GemmMaps m{};
+  bool ok = make_map(&m.a[0], g.x_routed, g.d, g.routed_rows, kBM) &&
+            make_map(&m.b[0], g.wg, g.d, (uint64_t)g.N * g.F, kBNGateUp) &&
+            make_map(&m.bu[0], g.wu, g.d, (uint64_t)g.N * g.F, kBNGateUp);
+  if (ok && sh)
+    ok = make_map(&m.a[1], g.x_shared, g.d, g.T, kBM) &&
+         make_map(&m.b[1], g.sg, g.d, (uint64_t)g.S * g.Fs, kBNGateUp) &&
+         make_map(&m.bu[1], g.su, g.d, (uint64_t)g.S * g.Fs, kBNGateUp);
+  if (!ok) return MOE_ERR_CUDA;
+  if (!sh) {
+    m.a[1] = m.a[0];
+    m.b[1] = m.b[0];
+    m.bu[1] = m.bu[0];
+  }
+  GemmArgs a{};
+  a.groups = g.groups;
+  a.G = g.N + g.S;
+  a.err = g.err;
+  a.d = g.d;
+  a.top_k = g.K;
+
+  // gate/up + SwiGLU
+  a.tile_start = g.ts_gu;
+  a.n_ext[0] = g.F;
+  a.n_ext[1] = sh ? g.Fs : g.F;
+  a.k_blocks[0] = a.k_blocks[1] = (g.d + kBK - 1) / kBK;
+  a.w_rows[0] = g.F;
+  a.w_rows[1] = sh ? g.Fs : g.F;
+  a.h[0] = g.h;
+  a.h[1] = sh ? g.h_sh : g.h;
+  a.ldh[0] = g.F;
+  a.ldh[1] = sh ? g.Fs : g.F;
+  int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d);
+  MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseGateUp, kEpiSwiGLU, m, a, bound, s)));
+  if (ev_after_gateup) MOE_TRY(cuda_status(cudaEventRecord(ev_after_gateup[0], s)));
+
+  // down (+ weighted scatter-add or plain store)
+  GemmMaps md{};
+  ok = make_map(&md.a[0], g.h, g.F, g.routed_rows, kBM) &&
+       make_map(&md.b[0], g.wd, g.F, (uint64_t)g.N * g.d, kBNDown);
+  if (ok && sh)
+    ok = make_map(&md.a[1], g.h_sh, g.Fs, (uint64_t)g.S * g.T, kBM) &&
+         make_map(&md.b[1], g.sd, g.Fs, (uint64_t)g.S * g.d, kBNDown);
+  if (!ok) return MOE_ERR_CUDA;
+  if (!sh) {
+    md.a[1] = md.a[0];
+    md.b[1] = md.b[0];
+  }
+  md.bu[0] = md.b[0];
+  md.bu[1] = md.b[1];
+  a.tile_start = g.ts_dn;
+  a.n_ext[0] = a.n_ext[1] = g.d;
+  a.k_blocks[0] = (g.F + kBK - 1) / kBK;
+  a.k_blocks[1] = sh ? (g.Fs + kBK - 1) / kBK : a.k_blocks[0];
+  a.w_rows[0] = a.w_rows[1] = g.d;
+  a.out_acc = g.out_acc;
+  a.perm_src = g.perm_src;
+  a.topk_w = g.topk_w;
+  a.y = g.y;
+  bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d);
+  MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseDown, g.epilogue, md, a, bound, s)));
+  if (ev_after_gateup) MOE_TRY(cuda_status(cudaEventRecord(ev_after_gateup[1], s)));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: problem not supported by this build";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device pipeline wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS: an input index was out of range";
+    default: return "MOE_ERR_UNKNOWN: unrecognised status";
+  }
+}
+
+moe_status_t moe_problem_check(const moe_problem_t* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->d_model <= 0 || (p->d_model % 8) != 0) return MOE_ERR_INVALID_ARG;
+  if (p->n_experts < 1 || p->top_k < 1 || p->top_k > p->n_experts) return MOE_ERR_INVALID_ARG;
+  if (p->ffn <= 0 || (p->ffn % 8) != 0) return MOE_ERR_INVALID_ARG;
+  if (p->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (p->n_shared > 0 && (p->shared_ffn <= 0 || (p->shared_ffn % 8) != 0)) return MOE_ERR_INVALID_ARG;
+  if (p->score_fn != MOE_SCORE_SOFTMAX && p->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (p->renormalize != 0 && p->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (p->hidden_dtype != MOE_F32 && p->hidden_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (p->n_experts > kMaxExperts || p->top_k > kMaxTopK || p->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
+  if (p->T * p->top_k > kInt32Max || p->T * (p->n_shared > 0 ? p->n_shared : 1) > kInt32Max)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_problem_t* p, int32_t call) {
+  if (moe_problem_check(p) != MOE_OK) return 0;
+  if (call != MOE_CALL_PERMUTE && call != MOE_CALL_GROUPED_SWIGLU && call != MOE_CALL_LAYER_FORWARD) return 0;
+  return make_layout(*p, call).total;
+}
+
+moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const float* w_router,
+                             const float* router_bias, const float* sel_bias, int32_t* topk_idx, float* topk_w,
+                             float* logits_opt, void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (p->T == 0) return MOE_OK;
+  if (!hidden || !w_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (sel_bias && p->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_UNSUPPORTED;
+  RouterArgs a{p->T, p->d_model, p->n_experts, p->top_k, p->score_fn, p->renormalize,
+               hidden, w_router, router_bias, sel_bias, topk_idx, topk_w, logits_opt};
+  return cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx, const void* hidden, int32_t* counts,
+                         int32_t* offsets, int32_t* perm_src, int32_t* inv_row, void* x_perm, void* ws,
+                         size_t ws_bytes, void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!topk_idx || !hidden || !perm_src || !inv_row || !x_perm)) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!aligned16(hidden) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  MOE_TRY(check_ws(p, MOE_CALL_PERMUTE, ws, ws_bytes, &L));
+  PermuteArgs a{};
+  a.T = p->T;
+  a.d = p->d_model;
+  a.N = p->n_experts;
+  a.K = p->top_k;
+  a.C = (int32_t)((p->T + kTokensPerChunk - 1) / kTokensPerChunk);
+  a.topk_idx = topk_idx;
+  a.hidden = hidden;
+  a.hidden_bf16 = p->hidden_dtype == MOE_BF16;
+  a.chunk_counts = at<int32_t>(ws, L.chunk);
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm_src = perm_src;
+  a.inv_row = inv_row;
+  a.x_perm = static_cast<__nv_bfloat16*>(x_perm);
+  a.err = at<uint32_t>(ws, L.err);
+  return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
+                                const void* w_gate, const void* w_up, const void* w_down, void* h_perm,
+                                void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (!offsets || !w_gate || !w_up || !w_down) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down)) return MOE_ERR_INVALID_ARG;
+  const int64_t rows = p->T * p->top_k;
+  if (rows > 0 && (!x_perm || !h_perm || !y_perm)) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!aligned16(x_perm) || !aligned16(h_perm) || !aligned16(y_perm))) return MOE_ERR_INVALID_ARG;
+  moe_problem_t q = *p;
+  q.n_shared = 0;
+  Layout L;
+  MOE_TRY(check_ws(&q, MOE_CALL_GROUPED_SWIGLU, ws, ws_bytes, &L));
+  if (rows == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ScheduleArgs sa{q.n_experts, 0, q.ffn, 0, q.d_model, q.T, offsets, at<GroupDesc>(ws, L.groups),
+                  at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
+  MOE_TRY(cuda_status(launch_schedule(sa, s)));
+  GemmPlan g{};
+  g.N = q.n_experts;
+  g.S = 0;
+  g.F = q.ffn;
+  g.Fs = 0;
+  g.d = q.d_model;
+  g.K = q.top_k;
+  g.T = q.T;
+  g.routed_rows = rows;
+  g.x_routed = x_perm;
+  g.wg = w_gate;
+  g.wu = w_up;
+  g.wd = w_down;
+  g.h = static_cast<__nv_bfloat16*>(h_perm);
+  g.epilogue = kEpiStoreY;
+  g.y = static_cast<__nv_bfloat16*>(y_perm);
+  g.groups = at<GroupDesc>(ws, L.groups);
+  g.ts_gu = at<int32_t>(ws, L.ts_gu);
+  g.ts_dn = at<int32_t>(ws, L.ts_dn);
+  g.err = at<uint32_t>(ws, L.err);
+  return run_gemms(g, s);
+}
+
+moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm, const int32_t* inv_row, const float* topk_w,
+                         const void* shared_out, void* out, void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (p->T == 0) return MOE_OK;
+  if (!y_perm || !inv_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(p->T, p->top_k, p->d_model, static_cast<const __nv_bfloat16*>(y_perm),
+                                    inv_row, topk_w, static_cast<const __nv_bfloat16*>(shared_out),
+                                    static_cast<__nv_bfloat16*>(out), static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+moe_status_t record(cudaEvent_t* ev, int i, cudaStream_t s) {
+  if (!ev) return MOE_OK;
+  return cuda_status(cudaEventRecord(ev[i], s));
+}
+
+moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, const void* hidden, void* out,
+                                int32_t* topk_idx_opt, float* topk_w_opt, int32_t* counts_opt, void* ws,
+                                size_t ws_bytes, cudaEvent_t* ev, void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (!w || !w->w_router || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (p->n_shared > 0 && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
+  if (w->sel_bias && p->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(w->w_gate) || !aligned16(w->w_up) || !aligned16(w->w_down)) return MOE_ERR_INVALID_ARG;
+  if (p->n_shared > 0 && (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  MOE_TRY(check_ws(p, MOE_CALL_LAYER_FORWARD, ws, ws_bytes, &L));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t T = p->T;
+  const int32_t N = p->n_experts, K = p->top_k, S = p->n_shared;
+  int32_t* topk_idx = topk_idx_opt ? topk_idx_opt : at<int32_t>(ws, L.topk_idx);
+  float* topk_w = topk_w_opt ? topk_w_opt : at<float>(ws, L.topk_w);
+  int32_t* counts = counts_opt ? counts_opt : at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  const bool hbf16 = p->hidden_dtype == MOE_BF16;
+
+  if (T == 0) {  // no tokens: counts are all zero
+    PermuteArgs pa{};
+    pa.N = N;
+    pa.K = K;
+    pa.chunk_counts = at<int32_t>(ws, L.chunk);
+    pa.counts = counts;
+    pa.offsets = offsets;
+    pa.err = err;
+    return cuda_status(launch_permute(pa, s));
+  }
+
+  // 1. router, scoring, top-K, gate weights
+  MOE_TRY(record(ev, 0, s));
+  RouterArgs ra{T, p->d_model, N, K, p->score_fn, p->renormalize, hidden, w->w_router,
+                w->router_bias, w->sel_bias, topk_idx, topk_w, nullptr};
+  MOE_TRY(cuda_status(launch_router(ra, hbf16, s)));
+  MOE_TRY(record(ev, 1, s));
+
+  // 2. route and pack (+ clear the fp32 accumulator, + bf16 copy of an fp32 hidden for shared experts)
+  PermuteArgs pa{};
+  pa.T = T;
+  pa.d = p->d_model;
+  pa.N = N;
+  pa.K = K;
+  pa.C = (int32_t)((T + kTokensPerChunk - 1) / kTokensPerChunk);
+  pa.topk_idx = topk_idx;
+  pa.hidden = hidden;
+  pa.hidden_bf16 = hbf16;
+  pa.chunk_counts = at<int32_t>(ws, L.chunk);
+  pa.counts = counts;
+  pa.offsets = offsets;
+  pa.perm_src = at<int32_t>(ws, L.perm_src);
+  pa.inv_row = at<int32_t>(ws, L.inv_row);
+  pa.x_perm = at<__nv_bfloat16>(ws, L.x_perm);
+  pa.zero_rows = at<float>(ws, L.out_acc);
+  pa.x_bf16 = (S > 0 && !hbf16) ? at<__nv_bfloat16>(ws, L.x_bf16) : nullptr;
+  pa.err = err;
+  MOE_TRY(cuda_status(launch_permute(pa, s)));
+  MOE_TRY(record(ev, 2, s));
+
+  // 3. GEMM schedule: routed experts from offsets, then the shared experts
+  ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, T, offsets, at<GroupDesc>(ws, L.groups),
+                  at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
+  MOE_TRY(cuda_status(launch_schedule(sa, s)));
+  MOE_TRY(record(ev, 3, s));
+
+  // 4-5. grouped SwiGLU GEMMs with the fused weighted scatter-add
+  GemmPlan g{};
+  g.N = N;
+  g.S = S;
+  g.F = p->ffn;
+  g.Fs = p->shared_ffn;
+  g.d = p->d_model;
+  g.K = K;
+  g.T = T;
+  g.routed_rows = T * K;
+  g.x_routed = pa.x_perm;
+  g.x_shared = hbf16 ? hidden : pa.x_bf16;
+  g.wg = w->w_gate;
+  g.wu = w->w_up;
+  g.wd = w->w_down;
+  g.sg = w->ws_gate;
+  g.su = w->ws_up;
+  g.sd = w->ws_down;
+  g.h = at<__nv_bfloat16>(ws, L.h);
+  g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
+  g.epilogue = kEpiScatter;
+  g.out_acc = at<float>(ws, L.out_acc);
+  g.perm_src = pa.perm_src;
+  g.topk_w = topk_w;
+  g.groups = at<GroupDesc>(ws, L.groups);
+  g.ts_gu = at<int32_t>(ws, L.ts_gu);
+  g.ts_dn = at<int32_t>(ws, L.ts_dn);
+  g.err = err;
+  MOE_TRY(run_gemms(g, s, ev ? ev + 4 : nullptr));
+
+  // 6. fp32 -> bf16
+  MOE_TRY(cuda_status(launch_finalize(g.out_acc, static_cast<__nv_bfloat16*>(out), T * p->d_model, s)));
+  return record(ev, 6, s);
+}
+
+}  // namespace
+
+moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w, const void* hidden, void* out,
+                               int32_t* topk_idx_opt, float* topk_w_opt, int32_t* counts_opt, void* ws,
+                               size_t ws_bytes, void* stream) {
+  return layer_forward_impl(p, w, hidden, out, topk_idx_opt, topk_w_opt, counts_opt, ws, ws_bytes, nullptr,
+                            stream);
+}
+
+moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weights_t* w, const void* hidden,
+                                        void* out, void* ws, size_t ws_bytes, void* const* stage_events,
+                                        void* stream) {
+  if (!stage_events) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[MOE_LAYER_STAGES + 1];
+  for (int i = 0; i <= MOE_LAYER_STAGES; ++i) {
+    if (!stage_events[i]) return MOE_ERR_INVALID_ARG;
+    ev[i] = static_cast<cudaEvent_t>(stage_events[i]);
+  }
+  return layer_forward_impl(p, w, hidden, out, nullptr, nullptr, nullptr, ws, ws_bytes, ev, stream);
+}
+
+int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
+  if (moe_problem_check(p) != MOE_OK) return 0;
+  if (p->T == 0) return 1;  // the histogram scan that writes zero counts
+  // router, histogram, scan, scatter+gather, schedule, gate/up GEMM, down GEMM, finalise
+  return 8;
+}
+
+moe_status_t moe_get_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof word, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kErrBounds) return MOE_ERR_DEVICE_BOUNDS;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,263 @@
+// permute.cu — route and pack: per-expert histogram, prefix sum and a stable
+// expert-major permutation of the T*K token copies, plus the row gather.
+//
+// "Chapter 19: Mixture-of-Experts Models", §19.6.3 "How expert parallelism
+// dispatches tokens": token hidden states are routed and packed so that each
+// expert receives its tokens as one contiguous batch ("Route and pack"), and
+// results are later returned to the original tokens.
+//
+// Design (deterministic, no ordering races): tokens are cut into 32-token
+// chunks, one warp per chunk, one token per lane. For every expert a warp
+// builds a 32-bit lane mask in shared memory (atomicOr: order-independent);
+// popc(mask) is the chunk's count, popc(mask & lanes_below) a copy's rank
+// inside the chunk. One CTA scans counts over chunks and experts, giving each
+// (expert, chunk) its first output row. A copy's row is then
+//   offsets[e] + rows of e in earlier chunks + rank in its chunk,
+// i.e. expert ascending, token ascending: the same order as a stable sort.
+// The gather moves each hidden row to its permuted rows with 16-byte vectors.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kHistWarps = 8;
+
+__device__ __forceinline__ void build_chunk_masks(uint32_t* masks, const int32_t* __restrict__ idx,
+                                                  int64_t T, int K, int N, int64_t chunk, int lane,
+                                                  uint32_t* err) {
+  for (int e = lane; e < N; e += 32) masks[e] = 0u;
+  __syncwarp();
+  const int64_t t = chunk * kTokensPerChunk + lane;
+  if (t < T) {
+    for (int k = 0; k < K; ++k) {
+      const int e = idx[t * K + k];
+      if (e < 0 || e >= N) {
+        atomicOr(err, kErrBounds);
+      } else {
+        atomicOr(&masks[e], 1u << lane);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kHistWarps * 32) route_hist_kernel(const PermuteArgs a) {
+  __shared__ uint32_t masks[kHistWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c = (int64_t)blockIdx.x * kHistWarps + warp;
+  if (c >= a.C) return;  // whole warp
+  build_chunk_masks(masks[warp], a.topk_idx, a.T, a.K, a.N, c, lane, a.err);
+  for (int e = lane; e < a.N; e += 32) a.chunk_counts[(int64_t)e * a.C + c] = __popc(masks[warp][e]);
+}
+
+// One CTA: counts[e] = sum over chunks, offsets = exclusive scan over experts,
+// chunk_counts[e][c] <- offsets[e] + sum_{c' < c} chunk_counts[e][c'].
+__global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
+  __shared__ int32_t s_counts[kMaxExperts];
+  __shared__ int32_t s_offsets[kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int N = a.N;
+  const int64_t C = a.C;
+  for (int e = warp; e < N; e += nwarps) {
+    const int32_t* row = a.chunk_counts + (int64_t)e * C;
+    int32_t s = 0;
+    for (int64_t c = lane; c < C; c += 32) s += row[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) s_counts[e] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of N <= 256 counts, 8 per lane
+    int32_t v[kMaxExperts / 32];
+    int32_t local = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane * (kMaxExperts / 32) + i;
+      v[i] = (e < N) ? s_counts[e] : 0;
+      local += v[i];
+    }
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int32_t run = incl - local;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane * (kMaxExperts / 32) + i;
+      if (e < N) s_offsets[e] = run;
+      run += v[i];
+    }
+    if (lane == 31) s_offsets[N] = incl;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= N; e += blockDim.x) {
+    a.offsets[e] = s_offsets[e];
+    if (e < N && a.counts) a.counts[e] = s_counts[e];
+  }
+  for (int e = warp; e < N; e += nwarps) {
+    int32_t* row = a.chunk_counts + (int64_t)e * C;
+    int32_t run = s_offsets[e];
+    for (int64_t c0 = 0; c0 < C; c0 += 32) {
+      const int64_t c = c0 + lane;
+      const int32_t v = (c < C) ? row[c] : 0;
+      int32_t incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < C) row[c] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+}
+
+constexpr int kGatherWarps = 8;
+
+// One CTA per chunk: warp 0 places the chunk's copies; then all warps copy rows.
+__global__ void __launch_bounds__(kGatherWarps * 32) route_scatter_gather_kernel(const PermuteArgs a) {
+  __shared__ uint32_t masks[kMaxExperts];
+  __shared__ int32_t rows[kTokensPerChunk * kMaxTopK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c = blockIdx.x;
+  const int K = a.K, N = a.N, d = a.d;
+  const int64_t t0 = c * kTokensPerChunk;
+  const int ntok = (int)min((int64_t)kTokensPerChunk, a.T - t0);
+  if (warp == 0) {
+    build_chunk_masks(masks, a.topk_idx, a.T, K, N, c, lane, a.err);
+    if (lane < ntok) {
+      const int64_t t = t0 + lane;
+      const uint32_t below = (1u << lane) - 1u;
+      for (int k = 0; k < K; ++k) {
+        const int e = a.topk_idx[t * K + k];
+        int32_t r = -1;
+        if (e >= 0 && e < N) {
+          r = a.chunk_counts[(int64_t)e * a.C + c] + __popc(masks[e] & below);
+          a.perm_src[r] = (int32_t)(t * K + k);
+          a.inv_row[t * K + k] = r;
+        }
+        rows[lane * K + k] = r;
+      }
+    }
+  }
+  __syncthreads();
+  // Row copies: hidden[t] -> x_perm[r] (bf16), 8 elements (16 B of output) per lane step.
+  const int nvec = d / 8;
+  for (int q = warp; q < ntok * K; q += kGatherWarps) {
+    const int r = rows[q];
+    if (r < 0) continue;
+    const int64_t t = t0 + q / K;
+    uint4* dst = reinterpret_cast<uint4*>(a.x_perm + (int64_t)r * d);
+    if (a.hidden_bf16) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * d);
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * d);
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        const float4 p = src[2 * v], q2 = src[2 * v + 1];
+        uint4 o;
+        o.x = pack_bf16x2(p.x, p.y);
+        o.y = pack_bf16x2(p.z, p.w);
+        o.z = pack_bf16x2(q2.x, q2.y);
+        o.w = pack_bf16x2(q2.z, q2.w);
+        dst[v] = o;
+      }
+    }
+  }
+  // Optional per-token work of the fused layer: clear the fp32 accumulator rows
+  // and write a bf16 copy of an fp32 hidden row (the shared experts' operand).
+  if (a.zero_rows || a.x_bf16) {
+    for (int tk = warp; tk < ntok; tk += kGatherWarps) {
+      const int64_t t = t0 + tk;
+      if (a.zero_rows) {
+        float4* z = reinterpret_cast<float4*>(a.zero_rows + t * d);
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int v = lane; v < d / 4; v += 32) z[v] = zero;
+      }
+      if (a.x_bf16) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * d);
+        uint4* dst = reinterpret_cast<uint4*>(a.x_bf16 + t * d);
+        for (int v = lane; v < nvec; v += 32) {
+          const float4 p = src[2 * v], q2 = src[2 * v + 1];
+          uint4 o;
+          o.x = pack_bf16x2(p.x, p.y);
+          o.y = pack_bf16x2(p.z, p.w);
+          o.z = pack_bf16x2(q2.x, q2.y);
+          o.w = pack_bf16x2(q2.z, q2.w);
+          dst[v] = o;
+        }
+      }
+    }
+  }
+}
+
+// One CTA: the GEMM groups (routed experts from offsets, then shared experts
+// over all T tokens) and the exclusive prefix of their tile counts per phase.
+__global__ void __launch_bounds__(512) schedule_kernel(const ScheduleArgs a) {
+  __shared__ int32_t s_gu[kMaxExperts + kMaxShared + 1];
+  __shared__ int32_t s_dn[kMaxExperts + kMaxShared + 1];
+  const int G = a.N + a.S;
+  const int nt_dn = (a.d + kBNDown - 1) / kBNDown;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    GroupDesc gd;
+    int F;
+    if (g < a.N) {
+      gd.kind = 0;
+      gd.index = g;
+      gd.a_row0 = a.offsets[g];
+      gd.rows = a.offsets[g + 1] - a.offsets[g];
+      gd.h_row0 = gd.a_row0;
+      F = a.F;
+    } else {
+      gd.kind = 1;
+      gd.index = g - a.N;
+      gd.a_row0 = 0;
+      gd.rows = (int32_t)a.T;
+      gd.h_row0 = (int32_t)((int64_t)gd.index * a.T);
+      F = a.Fs;
+    }
+    gd.m_tiles = (gd.rows + kBM - 1) / kBM;
+    gd.pad0 = gd.pad1 = 0;
+    a.groups[g] = gd;
+    s_gu[g] = gd.m_tiles * ((F + kBNGateUp - 1) / kBNGateUp);
+    s_dn[g] = gd.m_tiles * nt_dn;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t run_gu = 0, run_dn = 0;
+    for (int g = 0; g < G; ++g) {
+      const int32_t gu = s_gu[g], dn = s_dn[g];
+      a.tile_start_gu[g] = run_gu;
+      a.tile_start_dn[g] = run_dn;
+      run_gu += gu;
+      run_dn += dn;
+    }
+    a.tile_start_gu[G] = run_gu;
+    a.tile_start_dn[G] = run_dn;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
+  if (a.C == 0) {  // T == 0: empty histogram, offsets all zero
+    route_scan_kernel<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  route_hist_kernel<<<(unsigned)((a.C + kHistWarps - 1) / kHistWarps), kHistWarps * 32, 0, s>>>(a);
+  route_scan_kernel<<<1, 1024, 0, s>>>(a);
+  route_scatter_gather_kernel<<<(unsigned)a.C, kGatherWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
+  schedule_kernel<<<1, 512, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -137,8 +137,9 @@ def permute(topk_idx, N):
     return dict(counts=counts, offsets=offsets, perm_src=perm_src, inv_row=inv_row)
 
 
-def expert_ffn(x, w_gate, w_up, w_down):
-    """One SwiGLU expert on one token: x fp64 [d], weights bf16 bit patterns."""
+def expert_ffn(x, w_gate, w_up, w_down, return_h=False):
+    """One SwiGLU expert on one token: x fp64 [d], weights bf16 bit patterns.
+    Returns y (fp64 [d]), or (h, y) with the fp64 hidden activation h [F]."""
     lib = _load()
     x = _f64(x)
     wg, wu, wd = _bf16_bits(w_gate), _bf16_bits(w_up), _bf16_bits(w_down)
@@ -147,7 +148,7 @@ def expert_ffn(x, w_gate, w_up, w_down):
     h = np.empty((F,), np.float64)
     y = np.empty((d,), np.float64)
     lib.moe_oracle_expert_ffn(d, F, _ptr(x), _ptr(wg), _ptr(wu), _ptr(wd), _ptr(h), _ptr(y))
-    return y
+    return (h, y) if return_h else y
 
 
 def combine(w, y, shared=None):

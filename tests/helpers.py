@@ -1,0 +1,103 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI,
+run the oracle on the same inputs, and apply the acceptance bar.
+
+Acceptance (fixed for this layer):
+  * expert indices, per-expert counts and the permutation bit-exact; tokens
+    whose oracle top-K margin is below 1e-5 are counted and reported apart;
+  * gate weights within 1e-5 absolute (fp32 router);
+  * layer outputs (bf16, fp32 accumulation): max|gpu - ref| <= 2e-2 * max|ref|
+    and sum|gpu - ref| / sum|ref| <= 5e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from mixture_experts_layer_94_b300 import inputs
+from oracle import oracle
+
+MARGIN_TIE = 1e-5
+W_ATOL = 1e-5
+MAX_REL = 2e-2
+L1_REL = 5e-3
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def hidden_f32(ins) -> np.ndarray:
+    return ins["hidden"].float().cpu().numpy()
+
+
+def np32(t):
+    return None if t is None else t.detach().cpu().float().numpy()
+
+
+def oracle_router(cfg, ins, rows=None):
+    x = hidden_f32(ins)
+    if rows is not None:
+        x = x[rows]
+    return oracle.router(x, np32(ins["w_router"]), K=cfg.K, score_fn=cfg.score_fn,
+                         renormalize=cfg.renormalize, router_bias=np32(ins.get("router_bias")),
+                         sel_bias=np32(ins.get("sel_bias")))
+
+
+def oracle_layer_rows(cfg, ins, rows):
+    """Oracle layer output for the given token rows. Only the experts those
+    tokens pick are copied to the host."""
+    rows = np.asarray(rows, dtype=np.int64)
+    r = oracle_router(cfg, ins, rows)
+    used = sorted(set(r["idx"].reshape(-1).tolist()))
+    wg = [None] * cfg.N
+    wu = [None] * cfg.N
+    wd = [None] * cfg.N
+    for e in used:
+        wg[e] = bf16_bits(ins["w_gate"][e])
+        wu[e] = bf16_bits(ins["w_up"][e])
+        wd[e] = bf16_bits(ins["w_down"][e])
+    sh = {}
+    if cfg.S > 0:
+        sh = dict(ws_gate=[bf16_bits(ins["ws_gate"][s]) for s in range(cfg.S)],
+                  ws_up=[bf16_bits(ins["ws_up"][s]) for s in range(cfg.S)],
+                  ws_down=[bf16_bits(ins["ws_down"][s]) for s in range(cfg.S)])
+    return oracle.layer(hidden_f32(ins)[rows], np32(ins["w_router"]), wg, wu, wd, K=cfg.K,
+                        score_fn=cfg.score_fn, renormalize=cfg.renormalize,
+                        router_bias=np32(ins.get("router_bias")), sel_bias=np32(ins.get("sel_bias")),
+                        **sh)
+
+
+def output_errors(gpu: np.ndarray, ref: np.ndarray) -> dict:
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    diff = np.abs(gpu - ref)
+    mref = float(np.abs(ref).max()) if ref.size else 0.0
+    sref = float(np.abs(ref).sum()) if ref.size else 0.0
+    return dict(max_rel=float(diff.max()) / mref if ref.size and mref > 0 else float(diff.max(initial=0)),
+                l1_rel=float(diff.sum()) / sref if sref > 0 else float(diff.sum()))
+
+
+def assert_output_close(gpu, ref, what=""):
+    e = output_errors(gpu, ref)
+    assert e["max_rel"] <= MAX_REL and e["l1_rel"] <= L1_REL, f"{what}: {e}"
+    return e
+
+
+def compare_router(gpu_idx: np.ndarray, gpu_w: np.ndarray, ref: dict):
+    """Bit-exact indices on tokens with margin >= 1e-5 (near ties reported),
+    weights within 1e-5 wherever the indices agree. Returns the near-tie report."""
+    near = ref["margin"] < MARGIN_TIE
+    same = np.all(gpu_idx == ref["idx"], axis=1)
+    bad = ~same & ~near
+    assert not bad.any(), f"index mismatch on {int(bad.sum())} tokens with margin >= 1e-5: {np.nonzero(bad)[0][:10]}"
+    dw = np.abs(gpu_w.astype(np.float64) - ref["w"])[same]
+    assert dw.size == 0 or dw.max() <= W_ATOL, f"gate weight error {dw.max()}"
+    return dict(near_ties=int(near.sum()), near_tie_flips=int((~same & near).sum()),
+                flipped_tokens=np.nonzero(~same)[0])
+
+
+def make_case(cfg, seed=0, device="cuda", expert_device=None):
+    """Seeded inputs; router-side tensors on the CPU and a device copy of all."""
+    ins = inputs.make_inputs(cfg, seed=seed, device=expert_device or "cpu")
+    dev = {k: (None if v is None else v.to(device).contiguous()) for k, v in ins.items()}
+    return ins, dev

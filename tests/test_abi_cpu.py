@@ -1,0 +1,74 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/moe.h
+declares, and its host-only functions (status strings, problem validation,
+workspace sizing) behave as documented. No CUDA call is made here."""
+import ctypes
+import subprocess
+
+import pytest
+
+from mixture_experts_layer_94_b300 import binding as B
+from mixture_experts_layer_94_b300 import inputs
+
+
+def test_header_declares_the_abi():
+    names = B.header_functions()
+    for n in ("moe_router_topk", "moe_permute", "moe_grouped_swiglu", "moe_combine",
+              "moe_layer_forward", "moe_workspace_bytes", "moe_get_device_status",
+              "moe_status_string", "moe_problem_check"):
+        assert n in names
+
+
+def test_library_exports_every_header_symbol():
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in B.header_functions():
+        assert hasattr(lib, n), n
+    syms = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                          text=True, check=True).stdout
+    exported = {line.split()[-1] for line in syms.splitlines() if " T " in line}
+    assert set(B.header_functions()) <= exported
+
+
+def test_status_strings():
+    for s, key in ((0, "MOE_OK"), (-1, "INVALID_ARG"), (-2, "UNSUPPORTED"), (-3, "WORKSPACE"),
+                   (-4, "CUDA"), (-5, "TIMEOUT"), (-6, "DEVICE_BOUNDS"), (7, "UNKNOWN")):
+        assert key in B.status_string(s)
+
+
+@pytest.mark.parametrize("cfg", list(inputs.CONFIGS.values()), ids=list(inputs.CONFIGS))
+def test_workload_problems_are_valid(cfg):
+    p = B.problem(cfg)
+    assert B.problem_check(p) == 0
+    for call in (B.CALL_PERMUTE, B.CALL_GROUPED_SWIGLU, B.CALL_LAYER_FORWARD):
+        n = B.workspace_bytes(p, call)
+        assert n > 0 and n % 256 == 0
+    assert B.workspace_bytes(p, B.CALL_LAYER_FORWARD) > B.workspace_bytes(p, B.CALL_PERMUTE)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("T", -1, -1), ("d_model", 0, -1), ("d_model", 12, -1), ("n_experts", 0, -1),
+    ("top_k", 0, -1), ("top_k", 9, -1), ("ffn", 100, -1), ("n_shared", -1, -1),
+    ("score_fn", 2, -1), ("renormalize", 3, -1), ("hidden_dtype", 5, -1),
+    ("n_experts", 257, -2), ("n_shared", 9, -2),
+])
+def test_problem_check_rejects(field, value, status):
+    cfg = inputs.TINY.with_(Fs=64)
+    p = B.problem(cfg, **{field: value})
+    assert B.problem_check(p) == status
+    assert B.workspace_bytes(p, B.CALL_LAYER_FORWARD) == 0
+
+
+def test_problem_check_shared_width_and_topk_cap():
+    p = B.problem(inputs.TINY, n_shared=1, shared_ffn=0)
+    assert B.problem_check(p) == -1
+    p = B.problem(inputs.TINY, n_experts=64, top_k=33)
+    assert B.problem_check(p) == -2
+    assert B.lib.moe_problem_check(None) == -1
+
+
+def test_workspace_grows_with_tokens():
+    a = B.workspace_bytes(B.problem(inputs.MIXTRAL, T=1), B.CALL_LAYER_FORWARD)
+    b = B.workspace_bytes(B.problem(inputs.MIXTRAL, T=4096), B.CALL_LAYER_FORWARD)
+    assert b > a
+    # the fused layer needs x_perm, h and the fp32 accumulator at least
+    m = inputs.MIXTRAL
+    assert b >= m.T * m.K * (m.d + m.F) * 2 + m.T * m.d * 4

@@ -1,0 +1,313 @@
+"""GPU parity: every C-ABI entry point and the whole layer against the oracle.
+
+Run on a B300 with libmoe.so built. Inputs are the seeded synthetic workloads;
+the oracle sees exactly the tensors the GPU sees.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_94_b300 import inputs
+from oracle import oracle
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from mixture_experts_layer_94_b300 import binding as B
+
+
+def _dev(t):
+    return None if t is None else t.cuda().contiguous()
+
+
+# Small and mid-size workloads the full oracle finishes in seconds. They span
+# several 128-row tiles, ragged row / column / K tails, empty experts, shared
+# experts, both score functions and both hidden dtypes.
+MID = {
+    "tiny": inputs.TINY,
+    "ragged_softmax": inputs.MoEConfig("ragged_softmax", T=300, d=264, N=16, K=4, F=392),
+    "dsv3_like": inputs.MoEConfig("dsv3_like", T=333, d=256, N=64, K=6, F=200, S=1, Fs=136,
+                                  score="sigmoid", sel_bias_var=0.1, zipf=1.1),
+    "gptoss_like": inputs.MoEConfig("gptoss_like", T=200, d=320, N=32, K=4, F=320),
+    "two_shared_f32": inputs.MoEConfig("two_shared_f32", T=130, d=128, N=8, K=2, F=128, S=2, Fs=64,
+                                       hidden_dtype="f32"),
+    "no_renorm_sigmoid": inputs.MoEConfig("no_renorm_sigmoid", T=97, d=192, N=12, K=3, F=96,
+                                          score="sigmoid", renormalize=0),
+    "no_renorm_softmax": inputs.MoEConfig("no_renorm_softmax", T=64, d=64, N=8, K=2, F=64,
+                                          renormalize=0),
+    "K_equals_N": inputs.MoEConfig("K_equals_N", T=70, d=128, N=4, K=4, F=136),
+    "N_K_1": inputs.MoEConfig("N_K_1", T=129, d=128, N=1, K=1, F=256),
+    "T1": inputs.MoEConfig("T1", T=1, d=256, N=16, K=4, F=128),
+    "d72_tail": inputs.MoEConfig("d72_tail", T=150, d=72, N=6, K=2, F=40),
+}
+
+
+def _run_layer(cfg, dev, T=None):
+    layer = B.MoELayer(cfg, dev, T=T)
+    T = cfg.T if T is None else T
+    topk_idx = torch.empty(T, cfg.K, dtype=torch.int32, device="cuda")
+    topk_w = torch.empty(T, cfg.K, dtype=torch.float32, device="cuda")
+    counts = torch.empty(cfg.N, dtype=torch.int32, device="cuda")
+    out = layer.forward(dev["hidden"], topk_idx=topk_idx, topk_w=topk_w, counts=counts)
+    torch.cuda.synchronize()
+    assert layer.status(T) == 0
+    return out, topk_idx.cpu().numpy(), topk_w.cpu().numpy(), counts.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", list(MID))
+def test_layer_matches_oracle(name):
+    cfg = MID[name]
+    ins, dev = H.make_case(cfg)
+    out, idx, w, counts = _run_layer(cfg, dev)
+    ref = H.oracle_layer_rows(cfg, ins, np.arange(cfg.T))
+    rep = H.compare_router(idx, w, ref)
+    assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
+    keep = np.ones(cfg.T, bool)
+    keep[rep["flipped_tokens"]] = False
+    H.assert_output_close(out.float().cpu().numpy()[keep], ref["out"][keep], name)
+
+
+def test_layer_empty_batch():
+    cfg = inputs.TINY.with_(T=0)
+    _, dev = H.make_case(inputs.TINY)
+    layer = B.MoELayer(cfg, dev)
+    counts = torch.full((cfg.N,), -1, dtype=torch.int32, device="cuda")
+    out = layer.forward(dev["hidden"][:0], counts=counts)
+    torch.cuda.synchronize()
+    assert out.shape == (0, cfg.d) and torch.all(counts == 0)
+
+
+def test_layer_one_expert_takes_every_token():
+    """A router bias that sends every token to expert 5 first: one group holds
+    all T rows (many row tiles), the others get the second choices."""
+    cfg = inputs.MoEConfig("hot", T=640, d=128, N=8, K=2, F=256)
+    ins, dev = H.make_case(cfg)
+    rb = torch.zeros(cfg.N)
+    rb[5] = 50.0
+    ins["router_bias"] = rb
+    dev["router_bias"] = rb.cuda()
+    out, idx, w, counts = _run_layer(cfg, dev)
+    assert np.all(idx[:, 0] == 5) and counts[5] == cfg.T
+    ref = H.oracle_layer_rows(cfg, ins, np.arange(cfg.T))
+    H.compare_router(idx, w, ref)
+    H.assert_output_close(out.float().cpu().numpy(), ref["out"], "hot expert")
+
+
+def test_layer_is_repeatable():
+    cfg = MID["ragged_softmax"]
+    _, dev = H.make_case(cfg)
+    a = _run_layer(cfg, dev)[0]
+    b = _run_layer(cfg, dev)[0]
+    # fp32 scatter-add order may differ in the last bit of the fp32 sum; bf16 outputs agree to 1 ulp
+    diff = (a.float() - b.float()).abs()
+    assert float(diff.max()) <= float(a.float().abs().max()) * 2 ** -7
+
+
+# --------------------------------------------------------------------------- router
+ROUTER_CASES = ["tiny", "ragged_softmax", "dsv3_like", "no_renorm_sigmoid", "no_renorm_softmax",
+                "K_equals_N", "N_K_1", "T1"]
+
+
+@pytest.mark.parametrize("name", ROUTER_CASES)
+def test_router_matches_oracle(name):
+    cfg = MID[name]
+    ins = inputs.make_router_inputs(cfg, seed=1)
+    p = B.problem(cfg)
+    idx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device="cuda")
+    w = torch.empty(cfg.T, cfg.K, dtype=torch.float32, device="cuda")
+    logits = torch.empty(cfg.T, cfg.N, dtype=torch.float32, device="cuda")
+    B.router_topk(p, _dev(ins["hidden"]), _dev(ins["w_router"]), idx, w,
+                  router_bias=_dev(ins["router_bias"]), sel_bias=_dev(ins["sel_bias"]), logits=logits)
+    torch.cuda.synchronize()
+    ref = H.oracle_router(cfg, ins)
+    H.compare_router(idx.cpu().numpy(), w.cpu().numpy(), ref)
+    lg = logits.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["logits"]) <= 1e-5 * (1 + np.abs(ref["logits"])))
+
+
+def test_router_exact_ties_break_to_lower_index():
+    """Duplicated router columns give exactly equal logits on both sides."""
+    cfg = inputs.MoEConfig("ties", T=200, d=64, N=8, K=3, F=8)
+    ins = inputs.make_router_inputs(cfg, seed=2)
+    W = ins["w_router"].clone()
+    W[:, 6] = W[:, 1]
+    W[:, 3] = W[:, 0]
+    idx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device="cuda")
+    w = torch.empty(cfg.T, cfg.K, dtype=torch.float32, device="cuda")
+    B.router_topk(B.problem(cfg), _dev(ins["hidden"]), _dev(W), idx, w)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    for t in range(cfg.T):
+        for a, b in ((1, 6), (0, 3)):
+            if a in gi[t] and b in gi[t]:
+                assert list(gi[t]).index(a) < list(gi[t]).index(b)
+
+
+# --------------------------------------------------------------------------- permute
+PERMUTE_CASES = [(1, 8, 2, False), (37, 8, 2, False), (500, 64, 6, True), (1000, 256, 8, True),
+                 (4096, 8, 2, False), (33, 1, 1, False)]
+
+
+@pytest.mark.parametrize("T,N,K,skew", PERMUTE_CASES)
+@pytest.mark.parametrize("hidden_dtype", ["bf16", "f32"])
+def test_permute_bit_exact(T, N, K, skew, hidden_dtype):
+    rng = np.random.default_rng(T + N)
+    p_e = None
+    if skew:
+        p_e = 1.0 / np.arange(1, N + 1) ** 1.5
+        p_e /= p_e.sum()
+    idx = np.stack([rng.choice(N, size=K, replace=False, p=p_e) for _ in range(T)]).astype(np.int32)
+    d = 136
+    cfg = inputs.MoEConfig("perm", T=T, d=d, N=N, K=K, F=8, hidden_dtype=hidden_dtype)
+    hidden = inputs.make_router_inputs(cfg, seed=3)["hidden"]
+    p = B.problem(cfg)
+    ws = B.new_workspace(p, B.CALL_PERMUTE)
+    counts = torch.empty(N, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(N + 1, dtype=torch.int32, device="cuda")
+    perm_src = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    inv_row = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty(T * K, d, dtype=torch.bfloat16, device="cuda")
+    B.permute(p, _dev(torch.from_numpy(idx)), _dev(hidden), counts, offsets, perm_src, inv_row, x_perm, ws)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws) == 0
+    ref = oracle.permute(idx, N)
+    for k in ("counts", "offsets", "perm_src", "inv_row"):
+        assert np.array_equal(locals()[k].cpu().numpy(), ref[k]), k
+    expect = hidden.to(torch.bfloat16)[torch.from_numpy(ref["perm_src"] // K).long()]
+    assert torch.equal(x_perm.cpu().view(torch.int16), expect.view(torch.int16))
+
+
+def test_permute_reports_out_of_range_index():
+    cfg = inputs.MoEConfig("bad", T=40, d=64, N=8, K=2, F=8)
+    idx = np.tile(np.array([[0, 1]], np.int32), (cfg.T, 1))
+    idx[17, 1] = 9
+    p = B.problem(cfg)
+    ws = B.new_workspace(p, B.CALL_PERMUTE)
+    hidden = torch.zeros(cfg.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    t = lambda *s, dt=torch.int32: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    B.permute(p, _dev(torch.from_numpy(idx)), hidden, t(cfg.N), t(cfg.N + 1), t(cfg.T * 2),
+              t(cfg.T * 2), t(cfg.T * 2, cfg.d, dt=torch.bfloat16), ws)
+    assert B.get_device_status(ws) == -6  # MOE_ERR_DEVICE_BOUNDS
+    assert B.get_device_status(ws) == 0   # read-and-clear
+
+
+# --------------------------------------------------------------------------- grouped SwiGLU
+SWIGLU_CASES = [(128, 256, 8, 2, 64), (320, 200, 5, 2, 300), (72, 40, 3, 1, 130), (256, 512, 16, 4, 700)]
+
+
+@pytest.mark.parametrize("d,F,N,K,T", SWIGLU_CASES)
+def test_grouped_swiglu_matches_oracle(d, F, N, K, T):
+    cfg = inputs.MoEConfig("gs", T=T, d=d, N=N, K=K, F=F)
+    ins = inputs.make_inputs(cfg, seed=4)
+    rng = np.random.default_rng(d + F)
+    p_e = np.linspace(3.0, 0.0, N) ** 2 + 1e-9  # skewed, last expert (nearly) empty
+    p_e[-1] = 0.0
+    p_e /= p_e.sum()
+    K_eff = min(K, int((p_e > 0).sum()))
+    cfg = cfg.with_(K=K_eff)
+    idx = np.stack([rng.choice(N, size=K_eff, replace=False, p=p_e) for _ in range(T)]).astype(np.int32)
+    perm = oracle.permute(idx, N)
+    hid = ins["hidden"]
+    x_perm = hid[torch.from_numpy(perm["perm_src"] // K_eff).long()].to(torch.bfloat16).contiguous()
+    p = B.problem(cfg)
+    ws = B.new_workspace(p, B.CALL_GROUPED_SWIGLU)
+    h = torch.empty(T * K_eff, F, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(T * K_eff, d, dtype=torch.bfloat16, device="cuda")
+    B.grouped_swiglu(p, x_perm.cuda(), torch.from_numpy(perm["offsets"]).cuda(), _dev(ins["w_gate"]),
+                     _dev(ins["w_up"]), _dev(ins["w_down"]), h, y, ws)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws) == 0
+    hg, yg = h.float().cpu().numpy(), y.float().cpu().numpy()
+    href = np.empty((T * K_eff, F))
+    yref = np.empty((T * K_eff, d))
+    xp = x_perm.float().numpy().astype(np.float64)
+    for e in range(N):
+        wg, wu, wd = (H.bf16_bits(ins[k][e]) for k in ("w_gate", "w_up", "w_down"))
+        for r in range(perm["offsets"][e], perm["offsets"][e + 1]):
+            href[r], yref[r] = oracle.expert_ffn(xp[r], wg, wu, wd, return_h=True)
+    H.assert_output_close(hg, href, "h_perm")
+    H.assert_output_close(yg, yref, "y_perm")
+
+
+# --------------------------------------------------------------------------- combine
+@pytest.mark.parametrize("T,K,d,shared", [(1, 1, 8, False), (77, 2, 136, True), (300, 8, 512, False)])
+def test_combine_matches_oracle(T, K, d, shared):
+    g = torch.Generator().manual_seed(T * K)
+    y = torch.randn(T * K, d, generator=g).to(torch.bfloat16)
+    perm = torch.randperm(T * K, generator=g).to(torch.int32)          # inv_row: a bijection
+    w = torch.rand(T, K, generator=g)
+    w = (w / w.sum(1, keepdim=True)).float()
+    sh = torch.randn(T, d, generator=g).to(torch.bfloat16) if shared else None
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    p = B.problem(None, T=T, d_model=d, n_experts=max(K, 2), top_k=K, ffn=8, n_shared=0, shared_ffn=0,
+                  score_fn=0, renormalize=1, hidden_dtype=1)
+    B.combine(p, y.cuda(), perm.cuda(), w.cuda(), out, shared_out=_dev(sh))
+    torch.cuda.synchronize()
+    yf = y.double().numpy()
+    ref = np.stack([oracle.combine(w[t].double().numpy(), yf[perm[t * K:(t + 1) * K].long().numpy()],
+                                   None if sh is None else sh[t].double().numpy()) for t in range(T)])
+    got = out.double().cpu().numpy()
+    # one bf16 rounding of an fp32 sum: at most half an ulp of bf16 plus fp32 noise
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+# --------------------------------------------------------------------------- step-wise == fused
+def test_stepwise_path_matches_fused_layer():
+    cfg = MID["ragged_softmax"]
+    ins, dev = H.make_case(cfg)
+    fused, idx_f, w_f, _ = _run_layer(cfg, dev)
+    p = B.problem(cfg)
+    T, K, N, d, F = cfg.T, cfg.K, cfg.N, cfg.d, cfg.F
+    idx = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    B.router_topk(p, dev["hidden"], dev["w_router"], idx, w)
+    e = lambda *s, dt=torch.int32: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    counts, offsets, perm_src, inv_row = e(N), e(N + 1), e(T * K), e(T * K)
+    x_perm = e(T * K, d, dt=torch.bfloat16)
+    ws = B.new_workspace(p, B.CALL_LAYER_FORWARD)
+    B.permute(p, idx, dev["hidden"], counts, offsets, perm_src, inv_row, x_perm, ws)
+    h, y = e(T * K, F, dt=torch.bfloat16), e(T * K, d, dt=torch.bfloat16)
+    B.grouped_swiglu(p, x_perm, offsets, dev["w_gate"], dev["w_up"], dev["w_down"], h, y, ws)
+    out = e(T, d, dt=torch.bfloat16)
+    B.combine(p, y, inv_row, w, out)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws) == 0
+    assert np.array_equal(idx.cpu().numpy(), idx_f) and np.array_equal(w.cpu().numpy(), w_f)
+    H.assert_output_close(out.float().cpu().numpy(), fused.float().cpu().numpy(), "stepwise vs fused")
+
+
+# --------------------------------------------------------------------------- full-size workloads
+def _sample_rows(T, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {0, T - 1} | set(rng.choice(T, size=min(T, n), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+FULL = [("mixtral", inputs.MIXTRAL, 12), ("gptoss", inputs.GPTOSS, 12), ("dsv3", inputs.DSV3, 6)] + [
+    (f"qwen_decode_T{T}", inputs.QWEN_DECODE.with_(T=T), 6) for T in inputs.DECODE_BATCHES]
+
+
+@pytest.mark.parametrize("name,cfg,n_sample", FULL, ids=[f[0] for f in FULL])
+def test_full_size_workload(name, cfg, n_sample):
+    """The full-size workloads through moe_layer_forward (the launch configuration
+    the benchmark times): router and counts on every token; outputs on sampled
+    tokens the oracle computes one by one."""
+    ins = inputs.make_inputs(cfg, seed=0, device="cuda")
+    dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
+    out, idx, w, counts = _run_layer(cfg, dev)
+    ref_r = H.oracle_router(cfg, ins)
+    rep = H.compare_router(idx, w, ref_r)
+    # counts: the GPU's own histogram, and the oracle's up to the near-tie flips
+    assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
+    ref_counts = np.bincount(ref_r["idx"].reshape(-1), minlength=cfg.N)
+    fl = rep["flipped_tokens"]
+    delta = np.bincount(idx[fl].reshape(-1), minlength=cfg.N) - np.bincount(ref_r["idx"][fl].reshape(-1), minlength=cfg.N)
+    assert np.array_equal(counts - ref_counts, delta)
+    rows = np.array([r for r in _sample_rows(cfg.T, n_sample) if r not in set(fl.tolist())])
+    ref = H.oracle_layer_rows(cfg, ins, rows)
+    e = H.assert_output_close(out.float().cpu().numpy()[rows], ref["out"], name)
+    print(f"{name}: near ties {rep['near_ties']} (flipped {rep['near_tie_flips']}), errors {e}, "
+          f"touched experts {int((counts > 0).sum())}")
