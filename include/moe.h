@@ -70,7 +70,8 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 typedef enum {
   MOE_CALL_PERMUTE = 0,
   MOE_CALL_GROUPED_SWIGLU = 1,
-  MOE_CALL_LAYER_FORWARD = 2
+  MOE_CALL_LAYER_FORWARD = 2,
+  MOE_CALL_ROUTER = 3
 } moe_call_t;
 
 /*
@@ -146,15 +147,18 @@ size_t moe_workspace_bytes(const moe_problem_t* p, int32_t call);
  *               equal keys are broken toward the lower expert index
  *   topk_w      out fp32 [T][K]: gate weight of each chosen expert
  *   logits_opt  out fp32 [T][N] or NULL: the router logits (debug)
+ *   ws          workspace of moe_workspace_bytes(p, MOE_CALL_ROUTER) bytes
+ *               (partial logits when the d axis is split across CTAs)
  * Key used for selection: softmax -> the logit (monotone in the softmax);
  * sigmoid -> sigmoid(logit) + sel_bias. Weights: softmax -> softmax over the
  * chosen logits; sigmoid -> chosen sigmoid scores / their sum.
- * sel_bias with softmax scoring returns MOE_ERR_UNSUPPORTED.
+ * sel_bias with softmax scoring returns MOE_ERR_UNSUPPORTED. Deterministic.
  */
 moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden,
                              const float* w_router, const float* router_bias,
                              const float* sel_bias, int32_t* topk_idx,
-                             float* topk_w, float* logits_opt, void* stream);
+                             float* topk_w, float* logits_opt, void* ws,
+                             size_t ws_bytes, void* stream);
 
 /*
  * Route and pack ("Chapter 19", §19.6.3): per-expert histogram, exclusive

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_OK = 0
-CALL_PERMUTE, CALL_GROUPED_SWIGLU, CALL_LAYER_FORWARD = 0, 1, 2
+CALL_PERMUTE, CALL_GROUPED_SWIGLU, CALL_LAYER_FORWARD, CALL_ROUTER = 0, 1, 2, 3
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DT_F32, DT_BF16 = 0, 1
 
@@ -53,7 +53,7 @@ def _load():
         "moe_status_string": ([i32], ctypes.c_char_p),
         "moe_problem_check": ([pp], i32),
         "moe_workspace_bytes": ([pp, i32], sz),
-        "moe_router_topk": ([pp] + [P] * 8, i32),
+        "moe_router_topk": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_permute": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_grouped_swiglu": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_combine": ([pp] + [P] * 6, i32),
@@ -128,10 +128,12 @@ def _stream(stream):
 
 
 def router_topk(p: Problem, hidden, w_router, topk_idx, topk_w, router_bias=None, sel_bias=None,
-                logits=None, stream=None):
+                logits=None, ws=None, stream=None):
+    if ws is None:
+        ws = new_workspace(p, CALL_ROUTER, hidden.device)
     _check(lib.moe_router_topk(ctypes.byref(p), _p(hidden), _p(w_router), _p(router_bias),
-                               _p(sel_bias), _p(topk_idx), _p(topk_w), _p(logits), _stream(stream)),
-           "moe_router_topk")
+                               _p(sel_bias), _p(topk_idx), _p(topk_w), _p(logits), _p(ws), ws.numel(),
+                               _stream(stream)), "moe_router_topk")
 
 
 def permute(p: Problem, topk_idx, hidden, counts, offsets, perm_src, inv_row, x_perm, ws,

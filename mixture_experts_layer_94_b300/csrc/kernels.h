@@ -18,8 +18,19 @@ struct RouterArgs {
   const float* sel_bias;
   int32_t* topk_idx;
   float* topk_w;
-  float* logits;
+  float* logits;       // optional [T][N] output
+  float* partial;      // scratch [splits][T][N]
+  int32_t splits, d_slice;  // filled by launch_router
 };
+
+// How the router logits kernel tiles the problem: token tiles x d slices.
+struct RouterPlan {
+  int64_t token_tiles;
+  int32_t splits;   // number of d slices (partial logits summed in order)
+  int32_t d_slice;  // inputs per slice
+  int32_t np;       // N <= 32: N rounded up to a power of two; else 0
+};
+RouterPlan router_plan(int64_t T, int32_t d, int32_t N);
 cudaError_t launch_router(const RouterArgs& a, bool hidden_bf16, cudaStream_t s);
 
 struct PermuteArgs {

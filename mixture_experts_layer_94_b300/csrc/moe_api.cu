@@ -19,7 +19,7 @@ constexpr int64_t kInt32Max = 2147483647;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t err, chunk, groups, ts_gu, ts_dn;
+  size_t err, chunk, groups, ts_gu, ts_dn, router;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_bf16, h, h_sh, out_acc;
   size_t total;
 };
@@ -40,6 +40,10 @@ Layout make_layout(const moe_problem_t& p, int call) {
   L.groups = take((size_t)G * sizeof(GroupDesc));
   L.ts_gu = take((size_t)(G + 1) * 4);
   L.ts_dn = take((size_t)(G + 1) * 4);
+  if (call == MOE_CALL_ROUTER || call == MOE_CALL_LAYER_FORWARD) {
+    const RouterPlan rp = router_plan(T, p.d_model, p.n_experts);
+    L.router = take((size_t)rp.splits * T * p.n_experts * 4);
+  }
   if (call == MOE_CALL_LAYER_FORWARD) {
     L.topk_idx = take((size_t)TK * 4);
     L.topk_w = take((size_t)TK * 4);
@@ -238,19 +242,25 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
 
 size_t moe_workspace_bytes(const moe_problem_t* p, int32_t call) {
   if (moe_problem_check(p) != MOE_OK) return 0;
-  if (call != MOE_CALL_PERMUTE && call != MOE_CALL_GROUPED_SWIGLU && call != MOE_CALL_LAYER_FORWARD) return 0;
+  if (call != MOE_CALL_PERMUTE && call != MOE_CALL_GROUPED_SWIGLU && call != MOE_CALL_LAYER_FORWARD &&
+      call != MOE_CALL_ROUTER)
+    return 0;
   return make_layout(*p, call).total;
 }
 
 moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const float* w_router,
                              const float* router_bias, const float* sel_bias, int32_t* topk_idx, float* topk_w,
-                             float* logits_opt, void* stream) {
+                             float* logits_opt, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(moe_problem_check(p));
+  if (sel_bias && p->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_UNSUPPORTED;
+  Layout L;
+  MOE_TRY(check_ws(p, MOE_CALL_ROUTER, ws, ws_bytes, &L));
   if (p->T == 0) return MOE_OK;
   if (!hidden || !w_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-  if (sel_bias && p->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(hidden) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   RouterArgs a{p->T, p->d_model, p->n_experts, p->top_k, p->score_fn, p->renormalize,
-               hidden, w_router, router_bias, sel_bias, topk_idx, topk_w, logits_opt};
+               hidden, w_router, router_bias, sel_bias, topk_idx, topk_w, logits_opt,
+               at<float>(ws, L.router), 0, 0};
   return cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
 }
 
@@ -377,8 +387,9 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
 
   // 1. router, scoring, top-K, gate weights
   MOE_TRY(record(ev, 0, s));
+  if (!aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
   RouterArgs ra{T, p->d_model, N, K, p->score_fn, p->renormalize, hidden, w->w_router,
-                w->router_bias, w->sel_bias, topk_idx, topk_w, nullptr};
+                w->router_bias, w->sel_bias, topk_idx, topk_w, nullptr, at<float>(ws, L.router), 0, 0};
   MOE_TRY(cuda_status(launch_router(ra, hbf16, s)));
   MOE_TRY(record(ev, 1, s));
 
@@ -469,8 +480,9 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
 int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   if (moe_problem_check(p) != MOE_OK) return 0;
   if (p->T == 0) return 1;  // the histogram scan that writes zero counts
-  // router, histogram, scan, scatter+gather, schedule, gate/up GEMM, down GEMM, finalise
-  return 8;
+  // router logits, router top-K, histogram, scan, scatter, gather, schedule,
+  // gate/up GEMM, down GEMM, finalise
+  return 10;
 }
 
 moe_status_t moe_get_device_status(void* ws, void* stream) {

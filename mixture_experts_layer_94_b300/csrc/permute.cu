@@ -115,84 +115,73 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
   }
 }
 
-constexpr int kGatherWarps = 8;
+constexpr int kScatterWarps = 8;
 
-// One CTA per chunk: warp 0 places the chunk's copies; then all warps copy rows.
-__global__ void __launch_bounds__(kGatherWarps * 32) route_scatter_gather_kernel(const PermuteArgs a) {
-  __shared__ uint32_t masks[kMaxExperts];
-  __shared__ int32_t rows[kTokensPerChunk * kMaxTopK];
+// One warp per chunk: each copy's row = its chunk's base for the expert plus
+// its rank among the chunk's earlier tokens that chose the same expert.
+__global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const PermuteArgs a) {
+  __shared__ uint32_t masks[kScatterWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t c = blockIdx.x;
-  const int K = a.K, N = a.N, d = a.d;
-  const int64_t t0 = c * kTokensPerChunk;
-  const int ntok = (int)min((int64_t)kTokensPerChunk, a.T - t0);
-  if (warp == 0) {
-    build_chunk_masks(masks, a.topk_idx, a.T, K, N, c, lane, a.err);
-    if (lane < ntok) {
-      const int64_t t = t0 + lane;
-      const uint32_t below = (1u << lane) - 1u;
-      for (int k = 0; k < K; ++k) {
-        const int e = a.topk_idx[t * K + k];
-        int32_t r = -1;
-        if (e >= 0 && e < N) {
-          r = a.chunk_counts[(int64_t)e * a.C + c] + __popc(masks[e] & below);
-          a.perm_src[r] = (int32_t)(t * K + k);
-          a.inv_row[t * K + k] = r;
-        }
-        rows[lane * K + k] = r;
+  const int64_t c = (int64_t)blockIdx.x * kScatterWarps + warp;
+  if (c >= a.C) return;
+  const int K = a.K, N = a.N;
+  uint32_t* m = masks[warp];
+  build_chunk_masks(m, a.topk_idx, a.T, K, N, c, lane, a.err);
+  const int64_t t = c * kTokensPerChunk + lane;
+  if (t < a.T) {
+    const uint32_t below = (1u << lane) - 1u;
+    for (int k = 0; k < K; ++k) {
+      const int e = a.topk_idx[t * K + k];
+      if (e >= 0 && e < N) {
+        const int32_t r = a.chunk_counts[(int64_t)e * a.C + c] + __popc(m[e] & below);
+        a.perm_src[r] = (int32_t)(t * K + k);
+        a.inv_row[t * K + k] = r;
       }
     }
   }
-  __syncthreads();
-  // Row copies: hidden[t] -> x_perm[r] (bf16), 8 elements (16 B of output) per lane step.
-  const int nvec = d / 8;
-  for (int q = warp; q < ntok * K; q += kGatherWarps) {
-    const int r = rows[q];
-    if (r < 0) continue;
-    const int64_t t = t0 + q / K;
-    uint4* dst = reinterpret_cast<uint4*>(a.x_perm + (int64_t)r * d);
+}
+
+__device__ __forceinline__ uint4 cvt8_bf16(const float4 p, const float4 q) {
+  return make_uint4(pack_bf16x2(p.x, p.y), pack_bf16x2(p.z, p.w), pack_bf16x2(q.x, q.y), pack_bf16x2(q.z, q.w));
+}
+
+// Row gather into expert order, one warp per permuted row, 16-byte vectors;
+// grid-stride over rows so every SM streams. The fused layer also clears the
+// fp32 accumulator and writes a bf16 copy of an fp32 hidden (shared experts).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int d = a.d, nvec = d / 8;
+  // Only rows [0, offsets[N]) are placed; fewer than T*K when an input index
+  // was out of range (reported through the error word).
+  const int64_t placed = min(rows, (int64_t)__ldg(a.offsets + a.N));
+  for (int64_t r = warp0; r < placed; r += nwarps) {
+    const int32_t src = a.perm_src[r];
+    if (src < 0 || src >= rows) continue;
+    const int64_t t = src / a.K;
+    uint4* dst = reinterpret_cast<uint4*>(a.x_perm + r * d);
     if (a.hidden_bf16) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * d);
+      const uint4* sp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * d);
 #pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+      for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(sp + v);
     } else {
-      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * d);
+      const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * d);
 #pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) {
-        const float4 p = src[2 * v], q2 = src[2 * v + 1];
-        uint4 o;
-        o.x = pack_bf16x2(p.x, p.y);
-        o.y = pack_bf16x2(p.z, p.w);
-        o.z = pack_bf16x2(q2.x, q2.y);
-        o.w = pack_bf16x2(q2.z, q2.w);
-        dst[v] = o;
-      }
+      for (int v = lane; v < nvec; v += 32) dst[v] = cvt8_bf16(__ldg(sp + 2 * v), __ldg(sp + 2 * v + 1));
     }
   }
-  // Optional per-token work of the fused layer: clear the fp32 accumulator rows
-  // and write a bf16 copy of an fp32 hidden row (the shared experts' operand).
-  if (a.zero_rows || a.x_bf16) {
-    for (int tk = warp; tk < ntok; tk += kGatherWarps) {
-      const int64_t t = t0 + tk;
-      if (a.zero_rows) {
-        float4* z = reinterpret_cast<float4*>(a.zero_rows + t * d);
-        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int v = lane; v < d / 4; v += 32) z[v] = zero;
-      }
-      if (a.x_bf16) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * d);
-        uint4* dst = reinterpret_cast<uint4*>(a.x_bf16 + t * d);
-        for (int v = lane; v < nvec; v += 32) {
-          const float4 p = src[2 * v], q2 = src[2 * v + 1];
-          uint4 o;
-          o.x = pack_bf16x2(p.x, p.y);
-          o.y = pack_bf16x2(p.z, p.w);
-          o.z = pack_bf16x2(q2.x, q2.y);
-          o.w = pack_bf16x2(q2.z, q2.w);
-          dst[v] = o;
-        }
-      }
-    }
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  if (a.zero_rows) {
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* z = reinterpret_cast<float4*>(a.zero_rows);
+    for (int64_t i = tid; i < a.T * d / 4; i += nthr) z[i] = zero;
+  }
+  if (a.x_bf16) {
+    const float4* sp = reinterpret_cast<const float4*>(a.hidden);
+    uint4* dp = reinterpret_cast<uint4*>(a.x_bf16);
+    for (int64_t i = tid; i < a.T * nvec; i += nthr) dp[i] = cvt8_bf16(__ldg(sp + 2 * i), __ldg(sp + 2 * i + 1));
   }
 }
 
@@ -251,7 +240,13 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
   }
   route_hist_kernel<<<(unsigned)((a.C + kHistWarps - 1) / kHistWarps), kHistWarps * 32, 0, s>>>(a);
   route_scan_kernel<<<1, 1024, 0, s>>>(a);
-  route_scatter_gather_kernel<<<(unsigned)a.C, kGatherWarps * 32, 0, s>>>(a);
+  route_scatter_kernel<<<(unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s>>>(a);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t rows = a.T * a.K;
+  const int64_t want = (rows + 7) / 8;  // 8 rows (warps) per 256-thread CTA
+  const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
+  gather_rows_kernel<<<grid, 256, 0, s>>>(a, rows);
   return cudaGetLastError();
 }
 

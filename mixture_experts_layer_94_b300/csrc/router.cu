@@ -7,12 +7,20 @@
 // logits equals full softmax + renormalisation; §19.3.4: the balancing bias
 // shifts the scores used for selection only.
 //
-// Design: a CTA takes 32 tokens; d is walked in 32-wide chunks staged in shared
-// memory (the router matrix chunk is shared by all 32 tokens). Each warp owns 4
-// tokens and keeps their logits in registers, fp32 FMA. Lanes split the experts
-// (lane owns experts lane, lane+32, ... when N > 32) or, for N <= 32, split d
-// into 32/Npad lane groups that are reduced by shuffles at the end. Top-K is a
-// K-round shuffle argmax over (key desc, expert asc); slot k ends in lane k.
+// Two kernels, fp32 throughout (the router is kept in higher precision than the
+// experts, "Chapter 19", §19.6.2 table):
+//   R1 router_logits: partial logits over a slice of d, for a tile of tokens.
+//      The d axis is split into S slices when there are too few token tiles to
+//      fill the GPU (decode batches), so every SM streams part of W_router.
+//      N <= 32: lanes split d (8 consecutive inputs per lane, 16-byte loads),
+//      each lane keeps TPW tokens x N logits in registers, and a butterfly
+//      reduction ends the tile. N > 32: lanes split the experts (lane owns
+//      experts lane, lane+32, ...), each warp owns 4 tokens, and 32-wide chunks
+//      of hidden and W_router are staged in shared memory with the next chunk
+//      prefetched into registers while the current one is consumed.
+//   R2 router_topk: one warp per token sums the S partials in a fixed order
+//      (deterministic), adds the router bias, scores, and selects K by a
+//      K-round shuffle argmax over (key desc, expert asc); slot k ends in lane k.
 #include <math.h>
 
 #include "common.cuh"
@@ -21,186 +29,340 @@
 namespace moe {
 namespace {
 
-constexpr int kRouterWarps = 8;
-constexpr int kTokPerWarp = 4;
-constexpr int kTokPerCta = kRouterWarps * kTokPerWarp;  // 32
-constexpr int kDChunk = 32;
+constexpr int kWarps = 8;
+
+template <typename XT>
+__device__ __forceinline__ void load8(const XT* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
 
 template <typename T>
-__device__ __forceinline__ float load_as_float(const T* p);
+__device__ __forceinline__ float to_f(T v);
 template <>
-__device__ __forceinline__ float load_as_float<float>(const float* p) {
-  return *p;
-}
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <>
-__device__ __forceinline__ float load_as_float<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat162float(*p);
-}
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// EPL: experts per lane (N > 32), LPE: lanes per expert (N <= 32; d split).
-template <int EPL, int LPE, typename XT>
-__global__ void __launch_bounds__(kRouterWarps * 32) router_topk_kernel(const RouterArgs a) {
-  constexpr int NCOL = (LPE == 1) ? 32 * EPL : 32 / LPE;  // staged router columns
-  __shared__ float ws[kDChunk][NCOL];
-  __shared__ float xs[kTokPerCta][kDChunk];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t t0 = (int64_t)blockIdx.x * kTokPerCta;
-  const XT* __restrict__ x = static_cast<const XT*>(a.hidden);
+// ---------------------------------------------------------------- R1, N <= 32
+// NP: N rounded up to a power of two; TPW tokens per warp.
+template <int NP, int TPW, typename XT>
+__global__ void __launch_bounds__(kWarps * 32) logits_small_n_kernel(const RouterArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N, d = a.d;
-
-  const int ecol = (LPE == 1) ? lane : (lane % NCOL);  // lane's first expert column
-  const int jgrp = (LPE == 1) ? 0 : (lane / NCOL);     // lane's d sub-lattice
-
-  float acc[kTokPerWarp][EPL];
+  const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * TPW;
+  if (t0 >= a.T) return;
+  const int s = blockIdx.y;
+  const int j_begin = s * a.d_slice, j_end = min(d, j_begin + a.d_slice);
+  const XT* x = static_cast<const XT*>(a.hidden);
+  float acc[TPW][NP];
 #pragma unroll
-  for (int t = 0; t < kTokPerWarp; ++t)
+  for (int t = 0; t < TPW; ++t)
+#pragma unroll
+    for (int e = 0; e < NP; ++e) acc[t][e] = 0.f;
+  const bool vec_w = (N == NP) && (NP % 4 == 0);
+  for (int j0 = j_begin + lane * 8; j0 < j_end; j0 += 256) {
+    float xv[TPW][8];
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) {
+      if (t0 + t < a.T) load8<XT>(x + (t0 + t) * d + j0, xv[t]);
+      else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xv[t][q] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float* wrow = a.w_router + (int64_t)(j0 + q) * N;
+      float w[NP];
+      if (vec_w) {
+#pragma unroll
+        for (int e = 0; e < NP; e += 4) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(wrow + e));
+          w[e] = v.x; w[e + 1] = v.y; w[e + 2] = v.z; w[e + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < NP; ++e) w[e] = (e < N) ? __ldg(wrow + e) : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < TPW; ++t)
+#pragma unroll
+        for (int e = 0; e < NP; ++e) acc[t][e] = fmaf(xv[t][q], w[e], acc[t][e]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TPW; ++t)
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], off);
+  float* part = a.partial + (int64_t)s * a.T * N;
+#pragma unroll
+  for (int t = 0; t < TPW; ++t) {
+    if (t0 + t >= a.T) break;
+    float v = 0.f;
+#pragma unroll
+    for (int e = 0; e < NP; ++e)
+      if (e == lane) v = acc[t][e];
+    if (lane < N) part[(t0 + t) * N + lane] = v;
+  }
+}
+
+// ---------------------------------------------------------------- R1, N > 32
+constexpr int kTokPerWarpL = 4;
+constexpr int kTokPerCtaL = kWarps * kTokPerWarpL;  // 32
+constexpr int kDChunk = 32;
+
+template <int EPL, typename XT>
+__global__ void __launch_bounds__(kWarps * 32) logits_large_n_kernel(const RouterArgs a) {
+  constexpr int NCOL = 32 * EPL;
+  constexpr int W_PER_THR = kDChunk * NCOL / (kWarps * 32);       // EPL * 4
+  constexpr int X_PER_THR = kTokPerCtaL * kDChunk / (kWarps * 32);  // 4
+  __shared__ float ws[kDChunk][NCOL];
+  __shared__ float xs[kTokPerCtaL][kDChunk];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t t0 = (int64_t)blockIdx.x * kTokPerCtaL;
+  const int N = a.N, d = a.d;
+  const int s = blockIdx.y;
+  const int j_begin = s * a.d_slice, j_end = min(d, j_begin + a.d_slice);
+  const XT* x = static_cast<const XT*>(a.hidden);
+
+  float acc[kTokPerWarpL][EPL];
+#pragma unroll
+  for (int t = 0; t < kTokPerWarpL; ++t)
 #pragma unroll
     for (int i = 0; i < EPL; ++i) acc[t][i] = 0.f;
 
-  for (int j0 = 0; j0 < d; j0 += kDChunk) {
-    for (int i = tid; i < kDChunk * NCOL; i += kRouterWarps * 32) {
+  float wr[W_PER_THR], xr[X_PER_THR];
+  auto fetch = [&](int j0) {
+#pragma unroll
+    for (int q = 0; q < W_PER_THR; ++q) {
+      const int i = tid + q * kWarps * 32;
       const int j = i / NCOL, e = i % NCOL;
-      ws[j][e] = (e < N && j0 + j < d) ? a.w_router[(int64_t)(j0 + j) * N + e] : 0.f;
+      wr[q] = (e < N && j0 + j < j_end) ? __ldg(a.w_router + (int64_t)(j0 + j) * N + e) : 0.f;
     }
-    for (int i = tid; i < kTokPerCta * kDChunk; i += kRouterWarps * 32) {
+#pragma unroll
+    for (int q = 0; q < X_PER_THR; ++q) {
+      const int i = tid + q * kWarps * 32;
       const int tk = i / kDChunk, j = i % kDChunk;
       const int64_t t = t0 + tk;
-      xs[tk][j] = (t < a.T && j0 + j < d) ? load_as_float<XT>(x + t * d + j0 + j) : 0.f;
+      xr[q] = (t < a.T && j0 + j < j_end) ? to_f<XT>(x[t * d + j0 + j]) : 0.f;
     }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int q = 0; q < W_PER_THR; ++q) {
+      const int i = tid + q * kWarps * 32;
+      ws[i / NCOL][i % NCOL] = wr[q];
+    }
+#pragma unroll
+    for (int q = 0; q < X_PER_THR; ++q) {
+      const int i = tid + q * kWarps * 32;
+      xs[i / kDChunk][i % kDChunk] = xr[q];
+    }
+  };
+  fetch(j_begin);
+  for (int j0 = j_begin; j0 < j_end; j0 += kDChunk) {
+    __syncthreads();  // previous chunk fully consumed
+    stash();
     __syncthreads();
-#pragma unroll 4
-    for (int jj = 0; jj < kDChunk / LPE; ++jj) {
-      const int j = jj * LPE + jgrp;
+    if (j0 + kDChunk < j_end) fetch(j0 + kDChunk);  // in flight during the FMAs below
+#pragma unroll 8
+    for (int j = 0; j < kDChunk; ++j) {
       float w[EPL];
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) w[i] = ws[j][ecol + 32 * i];
+      for (int i = 0; i < EPL; ++i) w[i] = ws[j][lane + 32 * i];
 #pragma unroll
-      for (int t = 0; t < kTokPerWarp; ++t) {
-        const float xv = xs[warp * kTokPerWarp + t][j];
+      for (int t = 0; t < kTokPerWarpL; ++t) {
+        const float xv = xs[warp * kTokPerWarpL + t][j];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) acc[t][i] = fmaf(xv, w[i], acc[t][i]);
       }
     }
-    __syncthreads();
   }
-  if (LPE > 1) {
+  float* part = a.partial + (int64_t)s * a.T * N;
 #pragma unroll
-    for (int off = NCOL; off < 32; off <<= 1)
-#pragma unroll
-      for (int t = 0; t < kTokPerWarp; ++t) acc[t][0] += __shfl_xor_sync(0xffffffffu, acc[t][0], off);
-  }
-
-  const int K = a.K;
-#pragma unroll
-  for (int tk = 0; tk < kTokPerWarp; ++tk) {
-    const int64_t t = t0 + warp * kTokPerWarp + tk;
-    if (t >= a.T) continue;  // uniform across the warp
-    float key[EPL], sc[EPL];
-    bool valid[EPL];
+  for (int t = 0; t < kTokPerWarpL; ++t) {
+    const int64_t tt = t0 + warp * kTokPerWarpL + t;
+    if (tt >= a.T) break;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      const int e = ecol + 32 * i;
-      valid[i] = (e < N) && (jgrp == 0);
-      float l = acc[tk][i];
-      if (valid[i] && a.router_bias) l += a.router_bias[e];
-      if (valid[i] && a.logits) a.logits[t * N + e] = l;
-      if (a.score_fn == 0) {
-        sc[i] = l;
-        key[i] = l;
-      } else {
-        const float s = 1.0f / (1.0f + expf(-l));
-        sc[i] = s;
-        key[i] = s + ((valid[i] && a.sel_bias) ? a.sel_bias[e] : 0.f);
-      }
-    }
-    uint32_t taken = 0;
-    int my_e = -1;
-    float my_sc = 0.f;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = ecol + 32 * i;
-        if (valid[i] && !((taken >> i) & 1u) && (key[i] > bv || (key[i] == bv && e < be))) {
-          bv = key[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      // Owner of expert be: lane (be % 32) slot be/32 (N > 32) or lane be (N <= 32).
-      const int owner = (LPE == 1) ? (be & 31) : be;
-      const int slot = (LPE == 1) ? (be >> 5) : 0;
-      float v = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (i == slot) v = sc[i];
-      if (lane == owner) taken |= 1u << slot;
-      v = __shfl_sync(0xffffffffu, v, owner & 31);
-      if (lane == k) {
-        my_e = be;
-        my_sc = v;
-      }
-    }
-    float w;
-    if (a.score_fn == 0) {
-      const float lmax = __shfl_sync(0xffffffffu, my_sc, 0);  // slot 0 holds the largest logit
-      const float ex = (lane < K) ? expf(my_sc - lmax) : 0.f;
-      float z = 0.f;
-      if (a.renormalize) {
-        z = ex;
-      } else {
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-          if (valid[i]) z += expf(sc[i] - lmax);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-      w = ex / z;
-    } else {
-      float z = (lane < K) ? my_sc : 0.f;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-      w = a.renormalize ? my_sc / z : my_sc;
-    }
-    if (lane < K) {
-      a.topk_idx[t * K + lane] = my_e;
-      a.topk_w[t * K + lane] = w;
+      const int e = lane + 32 * i;
+      if (e < N) part[tt * N + e] = acc[t][i];
     }
   }
 }
 
+// ---------------------------------------------------------------- R2
+template <int EPL>
+__global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const int N = a.N, K = a.K;
+  float key[EPL], sc[EPL];
+  bool valid[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    valid[i] = e < N;
+    float l = 0.f;
+    if (valid[i]) {
+      for (int s = 0; s < a.splits; ++s) l += a.partial[((int64_t)s * a.T + t) * N + e];
+      if (a.router_bias) l += a.router_bias[e];
+      if (a.logits) a.logits[t * N + e] = l;
+    }
+    if (a.score_fn == 0) {
+      sc[i] = l;
+      key[i] = l;
+    } else {
+      const float sg = 1.0f / (1.0f + expf(-l));
+      sc[i] = sg;
+      key[i] = sg + ((valid[i] && a.sel_bias) ? a.sel_bias[e] : 0.f);
+    }
+  }
+  uint32_t taken = 0;
+  int my_e = -1;
+  float my_sc = 0.f;
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (valid[i] && !((taken >> i) & 1u) && (key[i] > bv || (key[i] == bv && e < be))) {
+        bv = key[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    const int owner = be & 31, slot = be >> 5;
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (i == slot) v = sc[i];
+    if (lane == owner) taken |= 1u << slot;
+    v = __shfl_sync(0xffffffffu, v, owner);
+    if (lane == k) {
+      my_e = be;
+      my_sc = v;
+    }
+  }
+  float w;
+  if (a.score_fn == 0) {
+    const float lmax = __shfl_sync(0xffffffffu, my_sc, 0);  // slot 0 holds the largest logit
+    const float ex = (lane < K) ? expf(my_sc - lmax) : 0.f;
+    float z = 0.f;
+    if (a.renormalize) {
+      z = ex;
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (valid[i]) z += expf(sc[i] - lmax);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    w = ex / z;
+  } else {
+    float z = (lane < K) ? my_sc : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    w = a.renormalize ? my_sc / z : my_sc;
+  }
+  if (lane < K) {
+    a.topk_idx[t * K + lane] = my_e;
+    a.topk_w[t * K + lane] = w;
+  }
+}
+
 template <typename XT>
-cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s) {
-  const dim3 grid((unsigned)((a.T + kTokPerCta - 1) / kTokPerCta));
-  const dim3 block(kRouterWarps * 32);
+cudaError_t launch_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_t s) {
+  const dim3 grid((unsigned)pl.token_tiles, (unsigned)pl.splits), block(kWarps * 32);
   const int N = a.N;
-  if (N <= 1) router_topk_kernel<1, 32, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 2) router_topk_kernel<1, 16, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 4) router_topk_kernel<1, 8, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 8) router_topk_kernel<1, 4, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 16) router_topk_kernel<1, 2, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 32) router_topk_kernel<1, 1, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 64) router_topk_kernel<2, 1, XT><<<grid, block, 0, s>>>(a);
-  else if (N <= 128) router_topk_kernel<4, 1, XT><<<grid, block, 0, s>>>(a);
-  else router_topk_kernel<8, 1, XT><<<grid, block, 0, s>>>(a);
+  if (N <= 32) {
+    if (pl.np == 1) logits_small_n_kernel<1, 4, XT><<<grid, block, 0, s>>>(a);
+    else if (pl.np == 2) logits_small_n_kernel<2, 4, XT><<<grid, block, 0, s>>>(a);
+    else if (pl.np == 4) logits_small_n_kernel<4, 4, XT><<<grid, block, 0, s>>>(a);
+    else if (pl.np == 8) logits_small_n_kernel<8, 4, XT><<<grid, block, 0, s>>>(a);
+    else if (pl.np == 16) logits_small_n_kernel<16, 2, XT><<<grid, block, 0, s>>>(a);
+    else logits_small_n_kernel<32, 1, XT><<<grid, block, 0, s>>>(a);
+  } else if (N <= 64) {
+    logits_large_n_kernel<2, XT><<<grid, block, 0, s>>>(a);
+  } else if (N <= 128) {
+    logits_large_n_kernel<4, XT><<<grid, block, 0, s>>>(a);
+  } else {
+    logits_large_n_kernel<8, XT><<<grid, block, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_router(const RouterArgs& a, bool hidden_bf16, cudaStream_t s) {
-  if (a.T == 0) return cudaSuccess;
-  return hidden_bf16 ? launch_router_t<__nv_bfloat16>(a, s) : launch_router_t<float>(a, s);
+RouterPlan router_plan(int64_t T, int32_t d, int32_t N) {
+  // Aim at ~2 CTAs per SM of a 148-SM part; the plan depends on sizes only so
+  // that workspace sizes are a host-side function of the problem.
+  constexpr int64_t kTargetCtas = 296;
+  RouterPlan pl{};
+  int chunk;
+  if (N <= 32) {
+    pl.np = 1;
+    while (pl.np < N) pl.np <<= 1;
+    const int tpw = pl.np <= 8 ? 4 : (pl.np == 16 ? 2 : 1);
+    pl.token_tiles = (T + (int64_t)kWarps * tpw - 1) / ((int64_t)kWarps * tpw);
+    chunk = 256;  // 32 lanes x 8 inputs
+  } else {
+    pl.np = 0;
+    pl.token_tiles = (T + kTokPerCtaL - 1) / kTokPerCtaL;
+    chunk = kDChunk;
+  }
+  const int64_t max_splits = (d + chunk - 1) / chunk;
+  int64_t splits = 1;
+  if (pl.token_tiles > 0 && pl.token_tiles < kTargetCtas) splits = (kTargetCtas + pl.token_tiles - 1) / pl.token_tiles;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  int64_t slice = (d + splits - 1) / splits;
+  slice = (slice + chunk - 1) / chunk * chunk;
+  pl.d_slice = (int32_t)slice;
+  pl.splits = (int32_t)((d + slice - 1) / slice);
+  return pl;
+}
+
+cudaError_t launch_router(const RouterArgs& a0, bool hidden_bf16, cudaStream_t s) {
+  if (a0.T == 0) return cudaSuccess;
+  const RouterPlan pl = router_plan(a0.T, a0.d, a0.N);
+  RouterArgs a = a0;
+  a.splits = pl.splits;
+  a.d_slice = pl.d_slice;
+  cudaError_t e = hidden_bf16 ? launch_logits<__nv_bfloat16>(a, pl, s) : launch_logits<float>(a, pl, s);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((a.T + kWarps - 1) / kWarps);
+  if (a.N <= 32) topk_kernel<1><<<grid, kWarps * 32, 0, s>>>(a);
+  else if (a.N <= 64) topk_kernel<2><<<grid, kWarps * 32, 0, s>>>(a);
+  else if (a.N <= 128) topk_kernel<4><<<grid, kWarps * 32, 0, s>>>(a);
+  else topk_kernel<8><<<grid, kWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -38,7 +38,7 @@ def test_status_strings():
 def test_workload_problems_are_valid(cfg):
     p = B.problem(cfg)
     assert B.problem_check(p) == 0
-    for call in (B.CALL_PERMUTE, B.CALL_GROUPED_SWIGLU, B.CALL_LAYER_FORWARD):
+    for call in (B.CALL_PERMUTE, B.CALL_GROUPED_SWIGLU, B.CALL_LAYER_FORWARD, B.CALL_ROUTER):
         n = B.workspace_bytes(p, call)
         assert n > 0 and n % 256 == 0
     assert B.workspace_bytes(p, B.CALL_LAYER_FORWARD) > B.workspace_bytes(p, B.CALL_PERMUTE)
@@ -72,3 +72,18 @@ def test_workspace_grows_with_tokens():
     # the fused layer needs x_perm, h and the fp32 accumulator at least
     m = inputs.MIXTRAL
     assert b >= m.T * m.K * (m.d + m.F) * 2 + m.T * m.d * 4
+
+
+def test_layer_kernel_count():
+    assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL)) == 10
+    assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, T=0)) == 1
+    assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, top_k=0)) == 0
+
+
+@pytest.mark.parametrize("cfg", list(inputs.CONFIGS.values()), ids=list(inputs.CONFIGS))
+def test_workspace_sizing_for_empty_and_single_token_batches(cfg):
+    for T in (0, 1, 3):
+        p = B.problem(cfg, T=T)
+        assert B.problem_check(p) == 0
+        for call in (B.CALL_PERMUTE, B.CALL_GROUPED_SWIGLU, B.CALL_LAYER_FORWARD, B.CALL_ROUTER):
+            assert B.workspace_bytes(p, call) >= 256

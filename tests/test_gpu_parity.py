@@ -42,6 +42,10 @@ MID = {
     "N_K_1": inputs.MoEConfig("N_K_1", T=129, d=128, N=1, K=1, F=256),
     "T1": inputs.MoEConfig("T1", T=1, d=256, N=16, K=4, F=128),
     "d72_tail": inputs.MoEConfig("d72_tail", T=150, d=72, N=6, K=2, F=40),
+    # router d-split paths (few token tiles): large N and small non-power-of-two N
+    "decode_like_T3": inputs.MoEConfig("decode_like_T3", T=3, d=1024, N=128, K=8, F=64),
+    "small_n_split_T5": inputs.MoEConfig("small_n_split_T5", T=5, d=2048, N=6, K=2, F=64,
+                                         hidden_dtype="f32"),
 }
 
 
@@ -108,7 +112,7 @@ def test_layer_is_repeatable():
 
 # --------------------------------------------------------------------------- router
 ROUTER_CASES = ["tiny", "ragged_softmax", "dsv3_like", "no_renorm_sigmoid", "no_renorm_softmax",
-                "K_equals_N", "N_K_1", "T1"]
+                "K_equals_N", "N_K_1", "T1", "decode_like_T3", "small_n_split_T5"]
 
 
 @pytest.mark.parametrize("name", ROUTER_CASES)
