@@ -182,6 +182,41 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx,
                          void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_permute_static: the same route and pack as moe_permute, for callers that
+ * cannot allocate device memory. The source pages have no counterpart to this
+ * entry point; it exists only for how the library is deployed.
+ *
+ * Who needs it: a caller that must not call cudaMalloc (or any allocator) on
+ * the routing path, e.g. a server that reserves all GPU memory up front and
+ * accounts for every byte, a plug-in inside a framework that owns the device
+ * allocator, or a latency-critical loop that cannot afford cudaMalloc's cost
+ * and implicit device synchronisation. moe_permute needs a workspace for its
+ * per-chunk expert counts; here that scratch is a fixed array compiled into
+ * the library, so the caller passes only the inputs and outputs below, with
+ * the same meaning, layout and results as in moe_permute.
+ *
+ * Limit: n_experts * ceil(T / 32) <= MOE_PERMUTE_STATIC_MAX_CHUNK_COUNTS
+ * (e.g. 256 experts with up to 8192 tokens, 8 experts with up to 262144);
+ * larger problems return MOE_ERR_UNSUPPORTED and enqueue nothing. The array
+ * (256 KB + 256 bytes) is reserved on every GPU that loads the library, until
+ * the process exits. The entry point allocates nothing.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call on a device shares the one array and leaves its contents
+ * behind: calls whose work overlaps on the GPU (different streams or host
+ * threads without ordering between them) race and give wrong results, so
+ * order them. The call clears the array's error word itself. There is no
+ * error word to read afterwards: an expert index outside [0, N) is skipped,
+ * and shows as offsets[N] < T*K.
+ */
+#define MOE_PERMUTE_STATIC_MAX_CHUNK_COUNTS 65536
+moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t* topk_idx,
+                                const void* hidden, int32_t* counts,
+                                int32_t* offsets, int32_t* perm_src,
+                                int32_t* inv_row, void* x_perm, void* stream);
+
+/*
  * The routed experts' SwiGLU FFNs over the packed rows, as grouped GEMMs on
  * the tensor cores (bf16 operands, fp32 accumulation):
  *   for every expert e and row r in [offsets[e], offsets[e+1]):
