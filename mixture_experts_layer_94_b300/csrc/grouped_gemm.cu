@@ -6,6 +6,9 @@
 //   down phase:     y = h W_down^T, then either
 //                   out_acc[token] += w_{t,k} * y   (fused gate-weighted combine)
 //                   or y_perm = bf16(y)             (step-wise path)
+//   router phase:   partial logits = hidden x (one exact bf16 part of the fp32
+//                   router matrix) over a slice of d, written in fp32; the
+//                   router's top-K kernel sums the partials in a fixed order
 // The expert FFN is the SwiGLU reading of the three-matrix expert ("Mixture of
 // Experts Explained: Conditional Computation From Zero", "The slot it replaces,
 // and what an expert is"); the weighted sum back to token order is "Chapter 19:
@@ -75,6 +78,21 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmArgs& a) {
   return ti;
 }
 
+struct RouterTile {
+  int m_blk, split, part, kb0, kb1;
+};
+
+__device__ __forceinline__ RouterTile decode_router_tile(int tile, const GemmArgs& a) {
+  RouterTile r;
+  r.m_blk = tile % a.r_m_tiles;
+  r.split = tile / a.r_m_tiles;
+  r.part = r.split / a.r_dslices;
+  const int slice = r.split - r.part * a.r_dslices;
+  r.kb0 = slice * a.r_kb_per_slice;
+  r.kb1 = min(a.r_nkb_d, r.kb0 + a.r_kb_per_slice);
+  return r;
+}
+
 __device__ __forceinline__ bool wait_raw(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
@@ -106,7 +124,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * (2 * kStages + 5) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = __ldg(a.tile_start + a.G);
+  const int total = (PHASE == kPhaseRouter) ? a.r_tiles : __ldg(a.tile_start + a.G);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -143,7 +161,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool aborted = false;
-      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total && !aborted && PHASE == kPhaseRouter; tile += gridDim.x) {
+        // Router: A = hidden rows of the m block, B = the router part's columns.
+        const RouterTile rt = decode_router_tile(tile, a);
+        const uint32_t bytes = kStageA + (uint32_t)a.r_np * kBK * 2u;
+        for (int kb = rt.kb0; kb < rt.kb1; ++kb) {
+          if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) {
+            aborted = true;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+          ptx::tma_load_2d(sA + stage * kStageA, &tmA0, full_bar(stage), kb * kBK, rt.m_blk * kBM);
+          ptx::tma_load_2d(sB + stage * kStageB, &tmB0, full_bar(stage), rt.part * a.r_d_pad + kb * kBK, 0);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int tile = blockIdx.x; tile < total && !aborted && PHASE != kPhaseRouter; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, a);
         const int kind = ti.g.kind;
         const CUtensorMap* mA = kind ? &tmA1 : &tmA0;
@@ -189,9 +226,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool aborted = false;
+      const uint32_t idesc = (PHASE == kPhaseRouter) ? a.r_idesc : kIdesc;
       for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(tile, a);
-        const int nkb = a.k_blocks[ti.g.kind];
+        int nkb;
+        if (PHASE == kPhaseRouter) {
+          const RouterTile rt = decode_router_tile(tile, a);
+          nkb = rt.kb1 - rt.kb0;
+        } else {
+          nkb = a.k_blocks[decode_tile(tile, a).g.kind];
+        }
         if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
@@ -205,7 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t bdesc = ptx::smem_desc_sw128(sB + stage * kStageB);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
           ptx::mma_commit(empty_bar(stage));
           if (++stage == kStages) {
             stage = 0;
@@ -231,7 +274,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total && PHASE == kPhaseRouter; tile += gridDim.x) {
+      // Router: fp32 partial logits of this (m block, split) for rows < T, experts < N.
+      const RouterTile rt = decode_router_tile(tile, a);
+      if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
+      ptx::tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
+      const int64_t t = (int64_t)rt.m_blk * kBM + row_in_tile;
+      float* prow = a.r_partial + ((int64_t)rt.split * a.r_T + (t < a.r_T ? t : 0)) * a.r_N;
+      const bool vec = (a.r_N & 3) == 0;
+#pragma unroll 1
+      for (int c = 0; c < a.r_np; c += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(tacc + c, v);
+        ptx::tmem_wait_ld();
+        if (t < a.r_T) {
+          if (vec) {
+#pragma unroll
+            for (int q = 0; q < 16; q += 4)
+              if (c + q < a.r_N)
+                *reinterpret_cast<float4*>(prow + c + q) =
+                    make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
+                                __uint_as_float(v[q + 3]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              if (c + q < a.r_N) prow[c + q] = __uint_as_float(v[q]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    for (int tile = blockIdx.x; tile < total && PHASE != kPhaseRouter; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, a);
       const int kind = ti.g.kind;
       if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
@@ -369,6 +448,7 @@ cudaError_t launch_grouped_gemm(int phase, int epilogue, const GemmMaps& maps, c
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = (int)(tile_bound < sms ? (tile_bound < 1 ? 1 : tile_bound) : sms);
+  if (phase == kPhaseRouter) return launch_t<kPhaseRouter, kEpiLogits>(maps, a, grid, s);
   if (phase == kPhaseGateUp) return launch_t<kPhaseGateUp, kEpiSwiGLU>(maps, a, grid, s);
   if (epilogue == kEpiScatter) return launch_t<kPhaseDown, kEpiScatter>(maps, a, grid, s);
   return launch_t<kPhaseDown, kEpiStoreY>(maps, a, grid, s);

@@ -20,18 +20,31 @@ struct RouterArgs {
   float* topk_w;
   float* logits;       // optional [T][N] output
   float* partial;      // scratch [splits][T][N]
+  __nv_bfloat16* w3;   // scratch for the tensor-core path: [np][3 * d_pad]
   int32_t splits, d_slice;  // filled by launch_router
 };
 
-// How the router logits kernel tiles the problem: token tiles x d slices.
+// How the router computes its logits.
+//  tensor == false: CUDA-core kernel, token tiles x `splits` d slices of
+//    `d_slice` inputs (np = N rounded to a power of two when N <= 32).
+//  tensor == true (bf16 hidden): tcgen05 GEMM of hidden [T, d] with the router
+//    matrix split exactly into three bf16 parts (hi + mid + lo = the fp32
+//    value), K = 3 parts x `dslices` slices of `kb_per_slice` 64-wide blocks;
+//    splits = 3 * dslices partial logits, MMA N = np (multiple of 16).
 struct RouterPlan {
+  bool tensor;
   int64_t token_tiles;
-  int32_t splits;   // number of d slices (partial logits summed in order)
-  int32_t d_slice;  // inputs per slice
-  int32_t np;       // N <= 32: N rounded up to a power of two; else 0
+  int32_t splits;
+  int32_t d_slice;
+  int32_t np;
+  int32_t dslices, kb_per_slice, nkb_d, d_pad;
 };
-RouterPlan router_plan(int64_t T, int32_t d, int32_t N);
+RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16);
 cudaError_t launch_router(const RouterArgs& a, bool hidden_bf16, cudaStream_t s);
+
+// bf16 row-major matrix [rows][inner] as a TMA tensor map: box [box_rows][64],
+// 128-byte swizzle, zero fill out of bounds. False if the driver refuses it.
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
 struct PermuteArgs {
   int64_t T;
@@ -61,8 +74,8 @@ struct ScheduleArgs {
 };
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s);
 
-enum GemmPhase { kPhaseGateUp = 0, kPhaseDown = 1 };
-enum GemmEpilogue { kEpiSwiGLU = 0, kEpiScatter = 1, kEpiStoreY = 2 };
+enum GemmPhase { kPhaseGateUp = 0, kPhaseDown = 1, kPhaseRouter = 2 };
+enum GemmEpilogue { kEpiSwiGLU = 0, kEpiScatter = 1, kEpiStoreY = 2, kEpiLogits = 3 };
 
 struct GemmArgs {
   const GroupDesc* groups;
@@ -81,6 +94,12 @@ struct GemmArgs {
   __nv_bfloat16* y;      // store epilogue: bf16 [rows][d]
   int32_t d;
   uint32_t* err;
+  // Router phase: one group of all T tokens; tile = (m block, split) with
+  // split = part * r_dslices + slice.
+  int32_t r_tiles, r_m_tiles, r_dslices, r_kb_per_slice, r_nkb_d, r_d_pad, r_np, r_N;
+  uint32_t r_idesc;
+  int64_t r_T;
+  float* r_partial;       // [3 * r_dslices][T][N]
 };
 
 struct GemmMaps {

@@ -19,7 +19,7 @@ constexpr int64_t kInt32Max = 2147483647;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t err, chunk, groups, ts_gu, ts_dn, router;
+  size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_bf16, h, h_sh, out_acc;
   size_t total;
 };
@@ -41,8 +41,9 @@ Layout make_layout(const moe_problem_t& p, int call) {
   L.ts_gu = take((size_t)(G + 1) * 4);
   L.ts_dn = take((size_t)(G + 1) * 4);
   if (call == MOE_CALL_ROUTER || call == MOE_CALL_LAYER_FORWARD) {
-    const RouterPlan rp = router_plan(T, p.d_model, p.n_experts);
+    const RouterPlan rp = router_plan(T, p.d_model, p.n_experts, p.hidden_dtype == MOE_BF16);
     L.router = take((size_t)rp.splits * T * p.n_experts * 4);
+    if (rp.tensor) L.router_w3 = take((size_t)rp.np * 3 * rp.d_pad * 2);
   }
   if (call == MOE_CALL_LAYER_FORWARD) {
     L.topk_idx = take((size_t)TK * 4);
@@ -79,9 +80,17 @@ bool have_encode() {
   return g_encode != nullptr;
 }
 
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  return moe::make_tmap_bf16(m, ptr, inner, rows, box_rows);
+}
+
+}  // namespace
+
+namespace moe {
 // bf16 matrix [rows][inner] (row stride = inner elements), box [box_rows][64],
 // 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  if (!have_encode()) return false;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
@@ -90,6 +99,9 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+}  // namespace moe
+
+namespace {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -260,7 +272,7 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const f
   if (!aligned16(hidden) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   RouterArgs a{p->T, p->d_model, p->n_experts, p->top_k, p->score_fn, p->renormalize,
                hidden, w_router, router_bias, sel_bias, topk_idx, topk_w, logits_opt,
-               at<float>(ws, L.router), 0, 0};
+               at<float>(ws, L.router), at<__nv_bfloat16>(ws, L.router_w3), 0, 0};
   return cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
 }
 
@@ -389,7 +401,8 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   MOE_TRY(record(ev, 0, s));
   if (!aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
   RouterArgs ra{T, p->d_model, N, K, p->score_fn, p->renormalize, hidden, w->w_router,
-                w->router_bias, w->sel_bias, topk_idx, topk_w, nullptr, at<float>(ws, L.router), 0, 0};
+                w->router_bias, w->sel_bias, topk_idx, topk_w, nullptr, at<float>(ws, L.router),
+                at<__nv_bfloat16>(ws, L.router_w3), 0, 0};
   MOE_TRY(cuda_status(launch_router(ra, hbf16, s)));
   MOE_TRY(record(ev, 1, s));
 
@@ -480,9 +493,9 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
 int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   if (moe_problem_check(p) != MOE_OK) return 0;
   if (p->T == 0) return 1;  // the histogram scan that writes zero counts
-  // router logits, router top-K, histogram, scan, scatter, gather, schedule,
-  // gate/up GEMM, down GEMM, finalise
-  return 10;
+  // router logits (bf16 hidden: router split + router GEMM), router top-K,
+  // histogram, scan, scatter, gather, schedule, gate/up GEMM, down GEMM, finalise
+  return p->hidden_dtype == MOE_BF16 ? 11 : 10;
 }
 
 moe_status_t moe_get_device_status(void* ws, void* stream) {

@@ -7,8 +7,10 @@
 // logits equals full softmax + renormalisation; §19.3.4: the balancing bias
 // shifts the scores used for selection only.
 //
-// Two kernels, fp32 throughout (the router is kept in higher precision than the
-// experts, "Chapter 19", §19.6.2 table):
+// fp32 throughout (the router is kept in higher precision than the experts,
+// "Chapter 19", §19.6.2 table). For a bf16 hidden the logits run on the tensor
+// cores (the grouped GEMM's router phase, see split_router_kernel below); for
+// an fp32 hidden, on CUDA cores:
 //   R1 router_logits: partial logits over a slice of d, for a tile of tokens.
 //      The d axis is split into S slices when there are too few token tiles to
 //      fill the GPU (decode batches), so every SM streams part of W_router.
@@ -25,6 +27,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -38,24 +41,11 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
   const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-    v[2 * i] = f.x;
-    v[2 * i + 1] = f.y;
-  }
-}
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
 template <>
 __device__ __forceinline__ float to_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // ---------------------------------------------------------------- R1, N <= 32
 // NP: N rounded up to a power of two; TPW tokens per warp.
@@ -297,6 +287,66 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- tensor-core path
+// W3[e][part * d_pad + j] for part 0, 1, 2 = hi, mid, lo with
+//   hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid),  w = W_router[j][e].
+// hi + mid + lo == w exactly for every normal fp32 w (8 + 8 + 8 significand
+// bits), and each bf16 x bf16 product is exact in fp32, so hidden x W3 over the
+// three parts is an fp32 dot product. Rows e >= N and columns j >= d are zero.
+// 32 x 32 tiles through shared memory: coalesced reads along e, writes along j.
+__global__ void __launch_bounds__(256) split_router_kernel(const float* __restrict__ w, int d, int N, int np,
+                                                           int d_pad, __nv_bfloat16* __restrict__ w3) {
+  __shared__ float tile[32][33];
+  const int j0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int r = ty; r < 32; r += 8) {
+    const int j = j0 + r, e = e0 + tx;
+    tile[r][tx] = (j < d && e < N) ? w[(int64_t)j * N + e] : 0.f;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int e = e0 + r, j = j0 + tx;
+    if (e < np && j < d_pad) {
+      const float v = tile[tx][r];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const float r1 = v - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+      __nv_bfloat16* row = w3 + (int64_t)e * 3 * d_pad;
+      row[j] = hi;
+      row[d_pad + j] = mid;
+      row[2 * d_pad + j] = lo;
+    }
+  }
+}
+
+cudaError_t launch_tensor_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_t s) {
+  const dim3 sgrid((unsigned)((pl.d_pad + 31) / 32), (unsigned)((pl.np + 31) / 32));
+  split_router_kernel<<<sgrid, 256, 0, s>>>(a.w_router, a.d, a.N, pl.np, pl.d_pad, a.w3);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  GemmMaps m{};
+  if (!make_tmap_bf16(&m.a[0], a.hidden, (uint64_t)a.d, (uint64_t)a.T, kBM) ||
+      !make_tmap_bf16(&m.b[0], a.w3, (uint64_t)3 * pl.d_pad, (uint64_t)pl.np, (uint32_t)pl.np))
+    return cudaErrorInvalidValue;
+  m.a[1] = m.a[0];
+  m.b[1] = m.bu[0] = m.bu[1] = m.b[0];
+  GemmArgs g{};
+  g.err = nullptr;
+  g.r_m_tiles = (int32_t)pl.token_tiles;
+  g.r_dslices = pl.dslices;
+  g.r_kb_per_slice = pl.kb_per_slice;
+  g.r_nkb_d = pl.nkb_d;
+  g.r_d_pad = pl.d_pad;
+  g.r_np = pl.np;
+  g.r_N = a.N;
+  g.r_T = a.T;
+  g.r_tiles = (int32_t)(pl.token_tiles * pl.splits);
+  g.r_idesc = ptx::idesc_bf16_f32(128, pl.np);
+  g.r_partial = a.partial;
+  return launch_grouped_gemm(kPhaseRouter, kEpiLogits, m, g, g.r_tiles, s);
+}
+
 template <typename XT>
 cudaError_t launch_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_t s) {
   const dim3 grid((unsigned)pl.token_tiles, (unsigned)pl.splits), block(kWarps * 32);
@@ -320,11 +370,29 @@ cudaError_t launch_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_
 
 }  // namespace
 
-RouterPlan router_plan(int64_t T, int32_t d, int32_t N) {
+RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
   // Aim at ~2 CTAs per SM of a 148-SM part; the plan depends on sizes only so
   // that workspace sizes are a host-side function of the problem.
   constexpr int64_t kTargetCtas = 296;
   RouterPlan pl{};
+  if (hidden_bf16) {
+    // Tensor cores: one CTA per SM; tiles = 128-token blocks x 3 parts x slices.
+    constexpr int64_t kTargetTiles = 148;
+    pl.tensor = true;
+    pl.np = (N + 15) / 16 * 16;
+    pl.token_tiles = (T + kBM - 1) / kBM;
+    pl.nkb_d = (d + kBK - 1) / kBK;
+    pl.d_pad = pl.nkb_d * kBK;
+    int64_t slices = 1;
+    if (pl.token_tiles > 0 && pl.token_tiles * 3 < kTargetTiles)
+      slices = (kTargetTiles + pl.token_tiles * 3 - 1) / (pl.token_tiles * 3);
+    if (slices > pl.nkb_d) slices = pl.nkb_d;
+    pl.kb_per_slice = (int32_t)((pl.nkb_d + slices - 1) / slices);
+    pl.dslices = (pl.nkb_d + pl.kb_per_slice - 1) / pl.kb_per_slice;
+    pl.splits = 3 * pl.dslices;
+    pl.d_slice = pl.kb_per_slice * kBK;
+    return pl;
+  }
   int chunk;
   if (N <= 32) {
     pl.np = 1;
@@ -351,11 +419,11 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N) {
 
 cudaError_t launch_router(const RouterArgs& a0, bool hidden_bf16, cudaStream_t s) {
   if (a0.T == 0) return cudaSuccess;
-  const RouterPlan pl = router_plan(a0.T, a0.d, a0.N);
+  const RouterPlan pl = router_plan(a0.T, a0.d, a0.N, hidden_bf16);
   RouterArgs a = a0;
   a.splits = pl.splits;
   a.d_slice = pl.d_slice;
-  cudaError_t e = hidden_bf16 ? launch_logits<__nv_bfloat16>(a, pl, s) : launch_logits<float>(a, pl, s);
+  cudaError_t e = pl.tensor ? launch_tensor_logits(a, pl, s) : launch_logits<float>(a, pl, s);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((a.T + kWarps - 1) / kWarps);
   if (a.N <= 32) topk_kernel<1><<<grid, kWarps * 32, 0, s>>>(a);
