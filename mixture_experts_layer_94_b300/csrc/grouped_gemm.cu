@@ -16,22 +16,29 @@
 // weights"); the shared expert adds with weight 1 ("Mixture of Experts for LLM
 // Inference", "Shared experts").
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: per K block, one 128x64 activation box and one
-//              256x64 weight box (gate rows | up rows, or 256 down rows), 128-byte
-//              swizzled, into a 4-stage shared-memory ring (48 KB per stage).
+// Kernel structure (persistent, 192 threads per CTA, one CTA per SM):
+//   warp 0     TMA producer: per K block an activation box and a weight box,
+//              128-byte swizzled, into a shared-memory ring.
 //   warp 1     allocates 512 TMEM columns; one lane issues tcgen05.mma
-//              (M=128, N=256, K=16, bf16 -> fp32) into one of two 256-column
-//              accumulators and commits stage releases / tile completion to
-//              mbarriers.
+//              (bf16 -> fp32, N = 256) into one of two 256-column accumulators
+//              and commits stage releases / tile completion to mbarriers.
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
 //              32*(w%4)..+31, one output row per thread), apply the fused
-//              SwiGLU or weighted scatter-add, release the accumulator.
+//              SwiGLU, weighted scatter-add or logits store, release it.
+// PAIR == 1: a CTA computes 128-row tiles alone (M=128; 4-stage x 48 KB ring).
+// PAIR == 2: a cluster of two CTAs computes 256-row tiles with the CTA-pair
+//   MMA (M=256). Each CTA loads its own 128 activation rows and its own half of
+//   the 256 weight rows (the gate tile on the leader, the up tile on the peer;
+//   or two halves of the down rows) with ordinary, non-multicast TMA loads into
+//   its own 6-stage x 32 KB ring, and each CTA's TMEM receives its own 128
+//   rows. The leader's thread issues the MMA; stage releases and tile
+//   completion are signalled to both CTAs' barriers. Per CTA this halves the
+//   weight bytes pulled from L2 per FLOP and deepens the ring.
 // The double-buffered accumulator lets the epilogue of tile i overlap the MMAs
 // of tile i+1. Tiles are (group, m block, n block), n-major inside a group so
-// CTAs running side by side share weight tiles in L2; a CTA walks tiles
-// blockIdx.x, +gridDim.x, ... and finds each tile's group by binary search over
-// the device-built prefix of tile counts (no host round trip).
+// CTAs running side by side share weight tiles in L2; a CTA (pair) walks tiles
+// unit, unit + units, ... and finds each tile's group by binary search over the
+// device-built prefix of tile counts (no host round trip).
 // Every mbarrier wait is bounded: on a stall the kernel records a timeout in
 // the workspace error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -45,18 +52,22 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;
-constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
-constexpr uint32_t kStageB = 256 * kBK * 2;   // 32 KB
-constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KB: 128 activation rows x 64
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 256);
 constexpr uint64_t kDrainTimeoutNs = 50000000ull;  // 50 ms per in-flight copy on abort
-
 constexpr size_t kBarrierBytes = 256;
-constexpr size_t kGemmSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + kBarrierBytes;
+
+template <int PAIR>
+struct Cfg {
+  static constexpr int kStages = PAIR == 2 ? 6 : 4;
+  static constexpr uint32_t kStageB = PAIR == 2 ? 128 * kBK * 2 : 256 * kBK * 2;  // this CTA's weight rows
+  static constexpr uint32_t kStageBytes = kStageA + kStageB;
+  static constexpr int kTileRows = kBM * PAIR;
+  static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128 * PAIR, 256);
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + kBarrierBytes;
+};
 
 struct TileInfo {
   GroupDesc g;
@@ -101,18 +112,24 @@ __device__ __forceinline__ bool wait_raw(uint32_t bar, uint32_t parity, uint64_t
   return true;
 }
 
-template <int PHASE, int EPI>
+template <int PHASE, int EPI, int PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmU1,
                         const GemmArgs a) {
+  using C = Cfg<PAIR>;
+  constexpr int kStages = C::kStages;
+  constexpr uint32_t kStageB = C::kStageB;
+  constexpr uint32_t kStageBytes = C::kStageBytes;
+  constexpr int kTileRows = C::kTileRows;
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_base);
   const uint32_t sA = base;                              // kStages x 16 KB
-  const uint32_t sB = base + kStages * kStageA;          // kStages x 32 KB
+  const uint32_t sB = base + kStages * kStageA;          // kStages x kStageB
   const uint32_t sBar = base + kStages * kStageBytes;    // barriers
   uint8_t* gBar = gbase + kStages * kStageBytes;
   auto full_bar = [&](int s) { return sBar + 8u * s; };
@@ -124,6 +141,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * (2 * kStages + 5) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR == 2 ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int total = (PHASE == kPhaseRouter) ? a.r_tiles : __ldg(a.tile_start + a.G);
 
   if (threadIdx.x == 0) {
@@ -133,7 +154,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(tfull_bar(i), 1);
-      ptx::mbar_init(tempty_bar(i), 128);
+      ptx::mbar_init(tempty_bar(i), 128 * PAIR);
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -146,11 +167,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (PHASE == kPhaseGateUp) ptx::prefetch_tmap(&tmU0);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    if (PAIR == 2) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
     ptx::tc_fence_before();
   }
   __syncthreads();
+  if (PAIR == 2) ptx::cluster_sync();  // the peer's barriers are initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -161,7 +188,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool aborted = false;
-      for (int tile = blockIdx.x; tile < total && !aborted && PHASE == kPhaseRouter; tile += gridDim.x) {
+      for (int tile = unit; tile < total && !aborted && PHASE == kPhaseRouter; tile += units) {
         // Router: A = hidden rows of the m block, B = the router part's columns.
         const RouterTile rt = decode_router_tile(tile, a);
         const uint32_t bytes = kStageA + (uint32_t)a.r_np * kBK * 2u;
@@ -180,28 +207,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      for (int tile = blockIdx.x; tile < total && !aborted && PHASE != kPhaseRouter; tile += gridDim.x) {
+      for (int tile = unit; tile < total && !aborted && PHASE != kPhaseRouter; tile += units) {
         const TileInfo ti = decode_tile(tile, a);
         const int kind = ti.g.kind;
         const CUtensorMap* mA = kind ? &tmA1 : &tmA0;
         const CUtensorMap* mB = kind ? &tmB1 : &tmB0;
         const CUtensorMap* mU = kind ? &tmU1 : &tmU0;
-        const int a_row = (PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kBM;
-        const int b_row = ti.g.index * a.w_rows[kind] +
-                          ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
+        const int a_row =
+            (PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kTileRows + (int)rank * kBM;
+        // Weight rows: gate/up -> rows n*128 of the expert in W_gate (and W_up);
+        // down -> rows n*256 (+ this CTA's 128-row half in a pair).
+        int b_row = ti.g.index * a.w_rows[kind] + ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
+        if (PAIR == 2 && PHASE == kPhaseDown) b_row += (int)rank * (kBNDown / 2);
         const int nkb = a.k_blocks[kind];
         for (int kb = 0; kb < nkb; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) {
             aborted = true;
             break;
           }
-          ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-          ptx::tma_load_2d(sA + stage * kStageA, mA, full_bar(stage), kb * kBK, a_row);
-          if (PHASE == kPhaseGateUp) {
-            ptx::tma_load_2d(sB + stage * kStageB, mB, full_bar(stage), kb * kBK, b_row);
-            ptx::tma_load_2d(sB + stage * kStageB + kStageB / 2, mU, full_bar(stage), kb * kBK, b_row);
+          const uint32_t dA = sA + stage * kStageA, dB = sB + stage * kStageB;
+          if (PAIR == 2) {
+            const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // the leader's barrier
+            if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2u * kStageBytes);
+            ptx::tma_load_2d_pair(dA, mA, fb, kb * kBK, a_row);
+            ptx::tma_load_2d_pair(dB, (PHASE == kPhaseGateUp && !leader) ? mU : mB, fb, kb * kBK, b_row);
           } else {
-            ptx::tma_load_2d(sB + stage * kStageB, mB, full_bar(stage), kb * kBK, b_row);
+            ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+            ptx::tma_load_2d(dA, mA, full_bar(stage), kb * kBK, a_row);
+            ptx::tma_load_2d(dB, mB, full_bar(stage), kb * kBK, b_row);
+            if (PHASE == kPhaseGateUp) ptx::tma_load_2d(dB + kStageB / 2, mU, full_bar(stage), kb * kBK, b_row);
           }
           ++issued;
           if (++stage == kStages) {
@@ -210,8 +244,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (aborted) {
-        // Wait for this CTA's own copies still in flight (the last kStages issues).
+      if (aborted && (PAIR == 1 || leader)) {
+        // Wait for the copies still in flight into this CTA's ring (the last kStages issues).
         const uint32_t n = issued < (uint32_t)kStages ? issued : (uint32_t)kStages;
         for (uint32_t j = issued - n; j < issued; ++j)
           wait_raw(full_bar(j % kStages), (j / kStages) & 1u, kDrainTimeoutNs);
@@ -220,14 +254,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (PAIR == 1 || leader)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool aborted = false;
-      const uint32_t idesc = (PHASE == kPhaseRouter) ? a.r_idesc : kIdesc;
-      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+      const uint32_t idesc = (PHASE == kPhaseRouter) ? a.r_idesc : C::kIdesc;
+      for (int tile = unit; tile < total && !aborted; tile += units) {
         int nkb;
         if (PHASE == kPhaseRouter) {
           const RouterTile rt = decode_router_tile(tile, a);
@@ -247,34 +281,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t adesc = ptx::smem_desc_sw128(sA + stage * kStageA);
           const uint64_t bdesc = ptx::smem_desc_sw128(sB + stage * kStageB);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          ptx::mma_commit(empty_bar(stage));
+          for (int k = 0; k < kBK / 16; ++k) {
+            if (PAIR == 2)
+              ptx::mma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          if (PAIR == 2) ptx::mma_commit_pair_multicast(empty_bar(stage), 0x3);
+          else ptx::mma_commit(empty_bar(stage));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (aborted) break;
-        ptx::mma_commit(tfull_bar(acc));
+        if (PAIR == 2) ptx::mma_commit_pair_multicast(tfull_bar(acc), 0x3);
+        else ptx::mma_commit(tfull_bar(acc));
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // Every MMA this thread issued must finish before TMEM is released.
-      ptx::mma_commit(drain_bar);
+      if (PAIR == 2) ptx::mma_commit_pair_multicast(drain_bar, 0x1);
+      else ptx::mma_commit(drain_bar);
       wait_raw(drain_bar, 0, kWaitTimeoutNs);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
-    const int row_in_tile = quad * 32 + lane;
+    const int row_in_tile = (int)rank * kBM + quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total && PHASE == kPhaseRouter; tile += gridDim.x) {
+    auto release = [&](int i) {
+      ptx::tc_fence_before();
+      if (PAIR == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(i), 0));
+      else ptx::mbar_arrive(tempty_bar(i));
+    };
+    for (int tile = unit; tile < total && PHASE == kPhaseRouter; tile += units) {
       // Router: fp32 partial logits of this (m block, split) for rows < T, experts < N.
       const RouterTile rt = decode_router_tile(tile, a);
       if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
@@ -303,20 +349,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty_bar(acc));
+      release(acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
-    for (int tile = blockIdx.x; tile < total && PHASE != kPhaseRouter; tile += gridDim.x) {
+    for (int tile = unit; tile < total && PHASE != kPhaseRouter; tile += units) {
       const TileInfo ti = decode_tile(tile, a);
       const int kind = ti.g.kind;
       if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
-      const int r_local = ti.m_blk * kBM + row_in_tile;
+      const int r_local = ti.m_blk * kTileRows + row_in_tile;
       const bool row_ok = r_local < ti.g.rows;
       if (PHASE == kPhaseGateUp) {
         const int n_ext = a.n_ext[kind];
@@ -394,8 +439,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty_bar(acc));
+      release(acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -404,54 +448,85 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
+  if (PAIR == 2) ptx::cluster_sync();  // no remote arrive or MMA read of this CTA is still pending
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR == 2) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <int PHASE, int EPI>
-cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<PHASE, EPI>;
-  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+template <int PHASE, int EPI, int PAIR>
+cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int64_t tile_bound, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<PHASE, EPI, PAIR>;
+  constexpr size_t smem = Cfg<PAIR>::kSmem;
+  // Per device: the shared-memory opt-in (a function attribute) and, for
+  // pairs, how many 2-CTA clusters of this kernel fit on the GPU at once.
   static std::atomic<uint64_t> configured{0};
+  static std::atomic<int> max_units[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  if (PAIR == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int units = sms;
+    if (PAIR == 2) {
+      int clusters = 0;
+      cfg.gridDim = dim3((unsigned)(sms & ~1));
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      units = clusters > 0 ? clusters : 1;
+    }
+    max_units[dev & 63].store(units);
     configured.fetch_or(bit);
   }
-  kern<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(m.a[0], m.a[1], m.b[0], m.b[1], m.bu[0], m.bu[1], a);
-  return cudaGetLastError();
+  int64_t units = max_units[dev & 63].load();
+  if (tile_bound < units) units = tile_bound < 1 ? 1 : tile_bound;
+  cfg.gridDim = dim3((unsigned)(units * PAIR));
+  return cudaLaunchKernelEx(&cfg, kern, m.a[0], m.a[1], m.b[0], m.b[1], m.bu[0], m.bu[1], a);
 }
 
 }  // namespace
 
 int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T, int32_t F,
-                        int32_t Fs, int32_t d) {
+                        int32_t Fs, int32_t d, int32_t tile_rows) {
   // sum_e ceil(n_e / BM) <= routed_rows / BM + N
-  const int64_t m_routed = routed_rows / kBM + N;
-  const int64_t m_shared = (int64_t)S * ((T + kBM - 1) / kBM);
+  const int64_t m_routed = routed_rows / tile_rows + N;
+  const int64_t m_shared = (int64_t)S * ((T + tile_rows - 1) / tile_rows);
   if (phase == kPhaseGateUp)
     return m_routed * ((F + kBNGateUp - 1) / kBNGateUp) + m_shared * ((Fs + kBNGateUp - 1) / kBNGateUp);
   return (m_routed + m_shared) * ((d + kBNDown - 1) / kBNDown);
 }
 
-cudaError_t launch_grouped_gemm(int phase, int epilogue, const GemmMaps& maps, const GemmArgs& a,
+cudaError_t launch_grouped_gemm(int phase, int epilogue, int pair, const GemmMaps& maps, const GemmArgs& a,
                                 int64_t tile_bound, cudaStream_t s) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const int grid = (int)(tile_bound < sms ? (tile_bound < 1 ? 1 : tile_bound) : sms);
-  if (phase == kPhaseRouter) return launch_t<kPhaseRouter, kEpiLogits>(maps, a, grid, s);
-  if (phase == kPhaseGateUp) return launch_t<kPhaseGateUp, kEpiSwiGLU>(maps, a, grid, s);
-  if (epilogue == kEpiScatter) return launch_t<kPhaseDown, kEpiScatter>(maps, a, grid, s);
-  return launch_t<kPhaseDown, kEpiStoreY>(maps, a, grid, s);
+  if (phase == kPhaseRouter) return launch_t<kPhaseRouter, kEpiLogits, 1>(maps, a, tile_bound, s);
+  if (pair == 2) {
+    if (phase == kPhaseGateUp) return launch_t<kPhaseGateUp, kEpiSwiGLU, 2>(maps, a, tile_bound, s);
+    if (epilogue == kEpiScatter) return launch_t<kPhaseDown, kEpiScatter, 2>(maps, a, tile_bound, s);
+    return launch_t<kPhaseDown, kEpiStoreY, 2>(maps, a, tile_bound, s);
+  }
+  if (phase == kPhaseGateUp) return launch_t<kPhaseGateUp, kEpiSwiGLU, 1>(maps, a, tile_bound, s);
+  if (epilogue == kEpiScatter) return launch_t<kPhaseDown, kEpiScatter, 1>(maps, a, tile_bound, s);
+  return launch_t<kPhaseDown, kEpiStoreY, 1>(maps, a, tile_bound, s);
 }
 
 }  // namespace moe

@@ -66,6 +66,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
 
 struct ScheduleArgs {
   int32_t N, S, F, Fs, d;
+  int32_t tile_rows;       // rows per GEMM tile: 128, or 256 for CTA pairs
   int64_t T;
   const int32_t* offsets;  // [N+1]
   GroupDesc* groups;       // [N+S]
@@ -110,8 +111,10 @@ struct GemmMaps {
 
 // Upper bound on the tile count (host, from sizes only), used for the grid.
 int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T,
-                        int32_t F, int32_t Fs, int32_t d);
-cudaError_t launch_grouped_gemm(int phase, int epilogue, const GemmMaps& maps, const GemmArgs& a,
+                        int32_t F, int32_t Fs, int32_t d, int32_t tile_rows);
+// pair = 1: 128-row tiles, one CTA each; pair = 2: 256-row tiles on 2-CTA
+// clusters (the down-phase weight maps then use 128-row boxes).
+cudaError_t launch_grouped_gemm(int phase, int epilogue, int pair, const GemmMaps& maps, const GemmArgs& a,
                                 int64_t tile_bound, cudaStream_t s);
 
 cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, int64_t n, cudaStream_t s);

@@ -126,8 +126,13 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// 256-row tiles on CTA pairs once the mean expert group fills one; decode
+// shapes (a few rows per expert) keep 128-row tiles on single CTAs.
+int32_t gemm_pair(int64_t routed_rows, int32_t N) { return routed_rows >= (int64_t)256 * N ? 2 : 1; }
+
 // The two GEMM phases over groups already described in the workspace.
 struct GemmPlan {
+  int32_t pair;
   int32_t N, S, F, Fs, d, K;
   int64_t T, routed_rows;
   const void* x_routed;   // [routed_rows][d] bf16
@@ -150,6 +155,16 @@ struct GemmPlan {
   const int32_t* ts_dn;
   uint32_t* err;
 };
+
+// While the stream is being captured into a CUDA graph, an external record
+// keeps the event a real record node of the graph; otherwise a plain record.
+cudaError_t record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t q = cudaStreamIsCapturing(s, &cs);
+  if (q != cudaSuccess) return q;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(e, s);
+}
 
 moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup = nullptr) {
   if (!have_encode()) return MOE_ERR_CUDA;
@@ -186,17 +201,19 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   a.h[1] = sh ? g.h_sh : g.h;
   a.ldh[0] = g.F;
   a.ldh[1] = sh ? g.Fs : g.F;
-  int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d);
-  MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseGateUp, kEpiSwiGLU, m, a, bound, s)));
-  if (ev_after_gateup) MOE_TRY(cuda_status(cudaEventRecord(ev_after_gateup[0], s)));
+  const int32_t rows = kBM * g.pair;
+  int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, rows);
+  MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseGateUp, kEpiSwiGLU, g.pair, m, a, bound, s)));
+  if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[0], s)));
 
   // down (+ weighted scatter-add or plain store)
   GemmMaps md{};
+  const uint32_t down_box = kBNDown / g.pair;  // a pair loads half the down rows per CTA
   ok = make_map(&md.a[0], g.h, g.F, g.routed_rows, kBM) &&
-       make_map(&md.b[0], g.wd, g.F, (uint64_t)g.N * g.d, kBNDown);
+       make_map(&md.b[0], g.wd, g.F, (uint64_t)g.N * g.d, down_box);
   if (ok && sh)
     ok = make_map(&md.a[1], g.h_sh, g.Fs, (uint64_t)g.S * g.T, kBM) &&
-         make_map(&md.b[1], g.sd, g.Fs, (uint64_t)g.S * g.d, kBNDown);
+         make_map(&md.b[1], g.sd, g.Fs, (uint64_t)g.S * g.d, down_box);
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
     md.a[1] = md.a[0];
@@ -213,9 +230,9 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   a.perm_src = g.perm_src;
   a.topk_w = g.topk_w;
   a.y = g.y;
-  bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d);
-  MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseDown, g.epilogue, md, a, bound, s)));
-  if (ev_after_gateup) MOE_TRY(cuda_status(cudaEventRecord(ev_after_gateup[1], s)));
+  bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, rows);
+  MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseDown, g.epilogue, g.pair, md, a, bound, s)));
+  if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[1], s)));
   return MOE_OK;
 }
 
@@ -319,10 +336,12 @@ moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, cons
   MOE_TRY(check_ws(&q, MOE_CALL_GROUPED_SWIGLU, ws, ws_bytes, &L));
   if (rows == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  ScheduleArgs sa{q.n_experts, 0, q.ffn, 0, q.d_model, q.T, offsets, at<GroupDesc>(ws, L.groups),
+  const int32_t pair = gemm_pair(rows, q.n_experts);
+  ScheduleArgs sa{q.n_experts, 0, q.ffn, 0, q.d_model, kBM * pair, q.T, offsets, at<GroupDesc>(ws, L.groups),
                   at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
   MOE_TRY(cuda_status(launch_schedule(sa, s)));
   GemmPlan g{};
+  g.pair = pair;
   g.N = q.n_experts;
   g.S = 0;
   g.F = q.ffn;
@@ -360,7 +379,7 @@ namespace {
 
 moe_status_t record(cudaEvent_t* ev, int i, cudaStream_t s) {
   if (!ev) return MOE_OK;
-  return cuda_status(cudaEventRecord(ev[i], s));
+  return cuda_status(record_event(ev[i], s));
 }
 
 moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, const void* hidden, void* out,
@@ -429,13 +448,15 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   MOE_TRY(record(ev, 2, s));
 
   // 3. GEMM schedule: routed experts from offsets, then the shared experts
-  ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, T, offsets, at<GroupDesc>(ws, L.groups),
+  const int32_t pair = gemm_pair(T * K, N);
+  ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, kBM * pair, T, offsets, at<GroupDesc>(ws, L.groups),
                   at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
   MOE_TRY(cuda_status(launch_schedule(sa, s)));
   MOE_TRY(record(ev, 3, s));
 
   // 4-5. grouped SwiGLU GEMMs with the fused weighted scatter-add
   GemmPlan g{};
+  g.pair = pair;
   g.N = N;
   g.S = S;
   g.F = p->ffn;

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(512) schedule_kernel(const ScheduleArgs a) {
       gd.h_row0 = (int32_t)((int64_t)gd.index * a.T);
       F = a.Fs;
     }
-    gd.m_tiles = (gd.rows + kBM - 1) / kBM;
+    gd.m_tiles = (gd.rows + a.tile_rows - 1) / a.tile_rows;
     gd.pad0 = gd.pad1 = 0;
     a.groups[g] = gd;
     s_gu[g] = gd.m_tiles * ((F + kBNGateUp - 1) / kBNGateUp);

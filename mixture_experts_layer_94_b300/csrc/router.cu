@@ -344,7 +344,7 @@ cudaError_t launch_tensor_logits(const RouterArgs& a, const RouterPlan& pl, cuda
   g.r_tiles = (int32_t)(pl.token_tiles * pl.splits);
   g.r_idesc = ptx::idesc_bf16_f32(128, pl.np);
   g.r_partial = a.partial;
-  return launch_grouped_gemm(kPhaseRouter, kEpiLogits, m, g, g.r_tiles, s);
+  return launch_grouped_gemm(kPhaseRouter, kEpiLogits, 1, m, g, g.r_tiles, s);
 }
 
 template <typename XT>

@@ -46,6 +46,10 @@ MID = {
     "decode_like_T3": inputs.MoEConfig("decode_like_T3", T=3, d=1024, N=128, K=8, F=64),
     "small_n_split_T5": inputs.MoEConfig("small_n_split_T5", T=5, d=2048, N=6, K=2, F=64,
                                          hidden_dtype="f32"),
+    # mean expert group >= 256 rows: 256-row tiles on 2-CTA clusters
+    "pair_ragged": inputs.MoEConfig("pair_ragged", T=700, d=264, N=4, K=2, F=392),
+    "pair_shared_sigmoid": inputs.MoEConfig("pair_shared_sigmoid", T=520, d=192, N=2, K=1, F=136, S=1,
+                                            Fs=72, score="sigmoid", sel_bias_var=0.1),
 }
 
 
@@ -199,7 +203,9 @@ def test_permute_reports_out_of_range_index():
 
 
 # --------------------------------------------------------------------------- grouped SwiGLU
-SWIGLU_CASES = [(128, 256, 8, 2, 64), (320, 200, 5, 2, 300), (72, 40, 3, 1, 130), (256, 512, 16, 4, 700)]
+SWIGLU_CASES = [(128, 256, 8, 2, 64), (320, 200, 5, 2, 300), (72, 40, 3, 1, 130), (256, 512, 16, 4, 700),
+                # pair tiles (mean group >= 256 rows), ragged rows / columns / K, an empty expert
+                (128, 256, 2, 1, 600), (320, 200, 3, 2, 500)]
 
 
 @pytest.mark.parametrize("d,F,N,K,T", SWIGLU_CASES)
