@@ -276,7 +276,8 @@ moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
  * cudaEventRecord on `stream` before the first kernel and after each stage.
  *   stage_events  array of MOE_LAYER_STAGES cudaEvent_t (passed as void*),
  *                 created by the caller; event i+1 minus event i is stage i:
- *                 0 router+top-K, 1 route and pack, 2 GEMM schedule,
+ *                 0 router+top-K, 1 route and pack, 2 GEMM schedule (built
+ *                 inside route and pack: an empty stage),
  *                 3 gate/up GEMM + SwiGLU, 4 down GEMM + weighted scatter-add,
  *                 5 fp32 -> bf16 finalise.
  * Used by the benchmark to time each kernel inside the timed region.

@@ -61,6 +61,12 @@ struct PermuteArgs {
   float* zero_rows;       // [T][d] fp32 to clear, or nullptr
   __nv_bfloat16* x_bf16;  // [T][d] bf16 copy of hidden, or nullptr
   uint32_t* err;
+  // Optional: also build the GEMM schedule (as launch_schedule) from the new
+  // offsets; skipped when groups == nullptr.
+  GroupDesc* groups;
+  int32_t* ts_gu;
+  int32_t* ts_dn;
+  int32_t S, F, Fs, tile_rows;
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
 

@@ -444,14 +444,18 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.zero_rows = at<float>(ws, L.out_acc);
   pa.x_bf16 = (S > 0 && !hbf16) ? at<__nv_bfloat16>(ws, L.x_bf16) : nullptr;
   pa.err = err;
+  // 3. the GEMM schedule (routed experts from offsets, then the shared
+  //    experts) is built by the same kernel that finishes the prefix sums
+  const int32_t pair = gemm_pair(T * K, N);
+  pa.groups = at<GroupDesc>(ws, L.groups);
+  pa.ts_gu = at<int32_t>(ws, L.ts_gu);
+  pa.ts_dn = at<int32_t>(ws, L.ts_dn);
+  pa.S = S;
+  pa.F = p->ffn;
+  pa.Fs = p->shared_ffn;
+  pa.tile_rows = kBM * pair;
   MOE_TRY(cuda_status(launch_permute(pa, s)));
   MOE_TRY(record(ev, 2, s));
-
-  // 3. GEMM schedule: routed experts from offsets, then the shared experts
-  const int32_t pair = gemm_pair(T * K, N);
-  ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, kBM * pair, T, offsets, at<GroupDesc>(ws, L.groups),
-                  at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
-  MOE_TRY(cuda_status(launch_schedule(sa, s)));
   MOE_TRY(record(ev, 3, s));
 
   // 4-5. grouped SwiGLU GEMMs with the fused weighted scatter-add
@@ -514,9 +518,12 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
 int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   if (moe_problem_check(p) != MOE_OK) return 0;
   if (p->T == 0) return 1;  // the histogram scan that writes zero counts
-  // router logits (bf16 hidden: router split + router GEMM), router top-K,
-  // histogram, scan, scatter, gather, schedule, gate/up GEMM, down GEMM, finalise
-  return p->hidden_dtype == MOE_BF16 ? 11 : 10;
+  // router: split + router GEMM (bf16 hidden) or logits kernel (fp32), then top-K;
+  // route and pack: histogram, scan (+ schedule), scatter -- one kernel for at
+  // most 32 chunks of 32 tokens -- then the gather; gate/up GEMM, down GEMM, finalise
+  const int router = p->hidden_dtype == MOE_BF16 ? 3 : 2;
+  const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
+  return router + route + 3;
 }
 
 moe_status_t moe_get_device_status(void* ws, void* stream) {

@@ -23,6 +23,9 @@ namespace {
 
 constexpr int kHistWarps = 8;
 
+__device__ void schedule_block(int N, int S, int F, int Fs, int d, int tile_rows, int64_t T,
+                               const int32_t* offs, GroupDesc* groups, int32_t* ts_gu, int32_t* ts_dn);
+
 __device__ __forceinline__ void build_chunk_masks(uint32_t* masks, const int32_t* __restrict__ idx,
                                                   int64_t T, int K, int N, int64_t chunk, int lane,
                                                   uint32_t* err) {
@@ -113,6 +116,10 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  if (a.groups) {
+    __syncthreads();
+    schedule_block(N, a.S, a.F, a.Fs, a.d, a.tile_rows, a.T, s_offsets, a.groups, a.ts_gu, a.ts_dn);
+  }
 }
 
 constexpr int kScatterWarps = 8;
@@ -185,49 +192,138 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
   }
 }
 
-// One CTA: the GEMM groups (routed experts from offsets, then shared experts
-// over all T tokens) and the exclusive prefix of their tile counts per phase.
-__global__ void __launch_bounds__(512) schedule_kernel(const ScheduleArgs a) {
+// The GEMM groups (routed experts from offsets, then shared experts over all
+// T tokens) and the exclusive prefix of their tile counts per phase. Called by
+// every thread of one CTA; `offs` may be shared or global memory.
+__device__ void schedule_block(int N, int S, int F, int Fs, int d, int tile_rows, int64_t T,
+                               const int32_t* offs, GroupDesc* groups, int32_t* ts_gu, int32_t* ts_dn) {
   __shared__ int32_t s_gu[kMaxExperts + kMaxShared + 1];
   __shared__ int32_t s_dn[kMaxExperts + kMaxShared + 1];
-  const int G = a.N + a.S;
-  const int nt_dn = (a.d + kBNDown - 1) / kBNDown;
+  const int G = N + S;
+  const int nt_dn = (d + kBNDown - 1) / kBNDown;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     GroupDesc gd;
-    int F;
-    if (g < a.N) {
+    int Fg;
+    if (g < N) {
       gd.kind = 0;
       gd.index = g;
-      gd.a_row0 = a.offsets[g];
-      gd.rows = a.offsets[g + 1] - a.offsets[g];
+      gd.a_row0 = offs[g];
+      gd.rows = offs[g + 1] - offs[g];
       gd.h_row0 = gd.a_row0;
-      F = a.F;
+      Fg = F;
     } else {
       gd.kind = 1;
-      gd.index = g - a.N;
+      gd.index = g - N;
       gd.a_row0 = 0;
-      gd.rows = (int32_t)a.T;
-      gd.h_row0 = (int32_t)((int64_t)gd.index * a.T);
-      F = a.Fs;
+      gd.rows = (int32_t)T;
+      gd.h_row0 = (int32_t)((int64_t)gd.index * T);
+      Fg = Fs;
     }
-    gd.m_tiles = (gd.rows + a.tile_rows - 1) / a.tile_rows;
+    gd.m_tiles = (gd.rows + tile_rows - 1) / tile_rows;
     gd.pad0 = gd.pad1 = 0;
-    a.groups[g] = gd;
-    s_gu[g] = gd.m_tiles * ((F + kBNGateUp - 1) / kBNGateUp);
+    groups[g] = gd;
+    s_gu[g] = gd.m_tiles * ((Fg + kBNGateUp - 1) / kBNGateUp);
     s_dn[g] = gd.m_tiles * nt_dn;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {  // exclusive scans of G <= 264 counts, one warp
+    const int lane = threadIdx.x;
     int32_t run_gu = 0, run_dn = 0;
-    for (int g = 0; g < G; ++g) {
-      const int32_t gu = s_gu[g], dn = s_dn[g];
-      a.tile_start_gu[g] = run_gu;
-      a.tile_start_dn[g] = run_dn;
-      run_gu += gu;
-      run_dn += dn;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      const int32_t vg = g < G ? s_gu[g] : 0, vd = g < G ? s_dn[g] : 0;
+      int32_t ig = vg, id = vd;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t og = __shfl_up_sync(0xffffffffu, ig, off), od = __shfl_up_sync(0xffffffffu, id, off);
+        if (lane >= off) {
+          ig += og;
+          id += od;
+        }
+      }
+      if (g < G) {
+        ts_gu[g] = run_gu + ig - vg;
+        ts_dn[g] = run_dn + id - vd;
+      }
+      run_gu += __shfl_sync(0xffffffffu, ig, 31);
+      run_dn += __shfl_sync(0xffffffffu, id, 31);
     }
-    a.tile_start_gu[G] = run_gu;
-    a.tile_start_dn[G] = run_dn;
+    if (lane == 0) {
+      ts_gu[G] = run_gu;
+      ts_dn[G] = run_dn;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(512) schedule_kernel(const ScheduleArgs a) {
+  schedule_block(a.N, a.S, a.F, a.Fs, a.d, a.tile_rows, a.T, a.offsets, a.groups, a.tile_start_gu,
+                 a.tile_start_dn);
+}
+
+// Small batches (at most 32 chunks = 1024 tokens): one CTA does the histogram,
+// both scans, the scatter and the schedule; one warp per chunk.
+constexpr int kSmallChunks = 32;
+
+__global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) {
+  __shared__ uint32_t masks[kSmallChunks][kMaxExperts];
+  __shared__ int32_t s_offsets[kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N, K = a.K, C = a.C;
+  if (warp < C) build_chunk_masks(masks[warp], a.topk_idx, a.T, K, N, warp, lane, a.err);
+  __syncthreads();
+  if (warp == 0) {  // counts and exclusive scan over experts, 8 experts per lane
+    int32_t v[kMaxExperts / 32];
+    int32_t local = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane * (kMaxExperts / 32) + i;
+      int32_t c = 0;
+      if (e < N)
+        for (int ch = 0; ch < C; ++ch) c += __popc(masks[ch][e]);
+      v[i] = c;
+      local += c;
+    }
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int32_t run = incl - local;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane * (kMaxExperts / 32) + i;
+      if (e < N) {
+        s_offsets[e] = run;
+        a.offsets[e] = run;
+        if (a.counts) a.counts[e] = v[i];
+      }
+      run += v[i];
+    }
+    if (lane == 31) {
+      s_offsets[N] = incl;
+      a.offsets[N] = incl;
+    }
+  }
+  __syncthreads();
+  if (warp < C) {
+    const int64_t t = (int64_t)warp * kTokensPerChunk + lane;
+    if (t < a.T) {
+      const uint32_t below = (1u << lane) - 1u;
+      for (int k = 0; k < K; ++k) {
+        const int e = a.topk_idx[t * K + k];
+        if (e >= 0 && e < N) {
+          int32_t r = s_offsets[e] + __popc(masks[warp][e] & below);
+          for (int ch = 0; ch < warp; ++ch) r += __popc(masks[ch][e]);
+          a.perm_src[r] = (int32_t)(t * K + k);
+          a.inv_row[t * K + k] = r;
+        }
+      }
+    }
+  }
+  if (a.groups) {
+    __syncthreads();
+    schedule_block(N, a.S, a.F, a.Fs, a.d, a.tile_rows, a.T, s_offsets, a.groups, a.ts_gu, a.ts_dn);
   }
 }
 
@@ -238,9 +334,13 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
     route_scan_kernel<<<1, 1024, 0, s>>>(a);
     return cudaGetLastError();
   }
-  route_hist_kernel<<<(unsigned)((a.C + kHistWarps - 1) / kHistWarps), kHistWarps * 32, 0, s>>>(a);
-  route_scan_kernel<<<1, 1024, 0, s>>>(a);
-  route_scatter_kernel<<<(unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s>>>(a);
+  if (a.C <= kSmallChunks) {
+    route_small_kernel<<<1, 1024, 0, s>>>(a);
+  } else {
+    route_hist_kernel<<<(unsigned)((a.C + kHistWarps - 1) / kHistWarps), kHistWarps * 32, 0, s>>>(a);
+    route_scan_kernel<<<1, 1024, 0, s>>>(a);
+    route_scatter_kernel<<<(unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s>>>(a);
+  }
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t rows = a.T * a.K;

@@ -212,7 +212,17 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
     valid[i] = e < N;
     float l = 0.f;
     if (valid[i]) {
-      for (int s = 0; s < a.splits; ++s) l += a.partial[((int64_t)s * a.T + t) * N + e];
+      // Partials summed in split order (deterministic), loaded 8 at a time so
+      // the loads are in flight together.
+      const float* pp = a.partial + t * N + e;
+      const int64_t stride = a.T * N;
+      for (int s0 = 0; s0 < a.splits; s0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = (s0 + q < a.splits) ? __ldg(pp + (int64_t)(s0 + q) * stride) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) l += v[q];
+      }
       if (a.router_bias) l += a.router_bias[e];
       if (a.logits) a.logits[t * N + e] = l;
     }
@@ -386,6 +396,7 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
     int64_t slices = 1;
     if (pl.token_tiles > 0 && pl.token_tiles * 3 < kTargetTiles)
       slices = (kTargetTiles + pl.token_tiles * 3 - 1) / (pl.token_tiles * 3);
+    if (slices > 16) slices = 16;  // bounds the partials the top-K kernel sums per logit
     if (slices > pl.nkb_d) slices = pl.nkb_d;
     pl.kb_per_slice = (int32_t)((pl.nkb_d + slices - 1) / slices);
     pl.dslices = (pl.nkb_d + pl.kb_per_slice - 1) / pl.kb_per_slice;

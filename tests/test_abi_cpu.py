@@ -75,8 +75,9 @@ def test_workspace_grows_with_tokens():
 
 
 def test_layer_kernel_count():
-    assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL)) == 11
-    assert B.layer_forward_kernel_count(B.problem(inputs.TINY)) == 10
+    assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL)) == 10
+    assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, T=1024)) == 8
+    assert B.layer_forward_kernel_count(B.problem(inputs.TINY)) == 7
     assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, T=0)) == 1
     assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, top_k=0)) == 0
 
