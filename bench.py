@@ -36,6 +36,7 @@ METRIC = "MoE layer tokens/s on 1 B300; % of roofline (bf16 TFLOP/s prefill, HBM
 WORKLOADS = {
     "mixtral": (inputs.MIXTRAL, "Mixtral-8x7B-shaped prefill layer"),
     "dsv3": (inputs.DSV3, "DeepSeek-V3-shaped prefill layer"),
+    "dsv3_grouped": (inputs.DSV3_GROUPED, "DeepSeek-V3-shaped prefill layer, node-limited routing (4 of 8 groups)"),
     "gptoss": (inputs.GPTOSS, "gpt-oss-120b-shaped layer"),
     "tiny": (inputs.TINY, "tiny Mixtral-style layer"),
 }
@@ -176,13 +177,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """The slowest rank's value (timing only; the layer itself exchanges nothing)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_tokens_per_second(tokens_per_rank, steps, elapsed_by_rank, world, device="cuda"):
+    """Whole-job throughput of `world` independent replicas: all tokens over the
+    slowest rank's elapsed seconds."""
+    slowest = max_over_ranks(elapsed_by_rank, world, device)
+    return world * tokens_per_rank * steps / slowest, slowest
 
 
 # ----------------------------------------------------------------------------- oracle legs
@@ -192,7 +201,7 @@ def oracle_rows_timed(cfg, ins, rows):
 
     x = ins["hidden"].float().cpu().numpy()[rows]
     r = oracle.router(x, ins["w_router"].cpu().numpy(), K=cfg.K, score_fn=cfg.score_fn,
-                      renormalize=cfg.renormalize,
+                      renormalize=cfg.renormalize, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
                       router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
                       sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy())
     used = sorted(set(r["idx"].reshape(-1).tolist()))
@@ -205,7 +214,7 @@ def oracle_rows_timed(cfg, ins, rows):
         sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in ("ws_gate", "ws_up", "ws_down")}
     t0 = time.perf_counter()
     oracle.layer(x, ins["w_router"].cpu().numpy(), wg, wu, wd, K=cfg.K, score_fn=cfg.score_fn,
-                 renormalize=cfg.renormalize,
+                 renormalize=cfg.renormalize, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
                  router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
                  sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), **sh)
     return len(rows), time.perf_counter() - t0, oracle.num_threads()
@@ -255,6 +264,7 @@ def run_reference(args, cfg, desc, world, rank):
 
 def config_block(cfg, desc, args):
     return {"workload": desc, "T": cfg.T, "d_model": cfg.d, "n_experts": cfg.N, "top_k": cfg.K,
+            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups,
             "ffn": cfg.F, "n_shared": cfg.S, "shared_ffn": cfg.Fs, "score": cfg.score,
             "hidden_dtype": cfg.hidden_dtype, "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",
@@ -329,14 +339,13 @@ def run_ours(args, cfg, desc, world, rank):
     barrier(world)
     t_wall1 = time.monotonic()
     sampler.stop()
-    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    value, elapsed_s = replica_tokens_per_second(cfg.T, args.steps, start.elapsed_time(end) / 1e3, world)
     st = B.get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {B.status_string(st)}")
     stage_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j in range(nst)]
 
-    value = world * cfg.T * args.steps / elapsed_s
     ms_step = 1e3 * elapsed_s / args.steps
     wm = work_model(cfg, counts_h)
     decode = cfg.T <= 512 and cfg.name == "qwen_decode"

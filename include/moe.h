@@ -92,6 +92,13 @@ typedef struct moe_problem {
                             0: softmax -> the full-softmax probability of each
                                chosen expert, sigmoid -> its raw sigmoid score */
   int32_t hidden_dtype;  /* moe_dtype_t of `hidden`                           */
+  int32_t n_groups;      /* group-limited routing: experts form n_groups equal
+                            groups of consecutive indices (0 or 1: off)      */
+  int32_t topk_groups;   /* groups a token may pick from (1..n_groups); a
+                            group's score is the sum of its two largest
+                            selection keys ("Mixture of Experts for LLM
+                            Inference", "Three tricks that tame the
+                            all-to-alls": node-limited routing)              */
 } moe_problem_t;
 
 /*

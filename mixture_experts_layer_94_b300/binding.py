@@ -34,7 +34,8 @@ class Problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("ffn", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("shared_ffn", ctypes.c_int32), ("score_fn", ctypes.c_int32),
-                ("renormalize", ctypes.c_int32), ("hidden_dtype", ctypes.c_int32)]
+                ("renormalize", ctypes.c_int32), ("hidden_dtype", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -92,7 +93,8 @@ def problem(cfg: MoEConfig = None, **kw) -> Problem:
     """A moe_problem_t from a workload config (fields may be overridden)."""
     f = dict(T=cfg.T, d_model=cfg.d, n_experts=cfg.N, top_k=cfg.K, ffn=cfg.F, n_shared=cfg.S,
              shared_ffn=cfg.Fs, score_fn=cfg.score_fn, renormalize=cfg.renormalize,
-             hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16) if cfg else {}
+             hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16, n_groups=cfg.n_groups,
+             topk_groups=cfg.topk_groups) if cfg else {}
     f.update(kw)
     return Problem(**f)
 

@@ -12,6 +12,7 @@ namespace moe {
 struct RouterArgs {
   int64_t T;
   int32_t d, N, K, score_fn, renormalize;
+  int32_t n_groups, topk_groups;  // group-limited routing when n_groups > 1
   const void* hidden;  // [T][d] fp32 or bf16
   const float* w_router;
   const float* router_bias;

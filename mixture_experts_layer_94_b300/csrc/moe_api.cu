@@ -263,6 +263,12 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (p->score_fn != MOE_SCORE_SOFTMAX && p->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (p->renormalize != 0 && p->renormalize != 1) return MOE_ERR_INVALID_ARG;
   if (p->hidden_dtype != MOE_F32 && p->hidden_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (p->n_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (p->n_groups > 1) {
+    if (p->n_experts % p->n_groups != 0 || p->topk_groups < 1 || p->topk_groups > p->n_groups)
+      return MOE_ERR_INVALID_ARG;
+    if (p->top_k > p->topk_groups * (p->n_experts / p->n_groups)) return MOE_ERR_INVALID_ARG;
+  }
   if (p->n_experts > kMaxExperts || p->top_k > kMaxTopK || p->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
   if (p->T * p->top_k > kInt32Max || p->T * (p->n_shared > 0 ? p->n_shared : 1) > kInt32Max)
     return MOE_ERR_UNSUPPORTED;
@@ -288,7 +294,7 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const f
   if (!hidden || !w_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   RouterArgs a{p->T, p->d_model, p->n_experts, p->top_k, p->score_fn, p->renormalize,
-               hidden, w_router, router_bias, sel_bias, topk_idx, topk_w, logits_opt,
+               p->n_groups, p->topk_groups, hidden, w_router, router_bias, sel_bias, topk_idx, topk_w, logits_opt,
                at<float>(ws, L.router), at<__nv_bfloat16>(ws, L.router_w3), 0, 0};
   return cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
 }
@@ -419,7 +425,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   // 1. router, scoring, top-K, gate weights
   MOE_TRY(record(ev, 0, s));
   if (!aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
-  RouterArgs ra{T, p->d_model, N, K, p->score_fn, p->renormalize, hidden, w->w_router,
+  RouterArgs ra{T, p->d_model, N, K, p->score_fn, p->renormalize, p->n_groups, p->topk_groups, hidden, w->w_router,
                 w->router_bias, w->sel_bias, topk_idx, topk_w, nullptr, at<float>(ws, L.router),
                 at<__nv_bfloat16>(ws, L.router_w3), 0, 0};
   MOE_TRY(cuda_status(launch_router(ra, hbf16, s)));

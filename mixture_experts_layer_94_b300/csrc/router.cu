@@ -200,8 +200,10 @@ __global__ void __launch_bounds__(kWarps * 32) logits_large_n_kernel(const Route
 // ---------------------------------------------------------------- R2
 template <int EPL>
 __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  __shared__ float s_key[kWarps][kMaxExperts];
+  __shared__ unsigned char s_kept[kWarps][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t t = (int64_t)blockIdx.x * kWarps + warp;
   if (t >= a.T) return;
   const int N = a.N, K = a.K;
   float key[EPL], sc[EPL];
@@ -233,6 +235,69 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
       const float sg = 1.0f / (1.0f + expf(-l));
       sc[i] = sg;
       key[i] = sg + ((valid[i] && a.sel_bias) ? a.sel_bias[e] : 0.f);
+    }
+  }
+  if (a.n_groups > 1 && a.topk_groups < a.n_groups) {
+    // Group-limited routing: a group's score is the sum of its two largest
+    // keys; keep the topk_groups best groups (score desc, group asc) and pick
+    // experts only from them.
+    const int G = a.n_groups, gs = N / G;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (valid[i]) s_key[warp][lane + 32 * i] = key[i];
+    __syncwarp();
+    float gsc[kMaxExperts / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxExperts / 32; ++j) {
+      const int g = lane + 32 * j;
+      float b1 = -INFINITY, b2 = -INFINITY;
+      if (g < G) {
+        for (int e = g * gs; e < (g + 1) * gs; ++e) {
+          const float v = s_key[warp][e];
+          if (v > b1) {
+            b2 = b1;
+            b1 = v;
+          } else if (v > b2) {
+            b2 = v;
+          }
+        }
+        gsc[j] = gs > 1 ? b1 + b2 : b1;
+        s_kept[warp][g] = 0;
+      } else {
+        gsc[j] = -INFINITY;
+      }
+    }
+    uint32_t gtaken = 0;
+    for (int r = 0; r < a.topk_groups; ++r) {
+      float bv = -INFINITY;
+      int bg = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j) {
+        const int g = lane + 32 * j;
+        if (g < G && !((gtaken >> j) & 1u) && (gsc[j] > bv || (gsc[j] == bv && g < bg))) {
+          bv = gsc[j];
+          bg = g;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int og = __shfl_xor_sync(0xffffffffu, bg, off);
+        if (ov > bv || (ov == bv && og < bg)) {
+          bv = ov;
+          bg = og;
+        }
+      }
+      if (lane == (bg & 31)) {
+        gtaken |= 1u << (bg >> 5);
+        s_kept[warp][bg] = 1;
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (valid[i] && !s_kept[warp][e / gs]) valid[i] = false;
     }
   }
   uint32_t taken = 0;
@@ -396,7 +461,7 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
     int64_t slices = 1;
     if (pl.token_tiles > 0 && pl.token_tiles * 3 < kTargetTiles)
       slices = (kTargetTiles + pl.token_tiles * 3 - 1) / (pl.token_tiles * 3);
-    if (slices > 16) slices = 16;  // bounds the partials the top-K kernel sums per logit
+    if (slices > 8) slices = 8;  // bounds the partials the top-K kernel sums per logit (<= 24)
     if (slices > pl.nkb_d) slices = pl.nkb_d;
     pl.kb_per_slice = (int32_t)((pl.nkb_d + slices - 1) / slices);
     pl.dslices = (pl.nkb_d + pl.kb_per_slice - 1) / pl.kb_per_slice;

@@ -73,13 +73,24 @@ static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
  * 4. margin = the smallest gap between consecutive keys among the first
  *    min(K+1, N) picks: how far the token is from a different choice or a
  *    different slot order.
+ *    Group-limited routing (n_groups > 1, topk_groups < n_groups): the N
+ *    experts form n_groups equal groups of consecutive indices; a group's
+ *    score is the sum of its two largest keys (its one key for groups of one);
+ *    the topk_groups best groups (score desc, group index asc) are kept and
+ *    the top-K picks above range over their experts only. The margin then
+ *    also covers the gaps between consecutive group scores among the first
+ *    topk_groups + 1 groups ("Mixture of Experts for LLM Inference", "Three
+ *    tricks that tame the all-to-alls": node-limited routing caps how many
+ *    nodes a token may visit; "AI Infrastructure series Part 12": at most 4
+ *    servers per token).
  * 5. weights: softmax + renormalise -> exp(l_j - l_max) / sum over the chosen;
  *    softmax, no renormalise -> probs of the chosen;
  *    sigmoid + renormalise -> s_j / sum of chosen s (unbiased: the selection
  *    bias never reaches the weights); sigmoid, no renormalise -> s_j.
  */
 static void router_one_token(int32_t d, int32_t N, int32_t K, int32_t score_fn,
-                             int32_t renormalize, const float* x,
+                             int32_t renormalize, int32_t n_groups, int32_t topk_groups,
+                             const float* x,
                              const float* w_router, const float* router_bias,
                              const float* sel_bias, double* logits_out,
                              double* probs_out, float* keys_out,
@@ -112,8 +123,50 @@ static void router_one_token(int32_t d, int32_t N, int32_t K, int32_t score_fn,
   if (probs_out) for (int32_t e = 0; e < N; ++e) probs_out[e] = prob[e];
   if (keys_out) for (int32_t e = 0; e < N; ++e) keys_out[e] = key[e];
 
-  int32_t picks = (K + 1 < N) ? K + 1 : N;
+  /* Experts a token may pick: all, or those of the kept groups. taken[e] = 1
+   * marks an expert already picked or not allowed. */
+  int32_t allowed = N;
+  double margin = INFINITY;
   for (int32_t e = 0; e < N; ++e) taken[e] = 0;
+  if (n_groups > 1 && topk_groups < n_groups) {
+    const int32_t gs = N / n_groups;
+    double gscore[256];
+    unsigned char gkept[256];
+    for (int32_t g = 0; g < n_groups; ++g) {
+      int32_t b1 = -1, b2 = -1; /* the group's two largest keys */
+      for (int32_t e = g * gs; e < (g + 1) * gs; ++e) {
+        if (b1 < 0 || key[e] > key[b1]) {
+          b2 = b1;
+          b1 = e;
+        } else if (b2 < 0 || key[e] > key[b2]) {
+          b2 = e;
+        }
+      }
+      gscore[g] = (double)key[b1] + (b2 >= 0 ? (double)key[b2] : 0.0);
+      gkept[g] = 0;
+    }
+    int32_t gpicks = (topk_groups + 1 < n_groups) ? topk_groups + 1 : n_groups;
+    int32_t gorder[257];
+    for (int32_t k = 0; k < gpicks; ++k) {
+      int32_t best = -1;
+      for (int32_t g = 0; g < n_groups; ++g) {
+        if (gkept[g]) continue;
+        if (best < 0 || gscore[g] > gscore[best]) best = g;
+      }
+      gkept[best] = 1;
+      gorder[k] = best;
+    }
+    for (int32_t k = 0; k + 1 < gpicks; ++k) {
+      double gap = gscore[gorder[k]] - gscore[gorder[k + 1]];
+      if (gap < margin) margin = gap;
+    }
+    for (int32_t g = 0; g < n_groups; ++g) gkept[g] = 0;
+    for (int32_t k = 0; k < topk_groups; ++k) gkept[gorder[k]] = 1;
+    allowed = topk_groups * gs;
+    for (int32_t e = 0; e < N; ++e)
+      if (!gkept[e / gs]) taken[e] = 1;
+  }
+  int32_t picks = (K + 1 < allowed) ? K + 1 : allowed;
   for (int32_t k = 0; k < picks; ++k) {
     int32_t best = -1;
     for (int32_t e = 0; e < N; ++e) {
@@ -123,7 +176,6 @@ static void router_one_token(int32_t d, int32_t N, int32_t K, int32_t score_fn,
     taken[best] = 1;
     order[k] = best;
   }
-  double margin = INFINITY;
   for (int32_t k = 0; k + 1 < picks; ++k) {
     double gap = (double)key[order[k]] - (double)key[order[k + 1]];
     if (gap < margin) margin = gap;
@@ -152,8 +204,13 @@ static void router_one_token(int32_t d, int32_t N, int32_t K, int32_t score_fn,
 }
 
 static int router_args_ok(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_fn,
+                          int32_t n_groups, int32_t topk_groups,
                           const float* hidden, const float* w_router) {
   if (T < 0 || d <= 0 || N <= 0 || K <= 0 || K > N) return 0;
+  if (n_groups > 1) {
+    if (N % n_groups != 0 || n_groups > 256 || topk_groups < 1 || topk_groups > n_groups) return 0;
+    if (K > topk_groups * (N / n_groups)) return 0;
+  }
   if (score_fn != 0 && score_fn != 1) return 0;
   if ((T > 0 && !hidden) || !w_router) return 0;
   return 1;
@@ -165,11 +222,12 @@ static int router_args_ok(int64_t T, int32_t d, int32_t N, int32_t K, int32_t sc
  * topk_idx [T][K], topk_w (fp64 [T][K]), margin (fp64 [T]).
  */
 int moe_oracle_router(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_fn,
-                      int32_t renormalize, const float* hidden, const float* w_router,
+                      int32_t renormalize, int32_t n_groups, int32_t topk_groups,
+                      const float* hidden, const float* w_router,
                       const float* router_bias, const float* sel_bias,
                       double* logits_out, double* probs_out, float* keys_out,
                       int32_t* topk_idx, double* topk_w, double* margin) {
-  if (!router_args_ok(T, d, N, K, score_fn, hidden, w_router)) return ORACLE_ERR_ARG;
+  if (!router_args_ok(T, d, N, K, score_fn, n_groups, topk_groups, hidden, w_router)) return ORACLE_ERR_ARG;
   if (!topk_idx || !topk_w || !margin) return ORACLE_ERR_ARG;
   int failed = 0;
 #pragma omp parallel
@@ -185,7 +243,7 @@ int moe_oracle_router(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_
     } else {
 #pragma omp for schedule(dynamic, 4)
       for (int64_t t = 0; t < T; ++t) {
-        router_one_token(d, N, K, score_fn, renormalize, hidden + t * d, w_router,
+        router_one_token(d, N, K, score_fn, renormalize, n_groups, topk_groups, hidden + t * d, w_router,
                          router_bias, sel_bias, logits_out ? logits_out + t * N : NULL,
                          probs_out ? probs_out + t * N : NULL,
                          keys_out ? keys_out + t * N : NULL, topk_idx + t * K,
@@ -294,13 +352,15 @@ void moe_oracle_combine(int32_t K, int32_t d, const double* w, const double* y,
  */
 int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
                      int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
+                     int32_t n_groups, int32_t topk_groups,
                      const float* hidden, const float* w_router, const float* router_bias,
                      const float* sel_bias, const uint16_t* const* w_gate,
                      const uint16_t* const* w_up, const uint16_t* const* w_down,
                      const uint16_t* const* ws_gate, const uint16_t* const* ws_up,
                      const uint16_t* const* ws_down, int32_t* topk_idx, double* topk_w,
                      double* margin, double* out) {
-  if (!router_args_ok(n_rows, d, N, K, score_fn, hidden, w_router)) return ORACLE_ERR_ARG;
+  if (!router_args_ok(n_rows, d, N, K, score_fn, n_groups, topk_groups, hidden, w_router))
+    return ORACLE_ERR_ARG;
   if (F <= 0 || S < 0 || (S > 0 && Fs <= 0)) return ORACLE_ERR_ARG;
   if (!w_gate || !w_up || !w_down || !topk_idx || !topk_w || !margin || !out)
     return ORACLE_ERR_ARG;
@@ -328,7 +388,7 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
         const float* xr = hidden + t * d;
         int32_t* idx = topk_idx + t * K;
         double* w = topk_w + t * K;
-        router_one_token(d, N, K, score_fn, renormalize, xr, w_router, router_bias,
+        router_one_token(d, N, K, score_fn, renormalize, n_groups, topk_groups, xr, w_router, router_bias,
                          sel_bias, NULL, NULL, NULL, idx, w, margin + t, l32, prob, key,
                          taken, order);
         for (int32_t j = 0; j < d; ++j) x[j] = (double)xr[j];

@@ -39,7 +39,7 @@ def _load():
         lib = ctypes.CDLL(_LIB_PATH)
         P = ctypes.c_void_p
         i32, i64 = ctypes.c_int32, ctypes.c_int64
-        lib.moe_oracle_router.argtypes = [i64, i32, i32, i32, i32, i32] + [P] * 10
+        lib.moe_oracle_router.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32] + [P] * 10
         lib.moe_oracle_router.restype = ctypes.c_int
         lib.moe_oracle_permute.argtypes = [i64, i32, i32, P, P, P, P, P]
         lib.moe_oracle_permute.restype = ctypes.c_int
@@ -47,7 +47,7 @@ def _load():
         lib.moe_oracle_expert_ffn.restype = None
         lib.moe_oracle_combine.argtypes = [i32, i32, P, P, P, P]
         lib.moe_oracle_combine.restype = None
-        lib.moe_oracle_layer.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32] + [P] * 14
+        lib.moe_oracle_layer.argtypes = [i64] + [i32] * 10 + [P] * 14
         lib.moe_oracle_layer.restype = ctypes.c_int
         lib.moe_oracle_silu.argtypes = [ctypes.c_double]
         lib.moe_oracle_silu.restype = ctypes.c_double
@@ -95,7 +95,7 @@ def silu(z: float) -> float:
 
 
 def router(hidden, w_router, K, score_fn=SOFTMAX, renormalize=1, router_bias=None,
-           sel_bias=None):
+           sel_bias=None, n_groups=0, topk_groups=0):
     """Router over the rows of `hidden` (fp32 [T][d]). Returns a dict with
     logits (fp64 [T][N]), probs (fp64 [T][N]: full softmax or sigmoid scores),
     keys (fp32 [T][N]), idx (int32 [T][K]), w (fp64 [T][K]), margin (fp64 [T])."""
@@ -112,7 +112,8 @@ def router(hidden, w_router, K, score_fn=SOFTMAX, renormalize=1, router_bias=Non
     idx = np.empty((T, K), np.int32)
     w = np.empty((T, K), np.float64)
     margin = np.empty((T,), np.float64)
-    rc = lib.moe_oracle_router(T, d, N, K, score_fn, renormalize, _ptr(x), _ptr(W), _ptr(rb),
+    rc = lib.moe_oracle_router(T, d, N, K, score_fn, renormalize, n_groups, topk_groups, _ptr(x),
+                               _ptr(W), _ptr(rb),
                                _ptr(sb), _ptr(logits), _ptr(probs), _ptr(keys), _ptr(idx),
                                _ptr(w), _ptr(margin))
     if rc != 0:
@@ -178,7 +179,8 @@ def _ptr_array(mats, n):
 
 
 def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormalize=1,
-          router_bias=None, sel_bias=None, ws_gate=None, ws_up=None, ws_down=None):
+          router_bias=None, sel_bias=None, ws_gate=None, ws_up=None, ws_down=None, n_groups=0,
+          topk_groups=0):
     """The whole layer for the rows of `hidden` (fp32 [n][d]).
 
     w_gate / w_up / w_down: sequences of N per-expert bf16 matrices (uint16 bit
@@ -205,7 +207,8 @@ def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormali
     w = np.empty((n, K), np.float64)
     margin = np.empty((n,), np.float64)
     out = np.empty((n, d), np.float64)
-    rc = lib.moe_oracle_layer(n, d, N, K, F, S, Fs, score_fn, renormalize, _ptr(x), _ptr(W),
+    rc = lib.moe_oracle_layer(n, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups,
+                              _ptr(x), _ptr(W),
                               _ptr(rb), _ptr(sb), ctypes.cast(g_arr, ctypes.c_void_p),
                               ctypes.cast(u_arr, ctypes.c_void_p),
                               ctypes.cast(d_arr, ctypes.c_void_p),

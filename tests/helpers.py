@@ -40,7 +40,8 @@ def oracle_router(cfg, ins, rows=None):
         x = x[rows]
     return oracle.router(x, np32(ins["w_router"]), K=cfg.K, score_fn=cfg.score_fn,
                          renormalize=cfg.renormalize, router_bias=np32(ins.get("router_bias")),
-                         sel_bias=np32(ins.get("sel_bias")))
+                         sel_bias=np32(ins.get("sel_bias")), n_groups=cfg.n_groups,
+                         topk_groups=cfg.topk_groups)
 
 
 def oracle_layer_rows(cfg, ins, rows):
@@ -64,7 +65,7 @@ def oracle_layer_rows(cfg, ins, rows):
     return oracle.layer(hidden_f32(ins)[rows], np32(ins["w_router"]), wg, wu, wd, K=cfg.K,
                         score_fn=cfg.score_fn, renormalize=cfg.renormalize,
                         router_bias=np32(ins.get("router_bias")), sel_bias=np32(ins.get("sel_bias")),
-                        **sh)
+                        n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, **sh)
 
 
 def output_errors(gpu: np.ndarray, ref: np.ndarray) -> dict:

@@ -89,3 +89,15 @@ def test_workspace_sizing_for_empty_and_single_token_batches(cfg):
         assert B.problem_check(p) == 0
         for call in (B.CALL_PERMUTE, B.CALL_GROUPED_SWIGLU, B.CALL_LAYER_FORWARD, B.CALL_ROUTER):
             assert B.workspace_bytes(p, call) >= 256
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_groups=3), -1),                      # 8 experts do not split into 3 groups
+    (dict(n_groups=4, topk_groups=0), -1),
+    (dict(n_groups=4, topk_groups=5), -1),
+    (dict(n_groups=4, topk_groups=1, top_k=3), -1),  # K > experts in the kept groups
+    (dict(n_groups=4, topk_groups=1), 0),
+    (dict(n_groups=-1), -1),
+])
+def test_problem_check_group_limited_routing(kw, status):
+    assert B.problem_check(B.problem(inputs.TINY, **kw)) == status

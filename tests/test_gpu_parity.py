@@ -46,6 +46,12 @@ MID = {
     "decode_like_T3": inputs.MoEConfig("decode_like_T3", T=3, d=1024, N=128, K=8, F=64),
     "small_n_split_T5": inputs.MoEConfig("small_n_split_T5", T=5, d=2048, N=6, K=2, F=64,
                                          hidden_dtype="f32"),
+    # group-limited routing: 8 groups of 8 experts, 3 groups per token
+    "grouped_routing": inputs.MoEConfig("grouped_routing", T=333, d=256, N=64, K=6, F=200, S=1, Fs=136,
+                                        score="sigmoid", sel_bias_var=0.1, zipf=1.1, n_groups=8,
+                                        topk_groups=3),
+    "grouped_softmax_f32": inputs.MoEConfig("grouped_softmax_f32", T=100, d=64, N=32, K=4, F=64,
+                                            hidden_dtype="f32", n_groups=16, topk_groups=2),
     # mean expert group >= 256 rows: 256-row tiles on 2-CTA clusters
     "pair_ragged": inputs.MoEConfig("pair_ragged", T=700, d=264, N=4, K=2, F=392),
     "pair_shared_sigmoid": inputs.MoEConfig("pair_shared_sigmoid", T=520, d=192, N=2, K=1, F=136, S=1,
@@ -116,7 +122,8 @@ def test_layer_is_repeatable():
 
 # --------------------------------------------------------------------------- router
 ROUTER_CASES = ["tiny", "ragged_softmax", "dsv3_like", "no_renorm_sigmoid", "no_renorm_softmax",
-                "K_equals_N", "N_K_1", "T1", "decode_like_T3", "small_n_split_T5"]
+                "K_equals_N", "N_K_1", "T1", "decode_like_T3", "small_n_split_T5", "grouped_routing",
+                "grouped_softmax_f32"]
 
 
 @pytest.mark.parametrize("name", ROUTER_CASES)
@@ -296,7 +303,8 @@ def _sample_rows(T, n, seed=0):
     return np.array(sorted(rows))
 
 
-FULL = [("mixtral", inputs.MIXTRAL, 12), ("gptoss", inputs.GPTOSS, 12), ("dsv3", inputs.DSV3, 6)] + [
+FULL = [("mixtral", inputs.MIXTRAL, 12), ("gptoss", inputs.GPTOSS, 12), ("dsv3", inputs.DSV3, 6),
+        ("dsv3_grouped", inputs.DSV3_GROUPED, 6)] + [
     (f"qwen_decode_T{T}", inputs.QWEN_DECODE.with_(T=T), 6) for T in inputs.DECODE_BATCHES]
 
 
@@ -310,6 +318,9 @@ def test_full_size_workload(name, cfg, n_sample):
     out, idx, w, counts = _run_layer(cfg, dev)
     ref_r = H.oracle_router(cfg, ins)
     rep = H.compare_router(idx, w, ref_r)
+    if cfg.n_groups > 1:  # every token's experts lie in at most topk_groups groups
+        gs = cfg.N // cfg.n_groups
+        assert max(len(set((row // gs).tolist())) for row in idx) <= cfg.topk_groups
     # counts: the GPU's own histogram, and the oracle's up to the near-tie flips
     assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
     ref_counts = np.bincount(ref_r["idx"].reshape(-1), minlength=cfg.N)

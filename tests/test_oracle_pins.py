@@ -388,3 +388,63 @@ def test_mixtral_router_scale_constant_matches_fixture():
     g = _golden("mixtral_router_scale.json")
     assert g["router_scale"] == inputs.MIXTRAL_ROUTER_SCALE
     assert abs(g["top1_share_at_scale"] - 0.40) < 0.002
+
+
+# ---------------------------------------------------------------------------
+# Group-limited (node-limited) routing
+# ---------------------------------------------------------------------------
+
+def test_group_limited_routing_hand_case():
+    """"Mixture of Experts for LLM Inference", 'Three tricks that tame the
+    all-to-alls' (node-limited routing caps how many nodes a token may visit):
+    8 experts in 4 groups of 2; a group's score is the sum of its two largest
+    keys."""
+    x, W = _identity_router([5.0, 0.0, 4.9, 4.8, 1.0, 1.0, 0.5, 0.2])
+    # group scores: g0 5.0, g1 9.7, g2 2.0, g3 0.7
+    assert oracle.router(x, W, K=2)["idx"][0].tolist() == [0, 2]
+    r1 = oracle.router(x, W, K=2, n_groups=4, topk_groups=1)
+    assert r1["idx"][0].tolist() == [2, 3]
+    # margin: group-score gaps (9.7 -> 5.0) and key gaps among the allowed picks (4.9 -> 4.8)
+    assert r1["margin"][0] == pytest.approx(0.1, abs=1e-6)
+    r2 = oracle.router(x, W, K=2, n_groups=4, topk_groups=2)
+    assert r2["idx"][0].tolist() == [0, 2]
+    # weights: softmax over the chosen logits, as without groups
+    e = np.exp(np.array([4.9, 4.8]) - 4.9)
+    np.testing.assert_allclose(r1["w"][0], e / e.sum(), atol=1e-7)
+
+
+@pytest.mark.parametrize("score_fn", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_group_limit_reduces_to_plain_topk_when_all_groups_kept(score_fn):
+    rng = np.random.default_rng(11)
+    x, W = _rand_router_case(rng, 500, 24, 16)
+    sb = (rng.standard_normal(16) * 0.3).astype(np.float32) if score_fn else None
+    ref = oracle.router(x, W, K=4, score_fn=score_fn, sel_bias=sb)
+    for ng in (1, 4):
+        r = oracle.router(x, W, K=4, score_fn=score_fn, sel_bias=sb, n_groups=ng, topk_groups=ng)
+        assert np.array_equal(r["idx"], ref["idx"])
+        np.testing.assert_array_equal(r["w"], ref["w"])
+
+
+@pytest.mark.parametrize("N,G,M,K", [(16, 4, 2, 4), (12, 6, 3, 5), (256, 8, 4, 8)])
+def test_group_limited_routing_against_library_sorts(N, G, M, K):
+    """Chosen experts lie in at most M groups, the kept groups are the M best by
+    (sum of the two largest keys, lower index first), and the chosen experts are
+    the stable top-K of the keys restricted to those groups."""
+    rng = np.random.default_rng(N + G)
+    x, W = _rand_router_case(rng, 300, 32, N)
+    sb = (rng.standard_normal(N) * 0.3).astype(np.float32)
+    r = oracle.router(x, W, K=K, score_fn=oracle.SIGMOID, sel_bias=sb, n_groups=G, topk_groups=M)
+    keys = r["keys"].astype(np.float64)
+    gs = N // G
+    for t in range(x.shape[0]):
+        groups_used = set((r["idx"][t] // gs).tolist())
+        assert len(groups_used) <= M
+        gk = np.sort(keys[t].reshape(G, gs), axis=1)[:, ::-1]
+        gscore = gk[:, 0] + (gk[:, 1] if gs > 1 else 0.0)
+        kept = np.lexsort((np.arange(G), -gscore))[:M]
+        allowed = np.zeros(N, bool)
+        for g in kept:
+            allowed[g * gs:(g + 1) * gs] = True
+        cand = np.nonzero(allowed)[0]
+        order = cand[np.lexsort((cand, -keys[t][cand]))]
+        assert r["idx"][t].tolist() == order[:K].tolist()
