@@ -35,6 +35,7 @@ from mixture_experts_layer_94_b300 import inputs  # noqa: E402
 METRIC = "MoE layer tokens/s on 1 B300; % of roofline (bf16 TFLOP/s prefill, HBM GB/s decode)"
 WORKLOADS = {
     "mixtral": (inputs.MIXTRAL, "Mixtral-8x7B-shaped prefill layer"),
+    "mixtral_capacity": (inputs.MIXTRAL_CAPACITY, "Mixtral-8x7B-shaped prefill layer, expert capacity factor 1.0"),
     "dsv3": (inputs.DSV3, "DeepSeek-V3-shaped prefill layer"),
     "dsv3_grouped": (inputs.DSV3_GROUPED, "DeepSeek-V3-shaped prefill layer, node-limited routing (4 of 8 groups)"),
     "gptoss": (inputs.GPTOSS, "gpt-oss-120b-shaped layer"),
@@ -212,11 +213,21 @@ def oracle_rows_timed(cfg, ins, rows):
     sh = {}
     if cfg.S:
         sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in ("ws_gate", "ws_up", "ws_down")}
+    keep = None
+    if cfg.capacity_factor > 0:  # which copies survive depends on the whole batch's routing
+        full = oracle.router(ins["hidden"].float().cpu().numpy(), ins["w_router"].cpu().numpy(), K=cfg.K,
+                             score_fn=cfg.score_fn, renormalize=cfg.renormalize, n_groups=cfg.n_groups,
+                             topk_groups=cfg.topk_groups,
+                             router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
+                             sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy())
+        inv = oracle.permute(full["idx"], cfg.N, capacity_factor=cfg.capacity_factor)["inv_row"]
+        keep = (inv >= 0).reshape(-1, cfg.K).astype(np.uint8)[rows]
     t0 = time.perf_counter()
     oracle.layer(x, ins["w_router"].cpu().numpy(), wg, wu, wd, K=cfg.K, score_fn=cfg.score_fn,
                  renormalize=cfg.renormalize, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
                  router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
-                 sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), **sh)
+                 sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), keep=keep,
+                 **sh)
     return len(rows), time.perf_counter() - t0, oracle.num_threads()
 
 
@@ -264,7 +275,7 @@ def run_reference(args, cfg, desc, world, rank):
 
 def config_block(cfg, desc, args):
     return {"workload": desc, "T": cfg.T, "d_model": cfg.d, "n_experts": cfg.N, "top_k": cfg.K,
-            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups,
+            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "capacity_factor": cfg.capacity_factor,
             "ffn": cfg.F, "n_shared": cfg.S, "shared_ffn": cfg.Fs, "score": cfg.score,
             "hidden_dtype": cfg.hidden_dtype, "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",
@@ -352,7 +363,11 @@ def run_ours(args, cfg, desc, world, rank):
     gu, dn = B.LAYER_STAGES.index("gateup_swiglu_gemm"), B.LAYER_STAGES.index("down_scatter_gemm")
     dom = gu if stage_ms[gu] >= stage_ms[dn] else dn
     dom_name = B.LAYER_STAGES[dom]
-    long_region = elapsed_s >= 1.0
+    clocks = sampler.summary(t_wall0, t_wall1)
+    # The recipe's denominators: the burst peak for a kernel timed alone, the
+    # sustained one for a kernel timed inside a long, power-capped run.
+    power_capped = bool(clocks and "sw_power_cap" in clocks["reasons"])
+    long_region = elapsed_s >= 1.0 or power_capped
     if decode:
         bytes_ = wm["bytes_gateup"] if dom == gu else wm["bytes_down"]
         achieved = bytes_ / (stage_ms[dom] * 1e-3) / 1e9
@@ -366,9 +381,11 @@ def run_ours(args, cfg, desc, world, rank):
         key = "bf16_tflops_sustained" if long_region and "bf16_tflops_sustained" in peaks else "bf16_tflops"
         peak = peaks[key]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "algorithmic_flops_per_launch": flops}
+                "frac": achieved / peak, "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                "algorithmic_flops_per_launch": flops}
         t_roof = max(wm["flops"] / (peak * 1e12), wm["bytes"] / (peaks["hbm_gbs"] * 1e9))
-    roof.update({"kernel": dom_name, "peak_source": f"{peak_src} ({'sustained' if (not decode and long_region) else 'burst'})",
+    roof.update({"kernel": dom_name,
+                 "peak_source": f"{peak_src} ({'sustained: run power-capped or >= 1 s' if (not decode and long_region) else 'burst'})",
                  "traffic": traffic_from_profiles(dom_name, args.workload)})
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -379,7 +396,7 @@ def run_ours(args, cfg, desc, world, rank):
             "stages_ms": dict(zip(B.LAYER_STAGES, stage_ms)),
             "gpu_launches": B.layer_forward_kernel_count(p) * args.steps,
             "cuda_graph": graph is not None,
-            "clocks": sampler.summary(t_wall0, t_wall1)}
+            "clocks": clocks}
 
     if not args.no_e2e:
         hid_host = torch.empty(hidden.shape, dtype=hidden.dtype, pin_memory=True)

@@ -99,6 +99,11 @@ typedef struct moe_problem {
                             selection keys ("Mixture of Experts for LLM
                             Inference", "Three tricks that tame the
                             all-to-alls": node-limited routing)              */
+  float capacity_factor; /* expert capacity C = ceil(c * T * K / N) for c > 0
+                            ("Chapter 19", §19.6.1); copies beyond the first
+                            C of an expert (token order) are dropped: they
+                            skip the FFN and contribute nothing, the kept
+                            weights are not renormalised. 0: dropless     */
 } moe_problem_t;
 
 /*
@@ -177,7 +182,10 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden,
  *   counts     out int32 [N]:   counts[e] = #{(t,k) : topk_idx[t][k] == e}
  *   offsets    out int32 [N+1]: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
  *   perm_src   out int32 [T*K]: permuted row r holds token copy perm_src[r] = t*K + k
- *   inv_row    out int32 [T*K]: inv_row[t*K + k] = r (the inverse of perm_src)
+ *   inv_row    out int32 [T*K]: inv_row[t*K + k] = r (the inverse of perm_src);
+ *              -1 for a copy dropped by its expert's capacity (p->capacity_factor
+ *              > 0), in which case offsets count kept copies only, perm_src lists
+ *              offsets[N] rows and counts still count every copy routed to e
  *   x_perm     out bf16 [T*K][d]: x_perm[r] = bf16(hidden[perm_src[r] / K])
  *   ws         workspace of moe_workspace_bytes(p, MOE_CALL_PERMUTE) bytes
  * The result is deterministic. An index outside [0, N) sets
@@ -249,7 +257,8 @@ moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm,
  * change is surprisingly local"):
  *   out[t] = bf16( sum_k topk_w[t][k] * y_perm[inv_row[t*K + k]]
  *                  + shared_out[t] )
- * with fp32 accumulation in slot order k = 0..K-1 (deterministic).
+ * with fp32 accumulation in slot order k = 0..K-1 (deterministic); slots with
+ * inv_row == -1 (dropped by capacity) are skipped.
  *   y_perm bf16 [T*K][d]; inv_row int32 [T*K]; topk_w fp32 [T][K]
  *   shared_out bf16 [T][d] or NULL;  out bf16 [T][d]
  */

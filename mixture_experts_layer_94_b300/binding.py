@@ -35,7 +35,8 @@ class Problem(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("ffn", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("shared_ffn", ctypes.c_int32), ("score_fn", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("hidden_dtype", ctypes.c_int32),
-                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32)]
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float)]
 
 
 class Weights(ctypes.Structure):
@@ -94,7 +95,7 @@ def problem(cfg: MoEConfig = None, **kw) -> Problem:
     f = dict(T=cfg.T, d_model=cfg.d, n_experts=cfg.N, top_k=cfg.K, ffn=cfg.F, n_shared=cfg.S,
              shared_ffn=cfg.Fs, score_fn=cfg.score_fn, renormalize=cfg.renormalize,
              hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16, n_groups=cfg.n_groups,
-             topk_groups=cfg.topk_groups) if cfg else {}
+             topk_groups=cfg.topk_groups, capacity_factor=cfg.capacity_factor) if cfg else {}
     f.update(kw)
     return Problem(**f)
 

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int32_t K, int3
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
     for (int k = 0; k < K; ++k) {
       const int64_t r = __ldg(inv_row + t * K + k);
+      if (r < 0) continue;  // dropped by its expert's capacity
       const float w = __ldg(topk_w + t * K + k);
       add_bf16x8(acc, reinterpret_cast<const uint4*>(y_perm + r * d)[v], w);
     }

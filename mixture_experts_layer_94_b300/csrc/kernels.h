@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
 #include "common.cuh"
 
 namespace moe {
@@ -50,6 +51,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t ro
 struct PermuteArgs {
   int64_t T;
   int32_t d, N, K, C;  // C = number of 32-token chunks
+  int32_t capacity;    // copies an expert keeps (token order); INT32_MAX: no cap
   const int32_t* topk_idx;
   const void* hidden;
   bool hidden_bf16;
@@ -70,6 +72,8 @@ struct PermuteArgs {
   int32_t S, F, Fs, tile_rows;
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
+// Expert capacity ceil(c * T * K / N) of a problem; INT32_MAX when dropless.
+int32_t expert_capacity(const moe_problem_t& p);
 
 struct ScheduleArgs {
   int32_t N, S, F, Fs, d;

@@ -64,6 +64,20 @@ Layout make_layout(const moe_problem_t& p, int call) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+namespace moe {
+// Expert capacity C = ceil(c * T * K / N) ("Chapter 19", §19.6.1), computed in
+// double; INT32_MAX when c == 0 (dropless).
+int32_t expert_capacity(const moe_problem_t& p) {
+  if (!(p.capacity_factor > 0.f)) return 2147483647;
+  const double c = ceil((double)p.capacity_factor * (double)p.T * (double)p.top_k / (double)p.n_experts);
+  return c >= 2147483647.0 ? 2147483647 : (int32_t)c;
+}
+}  // namespace moe
+
+namespace {
+
 // ---------------------------------------------------------------- TMA maps
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -264,6 +278,7 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (p->renormalize != 0 && p->renormalize != 1) return MOE_ERR_INVALID_ARG;
   if (p->hidden_dtype != MOE_F32 && p->hidden_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (p->n_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (!(p->capacity_factor >= 0.f) || p->capacity_factor > 1e30f) return MOE_ERR_INVALID_ARG;  // NaN fails too
   if (p->n_groups > 1) {
     if (p->n_experts % p->n_groups != 0 || p->topk_groups < 1 || p->topk_groups > p->n_groups)
       return MOE_ERR_INVALID_ARG;
@@ -314,6 +329,7 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx, const 
   a.N = p->n_experts;
   a.K = p->top_k;
   a.C = (int32_t)((p->T + kTokensPerChunk - 1) / kTokensPerChunk);
+  a.capacity = expert_capacity(*p);
   a.topk_idx = topk_idx;
   a.hidden = hidden;
   a.hidden_bf16 = p->hidden_dtype == MOE_BF16;
@@ -415,6 +431,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     PermuteArgs pa{};
     pa.N = N;
     pa.K = K;
+    pa.capacity = 2147483647;
     pa.chunk_counts = at<int32_t>(ws, L.chunk);
     pa.counts = counts;
     pa.offsets = offsets;
@@ -438,6 +455,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.N = N;
   pa.K = K;
   pa.C = (int32_t)((T + kTokensPerChunk - 1) / kTokensPerChunk);
+  pa.capacity = expert_capacity(*p);
   pa.topk_idx = topk_idx;
   pa.hidden = hidden;
   pa.hidden_bf16 = hbf16;

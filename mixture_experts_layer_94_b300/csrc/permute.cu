@@ -15,6 +15,9 @@
 //   offsets[e] + rows of e in earlier chunks + rank in its chunk,
 // i.e. expert ascending, token ascending: the same order as a stable sort.
 // The gather moves each hidden row to its permuted rows with 16-byte vectors.
+// With an expert capacity C ("Chapter 19", §19.6.1) a copy whose rank inside
+// its expert is C or more is dropped (inv_row = -1) and offsets count kept
+// copies: min(count, C) per expert.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -54,8 +57,9 @@ __global__ void __launch_bounds__(kHistWarps * 32) route_hist_kernel(const Permu
   for (int e = lane; e < a.N; e += 32) a.chunk_counts[(int64_t)e * a.C + c] = __popc(masks[warp][e]);
 }
 
-// One CTA: counts[e] = sum over chunks, offsets = exclusive scan over experts,
-// chunk_counts[e][c] <- offsets[e] + sum_{c' < c} chunk_counts[e][c'].
+// One CTA: counts[e] = sum over chunks, offsets = exclusive scan over experts
+// of the kept counts min(counts[e], capacity), and
+// chunk_counts[e][c] <- sum_{c' < c} chunk_counts[e][c'] (the rank base).
 __global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
   __shared__ int32_t s_counts[kMaxExperts];
   __shared__ int32_t s_offsets[kMaxExperts + 1];
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = lane * (kMaxExperts / 32) + i;
-      v[i] = (e < N) ? s_counts[e] : 0;
+      v[i] = (e < N) ? min(s_counts[e], a.capacity) : 0;
       local += v[i];
     }
     int32_t incl = local;
@@ -100,9 +104,9 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
     a.offsets[e] = s_offsets[e];
     if (e < N && a.counts) a.counts[e] = s_counts[e];
   }
-  for (int e = warp; e < N; e += nwarps) {
+  for (int e = warp; e < N; e += nwarps) {  // per chunk: the expert rank of its first copy
     int32_t* row = a.chunk_counts + (int64_t)e * C;
-    int32_t run = s_offsets[e];
+    int32_t run = 0;
     for (int64_t c0 = 0; c0 < C; c0 += 32) {
       const int64_t c = c0 + lane;
       const int32_t v = (c < C) ? row[c] : 0;
@@ -140,9 +144,14 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
     for (int k = 0; k < K; ++k) {
       const int e = a.topk_idx[t * K + k];
       if (e >= 0 && e < N) {
-        const int32_t r = a.chunk_counts[(int64_t)e * a.C + c] + __popc(m[e] & below);
-        a.perm_src[r] = (int32_t)(t * K + k);
-        a.inv_row[t * K + k] = r;
+        const int32_t rank = a.chunk_counts[(int64_t)e * a.C + c] + __popc(m[e] & below);
+        if (rank < a.capacity) {
+          const int32_t r = __ldg(a.offsets + e) + rank;
+          a.perm_src[r] = (int32_t)(t * K + k);
+          a.inv_row[t * K + k] = r;
+        } else {
+          a.inv_row[t * K + k] = -1;
+        }
       }
     }
   }
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) 
       if (e < N)
         for (int ch = 0; ch < C; ++ch) c += __popc(masks[ch][e]);
       v[i] = c;
-      local += c;
+      local += min(c, a.capacity);
     }
     int32_t incl = local;
 #pragma unroll
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) 
         a.offsets[e] = run;
         if (a.counts) a.counts[e] = v[i];
       }
-      run += v[i];
+      run += min(v[i], a.capacity);
     }
     if (lane == 31) {
       s_offsets[N] = incl;
@@ -313,10 +322,15 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) 
       for (int k = 0; k < K; ++k) {
         const int e = a.topk_idx[t * K + k];
         if (e >= 0 && e < N) {
-          int32_t r = s_offsets[e] + __popc(masks[warp][e] & below);
-          for (int ch = 0; ch < warp; ++ch) r += __popc(masks[ch][e]);
-          a.perm_src[r] = (int32_t)(t * K + k);
-          a.inv_row[t * K + k] = r;
+          int32_t rank = __popc(masks[warp][e] & below);
+          for (int ch = 0; ch < warp; ++ch) rank += __popc(masks[ch][e]);
+          if (rank < a.capacity) {
+            const int32_t r = s_offsets[e] + rank;
+            a.perm_src[r] = (int32_t)(t * K + k);
+            a.inv_row[t * K + k] = r;
+          } else {
+            a.inv_row[t * K + k] = -1;
+          }
         }
       }
     }

@@ -75,6 +75,7 @@ extern "C" moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t
   a.N = p->n_experts;
   a.K = p->top_k;
   a.C = (int32_t)chunks;
+  a.capacity = moe::expert_capacity(*p);
   a.topk_idx = topk_idx;
   a.hidden = hidden;
   a.hidden_bf16 = p->hidden_dtype == MOE_BF16;

@@ -256,6 +256,15 @@ int moe_oracle_router(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_
 }
 
 /*
+ * Expert capacity ("Chapter 19", §19.6.1): C = ceil(c * T * K / N) for
+ * capacity factor c > 0. Returns -1 (no cap) for c <= 0.
+ */
+int64_t moe_oracle_capacity(double c, int64_t T, int32_t K, int32_t N) {
+  if (!(c > 0.0)) return -1;
+  return (int64_t)ceil(c * (double)T * (double)K / (double)N);
+}
+
+/*
  * Route and pack ("Chapter 19", §19.6.3): a counting sort of the T*K token
  * copies by expert.
  *   counts[e]    = number of copies whose expert is e (histogram)
@@ -266,6 +275,49 @@ int moe_oracle_router(int64_t T, int32_t d, int32_t N, int32_t K, int32_t score_
  *   inv_row[t*K+k] = r, the inverse permutation.
  * Returns ORACLE_ERR_ARG if an index lies outside [0, N).
  */
+/*
+ * With a capacity cap >= 0 ("Chapter 19", §19.6.1 "capacity-limited";
+ * "Mixture of Experts Explained", "Routing collapses unless you stop it":
+ * copies beyond the cap skip the FFN and pass on the residual alone), only the
+ * first `cap` copies of each expert in (t, k) order are placed: offsets count
+ * kept copies, inv_row of a dropped copy is -1, counts still count every copy
+ * routed to the expert. cap < 0: no cap.
+ */
+int moe_oracle_permute_cap(int64_t T, int32_t K, int32_t N, int64_t cap, const int32_t* topk_idx,
+                           int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv_row) {
+  if (T < 0 || K <= 0 || N <= 0 || !counts || !offsets) return ORACLE_ERR_ARG;
+  if (T > 0 && (!topk_idx || !perm_src || !inv_row)) return ORACLE_ERR_ARG;
+  const int64_t n = T * K;
+  for (int32_t e = 0; e < N; ++e) counts[e] = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t e = topk_idx[i];
+    if (e < 0 || e >= N) return ORACLE_ERR_ARG;
+    counts[e] += 1;
+  }
+  offsets[0] = 0;
+  for (int32_t e = 0; e < N; ++e) {
+    int64_t kept = counts[e];
+    if (cap >= 0 && kept > cap) kept = cap;
+    offsets[e + 1] = offsets[e] + (int32_t)kept;
+  }
+  int32_t* seen = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  if (!seen) return ORACLE_ERR_ARG;
+  for (int32_t e = 0; e < N; ++e) seen[e] = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t e = topk_idx[i];
+    int32_t rank = seen[e]++;
+    if (cap >= 0 && rank >= cap) {
+      inv_row[i] = -1;
+      continue;
+    }
+    int32_t r = offsets[e] + rank;
+    perm_src[r] = (int32_t)i;
+    inv_row[i] = r;
+  }
+  free(seen);
+  return ORACLE_OK;
+}
+
 int moe_oracle_permute(int64_t T, int32_t K, int32_t N, const int32_t* topk_idx,
                        int32_t* counts, int32_t* offsets, int32_t* perm_src,
                        int32_t* inv_row) {
@@ -348,6 +400,9 @@ void moe_oracle_combine(int32_t K, int32_t d, const double* w, const double* y,
  * a NULL pointer means "not provided" and is an error only if a token picks it.
  *   w_gate[e], w_up[e]: bf16 [F][d];  w_down[e]: bf16 [d][F]
  *   ws_gate[s], ws_up[s]: bf16 [Fs][d]; ws_down[s]: bf16 [d][Fs]
+ * keep: uint8 [n][K] or NULL; keep[t][k] == 0 marks a copy dropped by its
+ * expert's capacity: it contributes nothing (topk_w still reports the router's
+ * weight; the kept weights are not renormalised).
  * Outputs: topk_idx [n][K], topk_w fp64 [n][K], margin fp64 [n], out fp64 [n][d].
  */
 int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
@@ -357,8 +412,8 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
                      const float* sel_bias, const uint16_t* const* w_gate,
                      const uint16_t* const* w_up, const uint16_t* const* w_down,
                      const uint16_t* const* ws_gate, const uint16_t* const* ws_up,
-                     const uint16_t* const* ws_down, int32_t* topk_idx, double* topk_w,
-                     double* margin, double* out) {
+                     const uint16_t* const* ws_down, const unsigned char* keep,
+                     int32_t* topk_idx, double* topk_w, double* margin, double* out) {
   if (!router_args_ok(n_rows, d, N, K, score_fn, n_groups, topk_groups, hidden, w_router))
     return ORACLE_ERR_ARG;
   if (F <= 0 || S < 0 || (S > 0 && Fs <= 0)) return ORACLE_ERR_ARG;
@@ -379,7 +434,8 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
     double* y = (double*)malloc(sizeof(double) * (size_t)K * (size_t)d);
     double* sh = (double*)malloc(sizeof(double) * (size_t)d);
     double* ys = (double*)malloc(sizeof(double) * (size_t)d);
-    if (!l32 || !prob || !key || !taken || !order || !x || !h || !y || !sh || !ys) {
+    double* wk = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!l32 || !prob || !key || !taken || !order || !x || !h || !y || !sh || !ys || !wk) {
 #pragma omp atomic write
       status = ORACLE_ERR_ARG;
     } else {
@@ -408,11 +464,13 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
           moe_oracle_expert_ffn(d, Fs, x, ws_gate[s], ws_up[s], ws_down[s], h, ys);
           for (int32_t i = 0; i < d; ++i) sh[i] += ys[i];
         }
-        moe_oracle_combine(K, d, w, y, S > 0 ? sh : NULL, out + t * d);
+        /* a copy dropped by its expert's capacity contributes nothing */
+        for (int32_t k = 0; k < K; ++k) wk[k] = (keep && !keep[t * K + k]) ? 0.0 : w[k];
+        moe_oracle_combine(K, d, wk, y, S > 0 ? sh : NULL, out + t * d);
       }
     }
     free(l32); free(prob); free(key); free(taken); free(order);
-    free(x); free(h); free(y); free(sh); free(ys);
+    free(x); free(h); free(y); free(sh); free(ys); free(wk);
   }
   return status;
 }

@@ -43,11 +43,15 @@ def _load():
         lib.moe_oracle_router.restype = ctypes.c_int
         lib.moe_oracle_permute.argtypes = [i64, i32, i32, P, P, P, P, P]
         lib.moe_oracle_permute.restype = ctypes.c_int
+        lib.moe_oracle_permute_cap.argtypes = [i64, i32, i32, i64, P, P, P, P, P]
+        lib.moe_oracle_permute_cap.restype = ctypes.c_int
+        lib.moe_oracle_capacity.argtypes = [ctypes.c_double, i64, i32, i32]
+        lib.moe_oracle_capacity.restype = i64
         lib.moe_oracle_expert_ffn.argtypes = [i32, i32, P, P, P, P, P, P]
         lib.moe_oracle_expert_ffn.restype = None
         lib.moe_oracle_combine.argtypes = [i32, i32, P, P, P, P]
         lib.moe_oracle_combine.restype = None
-        lib.moe_oracle_layer.argtypes = [i64] + [i32] * 10 + [P] * 14
+        lib.moe_oracle_layer.argtypes = [i64] + [i32] * 10 + [P] * 15
         lib.moe_oracle_layer.restype = ctypes.c_int
         lib.moe_oracle_silu.argtypes = [ctypes.c_double]
         lib.moe_oracle_silu.restype = ctypes.c_double
@@ -121,16 +125,30 @@ def router(hidden, w_router, K, score_fn=SOFTMAX, renormalize=1, router_bias=Non
     return dict(logits=logits, probs=probs, keys=keys, idx=idx, w=w, margin=margin)
 
 
-def permute(topk_idx, N):
+def capacity(capacity_factor, T, K, N):
+    """C = ceil(c T K / N), or -1 for no cap (c <= 0)."""
+    return int(_load().moe_oracle_capacity(float(capacity_factor), T, K, N))
+
+
+def permute(topk_idx, N, capacity_factor=0.0):
     """Counting sort of the token copies by expert. Returns counts, offsets,
-    perm_src, inv_row (int32)."""
+    perm_src, inv_row (int32). With capacity_factor > 0 only the first
+    ceil(c T K / N) copies of each expert (token order) are placed: offsets
+    count kept copies, perm_src lists them, inv_row is -1 for dropped ones."""
     lib = _load()
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
     T, K = idx.shape
     counts = np.empty((N,), np.int32)
     offsets = np.empty((N + 1,), np.int32)
-    perm_src = np.empty((T * K,), np.int32)
+    perm_src = np.full((T * K,), -1, np.int32)
     inv_row = np.empty((T * K,), np.int32)
+    if capacity_factor > 0:
+        cap = capacity(capacity_factor, T, K, N)
+        rc = lib.moe_oracle_permute_cap(T, K, N, cap, _ptr(idx), _ptr(counts), _ptr(offsets),
+                                        _ptr(perm_src), _ptr(inv_row))
+        if rc != 0:
+            raise ValueError(f"moe_oracle_permute_cap failed ({rc})")
+        return dict(counts=counts, offsets=offsets, perm_src=perm_src, inv_row=inv_row)
     rc = lib.moe_oracle_permute(T, K, N, _ptr(idx), _ptr(counts), _ptr(offsets), _ptr(perm_src),
                                 _ptr(inv_row))
     if rc != 0:
@@ -180,12 +198,13 @@ def _ptr_array(mats, n):
 
 def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormalize=1,
           router_bias=None, sel_bias=None, ws_gate=None, ws_up=None, ws_down=None, n_groups=0,
-          topk_groups=0):
+          topk_groups=0, keep=None):
     """The whole layer for the rows of `hidden` (fp32 [n][d]).
 
     w_gate / w_up / w_down: sequences of N per-expert bf16 matrices (uint16 bit
     patterns or torch bf16), an entry may be None if no token picks it.
     ws_*: sequences of S shared-expert matrices or None.
+    keep: uint8 [n][K] or None; 0 marks a copy dropped by its expert's capacity.
     Returns dict(idx, w, margin, out) with out fp64 [n][d].
     """
     lib = _load()
@@ -203,6 +222,7 @@ def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormali
     su_arr, k5 = _ptr_array(ws_up, max(S, 1))
     sd_arr, k6 = _ptr_array(ws_down, max(S, 1))
     rb, sb = _f32(router_bias), _f32(sel_bias)
+    keep_a = None if keep is None else np.ascontiguousarray(keep, dtype=np.uint8)
     idx = np.empty((n, K), np.int32)
     w = np.empty((n, K), np.float64)
     margin = np.empty((n,), np.float64)
@@ -215,7 +235,7 @@ def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormali
                               ctypes.cast(sg_arr, ctypes.c_void_p) if S else None,
                               ctypes.cast(su_arr, ctypes.c_void_p) if S else None,
                               ctypes.cast(sd_arr, ctypes.c_void_p) if S else None,
-                              _ptr(idx), _ptr(w), _ptr(margin), _ptr(out))
+                              _ptr(keep_a), _ptr(idx), _ptr(w), _ptr(margin), _ptr(out))
     del k1, k2, k3, k4, k5, k6
     if rc != 0:
         raise ValueError(f"moe_oracle_layer failed ({rc})")

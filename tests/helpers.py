@@ -44,9 +44,17 @@ def oracle_router(cfg, ins, rows=None):
                          topk_groups=cfg.topk_groups)
 
 
-def oracle_layer_rows(cfg, ins, rows):
+def capacity_keep(cfg, topk_idx):
+    """uint8 [T][K]: 1 where a copy survives its expert's capacity, computed by
+    the oracle's capacity-limited permutation of the given routing."""
+    inv = oracle.permute(np.asarray(topk_idx, np.int32), cfg.N, capacity_factor=cfg.capacity_factor)["inv_row"]
+    return (inv >= 0).reshape(-1, cfg.K).astype(np.uint8)
+
+
+def oracle_layer_rows(cfg, ins, rows, keep=None):
     """Oracle layer output for the given token rows. Only the experts those
-    tokens pick are copied to the host."""
+    tokens pick are copied to the host. keep: uint8 [len(rows)][K] capacity
+    mask, or None (dropless)."""
     rows = np.asarray(rows, dtype=np.int64)
     r = oracle_router(cfg, ins, rows)
     used = sorted(set(r["idx"].reshape(-1).tolist()))
@@ -65,7 +73,7 @@ def oracle_layer_rows(cfg, ins, rows):
     return oracle.layer(hidden_f32(ins)[rows], np32(ins["w_router"]), wg, wu, wd, K=cfg.K,
                         score_fn=cfg.score_fn, renormalize=cfg.renormalize,
                         router_bias=np32(ins.get("router_bias")), sel_bias=np32(ins.get("sel_bias")),
-                        n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, **sh)
+                        n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, keep=keep, **sh)
 
 
 def output_errors(gpu: np.ndarray, ref: np.ndarray) -> dict:

@@ -52,6 +52,11 @@ MID = {
                                         topk_groups=3),
     "grouped_softmax_f32": inputs.MoEConfig("grouped_softmax_f32", T=100, d=64, N=32, K=4, F=64,
                                             hidden_dtype="f32", n_groups=16, topk_groups=2),
+    # capacity-limited routing: copies beyond ceil(c T K / N) per expert are dropped
+    "capacity_ragged": inputs.MoEConfig("capacity_ragged", T=300, d=264, N=16, K=4, F=392,
+                                        capacity_factor=0.75),
+    "capacity_small_f32": inputs.MoEConfig("capacity_small_f32", T=40, d=128, N=8, K=2, F=64,
+                                           hidden_dtype="f32", capacity_factor=0.6),
     # mean expert group >= 256 rows: 256-row tiles on 2-CTA clusters
     "pair_ragged": inputs.MoEConfig("pair_ragged", T=700, d=264, N=4, K=2, F=392),
     "pair_shared_sigmoid": inputs.MoEConfig("pair_shared_sigmoid", T=520, d=192, N=2, K=1, F=136, S=1,
@@ -76,9 +81,12 @@ def test_layer_matches_oracle(name):
     cfg = MID[name]
     ins, dev = H.make_case(cfg)
     out, idx, w, counts = _run_layer(cfg, dev)
-    ref = H.oracle_layer_rows(cfg, ins, np.arange(cfg.T))
+    cap_keep = H.capacity_keep(cfg, idx) if cfg.capacity_factor > 0 else None
+    ref = H.oracle_layer_rows(cfg, ins, np.arange(cfg.T), keep=cap_keep)
     rep = H.compare_router(idx, w, ref)
     assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
+    if cap_keep is not None:
+        assert cap_keep.min() == 0  # the case does drop copies
     keep = np.ones(cfg.T, bool)
     keep[rep["flipped_tokens"]] = False
     H.assert_output_close(out.float().cpu().numpy()[keep], ref["out"][keep], name)
@@ -167,8 +175,8 @@ PERMUTE_CASES = [(1, 8, 2, False), (37, 8, 2, False), (500, 64, 6, True), (1000,
 
 
 @pytest.mark.parametrize("T,N,K,skew", PERMUTE_CASES)
-@pytest.mark.parametrize("hidden_dtype", ["bf16", "f32"])
-def test_permute_bit_exact(T, N, K, skew, hidden_dtype):
+@pytest.mark.parametrize("hidden_dtype,capacity_factor", [("bf16", 0.0), ("f32", 0.0), ("bf16", 0.8)])
+def test_permute_bit_exact(T, N, K, skew, hidden_dtype, capacity_factor):
     rng = np.random.default_rng(T + N)
     p_e = None
     if skew:
@@ -176,7 +184,8 @@ def test_permute_bit_exact(T, N, K, skew, hidden_dtype):
         p_e /= p_e.sum()
     idx = np.stack([rng.choice(N, size=K, replace=False, p=p_e) for _ in range(T)]).astype(np.int32)
     d = 136
-    cfg = inputs.MoEConfig("perm", T=T, d=d, N=N, K=K, F=8, hidden_dtype=hidden_dtype)
+    cfg = inputs.MoEConfig("perm", T=T, d=d, N=N, K=K, F=8, hidden_dtype=hidden_dtype,
+                           capacity_factor=capacity_factor)
     hidden = inputs.make_router_inputs(cfg, seed=3)["hidden"]
     p = B.problem(cfg)
     ws = B.new_workspace(p, B.CALL_PERMUTE)
@@ -188,11 +197,14 @@ def test_permute_bit_exact(T, N, K, skew, hidden_dtype):
     B.permute(p, _dev(torch.from_numpy(idx)), _dev(hidden), counts, offsets, perm_src, inv_row, x_perm, ws)
     torch.cuda.synchronize()
     assert B.get_device_status(ws) == 0
-    ref = oracle.permute(idx, N)
-    for k in ("counts", "offsets", "perm_src", "inv_row"):
-        assert np.array_equal(locals()[k].cpu().numpy(), ref[k]), k
-    expect = hidden.to(torch.bfloat16)[torch.from_numpy(ref["perm_src"] // K).long()]
-    assert torch.equal(x_perm.cpu().view(torch.int16), expect.view(torch.int16))
+    ref = oracle.permute(idx, N, capacity_factor=capacity_factor)
+    placed = int(ref["offsets"][-1])
+    got = dict(counts=counts, offsets=offsets, perm_src=perm_src, inv_row=inv_row)
+    for k in ("counts", "offsets", "inv_row"):
+        assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+    assert np.array_equal(perm_src.cpu().numpy()[:placed], ref["perm_src"][:placed])
+    expect = hidden.to(torch.bfloat16)[torch.from_numpy(ref["perm_src"][:placed] // K).long()]
+    assert torch.equal(x_perm.cpu()[:placed].view(torch.int16), expect.view(torch.int16))
 
 
 def test_permute_reports_out_of_range_index():
@@ -250,11 +262,14 @@ def test_grouped_swiglu_matches_oracle(d, F, N, K, T):
 
 
 # --------------------------------------------------------------------------- combine
-@pytest.mark.parametrize("T,K,d,shared", [(1, 1, 8, False), (77, 2, 136, True), (300, 8, 512, False)])
-def test_combine_matches_oracle(T, K, d, shared):
+@pytest.mark.parametrize("T,K,d,shared,dropped", [(1, 1, 8, False, 0), (77, 2, 136, True, 0),
+                                                  (300, 8, 512, False, 0), (64, 4, 64, True, 40)])
+def test_combine_matches_oracle(T, K, d, shared, dropped):
     g = torch.Generator().manual_seed(T * K)
     y = torch.randn(T * K, d, generator=g).to(torch.bfloat16)
     perm = torch.randperm(T * K, generator=g).to(torch.int32)          # inv_row: a bijection
+    if dropped:  # copies dropped by capacity: inv_row -1, they contribute nothing
+        perm[torch.randperm(T * K, generator=g)[:dropped]] = -1
     w = torch.rand(T, K, generator=g)
     w = (w / w.sum(1, keepdim=True)).float()
     sh = torch.randn(T, d, generator=g).to(torch.bfloat16) if shared else None
@@ -264,7 +279,9 @@ def test_combine_matches_oracle(T, K, d, shared):
     B.combine(p, y.cuda(), perm.cuda(), w.cuda(), out, shared_out=_dev(sh))
     torch.cuda.synchronize()
     yf = y.double().numpy()
-    ref = np.stack([oracle.combine(w[t].double().numpy(), yf[perm[t * K:(t + 1) * K].long().numpy()],
+    rows = perm.long().numpy().reshape(T, K)
+    wk = w.double().numpy() * (rows >= 0)
+    ref = np.stack([oracle.combine(wk[t], yf[np.maximum(rows[t], 0)],
                                    None if sh is None else sh[t].double().numpy()) for t in range(T)])
     got = out.double().cpu().numpy()
     # one bf16 rounding of an fp32 sum: at most half an ulp of bf16 plus fp32 noise
@@ -304,7 +321,7 @@ def _sample_rows(T, n, seed=0):
 
 
 FULL = [("mixtral", inputs.MIXTRAL, 12), ("gptoss", inputs.GPTOSS, 12), ("dsv3", inputs.DSV3, 6),
-        ("dsv3_grouped", inputs.DSV3_GROUPED, 6)] + [
+        ("dsv3_grouped", inputs.DSV3_GROUPED, 6), ("mixtral_capacity", inputs.MIXTRAL_CAPACITY, 12)] + [
     (f"qwen_decode_T{T}", inputs.QWEN_DECODE.with_(T=T), 6) for T in inputs.DECODE_BATCHES]
 
 
@@ -328,7 +345,16 @@ def test_full_size_workload(name, cfg, n_sample):
     delta = np.bincount(idx[fl].reshape(-1), minlength=cfg.N) - np.bincount(ref_r["idx"][fl].reshape(-1), minlength=cfg.N)
     assert np.array_equal(counts - ref_counts, delta)
     rows = np.array([r for r in _sample_rows(cfg.T, n_sample) if r not in set(fl.tolist())])
-    ref = H.oracle_layer_rows(cfg, ins, rows)
+    keep = None
+    if cfg.capacity_factor > 0:
+        keep_all = H.capacity_keep(cfg, idx)
+        # sample dropped copies too: the last tokens of the most loaded expert
+        hot = int(np.argmax(counts))
+        late = [t for t in np.nonzero((idx == hot).any(axis=1))[0][-4:] if t not in set(fl.tolist())]
+        rows = np.array(sorted(set(rows.tolist()) | set(late)))
+        keep = keep_all[rows]
+        assert keep_all.min() == 0
+    ref = H.oracle_layer_rows(cfg, ins, rows, keep=keep)
     e = H.assert_output_close(out.float().cpu().numpy()[rows], ref["out"], name)
     print(f"{name}: near ties {rep['near_ties']} (flipped {rep['near_tie_flips']}), errors {e}, "
           f"touched experts {int((counts > 0).sum())}")

@@ -448,3 +448,68 @@ def test_group_limited_routing_against_library_sorts(N, G, M, K):
         cand = np.nonzero(allowed)[0]
         order = cand[np.lexsort((cand, -keys[t][cand]))]
         assert r["idx"][t].tolist() == order[:K].tolist()
+
+
+# ---------------------------------------------------------------------------
+# Capacity-limited routing
+# ---------------------------------------------------------------------------
+
+def test_capacity_formula():
+    """"Chapter 19", §19.6.1: C = ceil(c T K / N)."""
+    assert oracle.capacity(1.0, 4096, 2, 8) == 1024
+    assert oracle.capacity(1.25, 100, 3, 7) == math.ceil(1.25 * 100 * 3 / 7)
+    assert oracle.capacity(0.0, 100, 3, 7) == -1
+
+
+def test_capacity_hand_case_drops_the_later_tokens():
+    """Four tokens all pick expert 0: with c = 1 (C = ceil(4 * 1 / 2) = 2) the
+    first two keep their copy, the last two pass on the residual alone
+    ("Mixture of Experts Explained", 'Routing collapses unless you stop it')."""
+    idx = np.array([[0], [0], [0], [0]], np.int32)
+    p = oracle.permute(idx, 2, capacity_factor=1.0)
+    assert p["counts"].tolist() == [4, 0]
+    assert p["offsets"].tolist() == [0, 2, 2]
+    assert p["perm_src"][:2].tolist() == [0, 1]
+    assert p["inv_row"].tolist() == [0, 1, -1, -1]
+
+
+@pytest.mark.parametrize("c", [0.5, 1.0, 1.25])
+def test_capacity_permute_against_library_sort(c):
+    rng = np.random.default_rng(12)
+    idx = _random_topk(rng, 400, 16, 3, skew=True)
+    cap = oracle.capacity(c, 400, 3, 16)
+    p = oracle.permute(idx, 16, capacity_factor=c)
+    flat = idx.reshape(-1)
+    order = np.argsort(flat, kind="stable")           # library stable sort
+    counts = np.bincount(flat, minlength=16)
+    kept = np.minimum(counts, cap)
+    assert np.array_equal(p["counts"], counts)
+    assert np.array_equal(p["offsets"], np.concatenate([[0], np.cumsum(kept)]))
+    start = np.concatenate([[0], np.cumsum(counts)])
+    expect = np.concatenate([order[start[e]:start[e] + kept[e]] for e in range(16)])
+    assert np.array_equal(p["perm_src"][:kept.sum()], expect)
+    inv = np.full(flat.size, -1)
+    inv[expect] = np.arange(expect.size)
+    assert np.array_equal(p["inv_row"], inv)
+    # a huge factor is dropless
+    q = oracle.permute(idx, 16, capacity_factor=1e6)
+    assert np.array_equal(q["perm_src"], oracle.permute(idx, 16)["perm_src"])
+
+
+def test_layer_keep_mask_drops_whole_copies():
+    """A dropped copy contributes nothing and the kept weights are not
+    renormalised: out = sum over kept k of w_k E_k(x)."""
+    rng = np.random.default_rng(13)
+    T, d, N, K, F = 6, 16, 4, 2, 20
+    x, W = _rand_router_case(rng, T, d, N)
+    wg, wu, wd = _rand_experts(rng, N, d, F)
+    keep = np.ones((T, K), np.uint8)
+    keep[1, 0] = keep[3, 1] = keep[4, :] = 0
+    r = oracle.layer(x, W, wg, wu, wd, K=K, keep=keep)
+    full = oracle.layer(x, W, wg, wu, wd, K=K)
+    assert np.array_equal(r["w"], full["w"])
+    for t in range(T):
+        ref = sum(full["w"][t, k] * _torch_swiglu(x[t].astype(np.float64), wg[r["idx"][t, k]],
+                                                  wu[r["idx"][t, k]], wd[r["idx"][t, k]])
+                  for k in range(K) if keep[t, k]) if keep[t].any() else np.zeros(d)
+        np.testing.assert_allclose(r["out"][t], ref, rtol=1e-10, atol=1e-13)
