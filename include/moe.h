@@ -99,11 +99,12 @@ typedef struct moe_problem {
                             selection keys ("Mixture of Experts for LLM
                             Inference", "Three tricks that tame the
                             all-to-alls": node-limited routing)              */
-  float capacity_factor; /* expert capacity C = ceil(c * T * K / N) for c > 0
+  double capacity_factor; /* expert capacity C = ceil(c * T * K / N) for c > 0
                             ("Chapter 19", §19.6.1); copies beyond the first
                             C of an expert (token order) are dropped: they
                             skip the FFN and contribute nothing, the kept
-                            weights are not renormalised. 0: dropless     */
+                            weights are not renormalised; C is computed in
+                            double precision. 0: dropless                  */
 } moe_problem_t;
 
 /*

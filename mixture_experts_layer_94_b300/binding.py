@@ -36,7 +36,7 @@ class Problem(ctypes.Structure):
                 ("shared_ffn", ctypes.c_int32), ("score_fn", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("hidden_dtype", ctypes.c_int32),
                 ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_double)]
 
 
 class Weights(ctypes.Structure):

@@ -70,8 +70,8 @@ namespace moe {
 // Expert capacity C = ceil(c * T * K / N) ("Chapter 19", §19.6.1), computed in
 // double; INT32_MAX when c == 0 (dropless).
 int32_t expert_capacity(const moe_problem_t& p) {
-  if (!(p.capacity_factor > 0.f)) return 2147483647;
-  const double c = ceil((double)p.capacity_factor * (double)p.T * (double)p.top_k / (double)p.n_experts);
+  if (!(p.capacity_factor > 0.0)) return 2147483647;
+  const double c = ceil(p.capacity_factor * (double)p.T * (double)p.top_k / (double)p.n_experts);
   return c >= 2147483647.0 ? 2147483647 : (int32_t)c;
 }
 }  // namespace moe
@@ -278,7 +278,7 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (p->renormalize != 0 && p->renormalize != 1) return MOE_ERR_INVALID_ARG;
   if (p->hidden_dtype != MOE_F32 && p->hidden_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (p->n_groups < 0) return MOE_ERR_INVALID_ARG;
-  if (!(p->capacity_factor >= 0.f) || p->capacity_factor > 1e30f) return MOE_ERR_INVALID_ARG;  // NaN fails too
+  if (!(p->capacity_factor >= 0.0) || p->capacity_factor > 1e30) return MOE_ERR_INVALID_ARG;  // NaN fails too
   if (p->n_groups > 1) {
     if (p->n_experts % p->n_groups != 0 || p->topk_groups < 1 || p->topk_groups > p->n_groups)
       return MOE_ERR_INVALID_ARG;

@@ -101,3 +101,9 @@ def test_workspace_sizing_for_empty_and_single_token_batches(cfg):
 ])
 def test_problem_check_group_limited_routing(kw, status):
     assert B.problem_check(B.problem(inputs.TINY, **kw)) == status
+
+
+def test_problem_check_capacity_factor():
+    assert B.problem_check(B.problem(inputs.TINY, capacity_factor=0.6)) == 0
+    assert B.problem_check(B.problem(inputs.TINY, capacity_factor=-1.0)) == -1
+    assert B.problem_check(B.problem(inputs.TINY, capacity_factor=float("nan"))) == -1
