@@ -389,6 +389,161 @@ void moe_oracle_combine(int32_t K, int32_t d, const double* w, const double* y,
 }
 
 /*
+ * Expert-choice routing ("Mixture of Experts for LLM Inference", "Token choice
+ * vs expert choice": each expert picks its own top tokens up to a fixed
+ * capacity; "Chapter 19", §19.6.1 "Expert Choice"; "Mixture of Experts
+ * Explained", "Expert-choice versus token-choice routing").
+ *   1. logits as in the router (fp64 sum, rounded to fp32), + router_bias;
+ *   2. score S[t][e]: softmax over the N experts of token t, or sigmoid;
+ *      rounded to fp32 (the precision the selection is decided in);
+ *   3. expert e takes the C tokens with the largest S[.][e] (equal scores:
+ *      lower token first); its rows list them in ascending token order;
+ *      row weight = S[t][e] in fp64 (no renormalisation);
+ *   4. margin[e] = S of e's C-th pick minus S of its (C+1)-th (fp32 values),
+ *      +inf when C >= T.
+ * Outputs: row_token [N][C], row_w fp64 [N][C], margin fp64 [N].
+ */
+int moe_oracle_expert_choice(int64_t T, int32_t d, int32_t N, int32_t score_fn, int64_t C,
+                             const float* hidden, const float* w_router, const float* router_bias,
+                             int32_t* row_token, double* row_w, double* margin) {
+  if (T <= 0 || d <= 0 || N <= 0 || C <= 0 || C > T || !hidden || !w_router) return ORACLE_ERR_ARG;
+  if (!row_token || !row_w || !margin || (score_fn != 0 && score_fn != 1)) return ORACLE_ERR_ARG;
+  double* s64 = (double*)malloc(sizeof(double) * (size_t)T * (size_t)N);
+  float* s32 = (float*)malloc(sizeof(float) * (size_t)T * (size_t)N);
+  if (!s64 || !s32) {
+    free(s64);
+    free(s32);
+    return ORACLE_ERR_ARG;
+  }
+#pragma omp parallel for schedule(dynamic, 8)
+  for (int64_t t = 0; t < T; ++t) {
+    float l[256];
+    for (int32_t e = 0; e < N; ++e) {
+      double acc = 0.0;
+      for (int32_t j = 0; j < d; ++j) acc += (double)hidden[t * d + j] * (double)w_router[(int64_t)j * N + e];
+      if (router_bias) acc += (double)router_bias[e];
+      l[e] = (float)acc;
+    }
+    if (score_fn == 0) {
+      double mx = -INFINITY, z = 0.0;
+      for (int32_t e = 0; e < N; ++e) if ((double)l[e] > mx) mx = (double)l[e];
+      for (int32_t e = 0; e < N; ++e) z += exp((double)l[e] - mx);
+      for (int32_t e = 0; e < N; ++e) s64[t * N + e] = exp((double)l[e] - mx) / z;
+    } else {
+      for (int32_t e = 0; e < N; ++e) s64[t * N + e] = sigmoid((double)l[e]);
+    }
+    for (int32_t e = 0; e < N; ++e) s32[t * N + e] = (float)s64[t * N + e];
+  }
+  int status = ORACLE_OK;
+#pragma omp parallel
+  {
+    unsigned char* picked = (unsigned char*)malloc((size_t)T);
+    if (!picked) {
+#pragma omp atomic write
+      status = ORACLE_ERR_ARG;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int32_t e = 0; e < N; ++e) {
+        for (int64_t t = 0; t < T; ++t) picked[t] = 0;
+        float last = 0.f;
+        for (int64_t c = 0; c < C; ++c) { /* selection: largest score, lower token on ties */
+          int64_t best = -1;
+          for (int64_t t = 0; t < T; ++t) {
+            if (picked[t]) continue;
+            if (best < 0 || s32[t * N + e] > s32[best * N + e]) best = t;
+          }
+          picked[best] = 1;
+          last = s32[best * N + e];
+        }
+        double gap = INFINITY;
+        if (C < T) {
+          int64_t next = -1;
+          for (int64_t t = 0; t < T; ++t) {
+            if (picked[t]) continue;
+            if (next < 0 || s32[t * N + e] > s32[next * N + e]) next = t;
+          }
+          gap = (double)last - (double)s32[next * N + e];
+        }
+        margin[e] = gap;
+        int64_t r = 0;
+        for (int64_t t = 0; t < T; ++t) {
+          if (!picked[t]) continue;
+          row_token[(int64_t)e * C + r] = (int32_t)t;
+          row_w[(int64_t)e * C + r] = s64[t * N + e];
+          ++r;
+        }
+      }
+    }
+    free(picked);
+  }
+  free(s64);
+  free(s32);
+  return status;
+}
+
+/*
+ * The layer under a given routing: out[t] = sum_k w[t][k] * E_{idx[t][k]}(x_t)
+ * (+ the shared experts), skipping slots with idx < 0. Used for expert-choice
+ * routing, where the number of experts per token varies (0..N).
+ *   idx int32 [n][M], w fp64 [n][M]; other arguments as moe_oracle_layer.
+ */
+int moe_oracle_layer_routed(int64_t n_rows, int32_t d, int32_t N, int32_t M, int32_t F, int32_t S,
+                            int32_t Fs, const float* hidden, const int32_t* idx, const double* w,
+                            const uint16_t* const* w_gate, const uint16_t* const* w_up,
+                            const uint16_t* const* w_down, const uint16_t* const* ws_gate,
+                            const uint16_t* const* ws_up, const uint16_t* const* ws_down, double* out) {
+  if (n_rows < 0 || d <= 0 || N <= 0 || M <= 0 || F <= 0 || S < 0 || (S > 0 && Fs <= 0)) return ORACLE_ERR_ARG;
+  if (!hidden || !idx || !w || !w_gate || !w_up || !w_down || !out) return ORACLE_ERR_ARG;
+  if (S > 0 && (!ws_gate || !ws_up || !ws_down)) return ORACLE_ERR_ARG;
+  const int32_t Fmax = (S > 0 && Fs > F) ? Fs : F;
+  int status = ORACLE_OK;
+#pragma omp parallel
+  {
+    double* x = (double*)malloc(sizeof(double) * (size_t)d);
+    double* h = (double*)malloc(sizeof(double) * (size_t)Fmax);
+    double* y = (double*)malloc(sizeof(double) * (size_t)M * (size_t)d);
+    double* wk = (double*)malloc(sizeof(double) * (size_t)M);
+    double* sh = (double*)malloc(sizeof(double) * (size_t)d);
+    double* ys = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!x || !h || !y || !wk || !sh || !ys) {
+#pragma omp atomic write
+      status = ORACLE_ERR_ARG;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t t = 0; t < n_rows; ++t) {
+        for (int32_t j = 0; j < d; ++j) x[j] = (double)hidden[t * d + j];
+        int bad = 0;
+        for (int32_t k = 0; k < M; ++k) {
+          const int32_t e = idx[t * M + k];
+          wk[k] = 0.0;
+          for (int32_t i = 0; i < d; ++i) y[(int64_t)k * d + i] = 0.0;
+          if (e < 0) continue;
+          if (e >= N || !w_gate[e] || !w_up[e] || !w_down[e]) {
+            bad = 1;
+            break;
+          }
+          moe_oracle_expert_ffn(d, F, x, w_gate[e], w_up[e], w_down[e], h, y + (int64_t)k * d);
+          wk[k] = w[t * M + k];
+        }
+        if (bad) {
+#pragma omp atomic write
+          status = ORACLE_ERR_MISSING_EXPERT;
+          continue;
+        }
+        for (int32_t i = 0; i < d; ++i) sh[i] = 0.0;
+        for (int32_t s = 0; s < S; ++s) {
+          moe_oracle_expert_ffn(d, Fs, x, ws_gate[s], ws_up[s], ws_down[s], h, ys);
+          for (int32_t i = 0; i < d; ++i) sh[i] += ys[i];
+        }
+        moe_oracle_combine(M, d, wk, y, S > 0 ? sh : NULL, out + t * d);
+      }
+    }
+    free(x); free(h); free(y); free(wk); free(sh); free(ys);
+  }
+  return status;
+}
+
+/*
  * The whole layer for `n_rows` tokens whose hidden rows are given (fp32
  * [n_rows][d]): router, top-K, every chosen expert's FFN, the always-on shared
  * experts ("Mixture of Experts for LLM Inference", "Shared experts": they run

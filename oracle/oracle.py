@@ -53,6 +53,10 @@ def _load():
         lib.moe_oracle_combine.restype = None
         lib.moe_oracle_layer.argtypes = [i64] + [i32] * 10 + [P] * 15
         lib.moe_oracle_layer.restype = ctypes.c_int
+        lib.moe_oracle_expert_choice.argtypes = [i64, i32, i32, i32, i64, P, P, P, P, P, P]
+        lib.moe_oracle_expert_choice.restype = ctypes.c_int
+        lib.moe_oracle_layer_routed.argtypes = [i64] + [i32] * 6 + [P] * 10
+        lib.moe_oracle_layer_routed.restype = ctypes.c_int
         lib.moe_oracle_silu.argtypes = [ctypes.c_double]
         lib.moe_oracle_silu.restype = ctypes.c_double
         lib.moe_oracle_num_threads.argtypes = []
@@ -240,3 +244,77 @@ def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormali
     if rc != 0:
         raise ValueError(f"moe_oracle_layer failed ({rc})")
     return dict(idx=idx, w=w, margin=margin, out=out)
+
+
+def expert_choice_capacity(capacity_factor, T, K, N):
+    """Tokens each expert takes under expert-choice routing: ceil(c T K / N)
+    (c = 1 when not given), at most T."""
+    c = capacity(capacity_factor if capacity_factor > 0 else 1.0, T, K, N)
+    return min(c, T)
+
+
+def expert_choice(hidden, w_router, C, score_fn=SOFTMAX, router_bias=None):
+    """Expert-choice selection over the rows of `hidden`: each expert's C
+    tokens (ascending), their scores and the per-expert selection margin.
+    Returns dict(row_token int32 [N][C], row_w fp64 [N][C], margin fp64 [N])."""
+    lib = _load()
+    x = _f32(hidden)
+    W = _f32(w_router)
+    T, d = x.shape
+    N = W.shape[1]
+    rb = _f32(router_bias)
+    row_token = np.empty((N, C), np.int32)
+    row_w = np.empty((N, C), np.float64)
+    margin = np.empty((N,), np.float64)
+    rc = lib.moe_oracle_expert_choice(T, d, N, score_fn, C, _ptr(x), _ptr(W), _ptr(rb), _ptr(row_token),
+                                      _ptr(row_w), _ptr(margin))
+    if rc != 0:
+        raise ValueError(f"moe_oracle_expert_choice failed ({rc})")
+    return dict(row_token=row_token, row_w=row_w, margin=margin)
+
+
+def routing_from_expert_choice(row_token, row_w, T):
+    """Per-token (expert, weight) lists, expert ascending, padded with -1 / 0."""
+    N, C = row_token.shape
+    lists = [[] for _ in range(T)]
+    for e in range(N):
+        for j in range(C):
+            lists[row_token[e, j]].append((e, row_w[e, j]))
+    M = max(1, max(len(v) for v in lists))
+    idx = np.full((T, M), -1, np.int32)
+    w = np.zeros((T, M), np.float64)
+    for t, v in enumerate(lists):
+        for k, (e, ww) in enumerate(v):
+            idx[t, k], w[t, k] = e, ww
+    return idx, w
+
+
+def layer_routed(hidden, idx, w, w_gate, w_up, w_down, ws_gate=None, ws_up=None, ws_down=None):
+    """out[t] = sum_k w[t][k] E_{idx[t][k]}(x_t) (+ shared), slots with idx < 0 skipped."""
+    lib = _load()
+    x = _f32(hidden)
+    n, d = x.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = _f64(w)
+    M = idx.shape[1]
+    N = len(w_gate)
+    F = next(_bf16_bits(m).shape[0] for m in w_gate if m is not None)
+    S = 0 if ws_gate is None else len(ws_gate)
+    Fs = _bf16_bits(ws_gate[0]).shape[0] if S else 0
+    g_arr, k1 = _ptr_array(w_gate, N)
+    u_arr, k2 = _ptr_array(w_up, N)
+    d_arr, k3 = _ptr_array(w_down, N)
+    sg_arr, k4 = _ptr_array(ws_gate, max(S, 1))
+    su_arr, k5 = _ptr_array(ws_up, max(S, 1))
+    sd_arr, k6 = _ptr_array(ws_down, max(S, 1))
+    out = np.empty((n, d), np.float64)
+    rc = lib.moe_oracle_layer_routed(n, d, N, M, F, S, Fs, _ptr(x), _ptr(idx), _ptr(w),
+                                     ctypes.cast(g_arr, ctypes.c_void_p), ctypes.cast(u_arr, ctypes.c_void_p),
+                                     ctypes.cast(d_arr, ctypes.c_void_p),
+                                     ctypes.cast(sg_arr, ctypes.c_void_p) if S else None,
+                                     ctypes.cast(su_arr, ctypes.c_void_p) if S else None,
+                                     ctypes.cast(sd_arr, ctypes.c_void_p) if S else None, _ptr(out))
+    del k1, k2, k3, k4, k5, k6
+    if rc != 0:
+        raise ValueError(f"moe_oracle_layer_routed failed ({rc})")
+    return out

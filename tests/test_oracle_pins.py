@@ -513,3 +513,71 @@ def test_layer_keep_mask_drops_whole_copies():
                                                   wu[r["idx"][t, k]], wd[r["idx"][t, k]])
                   for k in range(K) if keep[t, k]) if keep[t].any() else np.zeros(d)
         np.testing.assert_allclose(r["out"][t], ref, rtol=1e-10, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Expert-choice routing
+# ---------------------------------------------------------------------------
+
+def test_expert_choice_hand_case():
+    """"Mixture of Experts for LLM Inference", 'Token choice vs expert choice':
+    each expert picks its own top tokens up to a fixed capacity; a token nobody
+    picks is skipped for that layer."""
+    logits = np.array([[2.0, 0.0], [0.0, 2.0], [1.0, 1.0], [3.0, 0.0]], np.float32)
+    W = np.eye(2, dtype=np.float32)
+    # softmax scores: expert 0 column [0.881, 0.119, 0.5, 0.953]; expert 1 [0.119, 0.881, 0.5, 0.047]
+    r = oracle.expert_choice(logits, W, C=2)
+    assert r["row_token"].tolist() == [[0, 3], [1, 2]]
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    np.testing.assert_allclose(r["row_w"], [[p[0, 0], p[3, 0]], [p[1, 1], p[2, 1]]], atol=1e-7)
+    r1 = oracle.expert_choice(logits, W, C=1)
+    assert r1["row_token"].tolist() == [[3], [1]]  # tokens 0 and 2 are picked by nobody
+    idx, w = oracle.routing_from_expert_choice(r1["row_token"], r1["row_w"], 4)
+    assert idx[0].tolist() == [-1] and idx[2].tolist() == [-1]
+
+
+@pytest.mark.parametrize("score_fn", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_expert_choice_against_library_sort(score_fn):
+    """Balanced by construction (every expert takes exactly C tokens) and each
+    expert's tokens are its C best scores (stable: lower token first)."""
+    rng = np.random.default_rng(14)
+    T, d, N = 300, 24, 8
+    x, W = _rand_router_case(rng, T, d, N)
+    C = oracle.expert_choice_capacity(1.0, T, 2, N)
+    assert C == math.ceil(T * 2 / N)
+    r = oracle.expert_choice(x, W, C, score_fn=score_fn)
+    lg = (x.astype(np.float64) @ W.astype(np.float64)).astype(np.float32).astype(np.float64)
+    S = scipy.special.softmax(lg, axis=1) if score_fn == oracle.SOFTMAX else scipy.special.expit(lg)
+    S32 = S.astype(np.float32)
+    for e in range(N):
+        assert r["row_token"].shape[1] == C
+        if r["margin"][e] < 1e-6:
+            continue
+        pick = np.lexsort((np.arange(T), -S32[:, e].astype(np.float64)))[:C]
+        assert r["row_token"][e].tolist() == sorted(pick.tolist())
+        np.testing.assert_allclose(r["row_w"][e], S[r["row_token"][e], e], atol=1e-7)
+
+
+def test_expert_choice_with_every_token_is_the_dense_mixture():
+    """C = T: every expert takes every token, so the layer is
+    sum_e softmax(l)_e E_e(x): the token-choice layer with K = N."""
+    rng = np.random.default_rng(15)
+    T, d, N, F = 9, 16, 4, 24
+    x, W = _rand_router_case(rng, T, d, N)
+    wg, wu, wd = _rand_experts(rng, N, d, F)
+    r = oracle.expert_choice(x, W, C=T)
+    idx, w = oracle.routing_from_expert_choice(r["row_token"], r["row_w"], T)
+    out = oracle.layer_routed(x, idx, w, wg, wu, wd)
+    dense = oracle.layer(x, W, wg, wu, wd, K=N)["out"]
+    np.testing.assert_allclose(out, dense, rtol=1e-9, atol=1e-12)
+
+
+def test_layer_routed_matches_token_choice_layer():
+    """layer_routed under the router's own top-K routing is the token-choice layer."""
+    rng = np.random.default_rng(16)
+    T, d, N, K, F = 7, 16, 6, 2, 20
+    x, W = _rand_router_case(rng, T, d, N)
+    wg, wu, wd = _rand_experts(rng, N, d, F)
+    ref = oracle.layer(x, W, wg, wu, wd, K=K)
+    out = oracle.layer_routed(x, ref["idx"], ref["w"], wg, wu, wd)
+    np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-14)
