@@ -36,6 +36,7 @@ METRIC = "MoE layer tokens/s on 1 B300; % of roofline (bf16 TFLOP/s prefill, HBM
 WORKLOADS = {
     "mixtral": (inputs.MIXTRAL, "Mixtral-8x7B-shaped prefill layer"),
     "mixtral_capacity": (inputs.MIXTRAL_CAPACITY, "Mixtral-8x7B-shaped prefill layer, expert capacity factor 1.0"),
+    "mixtral_ec": (inputs.MIXTRAL_EC, "Mixtral-8x7B-shaped prefill layer, expert-choice routing (C = 1024)"),
     "dsv3": (inputs.DSV3, "DeepSeek-V3-shaped prefill layer"),
     "dsv3_grouped": (inputs.DSV3_GROUPED, "DeepSeek-V3-shaped prefill layer, node-limited routing (4 of 8 groups)"),
     "gptoss": (inputs.GPTOSS, "gpt-oss-120b-shaped layer"),
@@ -200,6 +201,8 @@ def oracle_rows_timed(cfg, ins, rows):
     """Run the oracle layer on the given token rows; returns (tokens, seconds, threads)."""
     from oracle import oracle
 
+    if cfg.routing == "expert":
+        return oracle_rows_timed_expert_choice(cfg, ins, rows)
     x = ins["hidden"].float().cpu().numpy()[rows]
     r = oracle.router(x, ins["w_router"].cpu().numpy(), K=cfg.K, score_fn=cfg.score_fn,
                       renormalize=cfg.renormalize, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
@@ -228,6 +231,26 @@ def oracle_rows_timed(cfg, ins, rows):
                  router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
                  sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), keep=keep,
                  **sh)
+    return len(rows), time.perf_counter() - t0, oracle.num_threads()
+
+
+def oracle_rows_timed_expert_choice(cfg, ins, rows):
+    """Expert choice: the batch-wide selection (untimed), then the given rows'
+    FFNs and combine through the oracle (timed)."""
+    from oracle import oracle
+
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    xa = ins["hidden"].float().cpu().numpy()
+    C = min(math.ceil((cfg.capacity_factor or 1.0) * cfg.T * cfg.K / cfg.N), cfg.T)
+    sel = oracle.expert_choice(xa, ins["w_router"].cpu().numpy(), C, score_fn=cfg.score_fn,
+                               router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy())
+    idx, w = oracle.routing_from_expert_choice(sel["row_token"], sel["row_w"], cfg.T)
+    wts = {k: [bits(ins[k][e]) for e in range(cfg.N)] for k in ("w_gate", "w_up", "w_down")}
+    sh = {}
+    if cfg.S:
+        sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in ("ws_gate", "ws_up", "ws_down")}
+    t0 = time.perf_counter()
+    oracle.layer_routed(xa[rows], idx[rows], w[rows], wts["w_gate"], wts["w_up"], wts["w_down"], **sh)
     return len(rows), time.perf_counter() - t0, oracle.num_threads()
 
 
@@ -276,6 +299,7 @@ def run_reference(args, cfg, desc, world, rank):
 def config_block(cfg, desc, args):
     return {"workload": desc, "T": cfg.T, "d_model": cfg.d, "n_experts": cfg.N, "top_k": cfg.K,
             "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "capacity_factor": cfg.capacity_factor,
+            "routing": cfg.routing,
             "ffn": cfg.F, "n_shared": cfg.S, "shared_ffn": cfg.Fs, "score": cfg.score,
             "hidden_dtype": cfg.hidden_dtype, "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",

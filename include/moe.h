@@ -65,6 +65,7 @@ typedef enum {
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn_t;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing_t;
 
 /* Which call a workspace is sized for (moe_workspace_bytes). */
 typedef enum {
@@ -105,6 +106,11 @@ typedef struct moe_problem {
                             skip the FFN and contribute nothing, the kept
                             weights are not renormalised; C is computed in
                             double precision. 0: dropless                  */
+  int32_t routing;       /* moe_routing_t: token choice (every token picks K
+                            experts) or expert choice (every expert picks
+                            C = min(ceil(c T K / N), T) tokens, c =
+                            capacity_factor or 1 when 0; K is then the mean
+                            number of experts per token)                    */
 } moe_problem_t;
 
 /*
@@ -189,6 +195,7 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden,
  *              offsets[N] rows and counts still count every copy routed to e
  *   x_perm     out bf16 [T*K][d]: x_perm[r] = bf16(hidden[perm_src[r] / K])
  *   ws         workspace of moe_workspace_bytes(p, MOE_CALL_PERMUTE) bytes
+ * Token-choice problems only (MOE_ERR_INVALID_ARG otherwise).
  * The result is deterministic. An index outside [0, N) sets
  * MOE_ERR_DEVICE_BOUNDS in the workspace error word; outputs are then undefined.
  */
@@ -196,6 +203,27 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx,
                          const void* hidden, int32_t* counts, int32_t* offsets,
                          int32_t* perm_src, int32_t* inv_row, void* x_perm,
                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Expert-choice routing ("Mixture of Experts for LLM Inference", "Token choice
+ * vs expert choice": each expert picks its own top tokens up to a fixed
+ * capacity; "Chapter 19", §19.6.1 "Expert Choice"), for problems with
+ * p->routing == MOE_ROUTING_EXPERT_CHOICE:
+ *   score S[t][e] = softmax over the experts of token t's fp32 logits, or
+ *   sigmoid(logit); expert e takes the C tokens with the largest S[.][e]
+ *   (equal scores: lower token first), C = min(ceil(c T K / N), T).
+ *   row_token out int32 [N][C]: expert e's tokens in ascending order
+ *   row_w     out fp32 [N][C]: their scores S[t][e] (not renormalised)
+ *   offsets   out int32 [N+1]: e * C (every expert is full by construction)
+ *   ws        workspace of moe_workspace_bytes(p, MOE_CALL_ROUTER) bytes
+ * A token no expert picks gets no routed contribution. Deterministic.
+ * Requires p->score_fn's router inputs as in moe_router_topk; no selection
+ * bias, no group limit (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status_t moe_expert_choice_select(const moe_problem_t* p, const void* hidden,
+                                      const float* w_router, const float* router_bias,
+                                      int32_t* row_token, float* row_w, int32_t* offsets,
+                                      void* ws, size_t ws_bytes, void* stream);
 
 /*
  * moe_permute_static: the same route and pack as moe_permute, for callers that
@@ -245,6 +273,8 @@ moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t* topk_idx,
  * p->n_shared is ignored here. A shared expert runs through this same call as
  * one group over every token: n_experts = 1, top_k = 1, offsets = {0, T},
  * x_perm = the hidden rows in bf16, weights = that shared expert's.
+ * For an expert-choice problem the packed rows are the N*C picks
+ * (moe_expert_choice_select) and offsets are e*C.
  */
 moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm,
                                 const int32_t* offsets, const void* w_gate,
@@ -281,6 +311,10 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm,
  * The fp32 scatter-add makes `out` reproducible only up to the order of
  * floating-point additions (last-bit differences between runs are possible);
  * the step-wise calls above are bit-reproducible.
+ * With p->routing == MOE_ROUTING_EXPERT_CHOICE the experts pick their tokens
+ * (moe_expert_choice_select) and each picked (token, expert) pair adds
+ * S[t][e] * E_e(x_t); topk_idx_opt and topk_w_opt must then be NULL and
+ * counts_opt receives C for every expert.
  */
 moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
                                const void* hidden, void* out,

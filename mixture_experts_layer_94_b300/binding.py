@@ -22,6 +22,7 @@ MOE_OK = 0
 CALL_PERMUTE, CALL_GROUPED_SWIGLU, CALL_LAYER_FORWARD, CALL_ROUTER = 0, 1, 2, 3
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DT_F32, DT_BF16 = 0, 1
+ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
 
 
 class MoEError(RuntimeError):
@@ -36,7 +37,7 @@ class Problem(ctypes.Structure):
                 ("shared_ffn", ctypes.c_int32), ("score_fn", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("hidden_dtype", ctypes.c_int32),
                 ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_double)]
+                ("capacity_factor", ctypes.c_double), ("routing", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -63,6 +64,8 @@ def _load():
         "moe_get_device_status": ([P, P], i32),
         "moe_layer_forward_profiled": ([pp, ctypes.POINTER(Weights)] + [P] * 3 + [sz, P, P], i32),
         "moe_layer_forward_kernel_count": ([pp], i32),
+        "moe_expert_choice_select": ([pp] + [P] * 7 + [sz, P], i32),
+        "moe_permute_static": ([pp] + [P] * 8, i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -95,7 +98,8 @@ def problem(cfg: MoEConfig = None, **kw) -> Problem:
     f = dict(T=cfg.T, d_model=cfg.d, n_experts=cfg.N, top_k=cfg.K, ffn=cfg.F, n_shared=cfg.S,
              shared_ffn=cfg.Fs, score_fn=cfg.score_fn, renormalize=cfg.renormalize,
              hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16, n_groups=cfg.n_groups,
-             topk_groups=cfg.topk_groups, capacity_factor=cfg.capacity_factor) if cfg else {}
+             topk_groups=cfg.topk_groups, capacity_factor=cfg.capacity_factor,
+             routing=ROUTING_EXPERT_CHOICE if cfg.routing == "expert" else ROUTING_TOKEN_CHOICE) if cfg else {}
     f.update(kw)
     return Problem(**f)
 
@@ -137,6 +141,23 @@ def router_topk(p: Problem, hidden, w_router, topk_idx, topk_w, router_bias=None
     _check(lib.moe_router_topk(ctypes.byref(p), _p(hidden), _p(w_router), _p(router_bias),
                                _p(sel_bias), _p(topk_idx), _p(topk_w), _p(logits), _p(ws), ws.numel(),
                                _stream(stream)), "moe_router_topk")
+
+
+def expert_choice_capacity(cfg: MoEConfig, T: int = None) -> int:
+    """Tokens every expert takes under expert-choice routing: min(ceil(c T K / N), T)."""
+    import math
+    T = cfg.T if T is None else T
+    c = cfg.capacity_factor if cfg.capacity_factor > 0 else 1.0
+    return min(math.ceil(c * T * cfg.K / cfg.N), T)
+
+
+def expert_choice_select(p: Problem, hidden, w_router, row_token, row_w, offsets, router_bias=None,
+                         ws=None, stream=None):
+    if ws is None:
+        ws = new_workspace(p, CALL_ROUTER, hidden.device)
+    _check(lib.moe_expert_choice_select(ctypes.byref(p), _p(hidden), _p(w_router), _p(router_bias),
+                                        _p(row_token), _p(row_w), _p(offsets), _p(ws), ws.numel(),
+                                        _stream(stream)), "moe_expert_choice_select")
 
 
 def permute(p: Problem, topk_idx, hidden, counts, offsets, perm_src, inv_row, x_perm, ws,

@@ -397,7 +397,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int64_t t = 0;
         float w = 1.f;
         if (EPI == kEpiScatter && row_ok) {
-          if (kind == 0) {
+          if (kind == 0 && a.row_w) {  // expert choice: the row's token and score
+            t = __ldg(a.perm_src + ti.g.h_row0 + r_local);
+            w = __ldg(a.row_w + ti.g.h_row0 + r_local);
+          } else if (kind == 0) {
             const int32_t src = __ldg(a.perm_src + ti.g.h_row0 + r_local);
             t = src / a.top_k;
             w = __ldg(a.topk_w + src);

@@ -24,7 +24,14 @@ struct RouterArgs {
   float* partial;      // scratch [splits][T][N]
   __nv_bfloat16* w3;   // scratch for the tensor-core path: [np][3 * d_pad]
   int32_t splits, d_slice;  // filled by launch_router
+  float* scores_t;     // expert choice: write S transposed [N][T] instead of a top-K
 };
+
+// Expert choice: every expert picks the C tokens with the largest score from
+// scores_t [N][T]; writes row_token / row_w [N][C], offsets [N+1], counts [N].
+cudaError_t launch_expert_choice_select(const float* scores_t, int64_t T, int32_t N, int32_t C,
+                                        int32_t* row_token, float* row_w, int32_t* offsets, int32_t* counts,
+                                        cudaStream_t s);
 
 // How the router computes its logits.
 //  tensor == false: CUDA-core kernel, token tiles x `splits` d slices of
@@ -52,6 +59,7 @@ struct PermuteArgs {
   int64_t T;
   int32_t d, N, K, C;  // C = number of 32-token chunks
   int32_t capacity;    // copies an expert keeps (token order); INT32_MAX: no cap
+  const int32_t* row_token;  // gather only: the token of each packed row (expert choice)
   const int32_t* topk_idx;
   const void* hidden;
   bool hidden_bf16;
@@ -72,6 +80,9 @@ struct PermuteArgs {
   int32_t S, F, Fs, tile_rows;
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
+// Only the row gather (+ the accumulator clear / bf16 copy), for rows already
+// placed: token of row r = row_token[r], rows = offsets[N].
+cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s);
 // Expert capacity ceil(c * T * K / N) of a problem; INT32_MAX when dropless.
 int32_t expert_capacity(const moe_problem_t& p);
 
@@ -104,6 +115,7 @@ struct GemmArgs {
   const float* topk_w;
   int32_t top_k;
   __nv_bfloat16* y;      // store epilogue: bf16 [rows][d]
+  const float* row_w;    // scatter epilogue, expert choice: perm_src is the row's token, row_w its weight
   int32_t d;
   uint32_t* err;
   // Router phase: one group of all T tokens; tile = (m block, split) with

@@ -19,10 +19,18 @@ constexpr int64_t kInt32Max = 2147483647;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3;
+  size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_bf16, h, h_sh, out_acc;
   size_t total;
 };
+
+// Tokens each expert takes under expert-choice routing: min(ceil(c T K / N), T),
+// c = capacity_factor or 1.
+int64_t ec_capacity(const moe_problem_t& p) {
+  const double c = p.capacity_factor > 0.0 ? p.capacity_factor : 1.0;
+  const double cap = ceil(c * (double)p.T * (double)p.top_k / (double)p.n_experts);
+  return cap >= (double)p.T ? p.T : (int64_t)cap;
+}
 
 Layout make_layout(const moe_problem_t& p, int call) {
   Layout L{};
@@ -44,6 +52,13 @@ Layout make_layout(const moe_problem_t& p, int call) {
     const RouterPlan rp = router_plan(T, p.d_model, p.n_experts, p.hidden_dtype == MOE_BF16);
     L.router = take((size_t)rp.splits * T * p.n_experts * 4);
     if (rp.tensor) L.router_w3 = take((size_t)rp.np * 3 * rp.d_pad * 2);
+    if (p.routing == MOE_ROUTING_EXPERT_CHOICE) L.ec_scores = take((size_t)p.n_experts * T * 4);
+  }
+  const int64_t ec_rows = p.routing == MOE_ROUTING_EXPERT_CHOICE ? (int64_t)p.n_experts * ec_capacity(p) : 0;
+  const int64_t rows = TK > ec_rows ? TK : ec_rows;  // packed rows of the layer
+  if (call == MOE_CALL_LAYER_FORWARD && ec_rows > 0) {
+    L.ec_token = take((size_t)ec_rows * 4);
+    L.ec_w = take((size_t)ec_rows * 4);
   }
   if (call == MOE_CALL_LAYER_FORWARD) {
     L.topk_idx = take((size_t)TK * 4);
@@ -52,9 +67,9 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.offsets = take((size_t)(p.n_experts + 1) * 4);
     L.perm_src = take((size_t)TK * 4);
     L.inv_row = take((size_t)TK * 4);
-    L.x_perm = take((size_t)TK * p.d_model * 2);
+    L.x_perm = take((size_t)rows * p.d_model * 2);
     if (p.n_shared > 0 && p.hidden_dtype == MOE_F32) L.x_bf16 = take((size_t)T * p.d_model * 2);
-    L.h = take((size_t)TK * p.ffn * 2);
+    L.h = take((size_t)rows * p.ffn * 2);
     if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
     L.out_acc = take((size_t)T * p.d_model * 4);
   }
@@ -163,6 +178,7 @@ struct GemmPlan {
   float* out_acc;
   const int32_t* perm_src;
   const float* topk_w;
+  const float* row_w;
   __nv_bfloat16* y;
   const GroupDesc* groups;
   const int32_t* ts_gu;
@@ -243,6 +259,7 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   a.out_acc = g.out_acc;
   a.perm_src = g.perm_src;
   a.topk_w = g.topk_w;
+  a.row_w = g.row_w;
   a.y = g.y;
   bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, rows);
   MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseDown, g.epilogue, g.pair, md, a, bound, s)));
@@ -279,6 +296,8 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (p->hidden_dtype != MOE_F32 && p->hidden_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (p->n_groups < 0) return MOE_ERR_INVALID_ARG;
   if (!(p->capacity_factor >= 0.0) || p->capacity_factor > 1e30) return MOE_ERR_INVALID_ARG;  // NaN fails too
+  if (p->routing != MOE_ROUTING_TOKEN_CHOICE && p->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+  if (p->routing == MOE_ROUTING_EXPERT_CHOICE && p->n_groups > 1) return MOE_ERR_UNSUPPORTED;
   if (p->n_groups > 1) {
     if (p->n_experts % p->n_groups != 0 || p->topk_groups < 1 || p->topk_groups > p->n_groups)
       return MOE_ERR_INVALID_ARG;
@@ -302,6 +321,7 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const f
                              const float* router_bias, const float* sel_bias, int32_t* topk_idx, float* topk_w,
                              float* logits_opt, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(moe_problem_check(p));
+  if (p->routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   if (sel_bias && p->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_UNSUPPORTED;
   Layout L;
   MOE_TRY(check_ws(p, MOE_CALL_ROUTER, ws, ws_bytes, &L));
@@ -314,10 +334,30 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const f
   return cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_expert_choice_select(const moe_problem_t* p, const void* hidden, const float* w_router,
+                                      const float* router_bias, int32_t* row_token, float* row_w,
+                                      int32_t* offsets, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (p->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  MOE_TRY(check_ws(p, MOE_CALL_ROUTER, ws, ws_bytes, &L));
+  if (p->T == 0) return MOE_OK;
+  if (!hidden || !w_router || !row_token || !row_w || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RouterArgs a{p->T, p->d_model, p->n_experts, p->top_k, p->score_fn, p->renormalize, 0, 0,
+               hidden, w_router, router_bias, nullptr, nullptr, nullptr, nullptr,
+               at<float>(ws, L.router), at<__nv_bfloat16>(ws, L.router_w3), 0, 0, at<float>(ws, L.ec_scores)};
+  MOE_TRY(cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, s)));
+  return cuda_status(launch_expert_choice_select(a.scores_t, p->T, p->n_experts, (int32_t)ec_capacity(*p),
+                                                 row_token, row_w, offsets, nullptr, s));
+}
+
 moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx, const void* hidden, int32_t* counts,
                          int32_t* offsets, int32_t* perm_src, int32_t* inv_row, void* x_perm, void* ws,
                          size_t ws_bytes, void* stream) {
   MOE_TRY(moe_problem_check(p));
+  if (p->routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && (!topk_idx || !hidden || !perm_src || !inv_row || !x_perm)) return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && (!aligned16(hidden) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
@@ -349,7 +389,9 @@ moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, cons
   MOE_TRY(moe_problem_check(p));
   if (!offsets || !w_gate || !w_up || !w_down) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down)) return MOE_ERR_INVALID_ARG;
-  const int64_t rows = p->T * p->top_k;
+  // packed rows: T*K copies (token choice) or N*C picks (expert choice)
+  const int64_t rows =
+      p->routing == MOE_ROUTING_EXPERT_CHOICE ? (int64_t)p->n_experts * ec_capacity(*p) : p->T * p->top_k;
   if (rows > 0 && (!x_perm || !h_perm || !y_perm)) return MOE_ERR_INVALID_ARG;
   if (rows > 0 && (!aligned16(x_perm) || !aligned16(h_perm) || !aligned16(y_perm))) return MOE_ERR_INVALID_ARG;
   moe_problem_t q = *p;
@@ -389,6 +431,7 @@ moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, cons
 moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm, const int32_t* inv_row, const float* topk_w,
                          const void* shared_out, void* out, void* stream) {
   MOE_TRY(moe_problem_check(p));
+  if (p->routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   if (p->T == 0) return MOE_OK;
   if (!y_perm || !inv_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(out) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
@@ -437,6 +480,78 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     pa.offsets = offsets;
     pa.err = err;
     return cuda_status(launch_permute(pa, s));
+  }
+
+  if (p->routing == MOE_ROUTING_EXPERT_CHOICE) {
+    if (topk_idx_opt || topk_w_opt) return MOE_ERR_INVALID_ARG;
+    if (w->sel_bias) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
+    const int32_t C = (int32_t)ec_capacity(*p);
+    const int64_t rows = (int64_t)N * C;
+    // 1. router logits and per-token scores, then every expert picks its C tokens
+    MOE_TRY(record(ev, 0, s));
+    RouterArgs ra{T, p->d_model, N, K, p->score_fn, p->renormalize, 0, 0, hidden, w->w_router, w->router_bias,
+                  nullptr, nullptr, nullptr, nullptr, at<float>(ws, L.router), at<__nv_bfloat16>(ws, L.router_w3),
+                  0, 0, at<float>(ws, L.ec_scores)};
+    MOE_TRY(cuda_status(launch_router(ra, hbf16, s)));
+    int32_t* row_token = at<int32_t>(ws, L.ec_token);
+    float* row_w = at<float>(ws, L.ec_w);
+    MOE_TRY(cuda_status(launch_expert_choice_select(ra.scores_t, T, N, C, row_token, row_w, offsets,
+                                                    counts_opt, s)));
+    MOE_TRY(record(ev, 1, s));
+    // 2. pack the picked rows (+ clear the accumulator, bf16 copy of an fp32 hidden)
+    PermuteArgs pa{};
+    pa.T = T;
+    pa.d = p->d_model;
+    pa.N = N;
+    pa.K = K;
+    pa.hidden = hidden;
+    pa.hidden_bf16 = hbf16;
+    pa.offsets = offsets;
+    pa.row_token = row_token;
+    pa.x_perm = at<__nv_bfloat16>(ws, L.x_perm);
+    pa.zero_rows = at<float>(ws, L.out_acc);
+    pa.x_bf16 = (S > 0 && !hbf16) ? at<__nv_bfloat16>(ws, L.x_bf16) : nullptr;
+    MOE_TRY(cuda_status(launch_gather(pa, rows, s)));
+    MOE_TRY(record(ev, 2, s));
+    // 3. GEMM schedule over the N full expert groups and the shared experts
+    const int32_t pair = gemm_pair(rows, N);
+    ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, kBM * pair, T, offsets,
+                    at<GroupDesc>(ws, L.groups), at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
+    MOE_TRY(cuda_status(launch_schedule(sa, s)));
+    MOE_TRY(record(ev, 3, s));
+    // 4-5. grouped SwiGLU GEMMs; the down epilogue adds S[t][e] * y to the row's token
+    GemmPlan g{};
+    g.pair = pair;
+    g.N = N;
+    g.S = S;
+    g.F = p->ffn;
+    g.Fs = p->shared_ffn;
+    g.d = p->d_model;
+    g.K = K;
+    g.T = T;
+    g.routed_rows = rows;
+    g.x_routed = pa.x_perm;
+    g.x_shared = hbf16 ? hidden : pa.x_bf16;
+    g.wg = w->w_gate;
+    g.wu = w->w_up;
+    g.wd = w->w_down;
+    g.sg = w->ws_gate;
+    g.su = w->ws_up;
+    g.sd = w->ws_down;
+    g.h = at<__nv_bfloat16>(ws, L.h);
+    g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
+    g.epilogue = kEpiScatter;
+    g.out_acc = at<float>(ws, L.out_acc);
+    g.perm_src = row_token;
+    g.row_w = row_w;
+    g.groups = at<GroupDesc>(ws, L.groups);
+    g.ts_gu = at<int32_t>(ws, L.ts_gu);
+    g.ts_dn = at<int32_t>(ws, L.ts_dn);
+    g.err = err;
+    MOE_TRY(run_gemms(g, s, ev ? ev + 4 : nullptr));
+    MOE_TRY(cuda_status(launch_finalize(g.out_acc, static_cast<__nv_bfloat16*>(out), T * p->d_model, s)));
+    return record(ev, 6, s);
   }
 
   // 1. router, scoring, top-K, gate weights
@@ -546,6 +661,7 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   // route and pack: histogram, scan (+ schedule), scatter -- one kernel for at
   // most 32 chunks of 32 tokens -- then the gather; gate/up GEMM, down GEMM, finalise
   const int router = p->hidden_dtype == MOE_BF16 ? 3 : 2;
+  if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
   return router + route + 3;
 }

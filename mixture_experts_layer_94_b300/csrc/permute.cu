@@ -173,9 +173,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
   // was out of range (reported through the error word).
   const int64_t placed = min(rows, (int64_t)__ldg(a.offsets + a.N));
   for (int64_t r = warp0; r < placed; r += nwarps) {
-    const int32_t src = a.perm_src[r];
-    if (src < 0 || src >= rows) continue;
-    const int64_t t = src / a.K;
+    int64_t t;
+    if (a.row_token) {
+      t = a.row_token[r];
+      if (t < 0 || t >= a.T) continue;
+    } else {
+      const int32_t src = a.perm_src[r];
+      if (src < 0 || src >= rows) continue;
+      t = src / a.K;
+    }
     uint4* dst = reinterpret_cast<uint4*>(a.x_perm + r * d);
     if (a.hidden_bf16) {
       const uint4* sp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * d);
@@ -359,6 +365,15 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t rows = a.T * a.K;
   const int64_t want = (rows + 7) / 8;  // 8 rows (warps) per 256-thread CTA
+  const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
+  gather_rows_kernel<<<grid, 256, 0, s>>>(a, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (rows + 7) / 8;
   const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
   gather_rows_kernel<<<grid, 256, 0, s>>>(a, rows);
   return cudaGetLastError();

@@ -54,6 +54,7 @@ extern "C" moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t
                                            void* x_perm, void* stream) {
   const moe_status_t st = moe_problem_check(p);
   if (st != MOE_OK) return st;
+  if (p->routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
   const int64_t chunks = (p->T + moe::kTokensPerChunk - 1) / moe::kTokensPerChunk;
   if ((int64_t)p->n_experts * chunks > MOE_PERMUTE_STATIC_MAX_CHUNK_COUNTS) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;

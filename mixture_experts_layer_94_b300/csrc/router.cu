@@ -300,6 +300,36 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
       if (valid[i] && !s_kept[warp][e / gs]) valid[i] = false;
     }
   }
+  if (a.scores_t) {
+    // Expert choice: the token's score for every expert, stored transposed
+    // (S[e][t]) for the per-expert selection.
+    float sv[EPL];
+    if (a.score_fn == 0) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (valid[i]) mx = fmaxf(mx, sc[i]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      float z = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        sv[i] = valid[i] ? expf(sc[i] - mx) : 0.f;
+        z += sv[i];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) sv[i] /= z;
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) sv[i] = sc[i];
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (valid[i]) a.scores_t[(int64_t)(lane + 32 * i) * a.T + t] = sv[i];
+    return;
+  }
   uint32_t taken = 0;
   int my_e = -1;
   float my_sc = 0.f;
@@ -422,6 +452,109 @@ cudaError_t launch_tensor_logits(const RouterArgs& a, const RouterPlan& pl, cuda
   return launch_grouped_gemm(kPhaseRouter, kEpiLogits, 1, m, g, g.r_tiles, s);
 }
 
+// ---------------------------------------------------------------- expert choice
+// One CTA per expert: the C-th largest score key is found by a 4-pass radix
+// select over the 32-bit keys (scores are >= 0, so their bit patterns order
+// like the values), then the tokens with a larger key, and the lowest-indexed
+// tokens equal to it, are written in ascending token order. Two block-wide
+// scans (ties, then picks) keep the result deterministic.
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < (kSelThreads / 32) ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    s_warp[lane] = wi - w;  // exclusive prefix of warp sums
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  const int res = s_warp[warp] + incl - v;
+  total = s_warp[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kSelThreads) expert_choice_select_kernel(const float* __restrict__ scores_t,
+                                                                            int64_t T, int32_t N, int32_t C,
+                                                                            int32_t* row_token, float* row_w,
+                                                                            int32_t* offsets, int32_t* counts) {
+  __shared__ int hist[256];
+  __shared__ int s_warp[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int e = blockIdx.x;
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(scores_t) + (int64_t)e * T;
+  uint32_t prefix = 0, pmask = 0;
+  int need = C;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
+      const uint32_t k = __ldg(keys + t);
+      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // the bin holding the need-th largest key
+      int above = 0, b = 255;
+      for (; b > 0; --b) {
+        if (above + hist[b] >= need) break;
+        above += hist[b];
+      }
+      s_prefix = prefix | ((uint32_t)b << shift);
+      s_need = need - above;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    pmask |= 255u << shift;
+    __syncthreads();
+  }
+  // prefix: the C-th largest key; `need` tokens equal to it are taken (lowest
+  // indices first). Each thread owns a contiguous run of tokens.
+  const int64_t per = (T + blockDim.x - 1) / blockDim.x;
+  const int64_t t0 = min((int64_t)threadIdx.x * per, T), t1 = min(t0 + per, T);
+  int n_eq = 0;
+  for (int64_t t = t0; t < t1; ++t) n_eq += __ldg(keys + t) == prefix;
+  int tot;
+  const int eq_before = block_exclusive_scan(n_eq, s_warp, tot);
+  int n_pick = 0, eq_seen = eq_before;
+  for (int64_t t = t0; t < t1; ++t) {
+    const uint32_t k = __ldg(keys + t);
+    if (k > prefix) ++n_pick;
+    else if (k == prefix) n_pick += (eq_seen++ < need);
+  }
+  int pos = block_exclusive_scan(n_pick, s_warp, tot);
+  eq_seen = eq_before;
+  for (int64_t t = t0; t < t1; ++t) {
+    const uint32_t k = __ldg(keys + t);
+    const bool take = k > prefix || (k == prefix && eq_seen++ < need);
+    if (take) {
+      row_token[(int64_t)e * C + pos] = (int32_t)t;
+      row_w[(int64_t)e * C + pos] = __uint_as_float(k);
+      ++pos;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[e] = e * C;
+    if (e == N - 1) offsets[N] = N * C;
+    if (counts) counts[e] = C;
+  }
+}
+
 template <typename XT>
 cudaError_t launch_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_t s) {
   const dim3 grid((unsigned)pl.token_tiles, (unsigned)pl.splits), block(kWarps * 32);
@@ -491,6 +624,13 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
   pl.d_slice = (int32_t)slice;
   pl.splits = (int32_t)((d + slice - 1) / slice);
   return pl;
+}
+
+cudaError_t launch_expert_choice_select(const float* scores_t, int64_t T, int32_t N, int32_t C,
+                                        int32_t* row_token, float* row_w, int32_t* offsets, int32_t* counts,
+                                        cudaStream_t s) {
+  expert_choice_select_kernel<<<N, kSelThreads, 0, s>>>(scores_t, T, N, C, row_token, row_w, offsets, counts);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_router(const RouterArgs& a0, bool hidden_bf16, cudaStream_t s) {

@@ -47,6 +47,7 @@ class MoEConfig:
     n_groups: int = 0        # group-limited routing (0: off)
     topk_groups: int = 0
     capacity_factor: float = 0.0  # expert capacity ceil(c T K / N) (0: dropless)
+    routing: str = "token"   # "token" (tokens pick K experts) | "expert" (experts pick C tokens)
 
     def with_(self, **kw) -> "MoEConfig":
         return dataclasses.replace(self, **kw)
@@ -73,11 +74,15 @@ DSV3 = MoEConfig("dsv3", T=8192, d=7168, N=256, K=8, F=2048, S=1, Fs=2048, score
 DSV3_GROUPED = DSV3.with_(name="dsv3_grouped", n_groups=8, topk_groups=4)
 # The Mixtral-shaped layer with expert capacity factor 1.0 (C = 1024 copies).
 MIXTRAL_CAPACITY = MIXTRAL.with_(name="mixtral_capacity", capacity_factor=1.0)
+# The Mixtral-shaped layer with expert-choice routing: every expert takes
+# C = T*K/N = 1024 tokens.
+MIXTRAL_EC = MIXTRAL.with_(name="mixtral_ec", routing="expert")
 GPTOSS = MoEConfig("gptoss", T=2048, d=2880, N=128, K=4, F=2880)
 QWEN_DECODE = MoEConfig("qwen_decode", T=1, d=4096, N=128, K=8, F=1536)
 DECODE_BATCHES = (1, 8, 32, 128, 512)
 
-CONFIGS = {c.name: c for c in (TINY, MIXTRAL, MIXTRAL_CAPACITY, DSV3, DSV3_GROUPED, GPTOSS, QWEN_DECODE)}
+CONFIGS = {c.name: c for c in (TINY, MIXTRAL, MIXTRAL_CAPACITY, MIXTRAL_EC, DSV3, DSV3_GROUPED, GPTOSS,
+                               QWEN_DECODE)}
 
 
 def _seed(seed: int, *parts) -> int:

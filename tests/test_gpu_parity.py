@@ -358,3 +358,83 @@ def test_full_size_workload(name, cfg, n_sample):
     e = H.assert_output_close(out.float().cpu().numpy()[rows], ref["out"], name)
     print(f"{name}: near ties {rep['near_ties']} (flipped {rep['near_tie_flips']}), errors {e}, "
           f"touched experts {int((counts > 0).sum())}")
+
+
+# --------------------------------------------------------------------------- expert choice
+EC_CASES = {
+    "ec_softmax": inputs.MoEConfig("ec_softmax", T=300, d=264, N=8, K=2, F=392, routing="expert"),
+    "ec_sigmoid_f32_half": inputs.MoEConfig("ec_sigmoid_f32_half", T=200, d=128, N=16, K=3, F=136,
+                                            score="sigmoid", hidden_dtype="f32", capacity_factor=0.5,
+                                            routing="expert"),
+    "ec_every_token": inputs.MoEConfig("ec_every_token", T=77, d=64, N=4, K=4, F=64, routing="expert"),
+    "ec_shared_pairs": inputs.MoEConfig("ec_shared_pairs", T=600, d=192, N=2, K=1, F=136, S=1, Fs=72,
+                                        routing="expert"),
+}
+
+
+def _ec_select_gpu(cfg, dev):
+    C = B.expert_choice_capacity(cfg)
+    row_token = torch.empty(cfg.N, C, dtype=torch.int32, device="cuda")
+    row_w = torch.empty(cfg.N, C, dtype=torch.float32, device="cuda")
+    offsets = torch.empty(cfg.N + 1, dtype=torch.int32, device="cuda")
+    B.expert_choice_select(B.problem(cfg), dev["hidden"], dev["w_router"], row_token, row_w, offsets,
+                           router_bias=dev.get("router_bias"))
+    torch.cuda.synchronize()
+    return C, row_token.cpu().numpy(), row_w.cpu().numpy(), offsets.cpu().numpy()
+
+
+def _ec_compare(cfg, ins, C, row_token, row_w, offsets):
+    ref = oracle.expert_choice(H.hidden_f32(ins), H.np32(ins["w_router"]), C, score_fn=cfg.score_fn,
+                               router_bias=H.np32(ins.get("router_bias")))
+    assert offsets.tolist() == [e * C for e in range(cfg.N + 1)]
+    exact = ref["margin"] >= H.MARGIN_TIE
+    assert exact.mean() > 0.5
+    for e in np.nonzero(exact)[0]:
+        assert np.array_equal(row_token[e], ref["row_token"][e]), e
+        assert np.abs(row_w[e].astype(np.float64) - ref["row_w"][e]).max() <= H.W_ATOL
+    return int((~exact).sum())
+
+
+@pytest.mark.parametrize("name", list(EC_CASES))
+def test_expert_choice_matches_oracle(name):
+    cfg = EC_CASES[name]
+    ins, dev = H.make_case(cfg)
+    C, row_token, row_w, offsets = _ec_select_gpu(cfg, dev)
+    _ec_compare(cfg, ins, C, row_token, row_w, offsets)
+    # the layer under that (verified) selection
+    out, _, _, counts = None, None, None, None
+    layer = B.MoELayer(cfg, dev)
+    counts = torch.empty(cfg.N, dtype=torch.int32, device="cuda")
+    out = layer.forward(dev["hidden"], counts=counts)
+    torch.cuda.synchronize()
+    assert layer.status(cfg.T) == 0
+    assert torch.all(counts == C)
+    idx, w = oracle.routing_from_expert_choice(row_token, row_w.astype(np.float64), cfg.T)
+    bits = {k: [H.bf16_bits(m) for m in ins[k]] for k in ("w_gate", "w_up", "w_down")}
+    sh = {}
+    if cfg.S:
+        sh = {k: [H.bf16_bits(m) for m in ins[k]] for k in ("ws_gate", "ws_up", "ws_down")}
+    ref = oracle.layer_routed(H.hidden_f32(ins), idx, w, bits["w_gate"], bits["w_up"], bits["w_down"], **sh)
+    H.assert_output_close(out.float().cpu().numpy(), ref, name)
+
+
+def test_expert_choice_full_size_mixtral():
+    """The Mixtral-shaped layer with expert-choice routing (C = 1024 tokens per
+    expert): selection bit-exact, outputs on sampled tokens."""
+    cfg = inputs.MIXTRAL_EC
+    ins = inputs.make_inputs(cfg, seed=0, device="cuda")
+    dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
+    C, row_token, row_w, offsets = _ec_select_gpu(cfg, dev)
+    _ec_compare(cfg, ins, C, row_token, row_w, offsets)
+    layer = B.MoELayer(cfg, dev)
+    out = layer.forward(dev["hidden"])
+    torch.cuda.synchronize()
+    assert layer.status(cfg.T) == 0
+    idx, w = oracle.routing_from_expert_choice(row_token, row_w.astype(np.float64), cfg.T)
+    rows = _sample_rows(cfg.T, 12)
+    picked_by = (idx >= 0).sum(axis=1)
+    rows = np.array(sorted(set(rows.tolist()) | {int(np.argmax(picked_by)), int(np.argmin(picked_by))}))
+    bits = {k: [H.bf16_bits(m) for m in ins[k]] for k in ("w_gate", "w_up", "w_down")}
+    ref = oracle.layer_routed(H.hidden_f32(ins)[rows], idx[rows], w[rows], bits["w_gate"], bits["w_up"],
+                              bits["w_down"])
+    H.assert_output_close(out.float().cpu().numpy()[rows], ref, "mixtral_ec")
