@@ -353,6 +353,16 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p);
  */
 moe_status_t moe_get_device_status(void* ws, void* stream);
 
+/*
+ * Failure-detection test hook (no counterpart on the pages): launches one warp
+ * that waits on an mbarrier nothing arrives at, through the same bounded wait
+ * the GEMM pipeline uses, with a limit of timeout_us microseconds (1..10^6).
+ * The wait gives up and records a timeout in the error word of `ws` (any
+ * workspace, >= 256 bytes); moe_get_device_status then returns MOE_ERR_TIMEOUT
+ * and the CUDA context stays usable.
+ */
+moe_status_t moe_debug_stall_wait(void* ws, size_t ws_bytes, uint32_t timeout_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,6 +66,7 @@ def _load():
         "moe_layer_forward_kernel_count": ([pp], i32),
         "moe_expert_choice_select": ([pp] + [P] * 7 + [sz, P], i32),
         "moe_permute_static": ([pp] + [P] * 8, i32),
+        "moe_debug_stall_wait": ([P, sz, ctypes.c_uint32, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -212,6 +213,12 @@ def layer_forward_profiled(p: Problem, weights: Weights, hidden, out, ws, events
 
 def layer_forward_kernel_count(p: Problem) -> int:
     return int(lib.moe_layer_forward_kernel_count(ctypes.byref(p)))
+
+
+def debug_stall_wait(ws, timeout_us: int, stream=None):
+    """Failure-detection hook: a bounded wait nothing satisfies (see include/moe.h)."""
+    _check(lib.moe_debug_stall_wait(_p(ws), ws.numel(), int(timeout_us), _stream(stream)),
+           "moe_debug_stall_wait")
 
 
 def get_device_status(ws, stream=None) -> int:
