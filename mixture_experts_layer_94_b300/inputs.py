@@ -13,6 +13,9 @@ Recipe (every tensor is drawn in this fixed order from its own seeded stream):
   * per routed expert e: W_gate[e], W_up[e] ~ N(0, 1/d) [F, d];
     W_down[e] ~ N(0, 1/F) [d, F]; drawn in fp32, rounded once to bf16
   * per shared expert s: the same with Fs in place of F
+  * FP8 expert weights (expert_dtype "fp8"): the same fp32 draws, then per
+    matrix row a scale amax(|row|) / 448 (fp32) and E4M3 codes of row / scale
+    (torch's round-to-nearest-even cast, clamped to +-448, so no NaN code)
 Router-side tensors (hidden, w_router, biases) always come from a CPU
 generator, so routing is identical whatever device holds the experts. Expert
 weights come from a generator on `device` seeded per expert: large workloads
@@ -48,6 +51,7 @@ class MoEConfig:
     topk_groups: int = 0
     capacity_factor: float = 0.0  # expert capacity ceil(c T K / N) (0: dropless)
     routing: str = "token"   # "token" (tokens pick K experts) | "expert" (experts pick C tokens)
+    expert_dtype: str = "bf16"  # "bf16" | "fp8" (E4M3 codes + one fp32 scale per matrix row)
 
     def with_(self, **kw) -> "MoEConfig":
         return dataclasses.replace(self, **kw)
@@ -79,10 +83,13 @@ MIXTRAL_CAPACITY = MIXTRAL.with_(name="mixtral_capacity", capacity_factor=1.0)
 MIXTRAL_EC = MIXTRAL.with_(name="mixtral_ec", routing="expert")
 GPTOSS = MoEConfig("gptoss", T=2048, d=2880, N=128, K=4, F=2880)
 QWEN_DECODE = MoEConfig("qwen_decode", T=1, d=4096, N=128, K=8, F=1536)
+# The same layers with FP8 E4M3 expert weights.
+MIXTRAL_FP8 = MIXTRAL.with_(name="mixtral_fp8", expert_dtype="fp8")
+QWEN_DECODE_FP8 = QWEN_DECODE.with_(name="qwen_decode_fp8", expert_dtype="fp8")
 DECODE_BATCHES = (1, 8, 32, 128, 512)
 
 CONFIGS = {c.name: c for c in (TINY, MIXTRAL, MIXTRAL_CAPACITY, MIXTRAL_EC, DSV3, DSV3_GROUPED, GPTOSS,
-                               QWEN_DECODE)}
+                               QWEN_DECODE, MIXTRAL_FP8, QWEN_DECODE_FP8)}
 
 
 def _seed(seed: int, *parts) -> int:
@@ -124,10 +131,58 @@ def _draw_bf16(out: torch.Tensor, gen: torch.Generator, std: float) -> None:
     out.copy_(tmp)
 
 
+E4M3_MAX = 448.0
+
+
+def _draw_fp8(codes: torch.Tensor, scale: torch.Tensor, gen: torch.Generator, std: float) -> None:
+    tmp = torch.randn(codes.shape, generator=gen, dtype=torch.float32, device=codes.device)
+    tmp.mul_(std)
+    s = tmp.abs().amax(dim=1).clamp_min(1e-30) / E4M3_MAX
+    scale.copy_(s)
+    tmp.div_(s[:, None]).clamp_(-E4M3_MAX, E4M3_MAX)
+    codes.copy_(tmp.to(torch.float8_e4m3fn).view(torch.uint8))
+
+
+def make_expert_weights_fp8(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
+    """Stacked FP8 E4M3 expert weights on `device`: codes (uint8) w_gate, w_up
+    [N, F, d], w_down [N, d, F] with fp32 row scales w_gate_scale, w_up_scale
+    [N, F], w_down_scale [N, d]; shared experts likewise (ws_*, None when
+    S == 0). Draws the same normal values as make_expert_weights."""
+    device = torch.device(device)
+    u8, f32 = torch.uint8, torch.float32
+    out = {}
+    g = torch.Generator(device=device)
+
+    def stack(kind, n, f):
+        gate = torch.empty(n, f, cfg.d, dtype=u8, device=device)
+        up = torch.empty_like(gate)
+        down = torch.empty(n, cfg.d, f, dtype=u8, device=device)
+        sg = torch.empty(n, f, dtype=f32, device=device)
+        su = torch.empty_like(sg)
+        sd = torch.empty(n, cfg.d, dtype=f32, device=device)
+        for e in range(n):
+            g.manual_seed(_seed(seed, kind, e))
+            _draw_fp8(gate[e], sg[e], g, 1.0 / math.sqrt(cfg.d))
+            _draw_fp8(up[e], su[e], g, 1.0 / math.sqrt(cfg.d))
+            _draw_fp8(down[e], sd[e], g, 1.0 / math.sqrt(f))
+        return gate, up, down, sg, su, sd
+
+    (out["w_gate"], out["w_up"], out["w_down"], out["w_gate_scale"], out["w_up_scale"],
+     out["w_down_scale"]) = stack("routed", cfg.N, cfg.F)
+    for k in ("ws_gate", "ws_up", "ws_down", "ws_gate_scale", "ws_up_scale", "ws_down_scale"):
+        out[k] = None
+    if cfg.S > 0:
+        (out["ws_gate"], out["ws_up"], out["ws_down"], out["ws_gate_scale"], out["ws_up_scale"],
+         out["ws_down_scale"]) = stack("shared", cfg.S, cfg.Fs)
+    return out
+
+
 def make_expert_weights(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
     """Stacked bf16 expert weights on `device`:
     w_gate, w_up [N, F, d]; w_down [N, d, F]; ws_gate, ws_up [S, Fs, d];
-    ws_down [S, d, Fs] (None when S == 0)."""
+    ws_down [S, d, Fs] (None when S == 0). FP8 configs: make_expert_weights_fp8."""
+    if cfg.expert_dtype == "fp8":
+        return make_expert_weights_fp8(cfg, seed, device)
     device = torch.device(device)
     bf = torch.bfloat16
     w_gate = torch.empty(cfg.N, cfg.F, cfg.d, dtype=bf, device=device)

@@ -14,9 +14,14 @@
  * fp32 keys: the same precision the device kernel decides in. Everything after
  * the decision (weights, expert FFNs, combine) is fp64.
  *
- * Expert weights arrive as bf16 bit patterns (uint16) and are widened exactly
- * to fp64 element by element; hidden rows arrive as fp32 (a bf16 hidden is
- * widened exactly by the caller).
+ * Expert weights arrive as bf16 bit patterns (uint16), or as FP8 E4M3 codes
+ * (uint8) with one fp32 scale per matrix row ("AI Infrastructure series, Part
+ * 12 of 24", "How do you serve an MoE model on your own GPUs?": quantise the
+ * experts' weights, keep the router in 16 bits or more; "Mixture of Experts
+ * Explained", "Total versus active parameters": the bytes a token reads fall
+ * by the same factor as the storage); either way each weight is widened
+ * exactly to fp64 element by element. Hidden rows arrive as fp32 (a bf16
+ * hidden is widened exactly by the caller).
  *
  * Parity status of every function: pinned (see the tests of the oracle).
  */
@@ -37,6 +42,59 @@ static double bf16_bits_to_double(uint16_t b) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* OCP FP8 E4M3 ("fn": no infinities): sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent 0 encodes subnormals m/8 * 2^-6; S.1111.111 is
+ * NaN. */
+double moe_oracle_e4m3_to_double(uint8_t b) {
+  const int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Expert weights in one of two storage formats: bf16 values (scale unused),
+ * or FP8 E4M3 codes with one fp32 scale per matrix row: w = e4m3(q) * scale. */
+typedef struct {
+  int fmt; /* 0 bf16, 1 fp8 e4m3 + per-row scale */
+  const void* q;
+  const float* scale;
+} wmat_t;
+
+static double wload(wmat_t w, int64_t row, int64_t ld, int64_t col) {
+  if (w.fmt == 0) return bf16_bits_to_double(((const uint16_t*)w.q)[row * ld + col]);
+  return moe_oracle_e4m3_to_double(((const uint8_t*)w.q)[row * ld + col]) * (double)w.scale[row];
+}
+
+/* A set of experts' matrices, one pointer per expert (NULL: not provided),
+ * all in one format; scales are used only for fp8. */
+typedef struct {
+  int fmt;
+  const void* const* gate;
+  const void* const* up;
+  const void* const* down;
+  const float* const* s_gate;
+  const float* const* s_up;
+  const float* const* s_down;
+} wset_t;
+
+/* Expert e of a set; returns 0 if any of its matrices (or scales) is missing. */
+static int wset_expert(const wset_t* ws, int32_t e, wmat_t* g, wmat_t* u, wmat_t* dn) {
+  if (!ws->gate[e] || !ws->up[e] || !ws->down[e]) return 0;
+  if (ws->fmt == 1 && (!ws->s_gate || !ws->s_up || !ws->s_down || !ws->s_gate[e] || !ws->s_up[e] ||
+                       !ws->s_down[e]))
+    return 0;
+  g->fmt = u->fmt = dn->fmt = ws->fmt;
+  g->q = ws->gate[e];
+  u->q = ws->up[e];
+  dn->q = ws->down[e];
+  g->scale = ws->fmt ? ws->s_gate[e] : NULL;
+  u->scale = ws->fmt ? ws->s_up[e] : NULL;
+  dn->scale = ws->fmt ? ws->s_down[e] : NULL;
+  return 1;
 }
 
 int moe_oracle_num_threads(void) {
@@ -346,30 +404,44 @@ int moe_oracle_permute(int64_t T, int32_t K, int32_t N, const int32_t* topk_idx,
 
 /*
  * One expert FFN on one token, SwiGLU reading:
- *   g = W_gate x,  u = W_up x         (W_gate, W_up: bf16 [F][d])
+ *   g = W_gate x,  u = W_up x         (W_gate, W_up: [F][d])
  *   h_f = SiLU(g_f) * u_f
- *   y = W_down h                      (W_down: bf16 [d][F])
- * `h` is caller scratch of F doubles; y is fp64 [d].
+ *   y = W_down h                      (W_down: [d][F])
+ * Each weight is decoded from its stored format (bf16, or FP8 E4M3 code times
+ * its row's scale) to an exact double. `h` is caller scratch of F doubles; y
+ * is fp64 [d].
  */
-void moe_oracle_expert_ffn(int32_t d, int32_t F, const double* x, const uint16_t* w_gate,
-                           const uint16_t* w_up, const uint16_t* w_down, double* h,
-                           double* y) {
+static void expert_ffn_w(int32_t d, int32_t F, const double* x, wmat_t wg, wmat_t wu, wmat_t wd,
+                         double* h, double* y) {
   for (int32_t f = 0; f < F; ++f) {
     double g = 0.0, u = 0.0;
-    const uint16_t* wg = w_gate + (int64_t)f * d;
-    const uint16_t* wu = w_up + (int64_t)f * d;
     for (int32_t j = 0; j < d; ++j) {
-      g += bf16_bits_to_double(wg[j]) * x[j];
-      u += bf16_bits_to_double(wu[j]) * x[j];
+      g += wload(wg, f, d, j) * x[j];
+      u += wload(wu, f, d, j) * x[j];
     }
     h[f] = moe_oracle_silu(g) * u;
   }
   for (int32_t i = 0; i < d; ++i) {
     double acc = 0.0;
-    const uint16_t* wd = w_down + (int64_t)i * F;
-    for (int32_t f = 0; f < F; ++f) acc += bf16_bits_to_double(wd[f]) * h[f];
+    for (int32_t f = 0; f < F; ++f) acc += wload(wd, i, F, f) * h[f];
     y[i] = acc;
   }
+}
+
+void moe_oracle_expert_ffn(int32_t d, int32_t F, const double* x, const uint16_t* w_gate,
+                           const uint16_t* w_up, const uint16_t* w_down, double* h,
+                           double* y) {
+  const wmat_t wg = {0, w_gate, NULL}, wu = {0, w_up, NULL}, wd = {0, w_down, NULL};
+  expert_ffn_w(d, F, x, wg, wu, wd, h, y);
+}
+
+/* The same expert with FP8 E4M3 weights and per-row scales: W_gate, W_up
+ * codes [F][d] with scales [F]; W_down codes [d][F] with scales [d]. */
+void moe_oracle_expert_ffn_fp8(int32_t d, int32_t F, const double* x, const uint8_t* q_gate,
+                               const float* s_gate, const uint8_t* q_up, const float* s_up,
+                               const uint8_t* q_down, const float* s_down, double* h, double* y) {
+  const wmat_t wg = {1, q_gate, s_gate}, wu = {1, q_up, s_up}, wd = {1, q_down, s_down};
+  expert_ffn_w(d, F, x, wg, wu, wd, h, y);
 }
 
 /*
@@ -560,21 +632,19 @@ int moe_oracle_layer_routed(int64_t n_rows, int32_t d, int32_t N, int32_t M, int
  * weight; the kept weights are not renormalised).
  * Outputs: topk_idx [n][K], topk_w fp64 [n][K], margin fp64 [n], out fp64 [n][d].
  */
-int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
-                     int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
-                     int32_t n_groups, int32_t topk_groups,
-                     const float* hidden, const float* w_router, const float* router_bias,
-                     const float* sel_bias, const uint16_t* const* w_gate,
-                     const uint16_t* const* w_up, const uint16_t* const* w_down,
-                     const uint16_t* const* ws_gate, const uint16_t* const* ws_up,
-                     const uint16_t* const* ws_down, const unsigned char* keep,
-                     int32_t* topk_idx, double* topk_w, double* margin, double* out) {
+static int layer_impl(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
+                      int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
+                      int32_t n_groups, int32_t topk_groups,
+                      const float* hidden, const float* w_router, const float* router_bias,
+                      const float* sel_bias, const wset_t* routed, const wset_t* shared,
+                      const unsigned char* keep,
+                      int32_t* topk_idx, double* topk_w, double* margin, double* out) {
   if (!router_args_ok(n_rows, d, N, K, score_fn, n_groups, topk_groups, hidden, w_router))
     return ORACLE_ERR_ARG;
   if (F <= 0 || S < 0 || (S > 0 && Fs <= 0)) return ORACLE_ERR_ARG;
-  if (!w_gate || !w_up || !w_down || !topk_idx || !topk_w || !margin || !out)
+  if (!routed->gate || !routed->up || !routed->down || !topk_idx || !topk_w || !margin || !out)
     return ORACLE_ERR_ARG;
-  if (S > 0 && (!ws_gate || !ws_up || !ws_down)) return ORACLE_ERR_ARG;
+  if (S > 0 && (!shared->gate || !shared->up || !shared->down)) return ORACLE_ERR_ARG;
   int status = ORACLE_OK;
   const int32_t Fmax = (S > 0 && Fs > F) ? Fs : F;
 #pragma omp parallel
@@ -605,9 +675,9 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
         for (int32_t j = 0; j < d; ++j) x[j] = (double)xr[j];
         int missing = 0;
         for (int32_t k = 0; k < K; ++k) {
-          int32_t e = idx[k];
-          if (!w_gate[e] || !w_up[e] || !w_down[e]) { missing = 1; break; }
-          moe_oracle_expert_ffn(d, F, x, w_gate[e], w_up[e], w_down[e], h, y + (int64_t)k * d);
+          wmat_t wg, wu, wd;
+          if (!wset_expert(routed, idx[k], &wg, &wu, &wd)) { missing = 1; break; }
+          expert_ffn_w(d, F, x, wg, wu, wd, h, y + (int64_t)k * d);
         }
         if (missing) {
 #pragma omp atomic write
@@ -615,9 +685,16 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
           continue;
         }
         for (int32_t i = 0; i < d; ++i) sh[i] = 0.0;
-        for (int32_t s = 0; s < S; ++s) {
-          moe_oracle_expert_ffn(d, Fs, x, ws_gate[s], ws_up[s], ws_down[s], h, ys);
+        for (int32_t s = 0; s < S && !missing; ++s) {
+          wmat_t wg, wu, wd;
+          if (!wset_expert(shared, s, &wg, &wu, &wd)) { missing = 1; break; }
+          expert_ffn_w(d, Fs, x, wg, wu, wd, h, ys);
           for (int32_t i = 0; i < d; ++i) sh[i] += ys[i];
+        }
+        if (missing) {
+#pragma omp atomic write
+          status = ORACLE_ERR_MISSING_EXPERT;
+          continue;
         }
         /* a copy dropped by its expert's capacity contributes nothing */
         for (int32_t k = 0; k < K; ++k) wk[k] = (keep && !keep[t * K + k]) ? 0.0 : w[k];
@@ -628,4 +705,55 @@ int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
     free(x); free(h); free(y); free(sh); free(ys); free(wk);
   }
   return status;
+}
+
+int moe_oracle_layer(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
+                     int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
+                     int32_t n_groups, int32_t topk_groups,
+                     const float* hidden, const float* w_router, const float* router_bias,
+                     const float* sel_bias, const uint16_t* const* w_gate,
+                     const uint16_t* const* w_up, const uint16_t* const* w_down,
+                     const uint16_t* const* ws_gate, const uint16_t* const* ws_up,
+                     const uint16_t* const* ws_down, const unsigned char* keep,
+                     int32_t* topk_idx, double* topk_w, double* margin, double* out) {
+  const wset_t routed = {0, (const void* const*)w_gate, (const void* const*)w_up,
+                         (const void* const*)w_down, NULL, NULL, NULL};
+  const wset_t shared = {0, (const void* const*)ws_gate, (const void* const*)ws_up,
+                         (const void* const*)ws_down, NULL, NULL, NULL};
+  return layer_impl(n_rows, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups, hidden,
+                    w_router, router_bias, sel_bias, &routed, &shared, keep, topk_idx, topk_w, margin,
+                    out);
+}
+
+/*
+ * The same layer with every expert matrix (routed and shared) stored as FP8
+ * E4M3 codes with one fp32 scale per matrix row, as moe_oracle_expert_ffn_fp8:
+ *   q_gate[e], q_up[e]: uint8 [F][d] with s_gate[e], s_up[e]: fp32 [F]
+ *   q_down[e]: uint8 [d][F] with s_down[e]: fp32 [d]
+ *   qs_* / ss_*: the same for the S shared experts (Fs in place of F).
+ * The router stays in full precision ("AI Infrastructure series, Part 12 of
+ * 24", "How do you serve an MoE model on your own GPUs?": only the experts'
+ * weights go to low precision).
+ */
+int moe_oracle_layer_fp8(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
+                         int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
+                         int32_t n_groups, int32_t topk_groups,
+                         const float* hidden, const float* w_router, const float* router_bias,
+                         const float* sel_bias, const uint8_t* const* q_gate,
+                         const uint8_t* const* q_up, const uint8_t* const* q_down,
+                         const float* const* s_gate, const float* const* s_up,
+                         const float* const* s_down, const uint8_t* const* qs_gate,
+                         const uint8_t* const* qs_up, const uint8_t* const* qs_down,
+                         const float* const* ss_gate, const float* const* ss_up,
+                         const float* const* ss_down, const unsigned char* keep,
+                         int32_t* topk_idx, double* topk_w, double* margin, double* out) {
+  if (!s_gate || !s_up || !s_down) return ORACLE_ERR_ARG;
+  if (S > 0 && (!ss_gate || !ss_up || !ss_down)) return ORACLE_ERR_ARG;
+  const wset_t routed = {1, (const void* const*)q_gate, (const void* const*)q_up,
+                         (const void* const*)q_down, s_gate, s_up, s_down};
+  const wset_t shared = {1, (const void* const*)qs_gate, (const void* const*)qs_up,
+                         (const void* const*)qs_down, ss_gate, ss_up, ss_down};
+  return layer_impl(n_rows, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups, hidden,
+                    w_router, router_bias, sel_bias, &routed, &shared, keep, topk_idx, topk_w, margin,
+                    out);
 }

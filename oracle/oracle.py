@@ -57,6 +57,12 @@ def _load():
         lib.moe_oracle_expert_choice.restype = ctypes.c_int
         lib.moe_oracle_layer_routed.argtypes = [i64] + [i32] * 6 + [P] * 10
         lib.moe_oracle_layer_routed.restype = ctypes.c_int
+        lib.moe_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.moe_oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.moe_oracle_expert_ffn_fp8.argtypes = [i32, i32] + [P] * 9
+        lib.moe_oracle_expert_ffn_fp8.restype = None
+        lib.moe_oracle_layer_fp8.argtypes = [i64] + [i32] * 10 + [P] * 21
+        lib.moe_oracle_layer_fp8.restype = ctypes.c_int
         lib.moe_oracle_silu.argtypes = [ctypes.c_double]
         lib.moe_oracle_silu.restype = ctypes.c_double
         lib.moe_oracle_num_threads.argtypes = []
@@ -174,6 +180,35 @@ def expert_ffn(x, w_gate, w_up, w_down, return_h=False):
     return (h, y) if return_h else y
 
 
+def e4m3_value(code: int) -> float:
+    """The value of one FP8 E4M3 code (0..255) as the oracle decodes it."""
+    return float(_load().moe_oracle_e4m3_to_double(int(code)))
+
+
+def _u8(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("fp8 expert weights must be E4M3 codes (uint8)")
+    return a
+
+
+def expert_ffn_fp8(x, q_gate, s_gate, q_up, s_up, q_down, s_down, return_h=False):
+    """One SwiGLU expert with FP8 E4M3 weights: codes uint8 ([F][d], [F][d],
+    [d][F]) and fp32 per-row scales ([F], [F], [d]). Returns y (or (h, y))."""
+    lib = _load()
+    x = _f64(x)
+    qg, qu, qd = _u8(q_gate), _u8(q_up), _u8(q_down)
+    sg, su, sd = _f32(s_gate), _f32(s_up), _f32(s_down)
+    F, d = qg.shape
+    assert x.shape == (d,) and qu.shape == (F, d) and qd.shape == (d, F)
+    assert sg.shape == (F,) and su.shape == (F,) and sd.shape == (d,)
+    h = np.empty((F,), np.float64)
+    y = np.empty((d,), np.float64)
+    lib.moe_oracle_expert_ffn_fp8(d, F, _ptr(x), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(qd),
+                                  _ptr(sd), _ptr(h), _ptr(y))
+    return (h, y) if return_h else y
+
+
 def combine(w, y, shared=None):
     """out = sum_k w[k] * y[k] (+ shared)."""
     lib = _load()
@@ -243,6 +278,61 @@ def layer(hidden, w_router, w_gate, w_up, w_down, K, score_fn=SOFTMAX, renormali
     del k1, k2, k3, k4, k5, k6
     if rc != 0:
         raise ValueError(f"moe_oracle_layer failed ({rc})")
+    return dict(idx=idx, w=w, margin=margin, out=out)
+
+
+def _raw_ptr_array(mats, n, conv):
+    arr = (ctypes.c_void_p * n)()
+    keep = []
+    for i in range(n):
+        m = mats[i] if mats is not None and i < len(mats) else None
+        if m is None:
+            arr[i] = None
+        else:
+            b = conv(m)
+            keep.append(b)
+            arr[i] = b.ctypes.data
+    return arr, keep
+
+
+def layer_fp8(hidden, w_router, q_gate, s_gate, q_up, s_up, q_down, s_down, K, score_fn=SOFTMAX,
+              renormalize=1, router_bias=None, sel_bias=None, qs_gate=None, ss_gate=None, qs_up=None,
+              ss_up=None, qs_down=None, ss_down=None, n_groups=0, topk_groups=0, keep=None):
+    """The whole layer with FP8 E4M3 expert weights (per-expert uint8 codes
+    and fp32 per-row scales; routed: q_*/s_*, shared: qs_*/ss_*). Otherwise
+    as layer(). Returns dict(idx, w, margin, out)."""
+    lib = _load()
+    x = _f32(hidden)
+    W = _f32(w_router)
+    n, d = x.shape
+    N = W.shape[1]
+    F = next(_u8(m).shape[0] for m in q_gate if m is not None)
+    S = 0 if qs_gate is None else len(qs_gate)
+    Fs = _u8(qs_gate[0]).shape[0] if S else 0
+    arrays = []
+    keepalive = []
+    for mats, cnt, conv in ((q_gate, N, _u8), (q_up, N, _u8), (q_down, N, _u8), (s_gate, N, _f32),
+                            (s_up, N, _f32), (s_down, N, _f32), (qs_gate, S, _u8), (qs_up, S, _u8),
+                            (qs_down, S, _u8), (ss_gate, S, _f32), (ss_up, S, _f32),
+                            (ss_down, S, _f32)):
+        if cnt == 0:
+            arrays.append(None)
+            continue
+        arr, k = _raw_ptr_array(mats, cnt, conv)
+        keepalive.append((arr, k))
+        arrays.append(ctypes.cast(arr, ctypes.c_void_p))
+    rb, sb = _f32(router_bias), _f32(sel_bias)
+    keep_a = None if keep is None else np.ascontiguousarray(keep, dtype=np.uint8)
+    idx = np.empty((n, K), np.int32)
+    w = np.empty((n, K), np.float64)
+    margin = np.empty((n,), np.float64)
+    out = np.empty((n, d), np.float64)
+    rc = lib.moe_oracle_layer_fp8(n, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups,
+                                  _ptr(x), _ptr(W), _ptr(rb), _ptr(sb), *arrays, _ptr(keep_a),
+                                  _ptr(idx), _ptr(w), _ptr(margin), _ptr(out))
+    del keepalive
+    if rc != 0:
+        raise ValueError(f"moe_oracle_layer_fp8 failed ({rc})")
     return dict(idx=idx, w=w, margin=margin, out=out)
 
 

@@ -581,3 +581,123 @@ def test_layer_routed_matches_token_choice_layer():
     ref = oracle.layer(x, W, wg, wu, wd, K=K)
     out = oracle.layer_routed(x, ref["idx"], ref["w"], wg, wu, wd)
     np.testing.assert_allclose(out, ref["out"], rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- FP8 E4M3 experts
+
+
+def test_e4m3_decode_closed_form_points():
+    # OCP 8-bit floating point, E4M3: bias 7, no infinities, S.1111.111 is NaN.
+    assert oracle.e4m3_value(0x00) == 0.0
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9            # smallest subnormal: 1/8 * 2^-6
+    assert oracle.e4m3_value(0x07) == 7 * 2.0 ** -9        # largest subnormal
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6            # smallest normal
+    assert oracle.e4m3_value(0x38) == 1.0                  # exponent 7 = bias
+    assert oracle.e4m3_value(0x3C) == 1.5
+    assert oracle.e4m3_value(0x7E) == 448.0                # largest finite
+    assert math.isnan(oracle.e4m3_value(0x7F))
+    assert math.isnan(oracle.e4m3_value(0xFF))
+    z = oracle.e4m3_value(0x80)
+    assert z == 0.0 and math.copysign(1.0, z) < 0
+    assert oracle.e4m3_value(0xFE) == -448.0
+
+
+def test_e4m3_decode_matches_torch_float8_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_value(c) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_decode_is_monotone_and_sign_symmetric():
+    pos = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+    assert np.all(np.diff(pos) > 0)
+    neg = np.array([oracle.e4m3_value(c | 0x80) for c in range(0x7F)])
+    assert np.array_equal(neg, -pos)
+
+
+def _fp8_case(rng, F, d, pow2_scales):
+    """E4M3 codes (no NaN) and row scales, plus the same weights as bf16 bits
+    (exact when the scales are powers of two: a code has at most 4 significant
+    bits, bf16 holds 8)."""
+    def mat(rows, cols):
+        q = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] ^= 0x01  # NaN -> the largest finite code of that sign
+        if pow2_scales:
+            s = np.ldexp(1.0, rng.integers(-12, -4, size=rows)).astype(np.float32)
+        else:
+            s = rng.uniform(1e-4, 3e-3, size=rows).astype(np.float32)
+        vals = torch.from_numpy(q.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        w = vals * s.astype(np.float64)[:, None]
+        return q, s, w
+    qg, sg, wg = mat(F, d)
+    qu, su, wu = mat(F, d)
+    qd, sd, wd = mat(d, F)
+    return (qg, sg, qu, su, qd, sd), (wg, wu, wd)
+
+
+def test_expert_ffn_fp8_equals_bf16_expert_on_exact_weights():
+    rng = np.random.default_rng(11)
+    F, d = 24, 40
+    (qg, sg, qu, su, qd, sd), (wg, wu, wd) = _fp8_case(rng, F, d, pow2_scales=True)
+    bits = [_bf16_bits(m) for m in (wg, wu, wd)]
+    for m, b in zip((wg, wu, wd), bits):
+        assert np.array_equal(_bf16_to_f64(b), m)  # the weights are exact in bf16
+    x = rng.standard_normal(d)
+    h8, y8 = oracle.expert_ffn_fp8(x, qg, sg, qu, su, qd, sd, return_h=True)
+    h16, y16 = oracle.expert_ffn(x, *bits, return_h=True)
+    assert np.array_equal(h8, h16)
+    assert np.array_equal(y8, y16)
+
+
+def test_expert_ffn_fp8_row_scales_factor_out():
+    # A per-row scale multiplies that row's dot product: u_f (hence h_f, since
+    # h = SiLU(g) * u) scales with s_up[f], and y_i with s_down[i].
+    rng = np.random.default_rng(12)
+    F, d = 16, 32
+    (qg, sg, qu, su, qd, sd), _ = _fp8_case(rng, F, d, pow2_scales=False)
+    x = rng.standard_normal(d)
+    ones_u, ones_d = np.ones(F, np.float32), np.ones(d, np.float32)
+    h, y = oracle.expert_ffn_fp8(x, qg, sg, qu, su, qd, sd, return_h=True)
+    h1, _ = oracle.expert_ffn_fp8(x, qg, sg, qu, ones_u, qd, sd, return_h=True)
+    np.testing.assert_allclose(h, h1 * su.astype(np.float64), rtol=1e-13, atol=0)
+    _, y1 = oracle.expert_ffn_fp8(x, qg, sg, qu, su, qd, ones_d, return_h=True)
+    np.testing.assert_allclose(y, y1 * sd.astype(np.float64), rtol=1e-13, atol=1e-300)
+
+
+def test_layer_fp8_equals_bf16_layer_on_exact_weights():
+    rng = np.random.default_rng(13)
+    T, d, N, K, F, Fs = 9, 32, 4, 2, 16, 24
+    hidden = rng.standard_normal((T, d)).astype(np.float32)
+    w_router = rng.standard_normal((d, N)).astype(np.float32)
+    routed = [_fp8_case(rng, F, d, True) for _ in range(N)]
+    shared = [_fp8_case(rng, Fs, d, True)]
+    q = lambda cases, j: [c[0][j] for c in cases]  # noqa: E731
+    b = lambda cases, j: [_bf16_bits(c[1][j]) for c in cases]  # noqa: E731
+    got = oracle.layer_fp8(hidden, w_router, q(routed, 0), q(routed, 1), q(routed, 2), q(routed, 3),
+                           q(routed, 4), q(routed, 5), K=K, score_fn=oracle.SIGMOID,
+                           qs_gate=q(shared, 0), ss_gate=q(shared, 1), qs_up=q(shared, 2),
+                           ss_up=q(shared, 3), qs_down=q(shared, 4), ss_down=q(shared, 5))
+    ref = oracle.layer(hidden, w_router, b(routed, 0), b(routed, 1), b(routed, 2), K=K,
+                       score_fn=oracle.SIGMOID, ws_gate=b(shared, 0), ws_up=b(shared, 1),
+                       ws_down=b(shared, 2))
+    assert np.array_equal(got["idx"], ref["idx"])
+    assert np.array_equal(got["w"], ref["w"])
+    assert np.array_equal(got["out"], ref["out"])
+
+
+def test_fp8_input_codes_decode_to_the_drawn_weights():
+    # The generator's codes times their row scale reproduce the normal draw to
+    # E4M3 precision (relative step 2^-3 for normal codes), and never hit NaN.
+    cfg = inputs.TINY.with_(expert_dtype="fp8")
+    w = inputs.make_expert_weights(cfg, seed=3)
+    q = w["w_gate"][0].numpy()
+    assert not np.any((q & 0x7F) == 0x7F)
+    s = w["w_gate_scale"][0].numpy().astype(np.float64)
+    vals = np.vectorize(oracle.e4m3_value)(q) * s[:, None]
+    assert np.allclose(np.abs(vals).max(axis=1), 448.0 * s, rtol=0, atol=0)
+    std = vals.std()
+    assert abs(std - 1.0 / math.sqrt(cfg.d)) < 0.1 / math.sqrt(cfg.d)
