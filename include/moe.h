@@ -39,7 +39,9 @@
  *     device (an expert index out of range, a pipeline wait that ran out of
  *     time) are recorded in an error word inside the workspace and reported by
  *     moe_get_device_status; kernels never trap.
- *   - Row-major layouts throughout. bf16 is IEEE bfloat16 stored as uint16.
+ *   - Row-major layouts throughout. bf16 is IEEE bfloat16 stored as uint16;
+ *     fp16 is IEEE binary16; FP8 E4M3 is the OCP 8-bit float with 4 exponent
+ *     bits (bias 7), 3 mantissa bits and no infinities, stored as uint8.
  *   - Layer outputs exclude the residual stream (the residual path lies
  *     outside the FFN slot the layer replaces).
  */
@@ -60,12 +62,34 @@ typedef enum {
   MOE_ERR_WORKSPACE = -3,     /* ws is NULL, misaligned or smaller than needed */
   MOE_ERR_CUDA = -4,          /* a CUDA runtime call or a launch failed */
   MOE_ERR_TIMEOUT = -5,       /* device: a bounded pipeline wait gave up */
-  MOE_ERR_DEVICE_BOUNDS = -6  /* device: an input index was out of range */
+  MOE_ERR_DEVICE_BOUNDS = -6, /* device: an input index was out of range */
+  MOE_ERR_RANGE = -7          /* device: an fp16 activation of the FP8-weight
+                                 path overflowed (|value| >= 65520) */
 } moe_status_t;
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn_t;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 typedef enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing_t;
+
+/*
+ * Storage format of the expert matrices (routed and shared alike; the router
+ * is always fp32). Storing only the experts in low precision is the serving
+ * recipe of "AI Infrastructure series, Part 12 of 24", "How do you serve an
+ * MoE model on your own GPUs?"; it cuts the bytes a token reads by the same
+ * factor ("Mixture of Experts Explained", "Total versus active parameters").
+ *   MOE_EXPERT_BF16      bf16 matrices
+ *   MOE_EXPERT_FP8_E4M3  FP8 E4M3 codes with one fp32 scale per matrix row:
+ *                        weight = e4m3(code) * scale[row]. NaN codes
+ *                        (0x7F, 0xFF) are not supported. The activations the
+ *                        expert GEMMs read (x_perm, h_perm) are then fp16
+ *                        instead of bf16: the tensor cores take both
+ *                        operands in one type, and fp16 holds every E4M3
+ *                        value exactly; the conversion to fp16 is exact for
+ *                        bf16 activations of magnitude 2^-14 .. 65504,
+ *                        within 2^-25 below that, and an overflow beyond it
+ *                        is reported as MOE_ERR_RANGE.
+ */
+typedef enum { MOE_EXPERT_BF16 = 0, MOE_EXPERT_FP8_E4M3 = 1 } moe_expert_dtype_t;
 
 /* Which call a workspace is sized for (moe_workspace_bytes). */
 typedef enum {
@@ -111,6 +135,9 @@ typedef struct moe_problem {
                             C = min(ceil(c T K / N), T) tokens, c =
                             capacity_factor or 1 when 0; K is then the mean
                             number of experts per token)                    */
+  int32_t expert_dtype;  /* moe_expert_dtype_t of every expert matrix. FP8
+                            requires d_model, ffn and shared_ffn to be
+                            multiples of 16                                */
 } moe_problem_t;
 
 /*
@@ -126,6 +153,12 @@ typedef struct moe_problem {
  *   sel_bias     fp32 [N] or NULL: selection-only bias, added to the sigmoid
  *                score before top-K, never to the mixing weights (sigmoid
  *                scoring only)
+ * With expert_dtype == MOE_EXPERT_FP8_E4M3 the expert matrices hold uint8
+ * codes in the same layouts, and the *_scale arrays hold one fp32 scale per
+ * matrix row (16-byte aligned):
+ *   w_gate_scale, w_up_scale [N][F]; w_down_scale [N][d];
+ *   ws_gate_scale, ws_up_scale [S][Fs]; ws_down_scale [S][d] (NULL when S == 0).
+ * They are ignored for bf16 experts.
  */
 typedef struct moe_weights {
   const float* w_router;
@@ -137,6 +170,12 @@ typedef struct moe_weights {
   const void* ws_gate;
   const void* ws_up;
   const void* ws_down;
+  const float* w_gate_scale;
+  const float* w_up_scale;
+  const float* w_down_scale;
+  const float* ws_gate_scale;
+  const float* ws_up_scale;
+  const float* ws_down_scale;
 } moe_weights_t;
 
 /* Human-readable name of a moe_status_t. Never NULL. Host only. */
@@ -184,7 +223,8 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden,
  * prefix sum and a stable expert-major permutation of the T*K token copies
  * (expert ascending, then token ascending), plus the gather of the hidden rows
  * into that order.
- *   topk_idx   int32 [T][K], every entry in [0, N)
+ *   topk_idx   int32 [T][K], every entry in [0, N), the K entries of a token
+ *              distinct (as top-K selection gives them)
  *   hidden     [T][d], p->hidden_dtype
  *   counts     out int32 [N]:   counts[e] = #{(t,k) : topk_idx[t][k] == e}
  *   offsets    out int32 [N+1]: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
@@ -193,7 +233,9 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden,
  *              -1 for a copy dropped by its expert's capacity (p->capacity_factor
  *              > 0), in which case offsets count kept copies only, perm_src lists
  *              offsets[N] rows and counts still count every copy routed to e
- *   x_perm     out bf16 [T*K][d]: x_perm[r] = bf16(hidden[perm_src[r] / K])
+ *   x_perm     out [T*K][d]: x_perm[r] = hidden[perm_src[r] / K] rounded to
+ *              bf16, or to fp16 when p->expert_dtype is FP8 (an fp16 overflow
+ *              sets MOE_ERR_RANGE in the workspace error word)
  *   ws         workspace of moe_workspace_bytes(p, MOE_CALL_PERMUTE) bytes
  * Token-choice problems only (MOE_ERR_INVALID_ARG otherwise).
  * The result is deterministic. An index outside [0, N) sets
@@ -275,12 +317,38 @@ moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t* topk_idx,
  * x_perm = the hidden rows in bf16, weights = that shared expert's.
  * For an expert-choice problem the packed rows are the N*C picks
  * (moe_expert_choice_select) and offsets are e*C.
+ * bf16 experts only (p->expert_dtype == MOE_EXPERT_BF16, else
+ * MOE_ERR_INVALID_ARG); FP8 experts use moe_grouped_swiglu_fp8.
  */
 moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm,
                                 const int32_t* offsets, const void* w_gate,
                                 const void* w_up, const void* w_down,
                                 void* h_perm, void* y_perm, void* ws,
                                 size_t ws_bytes, void* stream);
+
+/*
+ * moe_grouped_swiglu for FP8 E4M3 experts (p->expert_dtype ==
+ * MOE_EXPERT_FP8_E4M3, else MOE_ERR_INVALID_ARG):
+ *   h_perm[r] = fp16( SiLU(g) * u ),  g_f = sg[e][f] * (Q_gate[e] x_perm[r])_f,
+ *                                     u_f = su[e][f] * (Q_up[e] x_perm[r])_f
+ *   y_perm[r] = bf16( sd[e][i] * (Q_down[e] h_perm[r])_i )
+ * with Q the decoded E4M3 codes (exact), fp32 accumulation.
+ *   x_perm  fp16 [rows][d] (moe_permute writes fp16 for FP8 problems)
+ *   w_gate, w_up uint8 [N][F][d], w_gate_scale, w_up_scale fp32 [N][F]
+ *   w_down uint8 [N][d][F], w_down_scale fp32 [N][d]
+ *   h_perm  out fp16 [rows][F];  y_perm out bf16 [rows][d]
+ *   ws      workspace of moe_workspace_bytes(p, MOE_CALL_GROUPED_SWIGLU) bytes
+ * rows, offsets and shared experts as moe_grouped_swiglu (a shared expert is
+ * one group over every token with its own codes and scales). An h value
+ * beyond fp16's range sets MOE_ERR_RANGE in the workspace error word.
+ */
+moe_status_t moe_grouped_swiglu_fp8(const moe_problem_t* p, const void* x_perm,
+                                    const int32_t* offsets, const void* w_gate,
+                                    const float* w_gate_scale, const void* w_up,
+                                    const float* w_up_scale, const void* w_down,
+                                    const float* w_down_scale, void* h_perm,
+                                    void* y_perm, void* ws, size_t ws_bytes,
+                                    void* stream);
 
 /*
  * Gate-weighted combine back to token order ("Chapter 19", §19.2 flowchart,
@@ -315,6 +383,9 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm,
  * (moe_expert_choice_select) and each picked (token, expert) pair adds
  * S[t][e] * E_e(x_t); topk_idx_opt and topk_w_opt must then be NULL and
  * counts_opt receives C for every expert.
+ * With p->expert_dtype == MOE_EXPERT_FP8_E4M3 every expert (routed and
+ * shared) reads its E4M3 codes and row scales from `w` and the expert GEMMs
+ * run on fp16 activations (see moe_expert_dtype_t).
  */
 moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
                                const void* hidden, void* out,
@@ -349,7 +420,8 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p);
  * Synchronises `stream`, then reads and clears the device error word in `ws`
  * (a workspace previously passed to moe_permute, moe_grouped_swiglu or
  * moe_layer_forward). Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS,
- * or MOE_ERR_CUDA if the stream itself reports an error.
+ * MOE_ERR_RANGE (in that order of precedence when several are recorded), or
+ * MOE_ERR_CUDA if the stream itself reports an error.
  */
 moe_status_t moe_get_device_status(void* ws, void* stream);
 

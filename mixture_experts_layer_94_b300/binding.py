@@ -23,6 +23,8 @@ CALL_PERMUTE, CALL_GROUPED_SWIGLU, CALL_LAYER_FORWARD, CALL_ROUTER = 0, 1, 2, 3
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DT_F32, DT_BF16 = 0, 1
 ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
+EXPERT_BF16, EXPERT_FP8_E4M3 = 0, 1
+MOE_ERR_RANGE = -7
 
 
 class MoEError(RuntimeError):
@@ -37,12 +39,17 @@ class Problem(ctypes.Structure):
                 ("shared_ffn", ctypes.c_int32), ("score_fn", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("hidden_dtype", ctypes.c_int32),
                 ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_double), ("routing", ctypes.c_int32)]
+                ("capacity_factor", ctypes.c_double), ("routing", ctypes.c_int32),
+                ("expert_dtype", ctypes.c_int32)]
+
+
+WEIGHT_FIELDS = ("w_router", "router_bias", "sel_bias", "w_gate", "w_up", "w_down", "ws_gate", "ws_up",
+                 "ws_down", "w_gate_scale", "w_up_scale", "w_down_scale", "ws_gate_scale", "ws_up_scale",
+                 "ws_down_scale")
 
 
 class Weights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("w_router", "router_bias", "sel_bias", "w_gate", "w_up",
-                                                "w_down", "ws_gate", "ws_up", "ws_down")]
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
 
 
 def _load():
@@ -59,6 +66,7 @@ def _load():
         "moe_router_topk": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_permute": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_grouped_swiglu": ([pp] + [P] * 8 + [sz, P], i32),
+        "moe_grouped_swiglu_fp8": ([pp] + [P] * 11 + [sz, P], i32),
         "moe_combine": ([pp] + [P] * 6, i32),
         "moe_layer_forward": ([pp, ctypes.POINTER(Weights)] + [P] * 6 + [sz, P], i32),
         "moe_get_device_status": ([P, P], i32),
@@ -100,7 +108,8 @@ def problem(cfg: MoEConfig = None, **kw) -> Problem:
              shared_ffn=cfg.Fs, score_fn=cfg.score_fn, renormalize=cfg.renormalize,
              hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16, n_groups=cfg.n_groups,
              topk_groups=cfg.topk_groups, capacity_factor=cfg.capacity_factor,
-             routing=ROUTING_EXPERT_CHOICE if cfg.routing == "expert" else ROUTING_TOKEN_CHOICE) if cfg else {}
+             routing=ROUTING_EXPERT_CHOICE if cfg.routing == "expert" else ROUTING_TOKEN_CHOICE,
+             expert_dtype=EXPERT_FP8_E4M3 if cfg.expert_dtype == "fp8" else EXPERT_BF16) if cfg else {}
     f.update(kw)
     return Problem(**f)
 
@@ -175,6 +184,14 @@ def grouped_swiglu(p: Problem, x_perm, offsets, w_gate, w_up, w_down, h_perm, y_
                                   _stream(stream)), "moe_grouped_swiglu")
 
 
+def grouped_swiglu_fp8(p: Problem, x_perm, offsets, w_gate, w_gate_scale, w_up, w_up_scale, w_down,
+                       w_down_scale, h_perm, y_perm, ws, stream=None):
+    _check(lib.moe_grouped_swiglu_fp8(ctypes.byref(p), _p(x_perm), _p(offsets), _p(w_gate), _p(w_gate_scale),
+                                      _p(w_up), _p(w_up_scale), _p(w_down), _p(w_down_scale), _p(h_perm),
+                                      _p(y_perm), _p(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_swiglu_fp8")
+
+
 def combine(p: Problem, y_perm, inv_row, topk_w, out, shared_out=None, stream=None):
     _check(lib.moe_combine(ctypes.byref(p), _p(y_perm), _p(inv_row), _p(topk_w), _p(shared_out),
                            _p(out), _stream(stream)), "moe_combine")
@@ -184,8 +201,7 @@ def weights_struct(w: dict) -> Weights:
     def ptr(k):
         t = w.get(k)
         return None if t is None else t.data_ptr()
-    return Weights(*(ptr(k) for k in ("w_router", "router_bias", "sel_bias", "w_gate", "w_up",
-                                      "w_down", "ws_gate", "ws_up", "ws_down")))
+    return Weights(*(ptr(k) for k in WEIGHT_FIELDS))
 
 
 def layer_forward(p: Problem, weights: Weights, hidden, out, ws, topk_idx=None, topk_w=None,
@@ -229,16 +245,15 @@ class MoELayer:
     """One MoE FFN layer on the GPU: weights and workspace held on the device.
 
     weights: dict with w_router, router_bias, sel_bias, w_gate, w_up, w_down,
-    ws_gate, ws_up, ws_down (torch CUDA tensors or None).
+    ws_gate, ws_up, ws_down and, for FP8 experts, the *_scale row scales
+    (torch CUDA tensors or None).
     """
 
     def __init__(self, cfg: MoEConfig, weights: dict, T: int = None, device="cuda"):
         self.cfg = cfg if T is None else cfg.with_(T=T)
         self.device = torch.device(device)
         self.w = {k: (None if v is None else v.to(self.device).contiguous())
-                  for k, v in weights.items()
-                  if k in ("w_router", "router_bias", "sel_bias", "w_gate", "w_up", "w_down",
-                           "ws_gate", "ws_up", "ws_down")}
+                  for k, v in weights.items() if k in WEIGHT_FIELDS}
         self.ws_struct = weights_struct(self.w)
         self._ws = {}
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,6 +11,7 @@ namespace moe {
 // Bits of the device error word (first 4 bytes of every workspace).
 constexpr uint32_t kErrTimeout = 1u;  // a bounded pipeline wait gave up
 constexpr uint32_t kErrBounds = 2u;   // an input index was out of range
+constexpr uint32_t kErrRange = 4u;    // an fp16 activation (FP8-weight experts) overflowed
 
 // Bound on any single pipeline wait. The longest legitimate wait in this
 // library is one output tile of MMA work (well under a millisecond), so two
@@ -46,6 +48,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -48,6 +48,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_sched.cuh"
 
 namespace moe {
 namespace {
@@ -69,26 +70,6 @@ struct Cfg {
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + kBarrierBytes;
 };
 
-struct TileInfo {
-  GroupDesc g;
-  int m_blk, n_blk;
-};
-
-__device__ __forceinline__ TileInfo decode_tile(int tile, const GemmArgs& a) {
-  int lo = 0, hi = a.G - 1;
-  while (lo < hi) {  // last group whose first tile is <= tile (skips empty groups)
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(a.tile_start + mid) <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileInfo ti;
-  ti.g = a.groups[lo];
-  const int local = tile - __ldg(a.tile_start + lo);
-  ti.n_blk = local / ti.g.m_tiles;
-  ti.m_blk = local - ti.n_blk * ti.g.m_tiles;
-  return ti;
-}
-
 struct RouterTile {
   int m_blk, split, part, kb0, kb1;
 };
@@ -102,14 +83,6 @@ __device__ __forceinline__ RouterTile decode_router_tile(int tile, const GemmArg
   r.kb0 = slice * a.r_kb_per_slice;
   r.kb1 = min(a.r_nkb_d, r.kb0 + a.r_kb_per_slice);
   return r;
-}
-
-__device__ __forceinline__ bool wait_raw(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-  return true;
 }
 
 template <int PHASE, int EPI, int PAIR>

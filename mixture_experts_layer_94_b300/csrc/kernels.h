@@ -68,9 +68,10 @@ struct PermuteArgs {
   int32_t* offsets;       // [N+1]
   int32_t* perm_src;      // [T*K]
   int32_t* inv_row;       // [T*K]
-  __nv_bfloat16* x_perm;  // [T*K][d]
+  void* x_perm;           // [T*K][d] in the activation format (bf16, or fp16 when act_f16)
   float* zero_rows;       // [T][d] fp32 to clear, or nullptr
-  __nv_bfloat16* x_bf16;  // [T][d] bf16 copy of hidden, or nullptr
+  void* x_act;            // [T][d] copy of hidden in the activation format, or nullptr
+  bool act_f16;           // activations for FP8-weight experts: fp16 rows
   uint32_t* err;
   // Optional: also build the GEMM schedule (as launch_schedule) from the new
   // offsets; skipped when groups == nullptr.
@@ -80,7 +81,7 @@ struct PermuteArgs {
   int32_t S, F, Fs, tile_rows;
 };
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
-// Only the row gather (+ the accumulator clear / bf16 copy), for rows already
+// Only the row gather (+ the accumulator clear / activation copy), for rows already
 // placed: token of row r = row_token[r], rows = offsets[N].
 cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s);
 // Expert capacity ceil(c * T * K / N) of a problem; INT32_MAX when dropless.
@@ -118,6 +119,11 @@ struct GemmArgs {
   const float* row_w;    // scatter epilogue, expert choice: perm_src is the row's token, row_w its weight
   int32_t d;
   uint32_t* err;
+  // FP8 expert weights: fp32 scale of each weight row, per kind (gate/up
+  // phase: w_scale = gate rows, u_scale = up rows; down phase: w_scale = rows
+  // of W_down).
+  const float* w_scale[2];
+  const float* u_scale[2];
   // Router phase: one group of all T tokens; tile = (m block, split) with
   // split = part * r_dslices + slice.
   int32_t r_tiles, r_m_tiles, r_dslices, r_kb_per_slice, r_nkb_d, r_d_pad, r_np, r_N;
@@ -131,6 +137,28 @@ struct GemmMaps {
   CUtensorMap b[2];   // weights per kind (gate for the gate/up phase)
   CUtensorMap bu[2];  // up weights per kind (gate/up phase only)
 };
+
+// Tensor maps of the FP8-weight grouped GEMM. Activations (fp16, 128-byte
+// swizzle) per kind with boxes of 16, 32, 64 and 128 rows (a tile loads the
+// smallest box that holds its token rows); weights (E4M3 codes, no swizzle)
+// per kind with 128-row boxes: w = gate (gate/up phase) or down rows, u = up.
+struct F8Maps {
+  CUtensorMap x[2][4];
+  CUtensorMap w[2];
+  CUtensorMap u[2];
+};
+constexpr int kF8XBoxes = 4;  // box rows 16 << i
+
+// fp16 row-major matrix as a TMA tensor map, box [box_rows][64], 128-byte swizzle.
+bool make_tmap_f16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
+// uint8 (FP8 code) row-major matrix, box [box_rows][64 bytes], no swizzle.
+// The row pitch (`inner` bytes) must be a multiple of 16.
+bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
+
+// Grouped GEMM with FP8 E4M3 weights (one CTA per tile, 128 weight rows x up
+// to 128 token rows per MMA; tiles as launch_grouped_gemm with pair = 1).
+cudaError_t launch_grouped_gemm_fp8(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
+                                    int64_t tile_bound, cudaStream_t s);
 
 // Upper bound on the tile count (host, from sizes only), used for the grid.
 int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T,

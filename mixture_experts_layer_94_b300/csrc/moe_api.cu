@@ -20,7 +20,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
-  size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_bf16, h, h_sh, out_acc;
+  size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc;
   size_t total;
 };
 
@@ -30,6 +30,15 @@ int64_t ec_capacity(const moe_problem_t& p) {
   const double c = p.capacity_factor > 0.0 ? p.capacity_factor : 1.0;
   const double cap = ceil(c * (double)p.T * (double)p.top_k / (double)p.n_experts);
   return cap >= (double)p.T ? p.T : (int64_t)cap;
+}
+
+bool is_fp8(const moe_problem_t& p) { return p.expert_dtype == MOE_EXPERT_FP8_E4M3; }
+
+// The shared experts read every token's hidden row in the activation format
+// (bf16 for bf16 experts, fp16 for FP8 experts): a copy unless hidden is
+// already in it.
+bool needs_act_copy(const moe_problem_t& p) {
+  return p.n_shared > 0 && (is_fp8(p) || p.hidden_dtype == MOE_F32);
 }
 
 Layout make_layout(const moe_problem_t& p, int call) {
@@ -68,7 +77,7 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.perm_src = take((size_t)TK * 4);
     L.inv_row = take((size_t)TK * 4);
     L.x_perm = take((size_t)rows * p.d_model * 2);
-    if (p.n_shared > 0 && p.hidden_dtype == MOE_F32) L.x_bf16 = take((size_t)T * p.d_model * 2);
+    if (needs_act_copy(p)) L.x_act = take((size_t)T * p.d_model * 2);
     L.h = take((size_t)rows * p.ffn * 2);
     if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
     L.out_acc = take((size_t)T * p.d_model * 4);
@@ -128,6 +137,31 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t ro
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// fp16 matrix, same geometry as make_tmap_bf16.
+bool make_tmap_f16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  if (!have_encode()) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// uint8 codes [rows][inner], box [box_rows][64 bytes], dense rows in shared
+// memory (no swizzle), zero fill out of bounds.
+bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  if (!have_encode() || (inner % 16) != 0) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace moe
 
 namespace {
@@ -159,9 +193,15 @@ T* at(void* ws, size_t off) {
 // shapes (a few rows per expert) keep 128-row tiles on single CTAs.
 int32_t gemm_pair(int64_t routed_rows, int32_t N) { return routed_rows >= (int64_t)256 * N ? 2 : 1; }
 
+// Tile rows of the GEMM schedule: the FP8-weight kernel always takes 128.
+int32_t gemm_pair_for(const moe_problem_t& p, int64_t routed_rows) {
+  return is_fp8(p) ? 1 : gemm_pair(routed_rows, p.n_experts);
+}
+
 // The two GEMM phases over groups already described in the workspace.
 struct GemmPlan {
   int32_t pair;
+  bool fp8;               // FP8 E4M3 weights (+ the row scales below), fp16 activations
   int32_t N, S, F, Fs, d, K;
   int64_t T, routed_rows;
   const void* x_routed;   // [routed_rows][d] bf16
@@ -172,8 +212,14 @@ struct GemmPlan {
   const void* sg;         // [S][Fs][d]
   const void* su;
   const void* sd;         // [S][d][Fs]
-  __nv_bfloat16* h;       // [routed_rows][F]
-  __nv_bfloat16* h_sh;    // [S*T][Fs]
+  const float* wg_scale;  // FP8: [N][F], [N][F], [N][d]
+  const float* wu_scale;
+  const float* wd_scale;
+  const float* sg_scale;  // FP8: [S][Fs], [S][Fs], [S][d]
+  const float* su_scale;
+  const float* sd_scale;
+  __nv_bfloat16* h;       // [routed_rows][F] (fp16 bits when fp8)
+  __nv_bfloat16* h_sh;    // [S*T][Fs] (fp16 bits when fp8)
   int epilogue;           // kEpiScatter or kEpiStoreY
   float* out_acc;
   const int32_t* perm_src;
@@ -196,7 +242,10 @@ cudaError_t record_event(cudaEvent_t e, cudaStream_t s) {
                                              : cudaEventRecord(e, s);
 }
 
+moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup);
+
 moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup = nullptr) {
+  if (g.fp8) return run_gemms_fp8(g, s, ev_after_gateup);
   if (!have_encode()) return MOE_ERR_CUDA;
   const bool sh = g.S > 0;
   GemmMaps m{};
@@ -267,6 +316,88 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   return MOE_OK;
 }
 
+// The activation maps of one kind: boxes of 16, 32, 64 and 128 rows.
+bool make_x_maps(CUtensorMap (&m)[kF8XBoxes], const void* ptr, uint64_t inner, uint64_t rows) {
+  for (int i = 0; i < kF8XBoxes; ++i)
+    if (!make_tmap_f16(&m[i], ptr, inner, rows, 16u << i)) return false;
+  return true;
+}
+
+// The two GEMM phases for FP8 E4M3 experts (128-row tiles on single CTAs).
+moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup) {
+  if (!have_encode()) return MOE_ERR_CUDA;
+  const bool sh = g.S > 0;
+  F8Maps m{};
+  bool ok = make_x_maps(m.x[0], g.x_routed, g.d, g.routed_rows) &&
+            make_tmap_u8(&m.w[0], g.wg, g.d, (uint64_t)g.N * g.F, 128) &&
+            make_tmap_u8(&m.u[0], g.wu, g.d, (uint64_t)g.N * g.F, 128);
+  if (ok && sh)
+    ok = make_x_maps(m.x[1], g.x_shared, g.d, g.T) && make_tmap_u8(&m.w[1], g.sg, g.d, (uint64_t)g.S * g.Fs, 128) &&
+         make_tmap_u8(&m.u[1], g.su, g.d, (uint64_t)g.S * g.Fs, 128);
+  if (!ok) return MOE_ERR_CUDA;
+  if (!sh) {
+    for (int i = 0; i < kF8XBoxes; ++i) m.x[1][i] = m.x[0][i];
+    m.w[1] = m.w[0];
+    m.u[1] = m.u[0];
+  }
+  GemmArgs a{};
+  a.groups = g.groups;
+  a.G = g.N + g.S;
+  a.err = g.err;
+  a.d = g.d;
+  a.top_k = g.K;
+
+  // gate/up + SwiGLU
+  a.tile_start = g.ts_gu;
+  a.n_ext[0] = g.F;
+  a.n_ext[1] = sh ? g.Fs : g.F;
+  a.k_blocks[0] = a.k_blocks[1] = (g.d + kBK - 1) / kBK;
+  a.w_rows[0] = g.F;
+  a.w_rows[1] = sh ? g.Fs : g.F;
+  a.h[0] = g.h;
+  a.h[1] = sh ? g.h_sh : g.h;
+  a.ldh[0] = g.F;
+  a.ldh[1] = sh ? g.Fs : g.F;
+  a.w_scale[0] = g.wg_scale;
+  a.u_scale[0] = g.wu_scale;
+  a.w_scale[1] = sh ? g.sg_scale : g.wg_scale;
+  a.u_scale[1] = sh ? g.su_scale : g.wu_scale;
+  int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kBM);
+  MOE_TRY(cuda_status(launch_grouped_gemm_fp8(kPhaseGateUp, kEpiSwiGLU, m, a, bound, s)));
+  if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[0], s)));
+
+  // down (+ weighted scatter-add or plain store)
+  F8Maps md{};
+  ok = make_x_maps(md.x[0], g.h, g.F, g.routed_rows) && make_tmap_u8(&md.w[0], g.wd, g.F, (uint64_t)g.N * g.d, 128);
+  if (ok && sh)
+    ok = make_x_maps(md.x[1], g.h_sh, g.Fs, (uint64_t)g.S * g.T) &&
+         make_tmap_u8(&md.w[1], g.sd, g.Fs, (uint64_t)g.S * g.d, 128);
+  if (!ok) return MOE_ERR_CUDA;
+  if (!sh) {
+    for (int i = 0; i < kF8XBoxes; ++i) md.x[1][i] = md.x[0][i];
+    md.w[1] = md.w[0];
+  }
+  md.u[0] = md.w[0];
+  md.u[1] = md.w[1];
+  a.tile_start = g.ts_dn;
+  a.n_ext[0] = a.n_ext[1] = g.d;
+  a.k_blocks[0] = (g.F + kBK - 1) / kBK;
+  a.k_blocks[1] = sh ? (g.Fs + kBK - 1) / kBK : a.k_blocks[0];
+  a.w_rows[0] = a.w_rows[1] = g.d;
+  a.w_scale[0] = g.wd_scale;
+  a.w_scale[1] = sh ? g.sd_scale : g.wd_scale;
+  a.u_scale[0] = a.u_scale[1] = nullptr;
+  a.out_acc = g.out_acc;
+  a.perm_src = g.perm_src;
+  a.topk_w = g.topk_w;
+  a.row_w = g.row_w;
+  a.y = g.y;
+  bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kBM);
+  MOE_TRY(cuda_status(launch_grouped_gemm_fp8(kPhaseDown, g.epilogue, md, a, bound, s)));
+  if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[1], s)));
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -280,6 +411,7 @@ const char* moe_status_string(int32_t status) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device pipeline wait timed out";
     case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS: an input index was out of range";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE: an fp16 activation of the FP8-weight path overflowed";
     default: return "MOE_ERR_UNKNOWN: unrecognised status";
   }
 }
@@ -298,6 +430,11 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (!(p->capacity_factor >= 0.0) || p->capacity_factor > 1e30) return MOE_ERR_INVALID_ARG;  // NaN fails too
   if (p->routing != MOE_ROUTING_TOKEN_CHOICE && p->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE && p->n_groups > 1) return MOE_ERR_UNSUPPORTED;
+  if (p->expert_dtype != MOE_EXPERT_BF16 && p->expert_dtype != MOE_EXPERT_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+  if (p->expert_dtype == MOE_EXPERT_FP8_E4M3) {  // 16-byte rows of codes for the TMA boxes
+    if ((p->d_model % 16) != 0 || (p->ffn % 16) != 0) return MOE_ERR_INVALID_ARG;
+    if (p->n_shared > 0 && (p->shared_ffn % 16) != 0) return MOE_ERR_INVALID_ARG;
+  }
   if (p->n_groups > 1) {
     if (p->n_experts % p->n_groups != 0 || p->topk_groups < 1 || p->topk_groups > p->n_groups)
       return MOE_ERR_INVALID_ARG;
@@ -378,16 +515,24 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx, const 
   a.offsets = offsets;
   a.perm_src = perm_src;
   a.inv_row = inv_row;
-  a.x_perm = static_cast<__nv_bfloat16*>(x_perm);
+  a.x_perm = x_perm;
+  a.act_f16 = is_fp8(*p);
   a.err = at<uint32_t>(ws, L.err);
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
-                                const void* w_gate, const void* w_up, const void* w_down, void* h_perm,
-                                void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status_t grouped_swiglu_impl(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
+                                 const void* w_gate, const float* sg, const void* w_up, const float* su,
+                                 const void* w_down, const float* sd, void* h_perm, void* y_perm, void* ws,
+                                 size_t ws_bytes, void* stream) {
   MOE_TRY(moe_problem_check(p));
+  const bool fp8 = is_fp8(*p);
   if (!offsets || !w_gate || !w_up || !w_down) return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!sg || !su || !sd || !aligned16(sg) || !aligned16(su) || !aligned16(sd))) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down)) return MOE_ERR_INVALID_ARG;
   // packed rows: T*K copies (token choice) or N*C picks (expert choice)
   const int64_t rows =
@@ -400,12 +545,16 @@ moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, cons
   MOE_TRY(check_ws(&q, MOE_CALL_GROUPED_SWIGLU, ws, ws_bytes, &L));
   if (rows == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int32_t pair = gemm_pair(rows, q.n_experts);
+  const int32_t pair = gemm_pair_for(q, rows);
   ScheduleArgs sa{q.n_experts, 0, q.ffn, 0, q.d_model, kBM * pair, q.T, offsets, at<GroupDesc>(ws, L.groups),
                   at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
   MOE_TRY(cuda_status(launch_schedule(sa, s)));
   GemmPlan g{};
   g.pair = pair;
+  g.fp8 = fp8;
+  g.wg_scale = sg;
+  g.wu_scale = su;
+  g.wd_scale = sd;
   g.N = q.n_experts;
   g.S = 0;
   g.F = q.ffn;
@@ -426,6 +575,27 @@ moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, cons
   g.ts_dn = at<int32_t>(ws, L.ts_dn);
   g.err = at<uint32_t>(ws, L.err);
   return run_gemms(g, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
+                                const void* w_gate, const void* w_up, const void* w_down, void* h_perm,
+                                void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (p && is_fp8(*p)) return MOE_ERR_INVALID_ARG;
+  return grouped_swiglu_impl(p, x_perm, offsets, w_gate, nullptr, w_up, nullptr, w_down, nullptr, h_perm, y_perm,
+                             ws, ws_bytes, stream);
+}
+
+moe_status_t moe_grouped_swiglu_fp8(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
+                                    const void* w_gate, const float* w_gate_scale, const void* w_up,
+                                    const float* w_up_scale, const void* w_down, const float* w_down_scale,
+                                    void* h_perm, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (p && !is_fp8(*p)) return MOE_ERR_INVALID_ARG;
+  return grouped_swiglu_impl(p, x_perm, offsets, w_gate, w_gate_scale, w_up, w_up_scale, w_down, w_down_scale,
+                             h_perm, y_perm, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm, const int32_t* inv_row, const float* topk_w,
@@ -458,6 +628,17 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   if (p->n_shared > 0 && (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)))
     return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = is_fp8(*p);
+  if (fp8) {
+    const float* sc[3] = {w->w_gate_scale, w->w_up_scale, w->w_down_scale};
+    for (const float* q : sc)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (p->n_shared > 0) {
+      const float* ss[3] = {w->ws_gate_scale, w->ws_up_scale, w->ws_down_scale};
+      for (const float* q : ss)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    }
+  }
   Layout L;
   MOE_TRY(check_ws(p, MOE_CALL_LAYER_FORWARD, ws, ws_bytes, &L));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -509,13 +690,15 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     pa.hidden_bf16 = hbf16;
     pa.offsets = offsets;
     pa.row_token = row_token;
-    pa.x_perm = at<__nv_bfloat16>(ws, L.x_perm);
+    pa.x_perm = at<void>(ws, L.x_perm);
     pa.zero_rows = at<float>(ws, L.out_acc);
-    pa.x_bf16 = (S > 0 && !hbf16) ? at<__nv_bfloat16>(ws, L.x_bf16) : nullptr;
+    pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
+    pa.act_f16 = fp8;
+    pa.err = err;
     MOE_TRY(cuda_status(launch_gather(pa, rows, s)));
     MOE_TRY(record(ev, 2, s));
     // 3. GEMM schedule over the N full expert groups and the shared experts
-    const int32_t pair = gemm_pair(rows, N);
+    const int32_t pair = gemm_pair_for(*p, rows);
     ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, kBM * pair, T, offsets,
                     at<GroupDesc>(ws, L.groups), at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
     MOE_TRY(cuda_status(launch_schedule(sa, s)));
@@ -532,13 +715,20 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     g.T = T;
     g.routed_rows = rows;
     g.x_routed = pa.x_perm;
-    g.x_shared = hbf16 ? hidden : pa.x_bf16;
+    g.x_shared = pa.x_act ? pa.x_act : hidden;
     g.wg = w->w_gate;
     g.wu = w->w_up;
     g.wd = w->w_down;
     g.sg = w->ws_gate;
     g.su = w->ws_up;
     g.sd = w->ws_down;
+  g.fp8 = fp8;
+  g.wg_scale = w->w_gate_scale;
+  g.wu_scale = w->w_up_scale;
+  g.wd_scale = w->w_down_scale;
+  g.sg_scale = w->ws_gate_scale;
+  g.su_scale = w->ws_up_scale;
+  g.sd_scale = w->ws_down_scale;
     g.h = at<__nv_bfloat16>(ws, L.h);
     g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
     g.epilogue = kEpiScatter;
@@ -579,13 +769,14 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.offsets = offsets;
   pa.perm_src = at<int32_t>(ws, L.perm_src);
   pa.inv_row = at<int32_t>(ws, L.inv_row);
-  pa.x_perm = at<__nv_bfloat16>(ws, L.x_perm);
+  pa.x_perm = at<void>(ws, L.x_perm);
   pa.zero_rows = at<float>(ws, L.out_acc);
-  pa.x_bf16 = (S > 0 && !hbf16) ? at<__nv_bfloat16>(ws, L.x_bf16) : nullptr;
+  pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
+  pa.act_f16 = fp8;
   pa.err = err;
   // 3. the GEMM schedule (routed experts from offsets, then the shared
   //    experts) is built by the same kernel that finishes the prefix sums
-  const int32_t pair = gemm_pair(T * K, N);
+  const int32_t pair = gemm_pair_for(*p, T * K);
   pa.groups = at<GroupDesc>(ws, L.groups);
   pa.ts_gu = at<int32_t>(ws, L.ts_gu);
   pa.ts_dn = at<int32_t>(ws, L.ts_dn);
@@ -609,13 +800,20 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.T = T;
   g.routed_rows = T * K;
   g.x_routed = pa.x_perm;
-  g.x_shared = hbf16 ? hidden : pa.x_bf16;
+  g.x_shared = pa.x_act ? pa.x_act : hidden;
   g.wg = w->w_gate;
   g.wu = w->w_up;
   g.wd = w->w_down;
   g.sg = w->ws_gate;
   g.su = w->ws_up;
   g.sd = w->ws_down;
+  g.fp8 = fp8;
+  g.wg_scale = w->w_gate_scale;
+  g.wu_scale = w->w_up_scale;
+  g.wd_scale = w->w_down_scale;
+  g.sg_scale = w->ws_gate_scale;
+  g.su_scale = w->ws_up_scale;
+  g.sd_scale = w->ws_down_scale;
   g.h = at<__nv_bfloat16>(ws, L.h);
   g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
   g.epilogue = kEpiScatter;
@@ -678,6 +876,7 @@ moe_status_t moe_get_device_status(void* ws, void* stream) {
   }
   if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
   if (word & kErrBounds) return MOE_ERR_DEVICE_BOUNDS;
+  if (word & kErrRange) return MOE_ERR_RANGE;
   return MOE_OK;
 }
 

@@ -161,9 +161,39 @@ __device__ __forceinline__ uint4 cvt8_bf16(const float4 p, const float4 q) {
   return make_uint4(pack_bf16x2(p.x, p.y), pack_bf16x2(p.z, p.w), pack_bf16x2(q.x, q.y), pack_bf16x2(q.z, q.w));
 }
 
+__device__ __forceinline__ float4 bf16x4_to_f32(uint32_t lo, uint32_t hi) {
+  return make_float4(__uint_as_float(lo << 16), __uint_as_float(lo & 0xFFFF0000u), __uint_as_float(hi << 16),
+                     __uint_as_float(hi & 0xFFFF0000u));
+}
+
+// 8 values to fp16 (round to nearest even). `over` is set when a finite value
+// lies beyond fp16's range (|v| >= 65520 rounds to infinity).
+__device__ __forceinline__ uint4 cvt8_f16(const float4 p, const float4 q, bool& over) {
+  const float m = fmaxf(fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(p.z), fabsf(p.w))),
+                        fmaxf(fmaxf(fabsf(q.x), fabsf(q.y)), fmaxf(fabsf(q.z), fabsf(q.w))));
+  over |= (m >= 65520.f) && (m <= 3.402823466e38f);
+  return make_uint4(pack_f16x2(p.x, p.y), pack_f16x2(p.z, p.w), pack_f16x2(q.x, q.y), pack_f16x2(q.z, q.w));
+}
+
+// One 16-byte output vector (8 elements) of hidden row t, vector v, in the
+// activation format.
+__device__ __forceinline__ uint4 act_vec(const PermuteArgs& a, int64_t t, int v, bool& over) {
+  if (a.hidden_bf16) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * a.d) + v);
+    if (!a.act_f16) return x;
+    return cvt8_f16(bf16x4_to_f32(x.x, x.y), bf16x4_to_f32(x.z, x.w), over);
+  }
+  const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * a.d);
+  const float4 p = __ldg(sp + 2 * v), q = __ldg(sp + 2 * v + 1);
+  return a.act_f16 ? cvt8_f16(p, q, over) : cvt8_bf16(p, q);
+}
+
 // Row gather into expert order, one warp per permuted row, 16-byte vectors;
 // grid-stride over rows so every SM streams. The fused layer also clears the
-// fp32 accumulator and writes a bf16 copy of an fp32 hidden (shared experts).
+// fp32 accumulator and writes a copy of hidden in the activation format
+// (shared experts) when hidden is not already in it. Activations are bf16 for
+// bf16 experts and fp16 for FP8 experts; a value beyond fp16's range is
+// reported through the error word.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, int64_t rows) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -172,6 +202,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
   // Only rows [0, offsets[N]) are placed; fewer than T*K when an input index
   // was out of range (reported through the error word).
   const int64_t placed = min(rows, (int64_t)__ldg(a.offsets + a.N));
+  bool over = false;
   for (int64_t r = warp0; r < placed; r += nwarps) {
     int64_t t;
     if (a.row_token) {
@@ -182,16 +213,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
       if (src < 0 || src >= rows) continue;
       t = src / a.K;
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.x_perm + r * d);
-    if (a.hidden_bf16) {
-      const uint4* sp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * d);
+    uint4* dst = reinterpret_cast<uint4*>(a.x_perm) + r * nvec;
 #pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(sp + v);
-    } else {
-      const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * d);
-#pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) dst[v] = cvt8_bf16(__ldg(sp + 2 * v), __ldg(sp + 2 * v + 1));
-    }
+    for (int v = lane; v < nvec; v += 32) dst[v] = act_vec(a, t, v, over);
   }
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
@@ -200,11 +224,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
     float4* z = reinterpret_cast<float4*>(a.zero_rows);
     for (int64_t i = tid; i < a.T * d / 4; i += nthr) z[i] = zero;
   }
-  if (a.x_bf16) {
-    const float4* sp = reinterpret_cast<const float4*>(a.hidden);
-    uint4* dp = reinterpret_cast<uint4*>(a.x_bf16);
-    for (int64_t i = tid; i < a.T * nvec; i += nthr) dp[i] = cvt8_bf16(__ldg(sp + 2 * i), __ldg(sp + 2 * i + 1));
+  if (a.x_act) {
+    uint4* dp = reinterpret_cast<uint4*>(a.x_act);
+    for (int64_t i = tid; i < a.T * nvec; i += nthr) dp[i] = act_vec(a, i / nvec, (int)(i % nvec), over);
   }
+  if (over && a.err) atomicOr(a.err, kErrRange);
 }
 
 // The GEMM groups (routed experts from offsets, then shared experts over all

@@ -85,7 +85,8 @@ extern "C" moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t
   a.offsets = offsets;
   a.perm_src = perm_src;
   a.inv_row = inv_row;
-  a.x_perm = static_cast<__nv_bfloat16*>(x_perm);
+  a.x_perm = x_perm;
+  a.act_f16 = p->expert_dtype == MOE_EXPERT_FP8_E4M3;
   a.err = static_cast<uint32_t*>(base);
   return moe::launch_permute(a, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -559,14 +559,12 @@ int moe_oracle_expert_choice(int64_t T, int32_t d, int32_t N, int32_t score_fn, 
  * routing, where the number of experts per token varies (0..N).
  *   idx int32 [n][M], w fp64 [n][M]; other arguments as moe_oracle_layer.
  */
-int moe_oracle_layer_routed(int64_t n_rows, int32_t d, int32_t N, int32_t M, int32_t F, int32_t S,
-                            int32_t Fs, const float* hidden, const int32_t* idx, const double* w,
-                            const uint16_t* const* w_gate, const uint16_t* const* w_up,
-                            const uint16_t* const* w_down, const uint16_t* const* ws_gate,
-                            const uint16_t* const* ws_up, const uint16_t* const* ws_down, double* out) {
+static int layer_routed_impl(int64_t n_rows, int32_t d, int32_t N, int32_t M, int32_t F, int32_t S,
+                             int32_t Fs, const float* hidden, const int32_t* idx, const double* w,
+                             const wset_t* routed, const wset_t* shared, double* out) {
   if (n_rows < 0 || d <= 0 || N <= 0 || M <= 0 || F <= 0 || S < 0 || (S > 0 && Fs <= 0)) return ORACLE_ERR_ARG;
-  if (!hidden || !idx || !w || !w_gate || !w_up || !w_down || !out) return ORACLE_ERR_ARG;
-  if (S > 0 && (!ws_gate || !ws_up || !ws_down)) return ORACLE_ERR_ARG;
+  if (!hidden || !idx || !w || !routed->gate || !routed->up || !routed->down || !out) return ORACLE_ERR_ARG;
+  if (S > 0 && (!shared->gate || !shared->up || !shared->down)) return ORACLE_ERR_ARG;
   const int32_t Fmax = (S > 0 && Fs > F) ? Fs : F;
   int status = ORACLE_OK;
 #pragma omp parallel
@@ -590,22 +588,28 @@ int moe_oracle_layer_routed(int64_t n_rows, int32_t d, int32_t N, int32_t M, int
           wk[k] = 0.0;
           for (int32_t i = 0; i < d; ++i) y[(int64_t)k * d + i] = 0.0;
           if (e < 0) continue;
-          if (e >= N || !w_gate[e] || !w_up[e] || !w_down[e]) {
+          wmat_t wg, wu, wd;
+          if (e >= N || !wset_expert(routed, e, &wg, &wu, &wd)) {
             bad = 1;
             break;
           }
-          moe_oracle_expert_ffn(d, F, x, w_gate[e], w_up[e], w_down[e], h, y + (int64_t)k * d);
+          expert_ffn_w(d, F, x, wg, wu, wd, h, y + (int64_t)k * d);
           wk[k] = w[t * M + k];
+        }
+        for (int32_t i = 0; i < d; ++i) sh[i] = 0.0;
+        for (int32_t s = 0; s < S && !bad; ++s) {
+          wmat_t wg, wu, wd;
+          if (!wset_expert(shared, s, &wg, &wu, &wd)) {
+            bad = 1;
+            break;
+          }
+          expert_ffn_w(d, Fs, x, wg, wu, wd, h, ys);
+          for (int32_t i = 0; i < d; ++i) sh[i] += ys[i];
         }
         if (bad) {
 #pragma omp atomic write
           status = ORACLE_ERR_MISSING_EXPERT;
           continue;
-        }
-        for (int32_t i = 0; i < d; ++i) sh[i] = 0.0;
-        for (int32_t s = 0; s < S; ++s) {
-          moe_oracle_expert_ffn(d, Fs, x, ws_gate[s], ws_up[s], ws_down[s], h, ys);
-          for (int32_t i = 0; i < d; ++i) sh[i] += ys[i];
         }
         moe_oracle_combine(M, d, wk, y, S > 0 ? sh : NULL, out + t * d);
       }
@@ -613,6 +617,37 @@ int moe_oracle_layer_routed(int64_t n_rows, int32_t d, int32_t N, int32_t M, int
     free(x); free(h); free(y); free(wk); free(sh); free(ys);
   }
   return status;
+}
+
+int moe_oracle_layer_routed(int64_t n_rows, int32_t d, int32_t N, int32_t M, int32_t F, int32_t S,
+                            int32_t Fs, const float* hidden, const int32_t* idx, const double* w,
+                            const uint16_t* const* w_gate, const uint16_t* const* w_up,
+                            const uint16_t* const* w_down, const uint16_t* const* ws_gate,
+                            const uint16_t* const* ws_up, const uint16_t* const* ws_down, double* out) {
+  const wset_t routed = {0, (const void* const*)w_gate, (const void* const*)w_up,
+                         (const void* const*)w_down, NULL, NULL, NULL};
+  const wset_t shared = {0, (const void* const*)ws_gate, (const void* const*)ws_up,
+                         (const void* const*)ws_down, NULL, NULL, NULL};
+  return layer_routed_impl(n_rows, d, N, M, F, S, Fs, hidden, idx, w, &routed, &shared, out);
+}
+
+/* moe_oracle_layer_routed with FP8 E4M3 experts: codes and per-row scales as
+ * moe_oracle_layer_fp8. */
+int moe_oracle_layer_routed_fp8(int64_t n_rows, int32_t d, int32_t N, int32_t M, int32_t F, int32_t S,
+                                int32_t Fs, const float* hidden, const int32_t* idx, const double* w,
+                                const uint8_t* const* q_gate, const uint8_t* const* q_up,
+                                const uint8_t* const* q_down, const float* const* s_gate,
+                                const float* const* s_up, const float* const* s_down,
+                                const uint8_t* const* qs_gate, const uint8_t* const* qs_up,
+                                const uint8_t* const* qs_down, const float* const* ss_gate,
+                                const float* const* ss_up, const float* const* ss_down, double* out) {
+  if (!s_gate || !s_up || !s_down) return ORACLE_ERR_ARG;
+  if (S > 0 && (!ss_gate || !ss_up || !ss_down)) return ORACLE_ERR_ARG;
+  const wset_t routed = {1, (const void* const*)q_gate, (const void* const*)q_up,
+                         (const void* const*)q_down, s_gate, s_up, s_down};
+  const wset_t shared = {1, (const void* const*)qs_gate, (const void* const*)qs_up,
+                         (const void* const*)qs_down, ss_gate, ss_up, ss_down};
+  return layer_routed_impl(n_rows, d, N, M, F, S, Fs, hidden, idx, w, &routed, &shared, out);
 }
 
 /*

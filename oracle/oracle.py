@@ -63,6 +63,8 @@ def _load():
         lib.moe_oracle_expert_ffn_fp8.restype = None
         lib.moe_oracle_layer_fp8.argtypes = [i64] + [i32] * 10 + [P] * 21
         lib.moe_oracle_layer_fp8.restype = ctypes.c_int
+        lib.moe_oracle_layer_routed_fp8.argtypes = [i64] + [i32] * 6 + [P] * 16
+        lib.moe_oracle_layer_routed_fp8.restype = ctypes.c_int
         lib.moe_oracle_silu.argtypes = [ctypes.c_double]
         lib.moe_oracle_silu.restype = ctypes.c_double
         lib.moe_oracle_num_threads.argtypes = []
@@ -407,4 +409,36 @@ def layer_routed(hidden, idx, w, w_gate, w_up, w_down, ws_gate=None, ws_up=None,
     del k1, k2, k3, k4, k5, k6
     if rc != 0:
         raise ValueError(f"moe_oracle_layer_routed failed ({rc})")
+    return out
+
+
+def layer_routed_fp8(hidden, idx, w, q_gate, s_gate, q_up, s_up, q_down, s_down, qs_gate=None, ss_gate=None,
+                     qs_up=None, ss_up=None, qs_down=None, ss_down=None):
+    """layer_routed with FP8 E4M3 experts (codes + per-row scales, as layer_fp8)."""
+    lib = _load()
+    x = _f32(hidden)
+    n, d = x.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = _f64(w)
+    M = idx.shape[1]
+    N = len(q_gate)
+    F = next(_u8(m).shape[0] for m in q_gate if m is not None)
+    S = 0 if qs_gate is None else len(qs_gate)
+    Fs = _u8(qs_gate[0]).shape[0] if S else 0
+    arrays, keepalive = [], []
+    for mats, cnt, conv in ((q_gate, N, _u8), (q_up, N, _u8), (q_down, N, _u8), (s_gate, N, _f32),
+                            (s_up, N, _f32), (s_down, N, _f32), (qs_gate, S, _u8), (qs_up, S, _u8),
+                            (qs_down, S, _u8), (ss_gate, S, _f32), (ss_up, S, _f32),
+                            (ss_down, S, _f32)):
+        if cnt == 0:
+            arrays.append(None)
+            continue
+        arr, k = _raw_ptr_array(mats, cnt, conv)
+        keepalive.append((arr, k))
+        arrays.append(ctypes.cast(arr, ctypes.c_void_p))
+    out = np.empty((n, d), np.float64)
+    rc = lib.moe_oracle_layer_routed_fp8(n, d, N, M, F, S, Fs, _ptr(x), _ptr(idx), _ptr(w), *arrays, _ptr(out))
+    del keepalive
+    if rc != 0:
+        raise ValueError(f"moe_oracle_layer_routed_fp8 failed ({rc})")
     return out

@@ -51,13 +51,42 @@ def capacity_keep(cfg, topk_idx):
     return (inv >= 0).reshape(-1, cfg.K).astype(np.uint8)
 
 
+def u8(t) -> np.ndarray:
+    return t.detach().cpu().contiguous().numpy()
+
+
+def _oracle_layer_rows_fp8(cfg, ins, rows, used, keep):
+    q = {k: [None] * cfg.N for k in ("w_gate", "w_up", "w_down")}
+    sc = {k: [None] * cfg.N for k in ("w_gate_scale", "w_up_scale", "w_down_scale")}
+    for e in used:
+        for k in q:
+            q[k][e] = u8(ins[k][e])
+        for k in sc:
+            sc[k][e] = np32(ins[k][e])
+    sh = {}
+    if cfg.S > 0:
+        sh = dict(qs_gate=[u8(ins["ws_gate"][s]) for s in range(cfg.S)],
+                  qs_up=[u8(ins["ws_up"][s]) for s in range(cfg.S)],
+                  qs_down=[u8(ins["ws_down"][s]) for s in range(cfg.S)],
+                  ss_gate=[np32(ins["ws_gate_scale"][s]) for s in range(cfg.S)],
+                  ss_up=[np32(ins["ws_up_scale"][s]) for s in range(cfg.S)],
+                  ss_down=[np32(ins["ws_down_scale"][s]) for s in range(cfg.S)])
+    return oracle.layer_fp8(hidden_f32(ins)[rows], np32(ins["w_router"]), q["w_gate"], sc["w_gate_scale"],
+                            q["w_up"], sc["w_up_scale"], q["w_down"], sc["w_down_scale"], K=cfg.K,
+                            score_fn=cfg.score_fn, renormalize=cfg.renormalize,
+                            router_bias=np32(ins.get("router_bias")), sel_bias=np32(ins.get("sel_bias")),
+                            n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, keep=keep, **sh)
+
+
 def oracle_layer_rows(cfg, ins, rows, keep=None):
     """Oracle layer output for the given token rows. Only the experts those
     tokens pick are copied to the host. keep: uint8 [len(rows)][K] capacity
-    mask, or None (dropless)."""
+    mask, or None (dropless). FP8 configs use the oracle's FP8 layer."""
     rows = np.asarray(rows, dtype=np.int64)
     r = oracle_router(cfg, ins, rows)
     used = sorted(set(r["idx"].reshape(-1).tolist()))
+    if cfg.expert_dtype == "fp8":
+        return _oracle_layer_rows_fp8(cfg, ins, rows, used, keep)
     wg = [None] * cfg.N
     wu = [None] * cfg.N
     wd = [None] * cfg.N

@@ -30,7 +30,7 @@ def test_library_exports_every_header_symbol():
 
 def test_status_strings():
     for s, key in ((0, "MOE_OK"), (-1, "INVALID_ARG"), (-2, "UNSUPPORTED"), (-3, "WORKSPACE"),
-                   (-4, "CUDA"), (-5, "TIMEOUT"), (-6, "DEVICE_BOUNDS"), (7, "UNKNOWN")):
+                   (-4, "CUDA"), (-5, "TIMEOUT"), (-6, "DEVICE_BOUNDS"), (-7, "RANGE"), (7, "UNKNOWN")):
         assert key in B.status_string(s)
 
 
@@ -107,3 +107,30 @@ def test_problem_check_capacity_factor():
     assert B.problem_check(B.problem(inputs.TINY, capacity_factor=0.6)) == 0
     assert B.problem_check(B.problem(inputs.TINY, capacity_factor=-1.0)) == -1
     assert B.problem_check(B.problem(inputs.TINY, capacity_factor=float("nan"))) == -1
+
+
+def test_problem_check_fp8_experts():
+    fp8 = inputs.TINY.with_(expert_dtype="fp8")
+    assert B.problem_check(B.problem(fp8)) == 0
+    assert B.problem_check(B.problem(fp8, expert_dtype=2)) == -1
+    assert B.problem_check(B.problem(fp8, d_model=136)) == -1   # FP8 code rows: 16-byte multiples
+    assert B.problem_check(B.problem(fp8, ffn=264)) == -1
+    assert B.problem_check(B.problem(fp8, n_shared=1, shared_ffn=72)) == -1
+    assert B.problem_check(B.problem(fp8, n_shared=1, shared_ffn=80)) == 0
+    assert B.problem_check(B.problem(inputs.TINY, d_model=136)) == 0  # bf16 experts: multiples of 8
+
+
+def test_fp8_workspace_holds_an_fp16_copy_for_shared_experts():
+    base = inputs.TINY.with_(hidden_dtype="bf16", S=1, Fs=64)
+    n16 = B.workspace_bytes(B.problem(base), B.CALL_LAYER_FORWARD)
+    n8 = B.workspace_bytes(B.problem(base.with_(expert_dtype="fp8")), B.CALL_LAYER_FORWARD)
+    assert n8 >= n16 + base.T * base.d * 2
+
+
+def test_grouped_swiglu_entry_points_check_the_expert_format():
+    """Host-side checks only: each grouped-SwiGLU entry point refuses the other
+    format before touching the device."""
+    p8 = B.problem(inputs.TINY.with_(expert_dtype="fp8"))
+    assert B.lib.moe_grouped_swiglu(p8, *([None] * 8), 0, None) == -1
+    p16 = B.problem(inputs.TINY)
+    assert B.lib.moe_grouped_swiglu_fp8(p16, *([None] * 11), 0, None) == -1

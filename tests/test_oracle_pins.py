@@ -701,3 +701,22 @@ def test_fp8_input_codes_decode_to_the_drawn_weights():
     assert np.allclose(np.abs(vals).max(axis=1), 448.0 * s, rtol=0, atol=0)
     std = vals.std()
     assert abs(std - 1.0 / math.sqrt(cfg.d)) < 0.1 / math.sqrt(cfg.d)
+
+
+def test_layer_routed_fp8_equals_bf16_on_exact_weights():
+    rng = np.random.default_rng(14)
+    T, d, N, M, F, Fs = 7, 32, 3, 3, 16, 16
+    hidden = rng.standard_normal((T, d)).astype(np.float32)
+    idx = rng.integers(-1, N, size=(T, M)).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, size=(T, M))
+    routed = [_fp8_case(rng, F, d, True) for _ in range(N)]
+    shared = [_fp8_case(rng, Fs, d, True)]
+    q = lambda cases, j: [c[0][j] for c in cases]  # noqa: E731
+    b = lambda cases, j: [_bf16_bits(c[1][j]) for c in cases]  # noqa: E731
+    got = oracle.layer_routed_fp8(hidden, idx, w, q(routed, 0), q(routed, 1), q(routed, 2), q(routed, 3),
+                                  q(routed, 4), q(routed, 5), qs_gate=q(shared, 0), ss_gate=q(shared, 1),
+                                  qs_up=q(shared, 2), ss_up=q(shared, 3), qs_down=q(shared, 4),
+                                  ss_down=q(shared, 5))
+    ref = oracle.layer_routed(hidden, idx, w, b(routed, 0), b(routed, 1), b(routed, 2), ws_gate=b(shared, 0),
+                              ws_up=b(shared, 1), ws_down=b(shared, 2))
+    assert np.array_equal(got, ref)
