@@ -41,9 +41,12 @@ WORKLOADS = {
     "dsv3_grouped": (inputs.DSV3_GROUPED, "DeepSeek-V3-shaped prefill layer, node-limited routing (4 of 8 groups)"),
     "gptoss": (inputs.GPTOSS, "gpt-oss-120b-shaped layer"),
     "tiny": (inputs.TINY, "tiny Mixtral-style layer"),
+    "mixtral_fp8": (inputs.MIXTRAL_FP8, "Mixtral-8x7B-shaped prefill layer, FP8 E4M3 experts"),
 }
 for _T in inputs.DECODE_BATCHES:
     WORKLOADS[f"decode{_T}"] = (inputs.QWEN_DECODE.with_(T=_T), f"Qwen3-235B-like decode layer, T={_T}")
+    WORKLOADS[f"decode{_T}_fp8"] = (inputs.QWEN_DECODE_FP8.with_(T=_T),
+                                    f"Qwen3-235B-like decode layer, FP8 E4M3 experts, T={_T}")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -75,19 +78,22 @@ def load_peaks():
 
 def work_model(cfg, counts=None):
     """Algorithmic FLOPs and bytes of one layer forward (tile padding excluded).
-    Bytes: the weights of touched experts, the router, and hidden in + out."""
+    Bytes: the weights of touched experts (bf16: 2 bytes per weight; FP8: 1
+    byte plus a 4-byte scale per matrix row), the router, and hidden in + out."""
     T, d, N, K, F, S, Fs = cfg.T, cfg.d, cfg.N, cfg.K, cfg.F, cfg.S, cfg.Fs
     hid_b = 4 if cfg.hidden_dtype == "f32" else 2
+    wb, sb = (1, 4) if cfg.expert_dtype == "fp8" else (2, 0)
     flops_router = 2 * T * d * N
     flops_gu = 4 * d * F * T * K + 4 * d * Fs * T * S
     flops_dn = 2 * d * F * T * K + 2 * d * Fs * T * S
     touched = N if counts is None else int((np.asarray(counts) > 0).sum())
-    w_expert = 3 * d * F * 2
-    bytes_w = touched * w_expert + S * 3 * d * Fs * 2 + 4 * d * N
+    gu_e, gu_s = 2 * d * F * wb + 2 * F * sb, 2 * d * Fs * wb + 2 * Fs * sb
+    dn_e, dn_s = d * F * wb + d * sb, d * Fs * wb + d * sb
+    bytes_w = touched * (gu_e + dn_e) + S * (gu_s + dn_s) + 4 * d * N
     bytes_act = T * d * (hid_b + 2)
     return dict(flops=flops_router + flops_gu + flops_dn, flops_gateup=flops_gu, flops_down=flops_dn,
-                bytes=bytes_w + bytes_act, bytes_gateup=touched * 2 * d * F * 2 + S * 2 * d * Fs * 2,
-                bytes_down=touched * d * F * 2 + S * d * Fs * 2, touched=touched)
+                bytes=bytes_w + bytes_act, bytes_gateup=touched * gu_e + S * gu_s,
+                bytes_down=touched * dn_e + S * dn_s, touched=touched)
 
 
 class ClockSampler:
@@ -209,13 +215,23 @@ def oracle_rows_timed(cfg, ins, rows):
                       router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
                       sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy())
     used = sorted(set(r["idx"].reshape(-1).tolist()))
-    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    wg, wu, wd = [None] * cfg.N, [None] * cfg.N, [None] * cfg.N
+    fp8 = cfg.expert_dtype == "fp8"
+    if fp8:  # E4M3 codes and fp32 row scales
+        bits = lambda t: t.detach().cpu().contiguous().numpy()  # noqa: E731
+    else:
+        bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    names = ("w_gate", "w_up", "w_down") + (("w_gate_scale", "w_up_scale", "w_down_scale") if fp8 else ())
+    wts = {k: [None] * cfg.N for k in names}
     for e in used:
-        wg[e], wu[e], wd[e] = bits(ins["w_gate"][e]), bits(ins["w_up"][e]), bits(ins["w_down"][e])
+        for k in names:
+            wts[k][e] = bits(ins[k][e])
     sh = {}
     if cfg.S:
-        sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in ("ws_gate", "ws_up", "ws_down")}
+        sn = ("ws_gate", "ws_up", "ws_down") + (("ws_gate_scale", "ws_up_scale", "ws_down_scale") if fp8 else ())
+        sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in sn}
+        if fp8:
+            sh = {"qs_gate": sh["ws_gate"], "qs_up": sh["ws_up"], "qs_down": sh["ws_down"],
+                  "ss_gate": sh["ws_gate_scale"], "ss_up": sh["ws_up_scale"], "ss_down": sh["ws_down_scale"]}
     keep = None
     if cfg.capacity_factor > 0:  # which copies survive depends on the whole batch's routing
         full = oracle.router(ins["hidden"].float().cpu().numpy(), ins["w_router"].cpu().numpy(), K=cfg.K,
@@ -225,12 +241,16 @@ def oracle_rows_timed(cfg, ins, rows):
                              sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy())
         inv = oracle.permute(full["idx"], cfg.N, capacity_factor=cfg.capacity_factor)["inv_row"]
         keep = (inv >= 0).reshape(-1, cfg.K).astype(np.uint8)[rows]
+    kw = dict(K=cfg.K, score_fn=cfg.score_fn, renormalize=cfg.renormalize, n_groups=cfg.n_groups,
+              topk_groups=cfg.topk_groups,
+              router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
+              sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), keep=keep, **sh)
     t0 = time.perf_counter()
-    oracle.layer(x, ins["w_router"].cpu().numpy(), wg, wu, wd, K=cfg.K, score_fn=cfg.score_fn,
-                 renormalize=cfg.renormalize, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
-                 router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
-                 sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), keep=keep,
-                 **sh)
+    if fp8:
+        oracle.layer_fp8(x, ins["w_router"].cpu().numpy(), wts["w_gate"], wts["w_gate_scale"], wts["w_up"],
+                         wts["w_up_scale"], wts["w_down"], wts["w_down_scale"], **kw)
+    else:
+        oracle.layer(x, ins["w_router"].cpu().numpy(), wts["w_gate"], wts["w_up"], wts["w_down"], **kw)
     return len(rows), time.perf_counter() - t0, oracle.num_threads()
 
 
@@ -301,10 +321,12 @@ def config_block(cfg, desc, args):
             "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "capacity_factor": cfg.capacity_factor,
             "routing": cfg.routing,
             "ffn": cfg.F, "n_shared": cfg.S, "shared_ffn": cfg.Fs, "score": cfg.score,
-            "hidden_dtype": cfg.hidden_dtype, "global_batch": cfg.T * args.gpus,
+            "hidden_dtype": cfg.hidden_dtype, "expert_dtype": cfg.expert_dtype,
+            "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",
             "l2": "inputs larger than L2 (expert weights stream from HBM every step)"
-            if 3 * cfg.d * cfg.F * 2 * cfg.N > 126e6 else "L2 not flushed (working set fits in L2)"}
+            if 3 * cfg.d * cfg.F * (1 if cfg.expert_dtype == "fp8" else 2) * cfg.N > 126e6
+            else "L2 not flushed (working set fits in L2)"}
 
 
 def run_ours(args, cfg, desc, world, rank):
@@ -383,7 +405,7 @@ def run_ours(args, cfg, desc, world, rank):
 
     ms_step = 1e3 * elapsed_s / args.steps
     wm = work_model(cfg, counts_h)
-    decode = cfg.T <= 512 and cfg.name == "qwen_decode"
+    decode = cfg.T <= 512 and cfg.name.startswith("qwen_decode")
     gu, dn = B.LAYER_STAGES.index("gateup_swiglu_gemm"), B.LAYER_STAGES.index("down_scatter_gemm")
     dom = gu if stage_ms[gu] >= stage_ms[dn] else dn
     dom_name = B.LAYER_STAGES[dom]
@@ -415,7 +437,8 @@ def run_ours(args, cfg, desc, world, rank):
                  "traffic": traffic_from_profiles(dom_name, args.workload)})
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+            "vs_baseline": None, "dtype": "f16" if cfg.expert_dtype == "fp8" else "bf16",
+            "data": "synthetic (seeded; random-init weights)",
             "config": config_block(cfg, desc, args), "roofline": roof,
             "layer_roofline": {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],
                                "t_roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step},

@@ -80,14 +80,16 @@ typedef enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe
  *   MOE_EXPERT_BF16      bf16 matrices
  *   MOE_EXPERT_FP8_E4M3  FP8 E4M3 codes with one fp32 scale per matrix row:
  *                        weight = e4m3(code) * scale[row]. NaN codes
- *                        (0x7F, 0xFF) are not supported. The activations the
- *                        expert GEMMs read (x_perm, h_perm) are then fp16
- *                        instead of bf16: the tensor cores take both
- *                        operands in one type, and fp16 holds every E4M3
- *                        value exactly; the conversion to fp16 is exact for
- *                        bf16 activations of magnitude 2^-14 .. 65504,
- *                        within 2^-25 below that, and an overflow beyond it
- *                        is reported as MOE_ERR_RANGE.
+ *                        (0x7F, 0xFF) are not supported. The activations
+ *                        between the calls (x_perm, h_perm) are then fp16
+ *                        rows instead of bf16 (exact for bf16 values of
+ *                        magnitude 2^-14 .. 65504, within 2^-25 below that;
+ *                        an overflow beyond it is reported as MOE_ERR_RANGE).
+ *                        Inside the expert GEMMs the tensor cores multiply
+ *                        the E4M3 codes by a two-term E4M3 expansion of each
+ *                        activation row, x ~= s_row * (hi + lo), whose
+ *                        relative error is at most 2^-8 (that of a bf16
+ *                        activation), with fp32 accumulation.
  */
 typedef enum { MOE_EXPERT_BF16 = 0, MOE_EXPERT_FP8_E4M3 = 1 } moe_expert_dtype_t;
 

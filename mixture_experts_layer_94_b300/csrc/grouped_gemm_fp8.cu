@@ -10,36 +10,30 @@
 // and those bytes are what bound decode.
 //
 // Data path:
-//  * The weights are the MMA's A operand (M = 128 weight rows) and the token
-//    rows are its B operand (N = 16, 32, 64 or 128). One tile is two 128-row
-//    weight sub-tiles against up to 128 token rows of one expert group. The
-//    sub-tiles are the gate and up rows of the same 128 FFN units, or 256
-//    rows of W_down. With a few tokens per expert (decode) the tensor work
-//    per weight byte then scales with the token count rather than with a
-//    fixed 128-row tile, so the kernel stays bound by the weight stream.
-//  * TMA brings one fp16 activation box (128-byte swizzle; 16, 32, 64 or 128
-//    rows, the smallest that holds the tile's rows) and the raw code boxes
-//    (no swizzle, 64 codes per row) into a 4-stage ring.
-//  * Four converter warps write the codes as fp16 into a 2-stage ring, in the
-//    128-byte-swizzled K-major layout the MMA reads. An E4M3 code s.eeee.mmm
-//    placed as the fp16 bit pattern s.0eeee.mmm0000000 is exactly 2^-8 times
-//    its value. Normal codes map to normal fp16 numbers with the exponent
-//    re-biased by 8, and subnormal codes map to fp16 subnormals with the same
-//    shift. So the conversion is a byte permute, a shift and two masks per
-//    pair of codes, and it never rounds. NaN codes are not supported.
-//  * kind::f16 MMA: fp16 x fp16 -> fp32 accumulators in TMEM. Both operands
-//    have one type.
-//  * Epilogue: accumulator x (2^8 x the weight row's scale). Gate/up applies
-//    SiLU(g) * u and writes h as fp16. Down either scatter-adds w * y into
-//    the token's fp32 output row or stores y as bf16.
-//  The activations are fp16 on this path. A bf16 value is exact in fp16 when
-//  2^-14 <= |x| < 65520. Smaller magnitudes keep an absolute error below
-//  2^-25. Larger ones overflow and set kErrRange in the error word.
+//  * The tensor cores multiply E4M3 by E4M3 (tcgen05.mma kind::f8f6f4, fp32
+//    accumulators in TMEM) and read the expert codes exactly as TMA brings
+//    them from HBM: no conversion pass, and shared memory carries each code
+//    byte twice (TMA write, MMA read). Converting the codes to fp16 in shared
+//    memory instead costs three times that, which on this GPU is about the
+//    whole shared-memory bandwidth at the HBM rate.
+//  * The activations arrive as the two-term E4M3 expansion of act_quant.cu
+//    (x ~= s * (hi + lo), bf16-level precision) with the two terms in
+//    interleaved rows: a tile of up to 64 tokens is one 128-row MMA operand,
+//    token t's hi in row 2t and lo in row 2t+1. TMEM lanes 2t and 2t+1 then
+//    hold hi*W and lo*W, which the epilogue adds with one shuffle.
+//  * Tokens are the MMA's M, weights its N (256: the gate and up rows of 128
+//    FFN units, or 256 rows of W_down); an MMA takes time in proportion to
+//    M x K, so the weights go in N. K advances 128 codes (one 128-byte line
+//    per row) per pipeline stage, four MMAs of K = 32.
+//  * Epilogue: (hi + lo) x the token row's scale x the weight row's scale.
+//    Gate/up applies SiLU(g) * u and writes h as fp16 (quantised the same way
+//    for the down GEMM). Down either scatter-adds w * y into the token's fp32
+//    output row or stores y as bf16.
 //
-// Warps (320 threads, one CTA per SM, persistent over the tiles):
-//   0     TMA producer           1    TMEM allocation, MMA issue
-//   2-5   epilogue (warp w reads TMEM lanes 32*(w%4)..+31: one weight row per thread)
-//   6-9   FP8 -> fp16 converters
+// Warps (192 threads, one CTA per SM, persistent over the tiles):
+//   0     TMA producer (token-row box + weight-code boxes per stage)
+//   1     TMEM allocation, MMA issue
+//   2-5   epilogue (warp w reads TMEM lanes 32*(w%4)..+31)
 // Every mbarrier wait is bounded. On a stall the kernel records a timeout in
 // the error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -54,45 +48,34 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kConvThread0 = 192;  // first converter thread (warp 6)
-constexpr int kStages = 4;         // TMA ring: activation box + code boxes
-constexpr int kWStages = 2;        // converted fp16 weight ring
-constexpr int kWRows = 128;        // weight rows per MMA (M)
-constexpr uint32_t kXBytes = 128u * kBK * 2u;          // largest activation box: 128 rows x 128 B
-constexpr uint32_t kRawBytes = 2u * kWRows * kBK;      // two sub-tiles x 128 rows x 64 codes = 16 KB
-constexpr uint32_t kWBytes = 2u * kWRows * kBK * 2u;   // the same rows in fp16 = 32 KB
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr int kKq = 128;            // codes of K per stage (one 128-byte line per row)
+constexpr int kARows = 2 * kF8TileRows;  // two operand rows (hi, lo) per token
+constexpr int kWRows = 256;         // weight rows per tile (MMA N)
+constexpr uint32_t kABytes = (uint32_t)kARows * kKq;   // 16 KB
+constexpr uint32_t kBBytes = (uint32_t)kWRows * kKq;   // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 256;  // one accumulator: two sub-tiles x up to 128 token columns
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kIdesc = ptx::idesc_f8_f32(kARows, kWRows);
 constexpr uint64_t kDrainTimeoutNs = 50000000ull;
-constexpr int kNumBars = 2 * kStages + 2 * kWStages + 5;
-constexpr size_t kSmem =
-    1024 /*alignment slack*/ + (size_t)kStages * (kXBytes + kRawBytes) + (size_t)kWStages * kWBytes + 256;
-static_assert(8 * kNumBars + 8 <= 256, "barrier area");
+constexpr size_t kSmem = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + 256;
+static_assert(kSmem <= 232448, "shared memory per CTA");
 
-// Two E4M3 codes held in bits 8..15 and 24..31 (zeros elsewhere) -> two fp16
-// values 2^-8 times theirs: keep the signs, move the 7 magnitude bits down one.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t x) {
-  return (x & 0x80008000u) | ((x >> 1) & 0x3F803F80u);
-}
+// Operand box for a tile of n tokens: 16 << box_sel(n) rows (>= 2n).
+__device__ __forceinline__ int box_sel(int n) { return n <= 8 ? 0 : (n <= 16 ? 1 : (n <= 32 ? 2 : 3)); }
 
-// 16 codes (in K order) -> 16 fp16 values as two 16-byte chunks.
-__device__ __forceinline__ void convert16(const uint4 v, uint4& lo, uint4& hi) {
-  lo.x = e4m3x2_to_f16x2_scaled(__byte_perm(v.x, 0u, 0x1404));
-  lo.y = e4m3x2_to_f16x2_scaled(__byte_perm(v.x, 0u, 0x3424));
-  lo.z = e4m3x2_to_f16x2_scaled(__byte_perm(v.y, 0u, 0x1404));
-  lo.w = e4m3x2_to_f16x2_scaled(__byte_perm(v.y, 0u, 0x3424));
-  hi.x = e4m3x2_to_f16x2_scaled(__byte_perm(v.z, 0u, 0x1404));
-  hi.y = e4m3x2_to_f16x2_scaled(__byte_perm(v.z, 0u, 0x3424));
-  hi.z = e4m3x2_to_f16x2_scaled(__byte_perm(v.w, 0u, 0x1404));
-  hi.w = e4m3x2_to_f16x2_scaled(__byte_perm(v.w, 0u, 0x3424));
-}
-
-// Activation box for a tile with n token rows: 16 << box_sel(n) rows.
-__device__ __forceinline__ int box_sel(int n) { return n <= 16 ? 0 : (n <= 32 ? 1 : (n <= 64 ? 2 : 3)); }
-
-__device__ __forceinline__ int tile_rows_valid(const TileInfo& ti) {
-  return min(kBM, ti.g.rows - ti.m_blk * kBM);
+// This lane's sums of 16 accumulator columns of a (hi, lo) lane pair: the
+// even lane returns columns 0..15 of `v`, the odd lane columns 16..31, each
+// plus its neighbour's same column.
+__device__ __forceinline__ void pair_sum16(const uint32_t (&v)[32], int odd, float (&out)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float mine = __uint_as_float(odd ? v[j + 16] : v[j]);
+    const float send = __uint_as_float(odd ? v[j] : v[j + 16]);
+    out[j] = mine + __shfl_xor_sync(0xffffffffu, send, 1);
+  }
 }
 
 template <int PHASE, int EPI>
@@ -102,22 +85,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_base);
-  const uint32_t sX = base;                                 // kStages x 16 KB
-  const uint32_t sRaw = sX + kStages * kXBytes;             // kStages x 16 KB
-  const uint32_t sW = sRaw + kStages * kRawBytes;           // kWStages x 32 KB
-  const uint32_t sBar = sW + kWStages * kWBytes;
-  const uint8_t* gRaw = gbase + kStages * kXBytes;
-  uint8_t* gW = gbase + kStages * (kXBytes + kRawBytes);
-  uint8_t* gBar = gW + kWStages * kWBytes;
+  const uint32_t sA = base;                           // kStages x 16 KB
+  const uint32_t sB = base + kStages * kABytes;       // kStages x 32 KB
+  const uint32_t sBar = base + kStages * kStageBytes;
+  uint8_t* gBar = gbase + kStages * kStageBytes;
   auto full_bar = [&](int s) { return sBar + 8u * s; };
   auto empty_bar = [&](int s) { return sBar + 8u * (kStages + s); };
-  auto wfull_bar = [&](int s) { return sBar + 8u * (2 * kStages + s); };
-  auto wempty_bar = [&](int s) { return sBar + 8u * (2 * kStages + kWStages + s); };
-  auto tfull_bar = [&](int i) { return sBar + 8u * (2 * kStages + 2 * kWStages + i); };
-  auto tempty_bar = [&](int i) { return sBar + 8u * (2 * kStages + 2 * kWStages + 2 + i); };
-  const uint32_t drain_bar = sBar + 8u * (2 * kStages + 2 * kWStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 8 * kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * kNumBars + 4);
+  auto tfull_bar = [&](int i) { return sBar + 8u * (2 * kStages + i); };
+  auto tempty_bar = [&](int i) { return sBar + 8u * (2 * kStages + 2 + i); };
+  const uint32_t drain_bar = sBar + 8u * (2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 8 * (2 * kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * (2 * kStages + 5) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = __ldg(a.tile_start + a.G);
@@ -126,10 +104,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
-    }
-    for (int s = 0; s < kWStages; ++s) {
-      ptx::mbar_init(wfull_bar(s), 4);  // one arrival per converter warp
-      ptx::mbar_init(wempty_bar(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(tfull_bar(i), 1);
@@ -142,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&maps.w[0]);
-    ptx::prefetch_tmap(&maps.x[0][kF8XBoxes - 1]);
     if (PHASE == kPhaseGateUp) ptx::prefetch_tmap(&maps.u[0]);
   }
   if (warp == 1) {
@@ -163,29 +136,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, a);
         const int kind = ti.g.kind;
-        const int bsel = box_sel(tile_rows_valid(ti));
-        const uint32_t bytes = ((16u << bsel) * kBK * 2u) + kRawBytes;
-        const CUtensorMap* mX = &maps.x[kind][bsel];
+        const int bsel = box_sel(min(kF8TileRows, ti.g.rows - ti.m_blk * kF8TileRows));
+        const uint32_t bytes = (16u << bsel) * kKq + kBBytes;
+        const CUtensorMap* mA = &maps.x[kind][bsel];
         const CUtensorMap* mW = &maps.w[kind];
         const CUtensorMap* mU = &maps.u[kind];
-        const int x_row = (PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kBM;
+        const int a_row = 2 * ((PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kF8TileRows);
         // gate/up: rows n*128 of the expert in W_gate and in W_up;
-        // down: rows n*256 and n*256 + 128 of the expert in W_down.
-        const int w_row = ti.g.index * a.w_rows[kind] + ti.n_blk * (PHASE == kPhaseGateUp ? kWRows : 2 * kWRows);
+        // down: rows n*256 .. n*256 + 255 of the expert in W_down.
+        const int w_row = ti.g.index * a.w_rows[kind] + ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
         const int nkb = a.k_blocks[kind];
         for (int kb = 0; kb < nkb; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) {
             aborted = true;
             break;
           }
-          const uint32_t dRaw = sRaw + stage * kRawBytes;
+          const uint32_t dA = sA + stage * kABytes, dB = sB + stage * kBBytes;
           ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-          ptx::tma_load_2d(sX + stage * kXBytes, mX, full_bar(stage), kb * kBK, x_row);
-          ptx::tma_load_2d(dRaw, mW, full_bar(stage), kb * kBK, w_row);
-          if (PHASE == kPhaseGateUp)
-            ptx::tma_load_2d(dRaw + kRawBytes / 2, mU, full_bar(stage), kb * kBK, w_row);
-          else
-            ptx::tma_load_2d(dRaw + kRawBytes / 2, mW, full_bar(stage), kb * kBK, w_row + kWRows);
+          ptx::tma_load_2d(dA, mA, full_bar(stage), kb * kKq, a_row);
+          ptx::tma_load_2d(dB, mW, full_bar(stage), kb * kKq, w_row);
+          if (PHASE == kPhaseGateUp) ptx::tma_load_2d(dB + kBBytes / 2, mU, full_bar(stage), kb * kKq, w_row);
+          else ptx::tma_load_2d(dB + kBBytes / 2, mW, full_bar(stage), kb * kKq, w_row + kWRows / 2);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -197,48 +168,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Wait for the copies still in flight into the ring (the last kStages issues).
         const uint32_t n = issued < (uint32_t)kStages ? issued : (uint32_t)kStages;
         for (uint32_t j = issued - n; j < issued; ++j)
-          wait_raw(full_bar(j % kStages), (j / kStages) & 1u, kDrainTimeoutNs);
+          wait_raw(full_bar((int)(j % kStages)), (j / kStages) & 1u, kDrainTimeoutNs);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, ws = 0, acc = 0;
-      uint32_t phase = 0, wphase = 0, acc_phase = 0;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool aborted = false;
       for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(tile, a);
-        const uint32_t idesc = ptx::idesc_f16_f32(kWRows, 16 << box_sel(tile_rows_valid(ti)));
-        const int nkb = a.k_blocks[ti.g.kind];
+        const int nkb = a.k_blocks[decode_tile(tile, a).g.kind];
         if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) break;
         ptx::tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)acc * kAccCols;
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, a.err) ||
-              !ptx::mbar_wait(wfull_bar(ws), wphase, abort_flag, a.err)) {
+          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, a.err)) {
             aborted = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t a0 = ptx::smem_desc_sw128(sW + ws * kWBytes);
-          const uint64_t a1 = ptx::smem_desc_sw128(sW + ws * kWBytes + kWBytes / 2);
-          const uint64_t b = ptx::smem_desc_sw128(sX + stage * kXBytes);
+          const uint64_t adesc = ptx::smem_desc_sw128(sA + stage * kABytes);
+          const uint64_t bdesc = ptx::smem_desc_sw128(sB + stage * kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            ptx::mma_f16(d0, a0 + 2u * k, b + 2u * k, idesc, accum);
-            ptx::mma_f16(d0 + kWRows, a1 + 2u * k, b + 2u * k, idesc, accum);
-          }
+          for (int k = 0; k < kKq / 32; ++k)
+            ptx::mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
           ptx::mma_commit(empty_bar(stage));
-          ptx::mma_commit(wempty_bar(ws));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
-          }
-          if (++ws == kWStages) {
-            ws = 0;
-            wphase ^= 1u;
           }
         }
         if (aborted) break;
@@ -253,127 +212,111 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_raw(drain_bar, 0, kWaitTimeoutNs);
     }
     __syncwarp();
-  } else if (threadIdx.x >= kConvThread0) {
-    // ------------------------------------------------------------ converters
-    // Thread ct handles 16-code quarters i = ct, ct + 128, ..., of the 256
-    // code rows: row r = i / 4 (64 codes), quarter q = i % 4 -> fp16 chunks
-    // 2q and 2q+1 of the 128-byte row, placed at chunk ^ (r % 8) (the
-    // 128-byte swizzle the MMA descriptor expects; the ring is 1024-aligned).
-    const int ct = threadIdx.x - kConvThread0;
-    int stage = 0, ws = 0;
-    uint32_t phase = 0, wphase = 0;
-    bool aborted = false;
-    for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-      const int nkb = a.k_blocks[decode_tile(tile, a).g.kind];
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, a.err) ||
-            !ptx::mbar_wait(wempty_bar(ws), wphase ^ 1u, abort_flag, a.err)) {
-          aborted = true;
-          break;
-        }
-        const uint8_t* src = gRaw + stage * kRawBytes;
-        uint8_t* dst = gW + ws * kWBytes;
-#pragma unroll
-        for (int it = 0; it < (int)(kRawBytes / 16) / 128; ++it) {
-          const int i = it * 128 + ct;
-          const int r = i >> 2, q = i & 3, sw = r & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + q * 16);
-          uint4 lo, hi;
-          convert16(v, lo, hi);
-          uint8_t* row = dst + r * (kBK * 2);
-          *reinterpret_cast<uint4*>(row + (((2 * q) ^ sw) << 4)) = lo;
-          *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ sw) << 4)) = hi;
-        }
-        ptx::fence_proxy_async_shared();  // generic-proxy writes -> the MMA's async-proxy reads
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(wfull_bar(ws));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++ws == kWStages) {
-          ws = 0;
-          wphase ^= 1u;
-        }
-      }
-    }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Lane pair (2t, 2t+1) of the warp holds token t's hi and lo products;
+    // after the pair sum the even lane finishes columns 0..15 of each 32-column
+    // chunk and the odd lane columns 16..31.
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int wr = quad * 32 + lane;  // weight row inside a 128-row sub-tile
+    const int odd = lane & 1;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool over = false;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, a);
       const int kind = ti.g.kind;
-      const int n_valid = tile_rows_valid(ti);
       if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
+      const int r_local = ti.m_blk * kF8TileRows + ((quad * 32 + lane) >> 1);  // token row in the group
+      const bool row_ok = r_local < ti.g.rows;
+      const int64_t a_idx = (int64_t)(PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + (row_ok ? r_local : 0);
+      const float sx = row_ok ? __ldg(a.a_scale[kind] + a_idx) : 0.f;
       const int64_t wbase = (int64_t)ti.g.index * a.w_rows[kind];
       if (PHASE == kPhaseGateUp) {
-        const int f = ti.n_blk * kWRows + wr;
-        const bool f_ok = f < a.n_ext[kind];
-        const float sg = f_ok ? __ldg(a.w_scale[kind] + wbase + f) * 256.f : 0.f;
-        const float su = f_ok ? __ldg(a.u_scale[kind] + wbase + f) * 256.f : 0.f;
-        const int64_t ldh = a.ldh[kind];
-        __half* hcol = reinterpret_cast<__half*>(a.h[kind]) + (int64_t)(ti.g.h_row0 + ti.m_blk * kBM) * ldh + f;
+        const int n_ext = a.n_ext[kind];
+        __half* hrow = reinterpret_cast<__half*>(a.h[kind]) + (int64_t)(ti.g.h_row0 + (row_ok ? r_local : 0)) * a.ldh[kind];
+        const float* sgp = a.w_scale[kind] + wbase;
+        const float* sup = a.u_scale[kind] + wbase;
 #pragma unroll 1
-        for (int c = 0; c < n_valid; c += 16) {
-          uint32_t gv[16], uv[16];
-          ptx::tmem_ld_32x32b_x16(tacc + c, gv);
-          ptx::tmem_ld_32x32b_x16(tacc + kWRows + c, uv);
+        for (int c = 0; c < kBNGateUp / 32; ++c) {
+          uint32_t gv[32], uv[32];
+          ptx::tmem_ld_32x32b_x32(tacc + c * 32, gv);
+          ptx::tmem_ld_32x32b_x32(tacc + kBNGateUp + c * 32, uv);
           ptx::tmem_wait_ld();
-          if (f_ok) {
+          float g[16], u[16];
+          pair_sum16(gv, odd, g);
+          pair_sum16(uv, odd, u);
+          const int f0 = ti.n_blk * kBNGateUp + c * 32 + odd * 16;
+          if (row_ok && f0 < n_ext) {
+            uint32_t p[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c + j < n_valid) {
-                const float g = __uint_as_float(gv[j]) * sg;
-                const float u = __uint_as_float(uv[j]) * su;
-                const float hv = silu_f(g) * u;
-                over |= fabsf(hv) >= 65520.f;
-                hcol[(int64_t)(c + j) * ldh] = __float2half_rn(hv);
+            for (int q = 0; q < 4; ++q) {
+              const float4 sg = __ldg(reinterpret_cast<const float4*>(sgp + f0 + 4 * q));
+              const float4 su = __ldg(reinterpret_cast<const float4*>(sup + f0 + 4 * q));
+              const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
+              float hv[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float gg = g[4 * q + j] * sx * sgv[j];
+                const float uu = u[4 * q + j] * sx * suv[j];
+                hv[j] = silu_f(gg) * uu;
+                over |= fabsf(hv[j]) >= 65520.f;
               }
+              p[2 * q] = pack_f16x2(hv[0], hv[1]);
+              p[2 * q + 1] = pack_f16x2(hv[2], hv[3]);
             }
+            *reinterpret_cast<uint4*>(hrow + f0) = make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4*>(hrow + f0 + 8) = make_uint4(p[4], p[5], p[6], p[7]);
           }
         }
       } else {
+        const float* sdp = a.w_scale[kind] + wbase;
+        int64_t t = 0;
+        float w = 1.f;
+        if (EPI == kEpiScatter && row_ok) {
+          if (kind == 0 && a.row_w) {  // expert choice: the row's token and score
+            t = __ldg(a.perm_src + ti.g.h_row0 + r_local);
+            w = __ldg(a.row_w + ti.g.h_row0 + r_local);
+          } else if (kind == 0) {
+            const int32_t src = __ldg(a.perm_src + ti.g.h_row0 + r_local);
+            t = src / a.top_k;
+            w = __ldg(a.topk_w + src);
+          } else {
+            t = r_local;
+          }
+        }
+        const float ws = w * sx;
 #pragma unroll 1
-        for (int sub = 0; sub < 2; ++sub) {
-          const int i = ti.n_blk * 2 * kWRows + sub * kWRows + wr;  // output feature
-          const bool i_ok = i < a.d;
-          const float sd = i_ok ? __ldg(a.w_scale[kind] + wbase + i) * 256.f : 0.f;
-#pragma unroll 1
-          for (int c = 0; c < n_valid; c += 16) {
-            uint32_t yv[16];
-            ptx::tmem_ld_32x32b_x16(tacc + sub * kWRows + c, yv);
-            ptx::tmem_wait_ld();
-            if (!i_ok) continue;
+        for (int c = 0; c < kBNDown / 32; ++c) {
+          uint32_t yv[32];
+          ptx::tmem_ld_32x32b_x32(tacc + c * 32, yv);
+          ptx::tmem_wait_ld();
+          float y[16];
+          pair_sum16(yv, odd, y);
+          const int n0 = ti.n_blk * kBNDown + c * 32 + odd * 16;
+          if (row_ok && n0 < a.d) {
+            if (EPI == kEpiScatter) {
+              float* orow = a.out_acc + t * a.d + n0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c + j >= n_valid) continue;
-              const int r_local = ti.m_blk * kBM + c + j;
-              const float y = __uint_as_float(yv[j]) * sd;
-              if (EPI == kEpiScatter) {
-                int64_t t;
-                float w;
-                if (kind == 0 && a.row_w) {  // expert choice: the row's token and score
-                  t = __ldg(a.perm_src + ti.g.h_row0 + r_local);
-                  w = __ldg(a.row_w + ti.g.h_row0 + r_local);
-                } else if (kind == 0) {
-                  const int32_t src = __ldg(a.perm_src + ti.g.h_row0 + r_local);
-                  t = src / a.top_k;
-                  w = __ldg(a.topk_w + src);
-                } else {
-                  t = r_local;
-                  w = 1.f;
-                }
-                atomicAdd(a.out_acc + t * a.d + i, w * y);
-              } else {
-                a.y[(int64_t)(ti.g.h_row0 + r_local) * a.d + i] = __float2bfloat16_rn(y);
+              for (int q = 0; q < 4; ++q) {
+                const float4 sd = __ldg(reinterpret_cast<const float4*>(sdp + n0 + 4 * q));
+                atomicAdd(reinterpret_cast<float4*>(orow + 4 * q),
+                          make_float4(ws * sd.x * y[4 * q], ws * sd.y * y[4 * q + 1], ws * sd.z * y[4 * q + 2],
+                                      ws * sd.w * y[4 * q + 3]));
               }
+            } else {
+              __nv_bfloat16* yrow = a.y + (int64_t)(ti.g.h_row0 + r_local) * a.d + n0;
+              uint32_t p[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 sd = __ldg(reinterpret_cast<const float4*>(sdp + n0 + 4 * q));
+                p[2 * q] = pack_bf16x2(sx * sd.x * y[4 * q], sx * sd.y * y[4 * q + 1]);
+                p[2 * q + 1] = pack_bf16x2(sx * sd.z * y[4 * q + 2], sx * sd.w * y[4 * q + 3]);
+              }
+              *reinterpret_cast<uint4*>(yrow) = make_uint4(p[0], p[1], p[2], p[3]);
+              *reinterpret_cast<uint4*>(yrow + 8) = make_uint4(p[4], p[5], p[6], p[7]);
             }
           }
         }

@@ -124,6 +124,9 @@ struct GemmArgs {
   // of W_down).
   const float* w_scale[2];
   const float* u_scale[2];
+  // FP8 experts: the scale of each activation row, per kind (the token rows
+  // of the gate/up phase, the h rows of the down phase).
+  const float* a_scale[2];
   // Router phase: one group of all T tokens; tile = (m block, split) with
   // split = part * r_dslices + slice.
   int32_t r_tiles, r_m_tiles, r_dslices, r_kb_per_slice, r_nkb_d, r_d_pad, r_np, r_N;
@@ -138,25 +141,35 @@ struct GemmMaps {
   CUtensorMap bu[2];  // up weights per kind (gate/up phase only)
 };
 
-// Tensor maps of the FP8-weight grouped GEMM. Activations (fp16, 128-byte
-// swizzle) per kind with boxes of 16, 32, 64 and 128 rows (a tile loads the
-// smallest box that holds its token rows); weights (E4M3 codes, no swizzle)
+// Tensor maps of the FP8-weight grouped GEMM: activations (two-term E4M3
+// rows, see act_quant.cu) per kind with boxes of 16, 32, 64 and 128 rows (a
+// tile loads the smallest box that holds its 2 x tokens rows); weight codes
 // per kind with 128-row boxes: w = gate (gate/up phase) or down rows, u = up.
+// All boxes are 128 bytes of K wide, 128-byte swizzled.
+constexpr int kF8XBoxes = 4;     // box rows 16 << i
+constexpr int kF8TileRows = 64;  // tokens per tile of the FP8-weight GEMM
 struct F8Maps {
-  CUtensorMap x[2][4];
+  CUtensorMap x[2][kF8XBoxes];
   CUtensorMap w[2];
   CUtensorMap u[2];
 };
-constexpr int kF8XBoxes = 4;  // box rows 16 << i
+
+// An activation matrix for the FP8-weight GEMMs: src fp16 [rows][K] ->
+// dst uint8 [2*rows][K] (row 2r = hi, 2r+1 = lo E4M3 terms) and scale fp32
+// [rows], with src[r] ~= scale[r] * (hi + lo). K % 8 == 0.
+cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* dst, float* scale,
+                             cudaStream_t s);
+// uint8 row-major matrix [rows][inner] as a TMA tensor map: box
+// [box_rows][128 bytes], 128-byte swizzle, zero fill out of bounds. The row
+// pitch (`inner` bytes) must be a multiple of 16.
+bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
 // fp16 row-major matrix as a TMA tensor map, box [box_rows][64], 128-byte swizzle.
 bool make_tmap_f16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
-// uint8 (FP8 code) row-major matrix, box [box_rows][64 bytes], no swizzle.
-// The row pitch (`inner` bytes) must be a multiple of 16.
-bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
-// Grouped GEMM with FP8 E4M3 weights (one CTA per tile, 128 weight rows x up
-// to 128 token rows per MMA; tiles as launch_grouped_gemm with pair = 1).
+// Grouped GEMM with FP8 E4M3 weights on two-term E4M3 activations: tiles of
+// kF8TileRows tokens x 256 weight rows (the schedule built with tile_rows =
+// kF8TileRows), one CTA each.
 cudaError_t launch_grouped_gemm_fp8(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
                                     int64_t tile_bound, cudaStream_t s);
 

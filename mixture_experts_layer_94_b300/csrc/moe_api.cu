@@ -21,6 +21,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc;
+  size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 experts: two-term E4M3 activations + row scales
   size_t total;
 };
 
@@ -68,6 +69,18 @@ Layout make_layout(const moe_problem_t& p, int call) {
   if (call == MOE_CALL_LAYER_FORWARD && ec_rows > 0) {
     L.ec_token = take((size_t)ec_rows * 4);
     L.ec_w = take((size_t)ec_rows * 4);
+  }
+  if (is_fp8(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU)) {
+    L.xq = take((size_t)2 * rows * p.d_model);
+    L.sx = take((size_t)rows * 4);
+    L.hq = take((size_t)2 * rows * p.ffn);
+    L.sh = take((size_t)rows * 4);
+    if (call == MOE_CALL_LAYER_FORWARD && p.n_shared > 0) {
+      L.xq_sh = take((size_t)2 * T * p.d_model);
+      L.sx_sh = take((size_t)T * 4);
+      L.hq_sh = take((size_t)2 * p.n_shared * T * p.shared_ffn);
+      L.sh_sh = take((size_t)p.n_shared * T * 4);
+    }
   }
   if (call == MOE_CALL_LAYER_FORWARD) {
     L.topk_idx = take((size_t)TK * 4);
@@ -150,16 +163,17 @@ bool make_tmap_f16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t row
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// uint8 codes [rows][inner], box [box_rows][64 bytes], dense rows in shared
-// memory (no swizzle), zero fill out of bounds.
+
+// uint8 matrix [rows][inner], box [box_rows][128 bytes], 128-byte swizzle,
+// zero fill out of bounds.
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
   if (!have_encode() || (inner % 16) != 0) return false;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t box[2] = {128u, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace moe
@@ -193,9 +207,10 @@ T* at(void* ws, size_t off) {
 // shapes (a few rows per expert) keep 128-row tiles on single CTAs.
 int32_t gemm_pair(int64_t routed_rows, int32_t N) { return routed_rows >= (int64_t)256 * N ? 2 : 1; }
 
-// Tile rows of the GEMM schedule: the FP8-weight kernel always takes 128.
-int32_t gemm_pair_for(const moe_problem_t& p, int64_t routed_rows) {
-  return is_fp8(p) ? 1 : gemm_pair(routed_rows, p.n_experts);
+// Rows per tile of the GEMM schedule: 128 (single CTAs) or 256 (CTA pairs)
+// for bf16 experts, kF8TileRows tokens for the FP8-weight kernel.
+int32_t gemm_tile_rows(const moe_problem_t& p, int64_t routed_rows) {
+  return is_fp8(p) ? kF8TileRows : kBM * gemm_pair(routed_rows, p.n_experts);
 }
 
 // The two GEMM phases over groups already described in the workspace.
@@ -220,6 +235,14 @@ struct GemmPlan {
   const float* sd_scale;
   __nv_bfloat16* h;       // [routed_rows][F] (fp16 bits when fp8)
   __nv_bfloat16* h_sh;    // [S*T][Fs] (fp16 bits when fp8)
+  uint8_t* xq;            // FP8: two-term E4M3 activations [2 rows][K] and their row scales
+  float* sx;
+  uint8_t* hq;
+  float* sh;
+  uint8_t* xq_sh;
+  float* sx_sh;
+  uint8_t* hq_sh;
+  float* sh_sh;
   int epilogue;           // kEpiScatter or kEpiStoreY
   float* out_acc;
   const int32_t* perm_src;
@@ -316,23 +339,28 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   return MOE_OK;
 }
 
-// The activation maps of one kind: boxes of 16, 32, 64 and 128 rows.
+// The activation maps of one kind (two-term E4M3 rows): boxes of 16, 32, 64
+// and 128 rows.
 bool make_x_maps(CUtensorMap (&m)[kF8XBoxes], const void* ptr, uint64_t inner, uint64_t rows) {
   for (int i = 0; i < kF8XBoxes; ++i)
-    if (!make_tmap_f16(&m[i], ptr, inner, rows, 16u << i)) return false;
+    if (!make_tmap_u8(&m[i], ptr, inner, rows, 16u << i)) return false;
   return true;
 }
 
-// The two GEMM phases for FP8 E4M3 experts (128-row tiles on single CTAs).
+// The two GEMM phases for FP8 E4M3 experts: each phase's activations are
+// first split into two-term E4M3 rows (act_quant.cu).
 moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup) {
   if (!have_encode()) return MOE_ERR_CUDA;
   const bool sh = g.S > 0;
+  MOE_TRY(cuda_status(launch_act_quant(g.x_routed, g.routed_rows, g.d, g.xq, g.sx, s)));
+  if (sh) MOE_TRY(cuda_status(launch_act_quant(g.x_shared, g.T, g.d, g.xq_sh, g.sx_sh, s)));
   F8Maps m{};
-  bool ok = make_x_maps(m.x[0], g.x_routed, g.d, g.routed_rows) &&
+  bool ok = make_x_maps(m.x[0], g.xq, g.d, 2 * (uint64_t)g.routed_rows) &&
             make_tmap_u8(&m.w[0], g.wg, g.d, (uint64_t)g.N * g.F, 128) &&
             make_tmap_u8(&m.u[0], g.wu, g.d, (uint64_t)g.N * g.F, 128);
   if (ok && sh)
-    ok = make_x_maps(m.x[1], g.x_shared, g.d, g.T) && make_tmap_u8(&m.w[1], g.sg, g.d, (uint64_t)g.S * g.Fs, 128) &&
+    ok = make_x_maps(m.x[1], g.xq_sh, g.d, 2 * (uint64_t)g.T) &&
+         make_tmap_u8(&m.w[1], g.sg, g.d, (uint64_t)g.S * g.Fs, 128) &&
          make_tmap_u8(&m.u[1], g.su, g.d, (uint64_t)g.S * g.Fs, 128);
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
@@ -347,11 +375,11 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.d = g.d;
   a.top_k = g.K;
 
-  // gate/up + SwiGLU
+  // gate/up + SwiGLU (K advances 128 codes per stage)
   a.tile_start = g.ts_gu;
   a.n_ext[0] = g.F;
   a.n_ext[1] = sh ? g.Fs : g.F;
-  a.k_blocks[0] = a.k_blocks[1] = (g.d + kBK - 1) / kBK;
+  a.k_blocks[0] = a.k_blocks[1] = (g.d + 127) / 128;
   a.w_rows[0] = g.F;
   a.w_rows[1] = sh ? g.Fs : g.F;
   a.h[0] = g.h;
@@ -362,15 +390,20 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.u_scale[0] = g.wu_scale;
   a.w_scale[1] = sh ? g.sg_scale : g.wg_scale;
   a.u_scale[1] = sh ? g.su_scale : g.wu_scale;
-  int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kBM);
+  a.a_scale[0] = g.sx;
+  a.a_scale[1] = sh ? g.sx_sh : g.sx;
+  int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kF8TileRows);
   MOE_TRY(cuda_status(launch_grouped_gemm_fp8(kPhaseGateUp, kEpiSwiGLU, m, a, bound, s)));
   if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[0], s)));
 
   // down (+ weighted scatter-add or plain store)
+  MOE_TRY(cuda_status(launch_act_quant(g.h, g.routed_rows, g.F, g.hq, g.sh, s)));
+  if (sh) MOE_TRY(cuda_status(launch_act_quant(g.h_sh, (int64_t)g.S * g.T, g.Fs, g.hq_sh, g.sh_sh, s)));
   F8Maps md{};
-  ok = make_x_maps(md.x[0], g.h, g.F, g.routed_rows) && make_tmap_u8(&md.w[0], g.wd, g.F, (uint64_t)g.N * g.d, 128);
+  ok = make_x_maps(md.x[0], g.hq, g.F, 2 * (uint64_t)g.routed_rows) &&
+       make_tmap_u8(&md.w[0], g.wd, g.F, (uint64_t)g.N * g.d, 128);
   if (ok && sh)
-    ok = make_x_maps(md.x[1], g.h_sh, g.Fs, (uint64_t)g.S * g.T) &&
+    ok = make_x_maps(md.x[1], g.hq_sh, g.Fs, 2 * (uint64_t)g.S * g.T) &&
          make_tmap_u8(&md.w[1], g.sd, g.Fs, (uint64_t)g.S * g.d, 128);
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
@@ -381,18 +414,20 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   md.u[1] = md.w[1];
   a.tile_start = g.ts_dn;
   a.n_ext[0] = a.n_ext[1] = g.d;
-  a.k_blocks[0] = (g.F + kBK - 1) / kBK;
-  a.k_blocks[1] = sh ? (g.Fs + kBK - 1) / kBK : a.k_blocks[0];
+  a.k_blocks[0] = (g.F + 127) / 128;
+  a.k_blocks[1] = sh ? (g.Fs + 127) / 128 : a.k_blocks[0];
   a.w_rows[0] = a.w_rows[1] = g.d;
   a.w_scale[0] = g.wd_scale;
   a.w_scale[1] = sh ? g.sd_scale : g.wd_scale;
   a.u_scale[0] = a.u_scale[1] = nullptr;
+  a.a_scale[0] = g.sh;
+  a.a_scale[1] = sh ? g.sh_sh : g.sh;
   a.out_acc = g.out_acc;
   a.perm_src = g.perm_src;
   a.topk_w = g.topk_w;
   a.row_w = g.row_w;
   a.y = g.y;
-  bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kBM);
+  bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kF8TileRows);
   MOE_TRY(cuda_status(launch_grouped_gemm_fp8(kPhaseDown, g.epilogue, md, a, bound, s)));
   if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[1], s)));
   return MOE_OK;
@@ -545,8 +580,9 @@ moe_status_t grouped_swiglu_impl(const moe_problem_t* p, const void* x_perm, con
   MOE_TRY(check_ws(&q, MOE_CALL_GROUPED_SWIGLU, ws, ws_bytes, &L));
   if (rows == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int32_t pair = gemm_pair_for(q, rows);
-  ScheduleArgs sa{q.n_experts, 0, q.ffn, 0, q.d_model, kBM * pair, q.T, offsets, at<GroupDesc>(ws, L.groups),
+  const int32_t tile_rows = gemm_tile_rows(q, rows);
+  const int32_t pair = tile_rows == 2 * kBM ? 2 : 1;
+  ScheduleArgs sa{q.n_experts, 0, q.ffn, 0, q.d_model, tile_rows, q.T, offsets, at<GroupDesc>(ws, L.groups),
                   at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
   MOE_TRY(cuda_status(launch_schedule(sa, s)));
   GemmPlan g{};
@@ -555,6 +591,12 @@ moe_status_t grouped_swiglu_impl(const moe_problem_t* p, const void* x_perm, con
   g.wg_scale = sg;
   g.wu_scale = su;
   g.wd_scale = sd;
+  if (fp8) {
+    g.xq = at<uint8_t>(ws, L.xq);
+    g.sx = at<float>(ws, L.sx);
+    g.hq = at<uint8_t>(ws, L.hq);
+    g.sh = at<float>(ws, L.sh);
+  }
   g.N = q.n_experts;
   g.S = 0;
   g.F = q.ffn;
@@ -698,8 +740,9 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     MOE_TRY(cuda_status(launch_gather(pa, rows, s)));
     MOE_TRY(record(ev, 2, s));
     // 3. GEMM schedule over the N full expert groups and the shared experts
-    const int32_t pair = gemm_pair_for(*p, rows);
-    ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, kBM * pair, T, offsets,
+    const int32_t tile_rows = gemm_tile_rows(*p, rows);
+    const int32_t pair = tile_rows == 2 * kBM ? 2 : 1;
+    ScheduleArgs sa{N, S, p->ffn, p->shared_ffn, p->d_model, tile_rows, T, offsets,
                     at<GroupDesc>(ws, L.groups), at<int32_t>(ws, L.ts_gu), at<int32_t>(ws, L.ts_dn)};
     MOE_TRY(cuda_status(launch_schedule(sa, s)));
     MOE_TRY(record(ev, 3, s));
@@ -729,6 +772,18 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.sg_scale = w->ws_gate_scale;
   g.su_scale = w->ws_up_scale;
   g.sd_scale = w->ws_down_scale;
+  if (fp8) {
+    g.xq = at<uint8_t>(ws, L.xq);
+    g.sx = at<float>(ws, L.sx);
+    g.hq = at<uint8_t>(ws, L.hq);
+    g.sh = at<float>(ws, L.sh);
+    if (S > 0) {
+      g.xq_sh = at<uint8_t>(ws, L.xq_sh);
+      g.sx_sh = at<float>(ws, L.sx_sh);
+      g.hq_sh = at<uint8_t>(ws, L.hq_sh);
+      g.sh_sh = at<float>(ws, L.sh_sh);
+    }
+  }
     g.h = at<__nv_bfloat16>(ws, L.h);
     g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
     g.epilogue = kEpiScatter;
@@ -776,14 +831,15 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.err = err;
   // 3. the GEMM schedule (routed experts from offsets, then the shared
   //    experts) is built by the same kernel that finishes the prefix sums
-  const int32_t pair = gemm_pair_for(*p, T * K);
+  const int32_t tile_rows = gemm_tile_rows(*p, T * K);
+  const int32_t pair = tile_rows == 2 * kBM ? 2 : 1;
   pa.groups = at<GroupDesc>(ws, L.groups);
   pa.ts_gu = at<int32_t>(ws, L.ts_gu);
   pa.ts_dn = at<int32_t>(ws, L.ts_dn);
   pa.S = S;
   pa.F = p->ffn;
   pa.Fs = p->shared_ffn;
-  pa.tile_rows = kBM * pair;
+  pa.tile_rows = tile_rows;
   MOE_TRY(cuda_status(launch_permute(pa, s)));
   MOE_TRY(record(ev, 2, s));
   MOE_TRY(record(ev, 3, s));
@@ -814,6 +870,18 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.sg_scale = w->ws_gate_scale;
   g.su_scale = w->ws_up_scale;
   g.sd_scale = w->ws_down_scale;
+  if (fp8) {
+    g.xq = at<uint8_t>(ws, L.xq);
+    g.sx = at<float>(ws, L.sx);
+    g.hq = at<uint8_t>(ws, L.hq);
+    g.sh = at<float>(ws, L.sh);
+    if (S > 0) {
+      g.xq_sh = at<uint8_t>(ws, L.xq_sh);
+      g.sx_sh = at<float>(ws, L.sx_sh);
+      g.hq_sh = at<uint8_t>(ws, L.hq_sh);
+      g.sh_sh = at<float>(ws, L.sh_sh);
+    }
+  }
   g.h = at<__nv_bfloat16>(ws, L.h);
   g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
   g.epilogue = kEpiScatter;
@@ -859,9 +927,12 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   // route and pack: histogram, scan (+ schedule), scatter -- one kernel for at
   // most 32 chunks of 32 tokens -- then the gather; gate/up GEMM, down GEMM, finalise
   const int router = p->hidden_dtype == MOE_BF16 ? 3 : 2;
-  if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3;  // + select, gather, schedule
+  // FP8 experts: the two-term E4M3 split of each GEMM's activations (x, h;
+  // and the shared experts' x, h)
+  const int quant = is_fp8(*p) ? (p->n_shared > 0 ? 4 : 2) : 0;
+  if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
-  return router + route + 3;
+  return router + route + 3 + quant;
 }
 
 moe_status_t moe_get_device_status(void* ws, void* stream) {

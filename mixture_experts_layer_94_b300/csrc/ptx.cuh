@@ -268,18 +268,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// Instruction descriptor, kind::f16: fp32 D, fp16 A and B, both K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+// Instruction descriptor, kind::f8f6f4: fp32 D, E4M3 A and B (format code 0
+// for both), both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N) {
   return (1u << 4)                       // D format: f32
-         | ((uint32_t)(N >> 3) << 17)    // N / 8 (A and B format 0: f16)
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// D[tmem] (+)= A * B^T with fp16 operands (the same instruction as mma_bf16;
-// the operand type is carried by the instruction descriptor).
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  mma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, 8-bit floating-point operands
+// (K = 32 per instruction), fp32 accumulator.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 }  // namespace ptx
