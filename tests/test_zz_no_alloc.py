@@ -29,12 +29,12 @@ def _binding():
     return B
 
 
-def _case(T, N, K, d, seed):
+def _case(T, N, K, d, seed, expert_dtype="bf16"):
     rng = np.random.default_rng(seed)
     p_e = 1.0 / np.arange(1, N + 1) ** 1.2
     p_e /= p_e.sum()
     idx = np.stack([rng.choice(N, size=K, replace=False, p=p_e) for _ in range(T)]).astype(np.int32)
-    cfg = inputs.MoEConfig("noalloc", T=T, d=d, N=N, K=K, F=8)
+    cfg = inputs.MoEConfig("noalloc", T=T, d=d, N=N, K=K, F=16, expert_dtype=expert_dtype)
     hidden = inputs.make_router_inputs(cfg, seed=seed)["hidden"].cuda()
     return cfg, torch.from_numpy(idx).cuda(), hidden
 
@@ -71,8 +71,10 @@ def test_static_scratch_permute_matches_workspace_permute_on_two_calls():
     B = _binding()
     # First a problem that fills the whole array (256 experts x 256 chunks),
     # then a smaller one that finds the first call's counts still there.
-    for T, N, K, d, seed in ((8192, 256, 8, 64, 11), (300, 64, 6, 136, 12)):
-        cfg, idx, hidden = _case(T, N, K, d, seed)
+    # The third call is an FP8-expert problem: its packed rows are fp16.
+    for T, N, K, d, seed, dt in ((8192, 256, 8, 64, 11, "bf16"), (300, 64, 6, 136, 12, "bf16"),
+                                 (200, 16, 4, 144, 14, "fp8")):
+        cfg, idx, hidden = _case(T, N, K, d, seed, dt)
         got = _run_static(B, cfg, idx, hidden)
         torch.cuda.synchronize()
         ref = _run_workspace(B, cfg, idx, hidden)
