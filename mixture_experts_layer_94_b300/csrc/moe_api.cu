@@ -923,10 +923,11 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
 int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   if (moe_problem_check(p) != MOE_OK) return 0;
   if (p->T == 0) return 1;  // the histogram scan that writes zero counts
-  // router: split + router GEMM (bf16 hidden) or logits kernel (fp32), then top-K;
   // route and pack: histogram, scan (+ schedule), scatter -- one kernel for at
   // most 32 chunks of 32 tokens -- then the gather; gate/up GEMM, down GEMM, finalise
-  const int router = p->hidden_dtype == MOE_BF16 ? 3 : 2;
+  // router: split + router GEMM (tensor-core logits) or one CUDA-core logits
+  // kernel, then top-K
+  const int router = router_plan(p->T, p->d_model, p->n_experts, p->hidden_dtype == MOE_BF16).tensor ? 3 : 2;
   // FP8 experts: the two-term E4M3 split of each GEMM's activations (x, h;
   // and the shared experts' x, h)
   const int quant = is_fp8(*p) ? (p->n_shared > 0 ? 4 : 2) : 0;

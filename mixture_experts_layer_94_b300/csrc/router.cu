@@ -8,9 +8,10 @@
 // shifts the scores used for selection only.
 //
 // fp32 throughout (the router is kept in higher precision than the experts,
-// "Chapter 19", §19.6.2 table). For a bf16 hidden the logits run on the tensor
-// cores (the grouped GEMM's router phase, see split_router_kernel below); for
-// an fp32 hidden, on CUDA cores:
+// "Chapter 19", §19.6.2 table). For a bf16 hidden of more than 64 tokens the
+// logits run on the tensor cores (the grouped GEMM's router phase, see
+// split_router_kernel below); for an fp32 hidden or a small batch, on CUDA
+// cores:
 //   R1 router_logits: partial logits over a slice of d, for a tile of tokens.
 //      The d axis is split into S slices when there are too few token tiles to
 //      fill the GPU (decode batches), so every SM streams part of W_router.
@@ -42,10 +43,23 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[2 * q] = __uint_as_float(w[q] << 16);
+    v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
 template <>
 __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // ---------------------------------------------------------------- R1, N <= 32
 // NP: N rounded up to a power of two; TPW tokens per warp.
@@ -206,25 +220,37 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
   const int64_t t = (int64_t)blockIdx.x * kWarps + warp;
   if (t >= a.T) return;
   const int N = a.N, K = a.K;
-  float key[EPL], sc[EPL];
+  float key[EPL], sc[EPL], lg[EPL];
   bool valid[EPL];
+  // Partials summed in split order (deterministic). All of a lane's experts
+  // load 8 splits at a time, so EPL x 8 loads are in flight together.
+  {
+    const int64_t stride = a.T * N;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      valid[i] = lane + 32 * i < N;
+      lg[i] = 0.f;
+    }
+    for (int s0 = 0; s0 < a.splits; s0 += 8) {
+      float v[EPL][8];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const float* pp = a.partial + t * N + lane + 32 * i;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          v[i][q] = (valid[i] && s0 + q < a.splits) ? __ldg(pp + (int64_t)(s0 + q) * stride) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) lg[i] += v[i][q];
+    }
+  }
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    valid[i] = e < N;
-    float l = 0.f;
+    float l = lg[i];
     if (valid[i]) {
-      // Partials summed in split order (deterministic), loaded 8 at a time so
-      // the loads are in flight together.
-      const float* pp = a.partial + t * N + e;
-      const int64_t stride = a.T * N;
-      for (int s0 = 0; s0 < a.splits; s0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = (s0 + q < a.splits) ? __ldg(pp + (int64_t)(s0 + q) * stride) : 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) l += v[q];
-      }
       if (a.router_bias) l += a.router_bias[e];
       if (a.logits) a.logits[t * N + e] = l;
     }
@@ -578,12 +604,21 @@ cudaError_t launch_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_
 
 }  // namespace
 
+// Batches of at most this many tokens take the CUDA-core logits kernels even
+// with a bf16 hidden: they read the fp32 router matrix once, split over d
+// across CTAs, instead of splitting it into three bf16 parts for a tensor-core
+// GEMM with a single token tile.
+constexpr int64_t kCudaCoreMaxT = 64;
+// Most d slices the CUDA-core path splits a token tile into (the top-K kernel
+// sums this many partials per logit).
+constexpr int64_t kMaxSplits = 32;
+
 RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
   // Aim at ~2 CTAs per SM of a 148-SM part; the plan depends on sizes only so
   // that workspace sizes are a host-side function of the problem.
   constexpr int64_t kTargetCtas = 296;
   RouterPlan pl{};
-  if (hidden_bf16) {
+  if (hidden_bf16 && T > kCudaCoreMaxT) {
     // Tensor cores: one CTA per SM; tiles = 128-token blocks x 3 parts x slices.
     constexpr int64_t kTargetTiles = 148;
     pl.tensor = true;
@@ -617,6 +652,7 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
   const int64_t max_splits = (d + chunk - 1) / chunk;
   int64_t splits = 1;
   if (pl.token_tiles > 0 && pl.token_tiles < kTargetCtas) splits = (kTargetCtas + pl.token_tiles - 1) / pl.token_tiles;
+  if (splits > kMaxSplits) splits = kMaxSplits;
   if (splits > max_splits) splits = max_splits;
   if (splits < 1) splits = 1;
   int64_t slice = (d + splits - 1) / splits;
@@ -639,7 +675,8 @@ cudaError_t launch_router(const RouterArgs& a0, bool hidden_bf16, cudaStream_t s
   RouterArgs a = a0;
   a.splits = pl.splits;
   a.d_slice = pl.d_slice;
-  cudaError_t e = pl.tensor ? launch_tensor_logits(a, pl, s) : launch_logits<float>(a, pl, s);
+  cudaError_t e = pl.tensor ? launch_tensor_logits(a, pl, s)
+                  : (hidden_bf16 ? launch_logits<__nv_bfloat16>(a, pl, s) : launch_logits<float>(a, pl, s));
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((a.T + kWarps - 1) / kWarps);
   if (a.N <= 32) topk_kernel<1><<<grid, kWarps * 32, 0, s>>>(a);
