@@ -14,8 +14,9 @@
  * fp32 keys: the same precision the device kernel decides in. Everything after
  * the decision (weights, expert FFNs, combine) is fp64.
  *
- * Expert weights arrive as bf16 bit patterns (uint16), or as FP8 E4M3 codes
- * (uint8) with one fp32 scale per matrix row ("AI Infrastructure series, Part
+ * Expert weights arrive as bf16 bit patterns (uint16), as FP8 E4M3 codes
+ * (uint8) with one fp32 scale per matrix row, or as MXFP4 (E2M1 codes two
+ * per byte with one E8M0 scale per 32 elements of a row) ("AI Infrastructure series, Part
  * 12 of 24", "How do you serve an MoE model on your own GPUs?": quantise the
  * experts' weights, keep the router in 16 bits or more; "Mixture of Experts
  * Explained", "Total versus active parameters": the bytes a token reads fall
@@ -56,44 +57,68 @@ double moe_oracle_e4m3_to_double(uint8_t b) {
   return s ? -v : v;
 }
 
-/* Expert weights in one of two storage formats: bf16 values (scale unused),
- * or FP8 E4M3 codes with one fp32 scale per matrix row: w = e4m3(q) * scale. */
+/* OCP FP4 E2M1: sign, 2 exponent bits with bias 1, 1 mantissa bit; exponent
+ * 0 encodes the subnormal m * 0.5. Values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+ * their negatives. */
+double moe_oracle_e2m1_to_double(uint8_t c) {
+  const int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
+/* OCP E8M0 shared scale: 2^(E - 127); E = 255 is NaN. */
+double moe_oracle_e8m0_to_double(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+/* Expert weights in one of three storage formats:
+ *   0  bf16 values;
+ *   1  FP8 E4M3 codes with one fp32 scale per matrix row: w = e4m3(q) * scale[row];
+ *   2  MXFP4 (OCP microscaling): E2M1 codes packed two per byte (element 2i
+ *      in the low nibble, 2i+1 in the high nibble) and one E8M0 scale per 32
+ *      consecutive elements of a row: w = e2m1(q) * 2^(bscale[row][col/32] - 127). */
 typedef struct {
-  int fmt; /* 0 bf16, 1 fp8 e4m3 + per-row scale */
+  int fmt;
   const void* q;
-  const float* scale;
+  const float* scale;     /* fmt 1: [rows] */
+  const uint8_t* bscale;  /* fmt 2: [rows][ld / 32] */
 } wmat_t;
 
 static double wload(wmat_t w, int64_t row, int64_t ld, int64_t col) {
   if (w.fmt == 0) return bf16_bits_to_double(((const uint16_t*)w.q)[row * ld + col]);
-  return moe_oracle_e4m3_to_double(((const uint8_t*)w.q)[row * ld + col]) * (double)w.scale[row];
+  if (w.fmt == 1) return moe_oracle_e4m3_to_double(((const uint8_t*)w.q)[row * ld + col]) * (double)w.scale[row];
+  const uint8_t byte = ((const uint8_t*)w.q)[row * (ld / 2) + col / 2];
+  const uint8_t code = (col & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+  return moe_oracle_e2m1_to_double(code) * moe_oracle_e8m0_to_double(w.bscale[row * (ld / 32) + col / 32]);
 }
 
 /* A set of experts' matrices, one pointer per expert (NULL: not provided),
- * all in one format; scales are used only for fp8. */
+ * all in one format; the scale arrays (fp32 row scales for fmt 1, E8M0 block
+ * scales for fmt 2) are unused for bf16. */
 typedef struct {
   int fmt;
   const void* const* gate;
   const void* const* up;
   const void* const* down;
-  const float* const* s_gate;
-  const float* const* s_up;
-  const float* const* s_down;
+  const void* const* s_gate;
+  const void* const* s_up;
+  const void* const* s_down;
 } wset_t;
 
 /* Expert e of a set; returns 0 if any of its matrices (or scales) is missing. */
 static int wset_expert(const wset_t* ws, int32_t e, wmat_t* g, wmat_t* u, wmat_t* dn) {
   if (!ws->gate[e] || !ws->up[e] || !ws->down[e]) return 0;
-  if (ws->fmt == 1 && (!ws->s_gate || !ws->s_up || !ws->s_down || !ws->s_gate[e] || !ws->s_up[e] ||
+  if (ws->fmt != 0 && (!ws->s_gate || !ws->s_up || !ws->s_down || !ws->s_gate[e] || !ws->s_up[e] ||
                        !ws->s_down[e]))
     return 0;
   g->fmt = u->fmt = dn->fmt = ws->fmt;
   g->q = ws->gate[e];
   u->q = ws->up[e];
   dn->q = ws->down[e];
-  g->scale = ws->fmt ? ws->s_gate[e] : NULL;
-  u->scale = ws->fmt ? ws->s_up[e] : NULL;
-  dn->scale = ws->fmt ? ws->s_down[e] : NULL;
+  g->scale = ws->fmt == 1 ? (const float*)ws->s_gate[e] : NULL;
+  u->scale = ws->fmt == 1 ? (const float*)ws->s_up[e] : NULL;
+  dn->scale = ws->fmt == 1 ? (const float*)ws->s_down[e] : NULL;
+  g->bscale = ws->fmt == 2 ? (const uint8_t*)ws->s_gate[e] : NULL;
+  u->bscale = ws->fmt == 2 ? (const uint8_t*)ws->s_up[e] : NULL;
+  dn->bscale = ws->fmt == 2 ? (const uint8_t*)ws->s_down[e] : NULL;
   return 1;
 }
 
@@ -431,7 +456,7 @@ static void expert_ffn_w(int32_t d, int32_t F, const double* x, wmat_t wg, wmat_
 void moe_oracle_expert_ffn(int32_t d, int32_t F, const double* x, const uint16_t* w_gate,
                            const uint16_t* w_up, const uint16_t* w_down, double* h,
                            double* y) {
-  const wmat_t wg = {0, w_gate, NULL}, wu = {0, w_up, NULL}, wd = {0, w_down, NULL};
+  const wmat_t wg = {0, w_gate, NULL, NULL}, wu = {0, w_up, NULL, NULL}, wd = {0, w_down, NULL, NULL};
   expert_ffn_w(d, F, x, wg, wu, wd, h, y);
 }
 
@@ -440,7 +465,17 @@ void moe_oracle_expert_ffn(int32_t d, int32_t F, const double* x, const uint16_t
 void moe_oracle_expert_ffn_fp8(int32_t d, int32_t F, const double* x, const uint8_t* q_gate,
                                const float* s_gate, const uint8_t* q_up, const float* s_up,
                                const uint8_t* q_down, const float* s_down, double* h, double* y) {
-  const wmat_t wg = {1, q_gate, s_gate}, wu = {1, q_up, s_up}, wd = {1, q_down, s_down};
+  const wmat_t wg = {1, q_gate, s_gate, NULL}, wu = {1, q_up, s_up, NULL}, wd = {1, q_down, s_down, NULL};
+  expert_ffn_w(d, F, x, wg, wu, wd, h, y);
+}
+
+/* The same expert with MXFP4 weights: W_gate, W_up codes [F][d/2] with E8M0
+ * block scales [F][d/32]; W_down codes [d][F/2] with block scales [d][F/32]
+ * (d and F multiples of 32). */
+void moe_oracle_expert_ffn_mxfp4(int32_t d, int32_t F, const double* x, const uint8_t* q_gate,
+                                 const uint8_t* b_gate, const uint8_t* q_up, const uint8_t* b_up,
+                                 const uint8_t* q_down, const uint8_t* b_down, double* h, double* y) {
+  const wmat_t wg = {2, q_gate, NULL, b_gate}, wu = {2, q_up, NULL, b_up}, wd = {2, q_down, NULL, b_down};
   expert_ffn_w(d, F, x, wg, wu, wd, h, y);
 }
 
@@ -644,9 +679,11 @@ int moe_oracle_layer_routed_fp8(int64_t n_rows, int32_t d, int32_t N, int32_t M,
   if (!s_gate || !s_up || !s_down) return ORACLE_ERR_ARG;
   if (S > 0 && (!ss_gate || !ss_up || !ss_down)) return ORACLE_ERR_ARG;
   const wset_t routed = {1, (const void* const*)q_gate, (const void* const*)q_up,
-                         (const void* const*)q_down, s_gate, s_up, s_down};
+                         (const void* const*)q_down, (const void* const*)s_gate, (const void* const*)s_up,
+                         (const void* const*)s_down};
   const wset_t shared = {1, (const void* const*)qs_gate, (const void* const*)qs_up,
-                         (const void* const*)qs_down, ss_gate, ss_up, ss_down};
+                         (const void* const*)qs_down, (const void* const*)ss_gate, (const void* const*)ss_up,
+                         (const void* const*)ss_down};
   return layer_routed_impl(n_rows, d, N, M, F, S, Fs, hidden, idx, w, &routed, &shared, out);
 }
 
@@ -785,9 +822,42 @@ int moe_oracle_layer_fp8(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_
   if (!s_gate || !s_up || !s_down) return ORACLE_ERR_ARG;
   if (S > 0 && (!ss_gate || !ss_up || !ss_down)) return ORACLE_ERR_ARG;
   const wset_t routed = {1, (const void* const*)q_gate, (const void* const*)q_up,
-                         (const void* const*)q_down, s_gate, s_up, s_down};
+                         (const void* const*)q_down, (const void* const*)s_gate, (const void* const*)s_up,
+                         (const void* const*)s_down};
   const wset_t shared = {1, (const void* const*)qs_gate, (const void* const*)qs_up,
-                         (const void* const*)qs_down, ss_gate, ss_up, ss_down};
+                         (const void* const*)qs_down, (const void* const*)ss_gate, (const void* const*)ss_up,
+                         (const void* const*)ss_down};
+  return layer_impl(n_rows, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups, hidden,
+                    w_router, router_bias, sel_bias, &routed, &shared, keep, topk_idx, topk_w, margin,
+                    out);
+}
+
+/*
+ * The layer with every expert matrix (routed and shared) in MXFP4, as
+ * moe_oracle_expert_ffn_mxfp4: codes q_* [rows][K/2] and E8M0 block scales
+ * b_* [rows][K/32] per expert (shared: qs_*, bs_*). The router stays fp32.
+ */
+int moe_oracle_layer_mxfp4(int64_t n_rows, int32_t d, int32_t N, int32_t K, int32_t F,
+                           int32_t S, int32_t Fs, int32_t score_fn, int32_t renormalize,
+                           int32_t n_groups, int32_t topk_groups,
+                           const float* hidden, const float* w_router, const float* router_bias,
+                           const float* sel_bias, const uint8_t* const* q_gate,
+                           const uint8_t* const* q_up, const uint8_t* const* q_down,
+                           const uint8_t* const* b_gate, const uint8_t* const* b_up,
+                           const uint8_t* const* b_down, const uint8_t* const* qs_gate,
+                           const uint8_t* const* qs_up, const uint8_t* const* qs_down,
+                           const uint8_t* const* bs_gate, const uint8_t* const* bs_up,
+                           const uint8_t* const* bs_down, const unsigned char* keep,
+                           int32_t* topk_idx, double* topk_w, double* margin, double* out) {
+  if (!b_gate || !b_up || !b_down) return ORACLE_ERR_ARG;
+  if (S > 0 && (!bs_gate || !bs_up || !bs_down)) return ORACLE_ERR_ARG;
+  if ((d % 32) != 0 || (F % 32) != 0 || (S > 0 && (Fs % 32) != 0)) return ORACLE_ERR_ARG;
+  const wset_t routed = {2, (const void* const*)q_gate, (const void* const*)q_up,
+                         (const void* const*)q_down, (const void* const*)b_gate, (const void* const*)b_up,
+                         (const void* const*)b_down};
+  const wset_t shared = {2, (const void* const*)qs_gate, (const void* const*)qs_up,
+                         (const void* const*)qs_down, (const void* const*)bs_gate, (const void* const*)bs_up,
+                         (const void* const*)bs_down};
   return layer_impl(n_rows, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups, hidden,
                     w_router, router_bias, sel_bias, &routed, &shared, keep, topk_idx, topk_w, margin,
                     out);

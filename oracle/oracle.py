@@ -65,6 +65,14 @@ def _load():
         lib.moe_oracle_layer_fp8.restype = ctypes.c_int
         lib.moe_oracle_layer_routed_fp8.argtypes = [i64] + [i32] * 6 + [P] * 16
         lib.moe_oracle_layer_routed_fp8.restype = ctypes.c_int
+        lib.moe_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+        lib.moe_oracle_e2m1_to_double.restype = ctypes.c_double
+        lib.moe_oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+        lib.moe_oracle_e8m0_to_double.restype = ctypes.c_double
+        lib.moe_oracle_expert_ffn_mxfp4.argtypes = [i32, i32] + [P] * 9
+        lib.moe_oracle_expert_ffn_mxfp4.restype = None
+        lib.moe_oracle_layer_mxfp4.argtypes = [i64] + [i32] * 10 + [P] * 21
+        lib.moe_oracle_layer_mxfp4.restype = ctypes.c_int
         lib.moe_oracle_silu.argtypes = [ctypes.c_double]
         lib.moe_oracle_silu.restype = ctypes.c_double
         lib.moe_oracle_num_threads.argtypes = []
@@ -442,3 +450,70 @@ def layer_routed_fp8(hidden, idx, w, q_gate, s_gate, q_up, s_up, q_down, s_down,
     if rc != 0:
         raise ValueError(f"moe_oracle_layer_routed_fp8 failed ({rc})")
     return out
+
+
+def e2m1_value(code: int) -> float:
+    """The value of one FP4 E2M1 code (0..15) as the oracle decodes it."""
+    return float(_load().moe_oracle_e2m1_to_double(int(code)))
+
+
+def e8m0_value(code: int) -> float:
+    """The value of one E8M0 scale code (0..255) as the oracle decodes it."""
+    return float(_load().moe_oracle_e8m0_to_double(int(code)))
+
+
+def expert_ffn_mxfp4(x, q_gate, b_gate, q_up, b_up, q_down, b_down, return_h=False):
+    """One SwiGLU expert with MXFP4 weights: packed E2M1 codes uint8 ([F][d/2],
+    [F][d/2], [d][F/2]) and E8M0 block scales uint8 ([F][d/32], [F][d/32],
+    [d][F/32]). Returns y (or (h, y))."""
+    lib = _load()
+    x = _f64(x)
+    qg, qu, qd = _u8(q_gate), _u8(q_up), _u8(q_down)
+    bg, bu, bd = _u8(b_gate), _u8(b_up), _u8(b_down)
+    F, d2 = qg.shape
+    d = 2 * d2
+    assert x.shape == (d,) and qu.shape == (F, d2) and qd.shape == (d, F // 2)
+    assert bg.shape == (F, d // 32) and bu.shape == (F, d // 32) and bd.shape == (d, F // 32)
+    h = np.empty((F,), np.float64)
+    y = np.empty((d,), np.float64)
+    lib.moe_oracle_expert_ffn_mxfp4(d, F, _ptr(x), _ptr(qg), _ptr(bg), _ptr(qu), _ptr(bu), _ptr(qd),
+                                    _ptr(bd), _ptr(h), _ptr(y))
+    return (h, y) if return_h else y
+
+
+def layer_mxfp4(hidden, w_router, q_gate, b_gate, q_up, b_up, q_down, b_down, K, score_fn=SOFTMAX,
+                renormalize=1, router_bias=None, sel_bias=None, qs_gate=None, bs_gate=None, qs_up=None,
+                bs_up=None, qs_down=None, bs_down=None, n_groups=0, topk_groups=0, keep=None):
+    """The whole layer with MXFP4 expert weights (per-expert packed codes and
+    E8M0 block scales; routed: q_*/b_*, shared: qs_*/bs_*). Otherwise as
+    layer(). Returns dict(idx, w, margin, out)."""
+    lib = _load()
+    x = _f32(hidden)
+    W = _f32(w_router)
+    n, d = x.shape
+    N = W.shape[1]
+    F = next(_u8(m).shape[0] for m in q_gate if m is not None)
+    S = 0 if qs_gate is None else len(qs_gate)
+    Fs = _u8(qs_gate[0]).shape[0] if S else 0
+    arrays, keepalive = [], []
+    for mats, cnt in ((q_gate, N), (q_up, N), (q_down, N), (b_gate, N), (b_up, N), (b_down, N),
+                      (qs_gate, S), (qs_up, S), (qs_down, S), (bs_gate, S), (bs_up, S), (bs_down, S)):
+        if cnt == 0:
+            arrays.append(None)
+            continue
+        arr, k = _raw_ptr_array(mats, cnt, _u8)
+        keepalive.append((arr, k))
+        arrays.append(ctypes.cast(arr, ctypes.c_void_p))
+    rb, sb = _f32(router_bias), _f32(sel_bias)
+    keep_a = None if keep is None else np.ascontiguousarray(keep, dtype=np.uint8)
+    idx = np.empty((n, K), np.int32)
+    w = np.empty((n, K), np.float64)
+    margin = np.empty((n,), np.float64)
+    out = np.empty((n, d), np.float64)
+    rc = lib.moe_oracle_layer_mxfp4(n, d, N, K, F, S, Fs, score_fn, renormalize, n_groups, topk_groups,
+                                    _ptr(x), _ptr(W), _ptr(rb), _ptr(sb), *arrays, _ptr(keep_a), _ptr(idx),
+                                    _ptr(w), _ptr(margin), _ptr(out))
+    del keepalive
+    if rc != 0:
+        raise ValueError(f"moe_oracle_layer_mxfp4 failed ({rc})")
+    return dict(idx=idx, w=w, margin=margin, out=out)

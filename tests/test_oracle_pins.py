@@ -720,3 +720,70 @@ def test_layer_routed_fp8_equals_bf16_on_exact_weights():
     ref = oracle.layer_routed(hidden, idx, w, b(routed, 0), b(routed, 1), b(routed, 2), ws_gate=b(shared, 0),
                               ws_up=b(shared, 1), ws_down=b(shared, 2))
     assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- MXFP4 experts
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # OCP MX: FP4 E2M1 magnitudes, codes 0..7
+
+
+def test_e2m1_and_e8m0_decode():
+    for c in range(16):
+        v = oracle.e2m1_value(c)
+        mag = E2M1_TABLE[c & 7]
+        assert v == (-mag if c & 8 else mag)
+        assert math.copysign(1.0, v) == (-1.0 if c & 8 else 1.0)
+    assert oracle.e8m0_value(127) == 1.0
+    assert oracle.e8m0_value(0) == 2.0 ** -127
+    assert oracle.e8m0_value(254) == 2.0 ** 127
+    assert oracle.e8m0_value(120) == 2.0 ** -7
+    assert math.isnan(oracle.e8m0_value(255))
+
+
+def _mxfp4_case(rng, rows, cols, e_lo=118, e_hi=126):
+    """Weights built as E2M1 values x per-block powers of two, then packed by
+    the OCP layout (element 2i in the low nibble); returns (codes, scales, w)."""
+    mags = rng.integers(0, 8, size=(rows, cols))
+    signs = rng.integers(0, 2, size=(rows, cols))
+    exps = rng.integers(e_lo, e_hi + 1, size=(rows, cols // 32)).astype(np.uint8)
+    w = (np.array(E2M1_TABLE)[mags] * np.where(signs == 1, -1.0, 1.0) *
+         np.ldexp(1.0, np.repeat(exps.astype(np.int64) - 127, 32, axis=1)))
+    codes4 = (mags | (signs << 3)).astype(np.uint8)
+    packed = (codes4[:, 0::2] | (codes4[:, 1::2] << 4)).astype(np.uint8)
+    return packed, exps, w
+
+
+def test_expert_ffn_mxfp4_equals_bf16_expert_on_exact_weights():
+    # E2M1 values times powers of two have at most two significant bits:
+    # exact in bf16, so the MXFP4 expert must equal the bf16 expert bit for bit.
+    rng = np.random.default_rng(21)
+    F, d = 64, 96
+    qg, bg, wg = _mxfp4_case(rng, F, d)
+    qu, bu, wu = _mxfp4_case(rng, F, d)
+    qd, bd, wd = _mxfp4_case(rng, d, F)
+    bits = [_bf16_bits(m) for m in (wg, wu, wd)]
+    for m, b in zip((wg, wu, wd), bits):
+        assert np.array_equal(_bf16_to_f64(b), m)
+    x = rng.standard_normal(d)
+    h4, y4 = oracle.expert_ffn_mxfp4(x, qg, bg, qu, bu, qd, bd, return_h=True)
+    h16, y16 = oracle.expert_ffn(x, *bits, return_h=True)
+    assert np.array_equal(h4, h16) and np.array_equal(y4, y16)
+
+
+def test_layer_mxfp4_equals_bf16_layer_on_exact_weights():
+    rng = np.random.default_rng(22)
+    T, d, N, K, F, Fs = 7, 64, 4, 2, 32, 64
+    hidden = rng.standard_normal((T, d)).astype(np.float32)
+    w_router = rng.standard_normal((d, N)).astype(np.float32)
+    routed = [(_mxfp4_case(rng, F, d), _mxfp4_case(rng, F, d), _mxfp4_case(rng, d, F)) for _ in range(N)]
+    shared = [(_mxfp4_case(rng, Fs, d), _mxfp4_case(rng, Fs, d), _mxfp4_case(rng, d, Fs))]
+    q = lambda cases, m, j: [c[m][j] for c in cases]  # noqa: E731
+    b = lambda cases, m: [_bf16_bits(c[m][2]) for c in cases]  # noqa: E731
+    got = oracle.layer_mxfp4(hidden, w_router, q(routed, 0, 0), q(routed, 0, 1), q(routed, 1, 0),
+                             q(routed, 1, 1), q(routed, 2, 0), q(routed, 2, 1), K=K, qs_gate=q(shared, 0, 0),
+                             bs_gate=q(shared, 0, 1), qs_up=q(shared, 1, 0), bs_up=q(shared, 1, 1),
+                             qs_down=q(shared, 2, 0), bs_down=q(shared, 2, 1))
+    ref = oracle.layer(hidden, w_router, b(routed, 0), b(routed, 1), b(routed, 2), K=K, ws_gate=b(shared, 0),
+                       ws_up=b(shared, 1), ws_down=b(shared, 2))
+    assert np.array_equal(got["idx"], ref["idx"])
+    assert np.array_equal(got["out"], ref["out"])
