@@ -42,11 +42,14 @@ WORKLOADS = {
     "gptoss": (inputs.GPTOSS, "gpt-oss-120b-shaped layer"),
     "tiny": (inputs.TINY, "tiny Mixtral-style layer"),
     "mixtral_fp8": (inputs.MIXTRAL_FP8, "Mixtral-8x7B-shaped prefill layer, FP8 E4M3 experts"),
+    "gptoss_mxfp4": (inputs.GPTOSS_MXFP4, "gpt-oss-120b-shaped layer, MXFP4 experts"),
 }
 for _T in inputs.DECODE_BATCHES:
     WORKLOADS[f"decode{_T}"] = (inputs.QWEN_DECODE.with_(T=_T), f"Qwen3-235B-like decode layer, T={_T}")
     WORKLOADS[f"decode{_T}_fp8"] = (inputs.QWEN_DECODE_FP8.with_(T=_T),
                                     f"Qwen3-235B-like decode layer, FP8 E4M3 experts, T={_T}")
+    WORKLOADS[f"decode{_T}_mxfp4"] = (inputs.QWEN_DECODE_MXFP4.with_(T=_T),
+                                      f"Qwen3-235B-like decode layer, MXFP4 experts, T={_T}")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -79,10 +82,13 @@ def load_peaks():
 def work_model(cfg, counts=None):
     """Algorithmic FLOPs and bytes of one layer forward (tile padding excluded).
     Bytes: the weights of touched experts (bf16: 2 bytes per weight; FP8: 1
-    byte plus a 4-byte scale per matrix row), the router, and hidden in + out."""
+    byte plus a 4-byte scale per matrix row; MXFP4: half a byte plus a 1-byte
+    scale per 32 weights), the router, and hidden in + out."""
     T, d, N, K, F, S, Fs = cfg.T, cfg.d, cfg.N, cfg.K, cfg.F, cfg.S, cfg.Fs
     hid_b = 4 if cfg.hidden_dtype == "f32" else 2
-    wb, sb = (1, 4) if cfg.expert_dtype == "fp8" else (2, 0)
+    wb, sb = {"fp8": (1, 4), "mxfp4": (0.5, 0)}.get(cfg.expert_dtype, (2, 0))
+    if cfg.expert_dtype == "mxfp4":  # block scales: 1 byte per 32 weights
+        wb += 1 / 32
     flops_router = 2 * T * d * N
     flops_gu = 4 * d * F * T * K + 4 * d * Fs * T * S
     flops_dn = 2 * d * F * T * K + 2 * d * Fs * T * S
@@ -92,8 +98,8 @@ def work_model(cfg, counts=None):
     bytes_w = touched * (gu_e + dn_e) + S * (gu_s + dn_s) + 4 * d * N
     bytes_act = T * d * (hid_b + 2)
     return dict(flops=flops_router + flops_gu + flops_dn, flops_gateup=flops_gu, flops_down=flops_dn,
-                bytes=bytes_w + bytes_act, bytes_gateup=touched * gu_e + S * gu_s,
-                bytes_down=touched * dn_e + S * dn_s, touched=touched)
+                bytes=int(bytes_w + bytes_act), bytes_gateup=int(touched * gu_e + S * gu_s),
+                bytes_down=int(touched * dn_e + S * dn_s), touched=touched)
 
 
 class ClockSampler:
@@ -219,8 +225,9 @@ def oracle_rows_timed(cfg, ins, rows):
                       router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
                       sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy())
     used = sorted(set(r["idx"].reshape(-1).tolist()))
-    fp8 = cfg.expert_dtype == "fp8"
-    if fp8:  # E4M3 codes and fp32 row scales
+    fp8 = cfg.expert_dtype in ("fp8", "mxfp4")
+    mx = cfg.expert_dtype == "mxfp4"
+    if fp8:  # 8-bit codes (E4M3, or two packed E2M1) and fp32 row or E8M0 block scales
         bits = lambda t: t.detach().cpu().contiguous().numpy()  # noqa: E731
     else:
         bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
@@ -234,8 +241,10 @@ def oracle_rows_timed(cfg, ins, rows):
         sn = ("ws_gate", "ws_up", "ws_down") + (("ws_gate_scale", "ws_up_scale", "ws_down_scale") if fp8 else ())
         sh = {k: [bits(ins[k][s]) for s in range(cfg.S)] for k in sn}
         if fp8:
+            sk = "bs" if mx else "ss"
             sh = {"qs_gate": sh["ws_gate"], "qs_up": sh["ws_up"], "qs_down": sh["ws_down"],
-                  "ss_gate": sh["ws_gate_scale"], "ss_up": sh["ws_up_scale"], "ss_down": sh["ws_down_scale"]}
+                  f"{sk}_gate": sh["ws_gate_scale"], f"{sk}_up": sh["ws_up_scale"],
+                  f"{sk}_down": sh["ws_down_scale"]}
     keep = None
     if cfg.capacity_factor > 0:  # which copies survive depends on the whole batch's routing
         full = oracle.router(ins["hidden"].float().cpu().numpy(), ins["w_router"].cpu().numpy(), K=cfg.K,
@@ -250,7 +259,10 @@ def oracle_rows_timed(cfg, ins, rows):
               router_bias=None if ins["router_bias"] is None else ins["router_bias"].cpu().numpy(),
               sel_bias=None if ins["sel_bias"] is None else ins["sel_bias"].cpu().numpy(), keep=keep, **sh)
     t0 = time.perf_counter()
-    if fp8:
+    if mx:
+        oracle.layer_mxfp4(x, ins["w_router"].cpu().numpy(), wts["w_gate"], wts["w_gate_scale"], wts["w_up"],
+                           wts["w_up_scale"], wts["w_down"], wts["w_down_scale"], **kw)
+    elif fp8:
         oracle.layer_fp8(x, ins["w_router"].cpu().numpy(), wts["w_gate"], wts["w_gate_scale"], wts["w_up"],
                          wts["w_up_scale"], wts["w_down"], wts["w_down_scale"], **kw)
     else:
@@ -329,7 +341,7 @@ def config_block(cfg, desc, args):
             "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",
             "l2": "inputs larger than L2 (expert weights stream from HBM every step)"
-            if 3 * cfg.d * cfg.F * (1 if cfg.expert_dtype == "fp8" else 2) * cfg.N > 126e6
+            if 3 * cfg.d * cfg.F * {"fp8": 1, "mxfp4": 0.5}.get(cfg.expert_dtype, 2) * cfg.N > 126e6
             else "L2 not flushed (working set fits in L2)"}
 
 
@@ -505,7 +517,7 @@ def run_ours(args, cfg, desc, world, rank):
                  "traffic": traffic_from_profiles(dom_name, args.workload)})
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16" if cfg.expert_dtype == "fp8" else "bf16",
+            "vs_baseline": None, "dtype": "f16" if cfg.expert_dtype in ("fp8", "mxfp4") else "bf16",
             "data": "synthetic (seeded; random-init weights)",
             "config": config_block(cfg, desc, args), "roofline": roof,
             "layer_roofline": {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],

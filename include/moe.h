@@ -90,8 +90,18 @@ typedef enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe
  *                        activation row, x ~= s_row * (hi + lo), whose
  *                        relative error is at most 2^-8 (that of a bf16
  *                        activation), with fp32 accumulation.
+ *   MOE_EXPERT_MXFP4     OCP microscaling FP4 (the format gpt-oss ships its
+ *                        experts in): E2M1 codes packed two per byte (the
+ *                        even element of a row in the low nibble) and one
+ *                        E8M0 scale per 32 consecutive elements of a row:
+ *                        weight = e2m1(code) * 2^(scale - 127). Activations
+ *                        as for FP8. Inside the GEMMs each 32-element block
+ *                        becomes E4M3 codes relative to its row's reference
+ *                        exponent (the row's largest block exponent - 6):
+ *                        exact for blocks within 14 binades of the row's
+ *                        largest, rounded to nearest below that.
  */
-typedef enum { MOE_EXPERT_BF16 = 0, MOE_EXPERT_FP8_E4M3 = 1 } moe_expert_dtype_t;
+typedef enum { MOE_EXPERT_BF16 = 0, MOE_EXPERT_FP8_E4M3 = 1, MOE_EXPERT_MXFP4 = 2 } moe_expert_dtype_t;
 
 /* Which call a workspace is sized for (moe_workspace_bytes). */
 typedef enum {
@@ -139,7 +149,7 @@ typedef struct moe_problem {
                             number of experts per token)                    */
   int32_t expert_dtype;  /* moe_expert_dtype_t of every expert matrix. FP8
                             requires d_model, ffn and shared_ffn to be
-                            multiples of 16                                */
+                            multiples of 16, MXFP4 multiples of 32         */
 } moe_problem_t;
 
 /*
@@ -160,7 +170,12 @@ typedef struct moe_problem {
  * matrix row (16-byte aligned):
  *   w_gate_scale, w_up_scale [N][F]; w_down_scale [N][d];
  *   ws_gate_scale, ws_up_scale [S][Fs]; ws_down_scale [S][d] (NULL when S == 0).
- * They are ignored for bf16 experts.
+ * With expert_dtype == MOE_EXPERT_MXFP4 the expert matrices hold packed E2M1
+ * codes, half the bytes of each row (w_gate, w_up [N][F][d/2], w_down
+ * [N][d][F/2]; shared likewise), and the *_scale arrays hold the E8M0 block
+ * scales as uint8: w_gate_scale, w_up_scale [N][F][d/32], w_down_scale
+ * [N][d][F/32]; ws_* [S][Fs][d/32], [S][Fs][d/32], [S][d][Fs/32].
+ * The scale arrays are ignored for bf16 experts.
  */
 typedef struct moe_weights {
   const float* w_router;
@@ -172,12 +187,12 @@ typedef struct moe_weights {
   const void* ws_gate;
   const void* ws_up;
   const void* ws_down;
-  const float* w_gate_scale;
-  const float* w_up_scale;
-  const float* w_down_scale;
-  const float* ws_gate_scale;
-  const float* ws_up_scale;
-  const float* ws_down_scale;
+  const void* w_gate_scale;   /* fp32 row scales (FP8) or uint8 E8M0 block scales (MXFP4) */
+  const void* w_up_scale;
+  const void* w_down_scale;
+  const void* ws_gate_scale;
+  const void* ws_up_scale;
+  const void* ws_down_scale;
 } moe_weights_t;
 
 /* Human-readable name of a moe_status_t. Never NULL. Host only. */
@@ -353,6 +368,21 @@ moe_status_t moe_grouped_swiglu_fp8(const moe_problem_t* p, const void* x_perm,
                                     void* stream);
 
 /*
+ * moe_grouped_swiglu_fp8 for MXFP4 experts (p->expert_dtype ==
+ * MOE_EXPERT_MXFP4, else MOE_ERR_INVALID_ARG): w_gate, w_up uint8 [N][F][d/2]
+ * packed E2M1 codes with E8M0 block scales w_gate_bscale, w_up_bscale uint8
+ * [N][F][d/32]; w_down [N][d][F/2] with w_down_bscale [N][d][F/32]. Other
+ * arguments, layouts and results as moe_grouped_swiglu_fp8.
+ */
+moe_status_t moe_grouped_swiglu_mxfp4(const moe_problem_t* p, const void* x_perm,
+                                      const int32_t* offsets, const void* w_gate,
+                                      const void* w_gate_bscale, const void* w_up,
+                                      const void* w_up_bscale, const void* w_down,
+                                      const void* w_down_bscale, void* h_perm,
+                                      void* y_perm, void* ws, size_t ws_bytes,
+                                      void* stream);
+
+/*
  * Gate-weighted combine back to token order ("Chapter 19", §19.2 flowchart,
  * "Sum with gate weights"; "Mixture of Experts for LLM Inference", "The MoE
  * change is surprisingly local"):
@@ -385,9 +415,9 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm,
  * (moe_expert_choice_select) and each picked (token, expert) pair adds
  * S[t][e] * E_e(x_t); topk_idx_opt and topk_w_opt must then be NULL and
  * counts_opt receives C for every expert.
- * With p->expert_dtype == MOE_EXPERT_FP8_E4M3 every expert (routed and
- * shared) reads its E4M3 codes and row scales from `w` and the expert GEMMs
- * run on fp16 activations (see moe_expert_dtype_t).
+ * With p->expert_dtype == MOE_EXPERT_FP8_E4M3 (or MOE_EXPERT_MXFP4) every
+ * expert (routed and shared) reads its codes and scales from `w` and the
+ * expert GEMMs run on fp16 activations (see moe_expert_dtype_t).
  */
 moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
                                const void* hidden, void* out,

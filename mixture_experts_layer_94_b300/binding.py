@@ -23,7 +23,7 @@ CALL_PERMUTE, CALL_GROUPED_SWIGLU, CALL_LAYER_FORWARD, CALL_ROUTER = 0, 1, 2, 3
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DT_F32, DT_BF16 = 0, 1
 ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
-EXPERT_BF16, EXPERT_FP8_E4M3 = 0, 1
+EXPERT_BF16, EXPERT_FP8_E4M3, EXPERT_MXFP4 = 0, 1, 2
 MOE_ERR_RANGE = -7
 
 
@@ -67,6 +67,7 @@ def _load():
         "moe_permute": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_grouped_swiglu": ([pp] + [P] * 8 + [sz, P], i32),
         "moe_grouped_swiglu_fp8": ([pp] + [P] * 11 + [sz, P], i32),
+        "moe_grouped_swiglu_mxfp4": ([pp] + [P] * 11 + [sz, P], i32),
         "moe_combine": ([pp] + [P] * 6, i32),
         "moe_layer_forward": ([pp, ctypes.POINTER(Weights)] + [P] * 6 + [sz, P], i32),
         "moe_get_device_status": ([P, P], i32),
@@ -104,12 +105,14 @@ def _check(status: int, where: str) -> None:
 
 def problem(cfg: MoEConfig = None, **kw) -> Problem:
     """A moe_problem_t from a workload config (fields may be overridden)."""
-    f = dict(T=cfg.T, d_model=cfg.d, n_experts=cfg.N, top_k=cfg.K, ffn=cfg.F, n_shared=cfg.S,
-             shared_ffn=cfg.Fs, score_fn=cfg.score_fn, renormalize=cfg.renormalize,
-             hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16, n_groups=cfg.n_groups,
-             topk_groups=cfg.topk_groups, capacity_factor=cfg.capacity_factor,
-             routing=ROUTING_EXPERT_CHOICE if cfg.routing == "expert" else ROUTING_TOKEN_CHOICE,
-             expert_dtype=EXPERT_FP8_E4M3 if cfg.expert_dtype == "fp8" else EXPERT_BF16) if cfg else {}
+    f = {}
+    if cfg is not None:
+        f = dict(T=cfg.T, d_model=cfg.d, n_experts=cfg.N, top_k=cfg.K, ffn=cfg.F, n_shared=cfg.S,
+                 shared_ffn=cfg.Fs, score_fn=cfg.score_fn, renormalize=cfg.renormalize,
+                 hidden_dtype=DT_F32 if cfg.hidden_dtype == "f32" else DT_BF16, n_groups=cfg.n_groups,
+                 topk_groups=cfg.topk_groups, capacity_factor=cfg.capacity_factor,
+                 routing=ROUTING_EXPERT_CHOICE if cfg.routing == "expert" else ROUTING_TOKEN_CHOICE,
+                 expert_dtype={"fp8": EXPERT_FP8_E4M3, "mxfp4": EXPERT_MXFP4}.get(cfg.expert_dtype, EXPERT_BF16))
     f.update(kw)
     return Problem(**f)
 
@@ -190,6 +193,14 @@ def grouped_swiglu_fp8(p: Problem, x_perm, offsets, w_gate, w_gate_scale, w_up, 
                                       _p(w_up), _p(w_up_scale), _p(w_down), _p(w_down_scale), _p(h_perm),
                                       _p(y_perm), _p(ws), ws.numel(), _stream(stream)),
            "moe_grouped_swiglu_fp8")
+
+
+def grouped_swiglu_mxfp4(p: Problem, x_perm, offsets, w_gate, w_gate_bscale, w_up, w_up_bscale, w_down,
+                         w_down_bscale, h_perm, y_perm, ws, stream=None):
+    _check(lib.moe_grouped_swiglu_mxfp4(ctypes.byref(p), _p(x_perm), _p(offsets), _p(w_gate), _p(w_gate_bscale),
+                                        _p(w_up), _p(w_up_bscale), _p(w_down), _p(w_down_bscale), _p(h_perm),
+                                        _p(y_perm), _p(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_swiglu_mxfp4")
 
 
 def combine(p: Problem, y_perm, inv_row, topk_w, out, shared_out=None, stream=None):

@@ -38,6 +38,8 @@
 // the error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 
+#include <cuda_fp8.h>
+
 #include <atomic>
 
 #include "common.cuh"
@@ -76,6 +78,130 @@ __device__ __forceinline__ void pair_sum16(const uint32_t (&v)[32], int odd, flo
     const float send = __uint_as_float(odd ? v[j] : v[j + 16]);
     out[j] = mine + __shfl_xor_sync(0xffffffffu, send, 1);
   }
+}
+
+// The epilogue warps' loop over this CTA's tiles (warps 2-5, 128 threads):
+// tfull_bar(i) / tempty_bar(i) are the accumulator buffers' barriers.
+template <int PHASE, int EPI>
+__device__ __forceinline__ void epilogue_loop(const GemmArgs& a, int total, uint32_t tmem_base, uint32_t tbar0,
+                                              volatile int* abort_flag, int warp, int lane) {
+  auto tfull_bar = [&](int i) { return tbar0 + 8u * i; };
+  auto tempty_bar = [&](int i) { return tbar0 + 8u * (2 + i); };
+  // Lane pair (2t, 2t+1) of the warp holds token t's hi and lo products;
+  // after the pair sum the even lane finishes columns 0..15 of each 32-column
+  // chunk and the odd lane columns 16..31.
+  const int quad = warp & 3;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const int odd = lane & 1;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool over = false;
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    const TileInfo ti = decode_tile(tile, a);
+    const int kind = ti.g.kind;
+    if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
+    ptx::tc_fence_after();
+    const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
+    const int r_local = ti.m_blk * kF8TileRows + ((quad * 32 + lane) >> 1);  // token row in the group
+    const bool row_ok = r_local < ti.g.rows;
+    const int64_t a_idx = (int64_t)(PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + (row_ok ? r_local : 0);
+    const float sx = row_ok ? __ldg(a.a_scale[kind] + a_idx) : 0.f;
+    const int64_t wbase = (int64_t)ti.g.index * a.w_rows[kind];
+    if (PHASE == kPhaseGateUp) {
+      const int n_ext = a.n_ext[kind];
+      __half* hrow = reinterpret_cast<__half*>(a.h[kind]) + (int64_t)(ti.g.h_row0 + (row_ok ? r_local : 0)) * a.ldh[kind];
+      const float* sgp = a.w_scale[kind] + wbase;
+      const float* sup = a.u_scale[kind] + wbase;
+#pragma unroll 1
+      for (int c = 0; c < kBNGateUp / 32; ++c) {
+        uint32_t gv[32], uv[32];
+        ptx::tmem_ld_32x32b_x32(tacc + c * 32, gv);
+        ptx::tmem_ld_32x32b_x32(tacc + kBNGateUp + c * 32, uv);
+        ptx::tmem_wait_ld();
+        float g[16], u[16];
+        pair_sum16(gv, odd, g);
+        pair_sum16(uv, odd, u);
+        const int f0 = ti.n_blk * kBNGateUp + c * 32 + odd * 16;
+        if (row_ok && f0 < n_ext) {
+          uint32_t p[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 sg = __ldg(reinterpret_cast<const float4*>(sgp + f0 + 4 * q));
+            const float4 su = __ldg(reinterpret_cast<const float4*>(sup + f0 + 4 * q));
+            const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
+            float hv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float gg = g[4 * q + j] * sx * sgv[j];
+              const float uu = u[4 * q + j] * sx * suv[j];
+              hv[j] = silu_f(gg) * uu;
+              over |= fabsf(hv[j]) >= 65520.f;
+            }
+            p[2 * q] = pack_f16x2(hv[0], hv[1]);
+            p[2 * q + 1] = pack_f16x2(hv[2], hv[3]);
+          }
+          *reinterpret_cast<uint4*>(hrow + f0) = make_uint4(p[0], p[1], p[2], p[3]);
+          *reinterpret_cast<uint4*>(hrow + f0 + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+        }
+      }
+    } else {
+      const float* sdp = a.w_scale[kind] + wbase;
+      int64_t t = 0;
+      float w = 1.f;
+      if (EPI == kEpiScatter && row_ok) {
+        if (kind == 0 && a.row_w) {  // expert choice: the row's token and score
+          t = __ldg(a.perm_src + ti.g.h_row0 + r_local);
+          w = __ldg(a.row_w + ti.g.h_row0 + r_local);
+        } else if (kind == 0) {
+          const int32_t src = __ldg(a.perm_src + ti.g.h_row0 + r_local);
+          t = src / a.top_k;
+          w = __ldg(a.topk_w + src);
+        } else {
+          t = r_local;
+        }
+      }
+      const float ws = w * sx;
+#pragma unroll 1
+      for (int c = 0; c < kBNDown / 32; ++c) {
+        uint32_t yv[32];
+        ptx::tmem_ld_32x32b_x32(tacc + c * 32, yv);
+        ptx::tmem_wait_ld();
+        float y[16];
+        pair_sum16(yv, odd, y);
+        const int n0 = ti.n_blk * kBNDown + c * 32 + odd * 16;
+        if (row_ok && n0 < a.d) {
+          if (EPI == kEpiScatter) {
+            float* orow = a.out_acc + t * a.d + n0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 sd = __ldg(reinterpret_cast<const float4*>(sdp + n0 + 4 * q));
+              atomicAdd(reinterpret_cast<float4*>(orow + 4 * q),
+                        make_float4(ws * sd.x * y[4 * q], ws * sd.y * y[4 * q + 1], ws * sd.z * y[4 * q + 2],
+                                    ws * sd.w * y[4 * q + 3]));
+            }
+          } else {
+            __nv_bfloat16* yrow = a.y + (int64_t)(ti.g.h_row0 + r_local) * a.d + n0;
+            uint32_t p[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 sd = __ldg(reinterpret_cast<const float4*>(sdp + n0 + 4 * q));
+              p[2 * q] = pack_bf16x2(sx * sd.x * y[4 * q], sx * sd.y * y[4 * q + 1]);
+              p[2 * q + 1] = pack_bf16x2(sx * sd.z * y[4 * q + 2], sx * sd.w * y[4 * q + 3]);
+            }
+            *reinterpret_cast<uint4*>(yrow) = make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4*>(yrow + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+          }
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(tempty_bar(acc));
+    if (++acc == 2) {
+      acc = 0;
+      acc_phase ^= 1u;
+    }
+  }
+  if (over) atomicOr(a.err, kErrRange);
 }
 
 template <int PHASE, int EPI>
@@ -214,121 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Lane pair (2t, 2t+1) of the warp holds token t's hi and lo products;
-    // after the pair sum the even lane finishes columns 0..15 of each 32-column
-    // chunk and the odd lane columns 16..31.
-    const int quad = warp & 3;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int odd = lane & 1;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool over = false;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, a);
-      const int kind = ti.g.kind;
-      if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
-      ptx::tc_fence_after();
-      const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
-      const int r_local = ti.m_blk * kF8TileRows + ((quad * 32 + lane) >> 1);  // token row in the group
-      const bool row_ok = r_local < ti.g.rows;
-      const int64_t a_idx = (int64_t)(PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + (row_ok ? r_local : 0);
-      const float sx = row_ok ? __ldg(a.a_scale[kind] + a_idx) : 0.f;
-      const int64_t wbase = (int64_t)ti.g.index * a.w_rows[kind];
-      if (PHASE == kPhaseGateUp) {
-        const int n_ext = a.n_ext[kind];
-        __half* hrow = reinterpret_cast<__half*>(a.h[kind]) + (int64_t)(ti.g.h_row0 + (row_ok ? r_local : 0)) * a.ldh[kind];
-        const float* sgp = a.w_scale[kind] + wbase;
-        const float* sup = a.u_scale[kind] + wbase;
-#pragma unroll 1
-        for (int c = 0; c < kBNGateUp / 32; ++c) {
-          uint32_t gv[32], uv[32];
-          ptx::tmem_ld_32x32b_x32(tacc + c * 32, gv);
-          ptx::tmem_ld_32x32b_x32(tacc + kBNGateUp + c * 32, uv);
-          ptx::tmem_wait_ld();
-          float g[16], u[16];
-          pair_sum16(gv, odd, g);
-          pair_sum16(uv, odd, u);
-          const int f0 = ti.n_blk * kBNGateUp + c * 32 + odd * 16;
-          if (row_ok && f0 < n_ext) {
-            uint32_t p[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float4 sg = __ldg(reinterpret_cast<const float4*>(sgp + f0 + 4 * q));
-              const float4 su = __ldg(reinterpret_cast<const float4*>(sup + f0 + 4 * q));
-              const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
-              float hv[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float gg = g[4 * q + j] * sx * sgv[j];
-                const float uu = u[4 * q + j] * sx * suv[j];
-                hv[j] = silu_f(gg) * uu;
-                over |= fabsf(hv[j]) >= 65520.f;
-              }
-              p[2 * q] = pack_f16x2(hv[0], hv[1]);
-              p[2 * q + 1] = pack_f16x2(hv[2], hv[3]);
-            }
-            *reinterpret_cast<uint4*>(hrow + f0) = make_uint4(p[0], p[1], p[2], p[3]);
-            *reinterpret_cast<uint4*>(hrow + f0 + 8) = make_uint4(p[4], p[5], p[6], p[7]);
-          }
-        }
-      } else {
-        const float* sdp = a.w_scale[kind] + wbase;
-        int64_t t = 0;
-        float w = 1.f;
-        if (EPI == kEpiScatter && row_ok) {
-          if (kind == 0 && a.row_w) {  // expert choice: the row's token and score
-            t = __ldg(a.perm_src + ti.g.h_row0 + r_local);
-            w = __ldg(a.row_w + ti.g.h_row0 + r_local);
-          } else if (kind == 0) {
-            const int32_t src = __ldg(a.perm_src + ti.g.h_row0 + r_local);
-            t = src / a.top_k;
-            w = __ldg(a.topk_w + src);
-          } else {
-            t = r_local;
-          }
-        }
-        const float ws = w * sx;
-#pragma unroll 1
-        for (int c = 0; c < kBNDown / 32; ++c) {
-          uint32_t yv[32];
-          ptx::tmem_ld_32x32b_x32(tacc + c * 32, yv);
-          ptx::tmem_wait_ld();
-          float y[16];
-          pair_sum16(yv, odd, y);
-          const int n0 = ti.n_blk * kBNDown + c * 32 + odd * 16;
-          if (row_ok && n0 < a.d) {
-            if (EPI == kEpiScatter) {
-              float* orow = a.out_acc + t * a.d + n0;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 sd = __ldg(reinterpret_cast<const float4*>(sdp + n0 + 4 * q));
-                atomicAdd(reinterpret_cast<float4*>(orow + 4 * q),
-                          make_float4(ws * sd.x * y[4 * q], ws * sd.y * y[4 * q + 1], ws * sd.z * y[4 * q + 2],
-                                      ws * sd.w * y[4 * q + 3]));
-              }
-            } else {
-              __nv_bfloat16* yrow = a.y + (int64_t)(ti.g.h_row0 + r_local) * a.d + n0;
-              uint32_t p[8];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 sd = __ldg(reinterpret_cast<const float4*>(sdp + n0 + 4 * q));
-                p[2 * q] = pack_bf16x2(sx * sd.x * y[4 * q], sx * sd.y * y[4 * q + 1]);
-                p[2 * q + 1] = pack_bf16x2(sx * sd.z * y[4 * q + 2], sx * sd.w * y[4 * q + 3]);
-              }
-              *reinterpret_cast<uint4*>(yrow) = make_uint4(p[0], p[1], p[2], p[3]);
-              *reinterpret_cast<uint4*>(yrow + 8) = make_uint4(p[4], p[5], p[6], p[7]);
-            }
-          }
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty_bar(acc));
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-    if (over) atomicOr(a.err, kErrRange);
+    epilogue_loop<PHASE, EPI>(a, total, tmem_base, tfull_bar(0), abort_flag, warp, lane);
   }
 
   __syncthreads();
@@ -360,6 +372,365 @@ cudaError_t launch_t(const F8Maps& m, const GemmArgs& a, int64_t tile_bound, cud
   return cudaGetLastError();
 }
 
+// ============================================================================
+// MXFP4 experts. The expert matrices are E2M1 codes (two per byte, the even
+// element in the low nibble) with one E8M0 power-of-two scale per 32 elements
+// of a row (OCP microscaling), the format gpt-oss ships its experts in ("AI
+// Infrastructure series, Part 12 of 24", "How do you serve an MoE model on
+// your own GPUs?"). They reach the same 8-bit MMAs as FP8 experts:
+//  * TMA streams the packed codes (64 bytes = 128 elements of a row per
+//    stage, 64-byte swizzle) into a 4-stage ring; half the bytes of FP8.
+//  * Converter warps (one thread per weight row) rewrite each 32-element
+//    block as E4M3 codes of e2m1 * 2^(E_block - E_row): E_row is the row's
+//    reference exponent (its largest block exponent - 6, from
+//    mx_row_scale_kernel), so every block within 14 binades of the row's
+//    largest converts exactly (E4M3 spans 2^-9 .. 448; an E2M1 value has two
+//    significant bits); smaller blocks round to nearest. A block's eight
+//    magnitudes become one two-register table; one byte permute then converts
+//    four codes. The E4M3 rows go into a 3-stage ring in the 128-byte-swizzled
+//    K-major layout the MMA reads.
+//  * MMA and epilogue as for FP8 experts, with 2^(E_row - 127) as the weight
+//    row's scale.
+// Warps (480 threads): 0 TMA producer of the codes, 1 MMA, 2-5 epilogue,
+// 6-13 converters, 14 TMA producer of the token rows.
+
+constexpr int kMxConvWarps = 8;
+constexpr int kMxConv0 = 192;
+constexpr int kMxXWarp = kMxConv0 / 32 + kMxConvWarps;
+constexpr int kMxThreads = (kMxXWarp + 1) * 32;
+constexpr int kMxXStages = 4;
+constexpr int kMxRStages = 4;
+constexpr int kMxWStages = 3;
+constexpr uint32_t kMxRawBytes = (uint32_t)kWRows * (kKq / 2);  // 256 rows x 64 code bytes = 16 KB
+constexpr int kMxNumBars = 2 * (kMxXStages + kMxRStages + kMxWStages) + 5;
+constexpr size_t kMxBarrierBytes = 512;
+constexpr size_t kMxSmem = 1024 + (size_t)kMxXStages * kABytes + (size_t)kMxWStages * kBBytes +
+                           (size_t)kMxRStages * kMxRawBytes + kMxBarrierBytes;
+static_assert(8 * kMxNumBars + 8 <= kMxBarrierBytes, "barrier area");
+static_assert(kMxSmem <= 232448, "shared memory per CTA");
+
+// Eight E4M3 codes (as two table words) of the E2M1 magnitudes 0, 0.5, 1,
+// 1.5, 2, 3, 4, 6 times 2^k, rounded to nearest (exact for -8 <= k <= 6).
+__device__ __forceinline__ uint2 e2m1_table(int k) {
+  const float f = exp2f((float)k);
+  uint32_t b[8];
+  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = (uint32_t)__nv_cvt_float_to_fp8(mag[i] * f, __NV_SATFINITE, __NV_E4M3);
+  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// Four E2M1 codes (the low 16 bits of c, element i in nibble i) -> four E4M3
+// codes (byte i): the magnitude by table, the sign bit copied.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t c, uint2 tab) {
+  const uint32_t mag = __byte_perm(tab.x, tab.y, c & 0x7777u);
+  const uint32_t sgn = __byte_perm(0x8000u, 0u, (c >> 3) & 0x1111u);
+  return mag | sgn;
+}
+
+template <int PHASE, int EPI>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ F8Maps maps, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_base);
+  const uint32_t sX = base;                          // kMxXStages x 16 KB
+  const uint32_t sW = sX + kMxXStages * kABytes;     // kMxWStages x 32 KB
+  const uint32_t sRaw = sW + kMxWStages * kBBytes;   // kMxRStages x 16 KB
+  const uint32_t sBar = sRaw + kMxRStages * kMxRawBytes;
+  uint8_t* gW = gbase + (sW - base);
+  const uint8_t* gRaw = gbase + (sRaw - base);
+  uint8_t* gBar = gbase + (sBar - base);
+  auto xfull_bar = [&](int s) { return sBar + 8u * s; };
+  auto xempty_bar = [&](int s) { return sBar + 8u * (kMxXStages + s); };
+  auto rfull_bar = [&](int s) { return sBar + 8u * (2 * kMxXStages + s); };
+  auto rempty_bar = [&](int s) { return sBar + 8u * (2 * kMxXStages + kMxRStages + s); };
+  auto wfull_bar = [&](int s) { return sBar + 8u * (2 * (kMxXStages + kMxRStages) + s); };
+  auto wempty_bar = [&](int s) { return sBar + 8u * (2 * (kMxXStages + kMxRStages) + kMxWStages + s); };
+  constexpr int kT0 = 2 * (kMxXStages + kMxRStages + kMxWStages);
+  auto tfull_bar = [&](int i) { return sBar + 8u * (kT0 + i); };
+  auto tempty_bar = [&](int i) { return sBar + 8u * (kT0 + 2 + i); };
+  const uint32_t drain_bar = sBar + 8u * (kT0 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 8 * kMxNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * kMxNumBars + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = __ldg(a.tile_start + a.G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMxXStages; ++s) {
+      ptx::mbar_init(xfull_bar(s), 1);
+      ptx::mbar_init(xempty_bar(s), 1);
+    }
+    for (int s = 0; s < kMxRStages; ++s) {
+      ptx::mbar_init(rfull_bar(s), 1);
+      ptx::mbar_init(rempty_bar(s), kMxConvWarps);
+    }
+    for (int s = 0; s < kMxWStages; ++s) {
+      ptx::mbar_init(wfull_bar(s), kMxConvWarps);
+      ptx::mbar_init(wempty_bar(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(tfull_bar(i), 1);
+      ptx::mbar_init(tempty_bar(i), 128);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+    ptx::fence_proxy_async_shared();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&maps.w[0]);
+    if (PHASE == kPhaseGateUp) ptx::prefetch_tmap(&maps.u[0]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 || warp == kMxXWarp) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0: the packed codes (two 128-row boxes of 64 bytes per stage);
+    // warp kMxXWarp: the token rows.
+    if (lane == 0) {
+      const bool codes = warp == 0;
+      const int stages = codes ? kMxRStages : kMxXStages;
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, a);
+        const int kind = ti.g.kind;
+        const int bsel = box_sel(min(kF8TileRows, ti.g.rows - ti.m_blk * kF8TileRows));
+        const uint32_t xbytes = (16u << bsel) * kKq;
+        const CUtensorMap* mA = &maps.x[kind][bsel];
+        const CUtensorMap* mW = &maps.w[kind];
+        const CUtensorMap* mU = &maps.u[kind];
+        const int a_row = 2 * ((PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kF8TileRows);
+        const int w_row = ti.g.index * a.w_rows[kind] + ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
+        const int nkb = a.k_blocks[kind];
+        for (int kb = 0; kb < nkb; ++kb) {
+          const uint32_t full = codes ? rfull_bar(stage) : xfull_bar(stage);
+          const uint32_t empty = codes ? rempty_bar(stage) : xempty_bar(stage);
+          if (!ptx::mbar_wait(empty, phase ^ 1u, abort_flag, a.err)) {
+            aborted = true;
+            break;
+          }
+          if (codes) {
+            const uint32_t dR = sRaw + stage * kMxRawBytes;
+            ptx::mbar_arrive_expect_tx(full, kMxRawBytes);
+            ptx::tma_load_2d(dR, mW, full, kb * (kKq / 2), w_row);
+            if (PHASE == kPhaseGateUp) ptx::tma_load_2d(dR + kMxRawBytes / 2, mU, full, kb * (kKq / 2), w_row);
+            else ptx::tma_load_2d(dR + kMxRawBytes / 2, mW, full, kb * (kKq / 2), w_row + kWRows / 2);
+          } else {
+            ptx::mbar_arrive_expect_tx(full, xbytes);
+            ptx::tma_load_2d(sX + stage * kABytes, mA, full, kb * kKq, a_row);
+          }
+          ++issued;
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        const uint32_t n = issued < (uint32_t)stages ? issued : (uint32_t)stages;
+        for (uint32_t j = issued - n; j < issued; ++j) {
+          const int s = (int)(j % (uint32_t)stages);
+          wait_raw(codes ? rfull_bar(s) : xfull_bar(s), (j / (uint32_t)stages) & 1u, kDrainTimeoutNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int xs = 0, ws = 0, acc = 0;
+      uint32_t xphase = 0, wphase = 0, acc_phase = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+        const int nkb = a.k_blocks[decode_tile(tile, a).g.kind];
+        if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(wfull_bar(ws), wphase, abort_flag, a.err) ||
+              !ptx::mbar_wait(xfull_bar(xs), xphase, abort_flag, a.err)) {
+            aborted = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t adesc = ptx::smem_desc_sw128(sX + xs * kABytes);
+          const uint64_t bdesc = ptx::smem_desc_sw128(sW + ws * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kKq / 32; ++k)
+            ptx::mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          ptx::mma_commit(xempty_bar(xs));
+          ptx::mma_commit(wempty_bar(ws));
+          if (++xs == kMxXStages) {
+            xs = 0;
+            xphase ^= 1u;
+          }
+          if (++ws == kMxWStages) {
+            ws = 0;
+            wphase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        ptx::mma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      ptx::mma_commit(drain_bar);
+      wait_raw(drain_bar, 0, kWaitTimeoutNs);
+    }
+    __syncwarp();
+  } else if (threadIdx.x >= kMxConv0) {
+    // ------------------------------------------------------------ converters
+    // Thread R owns weight row R of the tile (rows 0..127: W_gate or the first
+    // 128 W_down rows; 128..255: W_up or the next 128). Per stage it reads the
+    // row's 64 code bytes (chunk c of the 64-byte-swizzled box row at
+    // c ^ ((R >> 1) & 3)) and the four block scales of those 128 elements,
+    // and writes the row's 128 E4M3 codes: chunk j at j ^ (R & 7) of the
+    // 128-byte-swizzled weight tile.
+    const int R = threadIdx.x - kMxConv0;
+    const int rsw = (R >> 1) & 3, wsw = R & 7;
+    int rs = 0, ws = 0;
+    uint32_t rphase = 0, wphase = 0;
+    bool aborted = false;
+    for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, a);
+      const int kind = ti.g.kind;
+      const int nkb = a.k_blocks[kind];
+      const int nblk = a.k_len[kind] / 32;  // block scales per row
+      const int64_t q_row = (int64_t)ti.g.index * a.w_rows[kind] +
+                            (int64_t)ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown) +
+                            (PHASE == kPhaseGateUp ? (R & 127) : R);
+      const bool row_ok = q_row < a.q_rows[kind];
+      const uint8_t* bs = ((PHASE == kPhaseGateUp && R >= 128) ? a.ub_scale[kind] : a.wb_scale[kind]) +
+                          (row_ok ? q_row : 0) * (int64_t)nblk;
+      const float* rsp = (PHASE == kPhaseGateUp && R >= 128) ? a.u_scale[kind] : a.w_scale[kind];
+      // The row's reference exponent: the biased exponent of its scale 2^(E_row - 127).
+      const int e_row = row_ok ? (int)((__float_as_uint(__ldg(rsp + q_row)) >> 23) & 255u) : 127;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!ptx::mbar_wait(rfull_bar(rs), rphase, abort_flag, a.err)) {
+          aborted = true;
+          break;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(gRaw + rs * kMxRawBytes + R * (kKq / 2));
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = src[c ^ rsw];
+        // Chunk c (16 code bytes = 32 elements) is exactly block 4*kb + c.
+        uint4 o[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int blk = 4 * kb + c;
+          const int eb = (row_ok && blk < nblk) ? (int)__ldg(bs + blk) : e_row;
+          const uint2 tab = e2m1_table(eb - e_row);
+          const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+          uint32_t r8[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            r8[2 * q] = e2m1x4_to_e4m3x4(w4[q], tab);
+            r8[2 * q + 1] = e2m1x4_to_e4m3x4(w4[q] >> 16, tab);
+          }
+          o[2 * c] = make_uint4(r8[0], r8[1], r8[2], r8[3]);
+          o[2 * c + 1] = make_uint4(r8[4], r8[5], r8[6], r8[7]);
+        }
+        // The code slot may be refilled only once every lane's loads have
+        // returned: the conversion above consumed all of them.
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(rempty_bar(rs));
+        if (++rs == kMxRStages) {
+          rs = 0;
+          rphase ^= 1u;
+        }
+        if (!ptx::mbar_wait(wempty_bar(ws), wphase ^ 1u, abort_flag, a.err)) {
+          aborted = true;
+          break;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(gW + ws * kBBytes + R * kKq);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j ^ wsw] = o[j];
+        ptx::fence_proxy_async_shared();  // generic-proxy writes -> the MMA's async-proxy reads
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(wfull_bar(ws));
+        if (++ws == kMxWStages) {
+          ws = 0;
+          wphase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    epilogue_loop<PHASE, EPI>(a, total, tmem_base, tfull_bar(0), abort_flag, warp, lane);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// The reference exponent of every weight row of the experts in use: E_row =
+// (largest E8M0 block exponent of the row, NaN scales aside) - 6, clamped to
+// 1..254; the row's scale 2^(E_row - 127) is written as fp32. A warp per row,
+// grid-stride; rows of experts with no routed rows are skipped.
+__global__ void __launch_bounds__(256) mx_row_scale_kernel(const uint8_t* __restrict__ bscale, int64_t rows,
+                                                          int32_t rows_per_expert, int32_t nblk,
+                                                          const int32_t* __restrict__ offsets,
+                                                          float* __restrict__ row_scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = warp0; r < rows; r += nwarps) {
+    if (offsets) {
+      const int64_t e = r / rows_per_expert;
+      if (__ldg(offsets + e + 1) == __ldg(offsets + e)) continue;
+    }
+    const uint8_t* p = bscale + r * (int64_t)nblk;
+    int m = 0;
+    for (int j = lane; j < nblk; j += 32) {
+      const int v = __ldg(p + j);
+      if (v != 255) m = max(m, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) row_scale[r] = __uint_as_float((uint32_t)min(max(m - 6, 1), 254) << 23);
+  }
+}
+
+template <int PHASE, int EPI>
+cudaError_t launch_mx(const F8Maps& m, const GemmArgs& a, int64_t tile_bound, cudaStream_t s) {
+  auto kern = grouped_gemm_mx_kernel<PHASE, EPI>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMxSmem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int64_t grid = sms;
+  if (tile_bound < grid) grid = tile_bound < 1 ? 1 : tile_bound;
+  kern<<<(unsigned)grid, kMxThreads, kMxSmem, s>>>(m, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_grouped_gemm_fp8(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
@@ -367,6 +738,24 @@ cudaError_t launch_grouped_gemm_fp8(int phase, int epilogue, const F8Maps& maps,
   if (phase == kPhaseGateUp) return launch_t<kPhaseGateUp, kEpiSwiGLU>(maps, a, tile_bound, s);
   if (epilogue == kEpiScatter) return launch_t<kPhaseDown, kEpiScatter>(maps, a, tile_bound, s);
   return launch_t<kPhaseDown, kEpiStoreY>(maps, a, tile_bound, s);
+}
+
+cudaError_t launch_grouped_gemm_mxfp4(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
+                                      int64_t tile_bound, cudaStream_t s) {
+  if (phase == kPhaseGateUp) return launch_mx<kPhaseGateUp, kEpiSwiGLU>(maps, a, tile_bound, s);
+  if (epilogue == kEpiScatter) return launch_mx<kPhaseDown, kEpiScatter>(maps, a, tile_bound, s);
+  return launch_mx<kPhaseDown, kEpiStoreY>(maps, a, tile_bound, s);
+}
+
+cudaError_t launch_mx_row_scale(const uint8_t* bscale, int64_t rows, int32_t rows_per_expert, int32_t nblk,
+                                const int32_t* offsets, float* row_scale, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (rows + 7) / 8;
+  const unsigned grid = (unsigned)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
+  mx_row_scale_kernel<<<grid, 256, 0, s>>>(bscale, rows, rows_per_expert, nblk, offsets, row_scale);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -124,9 +124,17 @@ struct GemmArgs {
   // of W_down).
   const float* w_scale[2];
   const float* u_scale[2];
-  // FP8 experts: the scale of each activation row, per kind (the token rows
-  // of the gate/up phase, the h rows of the down phase).
+  // FP8 / MXFP4 experts: the scale of each activation row, per kind (the
+  // token rows of the gate/up phase, the h rows of the down phase).
   const float* a_scale[2];
+  // MXFP4 experts: E8M0 block scales of the code matrices (w: gate or down,
+  // u: up) [rows][k_len / 32], the code rows' length in elements and the
+  // matrices' row counts, per kind. w_scale / u_scale then hold each row's
+  // reference scale 2^(E_row - 127).
+  const uint8_t* wb_scale[2];
+  const uint8_t* ub_scale[2];
+  int32_t k_len[2];
+  int64_t q_rows[2];
   // Router phase: one group of all T tokens; tile = (m block, split) with
   // split = part * r_dslices + slice.
   int32_t r_tiles, r_m_tiles, r_dslices, r_kb_per_slice, r_nkb_d, r_d_pad, r_np, r_N;
@@ -172,6 +180,17 @@ bool make_tmap_f16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t row
 // kF8TileRows), one CTA each.
 cudaError_t launch_grouped_gemm_fp8(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
                                     int64_t tile_bound, cudaStream_t s);
+// The same GEMMs for MXFP4 experts: F8Maps::w / u map the packed code
+// matrices ([rows][K/2] bytes, 128-row boxes of 64 bytes, 64-byte swizzle).
+cudaError_t launch_grouped_gemm_mxfp4(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
+                                      int64_t tile_bound, cudaStream_t s);
+// Reference scales 2^(E_row - 127) of MXFP4 weight rows: E_row = the row's
+// largest E8M0 block exponent - 6 (clamped to 1..254). Rows of experts whose
+// offsets show no routed rows are skipped (offsets may be NULL: all rows).
+cudaError_t launch_mx_row_scale(const uint8_t* bscale, int64_t rows, int32_t rows_per_expert, int32_t nblk,
+                                const int32_t* offsets, float* row_scale, cudaStream_t s);
+// uint8 matrix [rows][inner] with a box of [box_rows][64 bytes], 64-byte swizzle.
+bool make_tmap_u8_64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
 // Upper bound on the tile count (host, from sizes only), used for the grid.
 int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T,

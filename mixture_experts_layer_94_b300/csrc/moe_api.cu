@@ -21,7 +21,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc;
-  size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 experts: two-term E4M3 activations + row scales
+  size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 / MXFP4 experts: two-term E4M3 activations + row scales
+  size_t rs_gate, rs_up, rs_down, rs_sgate, rs_sup, rs_sdown;  // MXFP4 experts: weight rows' reference scales
   size_t total;
 };
 
@@ -34,12 +35,16 @@ int64_t ec_capacity(const moe_problem_t& p) {
 }
 
 bool is_fp8(const moe_problem_t& p) { return p.expert_dtype == MOE_EXPERT_FP8_E4M3; }
+bool is_mx(const moe_problem_t& p) { return p.expert_dtype == MOE_EXPERT_MXFP4; }
+// FP8 and MXFP4 experts both run on the 8-bit tensor path (fp16 activations
+// between calls, two-term E4M3 activations inside the GEMMs).
+bool is_lowp(const moe_problem_t& p) { return is_fp8(p) || is_mx(p); }
 
 // The shared experts read every token's hidden row in the activation format
 // (bf16 for bf16 experts, fp16 for FP8 experts): a copy unless hidden is
 // already in it.
 bool needs_act_copy(const moe_problem_t& p) {
-  return p.n_shared > 0 && (is_fp8(p) || p.hidden_dtype == MOE_F32);
+  return p.n_shared > 0 && (is_lowp(p) || p.hidden_dtype == MOE_F32);
 }
 
 Layout make_layout(const moe_problem_t& p, int call) {
@@ -70,7 +75,17 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.ec_token = take((size_t)ec_rows * 4);
     L.ec_w = take((size_t)ec_rows * 4);
   }
-  if (is_fp8(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU)) {
+  if (is_mx(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU)) {
+    L.rs_gate = take((size_t)p.n_experts * p.ffn * 4);
+    L.rs_up = take((size_t)p.n_experts * p.ffn * 4);
+    L.rs_down = take((size_t)p.n_experts * p.d_model * 4);
+    if (call == MOE_CALL_LAYER_FORWARD && p.n_shared > 0) {
+      L.rs_sgate = take((size_t)p.n_shared * p.shared_ffn * 4);
+      L.rs_sup = take((size_t)p.n_shared * p.shared_ffn * 4);
+      L.rs_sdown = take((size_t)p.n_shared * p.d_model * 4);
+    }
+  }
+  if (is_lowp(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU)) {
     L.xq = take((size_t)2 * rows * p.d_model);
     L.sx = take((size_t)rows * 4);
     L.hq = take((size_t)2 * rows * p.ffn);
@@ -176,6 +191,20 @@ bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// uint8 matrix [rows][inner], box [box_rows][64 bytes], 64-byte swizzle (the
+// 16-byte chunk c of box row R lands at chunk c ^ ((R >> 1) & 3)), zero fill
+// out of bounds.
+bool make_tmap_u8_64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  if (!have_encode() || (inner % 16) != 0) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace moe
 
 namespace {
@@ -210,13 +239,14 @@ int32_t gemm_pair(int64_t routed_rows, int32_t N) { return routed_rows >= (int64
 // Rows per tile of the GEMM schedule: 128 (single CTAs) or 256 (CTA pairs)
 // for bf16 experts, kF8TileRows tokens for the FP8-weight kernel.
 int32_t gemm_tile_rows(const moe_problem_t& p, int64_t routed_rows) {
-  return is_fp8(p) ? kF8TileRows : kBM * gemm_pair(routed_rows, p.n_experts);
+  return is_lowp(p) ? kF8TileRows : kBM * gemm_pair(routed_rows, p.n_experts);
 }
 
 // The two GEMM phases over groups already described in the workspace.
 struct GemmPlan {
   int32_t pair;
-  bool fp8;               // FP8 E4M3 weights (+ the row scales below), fp16 activations
+  bool fp8;               // FP8 or MXFP4 weights (+ the scales below), fp16 activations
+  bool mx;                // MXFP4: *_scale are E8M0 block scales; rs_* the rows' reference scales
   int32_t N, S, F, Fs, d, K;
   int64_t T, routed_rows;
   const void* x_routed;   // [routed_rows][d] bf16
@@ -227,12 +257,19 @@ struct GemmPlan {
   const void* sg;         // [S][Fs][d]
   const void* su;
   const void* sd;         // [S][d][Fs]
-  const float* wg_scale;  // FP8: [N][F], [N][F], [N][d]
-  const float* wu_scale;
-  const float* wd_scale;
-  const float* sg_scale;  // FP8: [S][Fs], [S][Fs], [S][d]
-  const float* su_scale;
-  const float* sd_scale;
+  const void* wg_scale;   // FP8: fp32 [N][F], [N][F], [N][d]; MXFP4: E8M0 [N][F][d/32], [N][F][d/32], [N][d][F/32]
+  const void* wu_scale;
+  const void* wd_scale;
+  const void* sg_scale;   // the same for the shared experts
+  const void* su_scale;
+  const void* sd_scale;
+  float* rs_gate;         // MXFP4: reference scale of each weight row, [N][F], [N][F], [N][d]
+  float* rs_up;
+  float* rs_down;
+  float* rs_sgate;        // shared: [S][Fs], [S][Fs], [S][d]
+  float* rs_sup;
+  float* rs_sdown;
+  const int32_t* offsets; // MXFP4: routed rows per expert (experts without rows are skipped)
   __nv_bfloat16* h;       // [routed_rows][F] (fp16 bits when fp8)
   __nv_bfloat16* h_sh;    // [S*T][Fs] (fp16 bits when fp8)
   uint8_t* xq;            // FP8: two-term E4M3 activations [2 rows][K] and their row scales
@@ -347,27 +384,50 @@ bool make_x_maps(CUtensorMap (&m)[kF8XBoxes], const void* ptr, uint64_t inner, u
   return true;
 }
 
-// The two GEMM phases for FP8 E4M3 experts: each phase's activations are
-// first split into two-term E4M3 rows (act_quant.cu).
+// The code maps of one weight matrix: FP8 rows of K bytes in 128-byte boxes,
+// MXFP4 rows of K/2 bytes in 64-byte boxes; 128 rows per box.
+bool make_code_map(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, bool mx) {
+  return mx ? make_tmap_u8_64(m, ptr, K / 2, rows, 128) : make_tmap_u8(m, ptr, K, rows, 128);
+}
+
+// The two GEMM phases for FP8 or MXFP4 experts: each phase's activations are
+// first split into two-term E4M3 rows (act_quant.cu); MXFP4 weight rows first
+// get their reference scales (mx_row_scale_kernel).
 moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup) {
   if (!have_encode()) return MOE_ERR_CUDA;
-  const bool sh = g.S > 0;
+  const bool sh = g.S > 0, mx = g.mx;
+  auto f32 = [](const void* p) { return static_cast<const float*>(p); };
+  auto u8 = [](const void* p) { return static_cast<const uint8_t*>(p); };
+  if (mx) {
+    MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.wg_scale), (int64_t)g.N * g.F, g.F, g.d / 32, g.offsets, g.rs_gate, s)));
+    MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.wu_scale), (int64_t)g.N * g.F, g.F, g.d / 32, g.offsets, g.rs_up, s)));
+    MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.wd_scale), (int64_t)g.N * g.d, g.d, g.F / 32, g.offsets, g.rs_down, s)));
+    if (sh) {
+      MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.sg_scale), (int64_t)g.S * g.Fs, g.Fs, g.d / 32, nullptr, g.rs_sgate, s)));
+      MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.su_scale), (int64_t)g.S * g.Fs, g.Fs, g.d / 32, nullptr, g.rs_sup, s)));
+      MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.sd_scale), (int64_t)g.S * g.d, g.d, g.Fs / 32, nullptr, g.rs_sdown, s)));
+    }
+  }
   MOE_TRY(cuda_status(launch_act_quant(g.x_routed, g.routed_rows, g.d, g.xq, g.sx, s)));
   if (sh) MOE_TRY(cuda_status(launch_act_quant(g.x_shared, g.T, g.d, g.xq_sh, g.sx_sh, s)));
   F8Maps m{};
   bool ok = make_x_maps(m.x[0], g.xq, g.d, 2 * (uint64_t)g.routed_rows) &&
-            make_tmap_u8(&m.w[0], g.wg, g.d, (uint64_t)g.N * g.F, 128) &&
-            make_tmap_u8(&m.u[0], g.wu, g.d, (uint64_t)g.N * g.F, 128);
+            make_code_map(&m.w[0], g.wg, g.d, (uint64_t)g.N * g.F, mx) &&
+            make_code_map(&m.u[0], g.wu, g.d, (uint64_t)g.N * g.F, mx);
   if (ok && sh)
     ok = make_x_maps(m.x[1], g.xq_sh, g.d, 2 * (uint64_t)g.T) &&
-         make_tmap_u8(&m.w[1], g.sg, g.d, (uint64_t)g.S * g.Fs, 128) &&
-         make_tmap_u8(&m.u[1], g.su, g.d, (uint64_t)g.S * g.Fs, 128);
+         make_code_map(&m.w[1], g.sg, g.d, (uint64_t)g.S * g.Fs, mx) &&
+         make_code_map(&m.u[1], g.su, g.d, (uint64_t)g.S * g.Fs, mx);
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
     for (int i = 0; i < kF8XBoxes; ++i) m.x[1][i] = m.x[0][i];
     m.w[1] = m.w[0];
     m.u[1] = m.u[0];
   }
+  auto launch = [&](int phase, int epi, const F8Maps& maps, const GemmArgs& args, int64_t bound) {
+    return mx ? launch_grouped_gemm_mxfp4(phase, epi, maps, args, bound, s)
+              : launch_grouped_gemm_fp8(phase, epi, maps, args, bound, s);
+  };
   GemmArgs a{};
   a.groups = g.groups;
   a.G = g.N + g.S;
@@ -386,14 +446,28 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.h[1] = sh ? g.h_sh : g.h;
   a.ldh[0] = g.F;
   a.ldh[1] = sh ? g.Fs : g.F;
-  a.w_scale[0] = g.wg_scale;
-  a.u_scale[0] = g.wu_scale;
-  a.w_scale[1] = sh ? g.sg_scale : g.wg_scale;
-  a.u_scale[1] = sh ? g.su_scale : g.wu_scale;
+  if (mx) {
+    a.w_scale[0] = g.rs_gate;
+    a.u_scale[0] = g.rs_up;
+    a.w_scale[1] = sh ? g.rs_sgate : g.rs_gate;
+    a.u_scale[1] = sh ? g.rs_sup : g.rs_up;
+    a.wb_scale[0] = u8(g.wg_scale);
+    a.ub_scale[0] = u8(g.wu_scale);
+    a.wb_scale[1] = sh ? u8(g.sg_scale) : a.wb_scale[0];
+    a.ub_scale[1] = sh ? u8(g.su_scale) : a.ub_scale[0];
+  } else {
+    a.w_scale[0] = f32(g.wg_scale);
+    a.u_scale[0] = f32(g.wu_scale);
+    a.w_scale[1] = sh ? f32(g.sg_scale) : a.w_scale[0];
+    a.u_scale[1] = sh ? f32(g.su_scale) : a.u_scale[0];
+  }
+  a.k_len[0] = a.k_len[1] = g.d;
+  a.q_rows[0] = (int64_t)g.N * g.F;
+  a.q_rows[1] = sh ? (int64_t)g.S * g.Fs : a.q_rows[0];
   a.a_scale[0] = g.sx;
   a.a_scale[1] = sh ? g.sx_sh : g.sx;
   int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kF8TileRows);
-  MOE_TRY(cuda_status(launch_grouped_gemm_fp8(kPhaseGateUp, kEpiSwiGLU, m, a, bound, s)));
+  MOE_TRY(cuda_status(launch(kPhaseGateUp, kEpiSwiGLU, m, a, bound)));
   if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[0], s)));
 
   // down (+ weighted scatter-add or plain store)
@@ -401,10 +475,10 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   if (sh) MOE_TRY(cuda_status(launch_act_quant(g.h_sh, (int64_t)g.S * g.T, g.Fs, g.hq_sh, g.sh_sh, s)));
   F8Maps md{};
   ok = make_x_maps(md.x[0], g.hq, g.F, 2 * (uint64_t)g.routed_rows) &&
-       make_tmap_u8(&md.w[0], g.wd, g.F, (uint64_t)g.N * g.d, 128);
+       make_code_map(&md.w[0], g.wd, g.F, (uint64_t)g.N * g.d, mx);
   if (ok && sh)
     ok = make_x_maps(md.x[1], g.hq_sh, g.Fs, 2 * (uint64_t)g.S * g.T) &&
-         make_tmap_u8(&md.w[1], g.sd, g.Fs, (uint64_t)g.S * g.d, 128);
+         make_code_map(&md.w[1], g.sd, g.Fs, (uint64_t)g.S * g.d, mx);
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
     for (int i = 0; i < kF8XBoxes; ++i) md.x[1][i] = md.x[0][i];
@@ -417,9 +491,21 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.k_blocks[0] = (g.F + 127) / 128;
   a.k_blocks[1] = sh ? (g.Fs + 127) / 128 : a.k_blocks[0];
   a.w_rows[0] = a.w_rows[1] = g.d;
-  a.w_scale[0] = g.wd_scale;
-  a.w_scale[1] = sh ? g.sd_scale : g.wd_scale;
+  if (mx) {
+    a.w_scale[0] = g.rs_down;
+    a.w_scale[1] = sh ? g.rs_sdown : g.rs_down;
+    a.wb_scale[0] = u8(g.wd_scale);
+    a.wb_scale[1] = sh ? u8(g.sd_scale) : a.wb_scale[0];
+  } else {
+    a.w_scale[0] = f32(g.wd_scale);
+    a.w_scale[1] = sh ? f32(g.sd_scale) : a.w_scale[0];
+  }
   a.u_scale[0] = a.u_scale[1] = nullptr;
+  a.ub_scale[0] = a.ub_scale[1] = nullptr;
+  a.k_len[0] = g.F;
+  a.k_len[1] = sh ? g.Fs : g.F;
+  a.q_rows[0] = (int64_t)g.N * g.d;
+  a.q_rows[1] = sh ? (int64_t)g.S * g.d : a.q_rows[0];
   a.a_scale[0] = g.sh;
   a.a_scale[1] = sh ? g.sh_sh : g.sh;
   a.out_acc = g.out_acc;
@@ -428,7 +514,7 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.row_w = g.row_w;
   a.y = g.y;
   bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kF8TileRows);
-  MOE_TRY(cuda_status(launch_grouped_gemm_fp8(kPhaseDown, g.epilogue, md, a, bound, s)));
+  MOE_TRY(cuda_status(launch(kPhaseDown, g.epilogue, md, a, bound)));
   if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[1], s)));
   return MOE_OK;
 }
@@ -446,7 +532,7 @@ const char* moe_status_string(int32_t status) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device pipeline wait timed out";
     case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS: an input index was out of range";
-    case MOE_ERR_RANGE: return "MOE_ERR_RANGE: an fp16 activation of the FP8-weight path overflowed";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE: an fp16 activation of the FP8 / MXFP4 path overflowed";
     default: return "MOE_ERR_UNKNOWN: unrecognised status";
   }
 }
@@ -465,7 +551,13 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (!(p->capacity_factor >= 0.0) || p->capacity_factor > 1e30) return MOE_ERR_INVALID_ARG;  // NaN fails too
   if (p->routing != MOE_ROUTING_TOKEN_CHOICE && p->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE && p->n_groups > 1) return MOE_ERR_UNSUPPORTED;
-  if (p->expert_dtype != MOE_EXPERT_BF16 && p->expert_dtype != MOE_EXPERT_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+  if (p->expert_dtype != MOE_EXPERT_BF16 && p->expert_dtype != MOE_EXPERT_FP8_E4M3 &&
+      p->expert_dtype != MOE_EXPERT_MXFP4)
+    return MOE_ERR_INVALID_ARG;
+  if (p->expert_dtype == MOE_EXPERT_MXFP4) {  // 32-element scale blocks; code rows in 16-byte units
+    if ((p->d_model % 32) != 0 || (p->ffn % 32) != 0) return MOE_ERR_INVALID_ARG;
+    if (p->n_shared > 0 && (p->shared_ffn % 32) != 0) return MOE_ERR_INVALID_ARG;
+  }
   if (p->expert_dtype == MOE_EXPERT_FP8_E4M3) {  // 16-byte rows of codes for the TMA boxes
     if ((p->d_model % 16) != 0 || (p->ffn % 16) != 0) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && (p->shared_ffn % 16) != 0) return MOE_ERR_INVALID_ARG;
@@ -551,7 +643,7 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx, const 
   a.perm_src = perm_src;
   a.inv_row = inv_row;
   a.x_perm = x_perm;
-  a.act_f16 = is_fp8(*p);
+  a.act_f16 = is_lowp(*p);
   a.err = at<uint32_t>(ws, L.err);
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
@@ -560,14 +652,22 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx, const 
 
 namespace {
 
+// The scale arrays a low-precision expert format needs: fp32 row scales
+// (16-byte aligned) for FP8, E8M0 block-scale bytes for MXFP4.
+bool scales_ok(const moe_problem_t& p, const void* a, const void* b, const void* c) {
+  if (!is_lowp(p)) return true;
+  if (!a || !b || !c) return false;
+  return is_mx(p) || (aligned16(a) && aligned16(b) && aligned16(c));
+}
+
 moe_status_t grouped_swiglu_impl(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
-                                 const void* w_gate, const float* sg, const void* w_up, const float* su,
-                                 const void* w_down, const float* sd, void* h_perm, void* y_perm, void* ws,
+                                 const void* w_gate, const void* sg, const void* w_up, const void* su,
+                                 const void* w_down, const void* sd, void* h_perm, void* y_perm, void* ws,
                                  size_t ws_bytes, void* stream) {
   MOE_TRY(moe_problem_check(p));
-  const bool fp8 = is_fp8(*p);
+  const bool fp8 = is_lowp(*p);
   if (!offsets || !w_gate || !w_up || !w_down) return MOE_ERR_INVALID_ARG;
-  if (fp8 && (!sg || !su || !sd || !aligned16(sg) || !aligned16(su) || !aligned16(sd))) return MOE_ERR_INVALID_ARG;
+  if (!scales_ok(*p, sg, su, sd)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down)) return MOE_ERR_INVALID_ARG;
   // packed rows: T*K copies (token choice) or N*C picks (expert choice)
   const int64_t rows =
@@ -588,14 +688,21 @@ moe_status_t grouped_swiglu_impl(const moe_problem_t* p, const void* x_perm, con
   GemmPlan g{};
   g.pair = pair;
   g.fp8 = fp8;
+  g.mx = is_mx(q);
   g.wg_scale = sg;
   g.wu_scale = su;
   g.wd_scale = sd;
+  g.offsets = offsets;
   if (fp8) {
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
     g.hq = at<uint8_t>(ws, L.hq);
     g.sh = at<float>(ws, L.sh);
+  }
+  if (g.mx) {
+    g.rs_gate = at<float>(ws, L.rs_gate);
+    g.rs_up = at<float>(ws, L.rs_up);
+    g.rs_down = at<float>(ws, L.rs_down);
   }
   g.N = q.n_experts;
   g.S = 0;
@@ -626,7 +733,7 @@ extern "C" {
 moe_status_t moe_grouped_swiglu(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
                                 const void* w_gate, const void* w_up, const void* w_down, void* h_perm,
                                 void* y_perm, void* ws, size_t ws_bytes, void* stream) {
-  if (p && is_fp8(*p)) return MOE_ERR_INVALID_ARG;
+  if (p && is_lowp(*p)) return MOE_ERR_INVALID_ARG;
   return grouped_swiglu_impl(p, x_perm, offsets, w_gate, nullptr, w_up, nullptr, w_down, nullptr, h_perm, y_perm,
                              ws, ws_bytes, stream);
 }
@@ -638,6 +745,15 @@ moe_status_t moe_grouped_swiglu_fp8(const moe_problem_t* p, const void* x_perm, 
   if (p && !is_fp8(*p)) return MOE_ERR_INVALID_ARG;
   return grouped_swiglu_impl(p, x_perm, offsets, w_gate, w_gate_scale, w_up, w_up_scale, w_down, w_down_scale,
                              h_perm, y_perm, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_grouped_swiglu_mxfp4(const moe_problem_t* p, const void* x_perm, const int32_t* offsets,
+                                      const void* w_gate, const void* w_gate_bscale, const void* w_up,
+                                      const void* w_up_bscale, const void* w_down, const void* w_down_bscale,
+                                      void* h_perm, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (p && !is_mx(*p)) return MOE_ERR_INVALID_ARG;
+  return grouped_swiglu_impl(p, x_perm, offsets, w_gate, w_gate_bscale, w_up, w_up_bscale, w_down,
+                             w_down_bscale, h_perm, y_perm, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm, const int32_t* inv_row, const float* topk_w,
@@ -670,17 +786,10 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   if (p->n_shared > 0 && (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)))
     return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && (!hidden || !out || !aligned16(hidden) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
-  const bool fp8 = is_fp8(*p);
-  if (fp8) {
-    const float* sc[3] = {w->w_gate_scale, w->w_up_scale, w->w_down_scale};
-    for (const float* q : sc)
-      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
-    if (p->n_shared > 0) {
-      const float* ss[3] = {w->ws_gate_scale, w->ws_up_scale, w->ws_down_scale};
-      for (const float* q : ss)
-        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
-    }
-  }
+  const bool fp8 = is_lowp(*p);
+  if (!scales_ok(*p, w->w_gate_scale, w->w_up_scale, w->w_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (p->n_shared > 0 && !scales_ok(*p, w->ws_gate_scale, w->ws_up_scale, w->ws_down_scale))
+    return MOE_ERR_INVALID_ARG;
   Layout L;
   MOE_TRY(check_ws(p, MOE_CALL_LAYER_FORWARD, ws, ws_bytes, &L));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -772,6 +881,18 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.sg_scale = w->ws_gate_scale;
   g.su_scale = w->ws_up_scale;
   g.sd_scale = w->ws_down_scale;
+  g.mx = is_mx(*p);
+  g.offsets = offsets;
+  if (g.mx) {
+    g.rs_gate = at<float>(ws, L.rs_gate);
+    g.rs_up = at<float>(ws, L.rs_up);
+    g.rs_down = at<float>(ws, L.rs_down);
+    if (S > 0) {
+      g.rs_sgate = at<float>(ws, L.rs_sgate);
+      g.rs_sup = at<float>(ws, L.rs_sup);
+      g.rs_sdown = at<float>(ws, L.rs_sdown);
+    }
+  }
   if (fp8) {
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
@@ -870,6 +991,18 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.sg_scale = w->ws_gate_scale;
   g.su_scale = w->ws_up_scale;
   g.sd_scale = w->ws_down_scale;
+  g.mx = is_mx(*p);
+  g.offsets = offsets;
+  if (g.mx) {
+    g.rs_gate = at<float>(ws, L.rs_gate);
+    g.rs_up = at<float>(ws, L.rs_up);
+    g.rs_down = at<float>(ws, L.rs_down);
+    if (S > 0) {
+      g.rs_sgate = at<float>(ws, L.rs_sgate);
+      g.rs_sup = at<float>(ws, L.rs_sup);
+      g.rs_sdown = at<float>(ws, L.rs_sdown);
+    }
+  }
   if (fp8) {
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
@@ -930,7 +1063,9 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   const int router = router_plan(p->T, p->d_model, p->n_experts, p->hidden_dtype == MOE_BF16).tensor ? 3 : 2;
   // FP8 experts: the two-term E4M3 split of each GEMM's activations (x, h;
   // and the shared experts' x, h)
-  const int quant = is_fp8(*p) ? (p->n_shared > 0 ? 4 : 2) : 0;
+  // (+ MXFP4: the reference scales of gate, up and down rows, and the
+  // shared experts')
+  const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 4 : 2) : 0) + (is_mx(*p) ? (p->n_shared > 0 ? 6 : 3) : 0);
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
   return router + route + 3 + quant;

@@ -16,6 +16,11 @@ Recipe (every tensor is drawn in this fixed order from its own seeded stream):
   * FP8 expert weights (expert_dtype "fp8"): the same fp32 draws, then per
     matrix row a scale amax(|row|) / 448 (fp32) and E4M3 codes of row / scale
     (torch's round-to-nearest-even cast, clamped to +-448, so no NaN code)
+  * MXFP4 expert weights (expert_dtype "mxfp4"): the same fp32 draws, then per
+    32 consecutive elements of a row the OCP microscaling recipe: shared
+    exponent X = floor(log2(amax)) - 2 (E8M0 code X + 127), elements rounded
+    to the nearest E2M1 value of v / 2^X (ties to the even code, saturating at
+    6), packed two per byte with the even element in the low nibble
 Router-side tensors (hidden, w_router, biases) always come from a CPU
 generator, so routing is identical whatever device holds the experts. Expert
 weights come from a generator on `device` seeded per expert: large workloads
@@ -51,7 +56,7 @@ class MoEConfig:
     topk_groups: int = 0
     capacity_factor: float = 0.0  # expert capacity ceil(c T K / N) (0: dropless)
     routing: str = "token"   # "token" (tokens pick K experts) | "expert" (experts pick C tokens)
-    expert_dtype: str = "bf16"  # "bf16" | "fp8" (E4M3 codes + one fp32 scale per matrix row)
+    expert_dtype: str = "bf16"  # "bf16" | "fp8" (E4M3 codes + fp32 row scales) | "mxfp4" (E2M1 + E8M0 per 32)
 
     def with_(self, **kw) -> "MoEConfig":
         return dataclasses.replace(self, **kw)
@@ -86,10 +91,13 @@ QWEN_DECODE = MoEConfig("qwen_decode", T=1, d=4096, N=128, K=8, F=1536)
 # The same layers with FP8 E4M3 expert weights.
 MIXTRAL_FP8 = MIXTRAL.with_(name="mixtral_fp8", expert_dtype="fp8")
 QWEN_DECODE_FP8 = QWEN_DECODE.with_(name="qwen_decode_fp8", expert_dtype="fp8")
+# MXFP4 expert weights: the format gpt-oss ships its experts in.
+GPTOSS_MXFP4 = GPTOSS.with_(name="gptoss_mxfp4", expert_dtype="mxfp4")
+QWEN_DECODE_MXFP4 = QWEN_DECODE.with_(name="qwen_decode_mxfp4", expert_dtype="mxfp4")
 DECODE_BATCHES = (1, 8, 32, 128, 512)
 
 CONFIGS = {c.name: c for c in (TINY, MIXTRAL, MIXTRAL_CAPACITY, MIXTRAL_EC, DSV3, DSV3_GROUPED, GPTOSS,
-                               QWEN_DECODE, MIXTRAL_FP8, QWEN_DECODE_FP8)}
+                               QWEN_DECODE, MIXTRAL_FP8, QWEN_DECODE_FP8, GPTOSS_MXFP4, QWEN_DECODE_MXFP4)}
 
 
 def _seed(seed: int, *parts) -> int:
@@ -143,6 +151,63 @@ def _draw_fp8(codes: torch.Tensor, scale: torch.Tensor, gen: torch.Generator, st
     codes.copy_(tmp.to(torch.float8_e4m3fn).view(torch.uint8))
 
 
+# E2M1 magnitudes by code (OCP microscaling FP4).
+E2M1_VALUES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _draw_mxfp4(codes: torch.Tensor, bscale: torch.Tensor, gen: torch.Generator, std: float) -> None:
+    rows, half = codes.shape
+    tmp = torch.randn((rows, 2 * half), generator=gen, dtype=torch.float32, device=codes.device)
+    tmp.mul_(std)
+    blk = tmp.view(rows, -1, 32)
+    amax = blk.abs().amax(dim=2).clamp_min(1e-30)
+    x = torch.floor(torch.log2(amax)) - 2  # the block's shared exponent
+    bscale.copy_((x + 127).clamp(0, 254).to(torch.uint8))
+    v = (blk / torch.exp2(x)[..., None]).abs().clamp_max(6.0)
+    grid = torch.tensor(E2M1_VALUES, dtype=torch.float32, device=codes.device)
+    dist = (v[..., None] - grid).abs()
+    # nearest E2M1 value; an exact tie goes to the even code (mantissa bit 0)
+    dist = dist + torch.tensor([0.0, 1e-30] * 4, device=codes.device) * (dist > 0)
+    mag = dist.argmin(dim=-1).to(torch.uint8)
+    sign = (blk < 0).to(torch.uint8) * 8
+    c4 = (mag | sign).view(rows, -1)
+    codes.copy_(c4[:, 0::2] | (c4[:, 1::2] << 4))
+
+
+def make_expert_weights_mxfp4(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
+    """Stacked MXFP4 expert weights on `device`: packed E2M1 codes (uint8)
+    w_gate, w_up [N, F, d/2], w_down [N, d, F/2] with E8M0 block scales
+    w_gate_scale, w_up_scale [N, F, d/32], w_down_scale [N, d, F/32]; shared
+    experts likewise. Draws the same normal values as make_expert_weights."""
+    device = torch.device(device)
+    u8 = torch.uint8
+    out = {}
+    g = torch.Generator(device=device)
+
+    def stack(kind, n, f):
+        gate = torch.empty(n, f, cfg.d // 2, dtype=u8, device=device)
+        up = torch.empty_like(gate)
+        down = torch.empty(n, cfg.d, f // 2, dtype=u8, device=device)
+        sg = torch.empty(n, f, cfg.d // 32, dtype=u8, device=device)
+        su = torch.empty_like(sg)
+        sd = torch.empty(n, cfg.d, f // 32, dtype=u8, device=device)
+        for e in range(n):
+            g.manual_seed(_seed(seed, kind, e))
+            _draw_mxfp4(gate[e], sg[e], g, 1.0 / math.sqrt(cfg.d))
+            _draw_mxfp4(up[e], su[e], g, 1.0 / math.sqrt(cfg.d))
+            _draw_mxfp4(down[e], sd[e], g, 1.0 / math.sqrt(f))
+        return gate, up, down, sg, su, sd
+
+    (out["w_gate"], out["w_up"], out["w_down"], out["w_gate_scale"], out["w_up_scale"],
+     out["w_down_scale"]) = stack("routed", cfg.N, cfg.F)
+    for k in ("ws_gate", "ws_up", "ws_down", "ws_gate_scale", "ws_up_scale", "ws_down_scale"):
+        out[k] = None
+    if cfg.S > 0:
+        (out["ws_gate"], out["ws_up"], out["ws_down"], out["ws_gate_scale"], out["ws_up_scale"],
+         out["ws_down_scale"]) = stack("shared", cfg.S, cfg.Fs)
+    return out
+
+
 def make_expert_weights_fp8(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
     """Stacked FP8 E4M3 expert weights on `device`: codes (uint8) w_gate, w_up
     [N, F, d], w_down [N, d, F] with fp32 row scales w_gate_scale, w_up_scale
@@ -183,6 +248,8 @@ def make_expert_weights(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
     ws_down [S, d, Fs] (None when S == 0). FP8 configs: make_expert_weights_fp8."""
     if cfg.expert_dtype == "fp8":
         return make_expert_weights_fp8(cfg, seed, device)
+    if cfg.expert_dtype == "mxfp4":
+        return make_expert_weights_mxfp4(cfg, seed, device)
     device = torch.device(device)
     bf = torch.bfloat16
     w_gate = torch.empty(cfg.N, cfg.F, cfg.d, dtype=bf, device=device)

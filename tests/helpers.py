@@ -56,22 +56,26 @@ def u8(t) -> np.ndarray:
 
 
 def _oracle_layer_rows_fp8(cfg, ins, rows, used, keep):
+    mx = cfg.expert_dtype == "mxfp4"
+    sconv = u8 if mx else np32  # E8M0 block scales (MXFP4) or fp32 row scales (FP8)
     q = {k: [None] * cfg.N for k in ("w_gate", "w_up", "w_down")}
     sc = {k: [None] * cfg.N for k in ("w_gate_scale", "w_up_scale", "w_down_scale")}
     for e in used:
         for k in q:
             q[k][e] = u8(ins[k][e])
         for k in sc:
-            sc[k][e] = np32(ins[k][e])
+            sc[k][e] = sconv(ins[k][e])
     sh = {}
     if cfg.S > 0:
+        sk = "bs" if mx else "ss"
         sh = dict(qs_gate=[u8(ins["ws_gate"][s]) for s in range(cfg.S)],
                   qs_up=[u8(ins["ws_up"][s]) for s in range(cfg.S)],
-                  qs_down=[u8(ins["ws_down"][s]) for s in range(cfg.S)],
-                  ss_gate=[np32(ins["ws_gate_scale"][s]) for s in range(cfg.S)],
-                  ss_up=[np32(ins["ws_up_scale"][s]) for s in range(cfg.S)],
-                  ss_down=[np32(ins["ws_down_scale"][s]) for s in range(cfg.S)])
-    return oracle.layer_fp8(hidden_f32(ins)[rows], np32(ins["w_router"]), q["w_gate"], sc["w_gate_scale"],
+                  qs_down=[u8(ins["ws_down"][s]) for s in range(cfg.S)])
+        sh[sk + "_gate"] = [sconv(ins["ws_gate_scale"][s]) for s in range(cfg.S)]
+        sh[sk + "_up"] = [sconv(ins["ws_up_scale"][s]) for s in range(cfg.S)]
+        sh[sk + "_down"] = [sconv(ins["ws_down_scale"][s]) for s in range(cfg.S)]
+    fn = oracle.layer_mxfp4 if mx else oracle.layer_fp8
+    return fn(hidden_f32(ins)[rows], np32(ins["w_router"]), q["w_gate"], sc["w_gate_scale"],
                             q["w_up"], sc["w_up_scale"], q["w_down"], sc["w_down_scale"], K=cfg.K,
                             score_fn=cfg.score_fn, renormalize=cfg.renormalize,
                             router_bias=np32(ins.get("router_bias")), sel_bias=np32(ins.get("sel_bias")),
@@ -85,7 +89,7 @@ def oracle_layer_rows(cfg, ins, rows, keep=None):
     rows = np.asarray(rows, dtype=np.int64)
     r = oracle_router(cfg, ins, rows)
     used = sorted(set(r["idx"].reshape(-1).tolist()))
-    if cfg.expert_dtype == "fp8":
+    if cfg.expert_dtype in ("fp8", "mxfp4"):
         return _oracle_layer_rows_fp8(cfg, ins, rows, used, keep)
     wg = [None] * cfg.N
     wu = [None] * cfg.N

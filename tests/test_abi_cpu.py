@@ -112,7 +112,7 @@ def test_problem_check_capacity_factor():
 def test_problem_check_fp8_experts():
     fp8 = inputs.TINY.with_(expert_dtype="fp8")
     assert B.problem_check(B.problem(fp8)) == 0
-    assert B.problem_check(B.problem(fp8, expert_dtype=2)) == -1
+    assert B.problem_check(B.problem(fp8, expert_dtype=3)) == -1
     assert B.problem_check(B.problem(fp8, d_model=136)) == -1   # FP8 code rows: 16-byte multiples
     assert B.problem_check(B.problem(fp8, ffn=264)) == -1
     assert B.problem_check(B.problem(fp8, n_shared=1, shared_ffn=72)) == -1
@@ -134,3 +134,17 @@ def test_grouped_swiglu_entry_points_check_the_expert_format():
     assert B.lib.moe_grouped_swiglu(p8, *([None] * 8), 0, None) == -1
     p16 = B.problem(inputs.TINY)
     assert B.lib.moe_grouped_swiglu_fp8(p16, *([None] * 11), 0, None) == -1
+
+
+def test_problem_check_mxfp4_experts():
+    mx = inputs.TINY.with_(expert_dtype="mxfp4")
+    assert B.problem_check(B.problem(mx)) == 0
+    assert B.problem_check(B.problem(mx, d_model=144)) == -1     # 32-element scale blocks
+    assert B.problem_check(B.problem(mx, ffn=272)) == -1
+    assert B.problem_check(B.problem(mx, n_shared=1, shared_ffn=80)) == -1
+    assert B.problem_check(B.problem(mx, n_shared=1, shared_ffn=96)) == 0
+    p = B.problem(mx)
+    assert B.lib.moe_grouped_swiglu_mxfp4(p, *([None] * 11), 0, None) == -1  # null pointers
+    assert B.lib.moe_grouped_swiglu_fp8(p, *([None] * 11), 0, None) == -1   # the other format
+    assert B.workspace_bytes(p, B.CALL_LAYER_FORWARD) > B.workspace_bytes(
+        B.problem(inputs.TINY.with_(expert_dtype="fp8")), B.CALL_LAYER_FORWARD)  # + row reference scales

@@ -1,0 +1,144 @@
+"""GPU parity of the MXFP4 expert path against the oracle's MXFP4 layer.
+
+The expert matrices are E2M1 codes (two per byte) with one E8M0 scale per
+32 elements of a row; the oracle decodes them exactly in fp64. The GPU
+rewrites each block as E4M3 codes relative to its row's reference exponent
+(exact for the synthetic weights, whose block exponents span a few binades)
+and runs the 8-bit tensor-core GEMMs on two-term E4M3 activations. The
+acceptance bar is the layer's: router bit-exact (near ties reported apart),
+outputs max|gpu - ref| <= 2e-2 max|ref| and mean relative L1 <= 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_94_b300 import inputs
+from oracle import oracle
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from mixture_experts_layer_94_b300 import binding as B
+
+
+def _cfg(name, **kw):
+    return inputs.MoEConfig(name, expert_dtype="mxfp4", **kw)
+
+
+MID = {
+    "mx_tiny_f32": _cfg("mx_tiny_f32", T=64, d=128, N=8, K=2, F=256, hidden_dtype="f32"),
+    "mx_shared_sigmoid": _cfg("mx_shared_sigmoid", T=333, d=256, N=64, K=6, F=224, S=1, Fs=160,
+                              score="sigmoid", sel_bias_var=0.1, zipf=1.1),
+    "mx_ragged": _cfg("mx_ragged", T=300, d=288, N=16, K=4, F=416),
+    "mx_multi_tile": _cfg("mx_multi_tile", T=700, d=416, N=4, K=2, F=160),
+    "mx_decode_T3": _cfg("mx_decode_T3", T=3, d=1024, N=128, K=8, F=64),
+    "mx_gptoss_like": _cfg("mx_gptoss_like", T=200, d=320, N=32, K=4, F=320),
+    "mx_capacity": _cfg("mx_capacity", T=300, d=288, N=16, K=4, F=416, capacity_factor=0.8),
+}
+
+
+def _run_layer(cfg, dev):
+    layer = B.MoELayer(cfg, dev)
+    idx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device="cuda")
+    w = torch.empty(cfg.T, cfg.K, dtype=torch.float32, device="cuda")
+    counts = torch.empty(cfg.N, dtype=torch.int32, device="cuda")
+    out = layer.forward(dev["hidden"], topk_idx=idx, topk_w=w, counts=counts)
+    torch.cuda.synchronize()
+    assert layer.status(cfg.T) == 0
+    return out, idx.cpu().numpy(), w.cpu().numpy(), counts.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", list(MID))
+def test_mxfp4_layer_matches_oracle(name):
+    cfg = MID[name]
+    ins, dev = H.make_case(cfg)
+    out, idx, w, counts = _run_layer(cfg, dev)
+    keep_cap = H.capacity_keep(cfg, idx) if cfg.capacity_factor > 0 else None
+    ref = H.oracle_layer_rows(cfg, ins, np.arange(cfg.T), keep=keep_cap)
+    rep = H.compare_router(idx, w, ref)
+    assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
+    keep = np.ones(cfg.T, bool)
+    keep[rep["flipped_tokens"]] = False
+    e = H.assert_output_close(out.float().cpu().numpy()[keep], ref["out"][keep], name)
+    print(f"{name}: {e}")
+
+
+SWIGLU_CASES = [(128, 256, 8, 2, 64), (288, 416, 5, 2, 300), (256, 512, 16, 4, 700)]
+
+
+@pytest.mark.parametrize("d,F,N,K,T", SWIGLU_CASES)
+def test_grouped_swiglu_mxfp4_matches_oracle(d, F, N, K, T):
+    cfg = _cfg("gs4", T=T, d=d, N=N, K=K, F=F)
+    ins = inputs.make_inputs(cfg, seed=6)
+    rng = np.random.default_rng(d + F + 1)
+    p_e = np.linspace(3.0, 0.0, N) ** 2 + 1e-9
+    p_e[-1] = 0.0
+    p_e /= p_e.sum()
+    K_eff = min(K, int((p_e > 0).sum()))
+    cfg = cfg.with_(K=K_eff)
+    idx = np.stack([rng.choice(N, size=K_eff, replace=False, p=p_e) for _ in range(T)]).astype(np.int32)
+    perm = oracle.permute(idx, N)
+    x_perm = ins["hidden"][torch.from_numpy(perm["perm_src"] // K_eff).long()].to(torch.float16).contiguous()
+    p = B.problem(cfg)
+    ws = B.new_workspace(p, B.CALL_GROUPED_SWIGLU)
+    h = torch.empty(T * K_eff, F, dtype=torch.float16, device="cuda")
+    y = torch.empty(T * K_eff, d, dtype=torch.bfloat16, device="cuda")
+    d_ = lambda k: ins[k].cuda().contiguous()  # noqa: E731
+    B.grouped_swiglu_mxfp4(p, x_perm.cuda(), torch.from_numpy(perm["offsets"]).cuda(), d_("w_gate"),
+                           d_("w_gate_scale"), d_("w_up"), d_("w_up_scale"), d_("w_down"), d_("w_down_scale"), h,
+                           y, ws)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws) == 0
+    hg, yg = h.float().cpu().numpy(), y.float().cpu().numpy()
+    href = np.empty((T * K_eff, F))
+    yref = np.empty((T * K_eff, d))
+    xp = x_perm.float().numpy().astype(np.float64)
+    for e in range(N):
+        q = [H.u8(ins[k][e]) for k in ("w_gate", "w_up", "w_down")]
+        s = [H.u8(ins[k][e]) for k in ("w_gate_scale", "w_up_scale", "w_down_scale")]
+        for r in range(perm["offsets"][e], perm["offsets"][e + 1]):
+            href[r], yref[r] = oracle.expert_ffn_mxfp4(xp[r], q[0], s[0], q[1], s[1], q[2], s[2], return_h=True)
+    H.assert_output_close(hg, href, "h_perm")
+    H.assert_output_close(yg, yref, "y_perm")
+
+
+def test_mxfp4_wide_exponent_span_rounds_small_blocks_only():
+    """A row whose block exponents span more than 14 binades: the blocks far
+    below the row's largest round to the E4M3 grid (no longer exact), which
+    moves the outputs by far less than the tolerance."""
+    cfg = _cfg("mx_span", T=64, d=128, N=4, K=2, F=64)
+    ins = inputs.make_inputs(cfg, seed=7)
+    for k in ("w_gate_scale", "w_up_scale", "w_down_scale"):
+        ins[k][:, :, 0] = (ins[k][:, :, 0].int() - 20).clamp_min(1).to(torch.uint8)  # first block 2^-20 smaller
+    dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
+    out, idx, w, _ = _run_layer(cfg, dev)
+    ref = H.oracle_layer_rows(cfg, ins, np.arange(cfg.T))
+    rep = H.compare_router(idx, w, ref)
+    keep = np.ones(cfg.T, bool)
+    keep[rep["flipped_tokens"]] = False
+    H.assert_output_close(out.float().cpu().numpy()[keep], ref["out"][keep], "wide span")
+
+
+def _sample_rows(T, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {0, T - 1} | set(rng.choice(T, size=min(T, n), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+FULL = [("gptoss_mxfp4", inputs.GPTOSS_MXFP4, 10)] + [
+    (f"qwen_decode_mxfp4_T{T}", inputs.QWEN_DECODE_MXFP4.with_(T=T), 6) for T in (1, 32, 512)]
+
+
+@pytest.mark.parametrize("name,cfg,n_sample", FULL, ids=[f[0] for f in FULL])
+def test_mxfp4_full_size_workload(name, cfg, n_sample):
+    ins = inputs.make_inputs(cfg, seed=0, device="cuda")
+    dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
+    out, idx, w, counts = _run_layer(cfg, dev)
+    rep = H.compare_router(idx, w, H.oracle_router(cfg, ins))
+    assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
+    fl = set(rep["flipped_tokens"].tolist())
+    rows = np.array([r for r in _sample_rows(cfg.T, n_sample) if r not in fl])
+    ref = H.oracle_layer_rows(cfg, ins, rows)
+    e = H.assert_output_close(out.float().cpu().numpy()[rows], ref["out"], name)
+    print(f"{name}: errors {e}")
