@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mx-per-call", action="store_true",
+                    help="MXFP4 experts: every step prepares the block scales of the experts it uses "
+                         "(default: prepared once when the layer is built, as a server loads weights)")
     return ap.parse_args()
 
 
@@ -338,6 +341,8 @@ def config_block(cfg, desc, args):
             "routing": cfg.routing,
             "ffn": cfg.F, "n_shared": cfg.S, "shared_ffn": cfg.Fs, "score": cfg.score,
             "hidden_dtype": cfg.hidden_dtype, "expert_dtype": cfg.expert_dtype,
+            **({"mxfp4_scale_prep": "every step" if args.mx_per_call else "once when the layer is built"}
+               if cfg.expert_dtype == "mxfp4" else {}),
             "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",
             "l2": "inputs larger than L2 (expert weights stream from HBM every step)"
@@ -410,7 +415,7 @@ def run_ours(args, cfg, desc, world, rank):
     if rank > 0:  # each replica its own batch
         ins["hidden"] = inputs.make_router_inputs(cfg, seed=rank)["hidden"]
     dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
-    layer = B.MoELayer(cfg, dev)
+    layer = B.MoELayer(cfg, dev, mx_prepare=not args.mx_per_call)
     p = B.problem(cfg)
     ws = layer.workspace(cfg.T)
     hidden = dev["hidden"]
@@ -523,7 +528,7 @@ def run_ours(args, cfg, desc, world, rank):
             "layer_roofline": {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],
                                "t_roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step},
             "stages_ms": dict(zip(B.LAYER_STAGES, stage_ms)),
-            "gpu_launches": B.layer_forward_kernel_count(p) * args.steps,
+            "gpu_launches": B.layer_forward_kernel_count(p, layer.ws_struct) * args.steps,
             "cuda_graph": graph is not None,
             "clocks": clocks}
 

@@ -149,7 +149,8 @@ typedef struct moe_problem {
                             number of experts per token)                    */
   int32_t expert_dtype;  /* moe_expert_dtype_t of every expert matrix. FP8
                             requires d_model, ffn and shared_ffn to be
-                            multiples of 16, MXFP4 multiples of 32         */
+                            multiples of 16, MXFP4 multiples of 32 (and at
+                            most 32768, else MOE_ERR_UNSUPPORTED)          */
 } moe_problem_t;
 
 /*
@@ -176,6 +177,12 @@ typedef struct moe_problem {
  * scales as uint8: w_gate_scale, w_up_scale [N][F][d/32], w_down_scale
  * [N][d][F/32]; ws_* [S][Fs][d/32], [S][Fs][d/32], [S][d][Fs/32].
  * The scale arrays are ignored for bf16 experts.
+ * mx_prep (MXFP4 only, else ignored): NULL, or a buffer moe_mxfp4_prepare
+ * filled from these same block scales for a problem with the same n_experts,
+ * n_shared, d_model, ffn and shared_ffn. With it a call skips the per-call
+ * preparation of the experts it uses (three launches, six with shared
+ * experts); the results are bit-identical. The caller prepares again after
+ * changing the block scales.
  */
 typedef struct moe_weights {
   const float* w_router;
@@ -193,6 +200,7 @@ typedef struct moe_weights {
   const void* ws_gate_scale;
   const void* ws_up_scale;
   const void* ws_down_scale;
+  const void* mx_prep;
 } moe_weights_t;
 
 /* Human-readable name of a moe_status_t. Never NULL. Host only. */
@@ -443,10 +451,39 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
                                         void* stream);
 
 /*
- * Number of kernels one moe_layer_forward call launches for problem p (host
- * only, no CUDA call); 0 if p is invalid.
+ * Number of kernels one moe_layer_forward call launches for problem p and
+ * weights w (host only, no CUDA call; only w->mx_prep is read, and w may be
+ * NULL: no prepared buffer); 0 if p is invalid.
  */
-int32_t moe_layer_forward_kernel_count(const moe_problem_t* p);
+int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights_t* w);
+
+/*
+ * MXFP4 experts: the weight-side preparation the expert GEMMs need, computed
+ * from the E8M0 block scales alone ("AI Infrastructure series, Part 12 of
+ * 24", on shipping gpt-oss experts as MXFP4). For every weight row R with
+ * block exponents E_b: its reference exponent E_R = max_b E_b - 6 (NaN
+ * scales 0xFF left out; clamped to 1..254), stored as the fp32 scale
+ * 2^(E_R - 127); and for every block its table index clamp(E_b - E_R, -15,
+ * 6) + 15, four blocks (128 elements, one K step of the GEMM) per 32-bit
+ * word, stored K-step-major so that one K step of 256 rows is one
+ * contiguous 1 KB. A call without a prepared buffer computes the same for
+ * the experts it uses, into its workspace.
+ *
+ * moe_mxfp4_prep_bytes: the buffer size for problem p (host only; 0 if p is
+ * invalid or not MXFP4). It depends on n_experts, n_shared, d_model, ffn and
+ * shared_ffn, not on T.
+ *
+ * moe_mxfp4_prepare: fills `prep` (device memory, 256-byte aligned,
+ * prep_bytes >= moe_mxfp4_prep_bytes(p), owned by the caller) from the block
+ * scales in w (w_gate_scale, w_up_scale, w_down_scale and, when n_shared >
+ * 0, the ws_*_scale arrays; every expert, used or not); asynchronous on
+ * `stream`. Returns MOE_ERR_INVALID_ARG (p not MXFP4, w or a scale array
+ * NULL), MOE_ERR_WORKSPACE (prep misaligned or too small) or MOE_ERR_CUDA.
+ * Set w->mx_prep = prep for later calls.
+ */
+size_t moe_mxfp4_prep_bytes(const moe_problem_t* p);
+moe_status_t moe_mxfp4_prepare(const moe_problem_t* p, const moe_weights_t* w, void* prep,
+                               size_t prep_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word in `ws`

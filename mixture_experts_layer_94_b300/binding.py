@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_OK = 0
+MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = -1, -2, -3, -4
+MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS = -5, -6
 CALL_PERMUTE, CALL_GROUPED_SWIGLU, CALL_LAYER_FORWARD, CALL_ROUTER = 0, 1, 2, 3
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DT_F32, DT_BF16 = 0, 1
@@ -45,7 +47,7 @@ class Problem(ctypes.Structure):
 
 WEIGHT_FIELDS = ("w_router", "router_bias", "sel_bias", "w_gate", "w_up", "w_down", "ws_gate", "ws_up",
                  "ws_down", "w_gate_scale", "w_up_scale", "w_down_scale", "ws_gate_scale", "ws_up_scale",
-                 "ws_down_scale")
+                 "ws_down_scale", "mx_prep")
 
 
 class Weights(ctypes.Structure):
@@ -72,7 +74,9 @@ def _load():
         "moe_layer_forward": ([pp, ctypes.POINTER(Weights)] + [P] * 6 + [sz, P], i32),
         "moe_get_device_status": ([P, P], i32),
         "moe_layer_forward_profiled": ([pp, ctypes.POINTER(Weights)] + [P] * 3 + [sz, P, P], i32),
-        "moe_layer_forward_kernel_count": ([pp], i32),
+        "moe_layer_forward_kernel_count": ([pp, ctypes.POINTER(Weights)], i32),
+        "moe_mxfp4_prep_bytes": ([pp], sz),
+        "moe_mxfp4_prepare": ([pp, ctypes.POINTER(Weights), P, sz, P], i32),
         "moe_expert_choice_select": ([pp] + [P] * 7 + [sz, P], i32),
         "moe_permute_static": ([pp] + [P] * 8, i32),
         "moe_debug_stall_wait": ([P, sz, ctypes.c_uint32, P], i32),
@@ -238,8 +242,20 @@ def layer_forward_profiled(p: Problem, weights: Weights, hidden, out, ws, events
            "moe_layer_forward_profiled")
 
 
-def layer_forward_kernel_count(p: Problem) -> int:
-    return int(lib.moe_layer_forward_kernel_count(ctypes.byref(p)))
+def layer_forward_kernel_count(p: Problem, weights: Weights = None) -> int:
+    return int(lib.moe_layer_forward_kernel_count(ctypes.byref(p), None if weights is None
+                                                  else ctypes.byref(weights)))
+
+
+def mxfp4_prep_bytes(p: Problem) -> int:
+    return int(lib.moe_mxfp4_prep_bytes(ctypes.byref(p)))
+
+
+def mxfp4_prepare(p: Problem, weights: Weights, prep: torch.Tensor, stream=None):
+    """Fill `prep` (a uint8 CUDA tensor of mxfp4_prep_bytes(p) bytes) with the
+    MXFP4 weight preparation; set weights.mx_prep to use it."""
+    _check(lib.moe_mxfp4_prepare(ctypes.byref(p), ctypes.byref(weights), _p(prep), prep.numel(),
+                                 _stream(stream)), "moe_mxfp4_prepare")
 
 
 def debug_stall_wait(ws, timeout_us: int, stream=None):
@@ -256,16 +272,24 @@ class MoELayer:
     """One MoE FFN layer on the GPU: weights and workspace held on the device.
 
     weights: dict with w_router, router_bias, sel_bias, w_gate, w_up, w_down,
-    ws_gate, ws_up, ws_down and, for FP8 experts, the *_scale row scales
-    (torch CUDA tensors or None).
+    ws_gate, ws_up, ws_down and, for FP8 / MXFP4 experts, the *_scale row or
+    block scales (torch CUDA tensors or None). MXFP4 weights are prepared once
+    here (moe_mxfp4_prepare) unless mx_prepare is False; every call then skips
+    the per-call preparation.
     """
 
-    def __init__(self, cfg: MoEConfig, weights: dict, T: int = None, device="cuda"):
+    def __init__(self, cfg: MoEConfig, weights: dict, T: int = None, device="cuda", mx_prepare: bool = True):
         self.cfg = cfg if T is None else cfg.with_(T=T)
         self.device = torch.device(device)
         self.w = {k: (None if v is None else v.to(self.device).contiguous())
-                  for k, v in weights.items() if k in WEIGHT_FIELDS}
+                  for k, v in weights.items() if k in WEIGHT_FIELDS and k != "mx_prep"}
         self.ws_struct = weights_struct(self.w)
+        self.mx_prep = None
+        if cfg.expert_dtype == "mxfp4" and mx_prepare:
+            p = problem(self.cfg)
+            self.mx_prep = torch.empty(mxfp4_prep_bytes(p), dtype=torch.uint8, device=self.device)
+            mxfp4_prepare(p, self.ws_struct, self.mx_prep)
+            self.ws_struct.mx_prep = self.mx_prep.data_ptr()
         self._ws = {}
 
     def workspace(self, T: int) -> torch.Tensor:

@@ -380,37 +380,48 @@ cudaError_t launch_t(const F8Maps& m, const GemmArgs& a, int64_t tile_bound, cud
 // your own GPUs?"). They reach the same 8-bit MMAs as FP8 experts:
 //  * TMA streams the packed codes (64 bytes = 128 elements of a row per
 //    stage, 64-byte swizzle) into a 4-stage ring; half the bytes of FP8.
+//  * A preparation pass (mx_prep_kernel) gives every weight row a reference
+//    exponent E_row (its largest block exponent - 6) and every block the
+//    index of its 8-entry table: E_block - E_row, stored K-block-major so
+//    that TMA brings a stage's 256 rows x 4 block indices (1 KB) into the
+//    code slot beside the codes.
 //  * Converter warps (one thread per weight row) rewrite each 32-element
-//    block as E4M3 codes of e2m1 * 2^(E_block - E_row): E_row is the row's
-//    reference exponent (its largest block exponent - 6, from
-//    mx_row_scale_kernel), so every block within 14 binades of the row's
-//    largest converts exactly (E4M3 spans 2^-9 .. 448; an E2M1 value has two
-//    significant bits); smaller blocks round to nearest. A block's eight
-//    magnitudes become one two-register table; one byte permute then converts
-//    four codes. The E4M3 rows go into a 3-stage ring in the 128-byte-swizzled
-//    K-major layout the MMA reads.
+//    block as E4M3 codes of e2m1 * 2^(E_block - E_row): every block within
+//    14 binades of the row's largest converts exactly (E4M3 spans 2^-9 ..
+//    448; an E2M1 value has two significant bits); smaller blocks round to
+//    nearest. The block's table (its eight magnitudes as E4M3 codes, built
+//    once per CTA in shared memory) turns four codes into four bytes with
+//    one byte permute; a second permute adds the signs. The E4M3 rows go
+//    into a ring in the 128-byte-swizzled K-major layout the MMA reads.
 //  * MMA and epilogue as for FP8 experts, with 2^(E_row - 127) as the weight
 //    row's scale.
 // Warps (480 threads): 0 TMA producer of the codes, 1 MMA, 2-5 epilogue,
-// 6-13 converters, 14 TMA producer of the token rows.
+// 6-13 converters (two groups of four warps taking alternate stages, so that
+// one group converts while the other waits), 14 TMA producer of the token
+// rows.
 
 constexpr int kMxConvWarps = 8;
+constexpr int kMxGroupWarps = kMxConvWarps / 2;  // converter warps per stage
 constexpr int kMxConv0 = 192;
 constexpr int kMxXWarp = kMxConv0 / 32 + kMxConvWarps;
 constexpr int kMxThreads = (kMxXWarp + 1) * 32;
-constexpr int kMxXStages = 4;
+constexpr int kMxXStages = 3;
 constexpr int kMxRStages = 4;
 constexpr int kMxWStages = 3;
 constexpr uint32_t kMxRawBytes = (uint32_t)kWRows * (kKq / 2);  // 256 rows x 64 code bytes = 16 KB
+constexpr uint32_t kMxIdxBytes = (uint32_t)kWRows * 4;           // 256 rows x 4 block indices
+constexpr uint32_t kMxSlotBytes = kMxRawBytes + kMxIdxBytes;      // a multiple of the 512-byte swizzle span
+constexpr int kMxTabEntries = 32;                                 // indices 0 .. kMxIdxBias + 6, padded
 constexpr int kMxNumBars = 2 * (kMxXStages + kMxRStages + kMxWStages) + 5;
 constexpr size_t kMxBarrierBytes = 512;
 constexpr size_t kMxSmem = 1024 + (size_t)kMxXStages * kABytes + (size_t)kMxWStages * kBBytes +
-                           (size_t)kMxRStages * kMxRawBytes + kMxBarrierBytes;
+                           (size_t)kMxRStages * kMxSlotBytes + 8 * kMxTabEntries + kMxBarrierBytes;
 static_assert(8 * kMxNumBars + 8 <= kMxBarrierBytes, "barrier area");
+static_assert(kMxSlotBytes % 512 == 0, "code slots keep the 64-byte swizzle's alignment");
 static_assert(kMxSmem <= 232448, "shared memory per CTA");
 
-// Eight E4M3 codes (as two table words) of the E2M1 magnitudes 0, 0.5, 1,
-// 1.5, 2, 3, 4, 6 times 2^k, rounded to nearest (exact for -8 <= k <= 6).
+// The eight E4M3 codes (as two table words) of the E2M1 magnitudes 0, 0.5,
+// 1, 1.5, 2, 3, 4, 6 times 2^k, rounded to nearest (exact for -8 <= k <= 6).
 __device__ __forceinline__ uint2 e2m1_table(int k) {
   const float f = exp2f((float)k);
   uint32_t b[8];
@@ -420,12 +431,26 @@ __device__ __forceinline__ uint2 e2m1_table(int k) {
   return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
-// Four E2M1 codes (the low 16 bits of c, element i in nibble i) -> four E4M3
-// codes (byte i): the magnitude by table, the sign bit copied.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t c, uint2 tab) {
-  const uint32_t mag = __byte_perm(tab.x, tab.y, c & 0x7777u);
-  const uint32_t sgn = __byte_perm(0x8000u, 0u, (c >> 3) & 0x1111u);
-  return mag | sgn;
+// prmt in its default mode: byte i of the result is source byte (c_i & 7) of
+// {b, a}, or, when bit 3 of selector nibble c_i is set, that byte's sign bit
+// replicated over all eight bits. Only c's low 16 bits are read.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Eight E2M1 codes (element i in nibble i of w) -> eight E4M3 codes (elements
+// 0-3 in lo, 4-7 in hi, element i in byte i % 4). The magnitude comes from
+// the block's table (the code's three low bits select the byte). The sign:
+// a permute of 0x80 bytes by the raw codes gives 0x80 for a positive code and
+// 0xff (the sign replicated) for a negative one, so bit 6 of each byte is the
+// sign; shifted left by one and masked it lands on bit 7.
+__device__ __forceinline__ void e2m1x8_to_e4m3x8(uint32_t w, uint2 tab, uint32_t& lo, uint32_t& hi) {
+  const uint32_t sel = w & 0x77777777u, wh = w >> 16;
+  const uint32_t sl = prmt(0x80808080u, 0x80808080u, w), sh = prmt(0x80808080u, 0x80808080u, wh);
+  lo = prmt(tab.x, tab.y, sel) | ((sl << 1) & 0x80808080u);
+  hi = prmt(tab.x, tab.y, sel >> 16) | ((sh << 1) & 0x80808080u);
 }
 
 template <int PHASE, int EPI>
@@ -437,10 +462,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw_base);
   const uint32_t sX = base;                          // kMxXStages x 16 KB
   const uint32_t sW = sX + kMxXStages * kABytes;     // kMxWStages x 32 KB
-  const uint32_t sRaw = sW + kMxWStages * kBBytes;   // kMxRStages x 16 KB
-  const uint32_t sBar = sRaw + kMxRStages * kMxRawBytes;
+  const uint32_t sRaw = sW + kMxWStages * kBBytes;   // kMxRStages x (16 KB codes + 1 KB block indices)
+  const uint32_t sTab = sRaw + kMxRStages * kMxSlotBytes;
+  const uint32_t sBar = sTab + 8 * kMxTabEntries;
   uint8_t* gW = gbase + (sW - base);
   const uint8_t* gRaw = gbase + (sRaw - base);
+  uint2* gTab = reinterpret_cast<uint2*>(gbase + (sTab - base));
   uint8_t* gBar = gbase + (sBar - base);
   auto xfull_bar = [&](int s) { return sBar + 8u * s; };
   auto xempty_bar = [&](int s) { return sBar + 8u * (kMxXStages + s); };
@@ -465,10 +492,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
     for (int s = 0; s < kMxRStages; ++s) {
       ptx::mbar_init(rfull_bar(s), 1);
-      ptx::mbar_init(rempty_bar(s), kMxConvWarps);
+      ptx::mbar_init(rempty_bar(s), kMxGroupWarps);
     }
     for (int s = 0; s < kMxWStages; ++s) {
-      ptx::mbar_init(wfull_bar(s), kMxConvWarps);
+      ptx::mbar_init(wfull_bar(s), kMxGroupWarps);
       ptx::mbar_init(wempty_bar(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -482,7 +509,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&maps.w[0]);
-    if (PHASE == kPhaseGateUp) ptx::prefetch_tmap(&maps.u[0]);
+    ptx::prefetch_tmap(&maps.kw[0]);
+    if (PHASE == kPhaseGateUp) {
+      ptx::prefetch_tmap(&maps.u[0]);
+      ptx::prefetch_tmap(&maps.ku[0]);
+    }
+  }
+  if (threadIdx.x >= kMxConv0 && threadIdx.x < kMxConv0 + kMxTabEntries) {
+    const int i = threadIdx.x - kMxConv0;
+    gTab[i] = i <= kMxIdxBias + 6 ? e2m1_table(i - kMxIdxBias) : make_uint2(0u, 0u);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -511,6 +546,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const CUtensorMap* mA = &maps.x[kind][bsel];
         const CUtensorMap* mW = &maps.w[kind];
         const CUtensorMap* mU = &maps.u[kind];
+        const CUtensorMap* mKW = &maps.kw[kind];
+        const CUtensorMap* mKU = &maps.ku[kind];
         const int a_row = 2 * ((PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kF8TileRows);
         const int w_row = ti.g.index * a.w_rows[kind] + ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
         const int nkb = a.k_blocks[kind];
@@ -522,11 +559,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             break;
           }
           if (codes) {
-            const uint32_t dR = sRaw + stage * kMxRawBytes;
-            ptx::mbar_arrive_expect_tx(full, kMxRawBytes);
+            const uint32_t dR = sRaw + stage * kMxSlotBytes, dI = dR + kMxRawBytes;
+            ptx::mbar_arrive_expect_tx(full, kMxSlotBytes);
             ptx::tma_load_2d(dR, mW, full, kb * (kKq / 2), w_row);
-            if (PHASE == kPhaseGateUp) ptx::tma_load_2d(dR + kMxRawBytes / 2, mU, full, kb * (kKq / 2), w_row);
-            else ptx::tma_load_2d(dR + kMxRawBytes / 2, mW, full, kb * (kKq / 2), w_row + kWRows / 2);
+            ptx::tma_load_2d(dI, mKW, full, w_row, kb);
+            if (PHASE == kPhaseGateUp) {
+              ptx::tma_load_2d(dR + kMxRawBytes / 2, mU, full, kb * (kKq / 2), w_row);
+              ptx::tma_load_2d(dI + kMxIdxBytes / 2, mKU, full, w_row, kb);
+            } else {
+              ptx::tma_load_2d(dR + kMxRawBytes / 2, mW, full, kb * (kKq / 2), w_row + kWRows / 2);
+              ptx::tma_load_2d(dI + kMxIdxBytes / 2, mKW, full, w_row + kWRows / 2, kb);
+            }
           } else {
             ptx::mbar_arrive_expect_tx(full, xbytes);
             ptx::tma_load_2d(sX + stage * kABytes, mA, full, kb * kKq, a_row);
@@ -594,75 +637,62 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     __syncwarp();
   } else if (threadIdx.x >= kMxConv0) {
     // ------------------------------------------------------------ converters
-    // Thread R owns weight row R of the tile (rows 0..127: W_gate or the first
-    // 128 W_down rows; 128..255: W_up or the next 128). Per stage it reads the
-    // row's 64 code bytes (chunk c of the 64-byte-swizzled box row at
-    // c ^ ((R >> 1) & 3)) and the four block scales of those 128 elements,
-    // and writes the row's 128 E4M3 codes: chunk j at j ^ (R & 7) of the
-    // 128-byte-swizzled weight tile.
-    const int R = threadIdx.x - kMxConv0;
-    const int rsw = (R >> 1) & 3, wsw = R & 7;
-    int rs = 0, ws = 0;
+    // Group grp takes the stages n with n % 2 == grp; its thread t converts
+    // weight rows t and t + 128 of the tile (W_gate and W_up row t, or W_down
+    // rows t and t + 128). Per row it reads the 64 code bytes (chunk c of the
+    // 64-byte-swizzled box row at c ^ ((R >> 1) & 3)) and the four block
+    // indices, and writes the row's 128 E4M3 codes: chunk j at j ^ (R & 7) of
+    // the 128-byte-swizzled weight tile.
+    const int grp = (threadIdx.x - kMxConv0) / (32 * kMxGroupWarps);
+    const int t = (threadIdx.x - kMxConv0) % (32 * kMxGroupWarps);
+    int rs = 0, ws = 0, n = 0;
     uint32_t rphase = 0, wphase = 0;
     bool aborted = false;
     for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, a);
-      const int kind = ti.g.kind;
-      const int nkb = a.k_blocks[kind];
-      const int nblk = a.k_len[kind] / 32;  // block scales per row
-      const int64_t q_row = (int64_t)ti.g.index * a.w_rows[kind] +
-                            (int64_t)ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown) +
-                            (PHASE == kPhaseGateUp ? (R & 127) : R);
-      const bool row_ok = q_row < a.q_rows[kind];
-      const uint8_t* bs = ((PHASE == kPhaseGateUp && R >= 128) ? a.ub_scale[kind] : a.wb_scale[kind]) +
-                          (row_ok ? q_row : 0) * (int64_t)nblk;
-      const float* rsp = (PHASE == kPhaseGateUp && R >= 128) ? a.u_scale[kind] : a.w_scale[kind];
-      // The row's reference exponent: the biased exponent of its scale 2^(E_row - 127).
-      const int e_row = row_ok ? (int)((__float_as_uint(__ldg(rsp + q_row)) >> 23) & 255u) : 127;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!ptx::mbar_wait(rfull_bar(rs), rphase, abort_flag, a.err)) {
-          aborted = true;
-          break;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(gRaw + rs * kMxRawBytes + R * (kKq / 2));
-        uint4 v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = src[c ^ rsw];
-        // Chunk c (16 code bytes = 32 elements) is exactly block 4*kb + c.
-        uint4 o[8];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int blk = 4 * kb + c;
-          const int eb = (row_ok && blk < nblk) ? (int)__ldg(bs + blk) : e_row;
-          const uint2 tab = e2m1_table(eb - e_row);
-          const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-          uint32_t r8[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            r8[2 * q] = e2m1x4_to_e4m3x4(w4[q], tab);
-            r8[2 * q + 1] = e2m1x4_to_e4m3x4(w4[q] >> 16, tab);
+      const int nkb = a.k_blocks[decode_tile(tile, a).g.kind];
+      for (int kb = 0; kb < nkb; ++kb, ++n) {
+        if ((n & 1) == grp) {
+          if (!ptx::mbar_wait(rfull_bar(rs), rphase, abort_flag, a.err) ||
+              !ptx::mbar_wait(wempty_bar(ws), wphase ^ 1u, abort_flag, a.err)) {
+            aborted = true;
+            break;
           }
-          o[2 * c] = make_uint4(r8[0], r8[1], r8[2], r8[3]);
-          o[2 * c + 1] = make_uint4(r8[4], r8[5], r8[6], r8[7]);
+          const uint8_t* slot = gRaw + rs * kMxSlotBytes;
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            const int R = t + 128 * half;
+            const uint4* src = reinterpret_cast<const uint4*>(slot + R * (kKq / 2));
+            const int rsw = (R >> 1) & 3;
+            uint4 v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = src[c ^ rsw];
+            const uint32_t kidx = reinterpret_cast<const uint32_t*>(slot + kMxRawBytes)[R];
+            uint4* dst = reinterpret_cast<uint4*>(gW + ws * kBBytes + R * kKq);
+            const int wsw = R & 7;
+            // Chunk c (16 code bytes = 32 elements) is exactly block 4*kb + c.
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint2 tab = gTab[(kidx >> (8 * c)) & (kMxTabEntries - 1)];
+              uint32_t r8[8];
+              e2m1x8_to_e4m3x8(v[c].x, tab, r8[0], r8[1]);
+              e2m1x8_to_e4m3x8(v[c].y, tab, r8[2], r8[3]);
+              e2m1x8_to_e4m3x8(v[c].z, tab, r8[4], r8[5]);
+              e2m1x8_to_e4m3x8(v[c].w, tab, r8[6], r8[7]);
+              dst[(2 * c) ^ wsw] = make_uint4(r8[0], r8[1], r8[2], r8[3]);
+              dst[(2 * c + 1) ^ wsw] = make_uint4(r8[4], r8[5], r8[6], r8[7]);
+            }
+          }
+          // Every lane's loads of the code slot have been consumed above.
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(rempty_bar(rs));
+          ptx::fence_proxy_async_shared();  // generic-proxy writes -> the MMA's async-proxy reads
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(wfull_bar(ws));
         }
-        // The code slot may be refilled only once every lane's loads have
-        // returned: the conversion above consumed all of them.
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(rempty_bar(rs));
         if (++rs == kMxRStages) {
           rs = 0;
           rphase ^= 1u;
         }
-        if (!ptx::mbar_wait(wempty_bar(ws), wphase ^ 1u, abort_flag, a.err)) {
-          aborted = true;
-          break;
-        }
-        uint4* dst = reinterpret_cast<uint4*>(gW + ws * kBBytes + R * kKq);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j ^ wsw] = o[j];
-        ptx::fence_proxy_async_shared();  // generic-proxy writes -> the MMA's async-proxy reads
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(wfull_bar(ws));
         if (++ws == kMxWStages) {
           ws = 0;
           wphase ^= 1u;
@@ -681,31 +711,111 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-// The reference exponent of every weight row of the experts in use: E_row =
-// (largest E8M0 block exponent of the row, NaN scales aside) - 6, clamped to
-// 1..254; the row's scale 2^(E_row - 127) is written as fp32. A warp per row,
-// grid-stride; rows of experts with no routed rows are skipped.
-__global__ void __launch_bounds__(256) mx_row_scale_kernel(const uint8_t* __restrict__ bscale, int64_t rows,
-                                                          int32_t rows_per_expert, int32_t nblk,
-                                                          const int32_t* __restrict__ offsets,
-                                                          float* __restrict__ row_scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t r = warp0; r < rows; r += nwarps) {
-    if (offsets) {
-      const int64_t e = r / rows_per_expert;
-      if (__ldg(offsets + e + 1) == __ldg(offsets + e)) continue;
+// The preparation of one MXFP4 weight matrix (see launch_mx_prep). A block
+// takes kMxPrepRows consecutive rows, whose block scales are one contiguous
+// span of global memory: the block copies it with 16-byte loads, all in
+// flight at once, into shared memory at a row pitch of an odd number of
+// words, so that one thread per row then reads its row without bank
+// conflicts; each thread finds its row's reference exponent and writes the
+// row's index words K-block-major (consecutive threads store consecutive
+// words). Row groups whose experts have no routed rows are skipped.
+constexpr int kMxPrepRows = 128;
+
+__device__ __forceinline__ int mx_prep_pitch(int nblk) { return ((nblk + 3) / 4) | 1; }  // words
+
+__global__ void __launch_bounds__(kMxPrepRows) mx_prep_kernel(const uint8_t* __restrict__ bscale, int64_t rows,
+                                                              int32_t rows_per_expert, int32_t nblk,
+                                                              int32_t kblocks, const int32_t* __restrict__ offsets,
+                                                              float* __restrict__ row_scale,
+                                                              uint32_t* __restrict__ kidx) {
+  extern __shared__ uint32_t st[];  // [kMxPrepRows][pitch] words
+  const int pitch = mx_prep_pitch(nblk);
+  const int t = threadIdx.x;
+  const bool vec = (reinterpret_cast<uintptr_t>(bscale) & 15u) == 0;
+  for (int64_t r0 = (int64_t)blockIdx.x * kMxPrepRows; r0 < rows; r0 += (int64_t)gridDim.x * kMxPrepRows) {
+    const int nrows = (int)min((int64_t)kMxPrepRows, rows - r0);
+    if (offsets) {  // a group spans the experts of its first and last rows (and any between)
+      const int64_t e0 = r0 / rows_per_expert, e1 = (r0 + nrows - 1) / rows_per_expert;
+      if (__ldg(offsets + e1 + 1) == __ldg(offsets + e0)) continue;
     }
-    const uint8_t* p = bscale + r * (int64_t)nblk;
-    int m = 0;
-    for (int j = lane; j < nblk; j += 32) {
-      const int v = __ldg(p + j);
-      if (v != 255) m = max(m, v);
-    }
+    const uint8_t* span = bscale + r0 * (int64_t)nblk;
+    const int bytes = nrows * nblk;  // a multiple of 16 (rows come in multiples of 32)
+    uint8_t* sb = reinterpret_cast<uint8_t*>(st);
+    if (vec) {
+      constexpr int kUnroll = 4;
+      for (int g0 = t; g0 < bytes / 16; g0 += kUnroll * kMxPrepRows) {
+        uint4 v[kUnroll];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) row_scale[r] = __uint_as_float((uint32_t)min(max(m - 6, 1), 254) << 23);
+        for (int u = 0; u < kUnroll; ++u) {
+          const int g = g0 + u * kMxPrepRows;
+          if (g < bytes / 16) v[u] = __ldg(reinterpret_cast<const uint4*>(span) + g);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int g = g0 + u * kMxPrepRows;
+          if (g >= bytes / 16) break;
+          int row = (16 * g) / nblk, col = 16 * g - row * nblk;
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          if ((nblk & 3) == 0) {  // words never straddle two rows
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              st[row * pitch + col / 4] = w4[j];
+              col += 4;
+              if (col == nblk) {
+                col = 0;
+                ++row;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              sb[4 * row * pitch + col] = (uint8_t)(w4[j >> 2] >> (8 * (j & 3)));
+              if (++col == nblk) {
+                col = 0;
+                ++row;
+              }
+            }
+          }
+        }
+      }
+    } else {
+      for (int o = t; o < bytes; o += kMxPrepRows) {
+        const int row = o / nblk;
+        sb[4 * row * pitch + (o - row * nblk)] = __ldg(span + o);
+      }
+    }
+    __syncthreads();
+    const int64_t r = r0 + t;
+    bool live = t < nrows;
+    if (live && offsets) {
+      const int64_t e = r / rows_per_expert;
+      live = __ldg(offsets + e + 1) != __ldg(offsets + e);
+    }
+    if (live) {
+      const uint32_t* row = st + t * pitch;
+      int m = 0;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t w = row[kb];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int v = (int)((w >> (8 * c)) & 255u);
+          if (4 * kb + c < nblk && v != 255) m = max(m, v);
+        }
+      }
+      const int e_row = min(max(m - 6, 1), 254);
+      row_scale[r] = __uint_as_float((uint32_t)e_row << 23);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t w = row[kb];
+        uint32_t o = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int k = min(max((int)((w >> (8 * c)) & 255u) - e_row, -kMxIdxBias), 6) + kMxIdxBias;
+          if (4 * kb + c < nblk) o |= (uint32_t)k << (8 * c);
+        }
+        kidx[(int64_t)kb * rows + r] = o;
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -747,14 +857,22 @@ cudaError_t launch_grouped_gemm_mxfp4(int phase, int epilogue, const F8Maps& map
   return launch_mx<kPhaseDown, kEpiStoreY>(maps, a, tile_bound, s);
 }
 
-cudaError_t launch_mx_row_scale(const uint8_t* bscale, int64_t rows, int32_t rows_per_expert, int32_t nblk,
-                                const int32_t* offsets, float* row_scale, cudaStream_t s) {
+cudaError_t launch_mx_prep(const uint8_t* bscale, int64_t rows, int32_t rows_per_expert, int32_t nblk,
+                           int32_t kblocks, const int32_t* offsets, float* row_scale, uint32_t* kidx,
+                           cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  const size_t smem = (size_t)kMxPrepRows * (size_t)((((nblk + 3) / 4) | 1)) * 4;
+  if (smem > kMxPrepMaxSmem) return cudaErrorInvalidValue;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (rows + 7) / 8;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(mx_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t want = (rows + kMxPrepRows - 1) / kMxPrepRows;
   const unsigned grid = (unsigned)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
-  mx_row_scale_kernel<<<grid, 256, 0, s>>>(bscale, rows, rows_per_expert, nblk, offsets, row_scale);
+  mx_prep_kernel<<<grid, kMxPrepRows, smem, s>>>(bscale, rows, rows_per_expert, nblk, kblocks, offsets, row_scale,
+                                                 kidx);
   return cudaGetLastError();
 }
 

@@ -119,22 +119,14 @@ struct GemmArgs {
   const float* row_w;    // scatter epilogue, expert choice: perm_src is the row's token, row_w its weight
   int32_t d;
   uint32_t* err;
-  // FP8 expert weights: fp32 scale of each weight row, per kind (gate/up
-  // phase: w_scale = gate rows, u_scale = up rows; down phase: w_scale = rows
-  // of W_down).
+  // FP8 / MXFP4 expert weights: fp32 scale of each weight row, per kind
+  // (gate/up phase: w_scale = gate rows, u_scale = up rows; down phase:
+  // w_scale = rows of W_down). MXFP4: the row's reference scale 2^(E_row - 127).
   const float* w_scale[2];
   const float* u_scale[2];
   // FP8 / MXFP4 experts: the scale of each activation row, per kind (the
   // token rows of the gate/up phase, the h rows of the down phase).
   const float* a_scale[2];
-  // MXFP4 experts: E8M0 block scales of the code matrices (w: gate or down,
-  // u: up) [rows][k_len / 32], the code rows' length in elements and the
-  // matrices' row counts, per kind. w_scale / u_scale then hold each row's
-  // reference scale 2^(E_row - 127).
-  const uint8_t* wb_scale[2];
-  const uint8_t* ub_scale[2];
-  int32_t k_len[2];
-  int64_t q_rows[2];
   // Router phase: one group of all T tokens; tile = (m block, split) with
   // split = part * r_dslices + slice.
   int32_t r_tiles, r_m_tiles, r_dslices, r_kb_per_slice, r_nkb_d, r_d_pad, r_np, r_N;
@@ -160,6 +152,8 @@ struct F8Maps {
   CUtensorMap x[2][kF8XBoxes];
   CUtensorMap w[2];
   CUtensorMap u[2];
+  CUtensorMap kw[2];  // MXFP4: block-table indices of the w / u rows (see launch_mx_prep)
+  CUtensorMap ku[2];
 };
 
 // An activation matrix for the FP8-weight GEMMs: src fp16 [rows][K] ->
@@ -184,11 +178,26 @@ cudaError_t launch_grouped_gemm_fp8(int phase, int epilogue, const F8Maps& maps,
 // matrices ([rows][K/2] bytes, 128-row boxes of 64 bytes, 64-byte swizzle).
 cudaError_t launch_grouped_gemm_mxfp4(int phase, int epilogue, const F8Maps& maps, const GemmArgs& a,
                                       int64_t tile_bound, cudaStream_t s);
-// Reference scales 2^(E_row - 127) of MXFP4 weight rows: E_row = the row's
-// largest E8M0 block exponent - 6 (clamped to 1..254). Rows of experts whose
-// offsets show no routed rows are skipped (offsets may be NULL: all rows).
-cudaError_t launch_mx_row_scale(const uint8_t* bscale, int64_t rows, int32_t rows_per_expert, int32_t nblk,
-                                const int32_t* offsets, float* row_scale, cudaStream_t s);
+// Per-call preparation of an MXFP4 weight matrix with E8M0 block scales
+// bscale [rows][nblk]: each row's reference exponent E_row = (its largest
+// block exponent, NaN scales aside) - 6, clamped to 1..254, written as the
+// fp32 row scale 2^(E_row - 127); and, for K block kb (128 elements = blocks
+// 4kb .. 4kb+3), kidx[kb][row] = four bytes, byte c = the table index of
+// block 4kb + c: clamp(E_block - E_row, -kMxIdxBias, 6) + kMxIdxBias (0 past
+// the row's last block). Rows of experts whose offsets show no routed rows
+// are skipped (offsets may be NULL: all rows).
+constexpr int kMxIdxBias = 15;
+// Shared memory the preparation of one row group may take: 128 rows of
+// nblk block scales (nblk <= 1024, i.e. K <= kMxMaxK elements).
+constexpr int kMxMaxK = 32768;
+constexpr size_t kMxPrepMaxSmem = 128 * 4 * 257;
+cudaError_t launch_mx_prep(const uint8_t* bscale, int64_t rows, int32_t rows_per_expert, int32_t nblk,
+                           int32_t kblocks, const int32_t* offsets, float* row_scale, uint32_t* kidx,
+                           cudaStream_t s);
+// uint32 matrix [kblocks][rows] (an MXFP4 block-index array) as a TMA tensor
+// map with a box of 128 rows of one K block; no swizzle, zero fill out of
+// bounds. rows % 4 == 0.
+bool make_tmap_mx_index(CUtensorMap* m, const uint32_t* ptr, uint64_t rows, uint64_t kblocks);
 // uint8 matrix [rows][inner] with a box of [box_rows][64 bytes], 64-byte swizzle.
 bool make_tmap_u8_64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows);
 

@@ -18,11 +18,43 @@ constexpr int64_t kInt32Max = 2147483647;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Where the MXFP4 preparation arrays of a weight set sit (in the workspace
+// for a per-call preparation, or in a buffer moe_mxfp4_prepare filled):
+// every weight row's reference scale (fp32) and block-table index words.
+struct MxOffsets {
+  size_t rs_gate, rs_up, rs_down, rs_sgate, rs_sup, rs_sdown;
+  size_t ki_gate, ki_up, ki_down, ki_sgate, ki_sup, ki_sdown;
+};
+
+// Lays the MXFP4 preparation arrays out with `take` (routed experts; the
+// shared ones too when `shared`).
+template <class Take>
+MxOffsets mx_offsets(const moe_problem_t& p, bool shared, Take&& take) {
+  MxOffsets o{};
+  const size_t kb_d = (p.d_model + 127) / 128, kb_f = (p.ffn + 127) / 128;
+  o.rs_gate = take((size_t)p.n_experts * p.ffn * 4);
+  o.rs_up = take((size_t)p.n_experts * p.ffn * 4);
+  o.rs_down = take((size_t)p.n_experts * p.d_model * 4);
+  o.ki_gate = take((size_t)p.n_experts * p.ffn * kb_d * 4);
+  o.ki_up = take((size_t)p.n_experts * p.ffn * kb_d * 4);
+  o.ki_down = take((size_t)p.n_experts * p.d_model * kb_f * 4);
+  if (shared) {
+    const size_t kb_fs = (p.shared_ffn + 127) / 128;
+    o.rs_sgate = take((size_t)p.n_shared * p.shared_ffn * 4);
+    o.rs_sup = take((size_t)p.n_shared * p.shared_ffn * 4);
+    o.rs_sdown = take((size_t)p.n_shared * p.d_model * 4);
+    o.ki_sgate = take((size_t)p.n_shared * p.shared_ffn * kb_d * 4);
+    o.ki_sup = take((size_t)p.n_shared * p.shared_ffn * kb_d * 4);
+    o.ki_sdown = take((size_t)p.n_shared * p.d_model * kb_fs * 4);
+  }
+  return o;
+}
+
 struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc;
   size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 / MXFP4 experts: two-term E4M3 activations + row scales
-  size_t rs_gate, rs_up, rs_down, rs_sgate, rs_sup, rs_sdown;  // MXFP4 experts: weight rows' reference scales
+  MxOffsets mx;  // MXFP4 experts: the per-call preparation of the weights in use
   size_t total;
 };
 
@@ -75,16 +107,8 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.ec_token = take((size_t)ec_rows * 4);
     L.ec_w = take((size_t)ec_rows * 4);
   }
-  if (is_mx(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU)) {
-    L.rs_gate = take((size_t)p.n_experts * p.ffn * 4);
-    L.rs_up = take((size_t)p.n_experts * p.ffn * 4);
-    L.rs_down = take((size_t)p.n_experts * p.d_model * 4);
-    if (call == MOE_CALL_LAYER_FORWARD && p.n_shared > 0) {
-      L.rs_sgate = take((size_t)p.n_shared * p.shared_ffn * 4);
-      L.rs_sup = take((size_t)p.n_shared * p.shared_ffn * 4);
-      L.rs_sdown = take((size_t)p.n_shared * p.d_model * 4);
-    }
-  }
+  if (is_mx(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU))
+    L.mx = mx_offsets(p, call == MOE_CALL_LAYER_FORWARD && p.n_shared > 0, take);
   if (is_lowp(p) && (call == MOE_CALL_LAYER_FORWARD || call == MOE_CALL_GROUPED_SWIGLU)) {
     L.xq = take((size_t)2 * rows * p.d_model);
     L.sx = take((size_t)rows * 4);
@@ -205,6 +229,17 @@ bool make_tmap_u8_64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t r
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+bool make_tmap_mx_index(CUtensorMap* m, const uint32_t* ptr, uint64_t rows, uint64_t kblocks) {
+  if (!have_encode() || (rows % 4) != 0) return false;
+  const cuuint64_t dims[2] = {rows, kblocks};
+  const cuuint64_t strides[1] = {rows * 4};
+  const cuuint32_t box[2] = {128u, 1u};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace moe
 
 namespace {
@@ -247,6 +282,7 @@ struct GemmPlan {
   int32_t pair;
   bool fp8;               // FP8 or MXFP4 weights (+ the scales below), fp16 activations
   bool mx;                // MXFP4: *_scale are E8M0 block scales; rs_* the rows' reference scales
+  bool mx_prepared;       // MXFP4: rs_* / ki_* were filled by moe_mxfp4_prepare (no per-call preparation)
   int32_t N, S, F, Fs, d, K;
   int64_t T, routed_rows;
   const void* x_routed;   // [routed_rows][d] bf16
@@ -269,6 +305,12 @@ struct GemmPlan {
   float* rs_sgate;        // shared: [S][Fs], [S][Fs], [S][d]
   float* rs_sup;
   float* rs_sdown;
+  uint32_t* ki_gate;      // MXFP4: block-table indices, [d/128][N F], [d/128][N F], [F/128][N d]
+  uint32_t* ki_up;
+  uint32_t* ki_down;
+  uint32_t* ki_sgate;     // shared: [d/128][S Fs], [d/128][S Fs], [Fs/128][S d]
+  uint32_t* ki_sup;
+  uint32_t* ki_sdown;
   const int32_t* offsets; // MXFP4: routed rows per expert (experts without rows are skipped)
   __nv_bfloat16* h;       // [routed_rows][F] (fp16 bits when fp8)
   __nv_bfloat16* h_sh;    // [S*T][Fs] (fp16 bits when fp8)
@@ -291,6 +333,50 @@ struct GemmPlan {
   const int32_t* ts_dn;
   uint32_t* err;
 };
+
+// The MXFP4 preparation arrays of a plan at `base` (routed experts; shared
+// ones too when `shared`).
+void set_mx_arrays(GemmPlan* g, void* base, const MxOffsets& o, bool shared) {
+  g->rs_gate = at<float>(base, o.rs_gate);
+  g->rs_up = at<float>(base, o.rs_up);
+  g->rs_down = at<float>(base, o.rs_down);
+  g->ki_gate = at<uint32_t>(base, o.ki_gate);
+  g->ki_up = at<uint32_t>(base, o.ki_up);
+  g->ki_down = at<uint32_t>(base, o.ki_down);
+  if (shared) {
+    g->rs_sgate = at<float>(base, o.rs_sgate);
+    g->rs_sup = at<float>(base, o.rs_sup);
+    g->rs_sdown = at<float>(base, o.rs_sdown);
+    g->ki_sgate = at<uint32_t>(base, o.ki_sgate);
+    g->ki_sup = at<uint32_t>(base, o.ki_sup);
+    g->ki_sdown = at<uint32_t>(base, o.ki_sdown);
+  }
+}
+
+// A buffer's layout of the preparation moe_mxfp4_prepare writes (offsets
+// from its start, 256-byte aligned) and its size.
+MxOffsets prep_offsets(const moe_problem_t& p, size_t* total) {
+  size_t off = 0;
+  const MxOffsets o = mx_offsets(p, p.n_shared > 0, [&](size_t bytes) {
+    const size_t at_ = off;
+    off = align256(off + bytes);
+    return at_;
+  });
+  if (total) *total = off;
+  return o;
+}
+
+// The plan's MXFP4 arrays: the caller's prepared buffer when the weights
+// carry one, else the workspace (prepared by this call).
+void set_mx_plan(GemmPlan* g, const moe_problem_t& p, const moe_weights_t* w, void* ws, const Layout& L,
+                 bool shared) {
+  if (w && w->mx_prep) {
+    set_mx_arrays(g, const_cast<void*>(w->mx_prep), prep_offsets(p, nullptr), shared);
+    g->mx_prepared = true;
+  } else {
+    set_mx_arrays(g, ws, L.mx, shared);
+  }
+}
 
 // While the stream is being captured into a CUDA graph, an external record
 // keeps the event a real record node of the graph; otherwise a plain record.
@@ -391,21 +477,25 @@ bool make_code_map(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, b
 }
 
 // The two GEMM phases for FP8 or MXFP4 experts: each phase's activations are
-// first split into two-term E4M3 rows (act_quant.cu); MXFP4 weight rows first
-// get their reference scales (mx_row_scale_kernel).
+// first split into two-term E4M3 rows (act_quant.cu); MXFP4 weight matrices
+// first get their rows' reference scales and block-table indices
+// (launch_mx_prep).
 moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_gateup) {
   if (!have_encode()) return MOE_ERR_CUDA;
   const bool sh = g.S > 0, mx = g.mx;
   auto f32 = [](const void* p) { return static_cast<const float*>(p); };
   auto u8 = [](const void* p) { return static_cast<const uint8_t*>(p); };
-  if (mx) {
-    MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.wg_scale), (int64_t)g.N * g.F, g.F, g.d / 32, g.offsets, g.rs_gate, s)));
-    MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.wu_scale), (int64_t)g.N * g.F, g.F, g.d / 32, g.offsets, g.rs_up, s)));
-    MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.wd_scale), (int64_t)g.N * g.d, g.d, g.F / 32, g.offsets, g.rs_down, s)));
+  const int32_t kb_d = (g.d + 127) / 128, kb_f = (g.F + 127) / 128, kb_fs = (g.Fs + 127) / 128;
+  if (mx && !g.mx_prepared) {
+    const int64_t nf = (int64_t)g.N * g.F, nd = (int64_t)g.N * g.d;
+    MOE_TRY(cuda_status(launch_mx_prep(u8(g.wg_scale), nf, g.F, g.d / 32, kb_d, g.offsets, g.rs_gate, g.ki_gate, s)));
+    MOE_TRY(cuda_status(launch_mx_prep(u8(g.wu_scale), nf, g.F, g.d / 32, kb_d, g.offsets, g.rs_up, g.ki_up, s)));
+    MOE_TRY(cuda_status(launch_mx_prep(u8(g.wd_scale), nd, g.d, g.F / 32, kb_f, g.offsets, g.rs_down, g.ki_down, s)));
     if (sh) {
-      MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.sg_scale), (int64_t)g.S * g.Fs, g.Fs, g.d / 32, nullptr, g.rs_sgate, s)));
-      MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.su_scale), (int64_t)g.S * g.Fs, g.Fs, g.d / 32, nullptr, g.rs_sup, s)));
-      MOE_TRY(cuda_status(launch_mx_row_scale(u8(g.sd_scale), (int64_t)g.S * g.d, g.d, g.Fs / 32, nullptr, g.rs_sdown, s)));
+      const int64_t sf = (int64_t)g.S * g.Fs, sd = (int64_t)g.S * g.d;
+      MOE_TRY(cuda_status(launch_mx_prep(u8(g.sg_scale), sf, g.Fs, g.d / 32, kb_d, nullptr, g.rs_sgate, g.ki_sgate, s)));
+      MOE_TRY(cuda_status(launch_mx_prep(u8(g.su_scale), sf, g.Fs, g.d / 32, kb_d, nullptr, g.rs_sup, g.ki_sup, s)));
+      MOE_TRY(cuda_status(launch_mx_prep(u8(g.sd_scale), sd, g.d, g.Fs / 32, kb_fs, nullptr, g.rs_sdown, g.ki_sdown, s)));
     }
   }
   MOE_TRY(cuda_status(launch_act_quant(g.x_routed, g.routed_rows, g.d, g.xq, g.sx, s)));
@@ -418,11 +508,18 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
     ok = make_x_maps(m.x[1], g.xq_sh, g.d, 2 * (uint64_t)g.T) &&
          make_code_map(&m.w[1], g.sg, g.d, (uint64_t)g.S * g.Fs, mx) &&
          make_code_map(&m.u[1], g.su, g.d, (uint64_t)g.S * g.Fs, mx);
+  if (ok && mx)
+    ok = make_tmap_mx_index(&m.kw[0], g.ki_gate, (uint64_t)g.N * g.F, kb_d) &&
+         make_tmap_mx_index(&m.ku[0], g.ki_up, (uint64_t)g.N * g.F, kb_d) &&
+         (!sh || (make_tmap_mx_index(&m.kw[1], g.ki_sgate, (uint64_t)g.S * g.Fs, kb_d) &&
+                  make_tmap_mx_index(&m.ku[1], g.ki_sup, (uint64_t)g.S * g.Fs, kb_d)));
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
     for (int i = 0; i < kF8XBoxes; ++i) m.x[1][i] = m.x[0][i];
     m.w[1] = m.w[0];
     m.u[1] = m.u[0];
+    m.kw[1] = m.kw[0];
+    m.ku[1] = m.ku[0];
   }
   auto launch = [&](int phase, int epi, const F8Maps& maps, const GemmArgs& args, int64_t bound) {
     return mx ? launch_grouped_gemm_mxfp4(phase, epi, maps, args, bound, s)
@@ -439,7 +536,7 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.tile_start = g.ts_gu;
   a.n_ext[0] = g.F;
   a.n_ext[1] = sh ? g.Fs : g.F;
-  a.k_blocks[0] = a.k_blocks[1] = (g.d + 127) / 128;
+  a.k_blocks[0] = a.k_blocks[1] = kb_d;
   a.w_rows[0] = g.F;
   a.w_rows[1] = sh ? g.Fs : g.F;
   a.h[0] = g.h;
@@ -451,19 +548,12 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
     a.u_scale[0] = g.rs_up;
     a.w_scale[1] = sh ? g.rs_sgate : g.rs_gate;
     a.u_scale[1] = sh ? g.rs_sup : g.rs_up;
-    a.wb_scale[0] = u8(g.wg_scale);
-    a.ub_scale[0] = u8(g.wu_scale);
-    a.wb_scale[1] = sh ? u8(g.sg_scale) : a.wb_scale[0];
-    a.ub_scale[1] = sh ? u8(g.su_scale) : a.ub_scale[0];
   } else {
     a.w_scale[0] = f32(g.wg_scale);
     a.u_scale[0] = f32(g.wu_scale);
     a.w_scale[1] = sh ? f32(g.sg_scale) : a.w_scale[0];
     a.u_scale[1] = sh ? f32(g.su_scale) : a.u_scale[0];
   }
-  a.k_len[0] = a.k_len[1] = g.d;
-  a.q_rows[0] = (int64_t)g.N * g.F;
-  a.q_rows[1] = sh ? (int64_t)g.S * g.Fs : a.q_rows[0];
   a.a_scale[0] = g.sx;
   a.a_scale[1] = sh ? g.sx_sh : g.sx;
   int64_t bound = gemm_tile_bound(kPhaseGateUp, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kF8TileRows);
@@ -479,33 +569,32 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   if (ok && sh)
     ok = make_x_maps(md.x[1], g.hq_sh, g.Fs, 2 * (uint64_t)g.S * g.T) &&
          make_code_map(&md.w[1], g.sd, g.Fs, (uint64_t)g.S * g.d, mx);
+  if (ok && mx)
+    ok = make_tmap_mx_index(&md.kw[0], g.ki_down, (uint64_t)g.N * g.d, kb_f) &&
+         (!sh || make_tmap_mx_index(&md.kw[1], g.ki_sdown, (uint64_t)g.S * g.d, kb_fs));
   if (!ok) return MOE_ERR_CUDA;
   if (!sh) {
     for (int i = 0; i < kF8XBoxes; ++i) md.x[1][i] = md.x[0][i];
     md.w[1] = md.w[0];
+    md.kw[1] = md.kw[0];
   }
   md.u[0] = md.w[0];
   md.u[1] = md.w[1];
+  md.ku[0] = md.kw[0];
+  md.ku[1] = md.kw[1];
   a.tile_start = g.ts_dn;
   a.n_ext[0] = a.n_ext[1] = g.d;
-  a.k_blocks[0] = (g.F + 127) / 128;
-  a.k_blocks[1] = sh ? (g.Fs + 127) / 128 : a.k_blocks[0];
+  a.k_blocks[0] = kb_f;
+  a.k_blocks[1] = sh ? kb_fs : kb_f;
   a.w_rows[0] = a.w_rows[1] = g.d;
   if (mx) {
     a.w_scale[0] = g.rs_down;
     a.w_scale[1] = sh ? g.rs_sdown : g.rs_down;
-    a.wb_scale[0] = u8(g.wd_scale);
-    a.wb_scale[1] = sh ? u8(g.sd_scale) : a.wb_scale[0];
   } else {
     a.w_scale[0] = f32(g.wd_scale);
     a.w_scale[1] = sh ? f32(g.sd_scale) : a.w_scale[0];
   }
   a.u_scale[0] = a.u_scale[1] = nullptr;
-  a.ub_scale[0] = a.ub_scale[1] = nullptr;
-  a.k_len[0] = g.F;
-  a.k_len[1] = sh ? g.Fs : g.F;
-  a.q_rows[0] = (int64_t)g.N * g.d;
-  a.q_rows[1] = sh ? (int64_t)g.S * g.d : a.q_rows[0];
   a.a_scale[0] = g.sh;
   a.a_scale[1] = sh ? g.sh_sh : g.sh;
   a.out_acc = g.out_acc;
@@ -557,6 +646,9 @@ moe_status_t moe_problem_check(const moe_problem_t* p) {
   if (p->expert_dtype == MOE_EXPERT_MXFP4) {  // 32-element scale blocks; code rows in 16-byte units
     if ((p->d_model % 32) != 0 || (p->ffn % 32) != 0) return MOE_ERR_INVALID_ARG;
     if (p->n_shared > 0 && (p->shared_ffn % 32) != 0) return MOE_ERR_INVALID_ARG;
+    // a weight row's block scales are staged whole in shared memory
+    if (p->d_model > kMxMaxK || p->ffn > kMxMaxK || (p->n_shared > 0 && p->shared_ffn > kMxMaxK))
+      return MOE_ERR_UNSUPPORTED;
   }
   if (p->expert_dtype == MOE_EXPERT_FP8_E4M3) {  // 16-byte rows of codes for the TMA boxes
     if ((p->d_model % 16) != 0 || (p->ffn % 16) != 0) return MOE_ERR_INVALID_ARG;
@@ -699,11 +791,7 @@ moe_status_t grouped_swiglu_impl(const moe_problem_t* p, const void* x_perm, con
     g.hq = at<uint8_t>(ws, L.hq);
     g.sh = at<float>(ws, L.sh);
   }
-  if (g.mx) {
-    g.rs_gate = at<float>(ws, L.rs_gate);
-    g.rs_up = at<float>(ws, L.rs_up);
-    g.rs_down = at<float>(ws, L.rs_down);
-  }
+  if (g.mx) set_mx_plan(&g, q, nullptr, ws, L, false);
   g.N = q.n_experts;
   g.S = 0;
   g.F = q.ffn;
@@ -883,16 +971,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.sd_scale = w->ws_down_scale;
   g.mx = is_mx(*p);
   g.offsets = offsets;
-  if (g.mx) {
-    g.rs_gate = at<float>(ws, L.rs_gate);
-    g.rs_up = at<float>(ws, L.rs_up);
-    g.rs_down = at<float>(ws, L.rs_down);
-    if (S > 0) {
-      g.rs_sgate = at<float>(ws, L.rs_sgate);
-      g.rs_sup = at<float>(ws, L.rs_sup);
-      g.rs_sdown = at<float>(ws, L.rs_sdown);
-    }
-  }
+  if (g.mx) set_mx_plan(&g, *p, w, ws, L, S > 0);
   if (fp8) {
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
@@ -993,16 +1072,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.sd_scale = w->ws_down_scale;
   g.mx = is_mx(*p);
   g.offsets = offsets;
-  if (g.mx) {
-    g.rs_gate = at<float>(ws, L.rs_gate);
-    g.rs_up = at<float>(ws, L.rs_up);
-    g.rs_down = at<float>(ws, L.rs_down);
-    if (S > 0) {
-      g.rs_sgate = at<float>(ws, L.rs_sgate);
-      g.rs_sup = at<float>(ws, L.rs_sup);
-      g.rs_sdown = at<float>(ws, L.rs_sdown);
-    }
-  }
+  if (g.mx) set_mx_plan(&g, *p, w, ws, L, S > 0);
   if (fp8) {
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
@@ -1053,7 +1123,47 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
   return layer_forward_impl(p, w, hidden, out, nullptr, nullptr, nullptr, ws, ws_bytes, ev, stream);
 }
 
-int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
+size_t moe_mxfp4_prep_bytes(const moe_problem_t* p) {
+  if (moe_problem_check(p) != MOE_OK || !is_mx(*p)) return 0;
+  size_t total = 0;
+  prep_offsets(*p, &total);
+  return total;
+}
+
+moe_status_t moe_mxfp4_prepare(const moe_problem_t* p, const moe_weights_t* w, void* prep, size_t prep_bytes,
+                               void* stream) {
+  MOE_TRY(moe_problem_check(p));
+  if (!is_mx(*p) || !w || !prep) return MOE_ERR_INVALID_ARG;
+  const bool sh = p->n_shared > 0;
+  if (!w->w_gate_scale || !w->w_up_scale || !w->w_down_scale) return MOE_ERR_INVALID_ARG;
+  if (sh && (!w->ws_gate_scale || !w->ws_up_scale || !w->ws_down_scale)) return MOE_ERR_INVALID_ARG;
+  size_t total = 0;
+  const MxOffsets o = prep_offsets(*p, &total);
+  if ((reinterpret_cast<uintptr_t>(prep) & 255u) != 0 || prep_bytes < total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto u8 = [](const void* q) { return static_cast<const uint8_t*>(q); };
+  const int32_t d = p->d_model, F = p->ffn, Fs = p->shared_ffn;
+  const int32_t kb_d = (d + 127) / 128, kb_f = (F + 127) / 128, kb_fs = (Fs + 127) / 128;
+  const int64_t nf = (int64_t)p->n_experts * F, nd = (int64_t)p->n_experts * d;
+  MOE_TRY(cuda_status(launch_mx_prep(u8(w->w_gate_scale), nf, F, d / 32, kb_d, nullptr, at<float>(prep, o.rs_gate),
+                                     at<uint32_t>(prep, o.ki_gate), s)));
+  MOE_TRY(cuda_status(launch_mx_prep(u8(w->w_up_scale), nf, F, d / 32, kb_d, nullptr, at<float>(prep, o.rs_up),
+                                     at<uint32_t>(prep, o.ki_up), s)));
+  MOE_TRY(cuda_status(launch_mx_prep(u8(w->w_down_scale), nd, d, F / 32, kb_f, nullptr, at<float>(prep, o.rs_down),
+                                     at<uint32_t>(prep, o.ki_down), s)));
+  if (sh) {
+    const int64_t sf = (int64_t)p->n_shared * Fs, sd = (int64_t)p->n_shared * d;
+    MOE_TRY(cuda_status(launch_mx_prep(u8(w->ws_gate_scale), sf, Fs, d / 32, kb_d, nullptr,
+                                       at<float>(prep, o.rs_sgate), at<uint32_t>(prep, o.ki_sgate), s)));
+    MOE_TRY(cuda_status(launch_mx_prep(u8(w->ws_up_scale), sf, Fs, d / 32, kb_d, nullptr,
+                                       at<float>(prep, o.rs_sup), at<uint32_t>(prep, o.ki_sup), s)));
+    MOE_TRY(cuda_status(launch_mx_prep(u8(w->ws_down_scale), sd, d, Fs / 32, kb_fs, nullptr,
+                                       at<float>(prep, o.rs_sdown), at<uint32_t>(prep, o.ki_sdown), s)));
+  }
+  return MOE_OK;
+}
+
+int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights_t* w) {
   if (moe_problem_check(p) != MOE_OK) return 0;
   if (p->T == 0) return 1;  // the histogram scan that writes zero counts
   // route and pack: histogram, scan (+ schedule), scatter -- one kernel for at
@@ -1063,9 +1173,10 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p) {
   const int router = router_plan(p->T, p->d_model, p->n_experts, p->hidden_dtype == MOE_BF16).tensor ? 3 : 2;
   // FP8 experts: the two-term E4M3 split of each GEMM's activations (x, h;
   // and the shared experts' x, h)
-  // (+ MXFP4: the reference scales of gate, up and down rows, and the
-  // shared experts')
-  const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 4 : 2) : 0) + (is_mx(*p) ? (p->n_shared > 0 ? 6 : 3) : 0);
+  // (+ MXFP4 without a prepared buffer: the preparation of gate, up and
+  // down, and of the shared experts')
+  const bool prep = is_mx(*p) && !(w && w->mx_prep);
+  const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 4 : 2) : 0) + (prep ? (p->n_shared > 0 ? 6 : 3) : 0);
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
   return router + route + 3 + quant;

@@ -82,6 +82,61 @@ def test_layer_kernel_count():
     assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, top_k=0)) == 0
 
 
+def _fake_prepared():
+    w = B.Weights()
+    w.mx_prep = 256  # only its nullness is read by the host-side count
+    return w
+
+
+def test_kernel_count_without_per_call_mxfp4_preparation():
+    # a prepared buffer removes the preparation of gate, up and down (and of
+    # the shared experts' three matrices)
+    for cfg, n in ((inputs.GPTOSS_MXFP4, 3), (inputs.GPTOSS_MXFP4.with_(S=1, Fs=256), 6)):
+        p = B.problem(cfg)
+        assert B.layer_forward_kernel_count(p) - B.layer_forward_kernel_count(p, _fake_prepared()) == n
+    p = B.problem(inputs.MIXTRAL_FP8)
+    assert B.layer_forward_kernel_count(p) == B.layer_forward_kernel_count(p, _fake_prepared())
+
+
+def test_mxfp4_prep_bytes_covers_every_array():
+    for cfg in (inputs.GPTOSS_MXFP4, inputs.QWEN_DECODE_MXFP4, inputs.GPTOSS_MXFP4.with_(S=2, Fs=320)):
+        N, S, d, F, Fs = cfg.N, cfg.S, cfg.d, cfg.F, cfg.Fs
+        kb = lambda k: -(-k // 128)  # noqa: E731  (K steps of 128 elements)
+        arrays = [N * F * 4, N * F * 4, N * d * 4, N * F * kb(d) * 4, N * F * kb(d) * 4, N * d * kb(F) * 4]
+        if S:
+            arrays += [S * Fs * 4, S * Fs * 4, S * d * 4, S * Fs * kb(d) * 4, S * Fs * kb(d) * 4,
+                       S * d * kb(Fs) * 4]
+        got = B.mxfp4_prep_bytes(B.problem(cfg))
+        assert sum(arrays) <= got < sum(arrays) + 256 * len(arrays)
+        assert got == B.mxfp4_prep_bytes(B.problem(cfg, T=1))  # weights only, not the batch
+    assert B.mxfp4_prep_bytes(B.problem(inputs.MIXTRAL_FP8)) == 0
+    assert B.mxfp4_prep_bytes(B.problem(inputs.MIXTRAL)) == 0
+
+
+def test_mxfp4_prepare_validates_before_any_cuda_call():
+    w = B.Weights()
+    w.w_gate_scale = w.w_up_scale = w.w_down_scale = 4096
+    P = B.lib.moe_mxfp4_prepare
+    p = B.problem(inputs.GPTOSS_MXFP4)
+    need = B.mxfp4_prep_bytes(p)
+    assert P(ctypes.byref(B.problem(inputs.MIXTRAL_FP8)), ctypes.byref(w), 256, need, None) == B.MOE_ERR_INVALID_ARG
+    assert P(ctypes.byref(p), None, 256, need, None) == B.MOE_ERR_INVALID_ARG
+    assert P(ctypes.byref(p), ctypes.byref(w), None, need, None) == B.MOE_ERR_INVALID_ARG
+    assert P(ctypes.byref(p), ctypes.byref(w), 256 + 16, need, None) == B.MOE_ERR_WORKSPACE
+    assert P(ctypes.byref(p), ctypes.byref(w), 256, need - 1, None) == B.MOE_ERR_WORKSPACE
+    w.w_up_scale = None
+    assert P(ctypes.byref(p), ctypes.byref(w), 256, need, None) == B.MOE_ERR_INVALID_ARG
+    ps = B.problem(inputs.GPTOSS_MXFP4.with_(S=1, Fs=256))  # shared experts need their scales too
+    w.w_up_scale = 4096
+    assert P(ctypes.byref(ps), ctypes.byref(w), 256, B.mxfp4_prep_bytes(ps), None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_mxfp4_rejects_rows_wider_than_the_preparation_stages():
+    assert B.problem_check(B.problem(inputs.GPTOSS_MXFP4.with_(d=32768))) == 0
+    assert B.problem_check(B.problem(inputs.GPTOSS_MXFP4.with_(d=32800))) == B.MOE_ERR_UNSUPPORTED
+    assert B.problem_check(B.problem(inputs.GPTOSS_MXFP4.with_(F=32800))) == B.MOE_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("cfg", list(inputs.CONFIGS.values()), ids=list(inputs.CONFIGS))
 def test_workspace_sizing_for_empty_and_single_token_batches(cfg):
     for T in (0, 1, 3):

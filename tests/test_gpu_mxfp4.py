@@ -135,6 +135,10 @@ def test_mxfp4_full_size_workload(name, cfg, n_sample):
     ins = inputs.make_inputs(cfg, seed=0, device="cuda")
     dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
     out, idx, w, counts = _run_layer(cfg, dev)
+    # the per-call preparation (only the experts in use) gives the same result
+    per_call = B.MoELayer(cfg, dev, mx_prepare=False).forward(dev["hidden"])
+    torch.cuda.synchronize()
+    _assert_same_but_summation_order(out, per_call, name)
     rep = H.compare_router(idx, w, H.oracle_router(cfg, ins))
     assert np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=cfg.N))
     fl = set(rep["flipped_tokens"].tolist())
@@ -142,3 +146,97 @@ def test_mxfp4_full_size_workload(name, cfg, n_sample):
     ref = H.oracle_layer_rows(cfg, ins, rows)
     e = H.assert_output_close(out.float().cpu().numpy()[rows], ref["out"], name)
     print(f"{name}: errors {e}")
+
+
+def _assert_same_but_summation_order(a, b, name):
+    """Two runs of the same GEMMs: the down GEMM adds a token's K expert rows
+    into fp32 with atomics, in no fixed order, so the bf16 outputs may differ
+    by the rounding of that order: one bf16 ulp, or, where the K terms nearly
+    cancel, the fp32 rounding of the terms themselves (bounded here by
+    2^-16 of the largest output), in few elements."""
+    a, b = a.float().cpu().numpy(), b.float().cpu().numpy()
+    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(a), np.abs(b)))[1] - 8)
+    diff = np.abs(a - b)
+    bound = ulp + np.ldexp(float(np.abs(a).max()), -16)
+    assert (diff <= bound).all(), (name, float((diff - bound).max()))
+    assert (diff > 0).mean() < 0.02, (name, float((diff > 0).mean()))
+
+
+def _prep_reference(bscale, nblk):
+    """The preparation of one weight matrix from its E8M0 block scales [rows][nblk]
+    (uint8), as the header defines it: E_R = clamp(max of the row's non-NaN
+    exponents - 6, 1, 254), the fp32 scale 2^(E_R - 127), and index
+    clamp(E_b - E_R, -15, 6) + 15 per block, four per word (block 4kb + c in
+    byte c, 0 past the row's end), K-step-major [kb][rows]."""
+    rows = bscale.shape[0]
+    e = bscale.astype(np.int64)
+    m = np.where(e == 255, 0, e).max(axis=1)
+    e_row = np.clip(m - 6, 1, 254)
+    rs = np.ldexp(1.0, e_row - 127).astype(np.float32)
+    kb = -(-nblk // 4)
+    idx = np.zeros((rows, 4 * kb), np.int64)
+    idx[:, :nblk] = np.clip(e - e_row[:, None], -15, 6) + 15
+    words = (idx.reshape(rows, kb, 4) << (8 * np.arange(4))).sum(axis=2).astype(np.uint32)
+    return rs, words.T.copy()
+
+
+def _prep_arrays(buf, cfg):
+    """Splits a prepared buffer into its arrays (header order, 256-byte aligned)."""
+    N, S, d, F, Fs = cfg.N, cfg.S, cfg.d, cfg.F, cfg.Fs
+    kb = lambda k: -(-k // 128)  # noqa: E731
+    shapes = [("rs", N * F), ("rs", N * F), ("rs", N * d), ("ki", (kb(d), N * F)), ("ki", (kb(d), N * F)),
+              ("ki", (kb(F), N * d))]
+    if S:
+        shapes += [("rs", S * Fs), ("rs", S * Fs), ("rs", S * d), ("ki", (kb(d), S * Fs)),
+                   ("ki", (kb(d), S * Fs)), ("ki", (kb(Fs), S * d))]
+    out, off = [], 0
+    for kind, shp in shapes:
+        n = int(np.prod(shp))
+        a = buf[off:off + 4 * n].view(np.float32 if kind == "rs" else np.uint32).reshape(shp)
+        out.append(a)
+        off = (off + 4 * n + 255) // 256 * 256
+    return out
+
+
+@pytest.mark.parametrize("d,F,Fs", [(288, 160, 96), (256, 128, 512)])
+def test_mxfp4_prepare_matches_its_definition(d, F, Fs):
+    # block scales with NaN blocks, blocks far below the row's largest (the
+    # index clamps at -15) and a row of all-zero exponents (E_R clamps at 1);
+    # rows of 9, 5, 3 blocks (byte-wise staging) and of 8, 4, 16 (word-wise)
+    cfg = _cfg("prep", T=4, d=d, N=4, K=2, F=F, S=1, Fs=Fs)
+    ins = inputs.make_inputs(cfg, seed=3)
+    rng = np.random.default_rng(11)
+    for k in ("w_gate_scale", "w_up_scale", "w_down_scale", "ws_gate_scale", "ws_up_scale", "ws_down_scale"):
+        s = rng.integers(100, 140, size=tuple(ins[k].shape)).astype(np.uint8)
+        flat = s.reshape(-1, s.shape[-1])
+        flat[1, 0] = 255
+        flat[2, :] = 255
+        flat[2, 1] = 120
+        flat[3, -1] = 2
+        flat[4, :] = 0
+        ins[k] = torch.from_numpy(s)
+    dev = {k: (None if v is None else v.cuda().contiguous()) for k, v in ins.items()}
+    layer = B.MoELayer(cfg, dev)
+    torch.cuda.synchronize()
+    got = _prep_arrays(layer.mx_prep.cpu().numpy(), cfg)
+    mats = [("w_gate_scale", cfg.d), ("w_up_scale", cfg.d), ("w_down_scale", cfg.F),
+            ("ws_gate_scale", cfg.d), ("ws_up_scale", cfg.d), ("ws_down_scale", cfg.Fs)]
+    refs = [_prep_reference(ins[k].numpy().reshape(-1, K // 32), K // 32) for k, K in mats]
+    for i, (rs, ki) in enumerate(refs):
+        j = i if i < 3 else i + 3
+        assert np.array_equal(got[j], rs), mats[i][0]
+        assert np.array_equal(got[j + 3], ki), mats[i][0]
+
+
+@pytest.mark.parametrize("name", ["mx_shared_sigmoid", "mx_decode_T3", "mx_ragged", "mx_capacity"])
+def test_mxfp4_prepared_and_per_call_agree(name):
+    cfg = MID[name]
+    ins, dev = H.make_case(cfg)
+    prepared = B.MoELayer(cfg, dev)
+    per_call = B.MoELayer(cfg, dev, mx_prepare=False)
+    assert prepared.mx_prep is not None and per_call.mx_prep is None
+    a = prepared.forward(dev["hidden"])
+    b = per_call.forward(dev["hidden"])
+    torch.cuda.synchronize()
+    assert prepared.status(cfg.T) == 0 and per_call.status(cfg.T) == 0
+    _assert_same_but_summation_order(a, b, name)
