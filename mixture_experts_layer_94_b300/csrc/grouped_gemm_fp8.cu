@@ -406,7 +406,7 @@ constexpr int kMxConv0 = 192;
 constexpr int kMxXWarp = kMxConv0 / 32 + kMxConvWarps;
 constexpr int kMxThreads = (kMxXWarp + 1) * 32;
 constexpr int kMxXStages = 3;
-constexpr int kMxRStages = 4;
+constexpr int kMxRStages = 4;  // even: a code slot is always refilled for the same converter group
 constexpr int kMxWStages = 3;
 constexpr uint32_t kMxRawBytes = (uint32_t)kWRows * (kKq / 2);  // 256 rows x 64 code bytes = 16 KB
 constexpr uint32_t kMxIdxBytes = (uint32_t)kWRows * 4;           // 256 rows x 4 block indices
@@ -419,6 +419,11 @@ constexpr size_t kMxSmem = 1024 + (size_t)kMxXStages * kABytes + (size_t)kMxWSta
 static_assert(8 * kMxNumBars + 8 <= kMxBarrierBytes, "barrier area");
 static_assert(kMxSlotBytes % 512 == 0, "code slots keep the 64-byte swizzle's alignment");
 static_assert(kMxSmem <= 232448, "shared memory per CTA");
+// The code ring's parity waits stay unambiguous because a slot is refilled
+// for the group that emptied it (an even ring). The E4M3 ring alternates
+// between the groups; a group reaches stage n only after the MMA consumed
+// stage n - 3, so its empty-slot wait never skips a phase.
+static_assert(kMxRStages % 2 == 0, "code slots stay with one converter group");
 
 // The eight E4M3 codes (as two table words) of the E2M1 magnitudes 0, 0.5,
 // 1, 1.5, 2, 3, 4, 6 times 2^k, rounded to nearest (exact for -8 <= k <= 6).
@@ -658,7 +663,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             break;
           }
           const uint8_t* slot = gRaw + rs * kMxSlotBytes;
-#pragma unroll 1
+#pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int R = t + 128 * half;
             const uint4* src = reinterpret_cast<const uint4*>(slot + R * (kKq / 2));
