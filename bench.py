@@ -208,6 +208,20 @@ def max_over_ranks(x, world, device="cuda"):
     return float(t.item())
 
 
+def record_event(event):
+    """Record `event` on the current stream; while that stream is being captured
+    into a CUDA graph, as an external record, so that the event stays a timing
+    record of the graph."""
+    stream = torch.cuda.current_stream()
+    if torch.cuda.is_current_stream_capturing():
+        from cuda.bindings import runtime as cudart
+        err, = cudart.cudaEventRecordWithFlags(event.cuda_event, stream.cuda_stream, cudart.cudaEventRecordExternal)
+        if err != cudart.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"cudaEventRecordWithFlags: {err}")
+    else:
+        event.record(stream)
+
+
 def replica_tokens_per_second(tokens_per_rank, steps, elapsed_by_rank, world, device="cuda"):
     """Whole-job throughput of `world` independent replicas: all tokens over the
     slowest rank's elapsed seconds."""
@@ -345,9 +359,7 @@ def config_block(cfg, desc, args):
                if cfg.expert_dtype == "mxfp4" else {}),
             "global_batch": cfg.T * args.gpus,
             "parallelism": f"replicas x{args.gpus}",
-            "l2": "inputs larger than L2 (expert weights stream from HBM every step)"
-            if 3 * cfg.d * cfg.F * {"fp8": 1, "mxfp4": 0.5}.get(cfg.expert_dtype, 2) * cfg.N > 126e6
-            else "L2 not flushed (working set fits in L2)"}
+            "l2": "flushed before every timed step (a write of twice the L2 size, outside the step's events)"}
 
 
 def end_to_end(layer, hidden, out, args, world, cfg):
@@ -431,31 +443,51 @@ def run_ours(args, cfg, desc, world, rank):
         raise RuntimeError(f"device status after first step: {B.status_string(st)}")
     counts_h = counts.cpu().numpy()
 
+    # Every step is timed between its own two events, after a write of twice
+    # the L2 size that evicts the previous step's lines (outside the events):
+    # the touched weights of a small decode batch would otherwise stay cached.
+    # The headline runs the plain moe_layer_forward; a second pass of the same
+    # steps through moe_layer_forward_profiled (an event between stages) gives
+    # the stage breakdown and the dominant kernel's duration.
+    l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda")
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    for e in [e for evs in evp + ev for e in evs]:
+        e.record(stream)  # torch creates an event on its first record
     for _ in range(args.warmup):
-        B.layer_forward_profiled(p, layer.ws_struct, hidden, out, ws, ev[0], stream)
+        flush.zero_()
+        B.layer_forward(p, layer.ws_struct, hidden, out, ws)
+        B.layer_forward_profiled(p, layer.ws_struct, hidden, out, ws, ev[0])
     torch.cuda.synchronize()
 
-    def steps():
+    def plain_steps():
         for i in range(args.steps):
+            flush.zero_()
+            record_event(evp[i][0])
+            B.layer_forward(p, layer.ws_struct, hidden, out, ws)
+            record_event(evp[i][1])
+
+    def profiled_steps():
+        for i in range(args.steps):
+            flush.zero_()
             B.layer_forward_profiled(p, layer.ws_struct, hidden, out, ws, ev[i])
 
-    graph = None
+    graphs = None
     if not args.no_graph:
-        # The K timed steps as one CUDA graph: the same kernels and arguments,
+        # The K timed steps as CUDA graphs: the same kernels and arguments,
         # launched without per-step host work (the library allocates nothing
         # and never synchronises, so a step captures as-is).
-        for evs in ev:
-            for e in evs:
-                e.record(stream)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream()
-        cap.wait_stream(stream)
-        with torch.cuda.graph(graph, stream=cap):
-            steps()
-        stream.wait_stream(cap)
-        graph.replay()  # warm replay
+        graphs = []
+        for fn in (plain_steps, profiled_steps):
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+            stream.wait_stream(cap)
+            g.replay()  # warm replay
+            graphs.append(g)
         torch.cuda.synchronize()
 
     sampler = ClockSampler(torch.cuda.current_device())
@@ -465,21 +497,29 @@ def run_ours(args, cfg, desc, world, rank):
     t_wall0 = time.monotonic()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    if graph is not None:
-        graph.replay()
+    if graphs is not None:
+        graphs[0].replay()
     else:
-        steps()
+        plain_steps()
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.monotonic()
     sampler.stop()
-    value, elapsed_s = replica_tokens_per_second(cfg.T, args.steps, start.elapsed_time(end) / 1e3, world)
+    step_s = [evp[i][0].elapsed_time(evp[i][1]) / 1e3 for i in range(args.steps)]
+    value, elapsed_s = replica_tokens_per_second(cfg.T, args.steps, sum(step_s), world)
+    region_ms = start.elapsed_time(end)
     st = B.get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {B.status_string(st)}")
+    if graphs is not None:
+        graphs[1].replay()
+    else:
+        profiled_steps()
+    torch.cuda.synchronize()
     stage_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j in range(nst)]
+    profiled_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][nst]) for i in range(args.steps))
 
     ms_step = 1e3 * elapsed_s / args.steps
     wm = work_model(cfg, counts_h)
@@ -528,8 +568,10 @@ def run_ours(args, cfg, desc, world, rank):
             "layer_roofline": {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],
                                "t_roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step},
             "stages_ms": dict(zip(B.LAYER_STAGES, stage_ms)),
+            "ms_per_step_profiled": profiled_ms,
+            "timed_region_ms": region_ms,
             "gpu_launches": B.layer_forward_kernel_count(p, layer.ws_struct) * args.steps,
-            "cuda_graph": graph is not None,
+            "cuda_graph": graphs is not None,
             "clocks": clocks}
 
     if not args.no_e2e:

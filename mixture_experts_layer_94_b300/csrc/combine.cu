@@ -16,6 +16,8 @@ namespace {
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc,
                                                        __nv_bfloat16* __restrict__ out, int64_t nvec) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * v];
     const float4 b = reinterpret_cast<const float4*>(acc)[2 * v + 1];
@@ -41,6 +43,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int32_t K, int3
                                                       const float* __restrict__ topk_w,
                                                       const __nv_bfloat16* __restrict__ shared_out,
                                                       __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t vpr = d / 8;  // 16-byte vectors per row
   const int64_t total = T * vpr;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -74,8 +78,8 @@ int grid_for(int64_t work, int threads) {
 cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, int64_t n, cudaStream_t s) {
   const int64_t nvec = n / 8;
   if (nvec == 0) return cudaSuccess;
-  finalize_kernel<<<grid_for(nvec, 256), 256, 0, s>>>(acc, out, nvec);
-  return cudaGetLastError();
+  if (const cudaError_t le_ = launch(finalize_kernel, grid_for(nvec, 256), 256, 0, s, acc, out, nvec); le_ != cudaSuccess) return le_;
+  return cudaSuccess;
 }
 
 cudaError_t launch_combine(int64_t T, int32_t K, int32_t d, const __nv_bfloat16* y_perm, const int32_t* inv_row,
@@ -83,8 +87,8 @@ cudaError_t launch_combine(int64_t T, int32_t K, int32_t d, const __nv_bfloat16*
                            cudaStream_t s) {
   const int64_t work = T * (d / 8);
   if (work == 0) return cudaSuccess;
-  combine_kernel<<<grid_for(work, 256), 256, 0, s>>>(T, K, d, y_perm, inv_row, topk_w, shared_out, out);
-  return cudaGetLastError();
+  if (const cudaError_t le_ = launch(combine_kernel, grid_for(work, 256), 256, 0, s, T, K, d, y_perm, inv_row, topk_w, shared_out, out); le_ != cudaSuccess) return le_;
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -40,6 +40,45 @@ struct GroupDesc {
   int32_t pad0, pad1;
 };
 
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialisation (launch() below): the next kernel in the
+// stream may start once every CTA of this one has called pdl_trigger(), and
+// it runs only its own setup until pdl_wait() returns, which is when the
+// previous grid has completed and its memory writes are visible. Every kernel
+// calls pdl_wait() before its first global-memory access and before any exit,
+// so a grid completes only after its predecessor did and the chain stays
+// transitive (a kernel may read what any earlier kernel of the stream wrote).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches kern<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialisation (see pdl_wait); `extra` adds one more launch attribute (a
+// cluster shape) when its id is not cudaLaunchAttributeIgnore.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_attr(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               const cudaLaunchAttribute& extra, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (extra.id != cudaLaunchAttributeIgnore) attr[cfg.numAttrs++] = extra;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+  cudaLaunchAttribute none{};
+  none.id = cudaLaunchAttributeIgnore;
+  return launch_attr(kern, grid, block, smem, s, none, static_cast<Args&&>(args)...);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

@@ -14,6 +14,8 @@ namespace moe {
 namespace {
 
 __global__ void __launch_bounds__(32) stall_wait_kernel(uint32_t* err, uint64_t limit_ns) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   const uint32_t b = ptx::smem_u32(&bar);
@@ -33,7 +35,8 @@ __global__ void __launch_bounds__(32) stall_wait_kernel(uint32_t* err, uint64_t 
 extern "C" moe_status_t moe_debug_stall_wait(void* ws, size_t ws_bytes, uint32_t timeout_us, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256) return MOE_ERR_WORKSPACE;
   if (timeout_us == 0 || timeout_us > 1000000u) return MOE_ERR_INVALID_ARG;
-  moe::stall_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(ws),
-                                                                         (uint64_t)timeout_us * 1000ull);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return moe::launch(moe::stall_wait_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream), static_cast<uint32_t*>(ws),
+                     (uint64_t)timeout_us * 1000ull) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }

@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmU1,
                         const GemmArgs a) {
+  pdl_trigger();
+  pdl_wait();
   using C = Cfg<PAIR>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kStageB = C::kStageB;
@@ -452,6 +454,7 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int64_t tile_bound, c
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeIgnore;
   if (PAIR == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -476,8 +479,8 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int64_t tile_bound, c
   }
   int64_t units = max_units[dev & 63].load();
   if (tile_bound < units) units = tile_bound < 1 ? 1 : tile_bound;
-  cfg.gridDim = dim3((unsigned)(units * PAIR));
-  return cudaLaunchKernelEx(&cfg, kern, m.a[0], m.a[1], m.b[0], m.b[1], m.bu[0], m.bu[1], a);
+  return launch_attr(kern, dim3((unsigned)(units * PAIR)), dim3(kGemmThreads), smem, s, attr[0], m.a[0], m.a[1],
+                     m.b[0], m.b[1], m.bu[0], m.bu[1], a);
 }
 
 }  // namespace

@@ -207,6 +207,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, int total, uint
 template <int PHASE, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ F8Maps maps, const GemmArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -368,8 +370,8 @@ cudaError_t launch_t(const F8Maps& m, const GemmArgs& a, int64_t tile_bound, cud
   if (e != cudaSuccess) return e;
   int64_t grid = sms;
   if (tile_bound < grid) grid = tile_bound < 1 ? 1 : tile_bound;
-  kern<<<(unsigned)grid, kThreads, kSmem, s>>>(m, a);
-  return cudaGetLastError();
+  if (const cudaError_t le_ = launch(kern, (unsigned)grid, kThreads, kSmem, s, m, a); le_ != cudaSuccess) return le_;
+  return cudaSuccess;
 }
 
 // ============================================================================
@@ -461,6 +463,8 @@ __device__ __forceinline__ void e2m1x8_to_e4m3x8(uint32_t w, uint2 tab, uint32_t
 template <int PHASE, int EPI>
 __global__ void __launch_bounds__(kMxThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ F8Maps maps, const GemmArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -733,6 +737,8 @@ __global__ void __launch_bounds__(kMxPrepRows) mx_prep_kernel(const uint8_t* __r
                                                               int32_t kblocks, const int32_t* __restrict__ offsets,
                                                               float* __restrict__ row_scale,
                                                               uint32_t* __restrict__ kidx) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t st[];  // [kMxPrepRows][pitch] words
   const int pitch = mx_prep_pitch(nblk);
   const int t = threadIdx.x;
@@ -842,8 +848,8 @@ cudaError_t launch_mx(const F8Maps& m, const GemmArgs& a, int64_t tile_bound, cu
   if (e != cudaSuccess) return e;
   int64_t grid = sms;
   if (tile_bound < grid) grid = tile_bound < 1 ? 1 : tile_bound;
-  kern<<<(unsigned)grid, kMxThreads, kMxSmem, s>>>(m, a);
-  return cudaGetLastError();
+  if (const cudaError_t le_ = launch(kern, (unsigned)grid, kMxThreads, kMxSmem, s, m, a); le_ != cudaSuccess) return le_;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -876,9 +882,8 @@ cudaError_t launch_mx_prep(const uint8_t* bscale, int64_t rows, int32_t rows_per
   }
   const int64_t want = (rows + kMxPrepRows - 1) / kMxPrepRows;
   const unsigned grid = (unsigned)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
-  mx_prep_kernel<<<grid, kMxPrepRows, smem, s>>>(bscale, rows, rows_per_expert, nblk, kblocks, offsets, row_scale,
-                                                 kidx);
-  return cudaGetLastError();
+  return launch(mx_prep_kernel, grid, kMxPrepRows, smem, s, bscale, rows, rows_per_expert, nblk, kblocks, offsets,
+                row_scale, kidx);
 }
 
 }  // namespace moe

@@ -49,6 +49,8 @@ __device__ __forceinline__ void build_chunk_masks(uint32_t* masks, const int32_t
 }
 
 __global__ void __launch_bounds__(kHistWarps * 32) route_hist_kernel(const PermuteArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t masks[kHistWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t c = (int64_t)blockIdx.x * kHistWarps + warp;
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(kHistWarps * 32) route_hist_kernel(const Permu
 // of the kept counts min(counts[e], capacity), and
 // chunk_counts[e][c] <- sum_{c' < c} chunk_counts[e][c'] (the rank base).
 __global__ void __launch_bounds__(1024) route_scan_kernel(const PermuteArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int32_t s_counts[kMaxExperts];
   __shared__ int32_t s_offsets[kMaxExperts + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -131,6 +135,8 @@ constexpr int kScatterWarps = 8;
 // One warp per chunk: each copy's row = its chunk's base for the expert plus
 // its rank among the chunk's earlier tokens that chose the same expert.
 __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const PermuteArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t masks[kScatterWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t c = (int64_t)blockIdx.x * kScatterWarps + warp;
@@ -188,37 +194,53 @@ __device__ __forceinline__ uint4 act_vec(const PermuteArgs& a, int64_t t, int v,
   return a.act_f16 ? cvt8_f16(p, q, over) : cvt8_bf16(p, q);
 }
 
-// Row gather into expert order, one warp per permuted row, 16-byte vectors;
-// grid-stride over rows so every SM streams. The fused layer also clears the
-// fp32 accumulator and writes a copy of hidden in the activation format
-// (shared experts) when hidden is not already in it. Activations are bf16 for
-// bf16 experts and fp16 for FP8 experts; a value beyond fp16's range is
-// reported through the error word.
+// Row gather into expert order: one thread per 16-byte output vector (8
+// elements), grid-stride, each thread with kGatherBatch vectors' loads in
+// flight at once, so that a small batch (a few rows) costs one index load and
+// one data load of latency rather than a chain of them. The fused layer also
+// clears the fp32 accumulator and writes a copy of hidden in the activation
+// format (shared experts) when hidden is not already in it. Activations are
+// bf16 for bf16 experts and fp16 for FP8 experts; a value beyond fp16's range
+// is reported through the error word.
+constexpr int kGatherBatch = 4;
+
 __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, int64_t rows) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_trigger();
+  pdl_wait();
   const int d = a.d, nvec = d / 8;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   // Only rows [0, offsets[N]) are placed; fewer than T*K when an input index
   // was out of range (reported through the error word).
   const int64_t placed = min(rows, (int64_t)__ldg(a.offsets + a.N));
+  const int64_t total = placed * nvec;
   bool over = false;
-  for (int64_t r = warp0; r < placed; r += nwarps) {
-    int64_t t;
-    if (a.row_token) {
-      t = a.row_token[r];
-      if (t < 0 || t >= a.T) continue;
-    } else {
-      const int32_t src = a.perm_src[r];
-      if (src < 0 || src >= rows) continue;
-      t = src / a.K;
+  uint4* xp = reinterpret_cast<uint4*>(a.x_perm);
+  for (int64_t i0 = tid; i0 < total; i0 += kGatherBatch * nthr) {
+    uint4 val[kGatherBatch];
+    int64_t at[kGatherBatch];
+#pragma unroll
+    for (int u = 0; u < kGatherBatch; ++u) {
+      const int64_t i = i0 + u * nthr;
+      at[u] = -1;
+      if (i >= total) continue;
+      const int64_t r = i / nvec;
+      int64_t t;
+      if (a.row_token) {
+        t = a.row_token[r];
+        if (t < 0 || t >= a.T) continue;
+      } else {
+        const int32_t src = a.perm_src[r];
+        if (src < 0 || src >= rows) continue;
+        t = src / a.K;
+      }
+      val[u] = act_vec(a, t, (int)(i - r * nvec), over);
+      at[u] = i;
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.x_perm) + r * nvec;
-#pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) dst[v] = act_vec(a, t, v, over);
+#pragma unroll
+    for (int u = 0; u < kGatherBatch; ++u)
+      if (at[u] >= 0) xp[at[u]] = val[u];
   }
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   if (a.zero_rows) {
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     float4* z = reinterpret_cast<float4*>(a.zero_rows);
@@ -295,6 +317,8 @@ __device__ void schedule_block(int N, int S, int F, int Fs, int d, int tile_rows
 }
 
 __global__ void __launch_bounds__(512) schedule_kernel(const ScheduleArgs a) {
+  pdl_trigger();
+  pdl_wait();
   schedule_block(a.N, a.S, a.F, a.Fs, a.d, a.tile_rows, a.T, a.offsets, a.groups, a.tile_start_gu,
                  a.tile_start_dn);
 }
@@ -304,6 +328,8 @@ __global__ void __launch_bounds__(512) schedule_kernel(const ScheduleArgs a) {
 constexpr int kSmallChunks = 32;
 
 __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t masks[kSmallChunks][kMaxExperts];
   __shared__ int32_t s_offsets[kMaxExperts + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -375,37 +401,30 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) 
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
   if (a.C == 0) {  // T == 0: empty histogram, offsets all zero
-    route_scan_kernel<<<1, 1024, 0, s>>>(a);
-    return cudaGetLastError();
+    if (const cudaError_t le_ = launch(route_scan_kernel, 1, 1024, 0, s, a); le_ != cudaSuccess) return le_;
+    return cudaSuccess;
   }
   if (a.C <= kSmallChunks) {
-    route_small_kernel<<<1, 1024, 0, s>>>(a);
+    if (const cudaError_t le_ = launch(route_small_kernel, 1, 1024, 0, s, a); le_ != cudaSuccess) return le_;
   } else {
-    route_hist_kernel<<<(unsigned)((a.C + kHistWarps - 1) / kHistWarps), kHistWarps * 32, 0, s>>>(a);
-    route_scan_kernel<<<1, 1024, 0, s>>>(a);
-    route_scatter_kernel<<<(unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s>>>(a);
+    if (const cudaError_t le_ = launch(route_hist_kernel, (unsigned)((a.C + kHistWarps - 1) / kHistWarps), kHistWarps * 32, 0, s, a); le_ != cudaSuccess) return le_;
+    if (const cudaError_t le_ = launch(route_scan_kernel, 1, 1024, 0, s, a); le_ != cudaSuccess) return le_;
+    if (const cudaError_t le_ = launch(route_scatter_kernel, (unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s, a); le_ != cudaSuccess) return le_;
   }
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t rows = a.T * a.K;
-  const int64_t want = (rows + 7) / 8;  // 8 rows (warps) per 256-thread CTA
-  const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
-  gather_rows_kernel<<<grid, 256, 0, s>>>(a, rows);
-  return cudaGetLastError();
+  return launch_gather(a, a.T * a.K, s);
 }
 
 cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (rows + 7) / 8;
+  const int64_t want = (rows * (a.d / 8) + 255) / 256;  // one 16-byte vector per thread
   const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
-  gather_rows_kernel<<<grid, 256, 0, s>>>(a, rows);
-  return cudaGetLastError();
+  return launch(gather_rows_kernel, grid, 256, 0, s, a, rows);
 }
 
 cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
-  schedule_kernel<<<1, 512, 0, s>>>(a);
-  return cudaGetLastError();
+  if (const cudaError_t le_ = launch(schedule_kernel, 1, 512, 0, s, a); le_ != cudaSuccess) return le_;
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -26,6 +26,8 @@
 //      K-round shuffle argmax over (key desc, expert asc); slot k ends in lane k.
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -65,6 +67,8 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 // NP: N rounded up to a power of two; TPW tokens per warp.
 template <int NP, int TPW, typename XT>
 __global__ void __launch_bounds__(kWarps * 32) logits_small_n_kernel(const RouterArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N, d = a.d;
   const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * TPW;
@@ -133,6 +137,8 @@ constexpr int kDChunk = 32;
 
 template <int EPL, typename XT>
 __global__ void __launch_bounds__(kWarps * 32) logits_large_n_kernel(const RouterArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NCOL = 32 * EPL;
   constexpr int W_PER_THR = kDChunk * NCOL / (kWarps * 32);       // EPL * 4
   constexpr int X_PER_THR = kTokPerCtaL * kDChunk / (kWarps * 32);  // 4
@@ -211,9 +217,88 @@ __global__ void __launch_bounds__(kWarps * 32) logits_large_n_kernel(const Route
   }
 }
 
+// ---------------------------------------------------------------- R1, N > 32, staged
+// The same partial logits when a CTA's d slice fits in shared memory (decode
+// batches): the slice of W_router (rows j_begin.., N floats each, contiguous)
+// and of the tile's 32 token rows are copied in with cp.async, every 16-byte
+// piece in flight at once, so the CTA pays one load latency instead of one per
+// 32-row chunk; then the FMAs read shared memory only. N % 4 == 0 and d % 8 ==
+// 0 (16-byte pieces of both rows).
+constexpr size_t kStagedMaxSmem = 100 * 1024;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+template <int EPL, typename XT>
+size_t staged_smem(int d_slice) {
+  return (size_t)d_slice * 32 * EPL * sizeof(float) + (size_t)kTokPerCtaL * d_slice * sizeof(XT);
+}
+
+template <int EPL, typename XT>
+__global__ void __launch_bounds__(kWarps * 32) logits_staged_kernel(const RouterArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int NCOL = 32 * EPL;
+  constexpr int XV = 16 / sizeof(XT);  // elements of hidden per 16-byte piece
+  extern __shared__ __align__(16) float st[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t t0 = (int64_t)blockIdx.x * kTokPerCtaL;
+  const int N = a.N, d = a.d, ds = a.d_slice;
+  const int j_begin = blockIdx.y * ds, jn = min(d - j_begin, ds);
+  float* ws = st;                                         // [ds][NCOL]
+  XT* xs = reinterpret_cast<XT*>(st + (size_t)ds * NCOL);  // [kTokPerCtaL][ds]
+  const XT* x = static_cast<const XT*>(a.hidden);
+  for (int i = tid; i < ds * (NCOL / 4); i += kWarps * 32) {
+    const int j = i / (NCOL / 4), c = 4 * (i % (NCOL / 4));
+    const bool ok = j < jn && c < N;
+    cp_async16(ws + j * NCOL + c, ok ? a.w_router + (int64_t)(j_begin + j) * N + c : a.w_router, ok);
+  }
+  for (int i = tid; i < kTokPerCtaL * (ds / XV); i += kWarps * 32) {
+    const int tk = i / (ds / XV), c = XV * (i % (ds / XV));
+    const bool ok = t0 + tk < a.T && c < jn;
+    cp_async16(xs + tk * ds + c, ok ? x + (t0 + tk) * d + j_begin + c : x, ok);
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  float acc[kTokPerWarpL][EPL];
+#pragma unroll
+  for (int t = 0; t < kTokPerWarpL; ++t)
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) acc[t][i] = 0.f;
+  const XT* xw = xs + warp * kTokPerWarpL * ds;
+#pragma unroll 4
+  for (int j = 0; j < jn; ++j) {
+    float w[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) w[i] = ws[j * NCOL + lane + 32 * i];
+#pragma unroll
+    for (int t = 0; t < kTokPerWarpL; ++t) {
+      const float xv = to_f<XT>(xw[t * ds + j]);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) acc[t][i] = fmaf(xv, w[i], acc[t][i]);
+    }
+  }
+  float* part = a.partial + (int64_t)blockIdx.y * a.T * N;
+#pragma unroll
+  for (int t = 0; t < kTokPerWarpL; ++t) {
+    const int64_t tt = t0 + warp * kTokPerWarpL + t;
+    if (tt >= a.T) break;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < N) part[tt * N + e] = acc[t][i];
+    }
+  }
+}
+
 // ---------------------------------------------------------------- R2
 template <int EPL>
 __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s_key[kWarps][kMaxExperts];
   __shared__ unsigned char s_kept[kWarps][kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -223,27 +308,29 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
   float key[EPL], sc[EPL], lg[EPL];
   bool valid[EPL];
   // Partials summed in split order (deterministic). All of a lane's experts
-  // load 8 splits at a time, so EPL x 8 loads are in flight together.
+  // load kSplitBatch splits at a time, so EPL x kSplitBatch loads are in
+  // flight together (two round trips for the 32 splits of a decode batch).
   {
+    constexpr int kSplitBatch = EPL <= 4 ? 16 : 8;
     const int64_t stride = a.T * N;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       valid[i] = lane + 32 * i < N;
       lg[i] = 0.f;
     }
-    for (int s0 = 0; s0 < a.splits; s0 += 8) {
-      float v[EPL][8];
+    for (int s0 = 0; s0 < a.splits; s0 += kSplitBatch) {
+      float v[EPL][kSplitBatch];
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const float* pp = a.partial + t * N + lane + 32 * i;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < kSplitBatch; ++q)
           v[i][q] = (valid[i] && s0 + q < a.splits) ? __ldg(pp + (int64_t)(s0 + q) * stride) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) lg[i] += v[i][q];
+        for (int q = 0; q < kSplitBatch; ++q) lg[i] += v[i][q];
     }
   }
 #pragma unroll
@@ -427,6 +514,8 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
 // 32 x 32 tiles through shared memory: coalesced reads along e, writes along j.
 __global__ void __launch_bounds__(256) split_router_kernel(const float* __restrict__ w, int d, int N, int np,
                                                            int d_pad, __nv_bfloat16* __restrict__ w3) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float tile[32][33];
   const int j0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
@@ -453,9 +542,7 @@ __global__ void __launch_bounds__(256) split_router_kernel(const float* __restri
 
 cudaError_t launch_tensor_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_t s) {
   const dim3 sgrid((unsigned)((pl.d_pad + 31) / 32), (unsigned)((pl.np + 31) / 32));
-  split_router_kernel<<<sgrid, 256, 0, s>>>(a.w_router, a.d, a.N, pl.np, pl.d_pad, a.w3);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (const cudaError_t le_ = launch(split_router_kernel, sgrid, 256, 0, s, a.w_router, a.d, a.N, pl.np, pl.d_pad, a.w3); le_ != cudaSuccess) return le_;
   GemmMaps m{};
   if (!make_tmap_bf16(&m.a[0], a.hidden, (uint64_t)a.d, (uint64_t)a.T, kBM) ||
       !make_tmap_bf16(&m.b[0], a.w3, (uint64_t)3 * pl.d_pad, (uint64_t)pl.np, (uint32_t)pl.np))
@@ -518,6 +605,8 @@ __global__ void __launch_bounds__(kSelThreads) expert_choice_select_kernel(const
                                                                             int64_t T, int32_t N, int32_t C,
                                                                             int32_t* row_token, float* row_w,
                                                                             int32_t* offsets, int32_t* counts) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int hist[256];
   __shared__ int s_warp[33];
   __shared__ uint32_t s_prefix;
@@ -581,25 +670,47 @@ __global__ void __launch_bounds__(kSelThreads) expert_choice_select_kernel(const
   }
 }
 
+// N > 32: the staged kernel when the slice fits in shared memory and the rows
+// split into 16-byte pieces, else the chunked one.
+template <int EPL, typename XT>
+cudaError_t launch_large_n(const RouterArgs& a, const RouterPlan& pl, dim3 grid, dim3 block, cudaStream_t s) {
+  const size_t smem = staged_smem<EPL, XT>(pl.d_slice);
+  if (a.N % 4 == 0 && a.d % 8 == 0 && smem <= kStagedMaxSmem) {
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+      e = cudaFuncSetAttribute(logits_staged_kernel<EPL, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kStagedMaxSmem);
+      if (e != cudaSuccess) return e;
+      configured.fetch_or(bit);
+    }
+    return launch(logits_staged_kernel<EPL, XT>, grid, block, smem, s, a);
+  }
+  return launch(logits_large_n_kernel<EPL, XT>, grid, block, 0, s, a);
+}
+
 template <typename XT>
 cudaError_t launch_logits(const RouterArgs& a, const RouterPlan& pl, cudaStream_t s) {
   const dim3 grid((unsigned)pl.token_tiles, (unsigned)pl.splits), block(kWarps * 32);
   const int N = a.N;
   if (N <= 32) {
-    if (pl.np == 1) logits_small_n_kernel<1, 4, XT><<<grid, block, 0, s>>>(a);
-    else if (pl.np == 2) logits_small_n_kernel<2, 4, XT><<<grid, block, 0, s>>>(a);
-    else if (pl.np == 4) logits_small_n_kernel<4, 4, XT><<<grid, block, 0, s>>>(a);
-    else if (pl.np == 8) logits_small_n_kernel<8, 4, XT><<<grid, block, 0, s>>>(a);
-    else if (pl.np == 16) logits_small_n_kernel<16, 2, XT><<<grid, block, 0, s>>>(a);
-    else logits_small_n_kernel<32, 1, XT><<<grid, block, 0, s>>>(a);
+    if (pl.np == 1) { if (const cudaError_t le_ = launch(logits_small_n_kernel<1, 4, XT>, grid, block, 0, s, a); le_ != cudaSuccess) return le_; }
+    else if (pl.np == 2) { if (const cudaError_t le_ = launch(logits_small_n_kernel<2, 4, XT>, grid, block, 0, s, a); le_ != cudaSuccess) return le_; }
+    else if (pl.np == 4) { if (const cudaError_t le_ = launch(logits_small_n_kernel<4, 4, XT>, grid, block, 0, s, a); le_ != cudaSuccess) return le_; }
+    else if (pl.np == 8) { if (const cudaError_t le_ = launch(logits_small_n_kernel<8, 4, XT>, grid, block, 0, s, a); le_ != cudaSuccess) return le_; }
+    else if (pl.np == 16) { if (const cudaError_t le_ = launch(logits_small_n_kernel<16, 2, XT>, grid, block, 0, s, a); le_ != cudaSuccess) return le_; }
+    else { if (const cudaError_t le_ = launch(logits_small_n_kernel<32, 1, XT>, grid, block, 0, s, a); le_ != cudaSuccess) return le_; }
   } else if (N <= 64) {
-    logits_large_n_kernel<2, XT><<<grid, block, 0, s>>>(a);
+    return launch_large_n<2, XT>(a, pl, grid, block, s);
   } else if (N <= 128) {
-    logits_large_n_kernel<4, XT><<<grid, block, 0, s>>>(a);
+    return launch_large_n<4, XT>(a, pl, grid, block, s);
   } else {
-    logits_large_n_kernel<8, XT><<<grid, block, 0, s>>>(a);
+    return launch_large_n<8, XT>(a, pl, grid, block, s);
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -665,8 +776,8 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
 cudaError_t launch_expert_choice_select(const float* scores_t, int64_t T, int32_t N, int32_t C,
                                         int32_t* row_token, float* row_w, int32_t* offsets, int32_t* counts,
                                         cudaStream_t s) {
-  expert_choice_select_kernel<<<N, kSelThreads, 0, s>>>(scores_t, T, N, C, row_token, row_w, offsets, counts);
-  return cudaGetLastError();
+  if (const cudaError_t le_ = launch(expert_choice_select_kernel, N, kSelThreads, 0, s, scores_t, T, N, C, row_token, row_w, offsets, counts); le_ != cudaSuccess) return le_;
+  return cudaSuccess;
 }
 
 cudaError_t launch_router(const RouterArgs& a0, bool hidden_bf16, cudaStream_t s) {
@@ -679,11 +790,11 @@ cudaError_t launch_router(const RouterArgs& a0, bool hidden_bf16, cudaStream_t s
                   : (hidden_bf16 ? launch_logits<__nv_bfloat16>(a, pl, s) : launch_logits<float>(a, pl, s));
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((a.T + kWarps - 1) / kWarps);
-  if (a.N <= 32) topk_kernel<1><<<grid, kWarps * 32, 0, s>>>(a);
-  else if (a.N <= 64) topk_kernel<2><<<grid, kWarps * 32, 0, s>>>(a);
-  else if (a.N <= 128) topk_kernel<4><<<grid, kWarps * 32, 0, s>>>(a);
-  else topk_kernel<8><<<grid, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.N <= 32) { if (const cudaError_t le_ = launch(topk_kernel<1>, grid, kWarps * 32, 0, s, a); le_ != cudaSuccess) return le_; }
+  else if (a.N <= 64) { if (const cudaError_t le_ = launch(topk_kernel<2>, grid, kWarps * 32, 0, s, a); le_ != cudaSuccess) return le_; }
+  else if (a.N <= 128) { if (const cudaError_t le_ = launch(topk_kernel<4>, grid, kWarps * 32, 0, s, a); le_ != cudaSuccess) return le_; }
+  else { if (const cudaError_t le_ = launch(topk_kernel<8>, grid, kWarps * 32, 0, s, a); le_ != cudaSuccess) return le_; }
+  return cudaSuccess;
 }
 
 }  // namespace moe
