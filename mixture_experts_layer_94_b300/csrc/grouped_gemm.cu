@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmU1,
                         const GemmArgs a) {
   pdl_trigger();
-  pdl_wait();
   using C = Cfg<PAIR>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kStageB = C::kStageB;
@@ -120,7 +119,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const bool leader = rank == 0;
   const int unit = PAIR == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int units = PAIR == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int total = (PHASE == kPhaseRouter) ? a.r_tiles : __ldg(a.tile_start + a.G);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -155,6 +153,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (PAIR == 2) ptx::cluster_sync();  // the peer's barriers are initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The setup above touches shared memory, TMEM and kernel parameters only;
+  // from here on the previous kernel's results are read.
+  pdl_wait();
+  const int total = (PHASE == kPhaseRouter) ? a.r_tiles : __ldg(a.tile_start + a.G);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer

@@ -208,7 +208,6 @@ template <int PHASE, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ F8Maps maps, const GemmArgs a) {
   pdl_trigger();
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -226,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * (2 * kStages + 5) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = __ldg(a.tile_start + a.G);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -254,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The setup above touches shared memory, TMEM and kernel parameters only;
+  // from here on the previous kernel's results are read.
+  pdl_wait();
+  const int total = __ldg(a.tile_start + a.G);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -464,7 +466,6 @@ template <int PHASE, int EPI>
 __global__ void __launch_bounds__(kMxThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ F8Maps maps, const GemmArgs a) {
   pdl_trigger();
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -492,7 +493,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gBar + 8 * kMxNumBars + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = __ldg(a.tile_start + a.G);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMxXStages; ++s) {
@@ -536,6 +536,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The setup above touches shared memory, TMEM and kernel parameters only;
+  // from here on the previous kernel's results are read.
+  pdl_wait();
+  const int total = __ldg(a.tile_start + a.G);
 
   if (warp == 0 || warp == kMxXWarp) {
     // ------------------------------------------------------------ TMA producers
