@@ -216,15 +216,36 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
   const int64_t total = placed * nvec;
   bool over = false;
   uint4* xp = reinterpret_cast<uint4*>(a.x_perm);
-  for (int64_t i0 = tid; i0 < total; i0 += kGatherBatch * nthr) {
+  // Item i = (row i / nvec, vector i % nvec). A thread's items are tid + k *
+  // nthr; their (row, vector) pairs advance by a fixed step, so no division
+  // is done per vector.
+  const int64_t adv = (int64_t)kGatherBatch * nthr;
+  const int64_t adv_r = adv / nvec;
+  const int adv_v = (int)(adv - adv_r * nvec);
+  int64_t rr[kGatherBatch];
+  int vv[kGatherBatch];
+#pragma unroll
+  for (int u = 0; u < kGatherBatch; ++u) {
+    const int64_t i = tid + u * nthr;
+    rr[u] = i / nvec;
+    vv[u] = (int)(i - rr[u] * nvec);
+  }
+  for (int64_t i0 = tid; i0 < total; i0 += adv) {
     uint4 val[kGatherBatch];
     int64_t at[kGatherBatch];
 #pragma unroll
     for (int u = 0; u < kGatherBatch; ++u) {
       const int64_t i = i0 + u * nthr;
+      const int64_t r = rr[u];
+      const int v = vv[u];
+      vv[u] += adv_v;
+      rr[u] += adv_r;
+      if (vv[u] >= nvec) {
+        vv[u] -= nvec;
+        ++rr[u];
+      }
       at[u] = -1;
       if (i >= total) continue;
-      const int64_t r = i / nvec;
       int64_t t;
       if (a.row_token) {
         t = a.row_token[r];
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const PermuteArgs a, i
         if (src < 0 || src >= rows) continue;
         t = src / a.K;
       }
-      val[u] = act_vec(a, t, (int)(i - r * nvec), over);
+      val[u] = act_vec(a, t, v, over);
       at[u] = i;
     }
 #pragma unroll
