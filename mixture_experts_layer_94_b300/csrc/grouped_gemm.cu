@@ -489,8 +489,8 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int64_t tile_bound, c
 
 int64_t gemm_tile_bound(int phase, int64_t routed_rows, int32_t N, int32_t S, int64_t T, int32_t F,
                         int32_t Fs, int32_t d, int32_t tile_rows) {
-  // sum_e ceil(n_e / BM) <= routed_rows / BM + N
-  const int64_t m_routed = routed_rows / tile_rows + N;
+  // sum_e ceil(n_e / BM) <= routed_rows / BM + (experts with rows) <= routed_rows / BM + min(N, routed_rows)
+  const int64_t m_routed = routed_rows / tile_rows + (routed_rows < N ? routed_rows : N);
   const int64_t m_shared = (int64_t)S * ((T + tile_rows - 1) / tile_rows);
   if (phase == kPhaseGateUp)
     return m_routed * ((F + kBNGateUp - 1) / kBNGateUp) + m_shared * ((Fs + kBNGateUp - 1) / kBNGateUp);

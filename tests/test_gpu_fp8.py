@@ -42,6 +42,9 @@ MID = {
     "fp8_two_shared_f32": _cfg("fp8_two_shared_f32", T=130, d=128, N=8, K=2, F=128, S=2, Fs=64,
                                hidden_dtype="f32", score="sigmoid"),
     "fp8_capacity": _cfg("fp8_capacity", T=300, d=272, N=16, K=4, F=400, capacity_factor=0.8),
+    # small batches with few GEMM tiles (a shared expert; a ragged K)
+    "fp8_small_shared": _cfg("fp8_small_shared", T=2, d=2048, N=64, K=4, F=272, S=1, Fs=256),
+    "fp8_small_ragged": _cfg("fp8_small_ragged", T=5, d=1552, N=32, K=3, F=400),
 }
 
 

@@ -35,6 +35,8 @@ MID = {
     "mx_decode_T3": _cfg("mx_decode_T3", T=3, d=1024, N=128, K=8, F=64),
     "mx_gptoss_like": _cfg("mx_gptoss_like", T=200, d=320, N=32, K=4, F=320),
     "mx_capacity": _cfg("mx_capacity", T=300, d=288, N=16, K=4, F=416, capacity_factor=0.8),
+    # a small batch with few GEMM tiles and a shared expert
+    "mx_small_shared": _cfg("mx_small_shared", T=2, d=2048, N=64, K=4, F=288, S=1, Fs=256),
 }
 
 
