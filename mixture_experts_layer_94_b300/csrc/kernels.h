@@ -72,6 +72,14 @@ struct PermuteArgs {
   float* zero_rows;       // [T][d] fp32 to clear, or nullptr
   void* x_act;            // [T][d] copy of hidden in the activation format, or nullptr
   bool act_f16;           // activations for FP8-weight experts: fp16 rows
+  // FP8 / MXFP4 experts in the fused layer: when xq is set the gather writes
+  // the two-term E4M3 split of each packed row (xq [2 rows][d], sx [rows])
+  // instead of x_perm, and of every token's row for the shared experts
+  // (xq_sh [2T][d], sx_sh [T]) when xq_sh is set; see launch_gather_quant.
+  uint8_t* xq;
+  float* sx;
+  uint8_t* xq_sh;
+  float* sx_sh;
   uint32_t* err;
   // Optional: also build the GEMM schedule (as launch_schedule) from the new
   // offsets; skipped when groups == nullptr.
@@ -159,6 +167,11 @@ struct F8Maps {
 // An activation matrix for the FP8-weight GEMMs: src fp16 [rows][K] ->
 // dst uint8 [2*rows][K] (row 2r = hi, 2r+1 = lo E4M3 terms) and scale fp32
 // [rows], with src[r] ~= scale[r] * (hi + lo). K % 8 == 0.
+// The row gather of the fused layer with the activation split folded in:
+// packed row r's token row of hidden, rounded to fp16 as the gather stores it,
+// split into xq / sx; then `shared_rows` token rows in order into xq_sh /
+// sx_sh. Also clears zero_rows and reports an fp16 overflow, as the gather.
+cudaError_t launch_gather_quant(const PermuteArgs& a, int64_t rows, int64_t shared_rows, cudaStream_t s);
 cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* dst, float* scale,
                              cudaStream_t s);
 // uint8 row-major matrix [rows][inner] as a TMA tensor map: box

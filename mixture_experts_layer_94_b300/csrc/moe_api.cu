@@ -283,6 +283,7 @@ struct GemmPlan {
   bool fp8;               // FP8 or MXFP4 weights (+ the scales below), fp16 activations
   bool mx;                // MXFP4: *_scale are E8M0 block scales; rs_* the rows' reference scales
   bool mx_prepared;       // MXFP4: rs_* / ki_* were filled by moe_mxfp4_prepare (no per-call preparation)
+  bool x_quantized;       // FP8 / MXFP4: xq / sx (and xq_sh / sx_sh) were written by the gather
   int32_t N, S, F, Fs, d, K;
   int64_t T, routed_rows;
   const void* x_routed;   // [routed_rows][d] bf16
@@ -376,6 +377,20 @@ void set_mx_plan(GemmPlan* g, const moe_problem_t& p, const moe_weights_t* w, vo
   } else {
     set_mx_arrays(g, ws, L.mx, shared);
   }
+}
+
+// FP8 / MXFP4 experts in the fused layer: the gather writes the two-term E4M3
+// split of the packed rows (and of the shared experts' token rows) directly;
+// no x_perm or activation copy is needed.
+void set_gather_quant(PermuteArgs* pa, void* ws, const Layout& L, bool shared) {
+  pa->xq = at<uint8_t>(ws, L.xq);
+  pa->sx = at<float>(ws, L.sx);
+  if (shared) {
+    pa->xq_sh = at<uint8_t>(ws, L.xq_sh);
+    pa->sx_sh = at<float>(ws, L.sx_sh);
+  }
+  pa->x_perm = nullptr;
+  pa->x_act = nullptr;
 }
 
 // While the stream is being captured into a CUDA graph, an external record
@@ -498,8 +513,10 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
       MOE_TRY(cuda_status(launch_mx_prep(u8(g.sd_scale), sd, g.d, g.Fs / 32, kb_fs, nullptr, g.rs_sdown, g.ki_sdown, s)));
     }
   }
-  MOE_TRY(cuda_status(launch_act_quant(g.x_routed, g.routed_rows, g.d, g.xq, g.sx, s)));
-  if (sh) MOE_TRY(cuda_status(launch_act_quant(g.x_shared, g.T, g.d, g.xq_sh, g.sx_sh, s)));
+  if (!g.x_quantized) {
+    MOE_TRY(cuda_status(launch_act_quant(g.x_routed, g.routed_rows, g.d, g.xq, g.sx, s)));
+    if (sh) MOE_TRY(cuda_status(launch_act_quant(g.x_shared, g.T, g.d, g.xq_sh, g.sx_sh, s)));
+  }
   F8Maps m{};
   bool ok = make_x_maps(m.x[0], g.xq, g.d, 2 * (uint64_t)g.routed_rows) &&
             make_code_map(&m.w[0], g.wg, g.d, (uint64_t)g.N * g.F, mx) &&
@@ -934,7 +951,8 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
     pa.act_f16 = fp8;
     pa.err = err;
-    MOE_TRY(cuda_status(launch_gather(pa, rows, s)));
+    if (fp8) set_gather_quant(&pa, ws, L, S > 0);
+    MOE_TRY(cuda_status(fp8 ? launch_gather_quant(pa, rows, S > 0 ? T : 0, s) : launch_gather(pa, rows, s)));
     MOE_TRY(record(ev, 2, s));
     // 3. GEMM schedule over the N full expert groups and the shared experts
     const int32_t tile_rows = gemm_tile_rows(*p, rows);
@@ -973,6 +991,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.offsets = offsets;
   if (g.mx) set_mx_plan(&g, *p, w, ws, L, S > 0);
   if (fp8) {
+    g.x_quantized = true;  // by the gather
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
     g.hq = at<uint8_t>(ws, L.hq);
@@ -1029,6 +1048,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
   pa.act_f16 = fp8;
   pa.err = err;
+  if (fp8) set_gather_quant(&pa, ws, L, S > 0);
   // 3. the GEMM schedule (routed experts from offsets, then the shared
   //    experts) is built by the same kernel that finishes the prefix sums
   const int32_t tile_rows = gemm_tile_rows(*p, T * K);
@@ -1074,6 +1094,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.offsets = offsets;
   if (g.mx) set_mx_plan(&g, *p, w, ws, L, S > 0);
   if (fp8) {
+    g.x_quantized = true;  // by the gather
     g.xq = at<uint8_t>(ws, L.xq);
     g.sx = at<float>(ws, L.sx);
     g.hq = at<uint8_t>(ws, L.hq);
@@ -1171,12 +1192,12 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights
   // router: split + router GEMM (tensor-core logits) or one CUDA-core logits
   // kernel, then top-K
   const int router = router_plan(p->T, p->d_model, p->n_experts, p->hidden_dtype == MOE_BF16).tensor ? 3 : 2;
-  // FP8 experts: the two-term E4M3 split of each GEMM's activations (x, h;
-  // and the shared experts' x, h)
+  // FP8 / MXFP4 experts: the two-term E4M3 split of the down GEMM's
+  // activations h (and the shared experts' h); x's is folded into the gather
   // (+ MXFP4 without a prepared buffer: the preparation of gate, up and
   // down, and of the shared experts')
   const bool prep = is_mx(*p) && !(w && w->mx_prep);
-  const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 4 : 2) : 0) + (prep ? (p->n_shared > 0 ? 6 : 3) : 0);
+  const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 2 : 1) : 0) + (prep ? (p->n_shared > 0 ? 6 : 3) : 0);
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
   return router + route + 3 + quant;

@@ -18,6 +18,7 @@
 // With an expert capacity C ("Chapter 19", §19.6.1) a copy whose rank inside
 // its expert is C or more is dropped (inv_row = -1) and offsets count kept
 // copies: min(count, C) per expert.
+#include "act_convert.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -163,35 +164,10 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   }
 }
 
-__device__ __forceinline__ uint4 cvt8_bf16(const float4 p, const float4 q) {
-  return make_uint4(pack_bf16x2(p.x, p.y), pack_bf16x2(p.z, p.w), pack_bf16x2(q.x, q.y), pack_bf16x2(q.z, q.w));
-}
-
-__device__ __forceinline__ float4 bf16x4_to_f32(uint32_t lo, uint32_t hi) {
-  return make_float4(__uint_as_float(lo << 16), __uint_as_float(lo & 0xFFFF0000u), __uint_as_float(hi << 16),
-                     __uint_as_float(hi & 0xFFFF0000u));
-}
-
-// 8 values to fp16 (round to nearest even). `over` is set when a finite value
-// lies beyond fp16's range (|v| >= 65520 rounds to infinity).
-__device__ __forceinline__ uint4 cvt8_f16(const float4 p, const float4 q, bool& over) {
-  const float m = fmaxf(fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(p.z), fabsf(p.w))),
-                        fmaxf(fmaxf(fabsf(q.x), fabsf(q.y)), fmaxf(fabsf(q.z), fabsf(q.w))));
-  over |= (m >= 65520.f) && (m <= 3.402823466e38f);
-  return make_uint4(pack_f16x2(p.x, p.y), pack_f16x2(p.z, p.w), pack_f16x2(q.x, q.y), pack_f16x2(q.z, q.w));
-}
-
 // One 16-byte output vector (8 elements) of hidden row t, vector v, in the
 // activation format.
 __device__ __forceinline__ uint4 act_vec(const PermuteArgs& a, int64_t t, int v, bool& over) {
-  if (a.hidden_bf16) {
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.hidden) + t * a.d) + v);
-    if (!a.act_f16) return x;
-    return cvt8_f16(bf16x4_to_f32(x.x, x.y), bf16x4_to_f32(x.z, x.w), over);
-  }
-  const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(a.hidden) + t * a.d);
-  const float4 p = __ldg(sp + 2 * v), q = __ldg(sp + 2 * v + 1);
-  return a.act_f16 ? cvt8_f16(p, q, over) : cvt8_bf16(p, q);
+  return hidden_vec(a.hidden, a.hidden_bf16, a.d, t, v, a.act_f16, over);
 }
 
 // Row gather into expert order: one thread per 16-byte output vector (8
@@ -432,6 +408,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
     if (const cudaError_t le_ = launch(route_scan_kernel, 1, 1024, 0, s, a); le_ != cudaSuccess) return le_;
     if (const cudaError_t le_ = launch(route_scatter_kernel, (unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s, a); le_ != cudaSuccess) return le_;
   }
+  if (a.xq) return launch_gather_quant(a, a.T * a.K, a.xq_sh ? a.T : 0, s);
   return launch_gather(a, a.T * a.K, s);
 }
 
