@@ -2,10 +2,12 @@
 //
 // finalize: out = bf16(out_acc), the last step of the fused layer whose
 //   down-projection epilogue already scatter-added w_{t,k} * y into out_acc.
-// combine:  the step-wise, deterministic gate-weighted sum ("Chapter 19:
+// combine:  the deterministic gate-weighted sum ("Chapter 19:
 //   Mixture-of-Experts Models", §19.3.2 and the §19.2 flowchart "Sum with gate
-//   weights"): out[t] = bf16(sum_k w[t][k] * y_perm[inv_row[t*K+k]] + shared[t]),
-//   fp32 accumulation in slot order.
+//   weights"): out[t] = bf16(sum_k w[t][k] * y_perm[inv_row[t*K+k]] +
+//   sum_s shared[s][t]), fp32 accumulation in slot order, then shared expert
+//   order. The step-wise API's last step, and the fused layer's when its fp32
+//   accumulator would not fit in L2 (the down epilogue then stores rows).
 // Both are HBM-bound streams: 16-byte vector loads and stores, one thread per
 // 8 output elements, grid-stride over the whole output.
 #include "common.cuh"
@@ -41,7 +43,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int32_t K, int3
                                                       const __nv_bfloat16* __restrict__ y_perm,
                                                       const int32_t* __restrict__ inv_row,
                                                       const float* __restrict__ topk_w,
-                                                      const __nv_bfloat16* __restrict__ shared_out,
+                                                      const __nv_bfloat16* __restrict__ shared_out, int32_t S,
                                                       __nv_bfloat16* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
@@ -52,13 +54,27 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int32_t K, int3
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    for (int k = 0; k < K; ++k) {
-      const int64_t r = __ldg(inv_row + t * K + k);
-      if (r < 0) continue;  // dropped by its expert's capacity
-      const float w = __ldg(topk_w + t * K + k);
-      add_bf16x8(acc, reinterpret_cast<const uint4*>(y_perm + r * d)[v], w);
+    // Four slots' rows in flight at a time; the sum stays in slot order.
+    for (int k0 = 0; k0 < K; k0 += 4) {
+      uint4 y[4];
+      float w[4];
+      bool ok[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = k0 + j;
+        const int64_t r = k < K ? __ldg(inv_row + t * K + k) : -1;
+        ok[j] = r >= 0;  // r < 0: dropped by its expert's capacity
+        if (ok[j]) {
+          w[j] = __ldg(topk_w + t * K + k);
+          y[j] = reinterpret_cast<const uint4*>(y_perm + r * d)[v];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (ok[j]) add_bf16x8(acc, y[j], w[j]);
     }
-    if (shared_out) add_bf16x8(acc, reinterpret_cast<const uint4*>(shared_out + t * d)[v], 1.f);
+    for (int sx = 0; sx < S; ++sx)
+      add_bf16x8(acc, reinterpret_cast<const uint4*>(shared_out + ((int64_t)sx * T + t) * d)[v], 1.f);
     reinterpret_cast<uint4*>(out + t * d)[v] =
         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                    pack_bf16x2(acc[6], acc[7]));
@@ -83,12 +99,12 @@ cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, int64_t n, cud
 }
 
 cudaError_t launch_combine(int64_t T, int32_t K, int32_t d, const __nv_bfloat16* y_perm, const int32_t* inv_row,
-                           const float* topk_w, const __nv_bfloat16* shared_out, __nv_bfloat16* out,
+                           const float* topk_w, const __nv_bfloat16* shared_out, int32_t S, __nv_bfloat16* out,
                            cudaStream_t s) {
   const int64_t work = T * (d / 8);
   if (work == 0) return cudaSuccess;
-  if (const cudaError_t le_ = launch(combine_kernel, grid_for(work, 256), 256, 0, s, T, K, d, y_perm, inv_row, topk_w, shared_out, out); le_ != cudaSuccess) return le_;
-  return cudaSuccess;
+  return launch(combine_kernel, grid_for(work, 256), 256, 0, s, T, K, d, y_perm, inv_row, topk_w, shared_out,
+                shared_out ? S : 0, out);
 }
 
 }  // namespace moe

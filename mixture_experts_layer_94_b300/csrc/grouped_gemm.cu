@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
               }
             } else {
-              __nv_bfloat16* yrow = a.y + (int64_t)(ti.g.h_row0 + r_local) * a.d;
+              __nv_bfloat16* yrow = (kind && a.y_sh ? a.y_sh : a.y) + (int64_t)(ti.g.h_row0 + r_local) * a.d;
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 const int n0 = col0 + c * 32 + v * 8;

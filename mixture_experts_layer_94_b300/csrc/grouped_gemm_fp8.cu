@@ -180,7 +180,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, int total, uint
                                     ws * sd.w * y[4 * q + 3]));
             }
           } else {
-            __nv_bfloat16* yrow = a.y + (int64_t)(ti.g.h_row0 + r_local) * a.d + n0;
+            __nv_bfloat16* yrow = (kind && a.y_sh ? a.y_sh : a.y) + (int64_t)(ti.g.h_row0 + r_local) * a.d + n0;
             uint32_t p[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

@@ -123,7 +123,8 @@ struct GemmArgs {
   const int32_t* perm_src;
   const float* topk_w;
   int32_t top_k;
-  __nv_bfloat16* y;      // store epilogue: bf16 [rows][d]
+  __nv_bfloat16* y;      // store epilogue: bf16 [rows][d] (routed groups)
+  __nv_bfloat16* y_sh;   // store epilogue, shared groups: bf16 [S*T][d] (nullptr: y)
   const float* row_w;    // scatter epilogue, expert choice: perm_src is the row's token, row_w its weight
   int32_t d;
   uint32_t* err;
@@ -223,8 +224,11 @@ cudaError_t launch_grouped_gemm(int phase, int epilogue, int pair, const GemmMap
                                 int64_t tile_bound, cudaStream_t s);
 
 cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, int64_t n, cudaStream_t s);
+// out[t] = bf16(sum_k topk_w[t][k] * y_perm[inv_row[t][k]] + sum_s shared_out[s][t]),
+// fp32 in slot order; slots with inv_row < 0 are skipped; shared_out [S][T][d]
+// or nullptr.
 cudaError_t launch_combine(int64_t T, int32_t K, int32_t d, const __nv_bfloat16* y_perm,
                            const int32_t* inv_row, const float* topk_w,
-                           const __nv_bfloat16* shared_out, __nv_bfloat16* out, cudaStream_t s);
+                           const __nv_bfloat16* shared_out, int32_t S, __nv_bfloat16* out, cudaStream_t s);
 
 }  // namespace moe

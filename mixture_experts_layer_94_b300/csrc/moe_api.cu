@@ -53,6 +53,7 @@ MxOffsets mx_offsets(const moe_problem_t& p, bool shared, Take&& take) {
 struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc;
+  size_t y_rows, y_sh;  // token choice with a large accumulator: the down GEMM's stored rows (see stored_combine)
   size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 / MXFP4 experts: two-term E4M3 activations + row scales
   MxOffsets mx;  // MXFP4 experts: the per-call preparation of the weights in use
   size_t total;
@@ -67,6 +68,17 @@ int64_t ec_capacity(const moe_problem_t& p) {
 }
 
 bool is_fp8(const moe_problem_t& p) { return p.expert_dtype == MOE_EXPERT_FP8_E4M3; }
+
+// The fused layer adds every expert row into an fp32 [T][d] accumulator with
+// atomics from the down GEMM's epilogue. Once that accumulator outgrows a good
+// share of the 126 MB L2, those read-modify-writes go to DRAM (K + S of them
+// per output element); token-choice layers then store the unweighted rows in
+// bf16 and sum each token's K rows (and shared rows) in a deterministic
+// combine instead.
+constexpr int64_t kAtomicAccMaxBytes = 96ll << 20;
+bool stored_combine(const moe_problem_t& p) {
+  return p.routing == MOE_ROUTING_TOKEN_CHOICE && p.T * (int64_t)p.d_model * 4 > kAtomicAccMaxBytes;
+}
 bool is_mx(const moe_problem_t& p) { return p.expert_dtype == MOE_EXPERT_MXFP4; }
 // FP8 and MXFP4 experts both run on the 8-bit tensor path (fp16 activations
 // between calls, two-term E4M3 activations inside the GEMMs).
@@ -133,6 +145,10 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.h = take((size_t)rows * p.ffn * 2);
     if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
     L.out_acc = take((size_t)T * p.d_model * 4);
+    if (stored_combine(p)) {
+      L.y_rows = take((size_t)TK * p.d_model * 2);
+      if (p.n_shared > 0) L.y_sh = take((size_t)p.n_shared * T * p.d_model * 2);
+    }
   }
   L.total = off;
   return L;
@@ -329,6 +345,7 @@ struct GemmPlan {
   const float* topk_w;
   const float* row_w;
   __nv_bfloat16* y;
+  __nv_bfloat16* y_sh;    // store epilogue, shared experts' rows (nullptr: y)
   const GroupDesc* groups;
   const int32_t* ts_gu;
   const int32_t* ts_dn;
@@ -471,6 +488,7 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   a.topk_w = g.topk_w;
   a.row_w = g.row_w;
   a.y = g.y;
+  a.y_sh = g.y_sh;
   bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, rows);
   MOE_TRY(cuda_status(launch_grouped_gemm(kPhaseDown, g.epilogue, g.pair, md, a, bound, s)));
   if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[1], s)));
@@ -619,6 +637,7 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   a.topk_w = g.topk_w;
   a.row_w = g.row_w;
   a.y = g.y;
+  a.y_sh = g.y_sh;
   bound = gemm_tile_bound(kPhaseDown, g.routed_rows, g.N, g.S, g.T, g.F, g.Fs, g.d, kF8TileRows);
   MOE_TRY(cuda_status(launch(kPhaseDown, g.epilogue, md, a, bound)));
   if (ev_after_gateup) MOE_TRY(cuda_status(record_event(ev_after_gateup[1], s)));
@@ -869,7 +888,7 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm, const int32
   if (!y_perm || !inv_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(out) || (shared_out && !aligned16(shared_out))) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_combine(p->T, p->top_k, p->d_model, static_cast<const __nv_bfloat16*>(y_perm),
-                                    inv_row, topk_w, static_cast<const __nv_bfloat16*>(shared_out),
+                                    inv_row, topk_w, static_cast<const __nv_bfloat16*>(shared_out), 1,
                                     static_cast<__nv_bfloat16*>(out), static_cast<cudaStream_t>(stream)));
 }
 
@@ -1043,8 +1062,9 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.offsets = offsets;
   pa.perm_src = at<int32_t>(ws, L.perm_src);
   pa.inv_row = at<int32_t>(ws, L.inv_row);
+  const bool combine = stored_combine(*p);
   pa.x_perm = at<void>(ws, L.x_perm);
-  pa.zero_rows = at<float>(ws, L.out_acc);
+  pa.zero_rows = combine ? nullptr : at<float>(ws, L.out_acc);
   pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
   pa.act_f16 = fp8;
   pa.err = err;
@@ -1108,8 +1128,12 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   }
   g.h = at<__nv_bfloat16>(ws, L.h);
   g.h_sh = S > 0 ? at<__nv_bfloat16>(ws, L.h_sh) : nullptr;
-  g.epilogue = kEpiScatter;
+  g.epilogue = combine ? kEpiStoreY : kEpiScatter;
   g.out_acc = at<float>(ws, L.out_acc);
+  if (combine) {
+    g.y = at<__nv_bfloat16>(ws, L.y_rows);
+    g.y_sh = S > 0 ? at<__nv_bfloat16>(ws, L.y_sh) : nullptr;
+  }
   g.perm_src = pa.perm_src;
   g.topk_w = topk_w;
   g.groups = at<GroupDesc>(ws, L.groups);
@@ -1118,8 +1142,12 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   g.err = err;
   MOE_TRY(run_gemms(g, s, ev ? ev + 4 : nullptr));
 
-  // 6. fp32 -> bf16
-  MOE_TRY(cuda_status(launch_finalize(g.out_acc, static_cast<__nv_bfloat16*>(out), T * p->d_model, s)));
+  // 6. fp32 -> bf16, or the gate-weighted sum of the stored rows
+  if (combine)
+    MOE_TRY(cuda_status(launch_combine(T, K, p->d_model, g.y, pa.inv_row, topk_w, g.y_sh, S,
+                                       static_cast<__nv_bfloat16*>(out), s)));
+  else
+    MOE_TRY(cuda_status(launch_finalize(g.out_acc, static_cast<__nv_bfloat16*>(out), T * p->d_model, s)));
   return record(ev, 6, s);
 }
 
