@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's batch T (a smaller case of the same shapes, e.g. for a profiler)")
     ap.add_argument("--mx-per-call", action="store_true",
                     help="MXFP4 experts: every step prepares the block scales of the experts it uses "
                          "(default: prepared once when the layer is built, as a server loads weights)")
@@ -586,6 +588,8 @@ def run_ours(args, cfg, desc, world, rank):
 def main():
     args = parse()
     cfg, desc = WORKLOADS[args.workload]
+    if args.tokens is not None:
+        cfg, desc = cfg.with_(T=args.tokens), f"{desc}, T={args.tokens}"
     world, rank, _ = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, cfg, desc, world, rank)
