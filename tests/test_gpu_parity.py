@@ -46,6 +46,12 @@ MID = {
     "decode_like_T3": inputs.MoEConfig("decode_like_T3", T=3, d=1024, N=128, K=8, F=64),
     "small_n_split_T5": inputs.MoEConfig("small_n_split_T5", T=5, d=2048, N=6, K=2, F=64,
                                          hidden_dtype="f32"),
+    # batches of at most 8 tokens with N > 32 (split-d logits, one warp per token in the top-K)
+    "fused_topk_grouped_T4": inputs.MoEConfig("fused_topk_grouped_T4", T=4, d=512, N=64, K=6, F=64, S=1, Fs=64,
+                                              score="sigmoid", sel_bias_var=0.1, n_groups=8, topk_groups=3),
+    "fused_topk_f32_T7": inputs.MoEConfig("fused_topk_f32_T7", T=7, d=384, N=256, K=8, F=64, hidden_dtype="f32",
+                                          renormalize=0),
+    "fused_topk_T8_N96": inputs.MoEConfig("fused_topk_T8_N96", T=8, d=256, N=96, K=4, F=64),
     # group-limited routing: 8 groups of 8 experts, 3 groups per token
     "grouped_routing": inputs.MoEConfig("grouped_routing", T=333, d=256, N=64, K=6, F=200, S=1, Fs=136,
                                         score="sigmoid", sel_bias_var=0.1, zipf=1.1, n_groups=8,
@@ -366,6 +372,7 @@ EC_CASES = {
     "ec_sigmoid_f32_half": inputs.MoEConfig("ec_sigmoid_f32_half", T=200, d=128, N=16, K=3, F=136,
                                             score="sigmoid", hidden_dtype="f32", capacity_factor=0.5,
                                             routing="expert"),
+    "ec_small_T6": inputs.MoEConfig("ec_small_T6", T=6, d=256, N=64, K=2, F=64, routing="expert"),
     "ec_every_token": inputs.MoEConfig("ec_every_token", T=77, d=64, N=4, K=4, F=64, routing="expert"),
     "ec_shared_pairs": inputs.MoEConfig("ec_shared_pairs", T=600, d=192, N=2, K=1, F=136, S=1, Fs=72,
                                         routing="expert"),
