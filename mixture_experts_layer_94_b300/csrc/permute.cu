@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
         } else {
           a.inv_row[t * K + k] = -1;
         }
+      } else {
+        a.inv_row[t * K + k] = -1;  // out-of-range expert (reported by the histogram)
       }
     }
   }
@@ -384,6 +386,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) 
           } else {
             a.inv_row[t * K + k] = -1;
           }
+        } else {
+          a.inv_row[t * K + k] = -1;
         }
       }
     }
@@ -394,7 +398,77 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const PermuteArgs a) 
   }
 }
 
+// Token-major form of the same copy, for large token-choice batches: a thread
+// reads a 16-byte vector of hidden row t once and stores it to each of the
+// token's K packed rows (inv_row; -1 = dropped). Hidden is then streamed from
+// HBM once, where the row-major gather above re-reads a row for each of its K
+// copies (in expert order, long after the first read once hidden and the
+// packed rows outgrow L2). Clears the accumulator and writes the
+// activation-format copy of hidden like the gather.
+constexpr int kScatterBatch = 2;
+
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const PermuteArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int d = a.d, nvec = d / 8, K = a.K;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  const int64_t placed = min(a.T * K, (int64_t)__ldg(a.offsets + a.N));
+  const int64_t total = a.T * nvec;
+  bool over = false;
+  uint4* xp = reinterpret_cast<uint4*>(a.x_perm);
+  uint4* dp = reinterpret_cast<uint4*>(a.x_act);
+  const int64_t adv = (int64_t)kScatterBatch * nthr;
+  const int64_t adv_t = adv / nvec;
+  const int adv_v = (int)(adv - adv_t * nvec);
+  int64_t tt[kScatterBatch];
+  int vv[kScatterBatch];
+#pragma unroll
+  for (int u = 0; u < kScatterBatch; ++u) {
+    const int64_t i = tid + u * nthr;
+    tt[u] = i / nvec;
+    vv[u] = (int)(i - tt[u] * nvec);
+  }
+  for (int64_t i0 = tid; i0 < total; i0 += adv) {
+    uint4 val[kScatterBatch];
+    int64_t t_of[kScatterBatch];
+    int v_of[kScatterBatch];
+#pragma unroll
+    for (int u = 0; u < kScatterBatch; ++u) {
+      const int64_t i = i0 + u * nthr;
+      t_of[u] = i < total ? tt[u] : -1;
+      v_of[u] = vv[u];
+      vv[u] += adv_v;
+      tt[u] += adv_t;
+      if (vv[u] >= nvec) {
+        vv[u] -= nvec;
+        ++tt[u];
+      }
+      if (t_of[u] >= 0) val[u] = act_vec(a, t_of[u], v_of[u], over);
+    }
+#pragma unroll
+    for (int u = 0; u < kScatterBatch; ++u) {
+      if (t_of[u] < 0) continue;
+      const int32_t* ir = a.inv_row + t_of[u] * K;
+      for (int k = 0; k < K; ++k) {
+        const int32_t r = __ldg(ir + k);
+        if (r >= 0 && r < placed) xp[(int64_t)r * nvec + v_of[u]] = val[u];
+      }
+      if (dp) dp[t_of[u] * nvec + v_of[u]] = val[u];
+    }
+  }
+  if (a.zero_rows) {
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* z = reinterpret_cast<float4*>(a.zero_rows);
+    for (int64_t i = tid; i < a.T * d / 4; i += nthr) z[i] = zero;
+  }
+  if (over && a.err) atomicOr(a.err, kErrRange);
+}
+
 }  // namespace
+
+// Token choice with at least this many copies takes the token-major copy.
+constexpr int64_t kScatterMinRows = 8192;
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
   if (a.C == 0) {  // T == 0: empty histogram, offsets all zero
@@ -415,6 +489,11 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
 cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!a.row_token && rows >= kScatterMinRows) {
+    const int64_t want = (a.T * (a.d / 8) + 255) / 256;
+    const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
+    return launch(scatter_rows_kernel, grid, 256, 0, s, a);
+  }
   const int64_t want = (rows * (a.d / 8) + 255) / 256;  // one 16-byte vector per thread
   const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
   return launch(gather_rows_kernel, grid, 256, 0, s, a, rows);

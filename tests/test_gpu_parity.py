@@ -52,6 +52,12 @@ MID = {
     "fused_topk_f32_T7": inputs.MoEConfig("fused_topk_f32_T7", T=7, d=384, N=256, K=8, F=64, hidden_dtype="f32",
                                           renormalize=0),
     "fused_topk_T8_N96": inputs.MoEConfig("fused_topk_T8_N96", T=8, d=256, N=96, K=4, F=64),
+    # T*K >= 8192 copies: the token-major row copy (ragged d; fp32 hidden with a shared
+    # expert and a capacity limit)
+    "scatter_copy_ragged": inputs.MoEConfig("scatter_copy_ragged", T=2100, d=264, N=16, K=4, F=136),
+    "scatter_copy_f32_shared_capacity": inputs.MoEConfig("scatter_copy_f32_shared_capacity", T=1100, d=136, N=8,
+                                                         K=8, F=72, S=1, Fs=64, hidden_dtype="f32",
+                                                         capacity_factor=0.8),
     # group-limited routing: 8 groups of 8 experts, 3 groups per token
     "grouped_routing": inputs.MoEConfig("grouped_routing", T=333, d=256, N=64, K=6, F=200, S=1, Fs=136,
                                         score="sigmoid", sel_bias_var=0.1, zipf=1.1, n_groups=8,
@@ -176,8 +182,9 @@ def test_router_exact_ties_break_to_lower_index():
 
 
 # --------------------------------------------------------------------------- permute
+# T*K >= 8192 copies take the token-major copy (each hidden row read once, stored K times)
 PERMUTE_CASES = [(1, 8, 2, False), (37, 8, 2, False), (500, 64, 6, True), (1000, 256, 8, True),
-                 (4096, 8, 2, False), (33, 1, 1, False)]
+                 (4096, 8, 2, False), (33, 1, 1, False), (2100, 64, 4, True), (1100, 16, 8, True)]
 
 
 @pytest.mark.parametrize("T,N,K,skew", PERMUTE_CASES)
@@ -225,6 +232,28 @@ def test_permute_reports_out_of_range_index():
               t(cfg.T * 2), t(cfg.T * 2, cfg.d, dt=torch.bfloat16), ws)
     assert B.get_device_status(ws) == -6  # MOE_ERR_DEVICE_BOUNDS
     assert B.get_device_status(ws) == 0   # read-and-clear
+
+
+def test_permute_out_of_range_index_token_major_copy():
+    # 8200 copies: the token-major copy; the bad copy has no row (inv_row -1),
+    # every placed row still holds its token's hidden row
+    cfg = inputs.MoEConfig("bad_large", T=4100, d=64, N=8, K=2, F=8)
+    idx = np.stack([np.arange(cfg.T) % 8, (np.arange(cfg.T) + 3) % 8], axis=1).astype(np.int32)
+    idx[1234, 0] = -2
+    p = B.problem(cfg)
+    ws = B.new_workspace(p, B.CALL_PERMUTE)
+    hidden = inputs.make_router_inputs(cfg, seed=5)["hidden"]
+    t = lambda *s, dt=torch.int32: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    offsets, perm_src, inv_row = t(cfg.N + 1), t(cfg.T * 2), t(cfg.T * 2)
+    x_perm = t(cfg.T * 2, cfg.d, dt=torch.bfloat16)
+    B.permute(p, _dev(torch.from_numpy(idx)), _dev(hidden), t(cfg.N), offsets, perm_src, inv_row, x_perm, ws)
+    assert B.get_device_status(ws) == -6  # MOE_ERR_DEVICE_BOUNDS
+    assert inv_row.cpu().numpy()[1234 * 2] == -1
+    placed = int(offsets.cpu().numpy()[-1])
+    assert placed == cfg.T * 2 - 1
+    src = perm_src.cpu().numpy()[:placed]
+    expect = hidden.to(torch.bfloat16)[torch.from_numpy(src // 2).long()]
+    assert torch.equal(x_perm.cpu()[:placed].view(torch.int16), expect.view(torch.int16))
 
 
 # --------------------------------------------------------------------------- grouped SwiGLU
