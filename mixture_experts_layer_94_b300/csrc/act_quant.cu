@@ -252,6 +252,53 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_block_kernel(Src src, int6
   quant_tail(o, over);
 }
 
+// Token-major form of the fused gather for large token-choice batches: one
+// warp per token splits its hidden row once and stores the two E4M3 rows and
+// the scale to each of the token's K packed rows (inv_row; -1 = dropped) and,
+// with shared experts, to the token's shared row. The split is a function of
+// the token's row alone, so every copy is the one the row-major form writes.
+__global__ void __launch_bounds__(256) quant_token_kernel(HiddenRows src, const int32_t* __restrict__ inv_row,
+                                                          int64_t shared_rows, QuantOut o) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t placed = min(src.routed, (int64_t)__ldg(src.placed_at));
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int K = src.d, nvec = K / 8, topk = src.K;
+  bool over = false;
+  for (int64_t t = warp0; t < src.T; t += nwarps) {
+    // lane k < topk holds copy k's packed row, or -1
+    int32_t r_own = lane < topk ? __ldg(inv_row + t * topk + lane) : -1;
+    if (r_own >= placed) r_own = -1;
+    float amax = 0.f;
+    for (int v = lane; v < nvec; v += 32) amax = amax8(src.vec(t, v, over), amax);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.f ? amax / 448.f : 1.f;
+    for (int v0 = 0; v0 < nvec; v0 += 32) {  // warp-uniform trips: every lane takes part in the shuffles
+      const int v = v0 + lane;
+      const bool on = v < nvec;
+      bool unused = false;
+      uint2 hi = make_uint2(0u, 0u), lo = hi;
+      if (on) quant8(src.vec(t, v, unused), sc, hi, lo);
+      for (int k = 0; k < topk; ++k) {
+        const int32_t r = __shfl_sync(0xffffffffu, r_own, k);
+        if (r < 0 || !on) continue;
+        reinterpret_cast<uint2*>(o.dst0 + (2 * (int64_t)r) * K)[v] = hi;
+        reinterpret_cast<uint2*>(o.dst0 + (2 * (int64_t)r + 1) * K)[v] = lo;
+      }
+      if (shared_rows && on) {
+        reinterpret_cast<uint2*>(o.dst1 + (2 * t) * K)[v] = hi;
+        reinterpret_cast<uint2*>(o.dst1 + (2 * t + 1) * K)[v] = lo;
+      }
+    }
+    if (r_own >= 0) o.scale0[r_own] = sc;
+    if (shared_rows && lane == 0) o.scale1[t] = sc;
+  }
+  quant_tail(o, over);
+}
+
 template <class Src>
 cudaError_t launch_quant(const Src& src, int64_t rows, int32_t K, const QuantOut& o, cudaStream_t s) {
   int dev = 0, sms = 148;
@@ -274,6 +321,13 @@ cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* 
 cudaError_t launch_gather_quant(const PermuteArgs& a, int64_t rows, int64_t shared_rows, cudaStream_t s) {
   HiddenRows src{a.hidden, a.hidden_bf16, a.d, a.K, a.T, rows, a.perm_src, a.row_token, a.offsets + a.N, 0};
   QuantOut o{a.xq, a.sx, a.xq_sh, a.sx_sh, rows, a.zero_rows, a.zero_rows ? a.T * a.d / 4 : 0, a.err};
+  if (!a.row_token && rows == a.T * a.K && rows >= kTokenMajorMinRows) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (a.T + 7) / 8;  // 8 tokens (warps) per 256-thread CTA
+    const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    return launch(quant_token_kernel, grid, 256, 0, s, src, (const int32_t*)a.inv_row, shared_rows, o);
+  }
   return launch_quant(src, rows + shared_rows, a.d, o, s);
 }
 

@@ -92,6 +92,10 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
 // Only the row gather (+ the accumulator clear / activation copy), for rows already
 // placed: token of row r = row_token[r], rows = offsets[N].
 cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s);
+// Token choice with at least this many packed rows copies (and splits) each
+// hidden row once, token-major, into its K packed rows instead of gathering
+// each packed row from hidden.
+constexpr int64_t kTokenMajorMinRows = 8192;
 // Expert capacity ceil(c * T * K / N) of a problem; INT32_MAX when dropless.
 int32_t expert_capacity(const moe_problem_t& p);
 

@@ -467,9 +467,6 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const PermuteArgs a) 
 
 }  // namespace
 
-// Token choice with at least this many copies takes the token-major copy.
-constexpr int64_t kScatterMinRows = 8192;
-
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
   if (a.C == 0) {  // T == 0: empty histogram, offsets all zero
     if (const cudaError_t le_ = launch(route_scan_kernel, 1, 1024, 0, s, a); le_ != cudaSuccess) return le_;
@@ -489,7 +486,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
 cudaError_t launch_gather(const PermuteArgs& a, int64_t rows, cudaStream_t s) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (!a.row_token && rows >= kScatterMinRows) {
+  if (!a.row_token && rows >= kTokenMajorMinRows) {
     const int64_t want = (a.T * (a.d / 8) + 255) / 256;
     const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want < 1 ? 1 : want) : (int64_t)sms * 8);
     return launch(scatter_rows_kernel, grid, 256, 0, s, a);
