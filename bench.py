@@ -528,6 +528,9 @@ def run_ours(args, cfg, desc, world, rank):
     gu, dn = B.LAYER_STAGES.index("gateup_swiglu_gemm"), B.LAYER_STAGES.index("down_scatter_gemm")
     dom = gu if stage_ms[gu] >= stage_ms[dn] else dn
     dom_name = B.LAYER_STAGES[dom]
+    if B.layer_small_batch(p):  # decode-sized batch: the expert FFNs run on the CUDA cores
+        dom_name = {"gateup_swiglu_gemm": "small_batch_ffn_gateup",
+                    "down_scatter_gemm": "small_batch_ffn_down"}[dom_name]
     clocks = sampler.summary(t_wall0, t_wall1)
     # The recipe's denominators: the burst peak for a kernel timed alone, the
     # sustained one for a kernel timed inside a long run that the power cap

@@ -426,6 +426,8 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm,
  * With p->expert_dtype == MOE_EXPERT_FP8_E4M3 (or MOE_EXPERT_MXFP4) every
  * expert (routed and shared) reads its codes and scales from `w` and the
  * expert GEMMs run on fp16 activations (see moe_expert_dtype_t).
+ * Decode-sized token-choice batches (moe_layer_small_batch) compute the same
+ * expert FFNs on the CUDA cores instead of the grouped GEMMs.
  */
 moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
                                const void* hidden, void* out,
@@ -456,6 +458,22 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
  * NULL: no prepared buffer); 0 if p is invalid.
  */
 int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights_t* w);
+
+/*
+ * 1 if moe_layer_forward runs problem p's expert FFNs on the CUDA cores
+ * (a decode-sized token-choice batch: T <= 4 tokens, T <= 2 for MXFP4
+ * experts), 0 if on the grouped tensor-core GEMMs, -1 if p is invalid. Host
+ * only, no CUDA call.
+ * With T tokens an expert holds at most T rows ("Part 12", "What happens when
+ * many users share the GPU?": each token reads its own experts' weights, and
+ * the bytes, not the arithmetic, set the time at small batch; "Mixture of
+ * Experts Explained", "Why batching erodes the advantage"). A 128-row tensor
+ * tile would then be almost all padding, so each touched weight row is instead
+ * streamed from HBM once by the CUDA cores and dotted with its expert's rows
+ * (fp32 products and sums; h rounded to bf16, or fp16 for FP8 / MXFP4 experts,
+ * as on the GEMM path). Same inputs, outputs, workspace and status codes.
+ */
+int32_t moe_layer_small_batch(const moe_problem_t* p);
 
 /*
  * MXFP4 experts: the weight-side preparation the expert GEMMs need, computed

@@ -75,6 +75,7 @@ def _load():
         "moe_get_device_status": ([P, P], i32),
         "moe_layer_forward_profiled": ([pp, ctypes.POINTER(Weights)] + [P] * 3 + [sz, P, P], i32),
         "moe_layer_forward_kernel_count": ([pp, ctypes.POINTER(Weights)], i32),
+        "moe_layer_small_batch": ([pp], i32),
         "moe_mxfp4_prep_bytes": ([pp], sz),
         "moe_mxfp4_prepare": ([pp, ctypes.POINTER(Weights), P, sz, P], i32),
         "moe_expert_choice_select": ([pp] + [P] * 7 + [sz, P], i32),
@@ -240,6 +241,15 @@ def layer_forward_profiled(p: Problem, weights: Weights, hidden, out, ws, events
     _check(lib.moe_layer_forward_profiled(ctypes.byref(p), ctypes.byref(weights), _p(hidden), _p(out),
                                           _p(ws), ws.numel(), arr, _stream(stream)),
            "moe_layer_forward_profiled")
+
+
+def layer_small_batch(p: Problem) -> bool:
+    """True when moe_layer_forward runs p's expert FFNs on the CUDA cores
+    (decode-sized token-choice batches), False on the grouped GEMMs."""
+    r = int(lib.moe_layer_small_batch(ctypes.byref(p)))
+    if r < 0:
+        raise ValueError("invalid problem")
+    return r == 1
 
 
 def layer_forward_kernel_count(p: Problem, weights: Weights = None) -> int:

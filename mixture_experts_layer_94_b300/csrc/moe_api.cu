@@ -91,6 +91,17 @@ bool needs_act_copy(const moe_problem_t& p) {
   return p.n_shared > 0 && (is_lowp(p) || p.hidden_dtype == MOE_F32);
 }
 
+// Token-choice batches of at most this many tokens run the expert FFNs on the
+// CUDA cores (small_batch.cu), one pass over each touched weight row, instead
+// of the grouped GEMMs: each expert then holds at most T rows. MXFP4 stops at
+// 2 tokens, where decoding the 4-bit codes for more rows would cost more ALU
+// time than the weights' HBM time.
+int32_t small_batch_rows(const moe_problem_t& p) {
+  if (p.routing != MOE_ROUTING_TOKEN_CHOICE || p.T < 1 || stored_combine(p)) return 0;
+  const int64_t max_t = is_mx(p) ? 2 : kSmallBatchMaxRows;
+  return p.T <= max_t ? (int32_t)p.T : 0;
+}
+
 Layout make_layout(const moe_problem_t& p, int call) {
   Layout L{};
   size_t off = 0;
@@ -1068,7 +1079,8 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
   pa.act_f16 = fp8;
   pa.err = err;
-  if (fp8) set_gather_quant(&pa, ws, L, S > 0);
+  const int32_t small_rows = small_batch_rows(*p);
+  if (fp8 && !small_rows) set_gather_quant(&pa, ws, L, S > 0);
   // 3. the GEMM schedule (routed experts from offsets, then the shared
   //    experts) is built by the same kernel that finishes the prefix sums
   const int32_t tile_rows = gemm_tile_rows(*p, T * K);
@@ -1083,6 +1095,50 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   MOE_TRY(cuda_status(launch_permute(pa, s)));
   MOE_TRY(record(ev, 2, s));
   MOE_TRY(record(ev, 3, s));
+
+  if (small_rows) {
+    // 4-5. decode-sized batch: SwiGLU and the weighted scatter-add on the CUDA
+    // cores, each touched weight row streamed once
+    SmallBatchArgs sb{};
+    sb.fmt = is_mx(*p) ? kSmallE2M1 : is_fp8(*p) ? kSmallE4M3 : kSmallBf16;
+    sb.max_rows = small_rows;
+    sb.N = N;
+    sb.S = S;
+    sb.d = p->d_model;
+    sb.F = p->ffn;
+    sb.Fs = p->shared_ffn;
+    sb.K = K;
+    sb.T = T;
+    sb.routed_rows = T * K;
+    sb.groups = pa.groups;
+    sb.x_routed = pa.x_perm;
+    sb.x_shared = pa.x_act ? pa.x_act : hidden;
+    sb.w_gate = w->w_gate;
+    sb.w_up = w->w_up;
+    sb.w_down = w->w_down;
+    sb.s_gate = w->ws_gate;
+    sb.s_up = w->ws_up;
+    sb.s_down = w->ws_down;
+    sb.w_gate_scale = w->w_gate_scale;
+    sb.w_up_scale = w->w_up_scale;
+    sb.w_down_scale = w->w_down_scale;
+    sb.s_gate_scale = w->ws_gate_scale;
+    sb.s_up_scale = w->ws_up_scale;
+    sb.s_down_scale = w->ws_down_scale;
+    sb.h = at<void>(ws, L.h);
+    sb.h_sh = S > 0 ? at<void>(ws, L.h_sh) : nullptr;
+    sb.out_acc = at<float>(ws, L.out_acc);
+    sb.perm_src = pa.perm_src;
+    sb.topk_w = topk_w;
+    sb.err = err;
+    MOE_TRY(cuda_status(launch_small_batch_ffn(sb, 0, s)));
+    MOE_TRY(record(ev, 4, s));
+    MOE_TRY(cuda_status(launch_small_batch_ffn(sb, 1, s)));
+    MOE_TRY(record(ev, 5, s));
+    // 6. fp32 -> bf16
+    MOE_TRY(cuda_status(launch_finalize(sb.out_acc, static_cast<__nv_bfloat16*>(out), T * p->d_model, s)));
+    return record(ev, 6, s);
+  }
 
   // 4-5. grouped SwiGLU GEMMs with the fused weighted scatter-add
   GemmPlan g{};
@@ -1228,7 +1284,13 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights
   const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 2 : 1) : 0) + (prep ? (p->n_shared > 0 ? 6 : 3) : 0);
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
+  if (small_batch_rows(*p)) return router + route + 3;  // gate/up, down, finalise on the CUDA cores
   return router + route + 3 + quant;
+}
+
+int32_t moe_layer_small_batch(const moe_problem_t* p) {
+  if (moe_problem_check(p) != MOE_OK) return -1;
+  return small_batch_rows(*p) > 0 ? 1 : 0;
 }
 
 moe_status_t moe_get_device_status(void* ws, void* stream) {

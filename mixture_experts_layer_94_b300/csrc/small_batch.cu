@@ -1,0 +1,369 @@
+// small_batch.cu — the expert FFNs of a decode-sized batch on the CUDA cores
+// (internal).
+//
+// With T <= 4 tokens every expert holds at most T packed rows, so a grouped
+// GEMM tile (128 activation rows) is almost all padding and its 256 weight
+// rows per tile leave most SMs idle (8 touched experts x 12 tiles at T = 1).
+// The work is a stream of weight rows, each used by at most T activation rows:
+// HBM-bound, with nothing for the tensor cores to gain. Here a warp takes four
+// weight rows of one expert (gate rows f, f+1 and up rows f, f+1; or W_down
+// rows j..j+3), streams them from HBM once in 16-byte units, and dots them with
+// the expert's activation rows, which stay in L1/L2. One 512-thread CTA per SM
+// walks all (expert, row block) items, so every SM streams weights.
+//
+// Formats: bf16 weights with bf16 activations; FP8 E4M3 codes with fp32 row
+// scales, or MXFP4 (E2M1 codes, E8M0 scale per 32 elements) with fp16
+// activations. Products and sums are fp32; h is rounded once, to bf16 (fp16
+// for FP8 / MXFP4 experts), as the grouped GEMMs store it.
+
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerItem = 4;  // weight rows a warp streams together
+
+// Elements in one 16-byte unit of weight codes.
+__host__ __device__ constexpr int unit_elems(int fmt) {
+  return fmt == kSmallBf16 ? 8 : fmt == kSmallE4M3 ? 16 : 32;
+}
+
+// 16 bytes of weight codes, read once: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float2 half2_bits_to_f32(uint32_t bits) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = bits;
+  return __half22float2(h);
+}
+
+// 8 activations (16 bytes: bf16, or fp16 when F16) to fp32.
+template <bool F16>
+__device__ __forceinline__ void act8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (F16) {
+      const float2 p = half2_bits_to_f32(w[i]);
+      f[2 * i] = p.x;
+      f[2 * i + 1] = p.y;
+    } else {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// Two E4M3 codes (low 16 bits of c; the lower byte is the earlier element).
+__device__ __forceinline__ float2 e4m3x2_f32(uint32_t c) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c & 0xFFFFu), __NV_E4M3);
+  return half2_bits_to_f32((uint32_t)h.x | ((uint32_t)h.y << 16));
+}
+
+// Two E2M1 codes of one byte (the low nibble is the earlier element).
+__device__ __forceinline__ float2 e2m1x2_f32(uint32_t c) {
+  const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(c & 0xFFu), __NV_E2M1);
+  return half2_bits_to_f32((uint32_t)h.x | ((uint32_t)h.y << 16));
+}
+
+// Elements 8s .. 8s+7 of a 16-byte unit of weight codes, as fp32 code values
+// (FP8 row scales and MXFP4 block scales are applied by the caller).
+template <int FMT>
+__device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  if (FMT == kSmallBf16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else if (FMT == kSmallE4M3) {  // 16 codes per unit: words 2s, 2s+1
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t c = w[2 * s + i];
+      const float2 a = e4m3x2_f32(c), b = e4m3x2_f32(c >> 16);
+      f[4 * i] = a.x;
+      f[4 * i + 1] = a.y;
+      f[4 * i + 2] = b.x;
+      f[4 * i + 3] = b.y;
+    }
+  } else {  // 32 codes per unit, two per byte: word s
+    const uint32_t c = w[s];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = e2m1x2_f32(c >> (8 * i));
+      f[2 * i] = a.x;
+      f[2 * i + 1] = a.y;
+    }
+  }
+}
+
+// E8M0 block scale 2^(e - 127); e = 0 is 2^-127 (an fp32 subnormal).
+__device__ __forceinline__ float e8m0_f32(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// acc[q][r] += (weight row q) . (activation row r) over `units` 16-byte units
+// of codes (unit j covers elements j*E .. j*E+E-1). Activation row r starts at
+// x + r * x_pitch (16-byte vectors of 8 elements); rows >= `rows` are skipped.
+// MXFP4: bsc[q] is row q's E8M0 block scales, one per unit.
+template <int FMT, int R>
+__device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem],
+                                         const uint8_t* const (&bsc)[kRowsPerItem], const uint4* x,
+                                         int64_t x_pitch, int rows, int units, int lane,
+                                         float (&acc)[kRowsPerItem][R]) {
+  constexpr int E = unit_elems(FMT), SUB = E / 8;
+  constexpr int U = R == 1 ? 4 : 2;  // units per row in flight per lane
+  constexpr bool kF16 = FMT != kSmallBf16;
+  for (int j0 = lane; j0 < units; j0 += 32 * U) {
+    uint4 wv[kRowsPerItem][U];
+    float sc[kRowsPerItem][U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u;
+#pragma unroll
+      for (int q = 0; q < kRowsPerItem; ++q) {
+        wv[q][u] = j < units ? ld_stream(w[q] + j) : make_uint4(0u, 0u, 0u, 0u);
+        if (FMT == kSmallE2M1) sc[q][u] = j < units ? e8m0_f32(__ldg(bsc[q] + j)) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u;
+      if (j < units) {
+        float part[kRowsPerItem][R];
+        if (FMT == kSmallE2M1) {
+#pragma unroll
+          for (int q = 0; q < kRowsPerItem; ++q)
+#pragma unroll
+            for (int r = 0; r < R; ++r) part[q][r] = 0.f;
+        }
+#pragma unroll
+        for (int s = 0; s < SUB; ++s) {
+          float xf[R][8];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            if (r < rows) act8<kF16>(__ldg(x + r * x_pitch + (int64_t)j * SUB + s), xf[r]);
+          }
+#pragma unroll
+          for (int q = 0; q < kRowsPerItem; ++q) {
+            float wf[8];
+            w8<FMT>(wv[q][u], s, wf);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              if (r < rows) {
+                float& dst = FMT == kSmallE2M1 ? part[q][r] : acc[q][r];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst = fmaf(wf[i], xf[r][i], dst);
+              }
+            }
+          }
+        }
+        if (FMT == kSmallE2M1) {
+#pragma unroll
+          for (int q = 0; q < kRowsPerItem; ++q)
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[q][r] = fmaf(sc[q][u], part[q][r], acc[q][r]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kRowsPerItem; ++q)
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[q][r] += __shfl_xor_sync(0xFFFFFFFFu, acc[q][r], off);
+}
+
+// 16-byte units of codes in one weight row of `k` elements.
+__device__ __forceinline__ int64_t row_units(int k, int fmt) { return k / unit_elems(fmt); }
+
+// PHASE 0: h[row r][f, f+1] = SiLU(g) * u for the item's gate rows f, f+1 and
+// up rows f, f+1. PHASE 1: out_acc[token of r][j..j+3] += w_r * y for W_down
+// rows j..j+3. Items: every routed expert holding rows (F/2 or d/4 items
+// each), then every shared expert (Fs/2 or d/4 items each).
+template <int FMT, int R, int PHASE>
+__global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const SmallBatchArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int32_t s_list[kMaxExperts];
+  __shared__ int32_t s_count[kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  // the routed experts that hold rows, in expert order (N <= 256 < kThreads)
+  const bool has = (int)threadIdx.x < N && a.groups[threadIdx.x].rows > 0;
+  const uint32_t ball = __ballot_sync(0xFFFFFFFFu, has);
+  if (lane == 0) s_count[warp] = __popc(ball);
+  __syncthreads();
+  int base = 0, nr = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = s_count[w];
+    base += w < warp ? c : 0;
+    nr += c;
+  }
+  if (has) s_list[base + __popc(ball & ((1u << lane) - 1u))] = (int32_t)threadIdx.x;
+  __syncthreads();
+
+  constexpr bool kF16 = FMT != kSmallBf16;
+  const int per_r = PHASE == 0 ? a.F / 2 : a.d / kRowsPerItem;
+  const int per_s = PHASE == 0 ? a.Fs / 2 : a.d / kRowsPerItem;
+  const int64_t n_r = (int64_t)nr * per_r;
+  const int64_t total = n_r + (a.S > 0 ? (int64_t)a.S * per_s : 0);
+  bool over = false;
+  for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < total; item += (int64_t)gridDim.x * kWarps) {
+    int g, blk;
+    if (item < n_r) {
+      g = s_list[item / per_r];
+      blk = (int)(item % per_r);
+    } else {
+      const int64_t i2 = item - n_r;
+      g = N + (int)(i2 / per_s);
+      blk = (int)(i2 % per_s);
+    }
+    const GroupDesc gd = a.groups[g];
+    const int kind = g < N ? 0 : 1;
+    const int e = kind ? g - N : g;
+    int rows = gd.rows;
+    if (rows > R) {  // cannot happen for token choice with T <= R
+      if (lane == 0) atomicOr(a.err, kErrBounds);
+      rows = R;
+    }
+    const int Fk = kind ? a.Fs : a.F;
+    float acc[kRowsPerItem][R];
+#pragma unroll
+    for (int q = 0; q < kRowsPerItem; ++q)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[q][r] = 0.f;
+
+    if (PHASE == 0) {
+      const int f0 = 2 * blk;
+      const int64_t units = row_units(a.d, FMT);
+      const int64_t row0 = (int64_t)e * Fk + f0;  // gate / up row f0 of this expert
+      const uint4* wg = static_cast<const uint4*>(kind ? a.s_gate : a.w_gate);
+      const uint4* wu = static_cast<const uint4*>(kind ? a.s_up : a.w_up);
+      const uint4* const w[kRowsPerItem] = {wg + row0 * units, wg + (row0 + 1) * units, wu + row0 * units,
+                                            wu + (row0 + 1) * units};
+      const uint8_t* bsc[kRowsPerItem] = {nullptr, nullptr, nullptr, nullptr};
+      if (FMT == kSmallE2M1) {
+        const uint8_t* bg = static_cast<const uint8_t*>(kind ? a.s_gate_scale : a.w_gate_scale);
+        const uint8_t* bu = static_cast<const uint8_t*>(kind ? a.s_up_scale : a.w_up_scale);
+        bsc[0] = bg + row0 * units;
+        bsc[1] = bg + (row0 + 1) * units;
+        bsc[2] = bu + row0 * units;
+        bsc[3] = bu + (row0 + 1) * units;
+      }
+      const uint4* x = static_cast<const uint4*>(kind ? a.x_shared : a.x_routed) + (int64_t)gd.a_row0 * (a.d / 8);
+      dot_rows<FMT, R>(w, bsc, x, a.d / 8, rows, (int)units, lane, acc);
+      float gs0 = 1.f, gs1 = 1.f, us0 = 1.f, us1 = 1.f;
+      if (FMT == kSmallE4M3) {
+        const float* sg = static_cast<const float*>(kind ? a.s_gate_scale : a.w_gate_scale);
+        const float* su = static_cast<const float*>(kind ? a.s_up_scale : a.w_up_scale);
+        gs0 = __ldg(sg + row0);
+        gs1 = __ldg(sg + row0 + 1);
+        us0 = __ldg(su + row0);
+        us1 = __ldg(su + row0 + 1);
+      }
+      uint32_t* h = static_cast<uint32_t*>(kind ? a.h_sh : a.h);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (lane == r && r < rows) {
+          const float h0 = silu_f(gs0 * acc[0][r]) * (us0 * acc[2][r]);
+          const float h1 = silu_f(gs1 * acc[1][r]) * (us1 * acc[3][r]);
+          if (kF16) over |= fmaxf(fabsf(h0), fabsf(h1)) >= 65520.f;
+          h[((int64_t)(gd.h_row0 + r) * Fk + f0) / 2] = kF16 ? pack_f16x2(h0, h1) : pack_bf16x2(h0, h1);
+        }
+      }
+    } else {
+      const int j0 = kRowsPerItem * blk;
+      const int64_t units = row_units(Fk, FMT);
+      const int64_t row0 = (int64_t)e * a.d + j0;  // W_down row j0 of this expert
+      const uint4* wd = static_cast<const uint4*>(kind ? a.s_down : a.w_down);
+      const uint4* const w[kRowsPerItem] = {wd + row0 * units, wd + (row0 + 1) * units, wd + (row0 + 2) * units,
+                                            wd + (row0 + 3) * units};
+      const uint8_t* bsc[kRowsPerItem] = {nullptr, nullptr, nullptr, nullptr};
+      if (FMT == kSmallE2M1) {
+        const uint8_t* bd = static_cast<const uint8_t*>(kind ? a.s_down_scale : a.w_down_scale);
+#pragma unroll
+        for (int q = 0; q < kRowsPerItem; ++q) bsc[q] = bd + (row0 + q) * units;
+      }
+      const uint4* x = static_cast<const uint4*>(kind ? a.h_sh : a.h) + (int64_t)gd.h_row0 * (Fk / 8);
+      dot_rows<FMT, R>(w, bsc, x, Fk / 8, rows, (int)units, lane, acc);
+      const int q = lane & (kRowsPerItem - 1), rl = lane / kRowsPerItem;
+      if (rl < rows) {
+        float y = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int qq = 0; qq < kRowsPerItem; ++qq)
+            if (r == rl && qq == q) y = acc[qq][r];
+        if (FMT == kSmallE4M3)
+          y *= __ldg(static_cast<const float*>(kind ? a.s_down_scale : a.w_down_scale) + row0 + q);
+        int64_t t = rl;
+        float wt = 1.f;
+        bool ok = true;
+        if (kind == 0) {
+          const int32_t src = __ldg(a.perm_src + gd.h_row0 + rl);
+          ok = src >= 0 && (int64_t)src < a.T * a.K;
+          t = ok ? src / a.K : 0;
+          wt = ok ? __ldg(a.topk_w + src) : 0.f;
+          if (!ok) atomicOr(a.err, kErrBounds);
+        }
+        if (ok) atomicAdd(a.out_acc + t * a.d + j0 + q, wt * y);
+      }
+    }
+  }
+  if (over) atomicOr(a.err, kErrRange);
+}
+
+template <int FMT, int R>
+cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, cudaStream_t s) {
+  return phase == 0 ? launch(small_batch_ffn_kernel<FMT, R, 0>, grid, kThreads, 0, s, a)
+                    : launch(small_batch_ffn_kernel<FMT, R, 1>, grid, kThreads, 0, s, a);
+}
+
+template <int FMT>
+cudaError_t launch_f(const SmallBatchArgs& a, int phase, unsigned grid, cudaStream_t s) {
+  if (a.max_rows <= 1) return launch_fr<FMT, 1>(a, phase, grid, s);
+  if (a.max_rows <= 2) return launch_fr<FMT, 2>(a, phase, grid, s);
+  if constexpr (FMT == kSmallE2M1) {
+    return cudaErrorInvalidValue;  // MXFP4 experts take this path for at most 2 rows
+  } else {
+    return launch_fr<FMT, 4>(a, phase, grid, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStream_t s) {
+  if (a.max_rows < 1 || a.max_rows > kSmallBatchMaxRows || a.N > kMaxExperts) return cudaErrorInvalidValue;
+  if (a.fmt != kSmallBf16 && a.fmt != kSmallE4M3 && a.fmt != kSmallE2M1) return cudaErrorInvalidValue;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // items: at most min(N, rows) routed experts hold rows
+  const int64_t touched = a.N < a.routed_rows ? a.N : a.routed_rows;
+  const int64_t per_r = phase == 0 ? a.F / 2 : a.d / kRowsPerItem;
+  const int64_t per_s = phase == 0 ? a.Fs / 2 : a.d / kRowsPerItem;
+  const int64_t items = touched * per_r + (a.S > 0 ? a.S * per_s : 0);
+  int64_t want = (items + kWarps - 1) / kWarps;
+  if (want < 1) want = 1;
+  const unsigned grid = (unsigned)(want < sms ? want : sms);
+  if (a.fmt == kSmallBf16) return launch_f<kSmallBf16>(a, phase, grid, s);
+  if (a.fmt == kSmallE4M3) return launch_f<kSmallE4M3>(a, phase, grid, s);
+  return launch_f<kSmallE2M1>(a, phase, grid, s);
+}
+
+}  // namespace moe

@@ -45,6 +45,9 @@ MID = {
     # small batches with few GEMM tiles (a shared expert; a ragged K)
     "fp8_small_shared": _cfg("fp8_small_shared", T=2, d=2048, N=64, K=4, F=272, S=1, Fs=256),
     "fp8_small_ragged": _cfg("fp8_small_ragged", T=5, d=1552, N=32, K=3, F=400),
+    # decode-sized batch on the CUDA cores: a capacity limit, a shared expert, fp32 hidden
+    "fp8_small_capacity_shared": _cfg("fp8_small_capacity_shared", T=4, d=144, N=8, K=3, F=80, S=1, Fs=48,
+                                      hidden_dtype="f32", capacity_factor=0.5),
     # T*K >= 8192 copies: each token's row is split once and stored to its K packed rows
     # (d / 8 = 34 vectors: a partial last trip of the warp's loop; fp32 hidden, a shared
     # expert and a capacity limit)

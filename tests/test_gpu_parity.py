@@ -52,6 +52,12 @@ MID = {
     "fused_topk_f32_T7": inputs.MoEConfig("fused_topk_f32_T7", T=7, d=384, N=256, K=8, F=64, hidden_dtype="f32",
                                           renormalize=0),
     "fused_topk_T8_N96": inputs.MoEConfig("fused_topk_T8_N96", T=8, d=256, N=96, K=4, F=64),
+    # decode-sized batches (T <= 4): expert FFNs on the CUDA cores; ragged d (17
+    # 16-byte units per row), a capacity limit, two shared experts, fp32 hidden
+    "small_capacity_shared_f32": inputs.MoEConfig("small_capacity_shared_f32", T=4, d=136, N=8, K=3, F=72, S=2,
+                                                  Fs=40, hidden_dtype="f32", score="sigmoid",
+                                                  capacity_factor=0.5),
+    "small_T2_ragged": inputs.MoEConfig("small_T2_ragged", T=2, d=200, N=32, K=4, F=104),
     # T*K >= 8192 copies: the token-major row copy (ragged d; fp32 hidden with a shared
     # expert and a capacity limit)
     "scatter_copy_ragged": inputs.MoEConfig("scatter_copy_ragged", T=2100, d=264, N=16, K=4, F=136),

@@ -35,7 +35,7 @@ def _worker(rank, world, port, out):
 
 def test_replica_throughput_uses_the_slowest_rank():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
     for rank in range(world):
