@@ -461,17 +461,17 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights
 
 /*
  * 1 if moe_layer_forward runs problem p's expert FFNs on the CUDA cores
- * (a decode-sized token-choice batch: T <= 4 tokens, T <= 2 for MXFP4
- * experts), 0 if on the grouped tensor-core GEMMs, -1 if p is invalid. Host
- * only, no CUDA call.
+ * (a decode-sized token-choice batch: T <= 4 tokens with bf16 experts, one
+ * token with FP8 experts; never for MXFP4 experts), 0 if on the grouped
+ * tensor-core GEMMs, -1 if p is invalid. Host only, no CUDA call.
  * With T tokens an expert holds at most T rows ("Part 12", "What happens when
  * many users share the GPU?": each token reads its own experts' weights, and
  * the bytes, not the arithmetic, set the time at small batch; "Mixture of
  * Experts Explained", "Why batching erodes the advantage"). A 128-row tensor
  * tile would then be almost all padding, so each touched weight row is instead
  * streamed from HBM once by the CUDA cores and dotted with its expert's rows
- * (fp32 products and sums; h rounded to bf16, or fp16 for FP8 / MXFP4 experts,
- * as on the GEMM path). Same inputs, outputs, workspace and status codes.
+ * (fp32 products and sums; h rounded to bf16, or fp16 for FP8 experts, as on
+ * the GEMM path). Same inputs, outputs, workspace and status codes.
  */
 int32_t moe_layer_small_batch(const moe_problem_t* p);
 

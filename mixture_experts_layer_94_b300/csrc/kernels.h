@@ -180,9 +180,10 @@ cudaError_t launch_gather_quant(const PermuteArgs& a, int64_t rows, int64_t shar
 cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* dst, float* scale,
                              cudaStream_t s);
 // The expert FFNs of a decode-sized token-choice batch on the CUDA cores
-// (small_batch.cu): every group holds at most max_rows (<= 4) rows, so each
-// weight row is streamed from HBM once and dotted with the group's rows.
-enum SmallBatchFormat { kSmallBf16 = 0, kSmallE4M3 = 1, kSmallE2M1 = 2 };
+// (small_batch.cu): every group holds at most max_rows (<= 4; 1 for FP8
+// experts) rows, so each weight row is streamed from HBM once and dotted with
+// the group's rows.
+enum SmallBatchFormat { kSmallBf16 = 0, kSmallE4M3 = 1 };
 constexpr int kSmallBatchMaxRows = 4;
 struct SmallBatchArgs {
   int32_t fmt;               // SmallBatchFormat of the expert weights
@@ -191,23 +192,22 @@ struct SmallBatchArgs {
   int64_t T;
   int64_t routed_rows;       // T * K: bounds the experts that can hold rows
   const GroupDesc* groups;   // [N + S], built by the route kernels
-  const void* x_routed;      // [rows][d] packed rows: bf16, or fp16 for FP8 / MXFP4 experts
+  const void* x_routed;      // [rows][d] packed rows: bf16, or fp16 for FP8 experts
   const void* x_shared;      // [T][d] in the same format (S > 0)
-  const void* w_gate;        // codes [N][F][d], [N][F][d], [N][d][F] (bf16, E4M3, or packed E2M1)
+  const void* w_gate;        // codes [N][F][d], [N][F][d], [N][d][F] (bf16 or E4M3)
   const void* w_up;
   const void* w_down;
   const void* s_gate;        // shared experts: [S][Fs][d], [S][Fs][d], [S][d][Fs]
   const void* s_up;
   const void* s_down;
-  // FP8: fp32 scale per weight row; MXFP4: E8M0 scale per 32 elements of a
-  // row ([rows][K/32]); unused for bf16
+  // FP8: fp32 scale per weight row; unused for bf16
   const void* w_gate_scale;
   const void* w_up_scale;
   const void* w_down_scale;
   const void* s_gate_scale;
   const void* s_up_scale;
   const void* s_down_scale;
-  void* h;                   // [rows][F] SiLU(g) * u: bf16, or fp16 for FP8 / MXFP4 experts
+  void* h;                   // [rows][F] SiLU(g) * u: bf16, or fp16 for FP8 experts
   void* h_sh;                // [S*T][Fs]
   float* out_acc;            // [T][d] fp32, cleared beforehand
   const int32_t* perm_src;   // [rows] packed row -> t*K + k

@@ -93,12 +93,13 @@ bool needs_act_copy(const moe_problem_t& p) {
 
 // Token-choice batches of at most this many tokens run the expert FFNs on the
 // CUDA cores (small_batch.cu), one pass over each touched weight row, instead
-// of the grouped GEMMs: each expert then holds at most T rows. MXFP4 stops at
-// 2 tokens, where decoding the 4-bit codes for more rows would cost more ALU
-// time than the weights' HBM time.
+// of the grouped GEMMs: each expert then holds at most T rows. The bounds are
+// measured: bf16 weights gain up to 4 tokens; FP8 codes only for a single
+// token, since widening them to fp32 costs ALU time that grows with the rows;
+// MXFP4 codes never (the tensor-core path is faster even for one token).
 int32_t small_batch_rows(const moe_problem_t& p) {
-  if (p.routing != MOE_ROUTING_TOKEN_CHOICE || p.T < 1 || stored_combine(p)) return 0;
-  const int64_t max_t = is_mx(p) ? 2 : kSmallBatchMaxRows;
+  if (p.routing != MOE_ROUTING_TOKEN_CHOICE || p.T < 1 || stored_combine(p) || is_mx(p)) return 0;
+  const int64_t max_t = is_fp8(p) ? 1 : kSmallBatchMaxRows;
   return p.T <= max_t ? (int32_t)p.T : 0;
 }
 
@@ -1100,7 +1101,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     // 4-5. decode-sized batch: SwiGLU and the weighted scatter-add on the CUDA
     // cores, each touched weight row streamed once
     SmallBatchArgs sb{};
-    sb.fmt = is_mx(*p) ? kSmallE2M1 : is_fp8(*p) ? kSmallE4M3 : kSmallBf16;
+    sb.fmt = is_fp8(*p) ? kSmallE4M3 : kSmallBf16;
     sb.max_rows = small_rows;
     sb.N = N;
     sb.S = S;

@@ -11,12 +11,12 @@
 // the expert's activation rows, which stay in L1/L2. One 512-thread CTA per SM
 // walks all (expert, row block) items, so every SM streams weights.
 //
-// Formats: bf16 weights with bf16 activations; FP8 E4M3 codes with fp32 row
-// scales, or MXFP4 (E2M1 codes, E8M0 scale per 32 elements) with fp16
-// activations. Products and sums are fp32; h is rounded once, to bf16 (fp16
-// for FP8 / MXFP4 experts), as the grouped GEMMs store it.
+// Formats: bf16 weights with bf16 activations (up to 4 rows per expert), or
+// FP8 E4M3 codes with fp32 row scales and fp16 activations (one row: widening
+// the codes to fp32 costs ALU time per row, so the tensor-core path wins from
+// two rows on). Products and sums are fp32; h is rounded once, to bf16 (fp16
+// for FP8 experts), as the grouped GEMMs store it.
 
-#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -30,9 +30,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerItem = 4;  // weight rows a warp streams together
 
 // Elements in one 16-byte unit of weight codes.
-__host__ __device__ constexpr int unit_elems(int fmt) {
-  return fmt == kSmallBf16 ? 8 : fmt == kSmallE4M3 ? 16 : 32;
-}
+__host__ __device__ constexpr int unit_elems(int fmt) { return fmt == kSmallBf16 ? 8 : 16; }
 
 // 16 bytes of weight codes, read once: no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -72,14 +70,8 @@ __device__ __forceinline__ float2 e4m3x2_f32(uint32_t c) {
   return half2_bits_to_f32((uint32_t)h.x | ((uint32_t)h.y << 16));
 }
 
-// Two E2M1 codes of one byte (the low nibble is the earlier element).
-__device__ __forceinline__ float2 e2m1x2_f32(uint32_t c) {
-  const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(c & 0xFFu), __NV_E2M1);
-  return half2_bits_to_f32((uint32_t)h.x | ((uint32_t)h.y << 16));
-}
-
 // Elements 8s .. 8s+7 of a 16-byte unit of weight codes, as fp32 code values
-// (FP8 row scales and MXFP4 block scales are applied by the caller).
+// (FP8 row scales are applied by the caller).
 template <int FMT>
 __device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -89,7 +81,7 @@ __device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
       f[2 * i] = __uint_as_float(w[i] << 16);
       f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
-  } else if (FMT == kSmallE4M3) {  // 16 codes per unit: words 2s, 2s+1
+  } else {  // 16 E4M3 codes per unit: words 2s, 2s+1
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const uint32_t c = w[2 * s + i];
@@ -99,57 +91,31 @@ __device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
       f[4 * i + 2] = b.x;
       f[4 * i + 3] = b.y;
     }
-  } else {  // 32 codes per unit, two per byte: word s
-    const uint32_t c = w[s];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 a = e2m1x2_f32(c >> (8 * i));
-      f[2 * i] = a.x;
-      f[2 * i + 1] = a.y;
-    }
   }
 }
 
-// E8M0 block scale 2^(e - 127); e = 0 is 2^-127 (an fp32 subnormal).
-__device__ __forceinline__ float e8m0_f32(uint32_t e) {
-  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
-}
-
 // acc[q][r] += (weight row q) . (activation row r) over `units` 16-byte units
-// of codes (unit j covers elements j*E .. j*E+E-1). Activation row r starts at
-// x + r * x_pitch (16-byte vectors of 8 elements); rows >= `rows` are skipped.
-// MXFP4: bsc[q] is row q's E8M0 block scales, one per unit.
+// of codes (unit j covers elements j*E .. j*E+E-1), then summed over the warp.
+// Activation row r starts at x + r * x_pitch (16-byte vectors of 8 elements);
+// rows >= `rows` are skipped.
 template <int FMT, int R>
-__device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem],
-                                         const uint8_t* const (&bsc)[kRowsPerItem], const uint4* x,
-                                         int64_t x_pitch, int rows, int units, int lane,
-                                         float (&acc)[kRowsPerItem][R]) {
+__device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], const uint4* x, int64_t x_pitch,
+                                         int rows, int units, int lane, float (&acc)[kRowsPerItem][R]) {
   constexpr int E = unit_elems(FMT), SUB = E / 8;
   constexpr int U = R == 1 ? 4 : 2;  // units per row in flight per lane
   constexpr bool kF16 = FMT != kSmallBf16;
   for (int j0 = lane; j0 < units; j0 += 32 * U) {
     uint4 wv[kRowsPerItem][U];
-    float sc[kRowsPerItem][U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int j = j0 + 32 * u;
 #pragma unroll
-      for (int q = 0; q < kRowsPerItem; ++q) {
-        wv[q][u] = j < units ? ld_stream(w[q] + j) : make_uint4(0u, 0u, 0u, 0u);
-        if (FMT == kSmallE2M1) sc[q][u] = j < units ? e8m0_f32(__ldg(bsc[q] + j)) : 0.f;
-      }
+      for (int q = 0; q < kRowsPerItem; ++q) wv[q][u] = j < units ? ld_stream(w[q] + j) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int j = j0 + 32 * u;
       if (j < units) {
-        float part[kRowsPerItem][R];
-        if (FMT == kSmallE2M1) {
-#pragma unroll
-          for (int q = 0; q < kRowsPerItem; ++q)
-#pragma unroll
-            for (int r = 0; r < R; ++r) part[q][r] = 0.f;
-        }
 #pragma unroll
         for (int s = 0; s < SUB; ++s) {
           float xf[R][8];
@@ -164,18 +130,11 @@ __device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem],
 #pragma unroll
             for (int r = 0; r < R; ++r) {
               if (r < rows) {
-                float& dst = FMT == kSmallE2M1 ? part[q][r] : acc[q][r];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst = fmaf(wf[i], xf[r][i], dst);
+                for (int i = 0; i < 8; ++i) acc[q][r] = fmaf(wf[i], xf[r][i], acc[q][r]);
               }
             }
           }
-        }
-        if (FMT == kSmallE2M1) {
-#pragma unroll
-          for (int q = 0; q < kRowsPerItem; ++q)
-#pragma unroll
-            for (int r = 0; r < R; ++r) acc[q][r] = fmaf(sc[q][u], part[q][r], acc[q][r]);
         }
       }
     }
@@ -257,17 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       const uint4* wu = static_cast<const uint4*>(kind ? a.s_up : a.w_up);
       const uint4* const w[kRowsPerItem] = {wg + row0 * units, wg + (row0 + 1) * units, wu + row0 * units,
                                             wu + (row0 + 1) * units};
-      const uint8_t* bsc[kRowsPerItem] = {nullptr, nullptr, nullptr, nullptr};
-      if (FMT == kSmallE2M1) {
-        const uint8_t* bg = static_cast<const uint8_t*>(kind ? a.s_gate_scale : a.w_gate_scale);
-        const uint8_t* bu = static_cast<const uint8_t*>(kind ? a.s_up_scale : a.w_up_scale);
-        bsc[0] = bg + row0 * units;
-        bsc[1] = bg + (row0 + 1) * units;
-        bsc[2] = bu + row0 * units;
-        bsc[3] = bu + (row0 + 1) * units;
-      }
       const uint4* x = static_cast<const uint4*>(kind ? a.x_shared : a.x_routed) + (int64_t)gd.a_row0 * (a.d / 8);
-      dot_rows<FMT, R>(w, bsc, x, a.d / 8, rows, (int)units, lane, acc);
+      dot_rows<FMT, R>(w, x, a.d / 8, rows, (int)units, lane, acc);
       float gs0 = 1.f, gs1 = 1.f, us0 = 1.f, us1 = 1.f;
       if (FMT == kSmallE4M3) {
         const float* sg = static_cast<const float*>(kind ? a.s_gate_scale : a.w_gate_scale);
@@ -294,14 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       const uint4* wd = static_cast<const uint4*>(kind ? a.s_down : a.w_down);
       const uint4* const w[kRowsPerItem] = {wd + row0 * units, wd + (row0 + 1) * units, wd + (row0 + 2) * units,
                                             wd + (row0 + 3) * units};
-      const uint8_t* bsc[kRowsPerItem] = {nullptr, nullptr, nullptr, nullptr};
-      if (FMT == kSmallE2M1) {
-        const uint8_t* bd = static_cast<const uint8_t*>(kind ? a.s_down_scale : a.w_down_scale);
-#pragma unroll
-        for (int q = 0; q < kRowsPerItem; ++q) bsc[q] = bd + (row0 + q) * units;
-      }
       const uint4* x = static_cast<const uint4*>(kind ? a.h_sh : a.h) + (int64_t)gd.h_row0 * (Fk / 8);
-      dot_rows<FMT, R>(w, bsc, x, Fk / 8, rows, (int)units, lane, acc);
+      dot_rows<FMT, R>(w, x, Fk / 8, rows, (int)units, lane, acc);
       const int q = lane & (kRowsPerItem - 1), rl = lane / kRowsPerItem;
       if (rl < rows) {
         float y = 0.f;
@@ -335,22 +279,12 @@ cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, cudaStr
                     : launch(small_batch_ffn_kernel<FMT, R, 1>, grid, kThreads, 0, s, a);
 }
 
-template <int FMT>
-cudaError_t launch_f(const SmallBatchArgs& a, int phase, unsigned grid, cudaStream_t s) {
-  if (a.max_rows <= 1) return launch_fr<FMT, 1>(a, phase, grid, s);
-  if (a.max_rows <= 2) return launch_fr<FMT, 2>(a, phase, grid, s);
-  if constexpr (FMT == kSmallE2M1) {
-    return cudaErrorInvalidValue;  // MXFP4 experts take this path for at most 2 rows
-  } else {
-    return launch_fr<FMT, 4>(a, phase, grid, s);
-  }
-}
 
 }  // namespace
 
 cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStream_t s) {
   if (a.max_rows < 1 || a.max_rows > kSmallBatchMaxRows || a.N > kMaxExperts) return cudaErrorInvalidValue;
-  if (a.fmt != kSmallBf16 && a.fmt != kSmallE4M3 && a.fmt != kSmallE2M1) return cudaErrorInvalidValue;
+  if (a.fmt == kSmallE4M3 ? a.max_rows != 1 : a.fmt != kSmallBf16) return cudaErrorInvalidValue;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // items: at most min(N, rows) routed experts hold rows
@@ -361,9 +295,10 @@ cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStrea
   int64_t want = (items + kWarps - 1) / kWarps;
   if (want < 1) want = 1;
   const unsigned grid = (unsigned)(want < sms ? want : sms);
-  if (a.fmt == kSmallBf16) return launch_f<kSmallBf16>(a, phase, grid, s);
-  if (a.fmt == kSmallE4M3) return launch_f<kSmallE4M3>(a, phase, grid, s);
-  return launch_f<kSmallE2M1>(a, phase, grid, s);
+  if (a.fmt == kSmallE4M3) return launch_fr<kSmallE4M3, 1>(a, phase, grid, s);
+  if (a.max_rows <= 1) return launch_fr<kSmallBf16, 1>(a, phase, grid, s);
+  if (a.max_rows <= 2) return launch_fr<kSmallBf16, 2>(a, phase, grid, s);
+  return launch_fr<kSmallBf16, 4>(a, phase, grid, s);
 }
 
 }  // namespace moe

@@ -83,24 +83,25 @@ def test_layer_kernel_count():
 
 
 def test_decode_sized_batches_take_the_cuda_core_expert_path():
-    # token choice with T <= 4 (T <= 2 for MXFP4 experts) runs the expert FFNs
-    # on the CUDA cores; larger batches and expert choice keep the GEMMs
+    # token choice with T <= 4 bf16 experts or one token with FP8 experts runs
+    # the expert FFNs on the CUDA cores; larger batches, MXFP4 experts and
+    # expert choice keep the GEMMs
     q = inputs.QWEN_DECODE
     for T, want in ((1, True), (2, True), (4, True), (5, False), (8, False), (0, False)):
         assert B.layer_small_batch(B.problem(q, T=T)) == want, T
-    for T, want in ((1, True), (4, True), (5, False)):
+    for T, want in ((1, True), (2, False)):
         assert B.layer_small_batch(B.problem(inputs.QWEN_DECODE_FP8, T=T)) == want, T
-    for T, want in ((1, True), (2, True), (3, False)):
-        assert B.layer_small_batch(B.problem(inputs.QWEN_DECODE_MXFP4, T=T)) == want, T
+    assert not B.layer_small_batch(B.problem(inputs.QWEN_DECODE_MXFP4, T=1))
     assert not B.layer_small_batch(B.problem(inputs.MIXTRAL_EC, T=2))
     with pytest.raises(ValueError):
         B.layer_small_batch(B.problem(q, top_k=0))
     # router (CUDA-core logits + top-K), route-and-pack (one CTA + gather),
-    # gate/up, down, finalise: no activation splits, no MXFP4 preparation
-    for cfg in (q, inputs.QWEN_DECODE_FP8, inputs.QWEN_DECODE_MXFP4,
-                q.with_(S=1, Fs=512, hidden_dtype="f32")):
+    # gate/up, down, finalise: no activation splits
+    for cfg in (q, inputs.QWEN_DECODE_FP8, q.with_(S=1, Fs=512, hidden_dtype="f32")):
         assert B.layer_forward_kernel_count(B.problem(cfg, T=1)) == 7, cfg.name
-    assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_MXFP4, T=3)) == 11
+    # the GEMM path adds the split of h (FP8), or of h and the MXFP4 preparation
+    assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_FP8, T=2)) == 8
+    assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_MXFP4, T=1)) == 11
 
 
 def _fake_prepared():

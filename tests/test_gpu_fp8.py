@@ -45,7 +45,10 @@ MID = {
     # small batches with few GEMM tiles (a shared expert; a ragged K)
     "fp8_small_shared": _cfg("fp8_small_shared", T=2, d=2048, N=64, K=4, F=272, S=1, Fs=256),
     "fp8_small_ragged": _cfg("fp8_small_ragged", T=5, d=1552, N=32, K=3, F=400),
-    # decode-sized batch on the CUDA cores: a capacity limit, a shared expert, fp32 hidden
+    # a single token: expert FFNs on the CUDA cores (ragged d: 9 16-byte units of
+    # codes per row), a shared expert, fp32 hidden
+    "fp8_T1_shared_f32": _cfg("fp8_T1_shared_f32", T=1, d=144, N=8, K=3, F=80, S=1, Fs=48, hidden_dtype="f32"),
+    # a small batch with a capacity limit and a shared expert
     "fp8_small_capacity_shared": _cfg("fp8_small_capacity_shared", T=4, d=144, N=8, K=3, F=80, S=1, Fs=48,
                                       hidden_dtype="f32", capacity_factor=0.5),
     # T*K >= 8192 copies: each token's row is split once and stored to its K packed rows

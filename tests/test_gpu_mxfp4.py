@@ -37,8 +37,8 @@ MID = {
     "mx_capacity": _cfg("mx_capacity", T=300, d=288, N=16, K=4, F=416, capacity_factor=0.8),
     # a small batch with few GEMM tiles and a shared expert
     "mx_small_shared": _cfg("mx_small_shared", T=2, d=2048, N=64, K=4, F=288, S=1, Fs=256),
-    # decode-sized batch on the CUDA cores: a capacity limit (two tokens on three
-    # experts always share one), a shared expert, fp32 hidden
+    # a small batch with a capacity limit (two tokens on three experts always
+    # share one), a shared expert, fp32 hidden
     "mx_small_capacity_shared_f32": _cfg("mx_small_capacity_shared_f32", T=2, d=96, N=3, K=2, F=160, S=1, Fs=64,
                                          hidden_dtype="f32", capacity_factor=0.5),
     # T*K >= 8192 copies: the token-major split, with a shared expert

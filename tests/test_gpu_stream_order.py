@@ -23,8 +23,8 @@ CASES = {
     "bf16_prefill_shared": inputs.MoEConfig("bf16_prefill_shared", T=700, d=512, N=16, K=4, F=384, S=1, Fs=256,
                                             score="sigmoid", sel_bias_var=0.1),
     "fp8_decode": inputs.MoEConfig("fp8_decode", T=5, d=1024, N=64, K=4, F=256, expert_dtype="fp8"),
-    # decode-sized batches: expert FFNs on the CUDA cores
-    "fp8_decode_T2_shared": inputs.MoEConfig("fp8_decode_T2_shared", T=2, d=1024, N=64, K=4, F=256, S=1, Fs=128,
+    # single tokens: expert FFNs on the CUDA cores (FP8), on the GEMMs (MXFP4)
+    "fp8_decode_T1_shared": inputs.MoEConfig("fp8_decode_T1_shared", T=1, d=1024, N=64, K=4, F=256, S=1, Fs=128,
                                              expert_dtype="fp8"),
     "mxfp4_decode_T1": inputs.MoEConfig("mxfp4_decode_T1", T=1, d=1024, N=64, K=4, F=256, expert_dtype="mxfp4"),
     "mxfp4_mixed": inputs.MoEConfig("mxfp4_mixed", T=40, d=512, N=32, K=4, F=320, S=1, Fs=128,
