@@ -81,6 +81,8 @@ struct PermuteArgs {
   uint8_t* xq_sh;
   float* sx_sh;
   uint32_t* err;
+  // Only the histogram, scans, scatter (and schedule): no row copy.
+  bool route_only;
   // Optional: also build the GEMM schedule (as launch_schedule) from the new
   // offsets; skipped when groups == nullptr.
   GroupDesc* groups;
@@ -192,8 +194,8 @@ struct SmallBatchArgs {
   int64_t T;
   int64_t routed_rows;       // T * K: bounds the experts that can hold rows
   const GroupDesc* groups;   // [N + S], built by the route kernels
-  const void* x_routed;      // [rows][d] packed rows: bf16, or fp16 for FP8 experts
-  const void* x_shared;      // [T][d] in the same format (S > 0)
+  const void* hidden;        // [T][d] the layer's input rows (a packed row's token via perm_src)
+  bool hidden_bf16;          // bf16 hidden, else fp32
   const void* w_gate;        // codes [N][F][d], [N][F][d], [N][d][F] (bf16 or E4M3)
   const void* w_up;
   const void* w_down;
@@ -209,12 +211,16 @@ struct SmallBatchArgs {
   const void* s_down_scale;
   void* h;                   // [rows][F] SiLU(g) * u: bf16, or fp16 for FP8 experts
   void* h_sh;                // [S*T][Fs]
-  float* out_acc;            // [T][d] fp32, cleared beforehand
+  float* out_acc;            // [T][d] fp32 (cleared by phase 0)
+  __nv_bfloat16* out;        // [T][d] bf16(out_acc), written by phase 1's last CTA
+  uint32_t* done;            // phase 1's count of finished CTAs (reset by phase 0)
   const int32_t* perm_src;   // [rows] packed row -> t*K + k
   const float* topk_w;       // [T*K]
   uint32_t* err;
 };
-// phase 0: h = SiLU(x W_gate^T) * (x W_up^T); phase 1: out_acc[t] += w * h W_down^T.
+// phase 0: h = SiLU(x W_gate^T) * (x W_up^T) with x each packed row's token
+// row of hidden, rounded to the activation format; out_acc = 0.
+// phase 1: out_acc[t] += w * h W_down^T, then out = bf16(out_acc).
 cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStream_t s);
 
 // uint8 row-major matrix [rows][inner] as a TMA tensor map: box

@@ -52,7 +52,7 @@ MxOffsets mx_offsets(const moe_problem_t& p, bool shared, Take&& take) {
 
 struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
-  size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc;
+  size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc, done;
   size_t y_rows, y_sh;  // token choice with a large accumulator: the down GEMM's stored rows (see stored_combine)
   size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 / MXFP4 experts: two-term E4M3 activations + row scales
   MxOffsets mx;  // MXFP4 experts: the per-call preparation of the weights in use
@@ -157,6 +157,7 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.h = take((size_t)rows * p.ffn * 2);
     if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
     L.out_acc = take((size_t)T * p.d_model * 4);
+    L.done = take(4);
     if (stored_combine(p)) {
       L.y_rows = take((size_t)TK * p.d_model * 2);
       if (p.n_shared > 0) L.y_sh = take((size_t)p.n_shared * T * p.d_model * 2);
@@ -1081,7 +1082,15 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.act_f16 = fp8;
   pa.err = err;
   const int32_t small_rows = small_batch_rows(*p);
-  if (fp8 && !small_rows) set_gather_quant(&pa, ws, L, S > 0);
+  if (small_rows) {
+    // the CUDA-core FFNs read the tokens' rows from hidden and clear the
+    // accumulator themselves: routing only
+    pa.route_only = true;
+    pa.zero_rows = nullptr;
+    pa.x_act = nullptr;
+  } else if (fp8) {
+    set_gather_quant(&pa, ws, L, S > 0);
+  }
   // 3. the GEMM schedule (routed experts from offsets, then the shared
   //    experts) is built by the same kernel that finishes the prefix sums
   const int32_t tile_rows = gemm_tile_rows(*p, T * K);
@@ -1112,8 +1121,8 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     sb.T = T;
     sb.routed_rows = T * K;
     sb.groups = pa.groups;
-    sb.x_routed = pa.x_perm;
-    sb.x_shared = pa.x_act ? pa.x_act : hidden;
+    sb.hidden = hidden;
+    sb.hidden_bf16 = hbf16;
     sb.w_gate = w->w_gate;
     sb.w_up = w->w_up;
     sb.w_down = w->w_down;
@@ -1129,15 +1138,16 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     sb.h = at<void>(ws, L.h);
     sb.h_sh = S > 0 ? at<void>(ws, L.h_sh) : nullptr;
     sb.out_acc = at<float>(ws, L.out_acc);
+    sb.out = static_cast<__nv_bfloat16*>(out);
+    sb.done = at<uint32_t>(ws, L.done);
     sb.perm_src = pa.perm_src;
     sb.topk_w = topk_w;
     sb.err = err;
     MOE_TRY(cuda_status(launch_small_batch_ffn(sb, 0, s)));
     MOE_TRY(record(ev, 4, s));
+    // 6. (the down kernel's last CTA rounds the accumulator to the output)
     MOE_TRY(cuda_status(launch_small_batch_ffn(sb, 1, s)));
     MOE_TRY(record(ev, 5, s));
-    // 6. fp32 -> bf16
-    MOE_TRY(cuda_status(launch_finalize(sb.out_acc, static_cast<__nv_bfloat16*>(out), T * p->d_model, s)));
     return record(ev, 6, s);
   }
 
@@ -1285,7 +1295,8 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights
   const int quant = (is_lowp(*p) ? (p->n_shared > 0 ? 2 : 1) : 0) + (prep ? (p->n_shared > 0 ? 6 : 3) : 0);
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
-  if (small_batch_rows(*p)) return router + route + 3;  // gate/up, down, finalise on the CUDA cores
+  // routing without the row copy; gate/up and down (+ finalise) on the CUDA cores
+  if (small_batch_rows(*p)) return router + 1 + 2;
   return router + route + 3 + quant;
 }
 

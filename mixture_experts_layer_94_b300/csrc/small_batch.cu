@@ -11,6 +11,12 @@
 // the expert's activation rows, which stay in L1/L2. One 512-thread CTA per SM
 // walks all (expert, row block) items, so every SM streams weights.
 //
+// Two launches do the whole FFN part of the layer: the gate/up kernel reads
+// each packed row's token straight from hidden (no permuted copy), rounded as
+// the row gather would store it, and clears the fp32 accumulator; the down
+// kernel adds the gate-weighted rows into it, and its last CTA to finish
+// rounds it to the bf16 output (no separate finalise launch).
+//
 // Formats: bf16 weights with bf16 activations (up to 4 rows per expert), or
 // FP8 E4M3 codes with fp32 row scales and fp16 activations (one row: widening
 // the codes to fp32 costs ALU time per row, so the tensor-core path wins from
@@ -94,13 +100,50 @@ __device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
   }
 }
 
+// Where the dot products' activation rows come from.
+enum XSource {
+  kXAct16 = 0,      // rows in the activation format (h: bf16, or fp16 for FP8 experts)
+  kXHiddenBf16 = 1, // bf16 hidden rows
+  kXHiddenF32 = 2,  // fp32 hidden rows
+};
+
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// x rounded to fp16 (nearest even); `over` is set when a finite x lies beyond
+// fp16's range, as the row gather reports it.
+__device__ __forceinline__ float round_f16(float x, bool& over) {
+  const float m = fabsf(x);
+  over |= (m >= 65520.f) && (m <= 3.402823466e38f);
+  return __half2float(__float2half_rn(x));
+}
+
+// Elements 8v .. 8v+7 of an activation row as fp32, rounded as the layer's
+// activation format holds them: bf16 for bf16 experts, fp16 (F16) for FP8.
+template <int XS, bool F16>
+__device__ __forceinline__ void x8(const void* row, int64_t v, float (&f)[8], bool& over) {
+  if (XS == kXHiddenF32) {
+    const float4* p = static_cast<const float4*>(row) + 2 * v;
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = F16 ? round_f16(t[i], over) : round_bf16(t[i]);
+  } else {
+    const uint4 u = __ldg(static_cast<const uint4*>(row) + v);
+    act8<XS == kXAct16 && F16>(u, f);
+    if (XS == kXHiddenBf16 && F16) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = round_f16(f[i], over);
+    }
+  }
+}
+
 // acc[q][r] += (weight row q) . (activation row r) over `units` 16-byte units
 // of codes (unit j covers elements j*E .. j*E+E-1), then summed over the warp.
-// Activation row r starts at x + r * x_pitch (16-byte vectors of 8 elements);
-// rows >= `rows` are skipped.
-template <int FMT, int R>
-__device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], const uint4* x, int64_t x_pitch,
-                                         int rows, int units, int lane, float (&acc)[kRowsPerItem][R]) {
+// Activation row r starts at xr[r]; rows >= `rows` are skipped.
+template <int FMT, int R, int XS>
+__device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], const void* const (&xr)[R],
+                                         int rows, int units, int lane, float (&acc)[kRowsPerItem][R],
+                                         bool& over) {
   constexpr int E = unit_elems(FMT), SUB = E / 8;
   constexpr int U = R == 1 ? 4 : 2;  // units per row in flight per lane
   constexpr bool kF16 = FMT != kSmallBf16;
@@ -121,7 +164,7 @@ __device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], 
           float xf[R][8];
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            if (r < rows) act8<kF16>(__ldg(x + r * x_pitch + (int64_t)j * SUB + s), xf[r]);
+            if (r < rows) x8<XS, kF16>(xr[r], (int64_t)j * SUB + s, xf[r], over);
           }
 #pragma unroll
           for (int q = 0; q < kRowsPerItem; ++q) {
@@ -151,17 +194,29 @@ __device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], 
 __device__ __forceinline__ int64_t row_units(int k, int fmt) { return k / unit_elems(fmt); }
 
 // PHASE 0: h[row r][f, f+1] = SiLU(g) * u for the item's gate rows f, f+1 and
-// up rows f, f+1. PHASE 1: out_acc[token of r][j..j+3] += w_r * y for W_down
-// rows j..j+3. Items: every routed expert holding rows (F/2 or d/4 items
-// each), then every shared expert (Fs/2 or d/4 items each).
-template <int FMT, int R, int PHASE>
+// up rows f, f+1, with the rows' tokens read from hidden (source XS); also
+// clears out_acc and the down kernel's completion count. PHASE 1 (XS =
+// kXAct16): out_acc[token of r][j..j+3] += w_r * y for W_down rows j..j+3; the
+// last CTA to finish writes out = bf16(out_acc). Items: every routed expert
+// holding rows (F/2 or d/4 items each), then every shared expert (Fs/2 or d/4
+// items each); item i goes to warp i / gridDim.x of CTA i % gridDim.x, so a
+// partial last round still spreads over every SM.
+template <int FMT, int R, int PHASE, int XS>
 __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const SmallBatchArgs a) {
   pdl_trigger();
   pdl_wait();
   __shared__ int32_t s_list[kMaxExperts];
   __shared__ int32_t s_count[kWarps];
+  __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
+  if (PHASE == 0) {
+    const int64_t nacc = a.T * a.d / 4;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nacc; i += (int64_t)gridDim.x * kThreads)
+      reinterpret_cast<float4*>(a.out_acc)[i] = zero;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.done = 0u;
+  }
   // the routed experts that hold rows, in expert order (N <= 256 < kThreads)
   const bool has = (int)threadIdx.x < N && a.groups[threadIdx.x].rows > 0;
   const uint32_t ball = __ballot_sync(0xFFFFFFFFu, has);
@@ -183,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
   const int64_t n_r = (int64_t)nr * per_r;
   const int64_t total = n_r + (a.S > 0 ? (int64_t)a.S * per_s : 0);
   bool over = false;
-  for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < total; item += (int64_t)gridDim.x * kWarps) {
+  for (int64_t item = (int64_t)warp * gridDim.x + blockIdx.x; item < total; item += (int64_t)gridDim.x * kWarps) {
     int g, blk;
     if (item < n_r) {
       g = s_list[item / per_r];
@@ -216,8 +271,23 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       const uint4* wu = static_cast<const uint4*>(kind ? a.s_up : a.w_up);
       const uint4* const w[kRowsPerItem] = {wg + row0 * units, wg + (row0 + 1) * units, wu + row0 * units,
                                             wu + (row0 + 1) * units};
-      const uint4* x = static_cast<const uint4*>(kind ? a.x_shared : a.x_routed) + (int64_t)gd.a_row0 * (a.d / 8);
-      dot_rows<FMT, R>(w, x, a.d / 8, rows, (int)units, lane, acc);
+      // row r's token: its packed copy's source slot / K (routed), or r (shared)
+      int64_t tok = 0;
+      if (lane < rows) {
+        if (kind) {
+          tok = lane;
+        } else {
+          const int32_t src = __ldg(a.perm_src + gd.a_row0 + lane);
+          if (src >= 0 && (int64_t)src < a.T * a.K) tok = src / a.K;
+          else atomicOr(a.err, kErrBounds);
+        }
+      }
+      const int64_t row_bytes = (int64_t)a.d * (XS == kXHiddenF32 ? 4 : 2);
+      const void* xr[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        xr[r] = static_cast<const char*>(a.hidden) + __shfl_sync(0xFFFFFFFFu, tok, r) * row_bytes;
+      dot_rows<FMT, R, XS>(w, xr, rows, (int)units, lane, acc, over);
       float gs0 = 1.f, gs1 = 1.f, us0 = 1.f, us1 = 1.f;
       if (FMT == kSmallE4M3) {
         const float* sg = static_cast<const float*>(kind ? a.s_gate_scale : a.w_gate_scale);
@@ -244,8 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       const uint4* wd = static_cast<const uint4*>(kind ? a.s_down : a.w_down);
       const uint4* const w[kRowsPerItem] = {wd + row0 * units, wd + (row0 + 1) * units, wd + (row0 + 2) * units,
                                             wd + (row0 + 3) * units};
-      const uint4* x = static_cast<const uint4*>(kind ? a.h_sh : a.h) + (int64_t)gd.h_row0 * (Fk / 8);
-      dot_rows<FMT, R>(w, x, Fk / 8, rows, (int)units, lane, acc);
+      const uint16_t* hb = static_cast<const uint16_t*>(kind ? a.h_sh : a.h);
+      const void* xr[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) xr[r] = hb + (int64_t)(gd.h_row0 + r) * Fk;
+      dot_rows<FMT, R, kXAct16>(w, xr, rows, (int)units, lane, acc, over);
       const int q = lane & (kRowsPerItem - 1), rl = lane / kRowsPerItem;
       if (rl < rows) {
         float y = 0.f;
@@ -271,14 +344,49 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
     }
   }
   if (over) atomicOr(a.err, kErrRange);
+  if (PHASE == 1) {
+    // the last CTA to finish rounds the accumulator to the bf16 output
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const int64_t nvec = a.T * a.d / 8;
+      const float4* acc4 = reinterpret_cast<const float4*>(a.out_acc);
+      for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
+        const float4 p = __ldcg(acc4 + 2 * v), q = __ldcg(acc4 + 2 * v + 1);
+        reinterpret_cast<uint4*>(a.out)[v] =
+            make_uint4(pack_bf16x2(p.x, p.y), pack_bf16x2(p.z, p.w), pack_bf16x2(q.x, q.y), pack_bf16x2(q.z, q.w));
+      }
+    }
+  }
+}
+
+// These grids are launched without programmatic stream serialisation (their
+// griddepcontrol.wait is then a no-op): measured, letting them start early
+// behind the previous kernel made a 2-token layer 13 % and a 4-token layer
+// 14 % slower, with every stage's own time unchanged.
+cudaError_t launch_serial(void (*kern)(const SmallBatchArgs), unsigned grid, cudaStream_t s,
+                          const SmallBatchArgs& a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <int FMT, int R>
 cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, cudaStream_t s) {
-  return phase == 0 ? launch(small_batch_ffn_kernel<FMT, R, 0>, grid, kThreads, 0, s, a)
-                    : launch(small_batch_ffn_kernel<FMT, R, 1>, grid, kThreads, 0, s, a);
+  if (phase == 1) return launch_serial(small_batch_ffn_kernel<FMT, R, 1, kXAct16>, grid, s, a);
+  return a.hidden_bf16 ? launch_serial(small_batch_ffn_kernel<FMT, R, 0, kXHiddenBf16>, grid, s, a)
+                       : launch_serial(small_batch_ffn_kernel<FMT, R, 0, kXHiddenF32>, grid, s, a);
 }
-
 
 }  // namespace
 

@@ -180,6 +180,23 @@ def test_fp8_activation_overflow_is_reported():
     assert layer.status(cfg.T) == 0
 
 
+def test_fp8_single_token_activation_overflow_is_reported():
+    """The same report on the one-token path, whose CUDA-core FFNs round the
+    token's hidden row to fp16 themselves (no staged copy)."""
+    cfg = MID["fp8_T1_shared_f32"]
+    ins, dev = H.make_case(cfg)
+    layer = B.MoELayer(cfg, dev)
+    assert B.layer_small_batch(B.problem(cfg))
+    dev["hidden"][0, 7] = 1.0e6
+    layer.forward(dev["hidden"])
+    torch.cuda.synchronize()
+    assert layer.status(cfg.T) == B.MOE_ERR_RANGE
+    dev["hidden"][0, 7] = 1.0
+    layer.forward(dev["hidden"])
+    torch.cuda.synchronize()
+    assert layer.status(cfg.T) == 0
+
+
 def test_fp8_expert_choice_matches_oracle():
     cfg = _cfg("fp8_ec", T=300, d=272, N=8, K=2, F=400, S=1, Fs=144, routing="expert")
     ins, dev = H.make_case(cfg)
