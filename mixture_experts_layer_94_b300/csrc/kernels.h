@@ -187,6 +187,8 @@ cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* 
 // the group's rows.
 enum SmallBatchFormat { kSmallBf16 = 0, kSmallE4M3 = 1 };
 constexpr int kSmallBatchMaxRows = 4;
+// The gate/up kernel stages the batch's T token rows as fp32 in shared memory.
+constexpr size_t kSmallBatchMaxSmem = 192u << 10;
 struct SmallBatchArgs {
   int32_t fmt;               // SmallBatchFormat of the expert weights
   int32_t max_rows;          // bound on any group's rows (1..kSmallBatchMaxRows)

@@ -8,22 +8,25 @@
 // HBM-bound, with nothing for the tensor cores to gain. Here a warp takes four
 // weight rows of one expert (gate rows f, f+1 and up rows f, f+1; or W_down
 // rows j..j+3), streams them from HBM once in 16-byte units, and dots them with
-// the expert's activation rows, which stay in L1/L2. One 512-thread CTA per SM
-// walks all (expert, row block) items, so every SM streams weights.
+// the expert's activation rows. One 512-thread CTA per SM walks all (expert,
+// row block) items, so every SM streams weights.
 //
-// Two launches do the whole FFN part of the layer: the gate/up kernel reads
-// each packed row's token straight from hidden (no permuted copy), rounded as
-// the row gather would store it, and clears the fp32 accumulator; the down
-// kernel adds the gate-weighted rows into it, and its last CTA to finish
-// rounds it to the bf16 output (no separate finalise launch).
+// Two launches do the whole FFN part of the layer. The gate/up kernel stages
+// the batch's T token rows of hidden in shared memory as fp32, rounded once as
+// the activation format holds them (no permuted copy in global memory), and
+// clears the fp32 accumulator; the down kernel adds the gate-weighted rows
+// into it, and its last CTA to finish rounds it to the bf16 output (no
+// separate finalise launch).
 //
-// Formats: bf16 weights with bf16 activations (up to 4 rows per expert), or
-// FP8 E4M3 codes with fp32 row scales and fp16 activations (one row: widening
-// the codes to fp32 costs ALU time per row, so the tensor-core path wins from
-// two rows on). Products and sums are fp32; h is rounded once, to bf16 (fp16
-// for FP8 experts), as the grouped GEMMs store it.
+// Formats: bf16 weights with bf16 activations, or FP8 E4M3 codes with fp32 row
+// scales and fp16 activations. Products and sums are fp32; h is rounded once,
+// to bf16 (fp16 for FP8 experts), as the grouped GEMMs store it. E4M3 codes
+// are widened on the integer pipe: the code's sign, exponent and mantissa bits
+// are placed into an fp32 word, which is the code's value times 2^-120 (a
+// subnormal code becomes an fp32 subnormal); the activations are held times
+// 2^60, so the products stay normal, and 2^60 is restored with the row scale.
 
-#include <cuda_fp8.h>
+#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -37,6 +40,11 @@ constexpr int kRowsPerItem = 4;  // weight rows a warp streams together
 
 // Elements in one 16-byte unit of weight codes.
 __host__ __device__ constexpr int unit_elems(int fmt) { return fmt == kSmallBf16 ? 8 : 16; }
+
+// Activations of FP8 experts are held times 2^60 and E4M3 codes decode to
+// their value times 2^-120 (see above): a dot product is 2^-60 times its value.
+constexpr float kE4M3ActScale = 1152921504606846976.0f;  // 2^60
+constexpr float kE4M3DotScale = 1152921504606846976.0f;  // 2^60
 
 // 16 bytes of weight codes, read once: no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -70,14 +78,15 @@ __device__ __forceinline__ void act8(const uint4 v, float (&f)[8]) {
   }
 }
 
-// Two E4M3 codes (low 16 bits of c; the lower byte is the earlier element).
-__device__ __forceinline__ float2 e4m3x2_f32(uint32_t c) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c & 0xFFFFu), __NV_E4M3);
-  return half2_bits_to_f32((uint32_t)h.x | ((uint32_t)h.y << 16));
+// E4M3 code k (byte k of w) as fp32 bits: s eeee mmm -> sign at bit 31, eeee
+// at bits 23..26, mmm at bits 20..22; the code's value times 2^-120.
+__device__ __forceinline__ float e4m3_scaled(uint32_t w, int k) {
+  const uint32_t x = __byte_perm(w, 0u, 0x0444u | ((uint32_t)k << 12));  // code in the top byte
+  return __uint_as_float(((x >> 4) & 0x07F00000u) | (x & 0x80000000u));
 }
 
-// Elements 8s .. 8s+7 of a 16-byte unit of weight codes, as fp32 code values
-// (FP8 row scales are applied by the caller).
+// Elements 8s .. 8s+7 of a 16-byte unit of weight codes as fp32: bf16 values,
+// or E4M3 values times 2^-120 (FP8 row scales are applied by the caller).
 template <int FMT>
 __device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -89,23 +98,11 @@ __device__ __forceinline__ void w8(const uint4 u, int s, float (&f)[8]) {
     }
   } else {  // 16 E4M3 codes per unit: words 2s, 2s+1
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t c = w[2 * s + i];
-      const float2 a = e4m3x2_f32(c), b = e4m3x2_f32(c >> 16);
-      f[4 * i] = a.x;
-      f[4 * i + 1] = a.y;
-      f[4 * i + 2] = b.x;
-      f[4 * i + 3] = b.y;
-    }
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) f[4 * i + k] = e4m3_scaled(w[2 * s + i], k);
   }
 }
-
-// Where the dot products' activation rows come from.
-enum XSource {
-  kXAct16 = 0,      // rows in the activation format (h: bf16, or fp16 for FP8 experts)
-  kXHiddenBf16 = 1, // bf16 hidden rows
-  kXHiddenF32 = 2,  // fp32 hidden rows
-};
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
@@ -117,22 +114,32 @@ __device__ __forceinline__ float round_f16(float x, bool& over) {
   return __half2float(__float2half_rn(x));
 }
 
-// Elements 8v .. 8v+7 of an activation row as fp32, rounded as the layer's
-// activation format holds them: bf16 for bf16 experts, fp16 (F16) for FP8.
-template <int XS, bool F16>
-__device__ __forceinline__ void x8(const void* row, int64_t v, float (&f)[8], bool& over) {
-  if (XS == kXHiddenF32) {
+// Where the dot products' activation rows come from.
+enum XSource {
+  kXShared = 0,  // fp32 token rows staged in shared memory (gate/up)
+  kXAct16 = 1,   // rows in the activation format in global memory (h: bf16, or fp16 for FP8 experts)
+};
+
+// Elements 8v .. 8v+7 of activation row `row` as fp32 (times 2^60 for FP8
+// experts; the staged rows already carry the factor).
+template <int XS, int FMT>
+__device__ __forceinline__ void x8(const void* row, int64_t v, float (&f)[8]) {
+  if (XS == kXShared) {
     const float4* p = static_cast<const float4*>(row) + 2 * v;
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = F16 ? round_f16(t[i], over) : round_bf16(t[i]);
+    const float4 a = p[0], b = p[1];
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = a.z;
+    f[3] = a.w;
+    f[4] = b.x;
+    f[5] = b.y;
+    f[6] = b.z;
+    f[7] = b.w;
   } else {
-    const uint4 u = __ldg(static_cast<const uint4*>(row) + v);
-    act8<XS == kXAct16 && F16>(u, f);
-    if (XS == kXHiddenBf16 && F16) {
+    act8<FMT != kSmallBf16>(__ldg(static_cast<const uint4*>(row) + v), f);
+    if (FMT == kSmallE4M3) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = round_f16(f[i], over);
+      for (int i = 0; i < 8; ++i) f[i] *= kE4M3ActScale;
     }
   }
 }
@@ -142,11 +149,9 @@ __device__ __forceinline__ void x8(const void* row, int64_t v, float (&f)[8], bo
 // Activation row r starts at xr[r]; rows >= `rows` are skipped.
 template <int FMT, int R, int XS>
 __device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], const void* const (&xr)[R],
-                                         int rows, int units, int lane, float (&acc)[kRowsPerItem][R],
-                                         bool& over) {
+                                         int rows, int units, int lane, float (&acc)[kRowsPerItem][R]) {
   constexpr int E = unit_elems(FMT), SUB = E / 8;
   constexpr int U = R == 1 ? 4 : 2;  // units per row in flight per lane
-  constexpr bool kF16 = FMT != kSmallBf16;
   for (int j0 = lane; j0 < units; j0 += 32 * U) {
     uint4 wv[kRowsPerItem][U];
 #pragma unroll
@@ -164,7 +169,7 @@ __device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], 
           float xf[R][8];
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            if (r < rows) x8<XS, kF16>(xr[r], (int64_t)j * SUB + s, xf[r], over);
+            if (r < rows) x8<XS, FMT>(xr[r], (int64_t)j * SUB + s, xf[r]);
           }
 #pragma unroll
           for (int q = 0; q < kRowsPerItem; ++q) {
@@ -193,29 +198,58 @@ __device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], 
 // 16-byte units of codes in one weight row of `k` elements.
 __device__ __forceinline__ int64_t row_units(int k, int fmt) { return k / unit_elems(fmt); }
 
-// PHASE 0: h[row r][f, f+1] = SiLU(g) * u for the item's gate rows f, f+1 and
-// up rows f, f+1, with the rows' tokens read from hidden (source XS); also
-// clears out_acc and the down kernel's completion count. PHASE 1 (XS =
-// kXAct16): out_acc[token of r][j..j+3] += w_r * y for W_down rows j..j+3; the
-// last CTA to finish writes out = bf16(out_acc). Items: every routed expert
-// holding rows (F/2 or d/4 items each), then every shared expert (Fs/2 or d/4
-// items each); item i goes to warp i / gridDim.x of CTA i % gridDim.x, so a
-// partial last round still spreads over every SM.
-template <int FMT, int R, int PHASE, int XS>
+// PHASE 0: stage the T token rows of hidden (bf16 when HB, else fp32) in
+// shared memory, rounded to the activation format (bf16, or fp16 for FP8
+// experts); clear out_acc and the down kernel's completion count; then
+// h[row r][f, f+1] = SiLU(g) * u for the item's gate rows f, f+1 and up rows
+// f, f+1. PHASE 1: out_acc[token of r][j..j+3] += w_r * y for W_down rows
+// j..j+3; the last CTA to finish writes out = bf16(out_acc). Items: every
+// routed expert holding rows (F/2 or d/4 items each), then every shared expert
+// (Fs/2 or d/4 items each); item i goes to warp i / gridDim.x of CTA
+// i % gridDim.x, so a partial last round still spreads over every SM.
+template <int FMT, int R, int PHASE, bool HB>
 __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const SmallBatchArgs a) {
   pdl_trigger();
   pdl_wait();
+  extern __shared__ float4 s_rows4[];  // PHASE 0: [T][d] fp32
   __shared__ int32_t s_list[kMaxExperts];
   __shared__ int32_t s_count[kWarps];
   __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
+  constexpr bool kF16 = FMT != kSmallBf16;
+  bool over = false;
+  const float* s_rows = reinterpret_cast<const float*>(s_rows4);
   if (PHASE == 0) {
     const int64_t nacc = a.T * a.d / 4;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nacc; i += (int64_t)gridDim.x * kThreads)
       reinterpret_cast<float4*>(a.out_acc)[i] = zero;
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.done = 0u;
+    // the token rows, 8 elements per step, as the row gather would store them
+    const int nvec = (int)(a.T * (a.d / 8));
+    for (int i = threadIdx.x; i < nvec; i += kThreads) {
+      float f[8];
+      if (HB) {
+        act8<false>(__ldg(static_cast<const uint4*>(a.hidden) + i), f);
+        if (kF16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = round_f16(f[k], over);
+        }
+      } else {
+        const float4* p = static_cast<const float4*>(a.hidden) + 2 * (int64_t)i;
+        const float4 u = __ldg(p), v = __ldg(p + 1);
+        const float t[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = kF16 ? round_f16(t[k], over) : round_bf16(t[k]);
+      }
+      if (kF16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] *= kE4M3ActScale;
+      }
+      s_rows4[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+      s_rows4[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
   }
   // the routed experts that hold rows, in expert order (N <= 256 < kThreads)
   const bool has = (int)threadIdx.x < N && a.groups[threadIdx.x].rows > 0;
@@ -232,12 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
   if (has) s_list[base + __popc(ball & ((1u << lane) - 1u))] = (int32_t)threadIdx.x;
   __syncthreads();
 
-  constexpr bool kF16 = FMT != kSmallBf16;
   const int per_r = PHASE == 0 ? a.F / 2 : a.d / kRowsPerItem;
   const int per_s = PHASE == 0 ? a.Fs / 2 : a.d / kRowsPerItem;
   const int64_t n_r = (int64_t)nr * per_r;
   const int64_t total = n_r + (a.S > 0 ? (int64_t)a.S * per_s : 0);
-  bool over = false;
   for (int64_t item = (int64_t)warp * gridDim.x + blockIdx.x; item < total; item += (int64_t)gridDim.x * kWarps) {
     int g, blk;
     if (item < n_r) {
@@ -272,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       const uint4* const w[kRowsPerItem] = {wg + row0 * units, wg + (row0 + 1) * units, wu + row0 * units,
                                             wu + (row0 + 1) * units};
       // row r's token: its packed copy's source slot / K (routed), or r (shared)
-      int64_t tok = 0;
+      int tok = 0;
       if (lane < rows) {
         if (kind) {
           tok = lane;
@@ -282,20 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
           else atomicOr(a.err, kErrBounds);
         }
       }
-      const int64_t row_bytes = (int64_t)a.d * (XS == kXHiddenF32 ? 4 : 2);
       const void* xr[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-        xr[r] = static_cast<const char*>(a.hidden) + __shfl_sync(0xFFFFFFFFu, tok, r) * row_bytes;
-      dot_rows<FMT, R, XS>(w, xr, rows, (int)units, lane, acc, over);
+      for (int r = 0; r < R; ++r) xr[r] = s_rows + (int64_t)__shfl_sync(0xFFFFFFFFu, tok, r) * a.d;
+      dot_rows<FMT, R, kXShared>(w, xr, rows, (int)units, lane, acc);
       float gs0 = 1.f, gs1 = 1.f, us0 = 1.f, us1 = 1.f;
       if (FMT == kSmallE4M3) {
         const float* sg = static_cast<const float*>(kind ? a.s_gate_scale : a.w_gate_scale);
         const float* su = static_cast<const float*>(kind ? a.s_up_scale : a.w_up_scale);
-        gs0 = __ldg(sg + row0);
-        gs1 = __ldg(sg + row0 + 1);
-        us0 = __ldg(su + row0);
-        us1 = __ldg(su + row0 + 1);
+        gs0 = __ldg(sg + row0) * kE4M3DotScale;
+        gs1 = __ldg(sg + row0 + 1) * kE4M3DotScale;
+        us0 = __ldg(su + row0) * kE4M3DotScale;
+        us1 = __ldg(su + row0 + 1) * kE4M3DotScale;
       }
       uint32_t* h = static_cast<uint32_t*>(kind ? a.h_sh : a.h);
 #pragma unroll
@@ -318,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       const void* xr[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) xr[r] = hb + (int64_t)(gd.h_row0 + r) * Fk;
-      dot_rows<FMT, R, kXAct16>(w, xr, rows, (int)units, lane, acc, over);
+      dot_rows<FMT, R, kXAct16>(w, xr, rows, (int)units, lane, acc);
       const int q = lane & (kRowsPerItem - 1), rl = lane / kRowsPerItem;
       if (rl < rows) {
         float y = 0.f;
@@ -328,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
           for (int qq = 0; qq < kRowsPerItem; ++qq)
             if (r == rl && qq == q) y = acc[qq][r];
         if (FMT == kSmallE4M3)
-          y *= __ldg(static_cast<const float*>(kind ? a.s_down_scale : a.w_down_scale) + row0 + q);
+          y *= __ldg(static_cast<const float*>(kind ? a.s_down_scale : a.w_down_scale) + row0 + q) * kE4M3DotScale;
         int64_t t = rl;
         float wt = 1.f;
         bool ok = true;
@@ -368,13 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
 // These grids are launched without programmatic stream serialisation (their
 // griddepcontrol.wait is then a no-op): measured, letting them start early
 // behind the previous kernel made a 2-token layer 13 % and a 4-token layer
-// 14 % slower, with every stage's own time unchanged.
-cudaError_t launch_serial(void (*kern)(const SmallBatchArgs), unsigned grid, cudaStream_t s,
-                          const SmallBatchArgs& a) {
+// 14 % slower, with every stage's own time unchanged. The gate/up grid's
+// dynamic shared memory (the token rows) may exceed the default 48 KB; its
+// limit is raised once per kernel and device.
+template <int FMT, int R, int PHASE, bool HB>
+cudaError_t launch_k(const SmallBatchArgs& a, unsigned grid, size_t smem, cudaStream_t s) {
+  void (*kern)(const SmallBatchArgs) = small_batch_ffn_kernel<FMT, R, PHASE, HB>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (PHASE == 0 && !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallBatchMaxSmem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
@@ -383,9 +426,9 @@ cudaError_t launch_serial(void (*kern)(const SmallBatchArgs), unsigned grid, cud
 
 template <int FMT, int R>
 cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, cudaStream_t s) {
-  if (phase == 1) return launch_serial(small_batch_ffn_kernel<FMT, R, 1, kXAct16>, grid, s, a);
-  return a.hidden_bf16 ? launch_serial(small_batch_ffn_kernel<FMT, R, 0, kXHiddenBf16>, grid, s, a)
-                       : launch_serial(small_batch_ffn_kernel<FMT, R, 0, kXHiddenF32>, grid, s, a);
+  if (phase == 1) return launch_k<FMT, R, 1, true>(a, grid, 0, s);
+  const size_t smem = (size_t)a.T * a.d * 4;
+  return a.hidden_bf16 ? launch_k<FMT, R, 0, true>(a, grid, smem, s) : launch_k<FMT, R, 0, false>(a, grid, smem, s);
 }
 
 }  // namespace
@@ -393,6 +436,7 @@ cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, cudaStr
 cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStream_t s) {
   if (a.max_rows < 1 || a.max_rows > kSmallBatchMaxRows || a.N > kMaxExperts) return cudaErrorInvalidValue;
   if (a.fmt == kSmallE4M3 ? a.max_rows != 1 : a.fmt != kSmallBf16) return cudaErrorInvalidValue;
+  if (a.T < 1 || a.T > a.max_rows || (size_t)a.T * a.d * 4 > kSmallBatchMaxSmem) return cudaErrorInvalidValue;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // items: at most min(N, rows) routed experts hold rows
