@@ -363,7 +363,9 @@ def _sample_rows(T, n, seed=0):
 
 FULL = [("mixtral", inputs.MIXTRAL, 12), ("gptoss", inputs.GPTOSS, 12), ("dsv3", inputs.DSV3, 6),
         ("dsv3_grouped", inputs.DSV3_GROUPED, 6), ("mixtral_capacity", inputs.MIXTRAL_CAPACITY, 12)] + [
-    (f"qwen_decode_T{T}", inputs.QWEN_DECODE.with_(T=T), 6) for T in inputs.DECODE_BATCHES]
+    (f"qwen_decode_T{T}", inputs.QWEN_DECODE.with_(T=T), 6) for T in inputs.DECODE_BATCHES] + [
+    # the largest batches of the CUDA-core expert path (2 and 4 rows per expert)
+    (f"qwen_decode_T{T}_cuda_cores", inputs.QWEN_DECODE.with_(T=T), 4) for T in (2, 4)]
 
 
 @pytest.mark.parametrize("name,cfg,n_sample", FULL, ids=[f[0] for f in FULL])
