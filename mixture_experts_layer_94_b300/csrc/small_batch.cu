@@ -24,16 +24,10 @@
 // scales and fp16 activations. Products and sums are fp32; h is rounded once,
 // to bf16 (fp16 for FP8 experts), as the grouped GEMMs store it.
 //
-// Several consumer warps share a stage, each taking a different use of it, so
-// a consumer must not test the stage's barrier for use n before use n - 1 has
-// completed (a parity wait cannot tell phase n from phase n - 2). The copy
-// warp publishes how many uses of each stage it has issued; it issues use n
-// only after use n - 1 was released, so once a consumer sees use n issued,
-// the barrier is in use n's phase and the parity wait is exact.
-//
-// Every wait is bounded (kWaitTimeoutNs); a wait that gives up records
-// kErrTimeout, raises the CTA's abort flag so the other waits return, and the
-// copy warp waits (bounded) for its copies in flight before the CTA exits.
+// Every mbarrier wait is bounded (kWaitTimeoutNs); a wait that gives up
+// records kErrTimeout, raises the CTA's abort flag so the other waits return,
+// and the copy warp waits (bounded) for its copies in flight before the CTA
+// exits.
 
 #include <cuda_fp8.h>
 
@@ -197,32 +191,6 @@ __device__ __forceinline__ void dot_stage(const uint8_t* stage, int srow, const 
       for (int off = 16; off > 0; off >>= 1) acc[q][r] += __shfl_xor_sync(0xFFFFFFFFu, acc[q][r], off);
 }
 
-// Bounded wait until the copy warp has issued use n of a stage (count > n);
-// false on abort or timeout (which records kErrTimeout and raises the abort
-// flag).
-__device__ __forceinline__ bool issued_wait(volatile uint32_t* count, uint32_t n, volatile int* abort_flag,
-                                            uint32_t* err_word) {
-  if (*count > n) {
-    __threadfence_block();
-    return true;
-  }
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (*count > n) {
-      __threadfence_block();
-      return true;
-    }
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        atomicOr(err_word, kErrTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
 // Item `item` of a phase: its group (a routed expert from the list of those
 // holding rows, then the shared experts) and its row block within the group.
 struct ItemRef {
@@ -273,7 +241,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
   __shared__ int32_t s_list[kMaxExperts];
   __shared__ int32_t s_count[kWarps];
   __shared__ __align__(8) uint64_t s_full[kMaxStages], s_empty[kMaxStages];
-  __shared__ volatile uint32_t s_issued[kMaxStages];  // uses of each stage whose copies were issued
   __shared__ int s_abort;
   __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -289,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_u32(&s_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&s_empty[s]), 1);
-      s_issued[s] = 0u;
     }
     ptx::fence_mbarrier_init();
   }
@@ -375,8 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
         const uint32_t dst = ptx::smem_u32(s_stage + (size_t)s * kRowsPerItem * srow);
 #pragma unroll
         for (int q = 0; q < kRowsPerItem; ++q) ptx::bulk_load(dst + (uint32_t)q * srow, src[q], bytes, bar);
-        __threadfence_block();
-        s_issued[s] = n + 1;
         issued = k + 1;
       }
       // the copies still in flight land before the CTA may exit (the normal
@@ -390,8 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
       if (item >= total) break;
       const int s = k % S;
       const uint32_t n = (uint32_t)(k / S);
-      bool ok = issued_wait(&s_issued[s], n, &s_abort, a.err);
-      ok = ok && ptx::mbar_wait(ptx::smem_u32(&s_full[s]), n & 1u, &s_abort, a.err);
+      const bool ok = ptx::mbar_wait(ptx::smem_u32(&s_full[s]), n & 1u, &s_abort, a.err);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       const ItemRef ir = item_ref(item, n_r, per_r, per_s, N, s_list);
       const GroupDesc gd = a.groups[ir.g];
