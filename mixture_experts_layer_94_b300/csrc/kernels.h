@@ -187,9 +187,8 @@ cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* 
 // the group's rows.
 enum SmallBatchFormat { kSmallBf16 = 0, kSmallE4M3 = 1 };
 constexpr int kSmallBatchMaxRows = 4;
-// Dynamic shared memory of the small-batch kernels: the gate/up kernel's T
-// token rows (fp32) and a ring of weight-row stages.
-constexpr size_t kSmallBatchMaxSmem = 224u << 10;
+// The gate/up kernel stages the batch's T token rows as fp32 in shared memory.
+constexpr size_t kSmallBatchMaxSmem = 192u << 10;
 struct SmallBatchArgs {
   int32_t fmt;               // SmallBatchFormat of the expert weights
   int32_t max_rows;          // bound on any group's rows (1..kSmallBatchMaxRows)
@@ -220,11 +219,7 @@ struct SmallBatchArgs {
   const int32_t* perm_src;   // [rows] packed row -> t*K + k
   const float* topk_w;       // [T*K]
   uint32_t* err;
-  int32_t stages, stage_row_bytes;  // shared-memory ring, set by launch_small_batch_ffn
 };
-// Whether a problem's shapes leave room for at least two weight-row stages
-// in each phase (the admission test of the small-batch path).
-bool small_batch_fits(int fmt, int64_t T, int32_t d, int32_t F, int32_t Fs, int32_t S);
 // phase 0: h = SiLU(x W_gate^T) * (x W_up^T) with x each packed row's token
 // row of hidden, rounded to the activation format; out_acc = 0.
 // phase 1: out_acc[t] += w * h W_down^T, then out = bf16(out_acc).

@@ -99,12 +99,9 @@ bool needs_act_copy(const moe_problem_t& p) {
 // MXFP4 codes never (the tensor-core path is faster even for one token).
 int32_t small_batch_rows(const moe_problem_t& p) {
   if (p.routing != MOE_ROUTING_TOKEN_CHOICE || p.T < 1 || stored_combine(p) || is_mx(p)) return 0;
+  if ((size_t)p.T * p.d_model * 4 > kSmallBatchMaxSmem) return 0;  // token rows staged in shared memory
   const int64_t max_t = is_fp8(p) ? 1 : kSmallBatchMaxRows;
-  if (p.T > max_t) return 0;
-  // the token rows and at least two stages of weight rows fit in shared memory
-  if (!small_batch_fits(is_fp8(p) ? kSmallE4M3 : kSmallBf16, p.T, p.d_model, p.ffn, p.shared_ffn, p.n_shared))
-    return 0;
-  return (int32_t)p.T;
+  return p.T <= max_t ? (int32_t)p.T : 0;
 }
 
 Layout make_layout(const moe_problem_t& p, int call) {

@@ -5,13 +5,11 @@
 // GEMM tile (128 activation rows) is almost all padding and its 256 weight
 // rows per tile leave most SMs idle (8 touched experts x 12 tiles at T = 1).
 // The work is a stream of weight rows, each used by at most T activation rows:
-// HBM-bound, with nothing for the tensor cores to gain. An item is four weight
-// rows of one expert (gate rows f, f+1 and up rows f, f+1; or W_down rows
-// j..j+3). One 512-thread CTA per SM walks its share of the items: warp 0
-// streams each item's rows from HBM into a ring of shared-memory stages with
-// 1-D bulk copies (the bytes in flight then hold no registers), and the other
-// 15 warps take one item each, dot its rows with the expert's activation rows
-// and write the results.
+// HBM-bound, with nothing for the tensor cores to gain. Here a warp takes four
+// weight rows of one expert (gate rows f, f+1 and up rows f, f+1; or W_down
+// rows j..j+3), streams them from HBM once in 16-byte units, and dots them with
+// the expert's activation rows. One 512-thread CTA per SM walks all (expert,
+// row block) items, so every SM streams weights.
 //
 // Two launches do the whole FFN part of the layer. The gate/up kernel stages
 // the batch's T token rows of hidden in shared memory as fp32, rounded once as
@@ -23,11 +21,6 @@
 // Formats: bf16 weights with bf16 activations, or FP8 E4M3 codes with fp32 row
 // scales and fp16 activations. Products and sums are fp32; h is rounded once,
 // to bf16 (fp16 for FP8 experts), as the grouped GEMMs store it.
-//
-// Every mbarrier wait is bounded (kWaitTimeoutNs); a wait that gives up
-// records kErrTimeout, raises the CTA's abort flag so the other waits return,
-// and the copy warp waits (bounded) for its copies in flight before the CTA
-// exits.
 
 #include <cuda_fp8.h>
 
@@ -35,24 +28,25 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "ptx.cuh"
-#include "tile_sched.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kConsumers = kWarps - 1;  // warp 0 issues the copies
-constexpr int kRowsPerItem = 4;         // weight rows of one item
-constexpr int kMaxStages = 32;
+constexpr int kRowsPerItem = 4;  // weight rows a warp streams together
 
 // Elements in one 16-byte unit of weight codes.
 __host__ __device__ constexpr int unit_elems(int fmt) { return fmt == kSmallBf16 ? 8 : 16; }
-// Bytes per weight element.
-__host__ __device__ constexpr int elem_bytes(int fmt) { return fmt == kSmallBf16 ? 2 : 1; }
 
-__host__ __device__ constexpr size_t align128(size_t x) { return (x + 127) & ~(size_t)127; }
+// 16 bytes of weight codes, read once: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ float2 half2_bits_to_f32(uint32_t bits) {
   __half2 h;
@@ -144,40 +138,44 @@ __device__ __forceinline__ void x8(const void* row, int64_t v, float (&f)[8]) {
   }
 }
 
-// acc[q][r] = (weight row q of the stage) . (activation row r), summed over
-// the warp. Row q of the stage starts at stage + q * srow; `units` 16-byte
-// units of codes per row (unit j covers elements j*E .. j*E+E-1); activation
-// row r starts at xr[r]; rows >= `rows` are skipped.
+// acc[q][r] += (weight row q) . (activation row r) over `units` 16-byte units
+// of codes (unit j covers elements j*E .. j*E+E-1), then summed over the warp.
+// Activation row r starts at xr[r]; rows >= `rows` are skipped.
 template <int FMT, int R, int XS>
-__device__ __forceinline__ void dot_stage(const uint8_t* stage, int srow, const void* const (&xr)[R], int rows,
-                                          int units, int lane, float (&acc)[kRowsPerItem][R]) {
-  constexpr int SUB = unit_elems(FMT) / 8;
+__device__ __forceinline__ void dot_rows(const uint4* const (&w)[kRowsPerItem], const void* const (&xr)[R],
+                                         int rows, int units, int lane, float (&acc)[kRowsPerItem][R]) {
+  constexpr int E = unit_elems(FMT), SUB = E / 8;
+  constexpr int U = R == 1 ? 4 : 2;  // units per row in flight per lane
+  for (int j0 = lane; j0 < units; j0 += 32 * U) {
+    uint4 wv[kRowsPerItem][U];
 #pragma unroll
-  for (int q = 0; q < kRowsPerItem; ++q)
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u;
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[q][r] = 0.f;
-#pragma unroll 2
-  for (int j = lane; j < units; j += 32) {
-    uint4 wv[kRowsPerItem];
+      for (int q = 0; q < kRowsPerItem; ++q) wv[q][u] = j < units ? ld_stream(w[q] + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-    for (int q = 0; q < kRowsPerItem; ++q)
-      wv[q] = *reinterpret_cast<const uint4*>(stage + (size_t)q * srow + (size_t)j * 16);
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + 32 * u;
+      if (j < units) {
 #pragma unroll
-    for (int s = 0; s < SUB; ++s) {
-      float xf[R][8];
+        for (int s = 0; s < SUB; ++s) {
+          float xf[R][8];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (r < rows) x8<XS, FMT>(xr[r], (int64_t)j * SUB + s, xf[r]);
-      }
+          for (int r = 0; r < R; ++r) {
+            if (r < rows) x8<XS, FMT>(xr[r], (int64_t)j * SUB + s, xf[r]);
+          }
 #pragma unroll
-      for (int q = 0; q < kRowsPerItem; ++q) {
-        float wf[8];
-        w8<FMT>(wv[q], s, wf);
+          for (int q = 0; q < kRowsPerItem; ++q) {
+            float wf[8];
+            w8<FMT>(wv[q][u], s, wf);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (r < rows) {
+            for (int r = 0; r < R; ++r) {
+              if (r < rows) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[q][r] = fmaf(wf[i], xf[r][i], acc[q][r]);
+                for (int i = 0; i < 8; ++i) acc[q][r] = fmaf(wf[i], xf[r][i], acc[q][r]);
+              }
+            }
           }
         }
       }
@@ -191,38 +189,8 @@ __device__ __forceinline__ void dot_stage(const uint8_t* stage, int srow, const 
       for (int off = 16; off > 0; off >>= 1) acc[q][r] += __shfl_xor_sync(0xFFFFFFFFu, acc[q][r], off);
 }
 
-// Item `item` of a phase: its group (a routed expert from the list of those
-// holding rows, then the shared experts) and its row block within the group.
-struct ItemRef {
-  int g, blk;
-};
-__device__ __forceinline__ ItemRef item_ref(int64_t item, int64_t n_r, int per_r, int per_s, int N,
-                                            const int32_t* s_list) {
-  ItemRef ir;
-  if (item < n_r) {
-    ir.g = s_list[item / per_r];
-    ir.blk = (int)(item % per_r);
-  } else {
-    const int64_t i2 = item - n_r;
-    ir.g = N + (int)(i2 / per_s);
-    ir.blk = (int)(i2 % per_s);
-  }
-  return ir;
-}
-
-// First weight row of an item in its stacked matrix (gate / up rows f0, f0+1
-// for phase 0, W_down rows j0..j0+3 for phase 1), and the row length.
-template <int PHASE>
-__device__ __forceinline__ int64_t item_row0(const SmallBatchArgs& a, int g, int blk, int* klen) {
-  const int kind = g < a.N ? 0 : 1, e = kind ? g - a.N : g;
-  const int Fk = kind ? a.Fs : a.F;
-  if (PHASE == 0) {
-    *klen = a.d;
-    return (int64_t)e * Fk + 2 * blk;
-  }
-  *klen = Fk;
-  return (int64_t)e * a.d + kRowsPerItem * blk;
-}
+// 16-byte units of codes in one weight row of `k` elements.
+__device__ __forceinline__ int64_t row_units(int k, int fmt) { return k / unit_elems(fmt); }
 
 // PHASE 0: stage the T token rows of hidden (bf16 when HB, else fp32) in
 // shared memory, rounded to the activation format (bf16, or fp16 for FP8
@@ -231,34 +199,21 @@ __device__ __forceinline__ int64_t item_row0(const SmallBatchArgs& a, int g, int
 // f, f+1. PHASE 1: out_acc[token of r][j..j+3] += w_r * y for W_down rows
 // j..j+3; the last CTA to finish writes out = bf16(out_acc). Items: every
 // routed expert holding rows (F/2 or d/4 items each), then every shared expert
-// (Fs/2 or d/4 items each); CTA b takes items b, b + grid, b + 2 grid, ... in
-// order, its k-th in stage k % stages, handled by consumer warp 1 + k % 15.
+// (Fs/2 or d/4 items each); item i goes to warp i / gridDim.x of CTA
+// i % gridDim.x, so a partial last round still spreads over every SM.
 template <int FMT, int R, int PHASE, bool HB>
 __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const SmallBatchArgs a) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ __align__(128) uint8_t s_dyn[];  // [x rows (phase 0)][stages]
+  extern __shared__ float4 s_rows4[];  // PHASE 0: [T][d] fp32
   __shared__ int32_t s_list[kMaxExperts];
   __shared__ int32_t s_count[kWarps];
-  __shared__ __align__(8) uint64_t s_full[kMaxStages], s_empty[kMaxStages];
-  __shared__ int s_abort;
   __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.N, S = a.stages;
+  const int N = a.N;
   constexpr bool kF16 = FMT != kSmallBf16;
   bool over = false;
-  const size_t x_bytes = PHASE == 0 ? align128((size_t)a.T * a.d * 4) : 0;
-  float4* s_rows4 = reinterpret_cast<float4*>(s_dyn);
-  const float* s_rows = reinterpret_cast<const float*>(s_dyn);
-  uint8_t* s_stage = s_dyn + x_bytes;
-  if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&s_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&s_empty[s]), 1);
-    }
-    ptx::fence_mbarrier_init();
-  }
+  const float* s_rows = reinterpret_cast<const float*>(s_rows4);
   if (PHASE == 0) {
     const int64_t nacc = a.T * a.d / 4;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -305,147 +260,113 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
   const int per_s = PHASE == 0 ? a.Fs / 2 : a.d / kRowsPerItem;
   const int64_t n_r = (int64_t)nr * per_r;
   const int64_t total = n_r + (a.S > 0 ? (int64_t)a.S * per_s : 0);
-  const int srow = a.stage_row_bytes;
-  constexpr int EB = elem_bytes(FMT);
-
-  if (warp == 0) {
-    // copies: item k of this CTA into stage k % S once its previous use is released
-    if (lane == 0) {
-      int issued = 0;
-      for (int k = 0;; ++k) {
-        const int64_t item = blockIdx.x + (int64_t)k * gridDim.x;
-        if (item >= total) break;
-        const int s = k % S;
-        const uint32_t n = (uint32_t)(k / S);
-        if (k >= S && !ptx::mbar_wait(ptx::smem_u32(&s_empty[s]), (n - 1) & 1u, &s_abort, a.err)) break;
-        const ItemRef ir = item_ref(item, n_r, per_r, per_s, N, s_list);
-        int klen = 0;
-        const int64_t row0 = item_row0<PHASE>(a, ir.g, ir.blk, &klen);
-        const uint32_t bytes = (uint32_t)klen * EB;
-        const int kind = ir.g < N ? 0 : 1;
-        const uint8_t* src[kRowsPerItem];
-        if (PHASE == 0) {
-          const uint8_t* wg = static_cast<const uint8_t*>(kind ? a.s_gate : a.w_gate);
-          const uint8_t* wu = static_cast<const uint8_t*>(kind ? a.s_up : a.w_up);
-          src[0] = wg + row0 * bytes;
-          src[1] = wg + (row0 + 1) * bytes;
-          src[2] = wu + row0 * bytes;
-          src[3] = wu + (row0 + 1) * bytes;
-        } else {
-          const uint8_t* wd = static_cast<const uint8_t*>(kind ? a.s_down : a.w_down);
-#pragma unroll
-          for (int q = 0; q < kRowsPerItem; ++q) src[q] = wd + (row0 + q) * bytes;
-        }
-        const uint32_t bar = ptx::smem_u32(&s_full[s]);
-        ptx::mbar_arrive_expect_tx(bar, kRowsPerItem * bytes);
-        const uint32_t dst = ptx::smem_u32(s_stage + (size_t)s * kRowsPerItem * srow);
-#pragma unroll
-        for (int q = 0; q < kRowsPerItem; ++q) ptx::bulk_load(dst + (uint32_t)q * srow, src[q], bytes, bar);
-        issued = k + 1;
-      }
-      // the copies still in flight land before the CTA may exit (the normal
-      // path has consumed them all; after an abort, wait a bounded time)
-      for (int k = issued > S ? issued - S : 0; k < issued; ++k)
-        wait_raw(ptx::smem_u32(&s_full[k % S]), (uint32_t)(k / S) & 1u, kWaitTimeoutNs);
+  for (int64_t item = (int64_t)warp * gridDim.x + blockIdx.x; item < total; item += (int64_t)gridDim.x * kWarps) {
+    int g, blk;
+    if (item < n_r) {
+      g = s_list[item / per_r];
+      blk = (int)(item % per_r);
+    } else {
+      const int64_t i2 = item - n_r;
+      g = N + (int)(i2 / per_s);
+      blk = (int)(i2 % per_s);
     }
-  } else {
-    for (int k = warp - 1;; k += kConsumers) {
-      const int64_t item = blockIdx.x + (int64_t)k * gridDim.x;
-      if (item >= total) break;
-      const int s = k % S;
-      const uint32_t n = (uint32_t)(k / S);
-      const bool ok = ptx::mbar_wait(ptx::smem_u32(&s_full[s]), n & 1u, &s_abort, a.err);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      const ItemRef ir = item_ref(item, n_r, per_r, per_s, N, s_list);
-      const GroupDesc gd = a.groups[ir.g];
-      const int kind = ir.g < N ? 0 : 1;
-      int rows = gd.rows;
-      if (rows > R) {  // cannot happen for token choice with T <= R
-        if (lane == 0) atomicOr(a.err, kErrBounds);
-        rows = R;
+    const GroupDesc gd = a.groups[g];
+    const int kind = g < N ? 0 : 1;
+    const int e = kind ? g - N : g;
+    int rows = gd.rows;
+    if (rows > R) {  // cannot happen for token choice with T <= R
+      if (lane == 0) atomicOr(a.err, kErrBounds);
+      rows = R;
+    }
+    const int Fk = kind ? a.Fs : a.F;
+    float acc[kRowsPerItem][R];
+#pragma unroll
+    for (int q = 0; q < kRowsPerItem; ++q)
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[q][r] = 0.f;
+
+    if (PHASE == 0) {
+      const int f0 = 2 * blk;
+      const int64_t units = row_units(a.d, FMT);
+      const int64_t row0 = (int64_t)e * Fk + f0;  // gate / up row f0 of this expert
+      const uint4* wg = static_cast<const uint4*>(kind ? a.s_gate : a.w_gate);
+      const uint4* wu = static_cast<const uint4*>(kind ? a.s_up : a.w_up);
+      const uint4* const w[kRowsPerItem] = {wg + row0 * units, wg + (row0 + 1) * units, wu + row0 * units,
+                                            wu + (row0 + 1) * units};
+      // row r's token: its packed copy's source slot / K (routed), or r (shared)
+      int tok = 0;
+      if (lane < rows) {
+        if (kind) {
+          tok = lane;
+        } else {
+          const int32_t src = __ldg(a.perm_src + gd.a_row0 + lane);
+          if (src >= 0 && (int64_t)src < a.T * a.K) tok = src / a.K;
+          else atomicOr(a.err, kErrBounds);
+        }
       }
-      int klen = 0;
-      const int64_t row0 = item_row0<PHASE>(a, ir.g, ir.blk, &klen);
-      const int Fk = kind ? a.Fs : a.F;
-      const uint8_t* stage = s_stage + (size_t)s * kRowsPerItem * srow;
-      const int units = klen / unit_elems(FMT);
-      float acc[kRowsPerItem][R];
-      if (PHASE == 0) {
-        // row r's token: its packed copy's source slot / K (routed), or r (shared)
-        int tok = 0;
-        if (lane < rows) {
-          if (kind) {
-            tok = lane;
-          } else {
-            const int32_t src = __ldg(a.perm_src + gd.a_row0 + lane);
-            if (src >= 0 && (int64_t)src < a.T * a.K) tok = src / a.K;
-            else atomicOr(a.err, kErrBounds);
-          }
+      const void* xr[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) xr[r] = s_rows + (int64_t)__shfl_sync(0xFFFFFFFFu, tok, r) * a.d;
+      dot_rows<FMT, R, kXShared>(w, xr, rows, (int)units, lane, acc);
+      float gs0 = 1.f, gs1 = 1.f, us0 = 1.f, us1 = 1.f;
+      if (FMT == kSmallE4M3) {
+        const float* sg = static_cast<const float*>(kind ? a.s_gate_scale : a.w_gate_scale);
+        const float* su = static_cast<const float*>(kind ? a.s_up_scale : a.w_up_scale);
+        gs0 = __ldg(sg + row0);
+        gs1 = __ldg(sg + row0 + 1);
+        us0 = __ldg(su + row0);
+        us1 = __ldg(su + row0 + 1);
+      }
+      uint32_t* h = static_cast<uint32_t*>(kind ? a.h_sh : a.h);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (lane == r && r < rows) {
+          const float h0 = silu_f(gs0 * acc[0][r]) * (us0 * acc[2][r]);
+          const float h1 = silu_f(gs1 * acc[1][r]) * (us1 * acc[3][r]);
+          if (kF16) over |= fmaxf(fabsf(h0), fabsf(h1)) >= 65520.f;
+          h[((int64_t)(gd.h_row0 + r) * Fk + f0) / 2] = kF16 ? pack_f16x2(h0, h1) : pack_bf16x2(h0, h1);
         }
-        const void* xr[R];
+      }
+    } else {
+      const int j0 = kRowsPerItem * blk;
+      const int64_t units = row_units(Fk, FMT);
+      const int64_t row0 = (int64_t)e * a.d + j0;  // W_down row j0 of this expert
+      const uint4* wd = static_cast<const uint4*>(kind ? a.s_down : a.w_down);
+      const uint4* const w[kRowsPerItem] = {wd + row0 * units, wd + (row0 + 1) * units, wd + (row0 + 2) * units,
+                                            wd + (row0 + 3) * units};
+      const uint16_t* hb = static_cast<const uint16_t*>(kind ? a.h_sh : a.h);
+      const void* xr[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) xr[r] = s_rows + (int64_t)__shfl_sync(0xFFFFFFFFu, tok, r) * a.d;
-        dot_stage<FMT, R, kXShared>(stage, srow, xr, rows, units, lane, acc);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s_empty[s]));
-        const int f0 = 2 * ir.blk;
-        float gs0 = 1.f, gs1 = 1.f, us0 = 1.f, us1 = 1.f;
-        if (FMT == kSmallE4M3) {
-          const float* sg = static_cast<const float*>(kind ? a.s_gate_scale : a.w_gate_scale);
-          const float* su = static_cast<const float*>(kind ? a.s_up_scale : a.w_up_scale);
-          gs0 = __ldg(sg + row0);
-          gs1 = __ldg(sg + row0 + 1);
-          us0 = __ldg(su + row0);
-          us1 = __ldg(su + row0 + 1);
+      for (int r = 0; r < R; ++r) xr[r] = hb + (int64_t)(gd.h_row0 + r) * Fk;
+      dot_rows<FMT, R, kXAct16>(w, xr, rows, (int)units, lane, acc);
+      const int q = lane & (kRowsPerItem - 1), rl = lane / kRowsPerItem;
+      if (rl < rows) {
+        float y = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int qq = 0; qq < kRowsPerItem; ++qq)
+            if (r == rl && qq == q) y = acc[qq][r];
+        if (FMT == kSmallE4M3)
+          y *= __ldg(static_cast<const float*>(kind ? a.s_down_scale : a.w_down_scale) + row0 + q);
+        int64_t t = rl;
+        float wt = 1.f;
+        bool ok = true;
+        if (kind == 0) {
+          const int32_t src = __ldg(a.perm_src + gd.h_row0 + rl);
+          ok = src >= 0 && (int64_t)src < a.T * a.K;
+          t = ok ? src / a.K : 0;
+          wt = ok ? __ldg(a.topk_w + src) : 0.f;
+          if (!ok) atomicOr(a.err, kErrBounds);
         }
-        uint32_t* h = static_cast<uint32_t*>(kind ? a.h_sh : a.h);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (lane == r && r < rows) {
-            const float h0 = silu_f(gs0 * acc[0][r]) * (us0 * acc[2][r]);
-            const float h1 = silu_f(gs1 * acc[1][r]) * (us1 * acc[3][r]);
-            if (kF16) over |= fmaxf(fabsf(h0), fabsf(h1)) >= 65520.f;
-            h[((int64_t)(gd.h_row0 + r) * Fk + f0) / 2] = kF16 ? pack_f16x2(h0, h1) : pack_bf16x2(h0, h1);
-          }
-        }
-      } else {
-        const uint16_t* hb = static_cast<const uint16_t*>(kind ? a.h_sh : a.h);
-        const void* xr[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) xr[r] = hb + (int64_t)(gd.h_row0 + r) * Fk;
-        dot_stage<FMT, R, kXAct16>(stage, srow, xr, rows, units, lane, acc);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&s_empty[s]));
-        const int j0 = kRowsPerItem * ir.blk;
-        const int q = lane & (kRowsPerItem - 1), rl = lane / kRowsPerItem;
-        if (rl < rows) {
-          float y = 0.f;
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int qq = 0; qq < kRowsPerItem; ++qq)
-              if (r == rl && qq == q) y = acc[qq][r];
-          if (FMT == kSmallE4M3)
-            y *= __ldg(static_cast<const float*>(kind ? a.s_down_scale : a.w_down_scale) + row0 + q);
-          int64_t t = rl;
-          float wt = 1.f;
-          bool valid = true;
-          if (kind == 0) {
-            const int32_t src = __ldg(a.perm_src + gd.h_row0 + rl);
-            valid = src >= 0 && (int64_t)src < a.T * a.K;
-            t = valid ? src / a.K : 0;
-            wt = valid ? __ldg(a.topk_w + src) : 0.f;
-            if (!valid) atomicOr(a.err, kErrBounds);
-          }
-          if (valid) atomicAdd(a.out_acc + t * a.d + j0 + q, wt * y);
-        }
+        if (ok) atomicAdd(a.out_acc + t * a.d + j0 + q, wt * y);
       }
     }
   }
   if (over) atomicOr(a.err, kErrRange);
-  __syncthreads();
   if (PHASE == 1) {
     // the last CTA to finish rounds the accumulator to the bf16 output
+    __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
       s_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
@@ -464,32 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) small_batch_ffn_kernel(const Smal
   }
 }
 
-// Shared memory of a phase: the staged token rows (phase 0) and the stages
-// (four rows of the longest weight row each); 0 stages if fewer than 2 fit.
-struct SmemPlan {
-  int stages;
-  int stage_row_bytes;
-  size_t bytes;
-};
-SmemPlan smem_plan(int fmt, int phase, int64_t T, int32_t d, int32_t F, int32_t Fs, int32_t S) {
-  SmemPlan p{};
-  const size_t x_bytes = phase == 0 ? align128((size_t)T * d * 4) : 0;
-  const int klen = phase == 0 ? d : (S > 0 && Fs > F ? Fs : F);
-  p.stage_row_bytes = (int)align128((size_t)klen * elem_bytes(fmt));
-  const size_t stage = (size_t)kRowsPerItem * p.stage_row_bytes;
-  if (x_bytes + 2 * stage > kSmallBatchMaxSmem) return SmemPlan{};
-  const size_t fit = (kSmallBatchMaxSmem - x_bytes) / stage;
-  p.stages = (int)(fit < (size_t)kMaxStages ? fit : (size_t)kMaxStages);
-  p.bytes = x_bytes + (size_t)p.stages * stage;
-  return p;
-}
-
 // These grids are launched without programmatic stream serialisation (their
 // griddepcontrol.wait is then a no-op): measured, letting them start early
 // behind the previous kernel made a 2-token layer 13 % and a 4-token layer
-// 14 % slower, with every stage's own time unchanged. Their dynamic shared
-// memory exceeds the default 48 KB; the limit is raised once per kernel and
-// device.
+// 14 % slower, with every stage's own time unchanged. The gate/up grid's
+// dynamic shared memory (the token rows) may exceed the default 48 KB; its
+// limit is raised once per kernel and device.
 template <int FMT, int R, int PHASE, bool HB>
 cudaError_t launch_k(const SmallBatchArgs& a, unsigned grid, size_t smem, cudaStream_t s) {
   void (*kern)(const SmallBatchArgs) = small_batch_ffn_kernel<FMT, R, PHASE, HB>;
@@ -498,7 +399,7 @@ cudaError_t launch_k(const SmallBatchArgs& a, unsigned grid, size_t smem, cudaSt
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load() & bit)) {
+  if (PHASE == 0 && !(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallBatchMaxSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
@@ -514,26 +415,18 @@ cudaError_t launch_k(const SmallBatchArgs& a, unsigned grid, size_t smem, cudaSt
 }
 
 template <int FMT, int R>
-cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, size_t smem, cudaStream_t s) {
-  if (phase == 1) return launch_k<FMT, R, 1, true>(a, grid, smem, s);
+cudaError_t launch_fr(const SmallBatchArgs& a, int phase, unsigned grid, cudaStream_t s) {
+  if (phase == 1) return launch_k<FMT, R, 1, true>(a, grid, 0, s);
+  const size_t smem = (size_t)a.T * a.d * 4;
   return a.hidden_bf16 ? launch_k<FMT, R, 0, true>(a, grid, smem, s) : launch_k<FMT, R, 0, false>(a, grid, smem, s);
 }
 
 }  // namespace
 
-bool small_batch_fits(int fmt, int64_t T, int32_t d, int32_t F, int32_t Fs, int32_t S) {
-  return smem_plan(fmt, 0, T, d, F, Fs, S).stages >= 2 && smem_plan(fmt, 1, T, d, F, Fs, S).stages >= 2;
-}
-
-cudaError_t launch_small_batch_ffn(const SmallBatchArgs& args, int phase, cudaStream_t s) {
-  SmallBatchArgs a = args;
+cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStream_t s) {
   if (a.max_rows < 1 || a.max_rows > kSmallBatchMaxRows || a.N > kMaxExperts) return cudaErrorInvalidValue;
   if (a.fmt == kSmallE4M3 ? a.max_rows != 1 : a.fmt != kSmallBf16) return cudaErrorInvalidValue;
-  if (a.T < 1 || a.T > a.max_rows) return cudaErrorInvalidValue;
-  const SmemPlan sp = smem_plan(a.fmt, phase, a.T, a.d, a.F, a.Fs, a.S);
-  if (sp.stages < 2) return cudaErrorInvalidValue;
-  a.stages = sp.stages;
-  a.stage_row_bytes = sp.stage_row_bytes;
+  if (a.T < 1 || a.T > a.max_rows || (size_t)a.T * a.d * 4 > kSmallBatchMaxSmem) return cudaErrorInvalidValue;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // items: at most min(N, rows) routed experts hold rows
@@ -541,13 +434,13 @@ cudaError_t launch_small_batch_ffn(const SmallBatchArgs& args, int phase, cudaSt
   const int64_t per_r = phase == 0 ? a.F / 2 : a.d / kRowsPerItem;
   const int64_t per_s = phase == 0 ? a.Fs / 2 : a.d / kRowsPerItem;
   const int64_t items = touched * per_r + (a.S > 0 ? a.S * per_s : 0);
-  int64_t want = (items + kConsumers - 1) / kConsumers;
+  int64_t want = (items + kWarps - 1) / kWarps;
   if (want < 1) want = 1;
   const unsigned grid = (unsigned)(want < sms ? want : sms);
-  if (a.fmt == kSmallE4M3) return launch_fr<kSmallE4M3, 1>(a, phase, grid, sp.bytes, s);
-  if (a.max_rows <= 1) return launch_fr<kSmallBf16, 1>(a, phase, grid, sp.bytes, s);
-  if (a.max_rows <= 2) return launch_fr<kSmallBf16, 2>(a, phase, grid, sp.bytes, s);
-  return launch_fr<kSmallBf16, 4>(a, phase, grid, sp.bytes, s);
+  if (a.fmt == kSmallE4M3) return launch_fr<kSmallE4M3, 1>(a, phase, grid, s);
+  if (a.max_rows <= 1) return launch_fr<kSmallBf16, 1>(a, phase, grid, s);
+  if (a.max_rows <= 2) return launch_fr<kSmallBf16, 2>(a, phase, grid, s);
+  return launch_fr<kSmallBf16, 4>(a, phase, grid, s);
 }
 
 }  // namespace moe
