@@ -93,6 +93,9 @@ def test_decode_sized_batches_take_the_cuda_core_expert_path():
         assert B.layer_small_batch(B.problem(inputs.QWEN_DECODE_FP8, T=T)) == want, T
     assert not B.layer_small_batch(B.problem(inputs.QWEN_DECODE_MXFP4, T=1))
     assert not B.layer_small_batch(B.problem(inputs.MIXTRAL_EC, T=2))
+    # the gate/up kernel stages the T token rows as fp32 in 192 KB of shared memory
+    assert B.layer_small_batch(B.problem(q, T=1, d_model=16384))
+    assert not B.layer_small_batch(B.problem(q, T=4, d_model=16384))
     with pytest.raises(ValueError):
         B.layer_small_batch(B.problem(q, top_k=0))
     # router (CUDA-core logits + top-K), routing (one CTA, no row copy), gate/up,
