@@ -593,11 +593,13 @@ def main():
     cfg, desc = WORKLOADS[args.workload]
     if args.tokens is not None:
         cfg, desc = cfg.with_(T=args.tokens), f"{desc}, T={args.tokens}"
-    world, rank, _ = dist_setup(args.gpus)
     if args.impl == "reference":
-        run_reference(args, cfg, desc, world, rank)
-    else:
-        run_ours(args, cfg, desc, world, rank)
+        # the oracle runs on the host cores: no GPU or process group is needed;
+        # under torchrun only rank 0 runs and prints
+        run_reference(args, cfg, desc, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, _ = dist_setup(args.gpus)
+    run_ours(args, cfg, desc, world, rank)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
