@@ -443,7 +443,10 @@ moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
  *                 0 router+top-K, 1 route and pack, 2 GEMM schedule (built
  *                 inside route and pack: an empty stage),
  *                 3 gate/up GEMM + SwiGLU, 4 down GEMM + weighted scatter-add,
- *                 5 fp32 -> bf16 finalise.
+ *                 5 fp32 -> bf16 finalise. On the CUDA-core path of a
+ *                 decode-sized batch (moe_layer_small_batch) stages 3 and 4
+ *                 are its two kernels, the rounding happens inside stage 4
+ *                 and stage 5 is empty.
  * Used by the benchmark to time each kernel inside the timed region.
  */
 #define MOE_LAYER_STAGES 6
