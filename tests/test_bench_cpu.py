@@ -32,6 +32,14 @@ def test_reference_arm_prints_one_json_line_without_a_gpu():
     assert d["config"]["T"] == 64 and d["config"]["workload"]
 
 
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    # under torchrun every rank but 0 returns at once, printing nothing
+    args = bench.argparse.Namespace(steps=1, warmup=0, gpus=2)
+    cfg, desc = bench.WORKLOADS["tiny"]
+    bench.run_reference(args, cfg, desc, world=2, rank=1)
+    assert capsys.readouterr().out == ""
+
+
 def test_work_model_matches_the_layers_closed_form():
     # Mixtral-shaped: router 2TdN, experts 6 d F T K; bytes: the 8 experts'
     # three bf16 matrices, the fp32 router, hidden in and out in bf16
