@@ -107,6 +107,35 @@ def test_decode_sized_batches_take_the_cuda_core_expert_path():
     assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_MXFP4, T=1)) == 11
 
 
+def test_small_batch_decision_agrees_with_the_launch_count():
+    # over random valid problems: the CUDA-core path runs router + routing +
+    # two kernels, never the activation splits, MXFP4 preparation or finalise
+    import numpy as np
+
+    rng = np.random.default_rng(0)
+    seen = set()
+    for _ in range(300):
+        fmt = ["bf16", "fp8", "mxfp4"][rng.integers(3)]
+        N = int(rng.integers(1, 257))
+        K = int(rng.integers(1, min(N, 32) + 1))
+        unit = 32 if fmt == "mxfp4" else 16 if fmt == "fp8" else 8
+        S = int(rng.integers(0, 3))
+        cfg = inputs.MoEConfig("rand", T=int(rng.integers(0, 9)), d=unit * int(rng.integers(1, 200)), N=N, K=K,
+                               F=unit * int(rng.integers(1, 100)), S=S, Fs=unit * int(rng.integers(1, 50)) if S else 0,
+                               hidden_dtype=["bf16", "f32"][rng.integers(2)], expert_dtype=fmt,
+                               routing="expert" if rng.random() < 0.2 else "token")
+        p = B.problem(cfg)
+        if B.problem_check(p) != B.MOE_OK:
+            continue
+        small = B.layer_small_batch(p)
+        seen.add(small)
+        if small:
+            assert cfg.routing == "token" and 1 <= cfg.T <= (1 if fmt == "fp8" else 4) and fmt != "mxfp4"
+            router = 2  # T <= 64: CUDA-core logits + top-K
+            assert B.layer_forward_kernel_count(p) == router + 1 + 2
+    assert seen == {True, False}
+
+
 def _fake_prepared():
     w = B.Weights()
     w.mx_prep = 256  # only its nullness is read by the host-side count
