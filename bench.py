@@ -51,6 +51,12 @@ for _T in inputs.DECODE_BATCHES:
     WORKLOADS[f"decode{_T}_mxfp4"] = (inputs.QWEN_DECODE_MXFP4.with_(T=_T),
                                       f"Qwen3-235B-like decode layer, MXFP4 experts, T={_T}")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# What the expert GEMMs multiply: bf16 x bf16, or the stored 8-bit weight
+# codes against 8-bit (two-term E4M3) splits of fp16 activations; fp32
+# accumulation throughout.
+DTYPES = {"bf16": "bf16",
+          "fp8": "e4m3 weights (row scales) x two-term e4m3 of fp16 activations",
+          "mxfp4": "mxfp4 (e2m1 + e8m0 block scales) weights x two-term e4m3 of fp16 activations"}
 
 
 def parse():
@@ -319,6 +325,7 @@ def cpu_baseline(cfg, ins, budget_s):
         n, s, _ = oracle_rows_timed(cfg, ins, rows)
         done, spent, start = done + n, spent + s, start + n
     return {"value": done / spent, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "precision": "fp64 arithmetic, fp32 router decision",
             "sample": f"first {done} tokens of the same workload through the fp64 oracle layer "
                       f"(router, top-K, SwiGLU experts, combine), {spent:.1f} s of CPU wall time"}
 
@@ -330,7 +337,7 @@ def run_reference(args, cfg, desc, world, rank):
         return
     from oracle import oracle
 
-    ins = inputs.make_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    ins = inputs.make_inputs(cfg, seed=0, device="cpu")
     thr = oracle.num_threads()
     rows = np.arange(min(cfg.T, thr))
     for _ in range(args.warmup):
@@ -345,6 +352,7 @@ def run_reference(args, cfg, desc, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(cfg, desc, args), "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                             "precision": "fp64 arithmetic, fp32 router decision",
                              "sample": f"{len(rows)} tokens of the workload per step through the fp64 "
                                        f"oracle layer"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -532,18 +540,21 @@ def run_ours(args, cfg, desc, world, rank):
         dom_name = {"gateup_swiglu_gemm": "small_batch_ffn_gateup",
                     "down_scatter_gemm": "small_batch_ffn_down"}[dom_name]
     clocks = sampler.summary(t_wall0, t_wall1)
-    # The recipe's denominators: the burst peak for a kernel timed alone, the
-    # sustained one for a kernel timed inside a long run that the power cap
-    # holds well below the maximum clock (where the sustained figure was taken).
-    power_capped = bool(clocks and "sw_power_cap" in clocks["reasons"] and clocks.get("sm_mhz")
-                        and clocks.get("sm_max_mhz") and clocks["sm_mhz"] < 0.85 * clocks["sm_max_mhz"])
-    long_region = elapsed_s >= 1.0 or power_capped
-    key = "bf16_tflops_sustained" if long_region and "bf16_tflops_sustained" in peaks else "bf16_tflops"
-    tpeak = peaks[key]
+    # The denominator is the measured burst bf16 peak: the dominant kernel is
+    # one launch of about a millisecond, timed on its own events inside a
+    # region well under a second. The sustained figure (cuBLAS looped for
+    # seconds under the power cap) is reported beside it, and so is the
+    # fraction at the maximum SM clock (the achieved rate scaled by the ratio
+    # of the maximum to the median sampled clock), for runs the power cap
+    # held below the maximum.
+    tpeak = peaks["bf16_tflops"]
+    sm_med = clocks.get("sm_mhz") if clocks else None
+    sm_max = (clocks.get("sm_max_mhz") if clocks else None) or peaks.get("sm_max_mhz")
+    clock_scale = (sm_max / sm_med) if (sm_med and sm_max and sm_med > 0) else None
     # The dominant kernel's bound: its algorithmic bytes at the HBM peak
-    # against its algorithmic FLOPs at the tensor peak. FP8 experts are held
-    # to the bf16 peak: each useful product is two E4M3 products (the two
-    # activation terms) at twice the bf16 rate.
+    # against its algorithmic FLOPs at the tensor peak. FP8 and MXFP4 experts
+    # are held to the bf16 peak: each useful product is two 8-bit products
+    # (the two activation terms) at twice the bf16 rate.
     flops = wm["flops_gateup"] if dom == gu else wm["flops_down"]
     bytes_ = wm["bytes_gateup"] if dom == gu else wm["bytes_down"]
     hbm_bound = bytes_ / (peaks["hbm_gbs"] * 1e9) >= flops / (tpeak * 1e12)
@@ -553,25 +564,31 @@ def run_ours(args, cfg, desc, world, rank):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "algorithmic_bytes_per_launch": bytes_}
-        src_note = "burst"
+        src_note = "copy bandwidth"
     else:
         achieved = flops / (stage_ms[dom] * 1e-3) / 1e12
         peak = tpeak
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
-                "algorithmic_flops_per_launch": flops}
-        src_note = ("sustained: run held by the power cap below 85% of max clock, or >= 1 s"
-                    if key == "bf16_tflops_sustained" else "burst")
+                "frac": achieved / peak, "algorithmic_flops_per_launch": flops}
+        if "bf16_tflops_sustained" in peaks:
+            roof["frac_of_sustained_peak"] = achieved / peaks["bf16_tflops_sustained"]
+        if clock_scale is not None:
+            roof["frac_at_max_clock"] = achieved * clock_scale / peak
+        src_note = "bf16 burst"
     roof.update({"kernel": dom_name,
                  "peak_source": f"{peak_src} ({src_note})",
                  "traffic": traffic_from_profiles(dom_name, args.workload)})
+    layer_roof = {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],
+                  "t_roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step,
+                  "peaks": "bf16 burst, HBM copy bandwidth"}
+    if clock_scale is not None and wm["flops"] / (tpeak * 1e12) >= wm["bytes"] / (peaks["hbm_gbs"] * 1e9):
+        layer_roof["frac_at_max_clock"] = 1e3 * t_roof / ms_step * clock_scale
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16" if cfg.expert_dtype in ("fp8", "mxfp4") else "bf16",
+            "vs_baseline": None, "dtype": DTYPES[cfg.expert_dtype],
             "data": "synthetic (seeded; random-init weights)",
             "config": config_block(cfg, desc, args), "roofline": roof,
-            "layer_roofline": {"flops": wm["flops"], "bytes": wm["bytes"], "touched_experts": wm["touched"],
-                               "t_roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step},
+            "layer_roofline": layer_roof,
             "stages_ms": dict(zip(B.LAYER_STAGES, stage_ms)),
             "ms_per_step_profiled": profiled_ms,
             "timed_region_ms": region_ms,

@@ -287,6 +287,16 @@ moe_status_t moe_permute(const moe_problem_t* p, const int32_t* topk_idx,
  * Requires p->score_fn's router inputs as in moe_router_topk; no selection
  * bias, no group limit (MOE_ERR_UNSUPPORTED otherwise).
  */
+/*
+ * The number of tokens C every expert takes under expert-choice routing:
+ * C = min(ceil(c * T * K / N), T), c = p->capacity_factor, or 1 when it is 0
+ * ("Chapter 19", §19.6.1, the capacity equation; here applied per expert to
+ * tokens instead of to token copies). Sizes row_token / row_w below and the
+ * layer's packed rows (N * C). Host only, no CUDA call; p->routing is not
+ * read. Returns -1 for an invalid problem.
+ */
+int64_t moe_expert_choice_capacity(const moe_problem_t* p);
+
 moe_status_t moe_expert_choice_select(const moe_problem_t* p, const void* hidden,
                                       const float* w_router, const float* router_bias,
                                       int32_t* row_token, float* row_w, int32_t* offsets,
@@ -314,7 +324,13 @@ moe_status_t moe_expert_choice_select(const moe_problem_t* p, const void* hidden
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress); make that first call before any stream
- * capture. Every call on a device shares the one array and leaves its contents
+ * capture. The address is cached per device together with the CUDA context
+ * it was looked up in, and looked up again when a call comes from another
+ * context. After cudaDeviceReset the primary context (and the array) is
+ * created anew and may reuse the old context handle: make a first call again
+ * before any capture, and do not reuse the array's contents across a reset.
+ * For FP8 and MXFP4 experts x_perm holds fp16 rows, as in moe_permute.
+ * Every call on a device shares the one array and leaves its contents
  * behind: calls whose work overlaps on the GPU (different streams or host
  * threads without ordering between them) race and give wrong results, so
  * order them. The call clears the array's error word itself. There is no

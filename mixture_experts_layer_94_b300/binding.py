@@ -79,6 +79,7 @@ def _load():
         "moe_mxfp4_prep_bytes": ([pp], sz),
         "moe_mxfp4_prepare": ([pp, ctypes.POINTER(Weights), P, sz, P], i32),
         "moe_expert_choice_select": ([pp] + [P] * 7 + [sz, P], i32),
+        "moe_expert_choice_capacity": ([pp], ctypes.c_int64),
         "moe_permute_static": ([pp] + [P] * 8, i32),
         "moe_debug_stall_wait": ([P, sz, ctypes.c_uint32, P], i32),
     }
@@ -95,7 +96,7 @@ lib = _load()
 def header_functions() -> list:
     """Names of the functions include/moe.h declares."""
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\*|moe_status_t|size_t|int32_t)\s+(moe_\w+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\*|moe_status_t|size_t|int32_t|int64_t)\s+(moe_\w+)\s*\(",
                                  text, re.M)))
 
 
@@ -162,11 +163,12 @@ def router_topk(p: Problem, hidden, w_router, topk_idx, topk_w, router_bias=None
 
 
 def expert_choice_capacity(cfg: MoEConfig, T: int = None) -> int:
-    """Tokens every expert takes under expert-choice routing: min(ceil(c T K / N), T)."""
-    import math
-    T = cfg.T if T is None else T
-    c = cfg.capacity_factor if cfg.capacity_factor > 0 else 1.0
-    return min(math.ceil(c * T * cfg.K / cfg.N), T)
+    """Tokens every expert takes under expert-choice routing, as the library
+    computes it (moe_expert_choice_capacity)."""
+    c = int(lib.moe_expert_choice_capacity(ctypes.byref(problem(cfg, **({} if T is None else {"T": T})))))
+    if c < 0:
+        raise ValueError("invalid problem")
+    return c
 
 
 def expert_choice_select(p: Problem, hidden, w_router, row_token, row_w, offsets, router_bias=None,

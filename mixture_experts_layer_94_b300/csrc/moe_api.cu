@@ -740,6 +740,11 @@ moe_status_t moe_router_topk(const moe_problem_t* p, const void* hidden, const f
   return cuda_status(launch_router(a, p->hidden_dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
 }
 
+int64_t moe_expert_choice_capacity(const moe_problem_t* p) {
+  if (moe_problem_check(p) != MOE_OK) return -1;
+  return ec_capacity(*p);
+}
+
 moe_status_t moe_expert_choice_select(const moe_problem_t* p, const void* hidden, const float* w_router,
                                       const float* router_bias, int32_t* row_token, float* row_w,
                                       int32_t* offsets, void* ws, size_t ws_bytes, void* stream) {

@@ -12,6 +12,7 @@
 //
 // The array below is reserved on every GPU that loads the library and stays
 // there until the process exits. Every call on a device uses the same array.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,19 +30,46 @@ static __device__ __align__(256) int32_t g_permute_scratch[kErrWords + MOE_PERMU
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+  CUcontext ctx;  // the context the address was looked up in
+  void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+// cuCtxGetCurrent through the runtime's driver entry point (no libcuda link).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
 
 // The device address of g_permute_scratch on `dev`. In host code the array's
-// name is only a host-side stand-in, so the address is looked up once per
-// device, with that device current, and cached.
+// name is only a host-side stand-in, so the address is looked up with the
+// device current and cached per device, together with the context it was
+// looked up in; a call from another context (a non-primary context on the
+// same device) looks it up again. Runs after the caller's cudaGetDevice, so
+// the device's primary context is current unless the caller made another one
+// current.
 moe_status_t scratch_address(int dev, void** out) {
+  CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& c = g_scratch_addr[dev];
+  if (!c.addr || c.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return MOE_OK;
 }
 
@@ -86,7 +114,9 @@ extern "C" moe_status_t moe_permute_static(const moe_problem_t* p, const int32_t
   a.perm_src = perm_src;
   a.inv_row = inv_row;
   a.x_perm = x_perm;
-  a.act_f16 = p->expert_dtype == MOE_EXPERT_FP8_E4M3;
+  // FP8 and MXFP4 experts read fp16 packed rows, bf16 experts bf16 ones
+  // (the rows moe_permute writes for the same problem).
+  a.act_f16 = p->expert_dtype == MOE_EXPERT_FP8_E4M3 || p->expert_dtype == MOE_EXPERT_MXFP4;
   a.err = static_cast<uint32_t*>(base);
   return moe::launch_permute(a, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -687,6 +687,28 @@ int moe_oracle_layer_routed_fp8(int64_t n_rows, int32_t d, int32_t N, int32_t M,
   return layer_routed_impl(n_rows, d, N, M, F, S, Fs, hidden, idx, w, &routed, &shared, out);
 }
 
+/* moe_oracle_layer_routed with MXFP4 experts: packed E2M1 codes and E8M0
+ * block scales as moe_oracle_layer_mxfp4. */
+int moe_oracle_layer_routed_mxfp4(int64_t n_rows, int32_t d, int32_t N, int32_t M, int32_t F, int32_t S,
+                                  int32_t Fs, const float* hidden, const int32_t* idx, const double* w,
+                                  const uint8_t* const* q_gate, const uint8_t* const* q_up,
+                                  const uint8_t* const* q_down, const uint8_t* const* b_gate,
+                                  const uint8_t* const* b_up, const uint8_t* const* b_down,
+                                  const uint8_t* const* qs_gate, const uint8_t* const* qs_up,
+                                  const uint8_t* const* qs_down, const uint8_t* const* bs_gate,
+                                  const uint8_t* const* bs_up, const uint8_t* const* bs_down, double* out) {
+  if (!b_gate || !b_up || !b_down) return ORACLE_ERR_ARG;
+  if (S > 0 && (!bs_gate || !bs_up || !bs_down)) return ORACLE_ERR_ARG;
+  if ((d % 32) != 0 || (F % 32) != 0 || (S > 0 && (Fs % 32) != 0)) return ORACLE_ERR_ARG;
+  const wset_t routed = {2, (const void* const*)q_gate, (const void* const*)q_up,
+                         (const void* const*)q_down, (const void* const*)b_gate, (const void* const*)b_up,
+                         (const void* const*)b_down};
+  const wset_t shared = {2, (const void* const*)qs_gate, (const void* const*)qs_up,
+                         (const void* const*)qs_down, (const void* const*)bs_gate, (const void* const*)bs_up,
+                         (const void* const*)bs_down};
+  return layer_routed_impl(n_rows, d, N, M, F, S, Fs, hidden, idx, w, &routed, &shared, out);
+}
+
 /*
  * The whole layer for `n_rows` tokens whose hidden rows are given (fp32
  * [n_rows][d]): router, top-K, every chosen expert's FFN, the always-on shared

@@ -65,6 +65,8 @@ def _load():
         lib.moe_oracle_layer_fp8.restype = ctypes.c_int
         lib.moe_oracle_layer_routed_fp8.argtypes = [i64] + [i32] * 6 + [P] * 16
         lib.moe_oracle_layer_routed_fp8.restype = ctypes.c_int
+        lib.moe_oracle_layer_routed_mxfp4.argtypes = [i64] + [i32] * 6 + [P] * 16
+        lib.moe_oracle_layer_routed_mxfp4.restype = ctypes.c_int
         lib.moe_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
         lib.moe_oracle_e2m1_to_double.restype = ctypes.c_double
         lib.moe_oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
@@ -517,3 +519,33 @@ def layer_mxfp4(hidden, w_router, q_gate, b_gate, q_up, b_up, q_down, b_down, K,
     if rc != 0:
         raise ValueError(f"moe_oracle_layer_mxfp4 failed ({rc})")
     return dict(idx=idx, w=w, margin=margin, out=out)
+
+
+def layer_routed_mxfp4(hidden, idx, w, q_gate, b_gate, q_up, b_up, q_down, b_down, qs_gate=None, bs_gate=None,
+                       qs_up=None, bs_up=None, qs_down=None, bs_down=None):
+    """layer_routed with MXFP4 experts (packed codes + E8M0 block scales, as layer_mxfp4)."""
+    lib = _load()
+    x = _f32(hidden)
+    n, d = x.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = _f64(w)
+    M = idx.shape[1]
+    N = len(q_gate)
+    F = next(_u8(m).shape[0] for m in q_gate if m is not None)
+    S = 0 if qs_gate is None else len(qs_gate)
+    Fs = _u8(qs_gate[0]).shape[0] if S else 0
+    arrays, keepalive = [], []
+    for mats, cnt in ((q_gate, N), (q_up, N), (q_down, N), (b_gate, N), (b_up, N), (b_down, N),
+                      (qs_gate, S), (qs_up, S), (qs_down, S), (bs_gate, S), (bs_up, S), (bs_down, S)):
+        if cnt == 0:
+            arrays.append(None)
+            continue
+        arr, k = _raw_ptr_array(mats, cnt, _u8)
+        keepalive.append((arr, k))
+        arrays.append(ctypes.cast(arr, ctypes.c_void_p))
+    out = np.empty((n, d), np.float64)
+    rc = lib.moe_oracle_layer_routed_mxfp4(n, d, N, M, F, S, Fs, _ptr(x), _ptr(idx), _ptr(w), *arrays, _ptr(out))
+    del keepalive
+    if rc != 0:
+        raise ValueError(f"moe_oracle_layer_routed_mxfp4 failed ({rc})")
+    return out

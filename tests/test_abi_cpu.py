@@ -257,3 +257,15 @@ def test_problem_check_mxfp4_experts():
     assert B.lib.moe_grouped_swiglu_fp8(p, *([None] * 11), 0, None) == -1   # the other format
     assert B.workspace_bytes(p, B.CALL_LAYER_FORWARD) > B.workspace_bytes(
         B.problem(inputs.TINY.with_(expert_dtype="fp8")), B.CALL_LAYER_FORWARD)  # + row reference scales
+
+
+@pytest.mark.parametrize("T,K,N,c", [(4096, 2, 8, 0.0), (40, 2, 8, 0.6), (7, 4, 4, 0.0), (6, 2, 64, 0.0),
+                                     (200, 3, 16, 0.5), (10, 8, 8, 3.0), (0, 2, 8, 0.0), (1, 1, 1, 0.0)])
+def test_expert_choice_capacity_is_the_oracles(T, K, N, c):
+    """The library's C (which sizes the binding's buffers) against the oracle's
+    capacity formula, min(ceil(c T K / N), T) with c = 1 when unset."""
+    from oracle import oracle
+
+    cfg = inputs.MoEConfig("ec", T=T, d=64, N=N, K=K, F=64, capacity_factor=c, routing="expert")
+    assert B.expert_choice_capacity(cfg) == oracle.expert_choice_capacity(c, T, K, N)
+    assert B.lib.moe_expert_choice_capacity(ctypes.byref(B.problem(cfg, top_k=N + 1))) == -1

@@ -787,3 +787,31 @@ def test_layer_mxfp4_equals_bf16_layer_on_exact_weights():
                        ws_up=b(shared, 1), ws_down=b(shared, 2))
     assert np.array_equal(got["idx"], ref["idx"])
     assert np.array_equal(got["out"], ref["out"])
+
+
+def test_layer_routed_mxfp4_equals_bf16_on_exact_weights():
+    """The MXFP4 routed layer (a given routing, slots with index -1 skipped)
+    equals the bf16 routed layer bit for bit on weights exact in both formats,
+    and equals the MXFP4 token-choice layer under that layer's own routing."""
+    rng = np.random.default_rng(23)
+    T, d, N, M, F, Fs = 7, 64, 4, 3, 32, 64
+    hidden = rng.standard_normal((T, d)).astype(np.float32)
+    idx = rng.integers(-1, N, size=(T, M)).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, size=(T, M))
+    routed = [(_mxfp4_case(rng, F, d), _mxfp4_case(rng, F, d), _mxfp4_case(rng, d, F)) for _ in range(N)]
+    shared = [(_mxfp4_case(rng, Fs, d), _mxfp4_case(rng, Fs, d), _mxfp4_case(rng, d, Fs))]
+    q = lambda cases, m, j: [c[m][j] for c in cases]  # noqa: E731
+    b = lambda cases, m: [_bf16_bits(c[m][2]) for c in cases]  # noqa: E731
+    mx = dict(qs_gate=q(shared, 0, 0), bs_gate=q(shared, 0, 1), qs_up=q(shared, 1, 0), bs_up=q(shared, 1, 1),
+              qs_down=q(shared, 2, 0), bs_down=q(shared, 2, 1))
+    got = oracle.layer_routed_mxfp4(hidden, idx, w, q(routed, 0, 0), q(routed, 0, 1), q(routed, 1, 0),
+                                    q(routed, 1, 1), q(routed, 2, 0), q(routed, 2, 1), **mx)
+    ref = oracle.layer_routed(hidden, idx, w, b(routed, 0), b(routed, 1), b(routed, 2), ws_gate=b(shared, 0),
+                              ws_up=b(shared, 1), ws_down=b(shared, 2))
+    assert np.array_equal(got, ref)
+    w_router = rng.standard_normal((d, N)).astype(np.float32)
+    tc = oracle.layer_mxfp4(hidden, w_router, q(routed, 0, 0), q(routed, 0, 1), q(routed, 1, 0), q(routed, 1, 1),
+                            q(routed, 2, 0), q(routed, 2, 1), K=2, **mx)
+    again = oracle.layer_routed_mxfp4(hidden, tc["idx"], tc["w"], q(routed, 0, 0), q(routed, 0, 1),
+                                      q(routed, 1, 0), q(routed, 1, 1), q(routed, 2, 0), q(routed, 2, 1), **mx)
+    np.testing.assert_allclose(again, tc["out"], rtol=1e-12, atol=1e-14)
