@@ -442,8 +442,8 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_perm,
  * With p->expert_dtype == MOE_EXPERT_FP8_E4M3 (or MOE_EXPERT_MXFP4) every
  * expert (routed and shared) reads its codes and scales from `w` and the
  * expert GEMMs run on fp16 activations (see moe_expert_dtype_t).
- * Decode-sized token-choice batches (moe_layer_small_batch) compute the same
- * expert FFNs on the CUDA cores instead of the grouped GEMMs.
+ * Decode-sized token-choice batches (moe_layer_small_batch) run the whole
+ * layer as one kernel instead; its result is reproducible bit for bit.
  */
 moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
                                const void* hidden, void* out,
@@ -459,10 +459,9 @@ moe_status_t moe_layer_forward(const moe_problem_t* p, const moe_weights_t* w,
  *                 0 router+top-K, 1 route and pack, 2 GEMM schedule (built
  *                 inside route and pack: an empty stage),
  *                 3 gate/up GEMM + SwiGLU, 4 down GEMM + weighted scatter-add,
- *                 5 fp32 -> bf16 finalise. On the CUDA-core path of a
- *                 decode-sized batch (moe_layer_small_batch) stages 3 and 4
- *                 are its two kernels, the rounding happens inside stage 4
- *                 and stage 5 is empty.
+ *                 5 fp32 -> bf16 finalise. A decode-sized batch
+ *                 (moe_layer_small_batch) is one kernel: stage 0 holds it
+ *                 and stages 1 to 5 are empty.
  * Used by the benchmark to time each kernel inside the timed region.
  */
 #define MOE_LAYER_STAGES 6
@@ -479,18 +478,25 @@ moe_status_t moe_layer_forward_profiled(const moe_problem_t* p, const moe_weight
 int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights_t* w);
 
 /*
- * 1 if moe_layer_forward runs problem p's expert FFNs on the CUDA cores
- * (a decode-sized token-choice batch: T <= 4 tokens with bf16 experts, one
- * token with FP8 experts; never for MXFP4 experts), 0 if on the grouped
- * tensor-core GEMMs, -1 if p is invalid. Host only, no CUDA call.
+ * 1 if moe_layer_forward runs problem p as one decode-sized kernel, 0 if
+ * through the router, route-and-pack and grouped tensor-core GEMM kernels, -1
+ * if p is invalid. Host only, no CUDA call. The one-kernel path takes
+ * token-choice batches of T <= 4 tokens with bf16 or FP8 E4M3 experts (not
+ * MXFP4) whose routing tables and staged rows fit its shared memory.
  * With T tokens an expert holds at most T rows ("Part 12", "What happens when
  * many users share the GPU?": each token reads its own experts' weights, and
  * the bytes, not the arithmetic, set the time at small batch; "Mixture of
  * Experts Explained", "Why batching erodes the advantage"). A 128-row tensor
- * tile would then be almost all padding, so each touched weight row is instead
- * streamed from HBM once by the CUDA cores and dotted with its expert's rows
- * (fp32 products and sums; h rounded to bf16, or fp16 for FP8 experts, as on
- * the GEMM path). Same inputs, outputs, workspace and status codes.
+ * tile would then be almost all padding, and the launches and hand-offs
+ * between kernels cost as much as the router. So one cooperative kernel (one
+ * CTA per SM) computes the router, top-K, routing, the gate/up rows and SwiGLU,
+ * then, after a grid-wide barrier, the down rows and the weighted combine;
+ * each touched weight row is streamed from HBM once. Products are exact and
+ * sums fp32 on the tensor cores (mma.sync, the token rows padded to 16); h is
+ * rounded to bf16, or fp16 for FP8 experts, as on the GEMM path. Same inputs,
+ * outputs, workspace and status codes; the output is the same from run to run.
+ * The grid barriers use two words at byte 128 of the workspace's first 256
+ * bytes (zeroed with the error word; the kernel leaves them at zero).
  */
 int32_t moe_layer_small_batch(const moe_problem_t* p);
 

@@ -81,8 +81,6 @@ struct PermuteArgs {
   uint8_t* xq_sh;
   float* sx_sh;
   uint32_t* err;
-  // Only the histogram, scans, scatter (and schedule): no row copy.
-  bool route_only;
   // Optional: also build the GEMM schedule (as launch_schedule) from the new
   // offsets; skipped when groups == nullptr.
   GroupDesc* groups;
@@ -181,49 +179,74 @@ struct F8Maps {
 cudaError_t launch_gather_quant(const PermuteArgs& a, int64_t rows, int64_t shared_rows, cudaStream_t s);
 cudaError_t launch_act_quant(const void* src, int64_t rows, int32_t K, uint8_t* dst, float* scale,
                              cudaStream_t s);
-// The expert FFNs of a decode-sized token-choice batch on the CUDA cores
-// (small_batch.cu): every group holds at most max_rows (<= 4; 1 for FP8
-// experts) rows, so each weight row is streamed from HBM once and dotted with
-// the group's rows.
-enum SmallBatchFormat { kSmallBf16 = 0, kSmallE4M3 = 1 };
-constexpr int kSmallBatchMaxRows = 4;
-// The gate/up kernel stages the batch's T token rows as fp32 in shared memory.
-constexpr size_t kSmallBatchMaxSmem = 192u << 10;
-struct SmallBatchArgs {
-  int32_t fmt;               // SmallBatchFormat of the expert weights
-  int32_t max_rows;          // bound on any group's rows (1..kSmallBatchMaxRows)
-  int32_t N, S, d, F, Fs, K;
+// ---------------------------------------------------------------- decode-sized batches in one kernel
+// decode_layer.cu: router, top-K, routing, gate/up + SwiGLU, down and the
+// weighted combine of a token-choice batch of at most kDecodeMaxTokens tokens
+// in one cooperative launch of one 512-thread CTA per SM.
+// Storage format of the expert matrices on this path.
+enum DecodeFormat { kDecodeBf16 = 0, kDecodeE4M3 = 1 };
+constexpr int kDecodeThreads = 512;
+constexpr int kDecodeMaxTokens = 4;
+constexpr int kDecodeMaxSplits = 128;     // router partials (slices of d)
+constexpr int kDecodeMaxGrid = 256;       // workspace bound on the grid (SMs)
+constexpr size_t kDecodeMaxSmem = 200u << 10;
+constexpr size_t kDecodeSyncOffset = 128;  // grid-barrier counters: bytes into the workspace's error block
+
+struct DecodePlan {
+  bool ok;            // the problem fits the kernel (token choice, T <= 4, shared memory)
+  int grid, rsplits, r_slice;
+  int x_stride;       // shared-memory row stride of the token rows (elements)
+  int z_len;          // elements of the zero row
+  int h_stride, hs_stride;  // row strides of h and of the shared experts' h (elements, padded)
+  int hsm_stride;           // shared-memory row stride of the staged h rows (elements)
+  size_t smem_x_bytes, smem_bytes;
+};
+DecodePlan decode_plan(const moe_problem_t& p, int sms);
+// Floats of the down phase's per-group results (workspace).
+size_t decode_ybuf_floats(const moe_problem_t& p);
+// 16-bit elements of the kernel's h rows (routed, or shared), padded rows.
+size_t decode_h_elems(const moe_problem_t& p, bool shared);
+
+struct DecodeArgs {
   int64_t T;
-  int64_t routed_rows;       // T * K: bounds the experts that can hold rows
-  const GroupDesc* groups;   // [N + S], built by the route kernels
-  const void* hidden;        // [T][d] the layer's input rows (a packed row's token via perm_src)
-  bool hidden_bf16;          // bf16 hidden, else fp32
-  const void* w_gate;        // codes [N][F][d], [N][F][d], [N][d][F] (bf16 or E4M3)
+  int32_t d, N, K, F, S, Fs;
+  int32_t score_fn, renormalize, n_groups, topk_groups;
+  int32_t capacity;            // copies an expert keeps (token order); INT32_MAX: no cap
+  int32_t fmt;                 // DecodeFormat of the expert weights
+  const void* hidden;          // [T][d] bf16 or fp32
+  bool hidden_bf16;
+  const float* w_router;       // [d][N]
+  const float* router_bias;    // [N] or null (added to every logit)
+  const float* sel_bias;       // [N] or null (selection only, sigmoid)
+  const void* w_gate;          // [N][F][d] (bf16 or E4M3 codes)
   const void* w_up;
-  const void* w_down;
-  const void* s_gate;        // shared experts: [S][Fs][d], [S][Fs][d], [S][d][Fs]
+  const void* w_down;          // [N][d][F]
+  const void* s_gate;          // shared: [S][Fs][d], [S][Fs][d], [S][d][Fs]
   const void* s_up;
   const void* s_down;
-  // FP8: fp32 scale per weight row; unused for bf16
-  const void* w_gate_scale;
+  const void* w_gate_scale;    // FP8: fp32 per weight row
   const void* w_up_scale;
   const void* w_down_scale;
   const void* s_gate_scale;
   const void* s_up_scale;
   const void* s_down_scale;
-  void* h;                   // [rows][F] SiLU(g) * u: bf16, or fp16 for FP8 experts
-  void* h_sh;                // [S*T][Fs]
-  float* out_acc;            // [T][d] fp32 (cleared by phase 0)
-  __nv_bfloat16* out;        // [T][d] bf16(out_acc), written by phase 1's last CTA
-  uint32_t* done;            // phase 1's count of finished CTAs (reset by phase 0)
-  const int32_t* perm_src;   // [rows] packed row -> t*K + k
-  const float* topk_w;       // [T*K]
+  __nv_bfloat16* out;          // [T][d]
+  int32_t* topk_idx;           // [T][K]
+  float* topk_w;               // [T][K]
+  int32_t* counts;             // [N] or null
+  float* router_part;          // [rsplits][T][N]
+  void* h;                     // [T*K][h_stride] 16-bit activation format
+  void* h_sh;                  // [S*T][hs_stride]
+  float* bnd_val;              // [grid*16 + 1][2][64] halves of gate/up groups split between warps
+  uint32_t* bnd_cnt;           // [grid*16 + 1]
+  float* ybuf;                 // [d/8][entries][2][64] down groups' results
+  uint32_t* blk_cnt;           // [d/8] steps done per output block
+  uint32_t* sync;              // two zeroed words (barrier count, exit count)
   uint32_t* err;
+  int32_t grid, rsplits, r_slice, x_stride, z_len, h_stride, hs_stride, hsm_stride;
+  size_t smem_x_bytes, smem_bytes;
 };
-// phase 0: h = SiLU(x W_gate^T) * (x W_up^T) with x each packed row's token
-// row of hidden, rounded to the activation format; out_acc = 0.
-// phase 1: out_acc[t] += w * h W_down^T, then out = bf16(out_acc).
-cudaError_t launch_small_batch_ffn(const SmallBatchArgs& a, int phase, cudaStream_t s);
+cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t s);
 
 // uint8 row-major matrix [rows][inner] as a TMA tensor map: box
 // [box_rows][128 bytes], 128-byte swizzle, zero fill out of bounds. The row

@@ -54,6 +54,7 @@ struct Layout {
   size_t err, chunk, groups, ts_gu, ts_dn, router, router_w3, ec_scores, ec_token, ec_w;
   size_t topk_idx, topk_w, counts, offsets, perm_src, inv_row, x_perm, x_act, h, h_sh, out_acc, done;
   size_t y_rows, y_sh;  // token choice with a large accumulator: the down GEMM's stored rows (see stored_combine)
+  size_t dec_part, dec_bnd_val, dec_bnd_cnt, dec_ybuf, dec_blk, dec_h, dec_h_sh;  // decode-sized batches
   size_t xq, sx, hq, sh, xq_sh, sx_sh, hq_sh, sh_sh;  // FP8 / MXFP4 experts: two-term E4M3 activations + row scales
   MxOffsets mx;  // MXFP4 experts: the per-call preparation of the weights in use
   size_t total;
@@ -91,17 +92,17 @@ bool needs_act_copy(const moe_problem_t& p) {
   return p.n_shared > 0 && (is_lowp(p) || p.hidden_dtype == MOE_F32);
 }
 
-// Token-choice batches of at most this many tokens run the expert FFNs on the
-// CUDA cores (small_batch.cu), one pass over each touched weight row, instead
-// of the grouped GEMMs: each expert then holds at most T rows. The bounds are
-// measured: bf16 weights gain up to 4 tokens; FP8 codes only for a single
-// token, since widening them to fp32 costs ALU time that grows with the rows;
-// MXFP4 codes never (the tensor-core path is faster even for one token).
-int32_t small_batch_rows(const moe_problem_t& p) {
-  if (p.routing != MOE_ROUTING_TOKEN_CHOICE || p.T < 1 || stored_combine(p) || is_mx(p)) return 0;
-  if ((size_t)p.T * p.d_model * 4 > kSmallBatchMaxSmem) return 0;  // token rows staged in shared memory
-  const int64_t max_t = is_fp8(p) ? 1 : kSmallBatchMaxRows;
-  return p.T <= max_t ? (int32_t)p.T : 0;
+// Token-choice batches of at most kDecodeMaxTokens tokens with bf16 or FP8
+// experts run as one kernel (decode_layer.cu) when its routing tables and
+// staged rows fit the kernel's shared memory: each expert then holds at most
+// T rows, and a 128-row GEMM tile would be almost all padding. MXFP4 experts,
+// expert choice and larger batches run on the grouped GEMMs. The decision
+// takes no CUDA call: the shared memory is sized for a grid of at least
+// kDecodePlanSms CTAs (the real grid only needs less).
+constexpr int kDecodePlanSms = 100;
+bool decode_fused(const moe_problem_t& p) {
+  if (p.routing != MOE_ROUTING_TOKEN_CHOICE || p.T < 1 || p.T > kDecodeMaxTokens || is_mx(p)) return false;
+  return decode_plan(p, kDecodePlanSms).ok;
 }
 
 Layout make_layout(const moe_problem_t& p, int call) {
@@ -159,6 +160,15 @@ Layout make_layout(const moe_problem_t& p, int call) {
     if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
     L.out_acc = take((size_t)T * p.d_model * 4);
     L.done = take(4);
+    if (T <= kDecodeMaxTokens) {
+      L.dec_part = take((size_t)kDecodeMaxSplits * T * p.n_experts * 4);
+      L.dec_bnd_val = take((size_t)(kDecodeMaxGrid * (kDecodeThreads / 32) + 1) * 128 * 4);
+      L.dec_bnd_cnt = take((size_t)(kDecodeMaxGrid * (kDecodeThreads / 32) + 1) * 4);
+      L.dec_ybuf = take(decode_ybuf_floats(p) * 4);
+      L.dec_blk = take((size_t)(p.d_model / 8) * 4);
+      L.dec_h = take(decode_h_elems(p, false) * 2);
+      if (p.n_shared > 0) L.dec_h_sh = take(decode_h_elems(p, true) * 2);
+    }
     if (stored_combine(p)) {
       L.y_rows = take((size_t)TK * p.d_model * 2);
       if (p.n_shared > 0) L.y_sh = take((size_t)p.n_shared * T * p.d_model * 2);
@@ -1056,6 +1066,75 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     return record(ev, 6, s);
   }
 
+  if (decode_fused(*p)) {
+    // decode-sized batch: the whole layer in one cooperative kernel
+    if (!aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (sms > kDecodeMaxGrid) sms = kDecodeMaxGrid;
+    const DecodePlan pl = decode_plan(*p, sms);
+    if (!pl.ok) return MOE_ERR_UNSUPPORTED;
+    DecodeArgs da{};
+    da.T = T;
+    da.d = p->d_model;
+    da.N = N;
+    da.K = K;
+    da.F = p->ffn;
+    da.S = S;
+    da.Fs = p->shared_ffn;
+    da.score_fn = p->score_fn;
+    da.renormalize = p->renormalize;
+    da.n_groups = p->n_groups;
+    da.topk_groups = p->topk_groups;
+    da.capacity = expert_capacity(*p);
+    da.fmt = is_fp8(*p) ? kDecodeE4M3 : kDecodeBf16;
+    da.hidden = hidden;
+    da.hidden_bf16 = hbf16;
+    da.w_router = w->w_router;
+    da.router_bias = w->router_bias;
+    da.sel_bias = w->sel_bias;
+    da.w_gate = w->w_gate;
+    da.w_up = w->w_up;
+    da.w_down = w->w_down;
+    da.s_gate = w->ws_gate;
+    da.s_up = w->ws_up;
+    da.s_down = w->ws_down;
+    da.w_gate_scale = w->w_gate_scale;
+    da.w_up_scale = w->w_up_scale;
+    da.w_down_scale = w->w_down_scale;
+    da.s_gate_scale = w->ws_gate_scale;
+    da.s_up_scale = w->ws_up_scale;
+    da.s_down_scale = w->ws_down_scale;
+    da.out = static_cast<__nv_bfloat16*>(out);
+    da.topk_idx = topk_idx;
+    da.topk_w = topk_w;
+    da.counts = counts;
+    da.router_part = at<float>(ws, L.dec_part);
+    da.h = at<void>(ws, L.dec_h);
+    da.h_sh = S > 0 ? at<void>(ws, L.dec_h_sh) : nullptr;
+    da.bnd_val = at<float>(ws, L.dec_bnd_val);
+    da.bnd_cnt = at<uint32_t>(ws, L.dec_bnd_cnt);
+    da.ybuf = at<float>(ws, L.dec_ybuf);
+    da.blk_cnt = at<uint32_t>(ws, L.dec_blk);
+    da.sync = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + L.err + kDecodeSyncOffset);
+    da.err = err;
+    da.grid = pl.grid;
+    da.rsplits = pl.rsplits;
+    da.r_slice = pl.r_slice;
+    da.x_stride = pl.x_stride;
+    da.z_len = pl.z_len;
+    da.h_stride = pl.h_stride;
+    da.hs_stride = pl.hs_stride;
+    da.hsm_stride = pl.hsm_stride;
+    da.smem_x_bytes = pl.smem_x_bytes;
+    da.smem_bytes = pl.smem_bytes;
+    MOE_TRY(record(ev, 0, s));
+    MOE_TRY(cuda_status(launch_decode_layer(da, s)));
+    for (int i = 1; i <= 6; ++i) MOE_TRY(record(ev, i, s));
+    return MOE_OK;
+  }
+
   // 1. router, scoring, top-K, gate weights
   MOE_TRY(record(ev, 0, s));
   if (!aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
@@ -1087,16 +1166,7 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
   pa.act_f16 = fp8;
   pa.err = err;
-  const int32_t small_rows = small_batch_rows(*p);
-  if (small_rows) {
-    // the CUDA-core FFNs read the tokens' rows from hidden and clear the
-    // accumulator themselves: routing only
-    pa.route_only = true;
-    pa.zero_rows = nullptr;
-    pa.x_act = nullptr;
-  } else if (fp8) {
-    set_gather_quant(&pa, ws, L, S > 0);
-  }
+  if (fp8) set_gather_quant(&pa, ws, L, S > 0);
   // 3. the GEMM schedule (routed experts from offsets, then the shared
   //    experts) is built by the same kernel that finishes the prefix sums
   const int32_t tile_rows = gemm_tile_rows(*p, T * K);
@@ -1111,51 +1181,6 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   MOE_TRY(cuda_status(launch_permute(pa, s)));
   MOE_TRY(record(ev, 2, s));
   MOE_TRY(record(ev, 3, s));
-
-  if (small_rows) {
-    // 4-5. decode-sized batch: SwiGLU and the weighted scatter-add on the CUDA
-    // cores, each touched weight row streamed once
-    SmallBatchArgs sb{};
-    sb.fmt = is_fp8(*p) ? kSmallE4M3 : kSmallBf16;
-    sb.max_rows = small_rows;
-    sb.N = N;
-    sb.S = S;
-    sb.d = p->d_model;
-    sb.F = p->ffn;
-    sb.Fs = p->shared_ffn;
-    sb.K = K;
-    sb.T = T;
-    sb.routed_rows = T * K;
-    sb.groups = pa.groups;
-    sb.hidden = hidden;
-    sb.hidden_bf16 = hbf16;
-    sb.w_gate = w->w_gate;
-    sb.w_up = w->w_up;
-    sb.w_down = w->w_down;
-    sb.s_gate = w->ws_gate;
-    sb.s_up = w->ws_up;
-    sb.s_down = w->ws_down;
-    sb.w_gate_scale = w->w_gate_scale;
-    sb.w_up_scale = w->w_up_scale;
-    sb.w_down_scale = w->w_down_scale;
-    sb.s_gate_scale = w->ws_gate_scale;
-    sb.s_up_scale = w->ws_up_scale;
-    sb.s_down_scale = w->ws_down_scale;
-    sb.h = at<void>(ws, L.h);
-    sb.h_sh = S > 0 ? at<void>(ws, L.h_sh) : nullptr;
-    sb.out_acc = at<float>(ws, L.out_acc);
-    sb.out = static_cast<__nv_bfloat16*>(out);
-    sb.done = at<uint32_t>(ws, L.done);
-    sb.perm_src = pa.perm_src;
-    sb.topk_w = topk_w;
-    sb.err = err;
-    MOE_TRY(cuda_status(launch_small_batch_ffn(sb, 0, s)));
-    MOE_TRY(record(ev, 4, s));
-    // 6. (the down kernel's last CTA rounds the accumulator to the output)
-    MOE_TRY(cuda_status(launch_small_batch_ffn(sb, 1, s)));
-    MOE_TRY(record(ev, 5, s));
-    return record(ev, 6, s);
-  }
 
   // 4-5. grouped SwiGLU GEMMs with the fused weighted scatter-add
   GemmPlan g{};
@@ -1302,13 +1327,14 @@ int32_t moe_layer_forward_kernel_count(const moe_problem_t* p, const moe_weights
   if (p->routing == MOE_ROUTING_EXPERT_CHOICE) return router + 3 + 3 + quant;  // + select, gather, schedule
   const int route = (p->T + kTokensPerChunk - 1) / kTokensPerChunk <= 32 ? 2 : 4;
   // routing without the row copy; gate/up and down (+ finalise) on the CUDA cores
-  if (small_batch_rows(*p)) return router + 1 + 2;
+  if (decode_fused(*p)) return 1;  // the whole layer in one kernel
+
   return router + route + 3 + quant;
 }
 
 int32_t moe_layer_small_batch(const moe_problem_t* p) {
   if (moe_problem_check(p) != MOE_OK) return -1;
-  return small_batch_rows(*p) > 0 ? 1 : 0;
+  return decode_fused(*p) ? 1 : 0;
 }
 
 moe_status_t moe_get_device_status(void* ws, void* stream) {

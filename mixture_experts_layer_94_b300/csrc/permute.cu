@@ -479,7 +479,6 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s) {
     if (const cudaError_t le_ = launch(route_scan_kernel, 1, 1024, 0, s, a); le_ != cudaSuccess) return le_;
     if (const cudaError_t le_ = launch(route_scatter_kernel, (unsigned)((a.C + kScatterWarps - 1) / kScatterWarps), kScatterWarps * 32, 0, s, a); le_ != cudaSuccess) return le_;
   }
-  if (a.route_only) return cudaSuccess;
   if (a.xq) return launch_gather_quant(a, a.T * a.K, a.xq_sh ? a.T : 0, s);
   return launch_gather(a, a.T * a.K, s);
 }

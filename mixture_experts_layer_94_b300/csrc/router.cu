@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -336,83 +337,14 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    float l = lg[i];
     if (valid[i]) {
-      if (a.router_bias) l += a.router_bias[e];
-      if (a.logits) a.logits[t * N + e] = l;
-    }
-    if (a.score_fn == 0) {
-      sc[i] = l;
-      key[i] = l;
-    } else {
-      const float sg = 1.0f / (1.0f + expf(-l));
-      sc[i] = sg;
-      key[i] = sg + ((valid[i] && a.sel_bias) ? a.sel_bias[e] : 0.f);
+      if (a.router_bias) lg[i] += a.router_bias[e];
+      if (a.logits) a.logits[t * N + e] = lg[i];
     }
   }
-  if (a.n_groups > 1 && a.topk_groups < a.n_groups) {
-    // Group-limited routing: a group's score is the sum of its two largest
-    // keys; keep the topk_groups best groups (score desc, group asc) and pick
-    // experts only from them.
-    const int G = a.n_groups, gs = N / G;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (valid[i]) s_key[warp][lane + 32 * i] = key[i];
-    __syncwarp();
-    float gsc[kMaxExperts / 32];
-#pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-      const int g = lane + 32 * j;
-      float b1 = -INFINITY, b2 = -INFINITY;
-      if (g < G) {
-        for (int e = g * gs; e < (g + 1) * gs; ++e) {
-          const float v = s_key[warp][e];
-          if (v > b1) {
-            b2 = b1;
-            b1 = v;
-          } else if (v > b2) {
-            b2 = v;
-          }
-        }
-        gsc[j] = gs > 1 ? b1 + b2 : b1;
-        s_kept[warp][g] = 0;
-      } else {
-        gsc[j] = -INFINITY;
-      }
-    }
-    uint32_t gtaken = 0;
-    for (int r = 0; r < a.topk_groups; ++r) {
-      float bv = -INFINITY;
-      int bg = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < kMaxExperts / 32; ++j) {
-        const int g = lane + 32 * j;
-        if (g < G && !((gtaken >> j) & 1u) && (gsc[j] > bv || (gsc[j] == bv && g < bg))) {
-          bv = gsc[j];
-          bg = g;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int og = __shfl_xor_sync(0xffffffffu, bg, off);
-        if (ov > bv || (ov == bv && og < bg)) {
-          bv = ov;
-          bg = og;
-        }
-      }
-      if (lane == (bg & 31)) {
-        gtaken |= 1u << (bg >> 5);
-        s_kept[warp][bg] = 1;
-      }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (valid[i] && !s_kept[warp][e / gs]) valid[i] = false;
-    }
-  }
+  router_scores<EPL>(lg, valid, lane, a.score_fn, a.sel_bias, sc, key);
+  if (a.n_groups > 1 && a.topk_groups < a.n_groups)
+    router_group_limit<EPL>(key, valid, lane, N, a.n_groups, a.topk_groups, s_key[warp], s_kept[warp]);
   if (a.scores_t) {
     // Expert choice: the token's score for every expert, stored transposed
     // (S[e][t]) for the per-expert selection.
@@ -443,62 +375,9 @@ __global__ void __launch_bounds__(kWarps * 32) topk_kernel(const RouterArgs a) {
       if (valid[i]) a.scores_t[(int64_t)(lane + 32 * i) * a.T + t] = sv[i];
     return;
   }
-  uint32_t taken = 0;
-  int my_e = -1;
-  float my_sc = 0.f;
-  for (int k = 0; k < K; ++k) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (valid[i] && !((taken >> i) & 1u) && (key[i] > bv || (key[i] == bv && e < be))) {
-        bv = key[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    const int owner = be & 31, slot = be >> 5;
-    float v = 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (i == slot) v = sc[i];
-    if (lane == owner) taken |= 1u << slot;
-    v = __shfl_sync(0xffffffffu, v, owner);
-    if (lane == k) {
-      my_e = be;
-      my_sc = v;
-    }
-  }
+  int my_e;
   float w;
-  if (a.score_fn == 0) {
-    const float lmax = __shfl_sync(0xffffffffu, my_sc, 0);  // slot 0 holds the largest logit
-    const float ex = (lane < K) ? expf(my_sc - lmax) : 0.f;
-    float z = 0.f;
-    if (a.renormalize) {
-      z = ex;
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (valid[i]) z += expf(sc[i] - lmax);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    w = ex / z;
-  } else {
-    float z = (lane < K) ? my_sc : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    w = a.renormalize ? my_sc / z : my_sc;
-  }
+  router_select<EPL>(sc, key, valid, lane, K, a.score_fn, a.renormalize, my_e, w);
   if (lane < K) {
     a.topk_idx[t * K + lane] = my_e;
     a.topk_w[t * K + lane] = w;

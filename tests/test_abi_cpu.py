@@ -82,34 +82,32 @@ def test_layer_kernel_count():
     assert B.layer_forward_kernel_count(B.problem(inputs.MIXTRAL, top_k=0)) == 0
 
 
-def test_decode_sized_batches_take_the_cuda_core_expert_path():
-    # token choice with T <= 4 bf16 experts or one token with FP8 experts runs
-    # the expert FFNs on the CUDA cores; larger batches, MXFP4 experts and
-    # expert choice keep the GEMMs
+def test_decode_sized_batches_run_as_one_kernel():
+    # token choice with T <= 4 and bf16 or FP8 experts runs the whole layer as
+    # one kernel; larger batches, MXFP4 experts and expert choice keep the
+    # router, route-and-pack and grouped GEMM kernels
     q = inputs.QWEN_DECODE
     for T, want in ((1, True), (2, True), (4, True), (5, False), (8, False), (0, False)):
         assert B.layer_small_batch(B.problem(q, T=T)) == want, T
-    for T, want in ((1, True), (2, False)):
+    for T, want in ((1, True), (4, True), (5, False)):
         assert B.layer_small_batch(B.problem(inputs.QWEN_DECODE_FP8, T=T)) == want, T
     assert not B.layer_small_batch(B.problem(inputs.QWEN_DECODE_MXFP4, T=1))
     assert not B.layer_small_batch(B.problem(inputs.MIXTRAL_EC, T=2))
-    # the gate/up kernel stages the T token rows as fp32 in 192 KB of shared memory
+    # the staged token rows and h rows must fit the kernel's shared memory
     assert B.layer_small_batch(B.problem(q, T=1, d_model=16384))
-    assert not B.layer_small_batch(B.problem(q, T=4, d_model=16384))
+    assert not B.layer_small_batch(B.problem(q, T=4, d_model=16384, top_k=32, ffn=4096))
     with pytest.raises(ValueError):
         B.layer_small_batch(B.problem(q, top_k=0))
-    # router (CUDA-core logits + top-K), routing (one CTA, no row copy), gate/up,
-    # down (its last CTA writes the bf16 output): no activation splits
     for cfg in (q, inputs.QWEN_DECODE_FP8, q.with_(S=1, Fs=512, hidden_dtype="f32")):
-        assert B.layer_forward_kernel_count(B.problem(cfg, T=1)) == 5, cfg.name
-    # the GEMM path adds the split of h (FP8), or of h and the MXFP4 preparation
-    assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_FP8, T=2)) == 8
+        assert B.layer_forward_kernel_count(B.problem(cfg, T=1)) == 1, cfg.name
+    # the GEMM path: router, routing, gather + activation split, gate/up, split of h, down, finalise
+    assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_FP8, T=5)) == 8
     assert B.layer_forward_kernel_count(B.problem(inputs.QWEN_DECODE_MXFP4, T=1)) == 11
 
 
-def test_small_batch_decision_agrees_with_the_launch_count():
-    # over random valid problems: the CUDA-core path runs router + routing +
-    # two kernels, never the activation splits, MXFP4 preparation or finalise
+def test_one_kernel_decision_agrees_with_the_launch_count():
+    # over random valid problems: the one-kernel path is token choice, T <= 4,
+    # bf16 or FP8 experts, and launches exactly one kernel
     import numpy as np
 
     rng = np.random.default_rng(0)
@@ -127,12 +125,13 @@ def test_small_batch_decision_agrees_with_the_launch_count():
         p = B.problem(cfg)
         if B.problem_check(p) != B.MOE_OK:
             continue
-        small = B.layer_small_batch(p)
-        seen.add(small)
-        if small:
-            assert cfg.routing == "token" and 1 <= cfg.T <= (1 if fmt == "fp8" else 4) and fmt != "mxfp4"
-            router = 2  # T <= 64: CUDA-core logits + top-K
-            assert B.layer_forward_kernel_count(p) == router + 1 + 2
+        one = B.layer_small_batch(p)
+        seen.add(one)
+        if one:
+            assert cfg.routing == "token" and 1 <= cfg.T <= 4 and fmt != "mxfp4"
+            assert B.layer_forward_kernel_count(p) == 1
+        else:
+            assert cfg.T == 0 or B.layer_forward_kernel_count(p) > 1
     assert seen == {True, False}
 
 

@@ -51,6 +51,11 @@ MID = {
     # a small batch with a capacity limit and a shared expert
     "fp8_small_capacity_shared": _cfg("fp8_small_capacity_shared", T=4, d=144, N=8, K=3, F=80, S=1, Fs=48,
                                       hidden_dtype="f32", capacity_factor=0.5),
+    # one-kernel decode batches of 2 and 4 tokens: sigmoid with a group limit;
+    # an FFN wider than d (whole 64-code steps and a ragged last one)
+    "fp8_decode_T4_grouped": _cfg("fp8_decode_T4_grouped", T=4, d=512, N=64, K=6, F=208, S=1, Fs=144,
+                                  score="sigmoid", sel_bias_var=0.1, n_groups=8, topk_groups=3),
+    "fp8_decode_T2_wide": _cfg("fp8_decode_T2_wide", T=2, d=160, N=16, K=4, F=1040),
     # T*K >= 8192 copies: each token's row is split once and stored to its K packed rows
     # (d / 8 = 34 vectors: a partial last trip of the warp's loop; fp32 hidden, a shared
     # expert and a capacity limit)
@@ -180,8 +185,8 @@ def test_fp8_activation_overflow_is_reported():
 
 
 def test_fp8_single_token_activation_overflow_is_reported():
-    """The same report on the one-token path, whose CUDA-core FFNs round the
-    token's hidden row to fp16 themselves (no staged copy)."""
+    """The same report on the one-kernel decode path, which rounds the token's
+    hidden row to fp16 itself (no staged copy)."""
     cfg = MID["fp8_T1_shared_f32"]
     ins, dev = H.make_case(cfg)
     layer = B.MoELayer(cfg, dev)
@@ -229,7 +234,7 @@ def _sample_rows(T, n, seed=0):
 
 
 FULL = [("mixtral_fp8", inputs.MIXTRAL_FP8, 64)] + [
-    (f"qwen_decode_fp8_T{T}", inputs.QWEN_DECODE_FP8.with_(T=T), 64) for T in inputs.DECODE_BATCHES]
+    (f"qwen_decode_fp8_T{T}", inputs.QWEN_DECODE_FP8.with_(T=T), 64) for T in inputs.DECODE_BATCHES + (2, 4)]
 
 
 @pytest.mark.parametrize("name,cfg,n_sample", FULL, ids=[f[0] for f in FULL])

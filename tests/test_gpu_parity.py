@@ -58,6 +58,19 @@ MID = {
                                                   Fs=40, hidden_dtype="f32", score="sigmoid",
                                                   capacity_factor=0.5),
     "small_T2_ragged": inputs.MoEConfig("small_T2_ragged", T=2, d=200, N=32, K=4, F=104),
+    # more one-kernel decode shapes: a single expert, K = N (a dense mixture),
+    # no renormalisation, an FFN much wider than d with a wider shared expert,
+    # 256 experts under a group limit, a d long enough for several router
+    # loads per thread
+    "decode_N1_K1_T2": inputs.MoEConfig("decode_N1_K1_T2", T=2, d=128, N=1, K=1, F=256),
+    "decode_K_equals_N_T3": inputs.MoEConfig("decode_K_equals_N_T3", T=3, d=128, N=4, K=4, F=136),
+    "decode_no_renorm_sigmoid_T4": inputs.MoEConfig("decode_no_renorm_sigmoid_T4", T=4, d=192, N=12, K=3, F=96,
+                                                    score="sigmoid", renormalize=0),
+    "decode_wide_ffn_T2": inputs.MoEConfig("decode_wide_ffn_T2", T=2, d=128, N=8, K=2, F=1000, S=1, Fs=1200),
+    "decode_256_grouped_T4": inputs.MoEConfig("decode_256_grouped_T4", T=4, d=512, N=256, K=8, F=128, S=1,
+                                              Fs=128, score="sigmoid", sel_bias_var=0.1, zipf=1.1, n_groups=8,
+                                              topk_groups=4),
+    "decode_long_d_T1": inputs.MoEConfig("decode_long_d_T1", T=1, d=16384, N=4, K=2, F=64, hidden_dtype="f32"),
     # T*K >= 8192 copies: the token-major row copy (ragged d; fp32 hidden with a shared
     # expert and a capacity limit)
     "scatter_copy_ragged": inputs.MoEConfig("scatter_copy_ragged", T=2100, d=264, N=16, K=4, F=136),
@@ -366,8 +379,8 @@ def _sample_rows(T, n, seed=0):
 FULL = [("mixtral", inputs.MIXTRAL, 64), ("gptoss", inputs.GPTOSS, 64), ("dsv3", inputs.DSV3, 64),
         ("dsv3_grouped", inputs.DSV3_GROUPED, 64), ("mixtral_capacity", inputs.MIXTRAL_CAPACITY, 64)] + [
     (f"qwen_decode_T{T}", inputs.QWEN_DECODE.with_(T=T), 64) for T in inputs.DECODE_BATCHES] + [
-    # the largest batches of the CUDA-core expert path (2 and 4 rows per expert)
-    (f"qwen_decode_T{T}_cuda_cores", inputs.QWEN_DECODE.with_(T=T), 4) for T in (2, 4)]
+    # the one-kernel decode path at 2 and 4 tokens
+    (f"qwen_decode_T{T}_one_kernel", inputs.QWEN_DECODE.with_(T=T), 4) for T in (2, 4)]
 
 
 @pytest.mark.parametrize("name,cfg,n_sample", FULL, ids=[f[0] for f in FULL])
