@@ -74,6 +74,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's batch T (a smaller case of the same shapes, e.g. for a profiler)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the number of routed experts N (a smaller weight set of the same shapes, "
+                         "e.g. for a profiler capture that must hold little device memory)")
     ap.add_argument("--mx-per-call", action="store_true",
                     help="MXFP4 experts: every step prepares the block scales of the experts it uses "
                          "(default: prepared once when the layer is built, as a server loads weights)")
@@ -610,6 +613,11 @@ def main():
     cfg, desc = WORKLOADS[args.workload]
     if args.tokens is not None:
         cfg, desc = cfg.with_(T=args.tokens), f"{desc}, T={args.tokens}"
+    if args.experts is not None:
+        groups = cfg.n_groups if cfg.n_groups and args.experts % cfg.n_groups == 0 else 0
+        cfg = cfg.with_(N=args.experts, K=min(cfg.K, args.experts), n_groups=groups,
+                        topk_groups=cfg.topk_groups if groups else 0)
+        desc = f"{desc}, N={args.experts}"
     if args.impl == "reference":
         # the oracle runs on the host cores: no GPU or process group is needed;
         # under torchrun only rank 0 runs and prints
