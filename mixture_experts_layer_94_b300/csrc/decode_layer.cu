@@ -367,18 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
     float* psum = red + pairs;  // [P][pairs]
     int P = 1;
     while (P * 2 * pairs <= kThreads && P * 2 <= a.rsplits) P *= 2;
+    // (up to 64 loads per thread in one batch: one L2 round trip for the
+    // partials of up to 4 tokens of 128 experts)
     for (int i = tid; i < P * pairs; i += kThreads) {
       const int p = i / pairs, pr = i - p * pairs;
       float s = 0.f;
-      for (int sp0 = p; sp0 < a.rsplits; sp0 += 16 * P) {
-        float v[16];
+      for (int sp0 = p; sp0 < a.rsplits; sp0 += 64 * P) {
+        float v[64];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 64; ++u) {
           const int sp = sp0 + u * P;
           v[u] = sp < a.rsplits ? __ldcg(a.router_part + (int64_t)sp * pairs + pr) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) s += v[u];
+        for (int u = 0; u < 64; ++u) s += v[u];
       }
       psum[i] = s;
     }
@@ -527,17 +529,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
       }
     }
     __syncthreads();
+    // the routing outputs: topk_idx / topk_w from CTA 0, counts from the
+    // last CTA (the same tables in every CTA)
     if (c == 0) {
       for (int i = tid; i < T * K; i += kThreads) {
         a.topk_idx[i] = rt.idx[i / K][i % K];
         a.topk_w[i] = rt.w[i / K][i % K];
       }
-      if (a.counts) {
-        for (int e = tid; e < N; e += kThreads) {
-          int cnt = 0;
-          for (int t = 0; t < T; ++t) cnt += s_slot[t][e] != 0xFF;
-          a.counts[e] = cnt;
-        }
+    }
+    if (c == G - 1 && a.counts) {
+      for (int e = tid; e < N; e += kThreads) {
+        int cnt = 0;
+        for (int t = 0; t < T; ++t) cnt += s_slot[t][e] != 0xFF;
+        a.counts[e] = cnt;
       }
     }
   }
@@ -547,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
   // entry's group is BF blocks of kDepth steps, a shared one BFs
   const int BF = ((a.F + EPS - 1) / EPS + kDepth - 1) / kDepth;
   const int BFs = a.S > 0 ? ((a.Fs + EPS - 1) / EPS + kDepth - 1) / kDepth : 0;
-  const int nU = ok ? rt.n_entries : 0, nR = ok ? rt.n_routed : 0;
+  const int nR = ok ? rt.n_routed : 0;
   const int per_ob = nR * BF + a.S * BFs;  // blocks per output block
   const int tb3 = (d / 8) * per_ob;
   const int bmax = BF > BFs ? BF : BFs;
