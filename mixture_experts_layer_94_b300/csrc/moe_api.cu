@@ -154,8 +154,11 @@ Layout make_layout(const moe_problem_t& p, int call) {
     L.offsets = take((size_t)(p.n_experts + 1) * 4);
     L.perm_src = take((size_t)TK * 4);
     L.inv_row = take((size_t)TK * 4);
-    L.x_perm = take((size_t)rows * p.d_model * 2);
-    if (needs_act_copy(p)) L.x_act = take((size_t)T * p.d_model * 2);
+    // FP8 / MXFP4 experts: the gather writes the E4M3 split directly (set_gather_quant)
+    if (!is_lowp(p)) {
+      L.x_perm = take((size_t)rows * p.d_model * 2);
+      if (needs_act_copy(p)) L.x_act = take((size_t)T * p.d_model * 2);
+    }
     L.h = take((size_t)rows * p.ffn * 2);
     if (p.n_shared > 0) L.h_sh = take((size_t)p.n_shared * T * p.shared_ffn * 2);
     L.out_acc = take((size_t)T * p.d_model * 4);
@@ -994,9 +997,9 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
     pa.hidden_bf16 = hbf16;
     pa.offsets = offsets;
     pa.row_token = row_token;
-    pa.x_perm = at<void>(ws, L.x_perm);
+    pa.x_perm = fp8 ? nullptr : at<void>(ws, L.x_perm);
     pa.zero_rows = at<float>(ws, L.out_acc);
-    pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
+    pa.x_act = !fp8 && needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
     pa.act_f16 = fp8;
     pa.err = err;
     if (fp8) set_gather_quant(&pa, ws, L, S > 0);
@@ -1161,9 +1164,9 @@ moe_status_t layer_forward_impl(const moe_problem_t* p, const moe_weights_t* w, 
   pa.perm_src = at<int32_t>(ws, L.perm_src);
   pa.inv_row = at<int32_t>(ws, L.inv_row);
   const bool combine = stored_combine(*p);
-  pa.x_perm = at<void>(ws, L.x_perm);
+  pa.x_perm = fp8 ? nullptr : at<void>(ws, L.x_perm);
   pa.zero_rows = combine ? nullptr : at<float>(ws, L.out_acc);
-  pa.x_act = needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
+  pa.x_act = !fp8 && needs_act_copy(*p) ? at<void>(ws, L.x_act) : nullptr;
   pa.act_f16 = fp8;
   pa.err = err;
   if (fp8) set_gather_quant(&pa, ws, L, S > 0);
