@@ -33,7 +33,9 @@
 //   its own 6-stage x 32 KB ring, and each CTA's TMEM receives its own 128
 //   rows. The leader's thread issues the MMA; stage releases and tile
 //   completion are signalled to both CTAs' barriers. Per CTA this halves the
-//   weight bytes pulled from L2 per FLOP and deepens the ring.
+//   weight bytes pulled from L2 per FLOP and deepens the ring. A group's last
+//   tile with at most 128 rows left runs as an M=128 pair MMA, 64 rows per CTA
+//   (see is_half_tile), so that it carries at most 127 padding rows, not 255.
 // The double-buffered accumulator lets the epilogue of tile i overlap the MMAs
 // of tile i+1. Tiles are (group, m block, n block), n-major inside a group so
 // CTAs running side by side share weight tiles in L2; a CTA (pair) walks tiles
@@ -67,8 +69,22 @@ struct Cfg {
   static constexpr uint32_t kStageBytes = kStageA + kStageB;
   static constexpr int kTileRows = kBM * PAIR;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128 * PAIR, 256);
+  // A pair's tail tile of at most 128 rows: M = 128, 64 rows from each CTA.
+  static constexpr uint32_t kIdescHalf = ptx::idesc_bf16_f32(128, 256);
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + kBarrierBytes;
 };
+
+// Whether a pair tile is the half form: the group's last tile with at most
+// 128 rows left runs as an M = 128 pair MMA (64 rows from each CTA), which
+// halves the padding rows of a group's last tile on average. Its accumulator
+// lands folded: TMEM lanes 0-63 of each CTA hold the CTA's 64 rows x the MMA's
+// first 128 columns (the leader's B rows), lanes 64-127 the same rows x the
+// last 128 (the peer's B rows), both in TMEM columns 0-127. So that SwiGLU
+// stays within a thread, a gate/up half tile's B rows are arranged as
+// [gate f0..f0+63; up f0..f0+63] on the leader and the next 64 on the peer.
+__device__ __forceinline__ bool is_half_tile(const TileInfo& ti) {
+  return ti.g.rows - ti.m_blk * 2 * kBM <= kBM;
+}
 
 struct RouterTile {
   int m_blk, split, part, kb0, kb1;
@@ -90,6 +106,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmU0, const __grid_constant__ CUtensorMap tmU1,
+                        const __grid_constant__ CUtensorMap tmBh0, const __grid_constant__ CUtensorMap tmBh1,
+                        const __grid_constant__ CUtensorMap tmUh0, const __grid_constant__ CUtensorMap tmUh1,
                         const GemmArgs a) {
   pdl_trigger();
   using C = Cfg<PAIR>;
@@ -190,8 +208,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const CUtensorMap* mA = kind ? &tmA1 : &tmA0;
         const CUtensorMap* mB = kind ? &tmB1 : &tmB0;
         const CUtensorMap* mU = kind ? &tmU1 : &tmU0;
-        const int a_row =
-            (PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kTileRows + (int)rank * kBM;
+        // a pair's half tile takes 64 rows from each CTA
+        const bool half = PAIR == 2 && is_half_tile(ti);
+        const int a_row = (PHASE == kPhaseGateUp ? ti.g.a_row0 : ti.g.h_row0) + ti.m_blk * kTileRows +
+                          (int)rank * (half ? kBM / 2 : kBM);
         // Weight rows: gate/up -> rows n*128 of the expert in W_gate (and W_up);
         // down -> rows n*256 (+ this CTA's 128-row half in a pair).
         int b_row = ti.g.index * a.w_rows[kind] + ti.n_blk * (PHASE == kPhaseGateUp ? kBNGateUp : kBNDown);
@@ -207,7 +227,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);  // the leader's barrier
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), 2u * kStageBytes);
             ptx::tma_load_2d_pair(dA, mA, fb, kb * kBK, a_row);
-            ptx::tma_load_2d_pair(dB, (PHASE == kPhaseGateUp && !leader) ? mU : mB, fb, kb * kBK, b_row);
+            if (PHASE == kPhaseGateUp && half) {
+              // gate and up rows f0..f0+63 on the leader, f0+64..f0+127 on the peer (64-row boxes)
+              const int hb = b_row + (int)rank * (kBNGateUp / 2);
+              ptx::tma_load_2d_pair(dB, kind ? &tmBh1 : &tmBh0, fb, kb * kBK, hb);
+              ptx::tma_load_2d_pair(dB + kStageB / 2, kind ? &tmUh1 : &tmUh0, fb, kb * kBK, hb);
+            } else {
+              ptx::tma_load_2d_pair(dB, (PHASE == kPhaseGateUp && !leader) ? mU : mB, fb, kb * kBK, b_row);
+            }
           } else {
             ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
             ptx::tma_load_2d(dA, mA, full_bar(stage), kb * kBK, a_row);
@@ -237,14 +264,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool aborted = false;
-      const uint32_t idesc = (PHASE == kPhaseRouter) ? a.r_idesc : C::kIdesc;
       for (int tile = unit; tile < total && !aborted; tile += units) {
         int nkb;
+        uint32_t idesc = C::kIdesc;
         if (PHASE == kPhaseRouter) {
           const RouterTile rt = decode_router_tile(tile, a);
           nkb = rt.kb1 - rt.kb0;
+          idesc = a.r_idesc;
         } else {
-          nkb = a.k_blocks[decode_tile(tile, a).g.kind];
+          const TileInfo ti = decode_tile(tile, a);
+          nkb = a.k_blocks[ti.g.kind];
+          if (PAIR == 2 && is_half_tile(ti)) idesc = C::kIdescHalf;
         }
         if (!ptx::mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err)) break;
         ptx::tc_fence_after();
@@ -338,22 +368,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ptx::mbar_wait(tfull_bar(acc), acc_phase, abort_flag, a.err)) break;
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + (uint32_t)acc * kAccCols;
-      const int r_local = ti.m_blk * kTileRows + row_in_tile;
+      // half tile (folded accumulator): lanes 64-127 hold the same 64 rows as
+      // lanes 0-63, for the MMA's last 128 columns
+      const bool half = PAIR == 2 && is_half_tile(ti);
+      const bool upper = half && quad >= 2;
+      const int tr = half ? (int)rank * (kBM / 2) + (quad & 1) * 32 + lane : row_in_tile;
+      const int r_local = ti.m_blk * kTileRows + tr;
       const bool row_ok = r_local < ti.g.rows;
       if (PHASE == kPhaseGateUp) {
         const int n_ext = a.n_ext[kind];
         const int col0 = ti.n_blk * kBNGateUp;
         __nv_bfloat16* hrow = a.h[kind] + (int64_t)(ti.g.h_row0 + (row_ok ? r_local : 0)) * a.ldh[kind];
+        // half tile: gate at TMEM columns 0-63, up at 64-127, for f0 + 64 (upper lanes) + 0..63
+        const int nf = half ? kBNGateUp / 2 : kBNGateUp;
+        const int fbase = col0 + (upper ? kBNGateUp / 2 : 0);
 #pragma unroll 1
-        for (int c = 0; c < kBNGateUp / 32; ++c) {
+        for (int c = 0; c < nf / 32; ++c) {
           uint32_t gv[32], uv[32];
           ptx::tmem_ld_32x32b_x32(tacc + c * 32, gv);
-          ptx::tmem_ld_32x32b_x32(tacc + kBNGateUp + c * 32, uv);
+          ptx::tmem_ld_32x32b_x32(tacc + nf + c * 32, uv);
           ptx::tmem_wait_ld();
           if (row_ok) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              const int f0 = col0 + c * 32 + v * 8;
+              const int f0 = fbase + c * 32 + v * 8;
               if (f0 < n_ext) {
                 uint32_t p[4];
 #pragma unroll
@@ -385,8 +423,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             t = r_local;
           }
         }
+        // half tile: TMEM columns 0-127 are output columns col0 + (128 on upper lanes) + 0..127
+        const int cbase = col0 + (upper ? kBNDown / 2 : 0);
 #pragma unroll 1
-        for (int c = 0; c < kBNDown / 32; ++c) {
+        for (int c = 0; c < (half ? kBNDown / 64 : kBNDown / 32); ++c) {
           uint32_t yv[32];
           ptx::tmem_ld_32x32b_x32(tacc + c * 32, yv);
           ptx::tmem_wait_ld();
@@ -395,7 +435,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               float* orow = a.out_acc + t * a.d;
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
-                const int n0 = col0 + c * 32 + v * 4;
+                const int n0 = cbase + c * 32 + v * 4;
                 if (n0 < a.d) {
                   float4 val = make_float4(w * __uint_as_float(yv[v * 4 + 0]), w * __uint_as_float(yv[v * 4 + 1]),
                                            w * __uint_as_float(yv[v * 4 + 2]), w * __uint_as_float(yv[v * 4 + 3]));
@@ -406,7 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               __nv_bfloat16* yrow = (kind && a.y_sh ? a.y_sh : a.y) + (int64_t)(ti.g.h_row0 + r_local) * a.d;
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
-                const int n0 = col0 + c * 32 + v * 8;
+                const int n0 = cbase + c * 32 + v * 8;
                 if (n0 < a.d) {
                   uint32_t p[4];
 #pragma unroll
@@ -482,7 +522,7 @@ cudaError_t launch_t(const GemmMaps& m, const GemmArgs& a, int64_t tile_bound, c
   int64_t units = max_units[dev & 63].load();
   if (tile_bound < units) units = tile_bound < 1 ? 1 : tile_bound;
   return launch_attr(kern, dim3((unsigned)(units * PAIR)), dim3(kGemmThreads), smem, s, attr[0], m.a[0], m.a[1],
-                     m.b[0], m.b[1], m.bu[0], m.bu[1], a);
+                     m.b[0], m.b[1], m.bu[0], m.bu[1], m.bh[0], m.bh[1], m.uh[0], m.uh[1], a);
 }
 
 }  // namespace

@@ -152,6 +152,8 @@ struct GemmMaps {
   CUtensorMap a[2];   // activations per kind
   CUtensorMap b[2];   // weights per kind (gate for the gate/up phase)
   CUtensorMap bu[2];  // up weights per kind (gate/up phase only)
+  CUtensorMap bh[2];  // gate/up phase on pairs: gate weights in 64-row boxes (half tiles)
+  CUtensorMap uh[2];  // ... and up weights
 };
 
 // Tensor maps of the FP8-weight grouped GEMM: activations (two-term E4M3

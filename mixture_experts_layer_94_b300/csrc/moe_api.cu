@@ -462,10 +462,26 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
          make_map(&m.b[1], g.sg, g.d, (uint64_t)g.S * g.Fs, kBNGateUp) &&
          make_map(&m.bu[1], g.su, g.d, (uint64_t)g.S * g.Fs, kBNGateUp);
   if (!ok) return MOE_ERR_CUDA;
+  // pairs: the half tiles' gate and up rows in 64-row boxes
+  if (ok && g.pair == 2)
+    ok = make_map(&m.bh[0], g.wg, g.d, (uint64_t)g.N * g.F, kBNGateUp / 2) &&
+         make_map(&m.uh[0], g.wu, g.d, (uint64_t)g.N * g.F, kBNGateUp / 2) &&
+         (!sh || (make_map(&m.bh[1], g.sg, g.d, (uint64_t)g.S * g.Fs, kBNGateUp / 2) &&
+                  make_map(&m.uh[1], g.su, g.d, (uint64_t)g.S * g.Fs, kBNGateUp / 2)));
+  if (!ok) return MOE_ERR_CUDA;
+  if (g.pair != 2) {
+    m.bh[0] = m.b[0];
+    m.uh[0] = m.bu[0];
+  }
   if (!sh) {
     m.a[1] = m.a[0];
     m.b[1] = m.b[0];
     m.bu[1] = m.bu[0];
+    m.bh[1] = m.bh[0];
+    m.uh[1] = m.uh[0];
+  } else if (g.pair != 2) {
+    m.bh[1] = m.b[1];
+    m.uh[1] = m.bu[1];
   }
   GemmArgs a{};
   a.groups = g.groups;
@@ -505,6 +521,8 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   }
   md.bu[0] = md.b[0];
   md.bu[1] = md.b[1];
+  md.bh[0] = md.uh[0] = md.b[0];
+  md.bh[1] = md.uh[1] = md.b[1];
   a.tile_start = g.ts_dn;
   a.n_ext[0] = a.n_ext[1] = g.d;
   a.k_blocks[0] = (g.F + kBK - 1) / kBK;

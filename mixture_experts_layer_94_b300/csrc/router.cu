@@ -428,6 +428,7 @@ cudaError_t launch_tensor_logits(const RouterArgs& a, const RouterPlan& pl, cuda
     return cudaErrorInvalidValue;
   m.a[1] = m.a[0];
   m.b[1] = m.bu[0] = m.bu[1] = m.b[0];
+  m.bh[0] = m.bh[1] = m.uh[0] = m.uh[1] = m.b[0];
   GemmArgs g{};
   g.err = nullptr;
   g.r_m_tiles = (int32_t)pl.token_tiles;
