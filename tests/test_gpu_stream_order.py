@@ -53,3 +53,35 @@ def test_back_to_back_calls_match_calls_made_alone(name):
     assert layer.status(cfg.T) == 0
     for i, (o, a) in enumerate(zip(outs, alone)):
         H.assert_same_but_summation_order(o, a, f"{name} call {i}")
+
+
+@pytest.mark.parametrize("name", ["bf16_prefill_shared", "bf16_decode", "bf16_expert_choice"])
+def test_calls_replayed_from_a_cuda_graph_match_eager_calls(name):
+    """The layer captured into a CUDA graph and replayed on new inputs gives
+    what eager calls give: every kernel's early start (programmatic dependent
+    launch) becomes a graph edge, and the workspace and weights are bound at
+    capture."""
+    cfg = CASES[name]
+    ins, dev = H.make_case(cfg)
+    layer = B.MoELayer(cfg, dev)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    xs = [torch.randn(dev["hidden"].shape, generator=g).to(dev["hidden"].dtype).cuda() for _ in range(2)]
+    eager = [layer.forward(x).clone() for x in xs]
+    torch.cuda.synchronize()
+    static_in = xs[0].clone()
+    static_out = torch.empty_like(eager[0])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # a first call outside capture (one-time launch attributes)
+        layer.forward(static_in, out=static_out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(static_in, out=static_out)
+    for x, e in zip(xs, eager):
+        static_in.copy_(x)
+        graph.replay()
+        torch.cuda.synchronize()
+        H.assert_same_but_summation_order(static_out, e, f"{name} graph replay")
+    assert layer.status(cfg.T) == 0
