@@ -202,9 +202,11 @@ __device__ __forceinline__ bool join_halves(float (&c)[4], float* slot, uint32_t
 
 // Token t's scores, group limit, top-K and gate weights from its summed
 // logits lg_s[t][.] (router bias added here); slot k's expert and weight
-// land in idx[k], w[k].
+// land in idx[k], w[k]. Group-limited routing only: kept out of line, so
+// that the rank-based path the other problems take stays compact (the
+// kernel's code is fetched cold from DRAM once per launch).
 template <int EPL>
-__device__ __forceinline__ void topk_token(const DecodeArgs& a, const float* lg_s, int t, int lane, int N, int K,
+__device__ __noinline__ void topk_token(const DecodeArgs& a, const float* lg_s, int t, int lane, int N, int K,
                                            float* s_key, unsigned char* s_kept, int32_t* idx, float* w) {
   float lg[EPL], sc[EPL], key[EPL];
   bool valid[EPL];
@@ -268,28 +270,70 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
       else static_cast<uint16_t*>(a.h_sh)[(int64_t)((i - nr) / ps) * a.hs_stride + a.Fs + (i - nr) % ps] = 0;
     }
   }
-  if (c < a.rsplits) {
-    const int j0 = c * a.r_slice, nj = min(a.r_slice, d - j0);
-    float* xsl = red;                   // [T][r_slice] fp32 slice of the token rows
-    float* part = red + T * a.r_slice;  // [Q][T][N]
-    const int Q = kThreads / N;         // threads per expert, splitting the slice's rows
-    const int q = tid / N, e = tid - q * N;
-    // this thread's first batch of router weights is loaded before the
-    // token rows' slice is staged; a slice longer than one batch per thread
-    // takes further batches
-    float wv[kRouterRowsPerThread];
+  // Router CTAs issue their first batch of router weights before anything
+  // else, so that its DRAM round trip overlaps the token rows' below.
+  const bool router_cta = c < a.rsplits;
+  const int j0 = c * a.r_slice, nj = router_cta ? min(a.r_slice, d - j0) : 0;
+  const int Q = kThreads / N;  // threads per expert, splitting the slice's rows
+  const int q = tid / N, e = tid - q * N;
+  float wv[kRouterRowsPerThread];
 #pragma unroll
-    for (int u = 0; u < kRouterRowsPerThread; ++u) {
-      const int j = q + u * Q;
-      wv[u] = q < Q && j < nj ? __ldg(a.w_router + (int64_t)(j0 + j) * N + e) : 0.f;
+  for (int u = 0; u < kRouterRowsPerThread; ++u) {
+    const int j = q + u * Q;
+    wv[u] = router_cta && q < Q && j < nj ? __ldg(a.w_router + (int64_t)(j0 + j) * N + e) : 0.f;
+  }
+  // the zero row, then the token rows rounded to the activation format and
+  // zero-padded to x_stride
+  for (int i = tid; i < (a.z_len + T * xstride) / 8; i += kThreads) {
+    const int j = i - a.z_len / 8;
+    const int t = j < 0 ? -1 : j / (xstride / 8), v = j - t * (xstride / 8);
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (t >= 0 && 8 * v < d) {
+      float f[8];
+      if (HB) {
+        const uint4 hv = __ldg(static_cast<const uint4*>(a.hidden) + ((int64_t)t * d) / 8 + v);
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f[2 * k] = __uint_as_float(hw[k] << 16);
+          f[2 * k + 1] = __uint_as_float(hw[k] & 0xFFFF0000u);
+        }
+      } else {
+        const float4* p = static_cast<const float4*>(a.hidden) + ((int64_t)t * d) / 4 + 2 * v;
+        const float4 u0 = __ldg(p), u1 = __ldg(p + 1);
+        f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w;
+        f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
+      }
+      if (kF16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = round_f16(f[k], over);
+        o = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                       pack_f16x2(f[6], f[7]));
+      } else {
+        o = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                       pack_bf16x2(f[6], f[7]));
+      }
     }
-    for (int i = tid; i < T * nj; i += kThreads) {
-      const int t = i / nj, j = i - t * nj;
-      const int64_t xi = (int64_t)t * d + j0 + j;
-      xsl[t * a.r_slice + j] = HB ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.hidden)[xi])
-                                  : static_cast<const float*>(a.hidden)[xi];
+    reinterpret_cast<uint4*>(zrow)[i] = o;
+  }
+  // bf16 hidden with bf16 experts: the staged rows hold the hidden values
+  // exactly, and the router reads its slice from them
+  constexpr bool kXsExact = HB && !kF16;
+  if (router_cta) {
+    float* xsl = red;                   // [T][r_slice] fp32 slice of the token rows (otherwise)
+    float* part = red + T * a.r_slice;  // [Q][T][N]
+    if (!kXsExact) {
+      for (int i = tid; i < T * nj; i += kThreads) {
+        const int t = i / nj, j = i - t * nj;
+        const int64_t xi = (int64_t)t * d + j0 + j;
+        xsl[t * a.r_slice + j] = HB ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.hidden)[xi])
+                                    : static_cast<const float*>(a.hidden)[xi];
+      }
     }
     __syncthreads();
+    auto xval = [&](int t, int j) {
+      return kXsExact ? __uint_as_float((uint32_t)xs[(int64_t)t * xstride + j0 + j] << 16) : xsl[t * a.r_slice + j];
+    };
     if (q < Q) {
       float acc[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
       for (int jb = q;; jb += kRouterRowsPerThread * Q) {
@@ -299,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
           if (j < nj) {
 #pragma unroll
             for (int t = 0; t < kDecodeMaxTokens; ++t)
-              if (t < T) acc[t] = fmaf(xsl[t * a.r_slice + j], wv[u], acc[t]);
+              if (t < T) acc[t] = fmaf(xval(t, j), wv[u], acc[t]);
           }
         }
         const int jn = jb + kRouterRowsPerThread * Q;
@@ -321,40 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
       for (int qq = 0; qq < Q; ++qq) s += part[(int64_t)qq * T * N + i];
       a.router_part[(int64_t)c * T * N + i] = s;
     }
-  }
-  // the zero row, then the token rows rounded to the activation format and
-  // zero-padded to x_stride
-  for (int i = tid; i < (a.z_len + T * xstride) / 8; i += kThreads) {
-    const int j = i - a.z_len / 8;
-    const int t = j < 0 ? -1 : j / (xstride / 8), v = j - t * (xstride / 8);
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (t >= 0 && 8 * v < d) {
-      float f[8];
-      if (HB) {
-        const uint4 hv = __ldg(static_cast<const uint4*>(a.hidden) + ((int64_t)t * d) / 8 + v);
-        const uint32_t wv[4] = {hv.x, hv.y, hv.z, hv.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          f[2 * k] = __uint_as_float(wv[k] << 16);
-          f[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
-        }
-      } else {
-        const float4* p = static_cast<const float4*>(a.hidden) + ((int64_t)t * d) / 4 + 2 * v;
-        const float4 u0 = __ldg(p), u1 = __ldg(p + 1);
-        f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w;
-        f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
-      }
-      if (kF16) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = round_f16(f[k], over);
-        o = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-                       pack_f16x2(f[6], f[7]));
-      } else {
-        o = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                       pack_bf16x2(f[6], f[7]));
-      }
-    }
-    reinterpret_cast<uint4*>(zrow)[i] = o;
   }
   ok = grid_barrier(a.sync, 1u, a.err, &s_ok);
 
@@ -385,29 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
       psum[i] = s;
     }
     __syncthreads();
+    const bool grouped = a.n_groups > 1 && a.topk_groups < a.n_groups;
+    // The P sums in order, and for the rank-based top-K every (token, expert)
+    // pair's selection key and score (the same fp32 arithmetic as
+    // router_scores). key_s and sc_s overlay psum's first two rows, whose
+    // column i only this thread reads, before it writes.
+    float* key_s = red + pairs;     // [T][N]
+    float* sc_s = red + 2 * pairs;  // [T][N]
     for (int i = tid; i < pairs; i += kThreads) {
       float s = 0.f;
       for (int p = 0; p < P; ++p) s += psum[p * pairs + i];
       lg_s[i] = s;
-    }
-    __syncthreads();
-    if (a.n_groups > 1 && a.topk_groups < a.n_groups) {
-      // group-limited routing: one warp per token (topk.cuh)
-      if (warp < T) {
-        if (N <= 128) topk_token<4>(a, lg_s, warp, lane, N, K, s_key[warp], s_kept[warp], rt.idx[warp], rt.w[warp]);
-        else topk_token<8>(a, lg_s, warp, lane, N, K, s_key[warp], s_kept[warp], rt.idx[warp], rt.w[warp]);
-      }
-    } else {
-      // Every (token, expert) pair's selection key and score (the same fp32
-      // arithmetic as router_scores), then its rank: the number of experts
-      // whose key is larger, or equal at a lower index. The experts of rank
-      // below K are the top-K, and the rank is the slot (key descending, ties
-      // to the lower index). P threads share a pair's comparisons.
-      float* key_s = red + pairs;     // [T][N]
-      float* sc_s = red + 2 * pairs;  // [T][N]
-      for (int i = tid; i < pairs; i += kThreads) {
-        const int t = i / N, e = i - t * N;
-        const float l = lg_s[t * N + e] + (a.router_bias ? a.router_bias[e] : 0.f);
+      if (!grouped) {
+        const int e = i - (i / N) * N;
+        const float l = s + (a.router_bias ? a.router_bias[e] : 0.f);
         if (a.score_fn == 0) {
           key_s[i] = l;
           sc_s[i] = l;
@@ -417,7 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
           key_s[i] = sg + (a.sel_bias ? a.sel_bias[e] : 0.f);
         }
       }
+    }
+    __syncthreads();
+    if (grouped) {
+      // group-limited routing: one warp per token (topk.cuh)
+      if (warp < T) {
+        if (N <= 128) topk_token<4>(a, lg_s, warp, lane, N, K, s_key[warp], s_kept[warp], rt.idx[warp], rt.w[warp]);
+        else topk_token<8>(a, lg_s, warp, lane, N, K, s_key[warp], s_kept[warp], rt.idx[warp], rt.w[warp]);
+      }
+      // slot of expert e in token t's choice (0xFF: not chosen)
+      for (int i = tid; i < T * N; i += kThreads) s_slot[i / N][i % N] = 0xFF;
       __syncthreads();
+      for (int i = tid; i < T * K; i += kThreads) s_slot[i / K][rt.idx[i / K][i % K]] = (uint8_t)(i % K);
+    } else {
+      // Each pair's rank: the number of experts whose key is larger, or
+      // equal at a lower index. The experts of rank below K are the top-K,
+      // and the rank is the slot (key descending, ties to the lower index);
+      // it also gives the slot map (0xFF: not chosen). P threads share a
+      // pair's comparisons.
       int P = 1;
       while (P < 32 && P * 2 * pairs <= kThreads) P *= 2;
       for (int i0 = 0; i0 < pairs * P; i0 += kThreads) {
@@ -425,16 +443,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
         const int pr = i / P, p = i - pr * P;
         int cnt = 0;
         if (pr < pairs) {
+          // this thread's contiguous share [j0, j1) of the token's keys, four at a time where aligned
           const int t = pr / N, e = pr - t * N;
           const float ke = key_s[pr];
           const float* kt = key_s + t * N;
-          for (int j = p; j < N; j += P) {
+          const int j0 = (N * p) / P, j1 = (N * (p + 1)) / P;
+          int j = j0;
+          if (((reinterpret_cast<uintptr_t>(kt + j0)) & 15u) == 0) {
+#pragma unroll 4
+            for (; j + 4 <= j1; j += 4) {
+              const float4 k4 = *reinterpret_cast<const float4*>(kt + j);
+              cnt += (k4.x > ke) || (k4.x == ke && j < e);
+              cnt += (k4.y > ke) || (k4.y == ke && j + 1 < e);
+              cnt += (k4.z > ke) || (k4.z == ke && j + 2 < e);
+              cnt += (k4.w > ke) || (k4.w == ke && j + 3 < e);
+            }
+          }
+          for (; j < j1; ++j) {
             const float kj = kt[j];
             cnt += (kj > ke) || (kj == ke && j < e);
           }
         }
         for (int off = 1; off < P; off <<= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, off);
-        if (pr < pairs && p == 0 && cnt < K) rt.idx[pr / N][cnt] = pr % N;
+        if (pr < pairs && p == 0) {
+          const int t = pr / N, e = pr - t * N;
+          s_slot[t][e] = cnt < K ? (uint8_t)cnt : (uint8_t)0xFF;
+          if (cnt < K) rt.idx[t][cnt] = e;
+        }
       }
       __syncthreads();
       // gate weights, warp t for token t, as router_select computes them
@@ -464,10 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
         if (lane < K) rt.w[warp][lane] = w;
       }
     }
-    // slot of expert e in token t's choice (0xFF: not chosen)
-    for (int i = tid; i < T * N; i += kThreads) s_slot[i / N][i % N] = 0xFF;
-    __syncthreads();
-    for (int i = tid; i < T * K; i += kThreads) s_slot[i / K][rt.idx[i / K][i % K]] = (uint8_t)(i % K);
     __syncthreads();
     {
       // capacity: the first `capacity` copies of each expert in token order
