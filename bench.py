@@ -57,6 +57,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 DTYPES = {"bf16": "bf16",
           "fp8": "e4m3 weights (row scales) x two-term e4m3 of fp16 activations",
           "mxfp4": "mxfp4 (e2m1 + e8m0 block scales) weights x two-term e4m3 of fp16 activations"}
+# The one-kernel decode layer widens FP8 codes to fp16 exactly and multiplies
+# them with fp16 activations.
+DTYPES_ONE_KERNEL = {"bf16": "bf16", "fp8": "e4m3 weights (row scales) widened to fp16 x fp16 activations"}
 
 
 def parse():
@@ -588,7 +591,8 @@ def run_ours(args, cfg, desc, world, rank):
         layer_roof["frac_at_max_clock"] = 1e3 * t_roof / ms_step * clock_scale
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": DTYPES[cfg.expert_dtype],
+            "vs_baseline": None,
+            "dtype": (DTYPES_ONE_KERNEL if fused else DTYPES).get(cfg.expert_dtype, DTYPES[cfg.expert_dtype]),
             "data": "synthetic (seeded; random-init weights)",
             "config": config_block(cfg, desc, args), "roofline": roof,
             "layer_roofline": layer_roof,
@@ -612,7 +616,7 @@ def main():
     args = parse()
     cfg, desc = WORKLOADS[args.workload]
     if args.tokens is not None:
-        cfg, desc = cfg.with_(T=args.tokens), f"{desc}, T={args.tokens}"
+        cfg, desc = cfg.with_(T=args.tokens), re.sub(r", T=\d+$", "", desc) + f", T={args.tokens}"
     if args.experts is not None:
         groups = cfg.n_groups if cfg.n_groups and args.experts % cfg.n_groups == 0 else 0
         cfg = cfg.with_(N=args.experts, K=min(cfg.K, args.experts), n_groups=groups,
