@@ -64,6 +64,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -237,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
   __shared__ bool s_ok;
   __shared__ int32_t s_wcount[kWarps];
   __shared__ uint8_t s_slot[kDecodeMaxTokens][kMaxExperts];
+  __shared__ __align__(8) uint64_t s_hbar;  // the h rows' bulk copies (phase 3)
+  __shared__ int s_abort;
   constexpr bool kF16 = FMT != kDecodeBf16;
   constexpr int EPS = FMT == kDecodeBf16 ? 32 : 64;  // elements of a row per step
   constexpr int EPL = EPS / 4;                       // elements per lane per step
@@ -248,6 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
   const int64_t GW = (int64_t)G * kWarps, gw = (int64_t)c * kWarps + warp;
   bool over = false;
   bool ok = true;
+  if (tid == 0) {
+    ptx::mbar_init(ptx::smem_u32(&s_hbar), 1);
+    ptx::fence_mbarrier_init();
+    s_abort = 0;
+  }
 
   // ------------------------------------------------------------ phase 0
   // shared memory: the zero row [z_len], then the token rows [T][x_stride]
@@ -759,31 +767,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
   uint16_t* hs = xs;  // phase 3: the h rows reuse the token rows' space
   const int hsm = a.hsm_stride;
   if (ok) {
-    // h rows into shared memory: routed rows t*K + k, then the shared rows,
-    // each with its zero padding. Every thread issues its loads (up to 16
-    // units of 16 bytes) before storing any.
-    const int vrow = hsm / 8;
-    const int nvec = rows_h * vrow;
-    for (int i0 = tid; i0 < nvec; i0 += 16 * kThreads) {
-      uint4 v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int i = i0 + q * kThreads;
-        const int rr = i / vrow, c8 = i - rr * vrow;
-        const bool sh = rr >= T * K;
+    // h rows into shared memory (routed rows t*K + k, then the shared rows):
+    // one bulk copy per row, issued by warp 0 and counted on one mbarrier.
+    // Unlike loads from every thread, the copies do not queue behind the
+    // down-row loads already in flight.
+    const uint32_t bar = ptx::smem_u32(&s_hbar);
+    if (warp == 0) {
+      if (lane == 0)
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)(T * K * a.h_stride + a.S * T * a.hs_stride) * 2u);
+      __syncwarp();
+      // the copies write shared memory the token rows held (read through the
+      // generic proxy) and read h rows other CTAs wrote before the barrier
+      ptx::fence_proxy_async_shared();
+      ptx::fence_proxy_async_global();
+      for (int r = lane; r < rows_h; r += 32) {
+        const bool sh = r >= T * K;
         const int len = sh ? a.hs_stride : a.h_stride;
-        v[q] = i < nvec && 8 * c8 < len
-                   ? __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(sh ? a.h_sh : a.h) +
-                                                           (int64_t)(sh ? rr - T * K : rr) * len) + c8)
-                   : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int i = i0 + q * kThreads;
-        if (i < nvec) reinterpret_cast<uint4*>(hs)[i] = v[q];
+        const uint16_t* src = static_cast<const uint16_t*>(sh ? a.h_sh : a.h) + (int64_t)(sh ? r - T * K : r) * len;
+        ptx::bulk_load(ptx::smem_u32(hs + (int64_t)r * hsm), src, (uint32_t)len * 2u, bar);
       }
     }
+    ptx::mbar_wait(bar, 0, &s_abort, a.err);
     __syncthreads();
+    if (s_abort) {
+      // timed out: the copies may still be landing; wait for them (bounded)
+      // before this CTA leaves
+      ok = false;
+      if (tid == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+        }
+      }
+      __syncthreads();
+    }
   }
   if (ok && active3) {
     int cob, cu, cstart, clen;
