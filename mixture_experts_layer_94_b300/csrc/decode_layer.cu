@@ -18,17 +18,18 @@
 //   barrier
 //   phase 1  every CTA sums the partials in split order (the same fp32
 //            result everywhere), scores, applies the group limit, takes the
-//            top-K and the gate weights (topk.cuh), the capacity drops
-//            ("Chapter 19", §19.6.1: the first C copies of an expert in token
-//            order stay), and lists the touched experts. CTA 0 stores topk_idx,
-//            topk_w and the per-expert counts.
+//            top-K (topk.cuh), the capacity drops ("Chapter 19", §19.6.1: the
+//            first C copies of an expert in token order stay), and lists the
+//            touched experts; the last CTA stores the per-expert counts.
 //   phase 2  gate/up: groups of 8 weight rows, gate rows f..f+3 and up rows
 //            f..f+3 of one touched (or shared) expert. The groups' steps are
 //            split into equal contiguous ranges over the grid's warps; a warp
 //            streams its steps once from HBM and stores h = SiLU(g) * u
 //            (16-bit) for each token that chose the expert.
 //   barrier  (each warp first issues its first down-row loads, so HBM stays
-//            busy across the barrier)
+//            busy across the barrier; while it completes, every CTA computes
+//            the gate weights, which nothing needs before the down phase, and
+//            CTA 0 stores topk_idx and topk_w)
 //   phase 3  down: groups of 8 consecutive rows W_down[e][8b..8b+7] of every
 //            touched (and shared) expert, split the same way. When the last
 //            group of output block b is done, the warp that finished it sums
@@ -167,12 +168,18 @@ __device__ bool wait_count(const uint32_t* ctr, uint32_t target) {
   return true;
 }
 
-// Grid barrier number `gen` (1, 2): every CTA adds one, then waits for gen*G.
-__device__ bool grid_barrier(uint32_t* ctr, uint32_t gen, uint32_t* err, bool* s_ok) {
+// Grid barrier number `gen` (1, 2): every CTA adds one (grid_arrive), then
+// waits for gen*G (grid_wait); a CTA may work in between.
+__device__ void grid_arrive(uint32_t* ctr) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(ctr, 1u);
+  }
+}
+
+__device__ bool grid_wait(uint32_t* ctr, uint32_t gen, uint32_t* err, bool* s_ok) {
+  if (threadIdx.x == 0) {
     const bool ok = wait_count(ctr, gen * gridDim.x);
     if (!ok) atomicOr(err, kErrTimeout);
     __threadfence();
@@ -180,6 +187,11 @@ __device__ bool grid_barrier(uint32_t* ctr, uint32_t gen, uint32_t* err, bool* s
   }
   __syncthreads();
   return *s_ok;
+}
+
+__device__ bool grid_barrier(uint32_t* ctr, uint32_t gen, uint32_t* err, bool* s_ok) {
+  grid_arrive(ctr);
+  return grid_wait(ctr, gen, err, s_ok);
 }
 
 // Adds the other half of a group split between two warps. `slot` holds two
@@ -444,18 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
       // and the rank is the slot (key descending, ties to the lower index);
       // it also gives the slot map (0xFF: not chosen). P threads share a
       // pair's comparisons.
-      int P = 1;
-      while (P < 32 && P * 2 * pairs <= kThreads) P *= 2;
+      int lp = 0;  // P = 2^lp
+      while (lp < 5 && (2 << lp) * pairs <= kThreads) ++lp;
+      const int P = 1 << lp;
       for (int i0 = 0; i0 < pairs * P; i0 += kThreads) {
         const int i = i0 + tid;
-        const int pr = i / P, p = i - pr * P;
+        const int pr = i >> lp, p = i & (P - 1);
+        // token t = pr / N for T <= 4, without a division
+        const int t = (pr >= N) + (pr >= 2 * N) + (pr >= 3 * N), e = pr - t * N;
         int cnt = 0;
         if (pr < pairs) {
           // this thread's contiguous share [j0, j1) of the token's keys, four at a time where aligned
-          const int t = pr / N, e = pr - t * N;
           const float ke = key_s[pr];
           const float* kt = key_s + t * N;
-          const int j0 = (N * p) / P, j1 = (N * (p + 1)) / P;
+          const int j0 = (N * p) >> lp, j1 = (N * (p + 1)) >> lp;
           int j = j0;
           if (((reinterpret_cast<uintptr_t>(kt + j0)) & 15u) == 0) {
 #pragma unroll 4
@@ -474,38 +488,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
         }
         for (int off = 1; off < P; off <<= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, off);
         if (pr < pairs && p == 0) {
-          const int t = pr / N, e = pr - t * N;
           s_slot[t][e] = cnt < K ? (uint8_t)cnt : (uint8_t)0xFF;
           if (cnt < K) rt.idx[t][cnt] = e;
         }
       }
-      __syncthreads();
-      // gate weights, warp t for token t, as router_select computes them
-      if (warp < T) {
-        const float* sct = sc_s + warp * N;
-        const int my_e = lane < K ? rt.idx[warp][lane] : 0;
-        const float my_sc = lane < K ? sct[my_e] : 0.f;
-        float w;
-        if (a.score_fn == 0) {
-          const float lmax = __shfl_sync(0xffffffffu, my_sc, 0);  // slot 0 holds the largest logit
-          const float ex = lane < K ? expf(my_sc - lmax) : 0.f;
-          float z = 0.f;
-          if (a.renormalize) {
-            z = ex;
-          } else {
-            for (int e = lane; e < N; e += 32) z += expf(sct[e] - lmax);
-          }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-          w = ex / z;
-        } else {
-          float z = lane < K ? my_sc : 0.f;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-          w = a.renormalize ? my_sc / z : my_sc;
-        }
-        if (lane < K) rt.w[warp][lane] = w;
-      }
+      // (the gate weights follow during the second grid barrier: nothing
+      // needs them before the down phase)
     }
     __syncthreads();
     {
@@ -568,14 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
       }
     }
     __syncthreads();
-    // the routing outputs: topk_idx / topk_w from CTA 0, counts from the
-    // last CTA (the same tables in every CTA)
-    if (c == 0) {
-      for (int i = tid; i < T * K; i += kThreads) {
-        a.topk_idx[i] = rt.idx[i / K][i % K];
-        a.topk_w[i] = rt.w[i / K][i % K];
-      }
-    }
+    // the per-expert counts from the last CTA (the same tables in every CTA)
     if (c == G - 1 && a.counts) {
       for (int e = tid; e < N; e += kThreads) {
         int cnt = 0;
@@ -762,7 +743,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const DecodeA
     const int st = lbg * kDepth + i;
     ring3[i] = active3 && st * EPS + EPL * t4 < lK ? ld_stream(lp3 + (int64_t)st * BPS) : make_uint4(0u, 0u, 0u, 0u);
   }
-  if (ok) ok = grid_barrier(a.sync, 2u, a.err, &s_ok);
+  if (ok) {
+    grid_arrive(a.sync);
+    // while the barrier completes: the gate weights of the rank-based top-K,
+    // warp t for token t, as router_select computes them (the group-limited
+    // path set them with its selection), then topk_idx / topk_w from CTA 0
+    const bool grouped = a.n_groups > 1 && a.topk_groups < a.n_groups;
+    if (!grouped && warp < T) {
+      const float* sc_s = red + 2 * T * N;
+      const float* sct = sc_s + warp * N;
+      const int my_e = lane < K ? rt.idx[warp][lane] : 0;
+      const float my_sc = lane < K ? sct[my_e] : 0.f;
+      float w;
+      if (a.score_fn == 0) {
+        const float lmax = __shfl_sync(0xffffffffu, my_sc, 0);  // slot 0 holds the largest logit
+        const float ex = lane < K ? expf(my_sc - lmax) : 0.f;
+        float z = 0.f;
+        if (a.renormalize) {
+          z = ex;
+        } else {
+          for (int e = lane; e < N; e += 32) z += expf(sct[e] - lmax);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        w = ex / z;
+      } else {
+        float z = lane < K ? my_sc : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        w = a.renormalize ? my_sc / z : my_sc;
+      }
+      if (lane < K) rt.w[warp][lane] = w;
+    }
+    __syncthreads();
+    if (c == 0) {
+      for (int i = tid; i < T * K; i += kThreads) {
+        a.topk_idx[i] = rt.idx[i / K][i % K];
+        a.topk_w[i] = rt.w[i / K][i % K];
+      }
+    }
+    ok = grid_wait(a.sync, 2u, a.err, &s_ok);
+  }
 
   uint16_t* hs = xs;  // phase 3: the h rows reuse the token rows' space
   const int hsm = a.hsm_stride;
