@@ -26,6 +26,9 @@ constexpr int kMaxShared = 8;
 // GEMM tiling shared by host and device.
 constexpr int kBM = 128;        // rows of the activation tile (MMA M)
 constexpr int kBK = 64;         // K elements per pipeline stage (128 B of bf16 = one swizzle atom)
+// Router GEMM: the three bf16 parts of the router matrix share a tile when
+// their columns (3 x np rows of 128 B) fit the 32 KB B stage of a 1-CTA tile.
+constexpr int kRouterMergedMaxNp = 80;
 constexpr int kBNGateUp = 128;  // gate columns per tile (the up tile adds another 128 -> MMA N = 256)
 constexpr int kBNDown = 256;    // output columns per down-projection tile (MMA N = 256)
 

@@ -94,7 +94,7 @@ __device__ __forceinline__ RouterTile decode_router_tile(int tile, const GemmArg
   RouterTile r;
   r.m_blk = tile % a.r_m_tiles;
   r.split = tile / a.r_m_tiles;
-  r.part = r.split / a.r_dslices;
+  r.part = a.r_merged ? 0 : r.split / a.r_dslices;
   const int slice = r.split - r.part * a.r_dslices;
   r.kb0 = slice * a.r_kb_per_slice;
   r.kb1 = min(a.r_nkb_d, r.kb0 + a.r_kb_per_slice);
@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int tile = unit; tile < total && !aborted && PHASE == kPhaseRouter; tile += units) {
         // Router: A = hidden rows of the m block, B = the router part's columns.
         const RouterTile rt = decode_router_tile(tile, a);
-        const uint32_t bytes = kStageA + (uint32_t)a.r_np * kBK * 2u;
+        // merged: the three parts' columns side by side in the B stage
+        const uint32_t part_bytes = (uint32_t)a.r_np * kBK * 2u;
+        const uint32_t bytes = kStageA + (a.r_merged ? 3u : 1u) * part_bytes;
         for (int kb = rt.kb0; kb < rt.kb1; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.err)) {
             aborted = true;
@@ -194,7 +196,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
           ptx::tma_load_2d(sA + stage * kStageA, &tmA0, full_bar(stage), kb * kBK, rt.m_blk * kBM);
-          ptx::tma_load_2d(sB + stage * kStageB, &tmB0, full_bar(stage), rt.part * a.r_d_pad + kb * kBK, 0);
+          if (a.r_merged) {
+            for (int p = 0; p < 3; ++p)
+              ptx::tma_load_2d(sB + stage * kStageB + (uint32_t)p * part_bytes, &tmB0, full_bar(stage),
+                               p * a.r_d_pad + kb * kBK, 0);
+          } else {
+            ptx::tma_load_2d(sB + stage * kStageB, &tmB0, full_bar(stage), rt.part * a.r_d_pad + kb * kBK, 0);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -287,12 +295,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::tc_fence_after();
           const uint64_t adesc = ptx::smem_desc_sw128(sA + stage * kStageA);
           const uint64_t bdesc = ptx::smem_desc_sw128(sB + stage * kStageB);
+          if (PHASE == kPhaseRouter && a.r_merged) {
+            // the hi, mid and lo parts of the router matrix into one accumulator
+            const uint32_t part_bytes = (uint32_t)a.r_np * kBK * 2u;
+            for (int p = 0; p < 3; ++p) {
+              const uint64_t pdesc = ptx::smem_desc_sw128(sB + stage * kStageB + (uint32_t)p * part_bytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            if (PAIR == 2)
-              ptx::mma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
-            else
-              ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < kBK / 16; ++k)
+                ptx::mma_bf16(d_tmem, adesc + 2u * k, pdesc + 2u * k, idesc, (kb | k | p) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              if (PAIR == 2)
+                ptx::mma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              else
+                ptx::mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           if (PAIR == 2) ptx::mma_commit_pair_multicast(empty_bar(stage), 0x3);
           else ptx::mma_commit(empty_bar(stage));

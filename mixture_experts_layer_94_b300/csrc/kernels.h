@@ -42,6 +42,7 @@ cudaError_t launch_expert_choice_select(const float* scores_t, int64_t T, int32_
 //    splits = 3 * dslices partial logits, MMA N = np (multiple of 16).
 struct RouterPlan {
   bool tensor;
+  bool merged;  // tensor path: the three parts share each tile (np <= kRouterMergedMaxNp)
   int64_t token_tiles;
   int32_t splits;
   int32_t d_slice;
@@ -141,11 +142,13 @@ struct GemmArgs {
   // token rows of the gate/up phase, the h rows of the down phase).
   const float* a_scale[2];
   // Router phase: one group of all T tokens; tile = (m block, split) with
-  // split = part * r_dslices + slice.
+  // split = part * r_dslices + slice, or, when r_merged, split = slice and
+  // the tile adds all three parts into one accumulator.
   int32_t r_tiles, r_m_tiles, r_dslices, r_kb_per_slice, r_nkb_d, r_d_pad, r_np, r_N;
+  int32_t r_merged;
   uint32_t r_idesc;
   int64_t r_T;
-  float* r_partial;       // [3 * r_dslices][T][N]
+  float* r_partial;       // [splits][T][N]: 3 * r_dslices, or r_dslices when merged
 };
 
 struct GemmMaps {

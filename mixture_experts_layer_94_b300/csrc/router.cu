@@ -437,6 +437,7 @@ cudaError_t launch_tensor_logits(const RouterArgs& a, const RouterPlan& pl, cuda
   g.r_nkb_d = pl.nkb_d;
   g.r_d_pad = pl.d_pad;
   g.r_np = pl.np;
+  g.r_merged = pl.merged ? 1 : 0;
   g.r_N = a.N;
   g.r_T = a.T;
   g.r_tiles = (int32_t)(pl.token_tiles * pl.splits);
@@ -610,21 +611,33 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
   constexpr int64_t kTargetCtas = 296;
   RouterPlan pl{};
   if (hidden_bf16 && T > kCudaCoreMaxT) {
-    // Tensor cores: one CTA per SM; tiles = 128-token blocks x 3 parts x slices.
+    // Tensor cores: one CTA per SM; tiles = 128-token blocks x 3 parts x
+    // slices. With few experts (np <= kRouterMergedMaxNp) the three parts'
+    // columns fit one B stage side by side, and a tile adds all three into
+    // one accumulator: each hidden tile is then read once, and the tile's
+    // k-block loop (its TMA round trips) is a third as long for the same
+    // number of tiles. Tiles are kept to one wave of 148 CTAs.
     constexpr int64_t kTargetTiles = 148;
     pl.tensor = true;
     pl.np = (N + 15) / 16 * 16;
     pl.token_tiles = (T + kBM - 1) / kBM;
     pl.nkb_d = (d + kBK - 1) / kBK;
     pl.d_pad = pl.nkb_d * kBK;
+    pl.merged = pl.np <= kRouterMergedMaxNp;
+    const int64_t per_slice = pl.merged ? pl.token_tiles : pl.token_tiles * 3;
     int64_t slices = 1;
-    if (pl.token_tiles > 0 && pl.token_tiles * 3 < kTargetTiles)
-      slices = (kTargetTiles + pl.token_tiles * 3 - 1) / (pl.token_tiles * 3);
-    if (slices > 8) slices = 8;  // bounds the partials the top-K kernel sums per logit (<= 24)
+    if (pl.merged) {
+      if (per_slice > 0 && per_slice < kTargetTiles) slices = kTargetTiles / per_slice;
+      if (slices > 16) slices = 16;  // bounds the partials the top-K kernel sums per logit
+    } else {
+      if (per_slice > 0 && per_slice < kTargetTiles) slices = (kTargetTiles + per_slice - 1) / per_slice;
+      if (slices > 8) slices = 8;  // bounds the partials the top-K kernel sums per logit (<= 24)
+    }
+    if (slices < 1) slices = 1;
     if (slices > pl.nkb_d) slices = pl.nkb_d;
     pl.kb_per_slice = (int32_t)((pl.nkb_d + slices - 1) / slices);
     pl.dslices = (pl.nkb_d + pl.kb_per_slice - 1) / pl.kb_per_slice;
-    pl.splits = 3 * pl.dslices;
+    pl.splits = (pl.merged ? 1 : 3) * pl.dslices;
     pl.d_slice = pl.kb_per_slice * kBK;
     return pl;
   }
