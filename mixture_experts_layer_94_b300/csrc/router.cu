@@ -616,7 +616,7 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
     // columns fit one B stage side by side, and a tile adds all three into
     // one accumulator: each hidden tile is then read once, and the tile's
     // k-block loop (its TMA round trips) is a third as long for the same
-    // number of tiles. Tiles are kept to one wave of 148 CTAs.
+    // number of tiles.
     constexpr int64_t kTargetTiles = 148;
     pl.tensor = true;
     pl.np = (N + 15) / 16 * 16;
@@ -625,16 +625,23 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t N, bool hidden_bf16) {
     pl.d_pad = pl.nkb_d * kBK;
     pl.merged = pl.np <= kRouterMergedMaxNp;
     const int64_t per_slice = pl.merged ? pl.token_tiles : pl.token_tiles * 3;
-    int64_t slices = 1;
-    if (pl.merged) {
-      if (per_slice > 0 && per_slice < kTargetTiles) slices = kTargetTiles / per_slice;
-      if (slices > 16) slices = 16;  // bounds the partials the top-K kernel sums per logit
-    } else {
-      if (per_slice > 0 && per_slice < kTargetTiles) slices = (kTargetTiles + per_slice - 1) / per_slice;
-      if (slices > 8) slices = 8;  // bounds the partials the top-K kernel sums per logit (<= 24)
+    // d slices: the fewest that minimise what one CTA runs, waves of tiles x
+    // (k-blocks per tile + about two k-blocks of per-tile overhead); a last,
+    // partly filled wave costs a whole one. At most 16 partials per logit
+    // merged, 24 (8 x 3) otherwise, and at most 32 MB of partials (a quarter
+    // of the L2; beyond that they evict what the next stages read).
+    const int64_t max_slices = pl.merged ? 16 : 8;
+    const int64_t part_bytes = (pl.merged ? 1 : 3) * T * (int64_t)N * 4;
+    int64_t slices = 1, best = -1;
+    for (int64_t sl = 1; sl <= max_slices && sl <= pl.nkb_d && (sl == 1 || sl * part_bytes <= (32ll << 20)); ++sl) {
+      const int64_t kbs = (pl.nkb_d + sl - 1) / sl;
+      const int64_t used = (pl.nkb_d + kbs - 1) / kbs;  // slices that hold k-blocks
+      const int64_t cost = (per_slice * used + kTargetTiles - 1) / kTargetTiles * (kbs + 2);
+      if (best < 0 || cost < best) {
+        best = cost;
+        slices = sl;
+      }
     }
-    if (slices < 1) slices = 1;
-    if (slices > pl.nkb_d) slices = pl.nkb_d;
     pl.kb_per_slice = (int32_t)((pl.nkb_d + slices - 1) / slices);
     pl.dslices = (pl.nkb_d + pl.kb_per_slice - 1) / pl.kb_per_slice;
     pl.splits = (pl.merged ? 1 : 3) * pl.dslices;

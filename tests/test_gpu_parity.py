@@ -42,6 +42,12 @@ MID = {
     "N_K_1": inputs.MoEConfig("N_K_1", T=129, d=128, N=1, K=1, F=256),
     "T1": inputs.MoEConfig("T1", T=1, d=256, N=16, K=4, F=128),
     "d72_tail": inputs.MoEConfig("d72_tail", T=150, d=72, N=6, K=2, F=40),
+    # the tensor-core router on both sides of the shared-tile limit (N <= 80):
+    # 80 experts with the three parts in one tile, 40 token blocks and a ragged
+    # d (not a whole number of 64-wide k-blocks); 96 experts with a tile per part
+    "router_merged_N80": inputs.MoEConfig("router_merged_N80", T=5000, d=1000, N=80, K=4, F=64),
+    "router_parts_N96": inputs.MoEConfig("router_parts_N96", T=300, d=512, N=96, K=6, F=64, score="sigmoid",
+                                         sel_bias_var=0.1),
     # router d-split paths (few token tiles): large N and small non-power-of-two N
     "decode_like_T3": inputs.MoEConfig("decode_like_T3", T=3, d=1024, N=128, K=8, F=64),
     "small_n_split_T5": inputs.MoEConfig("small_n_split_T5", T=5, d=2048, N=6, K=2, F=64,
@@ -163,7 +169,7 @@ def test_layer_is_repeatable():
 # --------------------------------------------------------------------------- router
 ROUTER_CASES = ["tiny", "ragged_softmax", "dsv3_like", "no_renorm_sigmoid", "no_renorm_softmax",
                 "K_equals_N", "N_K_1", "T1", "decode_like_T3", "small_n_split_T5", "grouped_routing",
-                "grouped_softmax_f32"]
+                "grouped_softmax_f32", "router_merged_N80", "router_parts_N96"]
 
 
 @pytest.mark.parametrize("name", ROUTER_CASES)
