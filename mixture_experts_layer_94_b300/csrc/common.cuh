@@ -40,7 +40,12 @@ struct GroupDesc {
   int32_t rows;       // rows of the group
   int32_t m_tiles;    // ceil(rows / kBM)
   int32_t h_row0;     // first row in the group's h / y matrix
-  int32_t pad0, pad1;
+  // Tile order of the group in the gate/up GEMM: 0 m fastest (the tiles of
+  // one weight column block run together), 1 n fastest (the tiles of one row
+  // block run together: for a group whose rows outweigh its weights, so that
+  // each row block is read from DRAM once). The down GEMM runs m fastest.
+  int32_t order_gu;
+  int32_t pad;
 };
 
 // Programmatic dependent launch. Every kernel of the library is launched with

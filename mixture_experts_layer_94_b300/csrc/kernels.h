@@ -117,6 +117,7 @@ enum GemmEpilogue { kEpiSwiGLU = 0, kEpiScatter = 1, kEpiStoreY = 2, kEpiLogits 
 struct GemmArgs {
   const GroupDesc* groups;
   const int32_t* tile_start;  // [G+1]
+  int32_t phase_dn;           // 1 for the down GEMM (always m fastest), 0 for gate/up (the groups' order_gu)
   int32_t G;
   int32_t n_ext[2];      // output columns of a group, per kind (gate/up: F, Fs; down: d)
   int32_t n_tiles[2];    // output column tiles of a group, per kind

@@ -492,6 +492,7 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
 
   // gate/up + SwiGLU
   a.tile_start = g.ts_gu;
+  a.phase_dn = 0;
   a.n_ext[0] = g.F;
   a.n_ext[1] = sh ? g.Fs : g.F;
   a.k_blocks[0] = a.k_blocks[1] = (g.d + kBK - 1) / kBK;
@@ -524,6 +525,7 @@ moe_status_t run_gemms(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_after_
   md.bh[0] = md.uh[0] = md.b[0];
   md.bh[1] = md.uh[1] = md.b[1];
   a.tile_start = g.ts_dn;
+  a.phase_dn = 1;
   a.n_ext[0] = a.n_ext[1] = g.d;
   a.k_blocks[0] = (g.F + kBK - 1) / kBK;
   a.k_blocks[1] = sh ? (g.Fs + kBK - 1) / kBK : a.k_blocks[0];
@@ -614,6 +616,7 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
 
   // gate/up + SwiGLU (K advances 128 codes per stage)
   a.tile_start = g.ts_gu;
+  a.phase_dn = 0;
   a.n_ext[0] = g.F;
   a.n_ext[1] = sh ? g.Fs : g.F;
   a.k_blocks[0] = a.k_blocks[1] = kb_d;
@@ -663,6 +666,7 @@ moe_status_t run_gemms_fp8(const GemmPlan& g, cudaStream_t s, cudaEvent_t* ev_af
   md.ku[0] = md.kw[0];
   md.ku[1] = md.kw[1];
   a.tile_start = g.ts_dn;
+  a.phase_dn = 1;
   a.n_ext[0] = a.n_ext[1] = g.d;
   a.k_blocks[0] = kb_f;
   a.k_blocks[1] = sh ? kb_fs : kb_f;

@@ -280,7 +280,10 @@ __device__ void schedule_block(int N, int S, int F, int Fs, int d, int tile_rows
       Fg = Fs;
     }
     gd.m_tiles = (gd.rows + tile_rows - 1) / tile_rows;
-    gd.pad0 = gd.pad1 = 0;
+    // n fastest where the group's activation rows outweigh its 2 Fg gate/up
+    // weight rows (the same K, d)
+    gd.order_gu = gd.rows > 2 * Fg ? 1 : 0;
+    gd.pad = 0;
     groups[g] = gd;
     s_gu[g] = gd.m_tiles * ((Fg + kBNGateUp - 1) / kBNGateUp);
     s_dn[g] = gd.m_tiles * nt_dn;

@@ -14,7 +14,8 @@ struct TileInfo {
 
 // Tile `tile` of a grouped GEMM: its group (the last group whose first tile
 // is <= tile, which skips empty groups) by binary search over the device-built
-// prefix of tile counts, then (n block, m block), m fastest inside a group.
+// prefix of tile counts, then (n block, m block) in the group's order for this
+// GEMM: m fastest, or (gate/up only) n fastest.
 __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmArgs& a) {
   int lo = 0, hi = a.G - 1;
   while (lo < hi) {
@@ -24,9 +25,16 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmArgs& a) {
   }
   TileInfo ti;
   ti.g = a.groups[lo];
-  const int local = tile - __ldg(a.tile_start + lo);
-  ti.n_blk = local / ti.g.m_tiles;
-  ti.m_blk = local - ti.n_blk * ti.g.m_tiles;
+  const int start = __ldg(a.tile_start + lo);
+  const int local = tile - start;
+  if (!a.phase_dn && ti.g.order_gu) {
+    const int n_tiles = (__ldg(a.tile_start + lo + 1) - start) / ti.g.m_tiles;
+    ti.m_blk = local / n_tiles;
+    ti.n_blk = local - ti.m_blk * n_tiles;
+  } else {
+    ti.n_blk = local / ti.g.m_tiles;
+    ti.m_blk = local - ti.n_blk * ti.g.m_tiles;
+  }
   return ti;
 }
 
