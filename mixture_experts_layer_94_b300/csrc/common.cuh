@@ -29,6 +29,8 @@ constexpr int kBK = 64;         // K elements per pipeline stage (128 B of bf16 
 // Router GEMM: the three bf16 parts of the router matrix share a tile when
 // their columns (3 x np rows of 128 B) fit the 32 KB B stage of a 1-CTA tile.
 constexpr int kRouterMergedMaxNp = 80;
+static_assert(3 * kRouterMergedMaxNp * kBK * 2 <= 256 * kBK * 2, "merged router parts exceed a 1-CTA B stage");
+static_assert(kRouterMergedMaxNp % 16 == 0, "each part's rows must start on a 1 KB swizzle atom");
 constexpr int kBNGateUp = 128;  // gate columns per tile (the up tile adds another 128 -> MMA N = 256)
 constexpr int kBNDown = 256;    // output columns per down-projection tile (MMA N = 256)
 
