@@ -42,6 +42,10 @@ MID = {
     "N_K_1": inputs.MoEConfig("N_K_1", T=129, d=128, N=1, K=1, F=256),
     "T1": inputs.MoEConfig("T1", T=1, d=256, N=16, K=4, F=128),
     "d72_tail": inputs.MoEConfig("d72_tail", T=150, d=72, N=6, K=2, F=40),
+    # gate/up groups whose rows outweigh their 2F weight rows run their tiles n
+    # fastest: 4 experts of about 1500 rows (6 pair row blocks x 3 column
+    # blocks, a half tile at each group's end) and a shared expert of 3000 rows
+    "n_fastest_pairs": inputs.MoEConfig("n_fastest_pairs", T=3000, d=320, N=4, K=2, F=384, S=1, Fs=256),
     # the tensor-core router on both sides of the shared-tile limit (N <= 80):
     # 80 experts with the three parts in one tile, 40 token blocks and a ragged
     # d (not a whole number of 64-wide k-blocks); 96 experts with a tile per part
